@@ -1,0 +1,147 @@
+"""CPU oracle for the split-K BF16 decode GEMM -- TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product path (the package
+``split_bf16_gemm_swapped_gb300``) never imports, calls or links it, and the
+two share no code: the oracle is plain C in ``splitk_oracle.c`` (float64
+accumulation, one round-to-nearest-even to bf16), loaded here through ctypes.
+
+Definition (module docstring of the vLLM ``splitk`` API page, SplitKGemm and
+its ``kernel`` / ``epilog_warp`` methods):
+
+    C[l, m, n] = RNE_bf16( sum_k f64(A[l, n, k]) * f64(B[l, m, k]) )
+
+with A[L, N, K] the weights, B[L, M, K] the tokens, C[L, M, N]; all bf16,
+passed here as uint16 bit patterns.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from pathlib import Path
+
+import numpy as np
+
+_HERE = Path(__file__).resolve().parent
+_SRC = _HERE / "splitk_oracle.c"
+_LIB = _HERE / "_lib" / "liboracle.so"
+
+_lib = None
+
+
+def build(force: bool = False) -> Path:
+    """Compile splitk_oracle.c with gcc into oracle/_lib/liboracle.so."""
+    _LIB.parent.mkdir(parents=True, exist_ok=True)
+    if force or not _LIB.exists() or _LIB.stat().st_mtime < _SRC.stat().st_mtime:
+        tmp = _LIB.with_suffix(f".{os.getpid()}.tmp")
+        cmd = ["gcc", "-O2", "-std=c11", "-Wall", "-Wextra", "-fPIC", "-shared",
+               "-pthread", str(_SRC), "-o", str(tmp), "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    build()
+    lib = ctypes.CDLL(str(_LIB))
+    u16p = ctypes.POINTER(ctypes.c_uint16)
+    i64 = ctypes.c_int64
+    lib.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
+    lib.oracle_bf16_to_f64.restype = ctypes.c_double
+    lib.oracle_f64_to_bf16.argtypes = [ctypes.c_double]
+    lib.oracle_f64_to_bf16.restype = ctypes.c_uint16
+    lib.oracle_dot_f64.argtypes = [u16p, u16p, i64, i64, i64, i64, i64, i64]
+    lib.oracle_dot_f64.restype = ctypes.c_double
+    lib.oracle_element.argtypes = [u16p, u16p, i64, i64, i64, i64, i64, i64]
+    lib.oracle_element.restype = ctypes.c_uint16
+    lib.oracle_elements.argtypes = [u16p, u16p, u16p, i64, i64, i64, i64,
+                                    ctypes.POINTER(ctypes.c_int64), i64]
+    lib.oracle_elements.restype = None
+    lib.oracle_gemm.argtypes = [u16p, u16p, u16p, i64, i64, i64, i64]
+    lib.oracle_gemm.restype = None
+    lib.oracle_gemm_threaded.argtypes = [u16p, u16p, u16p, i64, i64, i64, i64,
+                                         ctypes.c_int]
+    lib.oracle_gemm_threaded.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def _u16(a: np.ndarray) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint16:
+        raise TypeError("bf16 operands are passed as uint16 bit patterns")
+    return a
+
+
+def _ptr(a: np.ndarray, ctype=ctypes.c_uint16):
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def bf16_to_f64(h: int) -> float:
+    return _load().oracle_bf16_to_f64(int(h) & 0xFFFF)
+
+
+def f64_to_bf16(x: float) -> int:
+    return int(_load().oracle_f64_to_bf16(float(x)))
+
+
+def _shape(A: np.ndarray, B: np.ndarray):
+    if A.ndim == 2:
+        A = A[None]
+    if B.ndim == 2:
+        B = B[None]
+    L, N, K = A.shape
+    Lb, M, Kb = B.shape
+    if (Lb, Kb) != (L, K):
+        raise ValueError(f"shape mismatch A{A.shape} B{B.shape}")
+    return A, B, M, N, K, L
+
+
+def gemm(A: np.ndarray, B: np.ndarray, threads: int = 1) -> np.ndarray:
+    """C[L, M, N] (uint16 bf16 bits) for A[L, N, K], B[L, M, K] (2-D = L of 1)."""
+    squeeze = A.ndim == 2
+    A, B, M, N, K, L = _shape(_u16(A), _u16(B))
+    A = np.ascontiguousarray(A)
+    B = np.ascontiguousarray(B)
+    C = np.empty((L, M, N), dtype=np.uint16)
+    if threads <= 1:
+        _load().oracle_gemm(_ptr(A), _ptr(B), _ptr(C), M, N, K, L)
+    else:
+        _load().oracle_gemm_threaded(_ptr(A), _ptr(B), _ptr(C), M, N, K, L,
+                                     int(threads))
+    return C[0] if squeeze else C
+
+
+def gemm_threaded(A: np.ndarray, B: np.ndarray, threads: int):
+    """Like gemm(); also returns the number of host threads actually used."""
+    A, B, M, N, K, L = _shape(_u16(A), _u16(B))
+    A = np.ascontiguousarray(A)
+    B = np.ascontiguousarray(B)
+    C = np.empty((L, M, N), dtype=np.uint16)
+    used = _load().oracle_gemm_threaded(_ptr(A), _ptr(B), _ptr(C), M, N, K, L,
+                                        int(threads))
+    return C, int(used)
+
+
+def elements(A: np.ndarray, B: np.ndarray, flat_idx) -> np.ndarray:
+    """Selected outputs, flat index l*M*N + m*N + n, each computed alone."""
+    A, B, M, N, K, L = _shape(_u16(A), _u16(B))
+    A = np.ascontiguousarray(A)
+    B = np.ascontiguousarray(B)
+    idx = np.ascontiguousarray(np.asarray(flat_idx, dtype=np.int64))
+    out = np.empty(idx.shape[0], dtype=np.uint16)
+    _load().oracle_elements(_ptr(A), _ptr(B), _ptr(out), M, N, K, L,
+                            _ptr(idx, ctypes.c_int64), idx.shape[0])
+    return out
+
+
+def dot_f64(A: np.ndarray, B: np.ndarray, l: int, m: int, n: int) -> float:
+    """The unrounded float64 sum behind C[l, m, n]."""
+    A, B, M, N, K, L = _shape(_u16(A), _u16(B))
+    A = np.ascontiguousarray(A)
+    B = np.ascontiguousarray(B)
+    return float(_load().oracle_dot_f64(_ptr(A), _ptr(B), M, N, K, l, m, n))

@@ -1,0 +1,76 @@
+"""Seeded synthetic bf16 inputs (the shared input source of tests and bench).
+
+Holds no GEMM arithmetic: it only draws normal numbers and rounds them to
+bf16 bit patterns (see ``csrc/synthetic.c`` for the exact generator:
+SplitMix64 counter stream + Box-Muller, rounded f64 -> f32 -> bf16, each
+step to nearest-even).
+
+Streams: A (weights) draws from stream 0, B (activations) from stream 1, the
+outlier mask of B from stream 2, all under the workload's seed.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from . import _build
+
+STREAM_A = 0
+STREAM_B = 1
+STREAM_OUTLIER = 2
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(str(_build.build_synthetic()))
+        lib.synthetic_normal_bf16.argtypes = [
+            ctypes.POINTER(ctypes.c_uint16), ctypes.c_uint64, ctypes.c_uint64,
+            ctypes.c_uint64, ctypes.c_uint64, ctypes.c_double, ctypes.c_double,
+            ctypes.c_double, ctypes.c_uint64, ctypes.c_int]
+        lib.synthetic_normal_bf16.restype = ctypes.c_int
+        lib.synthetic_word.argtypes = [ctypes.c_uint64] * 3
+        lib.synthetic_word.restype = ctypes.c_uint64
+        _lib = lib
+    return _lib
+
+
+def host_threads() -> int:
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:  # pragma: no cover
+        return max(1, os.cpu_count() or 1)
+
+
+def normal_bf16(shape, seed: int, stream: int, sigma: float,
+                outlier_p: float = 0.0, outlier_scale: float = 1.0,
+                offset: int = 0, threads: int | None = None,
+                out: np.ndarray | None = None) -> np.ndarray:
+    """bf16 bit patterns (uint16) of sigma * N(0, 1), C-contiguous ``shape``.
+
+    ``offset`` starts the draw at that element of the stream, so a slice of
+    a large tensor can be drawn alone (the values equal those of the full
+    draw at the same positions).
+    """
+    shape = tuple(int(s) for s in (shape if isinstance(shape, (tuple, list)) else (shape,)))
+    count = int(np.prod(shape)) if shape else 1
+    if out is None:
+        out = np.empty(shape, dtype=np.uint16)
+    if out.dtype != np.uint16 or not out.flags.c_contiguous or out.size != count:
+        raise ValueError("out must be a C-contiguous uint16 array of the shape's size")
+    if count:
+        _load().synthetic_normal_bf16(
+            out.ctypes.data_as(ctypes.POINTER(ctypes.c_uint16)), int(offset), count,
+            int(seed), int(stream), float(sigma), float(outlier_p),
+            float(outlier_scale), STREAM_OUTLIER,
+            int(threads if threads is not None else host_threads()))
+    return out
+
+
+def word(seed: int, stream: int, i: int) -> int:
+    """The i-th raw 64-bit SplitMix64 word of (seed, stream)."""
+    return int(_load().synthetic_word(int(seed), int(stream), int(i)))

@@ -1,0 +1,259 @@
+"""Pins of the CPU oracle against facts fixed outside it.
+
+Each test would fail on a plausible mistake in ``oracle/splitk_oracle.c``:
+a wrong shift in the bf16 widening, truncation or round-half-up instead of
+ties-to-even, rounding twice (f64 -> f32 -> bf16), flushed subnormals, a
+transposed operand (A row m / B row n), a dropped or repeated k term, a wrong
+L stride.  References: exact rational arithmetic (tests/_exact.py), closed
+forms, library conversions (numpy bit views, torch's fp32 -> bf16), and the
+hand-derived table tests/golden/bf16_rounding.txt.
+"""
+from __future__ import annotations
+
+import math
+import random
+from fractions import Fraction
+from pathlib import Path
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests import _exact
+
+GOLDEN = Path(__file__).parent / "golden"
+
+
+# --------------------------------------------------------------------------
+# bf16 -> float64 widening
+# --------------------------------------------------------------------------
+def test_widen_every_bf16_pattern_matches_numpy_bit_view():
+    pats = np.arange(65536, dtype=np.uint32)
+    with np.errstate(invalid="ignore"):
+        ref = (pats << 16).view(np.float32).astype(np.float64)
+    got = np.array([oracle.bf16_to_f64(int(h)) for h in pats])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    # and the sign of zeros
+    assert math.copysign(1.0, oracle.bf16_to_f64(0x8000)) == -1.0
+
+
+def test_widen_matches_ieee_field_definition_on_samples():
+    rng = random.Random(7)
+    for h in [0x0001, 0x007F, 0x0080, 0x3F80, 0x7F7F, 0xC2F7] + \
+             [rng.randrange(65536) for _ in range(2000)]:
+        v = _exact.value(h)
+        got = oracle.bf16_to_f64(h)
+        if isinstance(v, float):
+            assert (math.isnan(v) and math.isnan(got)) or v == got
+        else:
+            assert Fraction(got) == v, hex(h)
+
+
+# --------------------------------------------------------------------------
+# float64 -> bf16 rounding
+# --------------------------------------------------------------------------
+def _golden_rounding_cases():
+    cases = []
+    for line in (GOLDEN / "bf16_rounding.txt").read_text().splitlines():
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        tok, bits, *_ = line.split()
+        x = {"zero": 0.0, "negzero": -0.0, "inf": math.inf, "-inf": -math.inf,
+             "nan": math.nan}.get(tok)
+        if x is None:
+            x = float.fromhex(tok)
+        cases.append((tok, x, int(bits, 16)))
+    return cases
+
+
+@pytest.mark.parametrize("tok,x,bits", _golden_rounding_cases())
+def test_rounding_golden_table(tok, x, bits):
+    assert oracle.f64_to_bf16(x) == bits, tok
+    if math.isfinite(x) and x != 0.0:
+        # the table itself agrees with exact rational rounding
+        assert _exact.round_bf16(Fraction(x)) == bits, tok
+
+
+def test_rounding_binary32_inputs_match_torch():
+    """For binary32 inputs one rounding to bf16 is torch's fp32->bf16 (RNE)."""
+    rng = np.random.default_rng(11)
+    pats = rng.integers(0, 2 ** 32, size=60000, dtype=np.uint64).astype(np.uint32)
+    # plus exact ties and near-ties around random bf16 values
+    base = rng.integers(0, 2 ** 16, size=4000, dtype=np.uint32) << 16
+    extra = np.concatenate([base | 0x8000, base | 0x7FFF, base | 0x8001, base])
+    pats = np.concatenate([pats, extra])
+    f32 = pats.view(np.float32)
+    f32 = f32[np.isfinite(f32)]
+    ref = torch.from_numpy(f32.copy()).to(torch.bfloat16).view(torch.int16).numpy()
+    ref = ref.astype(np.uint16)
+    got = np.array([oracle.f64_to_bf16(float(v)) for v in f32], dtype=np.uint16)
+    bad = np.flatnonzero(got != ref)
+    assert bad.size == 0, f"{bad.size} mismatches, first {f32[bad[0]]!r}"
+
+
+def test_rounding_float64_inputs_match_exact_rationals():
+    """Values with bits below binary32 precision: a single rounding decides."""
+    rng = random.Random(3)
+    xs = []
+    for _ in range(3000):
+        h = rng.randrange(0x0001, 0x7F7F)       # a finite positive bf16
+        lo = _exact.value(h)
+        hi = _exact.value(h + 1)
+        mid = (lo + hi) / 2
+        # just above / below the midpoint by an amount binary32 cannot hold
+        eps = (hi - lo) * Fraction(1, 2 ** rng.randrange(20, 40))
+        for v in (mid + eps, mid - eps, mid):
+            f = float(v)
+            if rng.random() < 0.5:
+                f = -f
+            xs.append(f)
+    for f in xs:
+        assert oracle.f64_to_bf16(f) == _exact.round_bf16(Fraction(f)), f.hex()
+
+
+def test_rounding_is_monotone_and_idempotent_on_bf16_values():
+    for h in range(0, 0x7F80, 7):
+        v = oracle.bf16_to_f64(h)
+        assert oracle.f64_to_bf16(v) == h
+        assert oracle.f64_to_bf16(-v) == (h | 0x8000)
+
+
+# --------------------------------------------------------------------------
+# The GEMM
+# --------------------------------------------------------------------------
+ONE = 0x3F80
+
+
+def _bf16_of_int(v: int) -> int:
+    return _exact.round_bf16(v)
+
+
+@pytest.mark.parametrize("K", [1, 7, 128, 1024, 2048, 7168])
+def test_all_ones_gives_K(K):
+    M, N, L = 3, 5, 2
+    A = np.full((L, N, K), ONE, np.uint16)
+    B = np.full((L, M, K), ONE, np.uint16)
+    C = oracle.gemm(A, B)
+    assert C.shape == (L, M, N)
+    assert np.all(C == _bf16_of_int(K))
+
+
+def test_identity_weights_pass_activations_through_bit_exactly():
+    rng = np.random.default_rng(5)
+    L, M, N, K = 2, 6, 40, 64
+    A = np.zeros((L, N, K), np.uint16)
+    for n in range(N):
+        A[:, n, n] = ONE
+    B = rng.integers(0, 2 ** 16, size=(L, M, K), dtype=np.uint16)
+    B[(B & 0x7F80) == 0x7F80] = ONE            # keep inputs finite
+    C = oracle.gemm(A, B)
+    expect = B[:, :, :N].copy()
+    expect[(expect & 0x7FFF) == 0] = 0          # -0 * 1 + 0 sums to +0
+    assert np.array_equal(C, expect)
+
+
+def test_single_nonzero_per_row_gives_rounded_scaled_copy():
+    rng = np.random.default_rng(9)
+    L, M, N, K = 1, 4, 33, 48
+    A = np.zeros((L, N, K), np.uint16)
+    perm = rng.integers(0, K, size=N)
+    scale = rng.integers(0x3C00, 0x4400, size=N).astype(np.uint16)
+    for n in range(N):
+        A[0, n, perm[n]] = scale[n]
+    B = rng.integers(0x3800, 0x4800, size=(L, M, K)).astype(np.uint16)
+    B[rng.random(B.shape) < 0.5] |= 0x8000
+    C = oracle.gemm(A, B)
+    for m in range(M):
+        for n in range(N):
+            exact = _exact.value(int(scale[n])) * _exact.value(int(B[0, m, perm[n]]))
+            assert C[0, m, n] == _exact.round_bf16(exact), (m, n)
+
+
+@pytest.mark.parametrize("L,M,N,K", [(1, 1, 1, 1), (1, 2, 3, 5), (2, 3, 4, 8),
+                                     (3, 5, 2, 16), (2, 4, 7, 9)])
+def test_brute_force_exact_rationals(L, M, N, K):
+    from split_bf16_gemm_swapped_gb300 import synthetic
+    A = synthetic.normal_bf16((L, N, K), seed=100 + K, stream=0, sigma=0.02)
+    B = synthetic.normal_bf16((L, M, K), seed=100 + K, stream=1, sigma=1.0)
+    C = oracle.gemm(A, B)
+    for l in range(L):
+        for m in range(M):
+            for n in range(N):
+                s = sum(_exact.value(int(A[l, n, k])) * _exact.value(int(B[l, m, k]))
+                        for k in range(K))
+                assert C[l, m, n] == _exact.round_bf16(s), (l, m, n)
+                assert Fraction(oracle.dot_f64(A, B, l, m, n)) == s
+
+
+def test_orientation_and_batch_index_on_a_structured_case():
+    """C[l, m, n] = sum_k A[l, n, k] * B[l, m, k] with distinct small ints."""
+    L, M, N, K = 2, 4, 4, 5
+    rng = np.random.default_rng(13)
+    Ai = rng.integers(-6, 7, size=(L, N, K))
+    Bi = rng.integers(-6, 7, size=(L, M, K))
+    enc = np.vectorize(lambda v: _exact.round_bf16(int(v)))
+    A = enc(Ai).astype(np.uint16)
+    B = enc(Bi).astype(np.uint16)
+    C = oracle.gemm(A, B)
+    ref = np.einsum("lnk,lmk->lmn", Ai, Bi)      # exact small integers
+    assert np.array_equal(C, enc(ref).astype(np.uint16))
+    # a transposed output or a mixed-up batch index would not match
+    assert not np.array_equal(ref, ref.transpose(0, 2, 1))
+    assert not np.array_equal(ref, ref[::-1])
+
+
+def test_float64_sum_matches_numpy_matmul_then_exact_rounding():
+    """Larger K: the f64 sum equals numpy's f64 matmul to within f64 rounding,
+    and rounding that sum once reproduces the oracle's output."""
+    from split_bf16_gemm_swapped_gb300 import synthetic
+    L, M, N, K = 1, 3, 64, 2048
+    A = synthetic.normal_bf16((L, N, K), seed=21, stream=0, sigma=0.02)
+    B = synthetic.normal_bf16((L, M, K), seed=21, stream=1, sigma=1.0)
+    af = (A.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    bf = (B.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    ref = np.einsum("lmk,lnk->lmn", bf, af)
+    C = oracle.gemm(A, B)
+    for m in range(M):
+        for n in range(N):
+            s = oracle.dot_f64(A, B, 0, m, n)
+            assert abs(s - ref[0, m, n]) <= 1e-12 * np.sum(np.abs(bf[0, m] * af[0, n]))
+            assert C[0, m, n] == _exact.round_bf16(Fraction(s))
+
+
+def test_threaded_and_element_paths_agree_with_the_plain_gemm():
+    from split_bf16_gemm_swapped_gb300 import synthetic
+    L, M, N, K = 2, 5, 96, 256
+    A = synthetic.normal_bf16((L, N, K), seed=31, stream=0, sigma=0.02)
+    B = synthetic.normal_bf16((L, M, K), seed=31, stream=1, sigma=1.0)
+    C = oracle.gemm(A, B)
+    C4, used = oracle.gemm_threaded(A, B, 4)
+    assert used >= 1
+    assert np.array_equal(C, C4)
+    idx = np.array([0, 17, L * M * N - 1, M * N + 3])
+    assert np.array_equal(oracle.elements(A, B, idx), C.reshape(-1)[idx])
+
+
+def test_pins_catch_planted_mistakes():
+    """Mistakes planted on the CPU, by feeding the oracle altered operands,
+    must change the output that the exact brute force pins: a dropped last k
+    term, a swapped pair of weight rows, a wrong batch slice."""
+    from split_bf16_gemm_swapped_gb300 import synthetic
+    L, M, N, K = 2, 3, 5, 16
+    A = synthetic.normal_bf16((L, N, K), seed=41, stream=0, sigma=0.02)
+    B = synthetic.normal_bf16((L, M, K), seed=41, stream=1, sigma=1.0)
+    exact = np.array([[[_exact.round_bf16(sum(
+        _exact.value(int(A[l, n, k])) * _exact.value(int(B[l, m, k]))
+        for k in range(K))) for n in range(N)] for m in range(M)]
+        for l in range(L)], dtype=np.uint16)
+    assert np.array_equal(oracle.gemm(A, B), exact)
+    planted = {
+        "dropped k": oracle.gemm(A[:, :, :-1], B[:, :, :-1]),
+        "rows swapped": oracle.gemm(A[:, [1, 0, 2, 3, 4]], B),
+        "batch mixed": oracle.gemm(A[::-1].copy(), B),
+    }
+    for name, out in planted.items():
+        assert not np.array_equal(out, exact), name
