@@ -1,0 +1,218 @@
+/*
+ * splitk.h -- C ABI of the GB300 (sm_103a) split-K BF16 decode GEMM.
+ *
+ *     C[l][m][n] = bf16_rne( sum_k A[l][n][k] * B[l][m][k] )
+ *
+ * Operation (the vLLM API page of module
+ * vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.gemm.splitk,
+ * class SplitKGemm and its module docstring): a BF16 GEMM whose K dimension is
+ * split across the CTAs of one thread-block cluster.  Each cluster rank
+ * accumulates an exact, contiguous K slice in FP32 (tensor memory); the peer
+ * ranks publish their FP32 partials to rank 0's shared memory; rank 0 adds
+ * them in rank order, converts once to BF16 (round to nearest even) and
+ * stores.  Operands are "swapped": the weight rows (public N) run along the
+ * 128-wide MMA M dimension and the few tokens (public M) along MMA N.
+ *
+ * Layouts (all row-major, compact, L outermost, bf16 = 2 bytes):
+ *   A  [L][N][K]  weights ("kernel A, K-major"), K contiguous
+ *   B  [L][M][K]  token activations, K contiguous
+ *   C  [L][M][N]  output, N contiguous
+ *
+ * Ownership: the caller owns A, B, C and the stream.  The library owns only
+ * its caches: device-resident CUDA tensor maps of A (128 bytes each, one per
+ * distinct (A pointer, N, K, L)) in a device pool allocated on first use, a
+ * pinned host mirror of that pool, and host-side tensor maps of B.
+ * splitk_release() frees them.
+ *
+ * Execution: every call is asynchronous on `stream` and returns after the
+ * enqueue.  Calls launch with programmatic dependent launch (PDL): the kernel
+ * may begin streaming A while the previous kernel on the stream is still
+ * running, and waits for that kernel's completion (griddepcontrol.wait)
+ * before it reads B or writes C.  So A must not be written by the kernel that
+ * immediately precedes the call on the same stream; pass SPLITK_FLAG_NO_PDL
+ * to splitk_gemm_bf16_planned() when it is.
+ *
+ * Errors: every int-returning call returns SPLITK_OK (0) or a negative
+ * splitk_status code; no exception crosses the ABI, nothing is printed.
+ * Failed argument checks enqueue no work.
+ */
+#ifndef SPLITK_H
+#define SPLITK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(_WIN32)
+#define SPLITK_API __declspec(dllexport)
+#else
+#define SPLITK_API __attribute__((visibility("default")))
+#endif
+
+/* A cudaStream_t (struct CUstream_st*).  NULL is the legacy default stream. */
+typedef struct CUstream_st *splitk_stream_t;
+
+enum splitk_status {
+    SPLITK_OK = 0,
+    /* M, N, K or L < 1, a size past a hardware limit, or K not a multiple of
+       128 * split_k (each rank takes whole 128-wide K tiles). */
+    SPLITK_ERR_INVALID_SHAPE = -1,
+    /* A or B not 16-byte aligned (TMA), or C not 2-byte aligned. */
+    SPLITK_ERR_MISALIGNED = -2,
+    /* split_k not in {0 (plan chooses), 1, 2, 4, 8}. */
+    SPLITK_ERR_UNSUPPORTED_SPLIT = -3,
+    /* No tile / stage configuration fits the shared-memory budget. */
+    SPLITK_ERR_NO_FIT = -4,
+    /* A CUDA runtime or driver call failed (launch, copy, allocation). */
+    SPLITK_ERR_CUDA = -5,
+    /* A bounded wait inside the kernel ran out (see splitk_get_fault). */
+    SPLITK_ERR_TIMEOUT = -6,
+    /* A required pointer argument is NULL. */
+    SPLITK_ERR_NULL = -7,
+    /* The device tensor-map pool is full; call splitk_release(). */
+    SPLITK_ERR_CACHE_FULL = -8,
+    /* No CUDA device, or the current device is not compute capability 10.3. */
+    SPLITK_ERR_UNSUPPORTED_DEVICE = -9,
+    /* A plan passed to splitk_gemm_bf16_planned() does not match the shape. */
+    SPLITK_ERR_BAD_PLAN = -10
+};
+
+/* Flags of splitk_gemm_bf16_planned(). */
+#define SPLITK_FLAG_NO_PDL 0x1u
+
+/*
+ * A launch configuration ("tactic": the page's SplitKTactic fields mma_m,
+ * mma_n, ab_stages, split_k, plus what the launcher derives from them).
+ */
+typedef struct splitk_plan_t {
+    int mma_m;             /* 128: weight rows per CTA tile (tcgen05 MMA M)    */
+    int mma_n;             /* 16, 32, 64 or 128: token columns per CTA tile    */
+    int stages;            /* shared-memory ring depth (2..8)                  */
+    int split_k;           /* CTAs per cluster, each owning K/split_k of K     */
+    int k_tiles_per_cta;   /* 128-wide K tiles each CTA accumulates            */
+    int mailbox_dedicated; /* 1: partials land in their own smem region;
+                              0: they reuse rank 0's drained weight ring       */
+    int mailbox_quads;     /* 4-column groups of partials per reduction round  */
+    int reduce_rounds;     /* rounds of the rank-0 reduction                    */
+    unsigned grid[3];      /* (split_k * ceil(M/mma_n), ceil(N/128), L)        */
+    unsigned cluster[3];   /* (split_k, 1, 1)                                  */
+    size_t smem_bytes;     /* dynamic shared memory per CTA                    */
+    int ctas_per_sm;       /* CTAs the smem budget was sized for               */
+} splitk_plan_t;
+
+/*
+ * Picks the tactic for the current CUDA device.  split_k = 0 lets the plan
+ * choose among {1, 2, 4, 8}.  Needs a device (SPLITK_ERR_UNSUPPORTED_DEVICE
+ * otherwise); writes *out only on success.
+ */
+SPLITK_API int splitk_plan(int M, int N, int K, int L, int split_k,
+                           splitk_plan_t *out);
+
+/*
+ * The same choice for a described device, without touching CUDA: num_sms
+ * streaming multiprocessors, smem_per_sm bytes of shared memory per SM and
+ * smem_per_block_optin bytes at most per CTA.
+ */
+SPLITK_API int splitk_plan_for(int M, int N, int K, int L, int split_k,
+                               int num_sms, size_t smem_per_sm,
+                               size_t smem_per_block_optin, splitk_plan_t *out);
+
+/*
+ * C = B * A^T with the tactic splitk_plan() picks for (M, N, K, L, split_k).
+ * a, b, c are device pointers (layouts above); a and b 16-byte aligned.
+ * C is written once (not accumulated); rows m >= M and columns n >= N of the
+ * padded tiles are never written.  The first call for a given A pointer and
+ * shape encodes A's tensor map and copies it to the device on `stream`
+ * (allocating the pool on the first call of all), so make that first call
+ * outside any CUDA graph capture.
+ */
+SPLITK_API int splitk_gemm_bf16(const void *a, const void *b, void *c,
+                                int M, int N, int K, int L, int split_k,
+                                splitk_stream_t stream);
+
+/*
+ * As splitk_gemm_bf16() with an explicit plan (from splitk_plan() or
+ * splitk_plan_for(), possibly with stages / mailbox fields edited; the call
+ * re-validates it) and flags (SPLITK_FLAG_NO_PDL).
+ */
+SPLITK_API int splitk_gemm_bf16_planned(const void *a, const void *b, void *c,
+                                        int M, int N, int K, int L,
+                                        const splitk_plan_t *plan,
+                                        unsigned flags, splitk_stream_t stream);
+
+/*
+ * End-to-end call with host activations and host output: enqueues on
+ * `stream` the copy b_host -> b_dev (M*K*L bf16), the GEMM with the resident
+ * device weights `a`, and the copy c_dev -> c_host (M*N*L bf16).  b_dev and
+ * c_dev are caller-owned device buffers of those sizes.  Host buffers should
+ * be pinned for the copies to be asynchronous; the caller synchronizes
+ * `stream` before reading c_host.
+ */
+SPLITK_API int splitk_gemm_bf16_hostio(const void *a, const void *b_host,
+                                       void *c_host, void *b_dev, void *c_dev,
+                                       int M, int N, int K, int L, int split_k,
+                                       splitk_stream_t stream);
+
+/*
+ * Diagnostic record of the first bounded wait that ran out on the current
+ * device since the last read (the Muse Spark AMD dev page's _spin_bounded:
+ * every wait is bounded, the first timeout leaves a record and a sticky
+ * failed state, later waits of the launch give up at once).
+ */
+typedef struct splitk_fault_t {
+    int code;        /* SPLITK_OK or SPLITK_ERR_TIMEOUT                        */
+    int role;        /* 0 weight TMA, 1 activation TMA, 2 MMA, 3 TMEM release,
+                        4 epilogue: MMA completion, 5 epilogue: partials
+                        (rank 0), 6 epilogue: mailbox free (peer)              */
+    int index;       /* K tile or reduction round being waited for             */
+    int parity;      /* mbarrier phase parity waited for                       */
+    int block[3];    /* blockIdx of the CTA                                    */
+    int cluster_rank;
+} splitk_fault_t;
+
+/*
+ * Synchronizes the current device, copies its fault record into *out (when
+ * out is not NULL), clears it, and returns its code (SPLITK_OK when no wait
+ * ran out, SPLITK_ERR_TIMEOUT otherwise, SPLITK_ERR_CUDA if the device
+ * cannot be read).
+ */
+SPLITK_API int splitk_get_fault(splitk_fault_t *out);
+
+/* splitk_get_fault(NULL). */
+SPLITK_API int splitk_get_status(void);
+
+/*
+ * Upper bound, in nanoseconds of %globaltimer, of every wait inside the
+ * kernel for launches made after this call (default 1e9 = 1 s).  ns = 0
+ * restores the default.
+ */
+SPLITK_API int splitk_set_wait_limit_ns(uint64_t ns);
+
+/*
+ * Test-only fault injection for launches made after this call.
+ * SPLITK_INJECT_SKIP_PUBLISH: cluster ranks other than 0 skip publishing
+ * their partials, so rank 0's bounded wait for them runs out and the call
+ * reports SPLITK_ERR_TIMEOUT (the output is then undefined).  No GPU fault is
+ * involved: nothing is stored remotely and every wait stays bounded.
+ * 0 turns injection off.
+ */
+#define SPLITK_INJECT_SKIP_PUBLISH 0x1u
+SPLITK_API int splitk_debug_inject(unsigned flags);
+
+/* Synchronizes every device the library used, then frees its caches. */
+SPLITK_API void splitk_release(void);
+
+/* A static description of a status code. */
+SPLITK_API const char *splitk_strerror(int code);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+SPLITK_API int splitk_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPLITK_H */

@@ -1,1 +1,266 @@
-"""GB300-native split-K BF16 decode GEMM (placeholder until the binding lands)."""
+"""GB300-native split-K BF16 decode GEMM: ``C[M, N] = B[M, K] @ A[N, K]^T``.
+
+A thin ctypes binding over the C ABI in ``include/splitk.h``
+(``_lib/libsplitk_sm103a.so``, built in-tree by ``__graft_entry__.build()`` or
+``split_bf16_gemm_swapped_gb300._build.build_all()``).  It only marshals
+arguments: every step of the GEMM runs in the library's sm_103a kernels, and
+there is no CPU or PyTorch fallback -- if the library is missing, importing a
+function that needs it raises.
+
+PyTorch supplies device memory and streams.  Tensors:
+  a  weights      [L, N, K] (or [N, K]) bfloat16, CUDA, contiguous
+  b  activations  [L, M, K] (or [M, K]) bfloat16, CUDA, contiguous
+  c  output       [L, M, N] (or [M, N]) bfloat16, CUDA, contiguous
+"""
+from __future__ import annotations
+
+import ctypes
+from pathlib import Path
+
+from . import _build
+
+__all__ = [
+    "SplitKError", "Plan", "Fault", "library_path", "load_library",
+    "splitk_plan", "splitk_plan_for", "splitk_gemm_bf16", "splitk_gemm_bf16_planned",
+    "splitk_gemm_bf16_hostio", "splitk_get_fault", "splitk_get_status",
+    "splitk_set_wait_limit_ns", "splitk_debug_inject", "splitk_release",
+    "splitk_strerror", "splitk_version", "FLAG_NO_PDL", "INJECT_SKIP_PUBLISH",
+    "STATUS",
+]
+
+FLAG_NO_PDL = 0x1
+INJECT_SKIP_PUBLISH = 0x1
+
+STATUS = {
+    0: "SPLITK_OK", -1: "SPLITK_ERR_INVALID_SHAPE", -2: "SPLITK_ERR_MISALIGNED",
+    -3: "SPLITK_ERR_UNSUPPORTED_SPLIT", -4: "SPLITK_ERR_NO_FIT", -5: "SPLITK_ERR_CUDA",
+    -6: "SPLITK_ERR_TIMEOUT", -7: "SPLITK_ERR_NULL", -8: "SPLITK_ERR_CACHE_FULL",
+    -9: "SPLITK_ERR_UNSUPPORTED_DEVICE", -10: "SPLITK_ERR_BAD_PLAN",
+}
+
+
+class SplitKError(RuntimeError):
+    def __init__(self, code: int, where: str = ""):
+        self.code = int(code)
+        self.name = STATUS.get(self.code, str(code))
+        msg = f"{self.name}: {splitk_strerror(self.code)}"
+        super().__init__(f"{where}: {msg}" if where else msg)
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [
+        ("mma_m", ctypes.c_int), ("mma_n", ctypes.c_int), ("stages", ctypes.c_int),
+        ("split_k", ctypes.c_int), ("k_tiles_per_cta", ctypes.c_int),
+        ("mailbox_dedicated", ctypes.c_int), ("mailbox_quads", ctypes.c_int),
+        ("reduce_rounds", ctypes.c_int), ("grid", ctypes.c_uint * 3),
+        ("cluster", ctypes.c_uint * 3), ("smem_bytes", ctypes.c_size_t),
+        ("ctas_per_sm", ctypes.c_int),
+    ]
+
+    def as_dict(self) -> dict:
+        d = {k: getattr(self, k) for k, _ in self._fields_}
+        d["grid"] = list(self.grid)
+        d["cluster"] = list(self.cluster)
+        return d
+
+    def __repr__(self) -> str:
+        return f"Plan({self.as_dict()})"
+
+
+class Fault(ctypes.Structure):
+    _fields_ = [("code", ctypes.c_int), ("role", ctypes.c_int), ("index", ctypes.c_int),
+                ("parity", ctypes.c_int), ("block", ctypes.c_int * 3),
+                ("cluster_rank", ctypes.c_int)]
+
+    def as_dict(self) -> dict:
+        d = {k: getattr(self, k) for k, _ in self._fields_}
+        d["block"] = list(self.block)
+        return d
+
+
+_lib = None
+
+
+def library_path() -> Path:
+    return _build.SPLITK_LIB
+
+
+def load_library():
+    """Loads the CUDA library; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not path.exists():
+        raise RuntimeError(
+            f"{path} is missing: build the sm_103a library first "
+            "(python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(str(path))
+    vp, i, u, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint, ctypes.c_size_t
+    lib.splitk_plan.argtypes = [i, i, i, i, i, ctypes.POINTER(Plan)]
+    lib.splitk_plan.restype = i
+    lib.splitk_plan_for.argtypes = [i, i, i, i, i, i, sz, sz, ctypes.POINTER(Plan)]
+    lib.splitk_plan_for.restype = i
+    lib.splitk_gemm_bf16.argtypes = [vp, vp, vp, i, i, i, i, i, vp]
+    lib.splitk_gemm_bf16.restype = i
+    lib.splitk_gemm_bf16_planned.argtypes = [vp, vp, vp, i, i, i, i, ctypes.POINTER(Plan), u, vp]
+    lib.splitk_gemm_bf16_planned.restype = i
+    lib.splitk_gemm_bf16_hostio.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, vp]
+    lib.splitk_gemm_bf16_hostio.restype = i
+    lib.splitk_get_fault.argtypes = [ctypes.POINTER(Fault)]
+    lib.splitk_get_fault.restype = i
+    lib.splitk_get_status.argtypes = []
+    lib.splitk_get_status.restype = i
+    lib.splitk_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+    lib.splitk_set_wait_limit_ns.restype = i
+    lib.splitk_debug_inject.argtypes = [u]
+    lib.splitk_debug_inject.restype = i
+    lib.splitk_release.argtypes = []
+    lib.splitk_release.restype = None
+    lib.splitk_strerror.argtypes = [i]
+    lib.splitk_strerror.restype = ctypes.c_char_p
+    lib.splitk_version.argtypes = []
+    lib.splitk_version.restype = i
+    _lib = lib
+    return lib
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != 0:
+        raise SplitKError(rc, where)
+
+
+# ---------------------------------------------------------------- planning
+def splitk_plan(M: int, N: int, K: int, L: int = 1, split_k: int = 0) -> Plan:
+    out = Plan()
+    _check(load_library().splitk_plan(M, N, K, L, split_k, ctypes.byref(out)), "splitk_plan")
+    return out
+
+
+def splitk_plan_for(M: int, N: int, K: int, L: int, split_k: int, num_sms: int,
+                    smem_per_sm: int, smem_per_block_optin: int) -> Plan:
+    out = Plan()
+    _check(load_library().splitk_plan_for(M, N, K, L, split_k, num_sms, smem_per_sm,
+                                          smem_per_block_optin, ctypes.byref(out)),
+           "splitk_plan_for")
+    return out
+
+
+# ---------------------------------------------------------------- GEMM
+def _dims(a, b):
+    import torch
+    if a.dim() not in (2, 3) or b.dim() != a.dim():
+        raise ValueError("a is [L, N, K] or [N, K]; b is [L, M, K] or [M, K]")
+    if a.dtype != torch.bfloat16 or b.dtype != torch.bfloat16:
+        raise TypeError("a and b must be bfloat16")
+    if a.dim() == 2:
+        (N, K), (M, Kb), L = a.shape, b.shape, 1
+        Lb = 1
+    else:
+        (L, N, K), (Lb, M, Kb) = a.shape, b.shape
+    if K != Kb or L != Lb:
+        raise ValueError(f"shape mismatch: a{tuple(a.shape)} b{tuple(b.shape)}")
+    return int(M), int(N), int(K), int(L)
+
+
+def _stream_handle(stream, device):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(int(stream.cuda_stream))
+
+
+def _out(c, a, M, N, L):
+    import torch
+    shape = (M, N) if a.dim() == 2 else (L, M, N)
+    if c is None:
+        return torch.empty(shape, dtype=torch.bfloat16, device=a.device)
+    if tuple(c.shape) != shape or c.dtype != torch.bfloat16 or not c.is_contiguous():
+        raise ValueError(f"c must be a contiguous bfloat16 tensor of shape {shape}")
+    return c
+
+
+def _require_cuda(*ts):
+    for t in ts:
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("operands must be contiguous CUDA tensors")
+
+
+def splitk_gemm_bf16(a, b, c=None, split_k: int = 0, stream=None):
+    """c = b @ a^T (per batch), written once; returns c."""
+    import torch
+    M, N, K, L = _dims(a, b)
+    _require_cuda(a, b)
+    c = _out(c, a, M, N, L)
+    _require_cuda(c)
+    with torch.cuda.device(a.device):
+        rc = load_library().splitk_gemm_bf16(
+            a.data_ptr(), b.data_ptr(), c.data_ptr(), M, N, K, L, int(split_k),
+            _stream_handle(stream, a.device))
+    _check(rc, "splitk_gemm_bf16")
+    return c
+
+
+def splitk_gemm_bf16_planned(a, b, c, plan: Plan, flags: int = 0, stream=None):
+    import torch
+    M, N, K, L = _dims(a, b)
+    _require_cuda(a, b)
+    c = _out(c, a, M, N, L)
+    _require_cuda(c)
+    with torch.cuda.device(a.device):
+        rc = load_library().splitk_gemm_bf16_planned(
+            a.data_ptr(), b.data_ptr(), c.data_ptr(), M, N, K, L, ctypes.byref(plan),
+            int(flags), _stream_handle(stream, a.device))
+    _check(rc, "splitk_gemm_bf16_planned")
+    return c
+
+
+def splitk_gemm_bf16_hostio(a, b_host, c_host, b_dev, c_dev, split_k: int = 0, stream=None):
+    """Copies b_host -> b_dev, runs the GEMM, copies c_dev -> c_host (all async)."""
+    import torch
+    M, N, K, L = _dims(a, b_dev)
+    _require_cuda(a, b_dev, c_dev)
+    if b_host.is_cuda or c_host.is_cuda:
+        raise ValueError("b_host and c_host must be host tensors")
+    if b_host.numel() != b_dev.numel() or c_host.numel() != c_dev.numel() or \
+            c_dev.numel() != L * M * N:
+        raise ValueError("host and device buffers must match in size")
+    with torch.cuda.device(a.device):
+        rc = load_library().splitk_gemm_bf16_hostio(
+            a.data_ptr(), b_host.data_ptr(), c_host.data_ptr(), b_dev.data_ptr(),
+            c_dev.data_ptr(), M, N, K, L, int(split_k), _stream_handle(stream, a.device))
+    _check(rc, "splitk_gemm_bf16_hostio")
+    return c_host
+
+
+# ---------------------------------------------------------------- status
+def splitk_get_fault() -> dict:
+    f = Fault()
+    rc = load_library().splitk_get_fault(ctypes.byref(f))
+    if rc not in (0, -6):
+        raise SplitKError(rc, "splitk_get_fault")
+    return f.as_dict()
+
+
+def splitk_get_status() -> int:
+    return int(load_library().splitk_get_status())
+
+
+def splitk_set_wait_limit_ns(ns: int) -> None:
+    _check(load_library().splitk_set_wait_limit_ns(int(ns)), "splitk_set_wait_limit_ns")
+
+
+def splitk_debug_inject(flags: int) -> None:
+    _check(load_library().splitk_debug_inject(int(flags)), "splitk_debug_inject")
+
+
+def splitk_release() -> None:
+    load_library().splitk_release()
+
+
+def splitk_strerror(code: int) -> str:
+    return load_library().splitk_strerror(int(code)).decode()
+
+
+def splitk_version() -> int:
+    return int(load_library().splitk_version())

@@ -1,0 +1,542 @@
+// Host side of the C ABI (include/splitk.h): tactic planning, tensor-map
+// caches, argument checks and launch.
+//
+// The page's launcher (SplitKGemm.__call__ on the vLLM "splitk" API page)
+// launches grid (ceil(Mk/mma_m), ceil(Nk/mma_n) * split_k, L) with a
+// (1, split_k, 1) cluster, 256 threads, the whole shared memory of the SM and
+// PDL, and takes A's tensor map as a device address.  Here the cluster runs
+// along grid x (grid = (split_k * m_tiles, n_tiles, L)) so the CTAs that
+// share a weight tile are launched next to each other, shared memory is sized
+// from the occupancy the grid needs instead of taking the whole SM, and the
+// device tensor maps of A live in a pool owned by this library.
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <unordered_map>
+
+#include "splitk.h"
+#include "splitk_internal.h"
+
+namespace splitk {
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kMapPoolSlots = 4096;     // 512 KiB of device tensor maps
+constexpr size_t kBMapCacheMax = 1024;
+
+std::atomic<unsigned long long> g_wait_limit_ns{kDefaultWaitLimitNs};
+std::atomic<unsigned> g_inject{0};
+
+
+bool valid_split(int s) { return s == 1 || s == 2 || s == 4 || s == 8; }
+
+int choose_mma_n(int M) {
+  if (M <= 16) return 16;
+  if (M <= 32) return 32;
+  if (M <= 64) return 64;
+  return 128;
+}
+
+size_t smem_bytes_for(int mma_n, int stages, uint32_t dedicated_mailbox_bytes) {
+  return (size_t)kAlignSlack + (size_t)stages * (kAStageBytes + b_stage_bytes(mma_n)) +
+         dedicated_mailbox_bytes + kBarRegionBytes;
+}
+
+// Split-K choice without a measured table: the smallest split whose grid
+// covers every SM at least once; else the largest legal split.
+int auto_split(int K, long long tiles, int num_sms) {
+  int best = 0;
+  for (int s : {1, 2, 4, 8}) {
+    if (K % (kCtaK * s) != 0) continue;
+    best = s;
+    if (tiles * s >= num_sms) return s;
+  }
+  return best;
+}
+
+int plan_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t smem_per_sm,
+              size_t smem_optin, splitk_plan_t* out) {
+  if (!out) return SPLITK_ERR_NULL;
+  if (M < 1 || N < 1 || K < 1 || L < 1) return SPLITK_ERR_INVALID_SHAPE;
+  if (split_k != 0 && !valid_split(split_k)) return SPLITK_ERR_UNSUPPORTED_SPLIT;
+  if (num_sms < 1 || smem_optin < 1 || smem_per_sm < 1) return SPLITK_ERR_UNSUPPORTED_DEVICE;
+  if (K % kCtaK != 0) return SPLITK_ERR_INVALID_SHAPE;
+  const int mma_n = choose_mma_n(M);
+  const long long m_tiles = (M + mma_n - 1) / mma_n;
+  const long long n_tiles = ((long long)N + kMmaM - 1) / kMmaM;
+  if (n_tiles > 65535 || L > 65535) return SPLITK_ERR_INVALID_SHAPE;
+  int split = split_k;
+  if (split == 0) split = auto_split(K, m_tiles * n_tiles * L, num_sms);
+  if (split == 0 || K % (kCtaK * split) != 0) return SPLITK_ERR_INVALID_SHAPE;
+  if (m_tiles * split > 0x7FFFFFFFLL) return SPLITK_ERR_INVALID_SHAPE;
+  const int k_tiles = K / kCtaK / split;
+
+  // Shared memory is sized so the whole grid is resident at once when it
+  // needs at most 3 CTAs per SM; a smaller footprint also lets the next
+  // kernel's CTAs start streaming weights early (PDL).
+  const long long ctas = (long long)split * m_tiles * n_tiles * L;
+  int per_sm = (int)std::min<long long>(3, std::max<long long>(1, (ctas + num_sms - 1) / num_sms));
+  const int nquads_max = (std::min(M, mma_n) + 3) / 4;
+  const int qmax = max_quads_per_round(mma_n);
+  const int quads_full = std::min(nquads_max, qmax);
+  const uint32_t ded_bytes = split > 1 ? (uint32_t)(split - 1) * (uint32_t)quads_full * kQuadBytes : 0u;
+  const bool prefer_dedicated = split > 1 && ded_bytes <= 16u * 1024u;
+  const int stages_cap = std::min(kMaxStages, std::max(2, std::min(k_tiles, 4)));
+
+  for (; per_sm >= 1; --per_sm) {
+    const size_t budget = std::min(smem_optin, smem_per_sm / (size_t)per_sm - 1024);
+    for (int stages = stages_cap; stages >= 2; --stages) {
+      const uint32_t ded = prefer_dedicated ? ded_bytes : 0u;
+      const size_t smem = smem_bytes_for(mma_n, stages, ded);
+      if (smem > budget) continue;
+      int quads = quads_full;
+      if (split > 1 && !prefer_dedicated) {
+        const int cap = (int)(((uint32_t)stages * kAStageBytes) / ((uint32_t)(split - 1) * kQuadBytes));
+        quads = std::max(1, std::min(quads_full, cap));
+      }
+      out->mma_m = kMmaM;
+      out->mma_n = mma_n;
+      out->stages = stages;
+      out->split_k = split;
+      out->k_tiles_per_cta = k_tiles;
+      out->mailbox_dedicated = prefer_dedicated ? 1 : 0;
+      out->mailbox_quads = split > 1 ? quads : quads_full;
+      out->reduce_rounds = split > 1 ? (nquads_max + quads - 1) / quads : 0;
+      out->grid[0] = (unsigned)(split * m_tiles);
+      out->grid[1] = (unsigned)n_tiles;
+      out->grid[2] = (unsigned)L;
+      out->cluster[0] = (unsigned)split;
+      out->cluster[1] = 1;
+      out->cluster[2] = 1;
+      out->smem_bytes = smem;
+      out->ctas_per_sm = per_sm;
+      return SPLITK_OK;
+    }
+  }
+  return SPLITK_ERR_NO_FIT;
+}
+
+// Re-derives everything a plan implies and checks it against the shape.
+int check_plan(const splitk_plan_t& pl, int M, int N, int K, int L, size_t smem_optin,
+               uint32_t* dedicated_bytes) {
+  if (pl.mma_m != kMmaM) return SPLITK_ERR_BAD_PLAN;
+  if (pl.mma_n != 16 && pl.mma_n != 32 && pl.mma_n != 64 && pl.mma_n != 128) return SPLITK_ERR_BAD_PLAN;
+  if (!valid_split(pl.split_k)) return SPLITK_ERR_UNSUPPORTED_SPLIT;
+  if (K % (kCtaK * pl.split_k) != 0) return SPLITK_ERR_INVALID_SHAPE;
+  if (pl.k_tiles_per_cta != K / kCtaK / pl.split_k) return SPLITK_ERR_BAD_PLAN;
+  if (pl.stages < 2 || pl.stages > kMaxStages) return SPLITK_ERR_BAD_PLAN;
+  const long long m_tiles = (M + pl.mma_n - 1) / pl.mma_n;
+  const long long n_tiles = ((long long)N + kMmaM - 1) / kMmaM;
+  if (n_tiles > 65535 || L > 65535) return SPLITK_ERR_INVALID_SHAPE;
+  if (pl.grid[0] != (unsigned)(pl.split_k * m_tiles) || pl.grid[1] != (unsigned)n_tiles ||
+      pl.grid[2] != (unsigned)L || pl.cluster[0] != (unsigned)pl.split_k || pl.cluster[1] != 1 ||
+      pl.cluster[2] != 1) {
+    return SPLITK_ERR_BAD_PLAN;
+  }
+  const int nquads_max = (std::min(M, pl.mma_n) + 3) / 4;
+  const int qmax = max_quads_per_round(pl.mma_n);
+  if (pl.mailbox_quads < 1 || pl.mailbox_quads > qmax) return SPLITK_ERR_BAD_PLAN;
+  uint32_t ded = 0;
+  if (pl.split_k > 1) {
+    const uint32_t round_bytes = (uint32_t)(pl.split_k - 1) * (uint32_t)pl.mailbox_quads * kQuadBytes;
+    if (pl.mailbox_dedicated) {
+      ded = round_bytes;
+    } else if (round_bytes > (uint32_t)pl.stages * kAStageBytes) {
+      return SPLITK_ERR_BAD_PLAN;
+    }
+  }
+  (void)nquads_max;
+  const size_t smem = smem_bytes_for(pl.mma_n, pl.stages, ded);
+  if (smem != pl.smem_bytes) return SPLITK_ERR_BAD_PLAN;
+  if (smem > smem_optin) return SPLITK_ERR_NO_FIT;
+  *dedicated_bytes = ded;
+  return SPLITK_OK;
+}
+
+// ------------------------------------------------------------ tensor maps
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess) {
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+  });
+  return fn;
+}
+
+// A 3-D bf16 tensor [d2][d1][d0] (d0 contiguous) read in boxes of
+// {64, rows, 1} with the 128-byte swizzle; out-of-range rows read as zero.
+bool encode_3d(CUtensorMap* map, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2,
+               uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {d0 * 2u, d0 * d1 * 2u};
+  cuuint32_t box[3] = {(cuuint32_t)kAtomK, box_rows, 1u};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+struct AKey {
+  uintptr_t ptr;
+  int N, K, L;
+  bool operator==(const AKey& o) const { return ptr == o.ptr && N == o.N && K == o.K && L == o.L; }
+};
+struct BKey {
+  uintptr_t ptr;
+  int M, K, L, rows;
+  bool operator==(const BKey& o) const {
+    return ptr == o.ptr && M == o.M && K == o.K && L == o.L && rows == o.rows;
+  }
+};
+inline uint64_t mix(uint64_t h, uint64_t v) {
+  h ^= v + 0x9E3779B97F4A7C15ull + (h << 6) + (h >> 2);
+  return h;
+}
+struct AKeyHash {
+  size_t operator()(const AKey& k) const {
+    return (size_t)mix(mix(mix(mix(0, k.ptr), (uint64_t)k.N), (uint64_t)k.K), (uint64_t)k.L);
+  }
+};
+struct BKeyHash {
+  size_t operator()(const BKey& k) const {
+    return (size_t)mix(mix(mix(mix(mix(0, k.ptr), (uint64_t)k.M), (uint64_t)k.K), (uint64_t)k.L),
+                       (uint64_t)k.rows);
+  }
+};
+
+struct DeviceState {
+  bool ready = false;
+  int num_sms = 0;
+  size_t smem_per_sm = 0;
+  size_t smem_optin = 0;
+  CUtensorMap* d_pool = nullptr;   // device tensor maps of A
+  CUtensorMap* h_pool = nullptr;   // pinned mirror, never rewritten once used
+  int used = 0;
+  std::unordered_map<AKey, int, AKeyHash> a_slots;
+  std::unordered_map<BKey, CUtensorMap, BKeyHash> b_maps;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+
+// Caller holds g_mu.  Returns the current device's state, initialised.
+int current_device(DeviceState** out, int* dev_out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return SPLITK_ERR_UNSUPPORTED_DEVICE;
+  }
+  DeviceState& st = g_dev[dev];
+  if (!st.ready) {
+    int major = 0, minor = 0, sms = 0, optin = 0, per_sm = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) !=
+            cudaSuccess) {
+      cudaGetLastError();
+      return SPLITK_ERR_UNSUPPORTED_DEVICE;
+    }
+    if (major != 10 || minor != 3) return SPLITK_ERR_UNSUPPORTED_DEVICE;
+    if (!encode_fn()) return SPLITK_ERR_CUDA;
+    if (prepare_kernels(optin) != cudaSuccess) {
+      cudaGetLastError();
+      return SPLITK_ERR_CUDA;
+    }
+    st.num_sms = sms;
+    st.smem_optin = (size_t)optin;
+    st.smem_per_sm = (size_t)per_sm;
+    st.ready = true;
+  }
+  *out = &st;
+  if (dev_out) *dev_out = dev;
+  return SPLITK_OK;
+}
+
+// Caller holds g_mu.  Device address of A's tensor map, encoding and
+// copying it on `stream` the first time.
+int a_map_for(DeviceState& st, const void* a, int N, int K, int L, cudaStream_t stream,
+              const CUtensorMap** out) {
+  AKey key{(uintptr_t)a, N, K, L};
+  auto it = st.a_slots.find(key);
+  if (it != st.a_slots.end()) {
+    *out = st.d_pool + it->second;
+    return SPLITK_OK;
+  }
+  if (!st.d_pool) {
+    if (cudaMalloc((void**)&st.d_pool, sizeof(CUtensorMap) * kMapPoolSlots) != cudaSuccess) {
+      cudaGetLastError();
+      st.d_pool = nullptr;
+      return SPLITK_ERR_CUDA;
+    }
+    if (cudaMallocHost((void**)&st.h_pool, sizeof(CUtensorMap) * kMapPoolSlots) != cudaSuccess) {
+      cudaGetLastError();
+      cudaFree(st.d_pool);
+      st.d_pool = nullptr;
+      st.h_pool = nullptr;
+      return SPLITK_ERR_CUDA;
+    }
+    st.used = 0;
+  }
+  if (st.used >= kMapPoolSlots) return SPLITK_ERR_CACHE_FULL;
+  const int slot = st.used;
+  if (!encode_3d(&st.h_pool[slot], a, (uint64_t)K, (uint64_t)N, (uint64_t)L, (uint32_t)kMmaM)) {
+    return SPLITK_ERR_CUDA;
+  }
+  if (cudaMemcpyAsync(st.d_pool + slot, st.h_pool + slot, sizeof(CUtensorMap), cudaMemcpyHostToDevice,
+                      stream) != cudaSuccess) {
+    cudaGetLastError();
+    return SPLITK_ERR_CUDA;
+  }
+  st.used = slot + 1;
+  st.a_slots.emplace(key, slot);
+  *out = st.d_pool + slot;
+  return SPLITK_OK;
+}
+
+int b_map_for(DeviceState& st, const void* b, int M, int K, int L, int rows, CUtensorMap* out) {
+  BKey key{(uintptr_t)b, M, K, L, rows};
+  auto it = st.b_maps.find(key);
+  if (it != st.b_maps.end()) {
+    *out = it->second;
+    return SPLITK_OK;
+  }
+  CUtensorMap m;
+  if (!encode_3d(&m, b, (uint64_t)K, (uint64_t)M, (uint64_t)L, (uint32_t)rows)) return SPLITK_ERR_CUDA;
+  if (st.b_maps.size() >= kBMapCacheMax) st.b_maps.clear();
+  st.b_maps.emplace(key, m);
+  *out = m;
+  return SPLITK_OK;
+}
+
+int check_pointers(const void* a, const void* b, const void* c) {
+  if (!a || !b || !c) return SPLITK_ERR_NULL;
+  if (((uintptr_t)a & 15u) || ((uintptr_t)b & 15u) || ((uintptr_t)c & 1u)) return SPLITK_ERR_MISALIGNED;
+  return SPLITK_OK;
+}
+
+// Caller holds g_mu.
+int launch_locked(DeviceState& st, const void* a, const void* b, void* c, int M, int N, int K, int L,
+                  const splitk_plan_t& pl, unsigned flags, cudaStream_t stream) {
+  uint32_t ded = 0;
+  int rc = check_plan(pl, M, N, K, L, st.smem_optin, &ded);
+  if (rc != SPLITK_OK) return rc;
+  const CUtensorMap* a_map = nullptr;
+  rc = a_map_for(st, a, N, K, L, stream, &a_map);
+  if (rc != SPLITK_OK) return rc;
+  CUtensorMap b_map;
+  rc = b_map_for(st, b, M, K, L, pl.mma_n, &b_map);
+  if (rc != SPLITK_OK) return rc;
+
+  KernelParams p;
+  p.a_map = a_map;
+  p.c = static_cast<uint16_t*>(c);
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.L = L;
+  p.split = pl.split_k;
+  p.stages = pl.stages;
+  p.k_tiles = pl.k_tiles_per_cta;
+  p.mailbox_dedicated = pl.split_k > 1 ? pl.mailbox_dedicated : 0;
+  p.mailbox_bytes = ded;
+  p.mailbox_quads = pl.mailbox_quads;
+  p.vec_store = ((N % 8) == 0 && ((uintptr_t)c & 15u) == 0) ? 1 : 0;
+  p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+  p.inject = g_inject.load(std::memory_order_relaxed);
+
+  LaunchArgs la;
+  la.mma_n = pl.mma_n;
+  la.grid = dim3(pl.grid[0], pl.grid[1], pl.grid[2]);
+  la.cluster_x = (unsigned)pl.split_k;
+  la.smem_bytes = pl.smem_bytes;
+  la.pdl = (flags & SPLITK_FLAG_NO_PDL) == 0;
+  if (launch_kernel(la, b_map, p, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return SPLITK_ERR_CUDA;
+  }
+  return SPLITK_OK;
+}
+
+int gemm_auto(const void* a, const void* b, void* c, int M, int N, int K, int L, int split_k,
+              unsigned flags, cudaStream_t stream) {
+  int rc = check_pointers(a, b, c);
+  if (rc != SPLITK_OK) return rc;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* st = nullptr;
+  rc = current_device(&st, nullptr);
+  if (rc != SPLITK_OK) return rc;
+  splitk_plan_t pl;
+  rc = plan_impl(M, N, K, L, split_k, st->num_sms, st->smem_per_sm, st->smem_optin, &pl);
+  if (rc != SPLITK_OK) return rc;
+  return launch_locked(*st, a, b, c, M, N, K, L, pl, flags, stream);
+}
+
+}  // namespace
+}  // namespace splitk
+
+using namespace splitk;
+
+extern "C" {
+
+SPLITK_API int splitk_plan_for(int M, int N, int K, int L, int split_k, int num_sms, size_t smem_per_sm,
+                               size_t smem_per_block_optin, splitk_plan_t* out) {
+  return plan_impl(M, N, K, L, split_k, num_sms, smem_per_sm, smem_per_block_optin, out);
+}
+
+SPLITK_API int splitk_plan(int M, int N, int K, int L, int split_k, splitk_plan_t* out) {
+  if (!out) return SPLITK_ERR_NULL;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* st = nullptr;
+  int rc = current_device(&st, nullptr);
+  if (rc != SPLITK_OK) return rc;
+  return plan_impl(M, N, K, L, split_k, st->num_sms, st->smem_per_sm, st->smem_optin, out);
+}
+
+SPLITK_API int splitk_gemm_bf16(const void* a, const void* b, void* c, int M, int N, int K, int L,
+                                int split_k, splitk_stream_t stream) {
+  return gemm_auto(a, b, c, M, N, K, L, split_k, 0u, reinterpret_cast<cudaStream_t>(stream));
+}
+
+SPLITK_API int splitk_gemm_bf16_planned(const void* a, const void* b, void* c, int M, int N, int K,
+                                        int L, const splitk_plan_t* plan, unsigned flags,
+                                        splitk_stream_t stream) {
+  if (!plan) return SPLITK_ERR_NULL;
+  int rc = check_pointers(a, b, c);
+  if (rc != SPLITK_OK) return rc;
+  if (M < 1 || N < 1 || K < 1 || L < 1) return SPLITK_ERR_INVALID_SHAPE;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* st = nullptr;
+  rc = current_device(&st, nullptr);
+  if (rc != SPLITK_OK) return rc;
+  return launch_locked(*st, a, b, c, M, N, K, L, *plan, flags, reinterpret_cast<cudaStream_t>(stream));
+}
+
+SPLITK_API int splitk_gemm_bf16_hostio(const void* a, const void* b_host, void* c_host, void* b_dev,
+                                       void* c_dev, int M, int N, int K, int L, int split_k,
+                                       splitk_stream_t stream) {
+  if (!b_host || !c_host) return SPLITK_ERR_NULL;
+  int rc = check_pointers(a, b_dev, c_dev);
+  if (rc != SPLITK_OK) return rc;
+  if (M < 1 || N < 1 || K < 1 || L < 1) return SPLITK_ERR_INVALID_SHAPE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* st = nullptr;
+  rc = current_device(&st, nullptr);
+  if (rc != SPLITK_OK) return rc;
+  splitk_plan_t pl;
+  rc = plan_impl(M, N, K, L, split_k, st->num_sms, st->smem_per_sm, st->smem_optin, &pl);
+  if (rc != SPLITK_OK) return rc;
+  const size_t b_bytes = (size_t)L * (size_t)M * (size_t)K * 2u;
+  const size_t c_bytes = (size_t)L * (size_t)M * (size_t)N * 2u;
+  if (cudaMemcpyAsync(b_dev, b_host, b_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) {
+    cudaGetLastError();
+    return SPLITK_ERR_CUDA;
+  }
+  rc = launch_locked(*st, a, b_dev, c_dev, M, N, K, L, pl, 0u, s);
+  if (rc != SPLITK_OK) return rc;
+  if (cudaMemcpyAsync(c_host, c_dev, c_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) {
+    cudaGetLastError();
+    return SPLITK_ERR_CUDA;
+  }
+  return SPLITK_OK;
+}
+
+SPLITK_API int splitk_get_fault(splitk_fault_t* out) {
+  int words[kFaultWords] = {0};
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+      cudaGetLastError();
+      return SPLITK_ERR_UNSUPPORTED_DEVICE;
+    }
+    if (read_and_clear_fault(words) != cudaSuccess) {
+      cudaGetLastError();
+      return SPLITK_ERR_CUDA;
+    }
+  }
+  if (out) {
+    out->code = words[0];
+    out->role = words[1];
+    out->index = words[2];
+    out->parity = words[3];
+    out->block[0] = words[4];
+    out->block[1] = words[5];
+    out->block[2] = words[6];
+    out->cluster_rank = words[7];
+  }
+  return words[0] == 0 ? SPLITK_OK : SPLITK_ERR_TIMEOUT;
+}
+
+SPLITK_API int splitk_get_status(void) { return splitk_get_fault(nullptr); }
+
+SPLITK_API int splitk_set_wait_limit_ns(uint64_t ns) {
+  g_wait_limit_ns.store(ns == 0 ? kDefaultWaitLimitNs : (unsigned long long)ns);
+  return SPLITK_OK;
+}
+
+SPLITK_API int splitk_debug_inject(unsigned flags) {
+  g_inject.store(flags & kInjectSkipPublish);
+  return SPLITK_OK;
+}
+
+SPLITK_API void splitk_release(void) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  int prev = -1;
+  bool have_prev = cudaGetDevice(&prev) == cudaSuccess;
+  for (int d = 0; d < kMaxDevices; ++d) {
+    DeviceState& st = g_dev[d];
+    if (!st.ready) continue;
+    if (cudaSetDevice(d) == cudaSuccess) {
+      cudaDeviceSynchronize();
+      if (st.d_pool) cudaFree(st.d_pool);
+      if (st.h_pool) cudaFreeHost(st.h_pool);
+    }
+    st.d_pool = nullptr;
+    st.h_pool = nullptr;
+    st.used = 0;
+    st.a_slots.clear();
+    st.b_maps.clear();
+  }
+  if (have_prev) cudaSetDevice(prev);
+  cudaGetLastError();
+}
+
+SPLITK_API const char* splitk_strerror(int code) {
+  switch (code) {
+    case SPLITK_OK: return "success";
+    case SPLITK_ERR_INVALID_SHAPE: return "invalid shape (M, N, K, L >= 1; K a multiple of 128*split_k)";
+    case SPLITK_ERR_MISALIGNED: return "misaligned pointer (A and B need 16 bytes, C 2 bytes)";
+    case SPLITK_ERR_UNSUPPORTED_SPLIT: return "split_k must be 0, 1, 2, 4 or 8";
+    case SPLITK_ERR_NO_FIT: return "no tactic fits the shared-memory budget";
+    case SPLITK_ERR_CUDA: return "a CUDA call failed";
+    case SPLITK_ERR_TIMEOUT: return "a bounded wait in the kernel ran out";
+    case SPLITK_ERR_NULL: return "null pointer argument";
+    case SPLITK_ERR_CACHE_FULL: return "device tensor-map pool full; call splitk_release()";
+    case SPLITK_ERR_UNSUPPORTED_DEVICE: return "no CUDA device of compute capability 10.3";
+    case SPLITK_ERR_BAD_PLAN: return "plan does not match the shape";
+    default: return "unknown status code";
+  }
+}
+
+SPLITK_API int splitk_version(void) { return 10000; }
+
+}  // extern "C"

@@ -1,0 +1,440 @@
+// The split-K BF16 decode GEMM kernel for sm_103a (GB300).
+//
+//   C[l][m][n] = bf16_rne( sum_k A[l][n][k] * B[l][m][k] )
+//
+// Method: the vLLM "splitk" API page (module
+// vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.gemm.splitk, class
+// SplitKGemm): a thread-block cluster of split_k CTAs shares one output tile;
+// rank r accumulates the contiguous K slice [r*K/split_k, (r+1)*K/split_k) in
+// FP32; ranks != 0 publish their partials into rank 0's shared memory over
+// DSMEM (st.async, completion counted in bytes on rank 0's mbarrier); rank 0
+// waits at cluster scope, adds them in rank order, converts once to BF16 and
+// stores.  Operands are swapped: 128 weight rows (public N) on the tcgen05
+// MMA M dimension, the tokens (public M) on MMA N.
+//
+// CTA roles (256 threads):
+//   warp 0      weight (A) producer: TMA from a tensor map in global memory,
+//               L2 evict_first, issued before the programmatic-dependent-launch
+//               wait; then launch_dependents (SplitKGemm.weight_warp)
+//   warp 1      activation (B) producer: griddepcontrol.wait, then TMA
+//               (SplitKGemm.activation_warp)
+//   warp 2      TMEM allocation, tcgen05.mma issue, TMEM release (mma_warp)
+//   warp 3      idle (keeps warps 4..7 on TMEM lane quadrants 0..3)
+//   warps 4..7  epilogue: TMEM -> registers, DSMEM publish / rank-0 reduce,
+//               BF16 packing, 16-byte stores (epilog_warp)
+//
+// Every mbarrier wait is bounded by %globaltimer (the Muse Spark AMD dev
+// page's _spin_bounded: a timeout records a diagnostic, sets a sticky failed
+// flag, and the CTA's later waits give up at once); TMEM is always released
+// and every CTA of a cluster meets at a final cluster barrier, so a failed
+// launch ends with no copy in flight into a departed CTA.
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "splitk.h"
+#include "splitk_device.cuh"
+#include "splitk_internal.h"
+
+namespace splitk {
+
+// First timeout of the device since the last read: code, role, index,
+// parity, blockIdx.{x,y,z}, cluster rank.
+__device__ int g_fault[kFaultWords];
+
+namespace {
+
+struct Waiter {
+  uint32_t abort_flag;            // shared-memory u32, sticky per CTA
+  unsigned long long limit_ns;
+
+  __device__ __forceinline__ void record(int role, int index, uint32_t parity) const {
+    if (atomicCAS(&g_fault[0], 0, (int)SPLITK_ERR_TIMEOUT) == 0) {
+      g_fault[1] = role;
+      g_fault[2] = index;
+      g_fault[3] = (int)parity;
+      g_fault[4] = (int)blockIdx.x;
+      g_fault[5] = (int)blockIdx.y;
+      g_fault[6] = (int)blockIdx.z;
+      g_fault[7] = (int)dev::cluster_ctarank();
+      __threadfence();
+    }
+  }
+
+  // Waits for the phase of `bar` with `parity` to complete.  Returns false if
+  // the limit ran out (and records it) or another wait of the CTA failed.
+  template <bool kClusterScope>
+  __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, int role, int index) const {
+    auto poll = [&]() {
+      return kClusterScope ? dev::mbar_try_wait_cluster(bar, parity) : dev::mbar_try_wait(bar, parity);
+    };
+    if (poll()) return true;
+    const uint64_t t0 = dev::globaltimer_ns();
+    while (true) {
+      if (poll()) return true;
+      if (dev::ld_shared_u32(abort_flag) != 0u) return false;
+      if (dev::globaltimer_ns() - t0 > limit_ns) {
+        dev::st_shared_u32(abort_flag, 1u);
+        record(role, index, parity);
+        return false;
+      }
+    }
+  }
+};
+
+}  // namespace
+
+template <int MMA_N>
+__global__ void __launch_bounds__(kThreads, 1)
+    splitk_gemm_bf16_kernel(const __grid_constant__ CUtensorMap b_map, const KernelParams p) {
+  constexpr uint32_t kBStage = b_stage_bytes(MMA_N);
+  constexpr uint32_t kBBox = kBStage / 2;                   // MMA_N rows x 128 B
+  constexpr int kQMax = max_quads_per_round(MMA_N);         // register budget
+  constexpr uint32_t kTmemCols = MMA_N < 32 ? 32u : (uint32_t)MMA_N;
+  constexpr uint32_t kIdesc = dev::idesc_bf16_f32(kMmaM, MMA_N);
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = dev::smem_u32(smem_raw);
+  const uint32_t base = (raw + (kAlignSlack - 1)) & ~(kAlignSlack - 1);
+
+  const int warp = (int)(threadIdx.x >> 5);
+  const int lane = (int)(threadIdx.x & 31);
+  const int split = p.split;
+  const int stages = p.stages;
+  const int rank = split > 1 ? (int)dev::cluster_ctarank() : 0;
+  const int m_tile = (int)blockIdx.x / split;
+  const int n0 = (int)blockIdx.y * kMmaM;
+  const int m0 = m_tile * MMA_N;
+  const int l = (int)blockIdx.z;
+  const int k_tiles = p.k_tiles;
+  const int kt0 = rank * k_tiles;
+
+  // Shared memory: [A ring][B ring][dedicated mailbox?][barriers].
+  const uint32_t sA = base;
+  const uint32_t sB = sA + (uint32_t)stages * kAStageBytes;
+  const uint32_t ring_end = sB + (uint32_t)stages * kBStage;
+  const uint32_t sMail = p.mailbox_dedicated ? ring_end : sA;
+  const uint32_t sBar = ring_end + (p.mailbox_dedicated ? p.mailbox_bytes : 0u);
+  const uint32_t bar_full0 = sBar;                       // [kMaxStages], count 2
+  const uint32_t bar_empty0 = sBar + 8u * kMaxStages;    // [kMaxStages], count 1
+  const uint32_t bar_mma_done = sBar + 16u * kMaxStages; // count 1
+  const uint32_t bar_tmem_empty = bar_mma_done + 8u;     // count 128
+  const uint32_t bar_reduce = bar_mma_done + 16u;        // count 1 + tx bytes
+  const uint32_t bar_ready = bar_mma_done + 24u;         // count 1 (rank 0 arrives)
+  const uint32_t slot_tmem = bar_mma_done + 32u;
+  const uint32_t slot_abort = bar_mma_done + 36u;
+
+  const Waiter waiter{slot_abort, p.wait_limit_ns};
+
+  // ---- set-up: barriers (thread 0), TMEM (warp 2), first weight loads.
+  int a_issued = 0;
+  uint64_t a_policy = 0;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      dev::mbar_init(bar_full0 + 8u * s, 2);
+      dev::mbar_init(bar_empty0 + 8u * s, 1);
+    }
+    dev::mbar_init(bar_mma_done, 1);
+    dev::mbar_init(bar_tmem_empty, kEpiThreads);
+    dev::mbar_init(bar_reduce, 1);
+    dev::mbar_init(bar_ready, 1);
+    dev::st_shared_u32(slot_abort, 0u);
+    dev::fence_barrier_init();
+    // The weight stream does not depend on the previous kernel: start it now.
+    dev::tensormap_acquire(p.a_map);
+    a_policy = dev::policy_evict_first();
+    const int first = k_tiles < stages ? k_tiles : stages;
+    for (; a_issued < first; ++a_issued) {
+      const uint32_t full = bar_full0 + 8u * a_issued;
+      const uint32_t dst = sA + (uint32_t)a_issued * kAStageBytes;
+      const int k = (kt0 + a_issued) * kCtaK;
+      dev::mbar_arrive_expect_tx(full, kAStageBytes);
+      dev::tma_load_3d_hint(dst, p.a_map, k, n0, l, full, a_policy);
+      dev::tma_load_3d_hint(dst + kABoxBytes, p.a_map, k + kAtomK, n0, l, full, a_policy);
+    }
+  }
+  if (warp == 2) {
+    dev::tmem_alloc(slot_tmem, kTmemCols);
+    dev::tmem_relinquish();
+    dev::tc_fence_before();
+  }
+  // Peers' barriers must exist before any remote arrival or st.async.
+  if (split > 1) {
+    dev::cluster_arrive_release();
+    dev::cluster_wait_acquire();
+  } else {
+    __syncthreads();
+  }
+  dev::tc_fence_after();
+  const uint32_t tmem_base = dev::ld_shared_u32(slot_tmem);
+
+  if (warp == 0) {
+    // ---- weight producer
+    if (lane == 0) {
+      for (int kt = a_issued; kt < k_tiles; ++kt) {
+        const int s = kt % stages;
+        const int r = kt / stages;
+        const uint32_t full = bar_full0 + 8u * s;
+        if (!waiter.wait<false>(bar_empty0 + 8u * s, (uint32_t)((r - 1) & 1), kRoleWeightTma, kt)) break;
+        const uint32_t dst = sA + (uint32_t)s * kAStageBytes;
+        const int k = (kt0 + kt) * kCtaK;
+        dev::mbar_arrive_expect_tx(full, kAStageBytes);
+        dev::tma_load_3d_hint(dst, p.a_map, k, n0, l, full, a_policy);
+        dev::tma_load_3d_hint(dst + kABoxBytes, p.a_map, k + kAtomK, n0, l, full, a_policy);
+      }
+      dev::griddep_launch_dependents();
+    }
+  } else if (warp == 1) {
+    // ---- activation producer: B may be the previous kernel's output.
+    if (lane == 0) {
+      dev::griddep_wait();
+      for (int kt = 0; kt < k_tiles; ++kt) {
+        const int s = kt % stages;
+        const int r = kt / stages;
+        const uint32_t full = bar_full0 + 8u * s;
+        if (kt >= stages &&
+            !waiter.wait<false>(bar_empty0 + 8u * s, (uint32_t)((r - 1) & 1), kRoleActTma, kt)) {
+          break;
+        }
+        const uint32_t dst = sB + (uint32_t)s * kBStage;
+        const int k = (kt0 + kt) * kCtaK;
+        dev::mbar_arrive_expect_tx(full, kBStage);
+        dev::tma_load_3d(dst, &b_map, k, m0, l, full);
+        dev::tma_load_3d(dst + kBBox, &b_map, k + kAtomK, m0, l, full);
+      }
+    }
+  } else if (warp == 2) {
+    // ---- MMA issuer: D[128 x MMA_N] += A[128 x 16] * B[MMA_N x 16]^T, 8 per K tile.
+    if (lane == 0) {
+      for (int kt = 0; kt < k_tiles; ++kt) {
+        const int s = kt % stages;
+        const int r = kt / stages;
+        if (!waiter.wait<false>(bar_full0 + 8u * s, (uint32_t)(r & 1), kRoleMma, kt)) break;
+        dev::tc_fence_after();
+        const uint32_t a_st = sA + (uint32_t)s * kAStageBytes;
+        const uint32_t b_st = sB + (uint32_t)s * kBStage;
+#pragma unroll
+        for (int kk = 0; kk < kCtaK / kMmaK; ++kk) {
+          const uint32_t a_off = (uint32_t)(kk >> 2) * kABoxBytes + (uint32_t)(kk & 3) * 32u;
+          const uint32_t b_off = (uint32_t)(kk >> 2) * kBBox + (uint32_t)(kk & 3) * 32u;
+          dev::mma_bf16(tmem_base, dev::smem_desc_sw128(a_st + a_off),
+                        dev::smem_desc_sw128(b_st + b_off), kIdesc, (kt | kk) != 0 ? 1u : 0u);
+        }
+        dev::mma_commit(bar_empty0 + 8u * s);  // stage free once these MMAs finish
+      }
+      dev::mma_commit(bar_mma_done);           // accumulator complete
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ---- epilogue: thread et owns TMEM lane et = weight row n0 + et.
+    const int et = (int)threadIdx.x - 128;
+    const uint32_t t_row = tmem_base + ((uint32_t)((warp & 3) * 32) << 16);
+    const int ncols = (p.M - m0) < MMA_N ? (p.M - m0) : MMA_N;    // real token columns
+    const int nquads = (ncols + 3) >> 2;
+    const int qr = p.mailbox_quads;
+    const bool owner = rank == 0;
+    const uint32_t stage_f32 = sB;   // rank 0's drained B ring: f32 [ncols][128]
+
+    waiter.wait<false>(bar_mma_done, 0u, kRoleEpiMma, 0);
+    __syncwarp();
+    dev::tc_fence_after();
+
+    int round = 0;
+    for (int qb = 0; qb < nquads; qb += qr, ++round) {
+      const int nq = (nquads - qb) < qr ? (nquads - qb) : qr;
+      uint32_t v[kQMax * 4];
+      __syncwarp();   // tcgen05.ld is warp-collective
+#pragma unroll
+      for (int j = 0; j < kQMax; ++j) {
+        if (j < nq) {
+          dev::tmem_ld_x4(t_row + (uint32_t)((qb + j) * 4), v[4 * j], v[4 * j + 1], v[4 * j + 2],
+                          v[4 * j + 3]);
+        } else {
+          v[4 * j] = v[4 * j + 1] = v[4 * j + 2] = v[4 * j + 3] = 0u;
+        }
+      }
+      dev::tmem_wait_ld();
+
+      if (split > 1) {
+        // The aliased mailbox (and any later round) waits for rank 0 to free it.
+        const bool need_ready = !(p.mailbox_dedicated && round == 0);
+        const uint32_t ready_parity = (uint32_t)((round - (p.mailbox_dedicated ? 1 : 0)) & 1);
+        const uint32_t round_bytes = (uint32_t)(split - 1) * (uint32_t)nq * kQuadBytes;
+        if (!owner) {
+          if (!(p.inject & kInjectSkipPublish)) {
+            if (!need_ready ||
+                waiter.wait<true>(bar_ready, ready_parity, kRoleEpiReady, round)) {
+              const uint32_t r_mail = dev::mapa(sMail, 0);
+              const uint32_t r_bar = dev::mapa(bar_reduce, 0);
+#pragma unroll
+              for (int j = 0; j < kQMax; ++j) {
+                if (j < nq) {
+                  const uint32_t off =
+                      ((uint32_t)((rank - 1) * nq + j) * kEpiThreads + (uint32_t)et) * 16u;
+                  dev::st_async_v4(r_mail + off, v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3],
+                                   r_bar);
+                }
+              }
+            }
+          }
+        } else {
+          if (et == 0) {
+            dev::mbar_arrive_expect_tx(bar_reduce, round_bytes);
+            if (need_ready) {
+              for (int peer = 1; peer < split; ++peer) {
+                dev::mbar_arrive_remote(dev::mapa(bar_ready, (uint32_t)peer));
+              }
+            }
+          }
+          waiter.wait<true>(bar_reduce, (uint32_t)(round & 1), kRoleEpiReduce, round);
+          // Owner's partial + peers 1, 2, ... in rank order.
+          for (int peer = 1; peer < split; ++peer) {
+#pragma unroll
+            for (int j = 0; j < kQMax; ++j) {
+              if (j < nq) {
+                uint32_t w0, w1, w2, w3;
+                const uint32_t off =
+                    ((uint32_t)((peer - 1) * nq + j) * kEpiThreads + (uint32_t)et) * 16u;
+                dev::ld_shared_v4(sMail + off, w0, w1, w2, w3);
+                v[4 * j] = __float_as_uint(__uint_as_float(v[4 * j]) + __uint_as_float(w0));
+                v[4 * j + 1] = __float_as_uint(__uint_as_float(v[4 * j + 1]) + __uint_as_float(w1));
+                v[4 * j + 2] = __float_as_uint(__uint_as_float(v[4 * j + 2]) + __uint_as_float(w2));
+                v[4 * j + 3] = __float_as_uint(__uint_as_float(v[4 * j + 3]) + __uint_as_float(w3));
+              }
+            }
+          }
+          // Every owner thread has read this round before the mailbox is reused.
+          if (qb + qr < nquads) dev::named_bar_sync(1, kEpiThreads);
+        }
+      }
+
+      if (owner) {
+#pragma unroll
+        for (int j = 0; j < kQMax; ++j) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int m = (qb + j) * 4 + i;
+            if (j < nq && m < ncols) {
+              dev::st_shared_f32(stage_f32 + ((uint32_t)m * kMmaM + (uint32_t)et) * 4u,
+                                 __uint_as_float(v[4 * j + i]));
+            }
+          }
+        }
+      }
+    }
+    // TMEM reads are done: let warp 2 release it.
+    dev::tc_fence_before();
+    dev::mbar_arrive(bar_tmem_empty);
+
+    if (owner) {
+      // Rank 0 stores the tile: 16 vectors of 8 bf16 per token row, coalesced along n.
+      dev::named_bar_sync(1, kEpiThreads);
+      const int total = ncols * (kMmaM / 8);
+      for (int idx = et; idx < total; idx += kEpiThreads) {
+        const int row = idx >> 4;
+        const int c8 = (idx & 15) * 8;
+        const int n = n0 + c8;
+        if (n >= p.N) continue;
+        uint32_t x0, x1, x2, x3, y0, y1, y2, y3;
+        const uint32_t src = stage_f32 + ((uint32_t)row * kMmaM + (uint32_t)c8) * 4u;
+        dev::ld_shared_v4(src, x0, x1, x2, x3);
+        dev::ld_shared_v4(src + 16u, y0, y1, y2, y3);
+        const uint32_t q0 = dev::pack_bf16x2(__uint_as_float(x0), __uint_as_float(x1));
+        const uint32_t q1 = dev::pack_bf16x2(__uint_as_float(x2), __uint_as_float(x3));
+        const uint32_t q2 = dev::pack_bf16x2(__uint_as_float(y0), __uint_as_float(y1));
+        const uint32_t q3 = dev::pack_bf16x2(__uint_as_float(y2), __uint_as_float(y3));
+        uint16_t* dst = p.c + ((size_t)((size_t)l * p.M + (size_t)(m0 + row)) * (size_t)p.N + (size_t)n);
+        if (p.vec_store && n + 8 <= p.N) {
+          dev::st_global_v4(dst, q0, q1, q2, q3);
+        } else {
+          const uint32_t q[4] = {q0, q1, q2, q3};
+          for (int e = 0; e < 8 && n + e < p.N; ++e) {
+            dst[e] = (uint16_t)((e & 1) ? (q[e >> 1] >> 16) : (q[e >> 1] & 0xFFFFu));
+          }
+        }
+      }
+    }
+  }
+
+  // ---- teardown
+  if (warp == 2) {
+    waiter.wait<false>(bar_mma_done, 0u, kRoleTmemRelease, 0);
+    waiter.wait<false>(bar_tmem_empty, 0u, kRoleTmemRelease, 1);
+    dev::tc_fence_after();
+    __syncwarp();
+    dev::tmem_dealloc(tmem_base, kTmemCols);
+  }
+  if (split > 1) {
+    // No CTA leaves while a peer may still address its shared memory.
+    __syncwarp();
+    dev::cluster_arrive_release();
+    dev::cluster_wait_acquire();
+  }
+}
+
+// ---------------------------------------------------------------- host side
+namespace {
+
+template <int MMA_N>
+cudaError_t launch_t(const LaunchArgs& la, const CUtensorMap& b_map, const KernelParams& p,
+                     cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = la.grid;
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = la.smem_bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attrs[2];
+  int n = 0;
+  attrs[n].id = cudaLaunchAttributeClusterDimension;
+  attrs[n].val.clusterDim.x = la.cluster_x;
+  attrs[n].val.clusterDim.y = 1;
+  attrs[n].val.clusterDim.z = 1;
+  ++n;
+  if (la.pdl) {
+    attrs[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  cfg.attrs = attrs;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, splitk_gemm_bf16_kernel<MMA_N>, b_map, p);
+}
+
+template <int MMA_N>
+cudaError_t prepare_t(int max_dynamic_smem) {
+  return cudaFuncSetAttribute(splitk_gemm_bf16_kernel<MMA_N>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, max_dynamic_smem);
+}
+
+}  // namespace
+
+cudaError_t launch_kernel(const LaunchArgs& la, const CUtensorMap& b_map, const KernelParams& p,
+                          cudaStream_t stream) {
+  switch (la.mma_n) {
+    case 16: return launch_t<16>(la, b_map, p, stream);
+    case 32: return launch_t<32>(la, b_map, p, stream);
+    case 64: return launch_t<64>(la, b_map, p, stream);
+    case 128: return launch_t<128>(la, b_map, p, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t prepare_kernels(int max_dynamic_smem) {
+  cudaError_t e;
+  if ((e = prepare_t<16>(max_dynamic_smem)) != cudaSuccess) return e;
+  if ((e = prepare_t<32>(max_dynamic_smem)) != cudaSuccess) return e;
+  if ((e = prepare_t<64>(max_dynamic_smem)) != cudaSuccess) return e;
+  return prepare_t<128>(max_dynamic_smem);
+}
+
+cudaError_t read_and_clear_fault(int* out_words) {
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return e;
+  e = cudaMemcpyFromSymbol(out_words, g_fault, sizeof(int) * kFaultWords);
+  if (e != cudaSuccess) return e;
+  int zeros[kFaultWords] = {0};
+  return cudaMemcpyToSymbol(g_fault, zeros, sizeof(zeros));
+}
+
+}  // namespace splitk

@@ -1,0 +1,125 @@
+"""The C ABI without a GPU: the library loads, exports every symbol that
+include/splitk.h declares, plans tactics on a described device, and rejects
+bad arguments before touching CUDA."""
+from __future__ import annotations
+
+import ctypes
+import re
+from pathlib import Path
+
+import pytest
+
+import split_bf16_gemm_swapped_gb300 as sk
+from split_bf16_gemm_swapped_gb300 import _build
+
+ROOT = Path(__file__).resolve().parent.parent
+GB300 = dict(num_sms=152, smem_per_sm=233472, smem_per_block_optin=232448)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    _build.build_splitk()
+
+
+def declared_symbols():
+    names = set()
+    for h in (ROOT / "include").glob("*.h"):
+        text = h.read_text()
+        names |= set(re.findall(r"SPLITK_API\s+[\w\s\*]+?\b(splitk_\w+)\s*\(", text))
+    return sorted(names)
+
+
+def test_every_declared_symbol_is_exported():
+    names = declared_symbols()
+    assert "splitk_gemm_bf16" in names and "splitk_plan" in names
+    lib = ctypes.CDLL(str(sk.library_path()))
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_version_and_strerror():
+    assert sk.splitk_version() >= 10000
+    for code, name in sk.STATUS.items():
+        assert sk.splitk_strerror(code)
+    assert sk.splitk_strerror(12345) == "unknown status code"
+
+
+def _plan(M, N, K, L=1, split=0):
+    return sk.splitk_plan_for(M, N, K, L, split, **GB300)
+
+
+def test_plan_of_the_decode_workloads():
+    p = _plan(1, 7168, 2048, 1, 4)
+    assert (p.mma_m, p.mma_n, p.split_k, p.k_tiles_per_cta) == (128, 16, 4, 4)
+    assert list(p.grid) == [4, 56, 1] and list(p.cluster) == [4, 1, 1]
+    assert p.smem_bytes <= GB300["smem_per_block_optin"]
+    p = _plan(16, 4096, 7168, 1, 8)
+    assert (p.mma_n, p.split_k, p.k_tiles_per_cta) == (16, 8, 7)
+    assert list(p.grid) == [8, 32, 1]
+    p = _plan(64, 18432, 7168, 1, 2)
+    assert (p.mma_n, list(p.grid)) == (64, [2, 144, 1])
+    p = _plan(128, 7168, 16384, 2, 8)
+    assert (p.mma_n, list(p.grid), p.k_tiles_per_cta) == (128, [8, 56, 2], 16)
+    assert p.reduce_rounds >= 1 and p.mailbox_quads <= 8
+
+
+def test_auto_split_covers_the_sms():
+    assert _plan(1, 7168, 2048).split_k == 4       # 56 tiles -> 224 CTAs
+    assert _plan(16, 4096, 7168).split_k == 8      # 32 tiles -> 256 CTAs
+    assert _plan(64, 18432, 7168).split_k == 2     # 144 tiles -> 288 CTAs
+    assert _plan(1, 128, 128).split_k == 1         # K of one tile: no split
+
+
+@pytest.mark.parametrize("M", [1, 4, 16, 17, 32, 33, 64, 65, 128, 129, 1000])
+@pytest.mark.parametrize("split", [1, 2, 4, 8])
+def test_every_plan_fits_and_is_consistent(M, split):
+    K = 128 * 8 * 4
+    p = _plan(M, 7168, K, 2, split)
+    assert p.mma_n >= min(M, 128) or p.mma_n == 128
+    assert p.grid[0] == split * -(-M // p.mma_n)
+    assert 2 <= p.stages <= 8
+    assert p.smem_bytes <= GB300["smem_per_block_optin"]
+    # the reduction's mailbox fits where it is placed
+    if split > 1:
+        round_bytes = (split - 1) * p.mailbox_quads * 128 * 16
+        if not p.mailbox_dedicated:
+            assert round_bytes <= p.stages * 32768
+        nquads = -(-min(M, p.mma_n) // 4)
+        assert p.reduce_rounds == -(-nquads // p.mailbox_quads)
+    # the f32 staging tile of rank 0 fits in its drained activation ring
+    assert min(M, p.mma_n) * 128 * 4 <= p.stages * p.mma_n * 256
+
+
+@pytest.mark.parametrize("args,code", [
+    ((0, 128, 128, 1, 1), -1), ((1, 0, 128, 1, 1), -1), ((1, 128, 0, 1, 1), -1),
+    ((1, 128, 128, 0, 1), -1), ((1, 128, 100, 1, 1), -1), ((1, 128, 1024, 1, 3), -3),
+    ((1, 128, 1024, 1, 16), -3), ((1, 128, 384, 1, 2), -1), ((1, 128 * 70000, 128, 1, 1), -1),
+])
+def test_plan_rejects_bad_shapes(args, code):
+    with pytest.raises(sk.SplitKError) as e:
+        sk.splitk_plan_for(*args, **GB300)
+    assert e.value.code == code
+
+
+def test_gemm_rejects_null_and_misaligned_pointers_before_cuda():
+    lib = sk.load_library()
+    assert lib.splitk_gemm_bf16(None, 16, 16, 1, 128, 128, 1, 1, None) == -7
+    assert lib.splitk_gemm_bf16(16, 16, None, 1, 128, 128, 1, 1, None) == -7
+    assert lib.splitk_gemm_bf16(8, 16, 16, 1, 128, 128, 1, 1, None) == -2
+    assert lib.splitk_gemm_bf16(16, 24, 16, 1, 128, 128, 1, 1, None) == -2
+    assert lib.splitk_gemm_bf16(16, 16, 17, 1, 128, 128, 1, 1, None) == -2
+
+
+def test_calls_needing_a_device_report_it_without_one():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    lib = sk.load_library()
+    plan = sk.Plan()
+    assert lib.splitk_plan(1, 128, 128, 1, 1, ctypes.byref(plan)) == -9
+    assert lib.splitk_gemm_bf16(16, 16, 16, 1, 128, 128, 1, 1, None) == -9
+
+
+def test_settings_calls():
+    assert sk.load_library().splitk_set_wait_limit_ns(0) == 0
+    assert sk.load_library().splitk_debug_inject(0) == 0

@@ -1,0 +1,111 @@
+"""GPU parity: the sm_103a split-K GEMM (through the C ABI) against the CPU
+oracle, element by element, on seeded synthetic inputs.
+
+Tolerance: one bf16 ulp of the oracle's value, or 1e-3*sqrt(K)*max|A|*max|B|
+for outputs near zero; bit-exact on the closed forms (all-ones, identity
+weights, one nonzero per row, small integers).
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover - CPU-only collection
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import oracle  # noqa: E402
+import split_bf16_gemm_swapped_gb300 as sk  # noqa: E402
+from split_bf16_gemm_swapped_gb300 import synthetic, workloads  # noqa: E402
+from tests._gpu import assert_parity, gemm_gpu, oracle_full, to_dev, to_host  # noqa: E402
+
+ONE = 0x3F80
+
+
+def _draw(L, M, N, K, seed, outlier_p=0.0, scale=1.0):
+    a = synthetic.normal_bf16((L, N, K), seed, synthetic.STREAM_A, 0.02)
+    b = synthetic.normal_bf16((L, M, K), seed, synthetic.STREAM_B, 1.0, outlier_p, scale)
+    return a, b
+
+
+def test_tiny_workload_full_parity():
+    w = workloads.TINY
+    a, b = w.make_a(), w.make_b()
+    c = gemm_gpu(a, b, split_k=w.split_k)
+    assert_parity(c, oracle_full(a, b), a, b, w.K)
+
+
+@pytest.mark.parametrize("split", [1, 2, 4, 8])
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 8, 13, 16, 17, 31, 32, 33, 63, 64, 65, 100, 128, 129])
+def test_every_split_and_token_tail(split, M):
+    L, N, K = 1, 300, 1024          # N=300: two full 128-row tiles and a ragged one
+    a, b = _draw(L, M, N, K, seed=1000 + M)
+    c = gemm_gpu(a, b, split_k=split)
+    assert_parity(c, oracle_full(a, b), a, b, K)
+
+
+@pytest.mark.parametrize("split", [1, 4])
+def test_batched_L_and_ragged_N(split):
+    L, M, N, K = 3, 7, 200, 2048
+    a, b = _draw(L, M, N, K, seed=77)
+    c = gemm_gpu(a, b, split_k=split)
+    assert_parity(c, oracle_full(a, b), a, b, K)
+
+
+@pytest.mark.parametrize("split", [1, 2, 4, 8])
+def test_all_ones_gives_K_exactly(split):
+    L, M, N, K = 2, 5, 384, 2048
+    a = np.full((L, N, K), ONE, np.uint16)
+    b = np.full((L, M, K), ONE, np.uint16)
+    c = gemm_gpu(a, b, split_k=split)
+    assert np.all(c == 0x4500)       # 2048 in bf16
+
+
+@pytest.mark.parametrize("split", [1, 2, 8])
+def test_identity_weights_pass_activations_bit_exactly(split):
+    L, M, N, K = 2, 20, 250, 1024
+    a = np.zeros((L, N, K), np.uint16)
+    for n in range(N):
+        a[:, n, n] = ONE
+    b = synthetic.normal_bf16((L, M, K), 5, synthetic.STREAM_B, 1.0)
+    c = gemm_gpu(a, b, split_k=split)
+    expect = b[:, :, :N].copy()
+    expect[(expect & 0x7FFF) == 0] = 0
+    assert np.array_equal(c, expect)
+
+
+def test_single_nonzero_per_row_bit_exact():
+    rng = np.random.default_rng(9)
+    L, M, N, K = 1, 9, 256, 2048
+    a = np.zeros((L, N, K), np.uint16)
+    perm = rng.integers(0, K, size=N)
+    a[0, np.arange(N), perm] = rng.integers(0x3C00, 0x4400, size=N).astype(np.uint16)
+    b = synthetic.normal_bf16((L, M, K), 6, synthetic.STREAM_B, 1.0)
+    c = gemm_gpu(a, b, split_k=4)
+    assert np.array_equal(c, oracle.gemm(a, b))
+
+
+@pytest.mark.parametrize("split", [1, 2, 4, 8])
+def test_small_integers_are_exact_for_every_split(split):
+    rng = np.random.default_rng(split)
+    L, M, N, K = 1, 16, 256, 1024
+    vals = np.array([0x0000, 0x3F80, 0x4000, 0x4040, 0x4080, 0x40A0, 0x40C0, 0x40E0, 0x4100,
+                     0xBF80, 0xC000, 0xC040, 0xC080, 0xC100], np.uint16)   # 0, +-1..8
+    a = vals[rng.integers(0, vals.size, size=(L, N, K))]
+    b = vals[rng.integers(0, vals.size, size=(L, M, K))]
+    c = gemm_gpu(a, b, split_k=split)
+    assert np.array_equal(c, oracle.gemm(a, b))
+
+
+def test_deterministic_run_to_run():
+    w = workloads.DECODE_M16.with_(N=1024)
+    a, b = w.make_a(), w.make_b()
+    ta, tb = to_dev(a), to_dev(b)
+    first = None
+    for _ in range(10):
+        c = to_host(sk.splitk_gemm_bf16(ta, tb, split_k=w.split_k))
+        if first is None:
+            first = c
+        assert np.array_equal(c, first)
