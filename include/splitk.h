@@ -101,6 +101,9 @@ typedef struct splitk_plan_t {
     unsigned cluster[3];   /* (split_k, 1, 1)                                  */
     size_t smem_bytes;     /* dynamic shared memory per CTA                    */
     int ctas_per_sm;       /* CTAs the smem budget was sized for               */
+    int pdl_trigger;       /* when a CTA lets the next kernel on the stream
+                              launch: 0 after its last weight TMA issue,
+                              1 as soon as its set-up is done                  */
 } splitk_plan_t;
 
 /*
@@ -201,6 +204,22 @@ SPLITK_API int splitk_set_wait_limit_ns(uint64_t ns);
  */
 #define SPLITK_INJECT_SKIP_PUBLISH 0x1u
 SPLITK_API int splitk_debug_inject(unsigned flags);
+
+/*
+ * Timeline tracing for launches made after this call.  `device_buffer`
+ * (caller-owned device memory, 8-byte aligned) receives, for each CTA with
+ * linear index (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x
+ * below bytes / 128, sixteen uint64 words: [0] SM id | cluster rank << 32,
+ * then %globaltimer nanoseconds at [1] CTA start, [2] set-up barrier passed,
+ * [3] last weight TMA issued, [4] activation producer past the PDL wait,
+ * [5] first and [6] last ring stage landed (MMA issuer), [7] accumulator
+ * complete, [8] partials published (ranks != 0) or summed (rank 0),
+ * [9] tile stored (rank 0), [10] CTA end, [11] mbarriers initialised,
+ * [12] A's tensor map acquired, [13] first ring pass of weight loads issued,
+ * [14] TMEM allocated, [15] epilogue past the set-up barrier.  Words never
+ * reached stay as they were.  NULL (or bytes = 0) turns tracing off.
+ */
+SPLITK_API int splitk_set_trace(void *device_buffer, size_t bytes);
 
 /* Synchronizes every device the library used, then frees its caches. */
 SPLITK_API void splitk_release(void);

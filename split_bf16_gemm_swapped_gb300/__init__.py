@@ -24,7 +24,8 @@ __all__ = [
     "splitk_plan", "splitk_plan_for", "splitk_gemm_bf16", "splitk_gemm_bf16_planned",
     "splitk_gemm_bf16_hostio", "splitk_get_fault", "splitk_get_status",
     "splitk_set_wait_limit_ns", "splitk_debug_inject", "splitk_release",
-    "splitk_strerror", "splitk_version", "FLAG_NO_PDL", "INJECT_SKIP_PUBLISH",
+    "splitk_strerror", "splitk_version", "splitk_set_trace", "FLAG_NO_PDL",
+    "INJECT_SKIP_PUBLISH", "TRACE_SLOTS", "TRACE_FIELDS",
     "STATUS",
 ]
 
@@ -54,7 +55,7 @@ class Plan(ctypes.Structure):
         ("mailbox_dedicated", ctypes.c_int), ("mailbox_quads", ctypes.c_int),
         ("reduce_rounds", ctypes.c_int), ("grid", ctypes.c_uint * 3),
         ("cluster", ctypes.c_uint * 3), ("smem_bytes", ctypes.c_size_t),
-        ("ctas_per_sm", ctypes.c_int),
+        ("ctas_per_sm", ctypes.c_int), ("pdl_trigger", ctypes.c_int),
     ]
 
     def as_dict(self) -> dict:
@@ -115,6 +116,8 @@ def load_library():
     lib.splitk_set_wait_limit_ns.restype = i
     lib.splitk_debug_inject.argtypes = [u]
     lib.splitk_debug_inject.restype = i
+    lib.splitk_set_trace.argtypes = [vp, sz]
+    lib.splitk_set_trace.restype = i
     lib.splitk_release.argtypes = []
     lib.splitk_release.restype = None
     lib.splitk_strerror.argtypes = [i]
@@ -252,6 +255,23 @@ def splitk_set_wait_limit_ns(ns: int) -> None:
 
 def splitk_debug_inject(flags: int) -> None:
     _check(load_library().splitk_debug_inject(int(flags)), "splitk_debug_inject")
+
+
+def splitk_set_trace(buffer=None) -> None:
+    """Trace later launches into `buffer` (a CUDA tensor, 16 uint64 words per
+    CTA, see splitk.h); None turns tracing off."""
+    if buffer is None:
+        _check(load_library().splitk_set_trace(None, 0), "splitk_set_trace")
+    else:
+        _check(load_library().splitk_set_trace(buffer.data_ptr(),
+                                               buffer.numel() * buffer.element_size()),
+               "splitk_set_trace")
+
+
+TRACE_SLOTS = 16
+TRACE_FIELDS = ("sm_rank", "start", "synced", "weights_issued", "act_ready", "first_full",
+                "last_full", "mma_done", "reduced", "stored", "end", "bar_init", "map_ready",
+                "prefetched", "tmem_alloc", "epi_synced")
 
 
 def splitk_release() -> None:

@@ -87,6 +87,14 @@ __device__ __forceinline__ void cluster_arrive_release() {
   asm volatile("barrier.cluster.arrive.release;" ::: "memory");
 }
 
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_acq_rel_cluster() {
+  asm volatile("fence.acq_rel.cluster;" ::: "memory");
+}
+
 __device__ __forceinline__ void cluster_wait_acquire() {
   asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
 }
@@ -246,6 +254,31 @@ __device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t& a, uint32_
                : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
                : "r"(addr)
                : "memory");
+}
+
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+// 4x4 transpose across the four lanes 4g..4g+3 of a warp: lane 4g+r holds
+// x[0..3] on entry; on exit o[u] = x[r] of lane 4g+u.  All 32 lanes call it.
+__device__ __forceinline__ void quad_transpose(float x0, float x1, float x2, float x3, int lane,
+                                               float o[4]) {
+  const int r = lane & 3;
+  const int g4 = lane & ~3;
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    const int e = (r - s) & 3;   // the element the receiving lane wants from us
+    const float offer = e == 0 ? x0 : e == 1 ? x1 : e == 2 ? x2 : x3;
+    const int u = (r + s) & 3;   // the lane we receive from
+    const float got = __shfl_sync(0xffffffffu, offer, g4 | u);
+    o[0] = u == 0 ? got : o[0];
+    o[1] = u == 1 ? got : o[1];
+    o[2] = u == 2 ? got : o[2];
+    o[3] = u == 3 ? got : o[3];
+  }
 }
 
 __device__ __forceinline__ void st_shared_f32(uint32_t addr, float v) {

@@ -33,6 +33,8 @@ constexpr size_t kBMapCacheMax = 1024;
 
 std::atomic<unsigned long long> g_wait_limit_ns{kDefaultWaitLimitNs};
 std::atomic<unsigned> g_inject{0};
+std::atomic<unsigned long long*> g_trace{nullptr};
+std::atomic<unsigned> g_trace_ctas{0};
 
 
 bool valid_split(int s) { return s == 1 || s == 2 || s == 4 || s == 8; }
@@ -47,6 +49,13 @@ int choose_mma_n(int M) {
 size_t smem_bytes_for(int mma_n, int stages, uint32_t dedicated_mailbox_bytes) {
   return (size_t)kAlignSlack + (size_t)stages * (kAStageBytes + b_stage_bytes(mma_n)) +
          dedicated_mailbox_bytes + kBarRegionBytes;
+}
+
+// Bytes of one reduction round: (split - 1) peers x the round's token
+// columns (at most 4 per quad, at most the tile's real columns) x 128 rows.
+uint32_t mailbox_round_bytes(int split, int quads, int ncols_max) {
+  const int cols = std::min(quads * 4, ncols_max);
+  return (uint32_t)(split - 1) * (uint32_t)cols * kColumnBytes;
 }
 
 // Split-K choice without a measured table: the smallest split whose grid
@@ -78,15 +87,17 @@ int plan_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t smem_
   if (m_tiles * split > 0x7FFFFFFFLL) return SPLITK_ERR_INVALID_SHAPE;
   const int k_tiles = K / kCtaK / split;
 
-  // Shared memory is sized so the whole grid is resident at once when it
-  // needs at most 3 CTAs per SM; a smaller footprint also lets the next
-  // kernel's CTAs start streaming weights early (PDL).
+  // Shared memory is sized so that this grid and the next kernel's grid can
+  // be resident together (up to 3 CTAs per SM): the next kernel's CTAs then
+  // start streaming their weights while this one finishes (PDL).
   const long long ctas = (long long)split * m_tiles * n_tiles * L;
-  int per_sm = (int)std::min<long long>(3, std::max<long long>(1, (ctas + num_sms - 1) / num_sms));
-  const int nquads_max = (std::min(M, mma_n) + 3) / 4;
+  int per_sm = (int)std::min<long long>(3, std::max<long long>(1, (2 * ctas + num_sms - 1) / num_sms));
+  const int ncols_max = std::min(M, mma_n);
+  const int nquads_max = (ncols_max + 3) / 4;
   const int qmax = max_quads_per_round(mma_n);
   const int quads_full = std::min(nquads_max, qmax);
-  const uint32_t ded_bytes = split > 1 ? (uint32_t)(split - 1) * (uint32_t)quads_full * kQuadBytes : 0u;
+  const uint32_t ded_bytes =
+      split > 1 ? mailbox_round_bytes(split, quads_full, ncols_max) : 0u;
   const bool prefer_dedicated = split > 1 && ded_bytes <= 16u * 1024u;
   const int stages_cap = std::min(kMaxStages, std::max(2, std::min(k_tiles, 4)));
 
@@ -98,8 +109,10 @@ int plan_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t smem_
       if (smem > budget) continue;
       int quads = quads_full;
       if (split > 1 && !prefer_dedicated) {
-        const int cap = (int)(((uint32_t)stages * kAStageBytes) / ((uint32_t)(split - 1) * kQuadBytes));
-        quads = std::max(1, std::min(quads_full, cap));
+        while (quads > 1 && mailbox_round_bytes(split, quads, ncols_max) >
+                                (uint32_t)stages * kAStageBytes) {
+          --quads;
+        }
       }
       out->mma_m = kMmaM;
       out->mma_n = mma_n;
@@ -107,7 +120,7 @@ int plan_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t smem_
       out->split_k = split;
       out->k_tiles_per_cta = k_tiles;
       out->mailbox_dedicated = prefer_dedicated ? 1 : 0;
-      out->mailbox_quads = split > 1 ? quads : quads_full;
+      out->mailbox_quads = quads;
       out->reduce_rounds = split > 1 ? (nquads_max + quads - 1) / quads : 0;
       out->grid[0] = (unsigned)(split * m_tiles);
       out->grid[1] = (unsigned)n_tiles;
@@ -117,6 +130,7 @@ int plan_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t smem_
       out->cluster[2] = 1;
       out->smem_bytes = smem;
       out->ctas_per_sm = per_sm;
+      out->pdl_trigger = 0;
       return SPLITK_OK;
     }
   }
@@ -140,19 +154,19 @@ int check_plan(const splitk_plan_t& pl, int M, int N, int K, int L, size_t smem_
       pl.cluster[2] != 1) {
     return SPLITK_ERR_BAD_PLAN;
   }
-  const int nquads_max = (std::min(M, pl.mma_n) + 3) / 4;
+  const int ncols_max = std::min(M, pl.mma_n);
   const int qmax = max_quads_per_round(pl.mma_n);
   if (pl.mailbox_quads < 1 || pl.mailbox_quads > qmax) return SPLITK_ERR_BAD_PLAN;
+  if (pl.pdl_trigger != 0 && pl.pdl_trigger != 1) return SPLITK_ERR_BAD_PLAN;
   uint32_t ded = 0;
   if (pl.split_k > 1) {
-    const uint32_t round_bytes = (uint32_t)(pl.split_k - 1) * (uint32_t)pl.mailbox_quads * kQuadBytes;
+    const uint32_t round_bytes = mailbox_round_bytes(pl.split_k, pl.mailbox_quads, ncols_max);
     if (pl.mailbox_dedicated) {
       ded = round_bytes;
     } else if (round_bytes > (uint32_t)pl.stages * kAStageBytes) {
       return SPLITK_ERR_BAD_PLAN;
     }
   }
-  (void)nquads_max;
   const size_t smem = smem_bytes_for(pl.mma_n, pl.stages, ded);
   if (smem != pl.smem_bytes) return SPLITK_ERR_BAD_PLAN;
   if (smem > smem_optin) return SPLITK_ERR_NO_FIT;
@@ -361,6 +375,9 @@ int launch_locked(DeviceState& st, const void* a, const void* b, void* c, int M,
   p.vec_store = ((N % 8) == 0 && ((uintptr_t)c & 15u) == 0) ? 1 : 0;
   p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
   p.inject = g_inject.load(std::memory_order_relaxed);
+  p.pdl_trigger_early = pl.pdl_trigger;
+  p.trace = g_trace.load(std::memory_order_relaxed);
+  p.trace_ctas = p.trace ? g_trace_ctas.load(std::memory_order_relaxed) : 0u;
 
   LaunchArgs la;
   la.mma_n = pl.mma_n;
@@ -495,6 +512,14 @@ SPLITK_API int splitk_set_wait_limit_ns(uint64_t ns) {
 
 SPLITK_API int splitk_debug_inject(unsigned flags) {
   g_inject.store(flags & kInjectSkipPublish);
+  return SPLITK_OK;
+}
+
+SPLITK_API int splitk_set_trace(void* device_buffer, size_t bytes) {
+  if (device_buffer && ((uintptr_t)device_buffer & 7u)) return SPLITK_ERR_MISALIGNED;
+  const size_t ctas = device_buffer ? bytes / (sizeof(unsigned long long) * kTraceSlots) : 0;
+  g_trace_ctas.store((unsigned)std::min<size_t>(ctas, 0xFFFFFFFFu));
+  g_trace.store(ctas ? static_cast<unsigned long long*>(device_buffer) : nullptr);
   return SPLITK_OK;
 }
 

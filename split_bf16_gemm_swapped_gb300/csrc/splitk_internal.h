@@ -23,8 +23,11 @@ constexpr uint32_t kAStageBytes = kMmaM * kCtaK * 2;        // 32 KiB
 constexpr uint32_t kABoxBytes = kMmaM * kAtomK * 2;         // 16 KiB
 constexpr uint32_t kBarRegionBytes = 256;
 constexpr uint32_t kAlignSlack = 1024;                      // swizzle-128B atoms
-constexpr uint32_t kQuadBytes = kEpiThreads * 4 * 4;        // one 4-column group
+constexpr uint32_t kColumnBytes = kEpiThreads * 4;          // one token column of f32 partials
 constexpr unsigned long long kDefaultWaitLimitNs = 1000000000ull;
+// Tiles with at most this many token columns are stored straight from
+// registers (warp-shuffle packing); larger ones go through shared memory.
+constexpr int kDirectStoreCols = 8;
 
 __host__ __device__ constexpr uint32_t b_stage_bytes(int mma_n) { return (uint32_t)mma_n * kCtaK * 2; }
 __host__ __device__ constexpr int max_quads_per_round(int mma_n) { return mma_n / 4 < 8 ? mma_n / 4 : 8; }
@@ -54,10 +57,34 @@ struct KernelParams {
   int k_tiles;                // K tiles per CTA
   int mailbox_dedicated;      // 1: own region after the ring, 0: rank 0's A ring
   uint32_t mailbox_bytes;     // size of the dedicated region (0 if aliased)
-  int mailbox_quads;          // 4-column groups per reduction round
+  int mailbox_quads;          // 4-column groups per reduction round (last may be partial)
   int vec_store;              // 16-byte stores of C allowed
   unsigned long long wait_limit_ns;
   unsigned inject;
+  int pdl_trigger_early;      // launch_dependents at CTA start, not after the weights
+  unsigned long long* trace;  // per-CTA %globaltimer stamps, or null
+  unsigned trace_ctas;        // CTAs the trace buffer holds
+};
+
+// Trace record of one CTA: kTraceSlots u64 words (see splitk_set_trace).
+constexpr int kTraceSlots = 16;
+enum TraceSlot : int {
+  kTrSmRank = 0,        // %smid | cluster rank << 32
+  kTrStart = 1,         // thread 0, first instruction
+  kTrSynced = 2,        // thread 0, after the CTA/cluster barrier of the set-up
+  kTrWeightsIssued = 3, // weight producer, after its last TMA issue
+  kTrActReady = 4,      // activation producer, after griddepcontrol.wait
+  kTrFirstFull = 5,     // MMA issuer, first stage landed
+  kTrLastFull = 6,      // MMA issuer, last stage landed
+  kTrMmaDone = 7,       // epilogue thread 0, accumulator complete
+  kTrReduced = 8,       // epilogue thread 0: partials published (peer) / summed (rank 0)
+  kTrStored = 9,        // epilogue thread 0 of rank 0, after its stores
+  kTrEnd = 10,          // thread 0, after the final barrier
+  kTrBarInit = 11,      // thread 0, mbarriers initialised and fenced
+  kTrMapReady = 12,     // thread 0, A's tensor map acquired
+  kTrPrefetched = 13,   // thread 0, weight loads of the first ring pass issued
+  kTrTmemAlloc = 14,    // warp 2, TMEM allocated
+  kTrEpiSynced = 15,    // epilogue thread 0, after the set-up barrier
 };
 
 struct LaunchArgs {

@@ -83,10 +83,39 @@ struct Waiter {
   }
 };
 
+__device__ __forceinline__ uint32_t smid() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(r));
+  return r;
+}
+
+// One %globaltimer stamp into this CTA's trace record (tracing on only).
+__device__ __forceinline__ void stamp(const KernelParams& p, int slot) {
+  if (p.trace != nullptr) {
+    const uint32_t cta = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+    if (cta < p.trace_ctas) p.trace[(size_t)cta * kTraceSlots + slot] = dev::globaltimer_ns();
+  }
+}
+
+// Eight consecutive bf16 of one C row starting at column n (packed in pairs,
+// low half first): one 16-byte store when allowed, else element stores
+// clipped at N.
+__device__ __forceinline__ void store8(uint16_t* dst, int n, int N, int vec_ok, uint32_t q0,
+                                       uint32_t q1, uint32_t q2, uint32_t q3) {
+  if (vec_ok && n + 8 <= N) {
+    dev::st_global_v4(dst, q0, q1, q2, q3);
+  } else {
+    const uint32_t q[4] = {q0, q1, q2, q3};
+    for (int e = 0; e < 8 && n + e < N; ++e) {
+      dst[e] = (uint16_t)((e & 1) ? (q[e >> 1] >> 16) : (q[e >> 1] & 0xFFFFu));
+    }
+  }
+}
+
 }  // namespace
 
 template <int MMA_N>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 3)
     splitk_gemm_bf16_kernel(const __grid_constant__ CUtensorMap b_map, const KernelParams p) {
   constexpr uint32_t kBStage = b_stage_bytes(MMA_N);
   constexpr uint32_t kBBox = kBStage / 2;                   // MMA_N rows x 128 B
@@ -128,9 +157,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const Waiter waiter{slot_abort, p.wait_limit_ns};
 
   // ---- set-up: barriers (thread 0), TMEM (warp 2), first weight loads.
+  // Every thread arrives on the cluster barrier (a 1-CTA cluster when
+  // split_k = 1) once its own set-up is published, and waits on it before
+  // touching shared state.  Thread 0 issues the first ring pass of weight
+  // loads between its arrival and its wait: an arrival with release
+  // semantics after those issues would hold the whole cluster until the
+  // loads have landed.
   int a_issued = 0;
   uint64_t a_policy = 0;
   if (threadIdx.x == 0) {
+    stamp(p, kTrStart);
     for (int s = 0; s < stages; ++s) {
       dev::mbar_init(bar_full0 + 8u * s, 2);
       dev::mbar_init(bar_empty0 + 8u * s, 1);
@@ -141,8 +177,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     dev::mbar_init(bar_ready, 1);
     dev::st_shared_u32(slot_abort, 0u);
     dev::fence_barrier_init();
+    stamp(p, kTrBarInit);
+  }
+  if (warp == 2) {
+    dev::tmem_alloc(slot_tmem, kTmemCols);
+    dev::tmem_relinquish();
+    dev::tc_fence_before();
+    if (lane == 0) stamp(p, kTrTmemAlloc);
+  }
+  dev::cluster_arrive_release();
+  if (threadIdx.x == 0) {
     // The weight stream does not depend on the previous kernel: start it now.
     dev::tensormap_acquire(p.a_map);
+    stamp(p, kTrMapReady);
     a_policy = dev::policy_evict_first();
     const int first = k_tiles < stages ? k_tiles : stages;
     for (; a_issued < first; ++a_issued) {
@@ -153,21 +200,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       dev::tma_load_3d_hint(dst, p.a_map, k, n0, l, full, a_policy);
       dev::tma_load_3d_hint(dst + kABoxBytes, p.a_map, k + kAtomK, n0, l, full, a_policy);
     }
+    stamp(p, kTrPrefetched);
   }
-  if (warp == 2) {
-    dev::tmem_alloc(slot_tmem, kTmemCols);
-    dev::tmem_relinquish();
-    dev::tc_fence_before();
-  }
-  // Peers' barriers must exist before any remote arrival or st.async.
-  if (split > 1) {
-    dev::cluster_arrive_release();
-    dev::cluster_wait_acquire();
-  } else {
-    __syncthreads();
-  }
+  // Peers' barriers (and this CTA's TMEM address) exist past this point.
+  dev::cluster_wait_acquire();
   dev::tc_fence_after();
   const uint32_t tmem_base = dev::ld_shared_u32(slot_tmem);
+  if (threadIdx.x == 0) {
+    stamp(p, kTrSynced);
+    if (p.trace != nullptr) {
+      const uint32_t cta = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+      if (cta < p.trace_ctas) {
+        p.trace[(size_t)cta * kTraceSlots + kTrSmRank] =
+            (unsigned long long)smid() | ((unsigned long long)rank << 32);
+      }
+    }
+    // Early trigger: the next kernel may launch once every CTA got here.
+    if (p.pdl_trigger_early) dev::griddep_launch_dependents();
+  }
+  if (threadIdx.x == 128) stamp(p, kTrEpiSynced);
 
   if (warp == 0) {
     // ---- weight producer
@@ -183,12 +234,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         dev::tma_load_3d_hint(dst, p.a_map, k, n0, l, full, a_policy);
         dev::tma_load_3d_hint(dst + kABoxBytes, p.a_map, k + kAtomK, n0, l, full, a_policy);
       }
-      dev::griddep_launch_dependents();
+      stamp(p, kTrWeightsIssued);
+      if (!p.pdl_trigger_early) dev::griddep_launch_dependents();
     }
   } else if (warp == 1) {
     // ---- activation producer: B may be the previous kernel's output.
     if (lane == 0) {
       dev::griddep_wait();
+      stamp(p, kTrActReady);
       for (int kt = 0; kt < k_tiles; ++kt) {
         const int s = kt % stages;
         const int r = kt / stages;
@@ -212,6 +265,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = kt / stages;
         if (!waiter.wait<false>(bar_full0 + 8u * s, (uint32_t)(r & 1), kRoleMma, kt)) break;
         dev::tc_fence_after();
+        if (kt == 0) stamp(p, kTrFirstFull);
+        if (kt == k_tiles - 1) stamp(p, kTrLastFull);
         const uint32_t a_st = sA + (uint32_t)s * kAStageBytes;
         const uint32_t b_st = sB + (uint32_t)s * kBStage;
 #pragma unroll
@@ -235,10 +290,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int qr = p.mailbox_quads;
     const bool owner = rank == 0;
     const uint32_t stage_f32 = sB;   // rank 0's drained B ring: f32 [ncols][128]
+    const bool direct_store = ncols <= kDirectStoreCols;
 
     waiter.wait<false>(bar_mma_done, 0u, kRoleEpiMma, 0);
     __syncwarp();
     dev::tc_fence_after();
+    if (et == 0) stamp(p, kTrMmaDone);
 
     int round = 0;
     for (int qb = 0; qb < nquads; qb += qr, ++round) {
@@ -257,23 +314,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       dev::tmem_wait_ld();
 
       if (split > 1) {
+        // Mailbox of a round: [peer - 1][column - c_lo][row], one f32 per
+        // (token column, weight row); only the round's real columns travel.
+        const int c_lo = qb * 4;
+        const int rc = (ncols - c_lo) < nq * 4 ? (ncols - c_lo) : nq * 4;
+        const uint32_t round_bytes = (uint32_t)(split - 1) * (uint32_t)rc * kColumnBytes;
         // The aliased mailbox (and any later round) waits for rank 0 to free it.
         const bool need_ready = !(p.mailbox_dedicated && round == 0);
         const uint32_t ready_parity = (uint32_t)((round - (p.mailbox_dedicated ? 1 : 0)) & 1);
-        const uint32_t round_bytes = (uint32_t)(split - 1) * (uint32_t)nq * kQuadBytes;
         if (!owner) {
           if (!(p.inject & kInjectSkipPublish)) {
             if (!need_ready ||
                 waiter.wait<true>(bar_ready, ready_parity, kRoleEpiReady, round)) {
-              const uint32_t r_mail = dev::mapa(sMail, 0);
               const uint32_t r_bar = dev::mapa(bar_reduce, 0);
+              const uint32_t r_mail =
+                  dev::mapa(sMail, 0) + (uint32_t)((rank - 1) * rc) * kColumnBytes;
+              const int sub = lane & 3;             // column of the quad this lane sends
+              const uint32_t rows4 = (uint32_t)((warp & 3) * 32 + (lane & ~3)) * 4u;
 #pragma unroll
               for (int j = 0; j < kQMax; ++j) {
                 if (j < nq) {
-                  const uint32_t off =
-                      ((uint32_t)((rank - 1) * nq + j) * kEpiThreads + (uint32_t)et) * 16u;
-                  dev::st_async_v4(r_mail + off, v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3],
-                                   r_bar);
+                  // Transpose 4x4 within each group of 4 lanes: lane 4g+r
+                  // gathers column 4j+r of rows 4g..4g+3.
+                  float o[4];
+                  dev::quad_transpose(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                      __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]),
+                                      lane, o);
+                  const int col = c_lo + 4 * j + sub;
+                  if (col < ncols) {
+                    dev::st_async_v4(r_mail + (uint32_t)(col - c_lo) * kColumnBytes + rows4,
+                                     __float_as_uint(o[0]), __float_as_uint(o[1]),
+                                     __float_as_uint(o[2]), __float_as_uint(o[3]), r_bar);
+                  }
                 }
               }
             }
@@ -285,23 +357,29 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int peer = 1; peer < split; ++peer) {
                 dev::mbar_arrive_remote(dev::mapa(bar_ready, (uint32_t)peer));
               }
+              // Performed before anything later, so the relaxed arrival on the
+              // final cluster barrier cannot overtake them.
+              dev::fence_acq_rel_cluster();
             }
           }
           waiter.wait<true>(bar_reduce, (uint32_t)(round & 1), kRoleEpiReduce, round);
-          // Owner's partial + peers 1, 2, ... in rank order.
+          // Owner's partial + peers 1, 2, ... in rank order.  Plain loads, so
+          // the compiler can issue a peer's loads together.
+          const float* mail = reinterpret_cast<const float*>(smem_raw + (sMail - raw)) + et;
           for (int peer = 1; peer < split; ++peer) {
+            const float* mp = mail + (size_t)(peer - 1) * (size_t)rc * kEpiThreads;
+            float w[kQMax * 4];
 #pragma unroll
             for (int j = 0; j < kQMax; ++j) {
-              if (j < nq) {
-                uint32_t w0, w1, w2, w3;
-                const uint32_t off =
-                    ((uint32_t)((peer - 1) * nq + j) * kEpiThreads + (uint32_t)et) * 16u;
-                dev::ld_shared_v4(sMail + off, w0, w1, w2, w3);
-                v[4 * j] = __float_as_uint(__uint_as_float(v[4 * j]) + __uint_as_float(w0));
-                v[4 * j + 1] = __float_as_uint(__uint_as_float(v[4 * j + 1]) + __uint_as_float(w1));
-                v[4 * j + 2] = __float_as_uint(__uint_as_float(v[4 * j + 2]) + __uint_as_float(w2));
-                v[4 * j + 3] = __float_as_uint(__uint_as_float(v[4 * j + 3]) + __uint_as_float(w3));
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const int col = c_lo + 4 * j + i;
+                w[4 * j + i] = (j < nq && col < ncols) ? mp[(size_t)(col - c_lo) * kEpiThreads] : 0.0f;
               }
+            }
+#pragma unroll
+            for (int e = 0; e < kQMax * 4; ++e) {
+              v[e] = __float_as_uint(__uint_as_float(v[e]) + w[e]);
             }
           }
           // Every owner thread has read this round before the mailbox is reused.
@@ -310,14 +388,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 
       if (owner) {
+        if (direct_store) {
+          // Few token columns: pack along n with warp shuffles and store each
+          // column's 256 contiguous bytes as 16-byte vectors, no staging.
 #pragma unroll
-        for (int j = 0; j < kQMax; ++j) {
+          for (int j = 0; j < kQMax; ++j) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int m = (qb + j) * 4 + i;
-            if (j < nq && m < ncols) {
-              dev::st_shared_f32(stage_f32 + ((uint32_t)m * kMmaM + (uint32_t)et) * 4u,
-                                 __uint_as_float(v[4 * j + i]));
+            for (int i = 0; i < 4; ++i) {
+              const int col = (qb + j) * 4 + i;
+              if (j < nq && col < ncols) {
+                const float x = __uint_as_float(v[4 * j + i]);
+                const float nb = __shfl_down_sync(0xffffffffu, x, 1);
+                const uint32_t pr = dev::pack_bf16x2(x, nb);
+                const uint32_t w1 = __shfl_down_sync(0xffffffffu, pr, 2);
+                const uint32_t w2 = __shfl_down_sync(0xffffffffu, pr, 4);
+                const uint32_t w3 = __shfl_down_sync(0xffffffffu, pr, 6);
+                const int n = n0 + (warp & 3) * 32 + lane;
+                if ((lane & 7) == 0 && n < p.N) {
+                  uint16_t* dst = p.c + ((size_t)((size_t)l * p.M + (size_t)(m0 + col)) * (size_t)p.N + (size_t)n);
+                  store8(dst, n, p.N, p.vec_store, pr, w1, w2, w3);
+                }
+              }
+            }
+          }
+        } else {
+          float* stage = reinterpret_cast<float*>(smem_raw + (stage_f32 - raw));
+#pragma unroll
+          for (int j = 0; j < kQMax; ++j) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int m = (qb + j) * 4 + i;
+              if (j < nq && m < ncols) stage[m * kMmaM + et] = __uint_as_float(v[4 * j + i]);
             }
           }
         }
@@ -326,34 +427,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     // TMEM reads are done: let warp 2 release it.
     dev::tc_fence_before();
     dev::mbar_arrive(bar_tmem_empty);
+    if (et == 0) stamp(p, kTrReduced);
 
-    if (owner) {
+    if (owner && !direct_store) {
       // Rank 0 stores the tile: 16 vectors of 8 bf16 per token row, coalesced along n.
       dev::named_bar_sync(1, kEpiThreads);
+      const float* stage = reinterpret_cast<const float*>(smem_raw + (stage_f32 - raw));
       const int total = ncols * (kMmaM / 8);
       for (int idx = et; idx < total; idx += kEpiThreads) {
         const int row = idx >> 4;
         const int c8 = (idx & 15) * 8;
         const int n = n0 + c8;
         if (n >= p.N) continue;
-        uint32_t x0, x1, x2, x3, y0, y1, y2, y3;
-        const uint32_t src = stage_f32 + ((uint32_t)row * kMmaM + (uint32_t)c8) * 4u;
-        dev::ld_shared_v4(src, x0, x1, x2, x3);
-        dev::ld_shared_v4(src + 16u, y0, y1, y2, y3);
-        const uint32_t q0 = dev::pack_bf16x2(__uint_as_float(x0), __uint_as_float(x1));
-        const uint32_t q1 = dev::pack_bf16x2(__uint_as_float(x2), __uint_as_float(x3));
-        const uint32_t q2 = dev::pack_bf16x2(__uint_as_float(y0), __uint_as_float(y1));
-        const uint32_t q3 = dev::pack_bf16x2(__uint_as_float(y2), __uint_as_float(y3));
+        const float4 x = *reinterpret_cast<const float4*>(stage + row * kMmaM + c8);
+        const float4 y = *reinterpret_cast<const float4*>(stage + row * kMmaM + c8 + 4);
         uint16_t* dst = p.c + ((size_t)((size_t)l * p.M + (size_t)(m0 + row)) * (size_t)p.N + (size_t)n);
-        if (p.vec_store && n + 8 <= p.N) {
-          dev::st_global_v4(dst, q0, q1, q2, q3);
-        } else {
-          const uint32_t q[4] = {q0, q1, q2, q3};
-          for (int e = 0; e < 8 && n + e < p.N; ++e) {
-            dst[e] = (uint16_t)((e & 1) ? (q[e >> 1] >> 16) : (q[e >> 1] & 0xFFFFu));
-          }
-        }
+        store8(dst, n, p.N, p.vec_store, dev::pack_bf16x2(x.x, x.y), dev::pack_bf16x2(x.z, x.w),
+               dev::pack_bf16x2(y.x, y.y), dev::pack_bf16x2(y.z, y.w));
       }
+    }
+    if (owner) {
+      if (et == 0) stamp(p, kTrStored);
     }
   }
 
@@ -366,11 +460,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     dev::tmem_dealloc(tmem_base, kTmemCols);
   }
   if (split > 1) {
-    // No CTA leaves while a peer may still address its shared memory.
+    // No CTA leaves while a peer may still address its shared memory.  The
+    // arrival is relaxed: rank 0 has already received every peer's bytes and
+    // its remote arrivals are fenced, and a release here would wait for the
+    // tile's global stores.
     __syncwarp();
-    dev::cluster_arrive_release();
+    dev::cluster_arrive_relaxed();
     dev::cluster_wait_acquire();
   }
+  if (threadIdx.x == 0) stamp(p, kTrEnd);
 }
 
 // ---------------------------------------------------------------- host side

@@ -63,6 +63,14 @@ def test_plan_of_the_decode_workloads():
     assert p.reduce_rounds >= 1 and p.mailbox_quads <= 8
 
 
+def test_decode_tactics_leave_room_for_the_next_kernel():
+    """Three CTAs per SM: this grid and the next one are resident together."""
+    for M, N, K, split in [(1, 7168, 2048, 4), (16, 4096, 7168, 8)]:
+        p = _plan(M, N, K, 1, split)
+        assert p.ctas_per_sm == 3
+        assert 3 * (p.smem_bytes + 1024) <= GB300["smem_per_sm"]
+
+
 def test_auto_split_covers_the_sms():
     assert _plan(1, 7168, 2048).split_k == 4       # 56 tiles -> 224 CTAs
     assert _plan(16, 4096, 7168).split_k == 8      # 32 tiles -> 256 CTAs
@@ -81,11 +89,14 @@ def test_every_plan_fits_and_is_consistent(M, split):
     assert p.smem_bytes <= GB300["smem_per_block_optin"]
     # the reduction's mailbox fits where it is placed
     if split > 1:
-        round_bytes = (split - 1) * p.mailbox_quads * 128 * 16
+        cols = min(4 * p.mailbox_quads, M, p.mma_n)
+        round_bytes = (split - 1) * cols * 128 * 4
+        ded = round_bytes if p.mailbox_dedicated else 0
         if not p.mailbox_dedicated:
             assert round_bytes <= p.stages * 32768
         nquads = -(-min(M, p.mma_n) // 4)
         assert p.reduce_rounds == -(-nquads // p.mailbox_quads)
+        assert p.smem_bytes == 1024 + p.stages * (32768 + p.mma_n * 256) + ded + 256
     # the f32 staging tile of rank 0 fits in its drained activation ring
     assert min(M, p.mma_n) * 128 * 4 <= p.stages * p.mma_n * 256
 

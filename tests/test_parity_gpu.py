@@ -109,3 +109,43 @@ def test_deterministic_run_to_run():
         if first is None:
             first = c
         assert np.array_equal(c, first)
+
+
+def _variant(base, stages, dedicated, quads, M, trigger=0):
+    p = sk.Plan.from_buffer_copy(base)
+    p.stages = stages
+    p.mailbox_dedicated = dedicated
+    p.mailbox_quads = quads
+    p.pdl_trigger = trigger
+    ncm = min(M, p.mma_n)
+    cols = min(4 * quads, ncm)
+    ded = (p.split_k - 1) * cols * 512 if (dedicated and p.split_k > 1) else 0
+    p.smem_bytes = 1024 + stages * (32768 + p.mma_n * 256) + ded + 256
+    return p
+
+
+@pytest.mark.parametrize("M", [1, 3, 6, 16, 30, 64, 100, 128])
+@pytest.mark.parametrize("split", [2, 8])
+def test_reduction_rounds_and_mailbox_placements(M, split):
+    """Force one 4-column group per reduction round (many rounds), with the
+    mailbox in its own region and aliased onto rank 0's drained weight ring."""
+    L, N, K = 1, 256, 2048
+    a, b = _draw(L, M, N, K, seed=500 + M)
+    ref = oracle_full(a, b)
+    base = sk.splitk_plan(M, N, K, L, split)
+    for stages, ded, quads, trig in [(2, 1, 1, 0), (3, 0, 1, 1), (2, 0, base.mailbox_quads, 0),
+                                     (4, 1, base.mailbox_quads, 1)]:
+        p = _variant(base, stages, ded, quads, M, trig)
+        if p.smem_bytes > 232448:
+            continue
+        c = gemm_gpu(a, b, plan=p)
+        assert_parity(c, ref, a, b, K)
+
+
+def test_no_pdl_flag_gives_identical_bits():
+    w = workloads.DECODE_M1.with_(N=1024)
+    a, b = w.make_a(), w.make_b()
+    p = sk.splitk_plan(w.M, w.N, w.K, w.L, w.split_k)
+    c0 = gemm_gpu(a, b, plan=p)
+    c1 = gemm_gpu(a, b, plan=p, flags=sk.FLAG_NO_PDL)
+    assert np.array_equal(c0, c1)
