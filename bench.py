@@ -266,7 +266,7 @@ def run_ours(args, w):
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 0) or 0) or 126 * 1024 * 1024
     a_bytes = a_host.nbytes
-    R = max(2, math.ceil(4 * l2 / a_bytes))
+    R = args.rotate if args.rotate else max(2, math.ceil(4 * l2 / a_bytes))
     a0 = to_dev(a_host, dev)
     As = [a0] + [a0.clone() for _ in range(R - 1)]
     b = to_dev(b_host, dev)
@@ -362,10 +362,10 @@ def run_ours(args, w):
 
     # end to end through the C ABI: pinned host activations in, host output out
     e2e = None
-    if rank == 0 or world > 1:
+    if args.e2e_steps > 0:
         b_pin = torch.from_numpy(b_host.view(np.int16)).view(torch.bfloat16).pin_memory()
         c_pin = torch.empty((w.L, w.M, w.N), dtype=torch.bfloat16).pin_memory()
-        n_e2e = min(args.steps, 2000)
+        n_e2e = min(args.steps, args.e2e_steps)
         with torch.cuda.stream(stream):
             for i in range(min(args.warmup, 10)):
                 sk.splitk_gemm_bf16_hostio(As[i % R], b_pin, c_pin, b, c, w.split_k, stream)
@@ -479,6 +479,10 @@ def main():
     ap.add_argument("--workload", default="decode_m1")
     ap.add_argument("--sweep", choices=["sweep", "all"], default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--rotate", type=int, default=0,
+                    help="weight copies to rotate (default: enough for 4x the L2 cache)")
+    ap.add_argument("--e2e-steps", type=int, default=2000,
+                    help="steps of the end-to-end host-I/O measurement (0 skips it)")
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of host time for the CPU oracle baseline")
     args = ap.parse_args()

@@ -87,17 +87,18 @@ int plan_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t smem_
   if (m_tiles * split > 0x7FFFFFFFLL) return SPLITK_ERR_INVALID_SHAPE;
   const int k_tiles = K / kCtaK / split;
 
-  // Shared memory is sized so that this grid and the next kernel's grid can
-  // be resident together (up to 3 CTAs per SM): the next kernel's CTAs then
-  // start streaming their weights while this one finishes (PDL).
+  // Shared memory is sized so the whole grid is resident at once (up to 2
+  // CTAs per SM), with as deep a ring as that leaves.  Measured on GB300 for
+  // the decode shapes: 3 stages at 2 CTAs/SM beat 2 stages at 3 CTAs/SM
+  // (where the next kernel's grid could be co-resident), because a stage
+  // that is already in flight when the previous kernel completes shortens
+  // the critical path more than early residency does.
   const long long ctas = (long long)split * m_tiles * n_tiles * L;
-  int per_sm = (int)std::min<long long>(3, std::max<long long>(1, (2 * ctas + num_sms - 1) / num_sms));
+  int per_sm = (int)std::min<long long>(2, std::max<long long>(1, (ctas + num_sms - 1) / num_sms));
   const int ncols_max = std::min(M, mma_n);
   const int nquads_max = (ncols_max + 3) / 4;
-  const int qmax = max_quads_per_round(mma_n);
-  const int quads_full = std::min(nquads_max, qmax);
   const uint32_t ded_bytes =
-      split > 1 ? mailbox_round_bytes(split, quads_full, ncols_max) : 0u;
+      split > 1 ? mailbox_round_bytes(split, nquads_max, ncols_max) : 0u;
   const bool prefer_dedicated = split > 1 && ded_bytes <= 16u * 1024u;
   const int stages_cap = std::min(kMaxStages, std::max(2, std::min(k_tiles, 4)));
 
@@ -107,11 +108,14 @@ int plan_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t smem_
       const uint32_t ded = prefer_dedicated ? ded_bytes : 0u;
       const size_t smem = smem_bytes_for(mma_n, stages, ded);
       if (smem > budget) continue;
-      int quads = quads_full;
-      if (split > 1 && !prefer_dedicated) {
-        while (quads > 1 && mailbox_round_bytes(split, quads, ncols_max) >
-                                (uint32_t)stages * kAStageBytes) {
-          --quads;
+      // One round when the partials fit, else rounds of whole 16-column
+      // groups (4 quads; at least one group always fits a 2-stage ring).
+      int quads = nquads_max;
+      if (split > 1 && !prefer_dedicated &&
+          mailbox_round_bytes(split, quads, ncols_max) > (uint32_t)stages * kAStageBytes) {
+        quads = 4;
+        while (mailbox_round_bytes(split, quads + 4, ncols_max) <= (uint32_t)stages * kAStageBytes) {
+          quads += 4;
         }
       }
       out->mma_m = kMmaM;
@@ -155,8 +159,11 @@ int check_plan(const splitk_plan_t& pl, int M, int N, int K, int L, size_t smem_
     return SPLITK_ERR_BAD_PLAN;
   }
   const int ncols_max = std::min(M, pl.mma_n);
-  const int qmax = max_quads_per_round(pl.mma_n);
-  if (pl.mailbox_quads < 1 || pl.mailbox_quads > qmax) return SPLITK_ERR_BAD_PLAN;
+  const int nquads_max = (ncols_max + 3) / 4;
+  if (pl.mailbox_quads < 1 || pl.mailbox_quads > pl.mma_n / 4 ||
+      (pl.mailbox_quads % 4 != 0 && pl.mailbox_quads < nquads_max)) {
+    return SPLITK_ERR_BAD_PLAN;
+  }
   if (pl.pdl_trigger != 0 && pl.pdl_trigger != 1) return SPLITK_ERR_BAD_PLAN;
   uint32_t ded = 0;
   if (pl.split_k > 1) {

@@ -25,12 +25,11 @@ constexpr uint32_t kBarRegionBytes = 256;
 constexpr uint32_t kAlignSlack = 1024;                      // swizzle-128B atoms
 constexpr uint32_t kColumnBytes = kEpiThreads * 4;          // one token column of f32 partials
 constexpr unsigned long long kDefaultWaitLimitNs = 1000000000ull;
-// Tiles with at most this many token columns are stored straight from
-// registers (warp-shuffle packing); larger ones go through shared memory.
-constexpr int kDirectStoreCols = 8;
+// Longest a waiting thread sleeps in one mbarrier try_wait before it looks
+// at the clock and the CTA's failure flag again.
+constexpr uint32_t kWaitHintNs = 1000000u;
 
 __host__ __device__ constexpr uint32_t b_stage_bytes(int mma_n) { return (uint32_t)mma_n * kCtaK * 2; }
-__host__ __device__ constexpr int max_quads_per_round(int mma_n) { return mma_n / 4 < 8 ? mma_n / 4 : 8; }
 
 // Fault record in device memory (one per device, see splitk_fault_t).
 constexpr int kFaultWords = 8;
@@ -57,7 +56,7 @@ struct KernelParams {
   int k_tiles;                // K tiles per CTA
   int mailbox_dedicated;      // 1: own region after the ring, 0: rank 0's A ring
   uint32_t mailbox_bytes;     // size of the dedicated region (0 if aliased)
-  int mailbox_quads;          // 4-column groups per reduction round (last may be partial)
+  int mailbox_quads;          // 4-column groups per reduction round: a multiple of 4, or all
   int vec_store;              // 16-byte stores of C allowed
   unsigned long long wait_limit_ns;
   unsigned inject;

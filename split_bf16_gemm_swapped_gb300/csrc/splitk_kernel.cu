@@ -45,41 +45,53 @@ __device__ int g_fault[kFaultWords];
 
 namespace {
 
+// Records the first timeout of the device (out of line: cold path).
+__device__ __noinline__ void record_fault(int role, int index, uint32_t parity) {
+  if (atomicCAS(&g_fault[0], 0, (int)SPLITK_ERR_TIMEOUT) == 0) {
+    g_fault[1] = role;
+    g_fault[2] = index;
+    g_fault[3] = (int)parity;
+    g_fault[4] = (int)blockIdx.x;
+    g_fault[5] = (int)blockIdx.y;
+    g_fault[6] = (int)blockIdx.z;
+    g_fault[7] = (int)dev::cluster_ctarank();
+    __threadfence();
+  }
+}
+
+template <bool kClusterScope>
+__device__ __forceinline__ bool poll_phase(uint32_t bar, uint32_t parity) {
+  return kClusterScope ? dev::mbar_try_wait_cluster(bar, parity, kWaitHintNs)
+                       : dev::mbar_try_wait(bar, parity, kWaitHintNs);
+}
+
+// The bounded part of a wait (out of line: reached only when the first
+// try_wait gave up).  Returns false if the limit ran out (recording it) or
+// another wait of the CTA already failed.
+template <bool kClusterScope>
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, uint32_t abort_flag,
+                                       unsigned long long limit_ns, int role, int index) {
+  const uint64_t t0 = dev::globaltimer_ns();
+  while (true) {
+    if (poll_phase<kClusterScope>(bar, parity)) return true;
+    if (dev::ld_shared_u32(abort_flag) != 0u) return false;
+    if (dev::globaltimer_ns() - t0 > limit_ns) {
+      dev::st_shared_u32(abort_flag, 1u);
+      record_fault(role, index, parity);
+      return false;
+    }
+  }
+}
+
 struct Waiter {
   uint32_t abort_flag;            // shared-memory u32, sticky per CTA
   unsigned long long limit_ns;
 
-  __device__ __forceinline__ void record(int role, int index, uint32_t parity) const {
-    if (atomicCAS(&g_fault[0], 0, (int)SPLITK_ERR_TIMEOUT) == 0) {
-      g_fault[1] = role;
-      g_fault[2] = index;
-      g_fault[3] = (int)parity;
-      g_fault[4] = (int)blockIdx.x;
-      g_fault[5] = (int)blockIdx.y;
-      g_fault[6] = (int)blockIdx.z;
-      g_fault[7] = (int)dev::cluster_ctarank();
-      __threadfence();
-    }
-  }
-
-  // Waits for the phase of `bar` with `parity` to complete.  Returns false if
-  // the limit ran out (and records it) or another wait of the CTA failed.
+  // Waits for the phase of `bar` with `parity` to complete (bounded).
   template <bool kClusterScope>
   __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, int role, int index) const {
-    auto poll = [&]() {
-      return kClusterScope ? dev::mbar_try_wait_cluster(bar, parity) : dev::mbar_try_wait(bar, parity);
-    };
-    if (poll()) return true;
-    const uint64_t t0 = dev::globaltimer_ns();
-    while (true) {
-      if (poll()) return true;
-      if (dev::ld_shared_u32(abort_flag) != 0u) return false;
-      if (dev::globaltimer_ns() - t0 > limit_ns) {
-        dev::st_shared_u32(abort_flag, 1u);
-        record(role, index, parity);
-        return false;
-      }
-    }
+    if (poll_phase<kClusterScope>(bar, parity)) return true;
+    return wait_slow<kClusterScope>(bar, parity, abort_flag, limit_ns, role, index);
   }
 };
 
@@ -97,18 +109,13 @@ __device__ __forceinline__ void stamp(const KernelParams& p, int slot) {
   }
 }
 
-// Eight consecutive bf16 of one C row starting at column n (packed in pairs,
-// low half first): one 16-byte store when allowed, else element stores
-// clipped at N.
-__device__ __forceinline__ void store8(uint16_t* dst, int n, int N, int vec_ok, uint32_t q0,
-                                       uint32_t q1, uint32_t q2, uint32_t q3) {
-  if (vec_ok && n + 8 <= N) {
-    dev::st_global_v4(dst, q0, q1, q2, q3);
-  } else {
-    const uint32_t q[4] = {q0, q1, q2, q3};
-    for (int e = 0; e < 8 && n + e < N; ++e) {
-      dst[e] = (uint16_t)((e & 1) ? (q[e >> 1] >> 16) : (q[e >> 1] & 0xFFFFu));
-    }
+// Element stores of up to 8 bf16 of one C row, clipped at N (cold path:
+// N not a multiple of 8, C not 16-byte aligned, or the row's last vector).
+__device__ __noinline__ void store8_clipped(uint16_t* dst, int n, int N, uint32_t q0, uint32_t q1,
+                                            uint32_t q2, uint32_t q3) {
+  const uint32_t q[4] = {q0, q1, q2, q3};
+  for (int e = 0; e < 8 && n + e < N; ++e) {
+    dst[e] = (uint16_t)((e & 1) ? (q[e >> 1] >> 16) : (q[e >> 1] & 0xFFFFu));
   }
 }
 
@@ -119,7 +126,6 @@ __global__ void __launch_bounds__(kThreads, 3)
     splitk_gemm_bf16_kernel(const __grid_constant__ CUtensorMap b_map, const KernelParams p) {
   constexpr uint32_t kBStage = b_stage_bytes(MMA_N);
   constexpr uint32_t kBBox = kBStage / 2;                   // MMA_N rows x 128 B
-  constexpr int kQMax = max_quads_per_round(MMA_N);         // register budget
   constexpr uint32_t kTmemCols = MMA_N < 32 ? 32u : (uint32_t)MMA_N;
   constexpr uint32_t kIdesc = dev::idesc_bf16_f32(kMmaM, MMA_N);
 
@@ -287,10 +293,11 @@ __global__ void __launch_bounds__(kThreads, 3)
     const uint32_t t_row = tmem_base + ((uint32_t)((warp & 3) * 32) << 16);
     const int ncols = (p.M - m0) < MMA_N ? (p.M - m0) : MMA_N;    // real token columns
     const int nquads = (ncols + 3) >> 2;
-    const int qr = p.mailbox_quads;
+    const int qr = p.mailbox_quads;                               // quads per round
     const bool owner = rank == 0;
-    const uint32_t stage_f32 = sB;   // rank 0's drained B ring: f32 [ncols][128]
-    const bool direct_store = ncols <= kDirectStoreCols;
+    // Rank 0 stages its f32 tile [ncols][128] in its drained activation ring.
+    float* const stage = reinterpret_cast<float*>(smem_raw + (sB - raw));
+    const float* const mail = reinterpret_cast<const float*>(smem_raw + (sMail - raw));
 
     waiter.wait<false>(bar_mma_done, 0u, kRoleEpiMma, 0);
     __syncwarp();
@@ -299,141 +306,102 @@ __global__ void __launch_bounds__(kThreads, 3)
 
     int round = 0;
     for (int qb = 0; qb < nquads; qb += qr, ++round) {
-      const int nq = (nquads - qb) < qr ? (nquads - qb) : qr;
-      uint32_t v[kQMax * 4];
-      __syncwarp();   // tcgen05.ld is warp-collective
-#pragma unroll
-      for (int j = 0; j < kQMax; ++j) {
-        if (j < nq) {
-          dev::tmem_ld_x4(t_row + (uint32_t)((qb + j) * 4), v[4 * j], v[4 * j + 1], v[4 * j + 2],
-                          v[4 * j + 3]);
-        } else {
-          v[4 * j] = v[4 * j + 1] = v[4 * j + 2] = v[4 * j + 3] = 0u;
-        }
-      }
-      dev::tmem_wait_ld();
-
+      const int q_end = (nquads - qb) < qr ? nquads : qb + qr;
+      const int c_lo = qb * 4;
+      // Mailbox of a round: [peer - 1][column - c_lo][row], f32; only the
+      // round's real token columns travel.
+      const int rc = ((ncols < q_end * 4) ? ncols : q_end * 4) - c_lo;
+      bool publish = false;
       if (split > 1) {
-        // Mailbox of a round: [peer - 1][column - c_lo][row], one f32 per
-        // (token column, weight row); only the round's real columns travel.
-        const int c_lo = qb * 4;
-        const int rc = (ncols - c_lo) < nq * 4 ? (ncols - c_lo) : nq * 4;
-        const uint32_t round_bytes = (uint32_t)(split - 1) * (uint32_t)rc * kColumnBytes;
         // The aliased mailbox (and any later round) waits for rank 0 to free it.
         const bool need_ready = !(p.mailbox_dedicated && round == 0);
-        const uint32_t ready_parity = (uint32_t)((round - (p.mailbox_dedicated ? 1 : 0)) & 1);
         if (!owner) {
-          if (!(p.inject & kInjectSkipPublish)) {
-            if (!need_ready ||
-                waiter.wait<true>(bar_ready, ready_parity, kRoleEpiReady, round)) {
-              const uint32_t r_bar = dev::mapa(bar_reduce, 0);
-              const uint32_t r_mail =
-                  dev::mapa(sMail, 0) + (uint32_t)((rank - 1) * rc) * kColumnBytes;
-              const int sub = lane & 3;             // column of the quad this lane sends
-              const uint32_t rows4 = (uint32_t)((warp & 3) * 32 + (lane & ~3)) * 4u;
-#pragma unroll
-              for (int j = 0; j < kQMax; ++j) {
-                if (j < nq) {
-                  // Transpose 4x4 within each group of 4 lanes: lane 4g+r
-                  // gathers column 4j+r of rows 4g..4g+3.
-                  float o[4];
-                  dev::quad_transpose(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                      __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]),
-                                      lane, o);
-                  const int col = c_lo + 4 * j + sub;
-                  if (col < ncols) {
-                    dev::st_async_v4(r_mail + (uint32_t)(col - c_lo) * kColumnBytes + rows4,
-                                     __float_as_uint(o[0]), __float_as_uint(o[1]),
-                                     __float_as_uint(o[2]), __float_as_uint(o[3]), r_bar);
-                  }
-                }
-              }
-            }
-          }
+          publish = !(p.inject & kInjectSkipPublish) &&
+                    (!need_ready ||
+                     waiter.wait<true>(bar_ready,
+                                       (uint32_t)((round - (p.mailbox_dedicated ? 1 : 0)) & 1),
+                                       kRoleEpiReady, round));
         } else {
           if (et == 0) {
-            dev::mbar_arrive_expect_tx(bar_reduce, round_bytes);
+            dev::mbar_arrive_expect_tx(bar_reduce, (uint32_t)(split - 1) * (uint32_t)rc * kColumnBytes);
             if (need_ready) {
               for (int peer = 1; peer < split; ++peer) {
                 dev::mbar_arrive_remote(dev::mapa(bar_ready, (uint32_t)peer));
               }
-              // Performed before anything later, so the relaxed arrival on the
-              // final cluster barrier cannot overtake them.
-              dev::fence_acq_rel_cluster();
             }
           }
           waiter.wait<true>(bar_reduce, (uint32_t)(round & 1), kRoleEpiReduce, round);
-          // Owner's partial + peers 1, 2, ... in rank order.  Plain loads, so
-          // the compiler can issue a peer's loads together.
-          const float* mail = reinterpret_cast<const float*>(smem_raw + (sMail - raw)) + et;
-          for (int peer = 1; peer < split; ++peer) {
-            const float* mp = mail + (size_t)(peer - 1) * (size_t)rc * kEpiThreads;
-            float w[kQMax * 4];
-#pragma unroll
-            for (int j = 0; j < kQMax; ++j) {
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const int col = c_lo + 4 * j + i;
-                w[4 * j + i] = (j < nq && col < ncols) ? mp[(size_t)(col - c_lo) * kEpiThreads] : 0.0f;
-              }
-            }
-#pragma unroll
-            for (int e = 0; e < kQMax * 4; ++e) {
-              v[e] = __float_as_uint(__uint_as_float(v[e]) + w[e]);
-            }
-          }
-          // Every owner thread has read this round before the mailbox is reused.
-          if (qb + qr < nquads) dev::named_bar_sync(1, kEpiThreads);
         }
       }
+      const uint32_t r_bar = dev::mapa(bar_reduce, 0);
+      const uint32_t r_mail = dev::mapa(sMail, 0) + (uint32_t)((rank - 1) * rc) * kColumnBytes;
 
-      if (owner) {
-        if (direct_store) {
-          // Few token columns: pack along n with warp shuffles and store each
-          // column's 256 contiguous bytes as 16-byte vectors, no staging.
+      // 16 token columns per TMEM load; quads of 4 columns within.
+#pragma unroll 1
+      for (int g = qb >> 2; g * 4 < q_end; ++g) {
+        uint32_t v[16];
+        __syncwarp();   // tcgen05.ld is warp-collective
+        dev::tmem_ld_x16(t_row + (uint32_t)(g * 16), v);
+        dev::tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < kQMax; ++j) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int col = (qb + j) * 4 + i;
-              if (j < nq && col < ncols) {
-                const float x = __uint_as_float(v[4 * j + i]);
-                const float nb = __shfl_down_sync(0xffffffffu, x, 1);
-                const uint32_t pr = dev::pack_bf16x2(x, nb);
-                const uint32_t w1 = __shfl_down_sync(0xffffffffu, pr, 2);
-                const uint32_t w2 = __shfl_down_sync(0xffffffffu, pr, 4);
-                const uint32_t w3 = __shfl_down_sync(0xffffffffu, pr, 6);
-                const int n = n0 + (warp & 3) * 32 + lane;
-                if ((lane & 7) == 0 && n < p.N) {
-                  uint16_t* dst = p.c + ((size_t)((size_t)l * p.M + (size_t)(m0 + col)) * (size_t)p.N + (size_t)n);
-                  store8(dst, n, p.N, p.vec_store, pr, w1, w2, w3);
-                }
+        for (int j = 0; j < 4; ++j) {
+          const int q = g * 4 + j;
+          if (q < qb || q >= q_end) continue;                     // warp-uniform
+          const int c0 = q * 4;
+          if (split > 1 && !owner) {
+            if (publish) {
+              // 4x4 transpose within lane quads: lane 4g'+r sends column c0+r
+              // of rows 4g'..4g'+3 as one 16-byte st.async.
+              float o[4];
+              dev::quad_transpose(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                  __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]),
+                                  lane, o);
+              const int col = c0 + (lane & 3);
+              if (col < ncols) {
+                const uint32_t rows4 = (uint32_t)((warp & 3) * 32 + (lane & ~3)) * 4u;
+                dev::st_async_v4(r_mail + (uint32_t)(col - c_lo) * kColumnBytes + rows4,
+                                 __float_as_uint(o[0]), __float_as_uint(o[1]), __float_as_uint(o[2]),
+                                 __float_as_uint(o[3]), r_bar);
               }
             }
-          }
-        } else {
-          float* stage = reinterpret_cast<float*>(smem_raw + (stage_f32 - raw));
-#pragma unroll
-          for (int j = 0; j < kQMax; ++j) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int m = (qb + j) * 4 + i;
-              if (j < nq && m < ncols) stage[m * kMmaM + et] = __uint_as_float(v[4 * j + i]);
+          } else {
+            float x0 = __uint_as_float(v[4 * j]), x1 = __uint_as_float(v[4 * j + 1]);
+            float x2 = __uint_as_float(v[4 * j + 2]), x3 = __uint_as_float(v[4 * j + 3]);
+            // rank 0's partial + peers 1, 2, ... in rank order
+#pragma unroll 1
+            for (int peer = 1; peer < split; ++peer) {
+              const float* mp = mail + ((size_t)((peer - 1) * rc + (c0 - c_lo)) * kEpiThreads + et);
+              const float w0 = mp[0];
+              const float w1 = (c0 + 1 < ncols) ? mp[kEpiThreads] : 0.0f;
+              const float w2 = (c0 + 2 < ncols) ? mp[2 * kEpiThreads] : 0.0f;
+              const float w3 = (c0 + 3 < ncols) ? mp[3 * kEpiThreads] : 0.0f;
+              x0 += w0;
+              x1 += w1;
+              x2 += w2;
+              x3 += w3;
             }
+            float* sp = stage + (size_t)c0 * kMmaM + et;
+            sp[0] = x0;
+            if (c0 + 1 < ncols) sp[kMmaM] = x1;
+            if (c0 + 2 < ncols) sp[2 * kMmaM] = x2;
+            if (c0 + 3 < ncols) sp[3 * kMmaM] = x3;
           }
         }
       }
+      // Every rank-0 thread has read this round before the mailbox is reused.
+      if (split > 1 && owner && q_end < nquads) dev::named_bar_sync(1, kEpiThreads);
     }
     // TMEM reads are done: let warp 2 release it.
     dev::tc_fence_before();
     dev::mbar_arrive(bar_tmem_empty);
     if (et == 0) stamp(p, kTrReduced);
 
-    if (owner && !direct_store) {
-      // Rank 0 stores the tile: 16 vectors of 8 bf16 per token row, coalesced along n.
+    if (owner) {
+      // Rank 0 stores the tile: 16 vectors of 8 bf16 per token row, packed in
+      // pairs (low half first) and coalesced along n.
       dev::named_bar_sync(1, kEpiThreads);
-      const float* stage = reinterpret_cast<const float*>(smem_raw + (stage_f32 - raw));
       const int total = ncols * (kMmaM / 8);
+#pragma unroll 1
       for (int idx = et; idx < total; idx += kEpiThreads) {
         const int row = idx >> 4;
         const int c8 = (idx & 15) * 8;
@@ -441,12 +409,15 @@ __global__ void __launch_bounds__(kThreads, 3)
         if (n >= p.N) continue;
         const float4 x = *reinterpret_cast<const float4*>(stage + row * kMmaM + c8);
         const float4 y = *reinterpret_cast<const float4*>(stage + row * kMmaM + c8 + 4);
+        const uint32_t q0 = dev::pack_bf16x2(x.x, x.y), q1 = dev::pack_bf16x2(x.z, x.w);
+        const uint32_t q2 = dev::pack_bf16x2(y.x, y.y), q3 = dev::pack_bf16x2(y.z, y.w);
         uint16_t* dst = p.c + ((size_t)((size_t)l * p.M + (size_t)(m0 + row)) * (size_t)p.N + (size_t)n);
-        store8(dst, n, p.N, p.vec_store, dev::pack_bf16x2(x.x, x.y), dev::pack_bf16x2(x.z, x.w),
-               dev::pack_bf16x2(y.x, y.y), dev::pack_bf16x2(y.z, y.w));
+        if (p.vec_store && n + 8 <= p.N) {
+          dev::st_global_v4(dst, q0, q1, q2, q3);
+        } else {
+          store8_clipped(dst, n, p.N, q0, q1, q2, q3);
+        }
       }
-    }
-    if (owner) {
       if (et == 0) stamp(p, kTrStored);
     }
   }
@@ -461,9 +432,12 @@ __global__ void __launch_bounds__(kThreads, 3)
   }
   if (split > 1) {
     // No CTA leaves while a peer may still address its shared memory.  The
-    // arrival is relaxed: rank 0 has already received every peer's bytes and
-    // its remote arrivals are fenced, and a release here would wait for the
-    // tile's global stores.
+    // arrival is relaxed (a release would wait for the tile's global
+    // stores): rank 0's remote arrivals on the peers' barriers were observed
+    // by the peers before they published, and rank 0 has received every
+    // peer's bytes.  A CTA whose wait failed fences its remote operations
+    // first instead.
+    if (dev::ld_shared_u32(slot_abort) != 0u) dev::fence_acq_rel_cluster();
     __syncwarp();
     dev::cluster_arrive_relaxed();
     dev::cluster_wait_acquire();

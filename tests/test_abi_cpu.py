@@ -60,15 +60,15 @@ def test_plan_of_the_decode_workloads():
     assert (p.mma_n, list(p.grid)) == (64, [2, 144, 1])
     p = _plan(128, 7168, 16384, 2, 8)
     assert (p.mma_n, list(p.grid), p.k_tiles_per_cta) == (128, [8, 56, 2], 16)
-    assert p.reduce_rounds >= 1 and p.mailbox_quads <= 8
+    assert p.reduce_rounds >= 1 and p.mailbox_quads % 4 == 0
 
 
-def test_decode_tactics_leave_room_for_the_next_kernel():
-    """Three CTAs per SM: this grid and the next one are resident together."""
+def test_decode_tactics_keep_the_grid_resident_with_three_stages():
+    """Two CTAs per SM hold the whole grid; three stages fit beside it."""
     for M, N, K, split in [(1, 7168, 2048, 4), (16, 4096, 7168, 8)]:
         p = _plan(M, N, K, 1, split)
-        assert p.ctas_per_sm == 3
-        assert 3 * (p.smem_bytes + 1024) <= GB300["smem_per_sm"]
+        assert p.ctas_per_sm == 2 and p.stages == 3
+        assert 2 * (p.smem_bytes + 1024) <= GB300["smem_per_sm"]
 
 
 def test_auto_split_covers_the_sms():

@@ -1,0 +1,141 @@
+"""The C ABI on a GPU: argument errors, guard bands around C, the host-I/O
+entry point, CUDA-graph capture, and programmatic-dependent-launch chains."""
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import oracle  # noqa: E402
+import split_bf16_gemm_swapped_gb300 as sk  # noqa: E402
+from split_bf16_gemm_swapped_gb300 import synthetic, workloads  # noqa: E402
+from tests._gpu import DEV, assert_parity, to_dev, to_host  # noqa: E402
+
+
+def _draw(L, M, N, K, seed):
+    a = synthetic.normal_bf16((L, N, K), seed, synthetic.STREAM_A, 0.02)
+    b = synthetic.normal_bf16((L, M, K), seed, synthetic.STREAM_B, 1.0)
+    return a, b
+
+
+def test_plan_on_the_device_matches_the_described_device():
+    props = torch.cuda.get_device_properties(DEV)
+    p = sk.splitk_plan(1, 7168, 2048, 1, 4)
+    q = sk.splitk_plan_for(1, 7168, 2048, 1, 4, props.multi_processor_count,
+                           props.shared_memory_per_multiprocessor,
+                           props.shared_memory_per_block_optin)
+    assert p.as_dict() == q.as_dict()
+
+
+def test_argument_errors_enqueue_nothing():
+    lib = sk.load_library()
+    ta = torch.zeros((256, 1024), dtype=torch.bfloat16, device=DEV)
+    tb = torch.zeros((4, 1024), dtype=torch.bfloat16, device=DEV)
+    tc = torch.full((4, 256), 7.0, dtype=torch.bfloat16, device=DEV)
+    s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    a, b, c = ta.data_ptr(), tb.data_ptr(), tc.data_ptr()
+    assert lib.splitk_gemm_bf16(a, b, c, 4, 256, 1000, 1, 1, s) == -1      # K % 128
+    assert lib.splitk_gemm_bf16(a, b, c, 4, 256, 1024, 1, 3, s) == -3      # split 3
+    assert lib.splitk_gemm_bf16(a, b, c, 4, 256, 128 * 3, 1, 2, s) == -1   # K % (128*split)
+    assert lib.splitk_gemm_bf16(a + 2, b, c, 4, 256, 1024, 1, 1, s) == -2  # misaligned A
+    assert lib.splitk_gemm_bf16(a, b, c, 0, 256, 1024, 1, 1, s) == -1
+    p = sk.splitk_plan(4, 256, 1024, 1, 4)
+    bad = sk.Plan.from_buffer_copy(p)
+    bad.stages = 9
+    assert lib.splitk_gemm_bf16_planned(a, b, c, 4, 256, 1024, 1, ctypes.byref(bad), 0, s) == -10
+    bad = sk.Plan.from_buffer_copy(p)
+    bad.smem_bytes += 16
+    assert lib.splitk_gemm_bf16_planned(a, b, c, 4, 256, 1024, 1, ctypes.byref(bad), 0, s) == -10
+    bad = sk.Plan.from_buffer_copy(p)
+    bad.grid[1] += 1
+    assert lib.splitk_gemm_bf16_planned(a, b, c, 4, 256, 1024, 1, ctypes.byref(bad), 0, s) == -10
+    torch.cuda.synchronize()
+    assert bool((tc == 7.0).all())
+
+
+@pytest.mark.parametrize("M,N,split", [(1, 300, 4), (5, 129, 2), (40, 200, 8), (128, 384, 1)])
+def test_guard_bands_around_C_are_untouched(M, N, split):
+    L, K = 2, 1024
+    a, b = _draw(L, M, N, K, seed=M * 7 + N)
+    pad = 4096
+    buf = torch.full((pad + L * M * N + pad,), float("nan"), dtype=torch.bfloat16, device=DEV)
+    canary = buf.view(torch.int16).clone()
+    c = buf[pad:pad + L * M * N].view(L, M, N)
+    sk.splitk_gemm_bf16(to_dev(a), to_dev(b), c, split_k=split)
+    torch.cuda.synchronize()
+    now = buf.view(torch.int16)
+    assert torch.equal(now[:pad], canary[:pad]) and torch.equal(now[-pad:], canary[-pad:])
+    assert_parity(to_host(c), oracle.gemm(a, b), a, b, K)
+
+
+def test_unaligned_C_and_N_not_multiple_of_8_use_element_stores():
+    L, M, N, K = 1, 3, 203, 1024
+    a, b = _draw(L, M, N, K, seed=31)
+    buf = torch.zeros((L * M * N + 1,), dtype=torch.bfloat16, device=DEV)
+    c = buf[1:].view(L, M, N)                          # 2-byte aligned only
+    sk.splitk_gemm_bf16(to_dev(a), to_dev(b), c, split_k=2)
+    torch.cuda.synchronize()
+    assert float(buf[0]) == 0.0
+    assert_parity(to_host(c), oracle.gemm(a, b), a, b, K)
+
+
+def test_host_io_entry_point_matches_the_device_path():
+    w = workloads.DECODE_M1
+    a, b = w.make_a(), w.make_b()
+    ta, tb = to_dev(a), to_dev(b)
+    ref = sk.splitk_gemm_bf16(ta, tb, split_k=w.split_k)
+    b_pin = torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).pin_memory()
+    c_pin = torch.zeros((w.L, w.M, w.N), dtype=torch.bfloat16).pin_memory()
+    b_dev = torch.empty_like(tb)
+    c_dev = torch.empty_like(ref)
+    sk.splitk_gemm_bf16_hostio(ta, b_pin, c_pin, b_dev, c_dev, w.split_k)
+    torch.cuda.synchronize()
+    assert torch.equal(c_pin.view(torch.int16), ref.cpu().view(torch.int16))
+
+
+def test_calls_captured_in_a_cuda_graph_replay_identically():
+    w = workloads.DECODE_M16.with_(N=1024)
+    a, b = w.make_a(), w.make_b()
+    ta, tb = to_dev(a), to_dev(b)
+    eager = sk.splitk_gemm_bf16(ta, tb, split_k=w.split_k)      # also caches A's map
+    torch.cuda.synchronize()
+    out = torch.empty_like(eager)
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(3):
+            sk.splitk_gemm_bf16(ta, tb, out, split_k=w.split_k, stream=s)
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
+
+
+def test_pdl_chain_matches_serialised_launches():
+    """C1 = B0 A1^T feeds the next call as its activations: the second kernel
+    must read C1 only after the first one completed (griddepcontrol.wait)."""
+    K1, N1, N2, M = 2048, 1024, 512, 8
+    a1 = synthetic.normal_bf16((N1, K1), 61, synthetic.STREAM_A, 0.02)
+    a2 = synthetic.normal_bf16((N2, N1), 62, synthetic.STREAM_A, 0.02)
+    b0 = synthetic.normal_bf16((M, K1), 61, synthetic.STREAM_B, 1.0)
+    ta1, ta2, tb0 = to_dev(a1), to_dev(a2), to_dev(b0)
+    torch.cuda.synchronize()
+    c1 = sk.splitk_gemm_bf16(ta1, tb0, split_k=4)
+    c2 = sk.splitk_gemm_bf16(ta2, c1, split_k=4)                # PDL on
+    torch.cuda.synchronize()
+    p1 = sk.splitk_plan(M, N1, K1, 1, 4)
+    p2 = sk.splitk_plan(M, N2, N1, 1, 4)
+    d1 = sk.splitk_gemm_bf16_planned(ta1, tb0, None, p1, sk.FLAG_NO_PDL)
+    torch.cuda.synchronize()
+    d2 = sk.splitk_gemm_bf16_planned(ta2, d1, None, p2, sk.FLAG_NO_PDL)
+    torch.cuda.synchronize()
+    assert torch.equal(c1.view(torch.int16), d1.view(torch.int16))
+    assert torch.equal(c2.view(torch.int16), d2.view(torch.int16))
+    assert_parity(to_host(c1), oracle.gemm(a1, b0), a1, b0, K1)
