@@ -77,7 +77,10 @@ enum splitk_status {
     /* No CUDA device, or the current device is not compute capability 10.3. */
     SPLITK_ERR_UNSUPPORTED_DEVICE = -9,
     /* A plan passed to splitk_gemm_bf16_planned() does not match the shape. */
-    SPLITK_ERR_BAD_PLAN = -10
+    SPLITK_ERR_BAD_PLAN = -10,
+    /* splitk_gemm_bf16_noalloc(): the call needs more scratch than its
+       static array holds. */
+    SPLITK_ERR_SCRATCH = -11
 };
 
 /* Flags of splitk_gemm_bf16_planned(). */
@@ -158,6 +161,40 @@ SPLITK_API int splitk_gemm_bf16_hostio(const void *a, const void *b_host,
                                        void *c_host, void *b_dev, void *c_dev,
                                        int M, int N, int K, int L, int split_k,
                                        splitk_stream_t stream);
+
+/*
+ * splitk_gemm_bf16() for callers that must not allocate device memory.
+ * (No counterpart on the method's pages; this is a library entry point.)
+ *
+ * Who needs it: code that runs where cudaMalloc is not an option -- inside a
+ * framework whose caching allocator owns the device memory budget, on a
+ * latency-critical path where cudaMalloc's implicit synchronisation and
+ * global lock are unacceptable, or in a process that pre-reserves all GPU
+ * memory and treats any later allocation as a failure.  splitk_gemm_bf16()
+ * allocates its tensor-map pool (and a pinned host mirror) on its first call;
+ * this entry point allocates nothing: no cudaMalloc, cudaFree or allocating
+ * library routine, and no host-side cache.
+ *
+ * Arguments, layouts, tiling and results are those of splitk_gemm_bf16()
+ * (same kernel, same plan; outputs are bit-identical).  The only scratch the
+ * kernel reads besides A, B and C -- one 128-byte CUDA tensor map of A -- is
+ * kept in a file-scope device array of 256 bytes inside the library, which
+ * every GPU that loads the library holds until the process exits.  A call
+ * whose scratch would exceed that array is rejected with SPLITK_ERR_SCRATCH
+ * (with one 128-byte map per call, no valid call does).
+ *
+ * The first call on a device (with that device current) looks up the
+ * array's device address once (cudaGetSymbolAddress); make that first call
+ * before any stream capture.  Every call rewrites the whole map on `stream`
+ * with a host-to-device copy ahead of its kernel, so nothing in the array
+ * has to start at zero and the array keeps the last call's map.  All calls
+ * on a device share that one array (each device has its own copy): calls
+ * that overlap on the GPU, such as calls on two streams of one device,
+ * race on it.  Calls issued in order on one stream do not overlap.
+ */
+SPLITK_API int splitk_gemm_bf16_noalloc(const void *a, const void *b, void *c,
+                                        int M, int N, int K, int L, int split_k,
+                                        splitk_stream_t stream);
 
 /*
  * Diagnostic record of the first bounded wait that ran out on the current

@@ -22,7 +22,8 @@ from . import _build
 __all__ = [
     "SplitKError", "Plan", "Fault", "library_path", "load_library",
     "splitk_plan", "splitk_plan_for", "splitk_gemm_bf16", "splitk_gemm_bf16_planned",
-    "splitk_gemm_bf16_hostio", "splitk_get_fault", "splitk_get_status",
+    "splitk_gemm_bf16_hostio", "splitk_gemm_bf16_noalloc", "splitk_get_fault",
+    "splitk_get_status",
     "splitk_set_wait_limit_ns", "splitk_debug_inject", "splitk_release",
     "splitk_strerror", "splitk_version", "splitk_set_trace", "FLAG_NO_PDL",
     "INJECT_SKIP_PUBLISH", "TRACE_SLOTS", "TRACE_FIELDS",
@@ -37,6 +38,7 @@ STATUS = {
     -3: "SPLITK_ERR_UNSUPPORTED_SPLIT", -4: "SPLITK_ERR_NO_FIT", -5: "SPLITK_ERR_CUDA",
     -6: "SPLITK_ERR_TIMEOUT", -7: "SPLITK_ERR_NULL", -8: "SPLITK_ERR_CACHE_FULL",
     -9: "SPLITK_ERR_UNSUPPORTED_DEVICE", -10: "SPLITK_ERR_BAD_PLAN",
+    -11: "SPLITK_ERR_SCRATCH",
 }
 
 
@@ -108,6 +110,8 @@ def load_library():
     lib.splitk_gemm_bf16_planned.restype = i
     lib.splitk_gemm_bf16_hostio.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, vp]
     lib.splitk_gemm_bf16_hostio.restype = i
+    lib.splitk_gemm_bf16_noalloc.argtypes = [vp, vp, vp, i, i, i, i, i, vp]
+    lib.splitk_gemm_bf16_noalloc.restype = i
     lib.splitk_get_fault.argtypes = [ctypes.POINTER(Fault)]
     lib.splitk_get_fault.restype = i
     lib.splitk_get_status.argtypes = []
@@ -201,6 +205,27 @@ def splitk_gemm_bf16(a, b, c=None, split_k: int = 0, stream=None):
             a.data_ptr(), b.data_ptr(), c.data_ptr(), M, N, K, L, int(split_k),
             _stream_handle(stream, a.device))
     _check(rc, "splitk_gemm_bf16")
+    return c
+
+
+def splitk_gemm_bf16_noalloc(a, b, c, split_k: int = 0, stream=None):
+    """c = b @ a^T through the allocation-free entry point.
+
+    For callers that cannot allocate device memory (see splitk.h): the C
+    call allocates nothing, so `c` must be given -- this wrapper does not
+    create it either.  Same kernel and results as splitk_gemm_bf16."""
+    import torch
+    M, N, K, L = _dims(a, b)
+    _require_cuda(a, b)
+    if c is None:
+        raise ValueError("splitk_gemm_bf16_noalloc needs a preallocated output c")
+    c = _out(c, a, M, N, L)
+    _require_cuda(c)
+    with torch.cuda.device(a.device):
+        rc = load_library().splitk_gemm_bf16_noalloc(
+            a.data_ptr(), b.data_ptr(), c.data_ptr(), M, N, K, L, int(split_k),
+            _stream_handle(stream, a.device))
+    _check(rc, "splitk_gemm_bf16_noalloc")
     return c
 
 

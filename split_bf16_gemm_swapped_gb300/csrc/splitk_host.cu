@@ -25,6 +25,15 @@
 #include "splitk_internal.h"
 
 namespace splitk {
+
+// Scratch of splitk_gemm_bf16_noalloc: room for the one CUDA tensor map of A
+// that a launch reads besides its operands.  A file-scope device array, so
+// every GPU that loads this library holds these bytes until the process
+// exits and the entry point never allocates.  In host code the name stands
+// for the device symbol; its device address comes from cudaGetSymbolAddress.
+constexpr size_t kNoAllocScratchBytes = 256;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -255,6 +264,8 @@ struct DeviceState {
 
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
+// Device address of g_noalloc_scratch per device (null until looked up).
+void* g_noalloc_addr[kMaxDevices] = {};
 
 // Caller holds g_mu.  Returns the current device's state, initialised.
 int current_device(DeviceState** out, int* dev_out) {
@@ -483,6 +494,81 @@ SPLITK_API int splitk_gemm_bf16_hostio(const void* a, const void* b_host, void* 
   return SPLITK_OK;
 }
 
+SPLITK_API int splitk_gemm_bf16_noalloc(const void* a, const void* b, void* c, int M, int N, int K,
+                                        int L, int split_k, splitk_stream_t stream) {
+  int rc = check_pointers(a, b, c);
+  if (rc != SPLITK_OK) return rc;
+  if (M < 1 || N < 1 || K < 1 || L < 1) return SPLITK_ERR_INVALID_SHAPE;
+  // The call needs one tensor map of scratch; the array holds that much.
+  if (sizeof(CUtensorMap) > kNoAllocScratchBytes) return SPLITK_ERR_SCRATCH;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* st = nullptr;
+  int dev = -1;
+  rc = current_device(&st, &dev);
+  if (rc != SPLITK_OK) return rc;
+  splitk_plan_t pl;
+  rc = plan_impl(M, N, K, L, split_k, st->num_sms, st->smem_per_sm, st->smem_optin, &pl);
+  if (rc != SPLITK_OK) return rc;
+  uint32_t ded = 0;
+  rc = check_plan(pl, M, N, K, L, st->smem_optin, &ded);
+  if (rc != SPLITK_OK) return rc;
+  // Set-up, once per device, with that device current: the device address of
+  // the scratch array.
+  if (g_noalloc_addr[dev] == nullptr) {
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || addr == nullptr) {
+      cudaGetLastError();
+      return SPLITK_ERR_CUDA;
+    }
+    g_noalloc_addr[dev] = addr;
+  }
+  CUtensorMap* scratch_map = static_cast<CUtensorMap*>(g_noalloc_addr[dev]);
+  // A's tensor map goes into the scratch array on the stream (the whole map is
+  // rewritten, so nothing in the array has to start at zero); B's is a launch
+  // parameter.  Both are encoded here, on the host, without caching.
+  CUtensorMap a_map, b_map;
+  if (!encode_3d(&a_map, a, (uint64_t)K, (uint64_t)N, (uint64_t)L, (uint32_t)kMmaM) ||
+      !encode_3d(&b_map, b, (uint64_t)K, (uint64_t)M, (uint64_t)L, (uint32_t)pl.mma_n)) {
+    return SPLITK_ERR_CUDA;
+  }
+  if (cudaMemcpyAsync(scratch_map, &a_map, sizeof(CUtensorMap), cudaMemcpyHostToDevice, s) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return SPLITK_ERR_CUDA;
+  }
+  KernelParams p;
+  p.a_map = scratch_map;
+  p.c = static_cast<uint16_t*>(c);
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.L = L;
+  p.split = pl.split_k;
+  p.stages = pl.stages;
+  p.k_tiles = pl.k_tiles_per_cta;
+  p.mailbox_dedicated = pl.split_k > 1 ? pl.mailbox_dedicated : 0;
+  p.mailbox_bytes = ded;
+  p.mailbox_quads = pl.mailbox_quads;
+  p.vec_store = ((N % 8) == 0 && ((uintptr_t)c & 15u) == 0) ? 1 : 0;
+  p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+  p.inject = g_inject.load(std::memory_order_relaxed);
+  p.pdl_trigger_early = pl.pdl_trigger;
+  p.trace = g_trace.load(std::memory_order_relaxed);
+  p.trace_ctas = p.trace ? g_trace_ctas.load(std::memory_order_relaxed) : 0u;
+  LaunchArgs la;
+  la.mma_n = pl.mma_n;
+  la.grid = dim3(pl.grid[0], pl.grid[1], pl.grid[2]);
+  la.cluster_x = (unsigned)pl.split_k;
+  la.smem_bytes = pl.smem_bytes;
+  la.pdl = true;
+  if (launch_kernel(la, b_map, p, s) != cudaSuccess) {
+    cudaGetLastError();
+    return SPLITK_ERR_CUDA;
+  }
+  return SPLITK_OK;
+}
+
 SPLITK_API int splitk_get_fault(splitk_fault_t* out) {
   int words[kFaultWords] = {0};
   {
@@ -565,6 +651,7 @@ SPLITK_API const char* splitk_strerror(int code) {
     case SPLITK_ERR_CACHE_FULL: return "device tensor-map pool full; call splitk_release()";
     case SPLITK_ERR_UNSUPPORTED_DEVICE: return "no CUDA device of compute capability 10.3";
     case SPLITK_ERR_BAD_PLAN: return "plan does not match the shape";
+    case SPLITK_ERR_SCRATCH: return "the call needs more scratch than the allocation-free array holds";
     default: return "unknown status code";
   }
 }
