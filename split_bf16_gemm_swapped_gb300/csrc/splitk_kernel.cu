@@ -88,10 +88,13 @@ struct Waiter {
   unsigned long long limit_ns;
 
   // Waits for the phase of `bar` with `parity` to complete (bounded).
+  // `spans` > 1 for waits that legitimately cover other bounded waits of the
+  // CTA (the TMEM release covers the whole epilogue), so those report first.
   template <bool kClusterScope>
-  __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, int role, int index) const {
+  __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, int role, int index,
+                                       unsigned spans = 1) const {
     if (poll_phase<kClusterScope>(bar, parity)) return true;
-    return wait_slow<kClusterScope>(bar, parity, abort_flag, limit_ns, role, index);
+    return wait_slow<kClusterScope>(bar, parity, abort_flag, limit_ns * spans, role, index);
   }
 };
 
@@ -309,82 +312,97 @@ __global__ void __launch_bounds__(kThreads, 3)
       const int q_end = (nquads - qb) < qr ? nquads : qb + qr;
       const int c_lo = qb * 4;
       // Mailbox of a round: [peer - 1][column - c_lo][row], f32; only the
-      // round's real token columns travel.
-      const int rc = ((ncols < q_end * 4) ? ncols : q_end * 4) - c_lo;
-      bool publish = false;
-      if (split > 1) {
-        // The aliased mailbox (and any later round) waits for rank 0 to free it.
-        const bool need_ready = !(p.mailbox_dedicated && round == 0);
-        if (!owner) {
-          publish = !(p.inject & kInjectSkipPublish) &&
-                    (!need_ready ||
-                     waiter.wait<true>(bar_ready,
-                                       (uint32_t)((round - (p.mailbox_dedicated ? 1 : 0)) & 1),
-                                       kRoleEpiReady, round));
-        } else {
-          if (et == 0) {
-            dev::mbar_arrive_expect_tx(bar_reduce, (uint32_t)(split - 1) * (uint32_t)rc * kColumnBytes);
-            if (need_ready) {
-              for (int peer = 1; peer < split; ++peer) {
-                dev::mbar_arrive_remote(dev::mapa(bar_ready, (uint32_t)peer));
-              }
-            }
-          }
-          waiter.wait<true>(bar_reduce, (uint32_t)(round & 1), kRoleEpiReduce, round);
+      // round's real token columns [c_lo, c_hi) travel.
+      const int c_hi = (ncols < q_end * 4) ? ncols : q_end * 4;
+      const int rc = c_hi - c_lo;
+      // The aliased mailbox (and any later round) waits for rank 0 to free it.
+      const bool need_ready = split > 1 && !(p.mailbox_dedicated && round == 0);
+      if (split > 1 && owner) {
+        if (et == 0) {
+          dev::mbar_arrive_expect_tx(bar_reduce, (uint32_t)(split - 1) * (uint32_t)rc * kColumnBytes);
+        }
+        // One thread per peer, in parallel: a release arrival waits for the
+        // issuing thread's earlier memory operations, so arrivals issued one
+        // after another from a single thread would serialise into round trips.
+        if (need_ready && et >= 1 && et < split) {
+          dev::mbar_arrive_remote(dev::mapa(bar_ready, (uint32_t)et));
         }
       }
       const uint32_t r_bar = dev::mapa(bar_reduce, 0);
       const uint32_t r_mail = dev::mapa(sMail, 0) + (uint32_t)((rank - 1) * rc) * kColumnBytes;
+      bool publish = split > 1 && !owner && !(p.inject & kInjectSkipPublish);
+      bool first_group = true;
 
       // 16 token columns per TMEM load; quads of 4 columns within.
 #pragma unroll 1
-      for (int g = qb >> 2; g * 4 < q_end; ++g) {
+      for (int g = qb >> 2; g * 4 < q_end; ++g, first_group = false) {
         uint32_t v[16];
         __syncwarp();   // tcgen05.ld is warp-collective
         dev::tmem_ld_x16(t_row + (uint32_t)(g * 16), v);
         dev::tmem_wait_ld();
+        if (split > 1 && !owner) {
+          // 4x4 transpose within lane quads: lane 4g'+r will send column
+          // c0+r of rows 4g'..4g'+3 as one 16-byte st.async.  Done before
+          // waiting for rank 0, so it overlaps that wait.
+          float o[16];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int q = g * 4 + j;
-          if (q < qb || q >= q_end) continue;                     // warp-uniform
-          const int c0 = q * 4;
-          if (split > 1 && !owner) {
-            if (publish) {
-              // 4x4 transpose within lane quads: lane 4g'+r sends column c0+r
-              // of rows 4g'..4g'+3 as one 16-byte st.async.
-              float o[4];
+          for (int j = 0; j < 4; ++j) {
+            const int c0 = g * 16 + 4 * j;
+            if (c0 >= c_lo && c0 < c_hi) {                      // live quad (warp-uniform)
               dev::quad_transpose(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                  __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]),
-                                  lane, o);
-              const int col = c0 + (lane & 3);
-              if (col < ncols) {
-                const uint32_t rows4 = (uint32_t)((warp & 3) * 32 + (lane & ~3)) * 4u;
+                                  __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]), lane,
+                                  &o[4 * j]);
+            }
+          }
+          if (first_group && publish && need_ready) {
+            publish = waiter.wait<true>(bar_ready,
+                                        (uint32_t)((round - (p.mailbox_dedicated ? 1 : 0)) & 1),
+                                        kRoleEpiReady, round);
+          }
+          if (publish) {
+            const uint32_t rows4 = (uint32_t)((warp & 3) * 32 + (lane & ~3)) * 4u;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int col = g * 16 + 4 * j + (lane & 3);
+              if (col >= c_lo && col < c_hi) {
                 dev::st_async_v4(r_mail + (uint32_t)(col - c_lo) * kColumnBytes + rows4,
-                                 __float_as_uint(o[0]), __float_as_uint(o[1]), __float_as_uint(o[2]),
-                                 __float_as_uint(o[3]), r_bar);
+                                 __float_as_uint(o[4 * j]), __float_as_uint(o[4 * j + 1]),
+                                 __float_as_uint(o[4 * j + 2]), __float_as_uint(o[4 * j + 3]), r_bar);
               }
             }
-          } else {
-            float x0 = __uint_as_float(v[4 * j]), x1 = __uint_as_float(v[4 * j + 1]);
-            float x2 = __uint_as_float(v[4 * j + 2]), x3 = __uint_as_float(v[4 * j + 3]);
-            // rank 0's partial + peers 1, 2, ... in rank order
+          }
+        } else {
+          float x[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) x[e] = __uint_as_float(v[e]);
+          if (split > 1) {
+            if (first_group) waiter.wait<true>(bar_reduce, (uint32_t)(round & 1), kRoleEpiReduce, round);
+            // rank 0's partial + peers 1, 2, ... in rank order; each peer's
+            // 16 columns are loaded together.
 #pragma unroll 1
             for (int peer = 1; peer < split; ++peer) {
-              const float* mp = mail + ((size_t)((peer - 1) * rc + (c0 - c_lo)) * kEpiThreads + et);
-              const float w0 = mp[0];
-              const float w1 = (c0 + 1 < ncols) ? mp[kEpiThreads] : 0.0f;
-              const float w2 = (c0 + 2 < ncols) ? mp[2 * kEpiThreads] : 0.0f;
-              const float w3 = (c0 + 3 < ncols) ? mp[3 * kEpiThreads] : 0.0f;
-              x0 += w0;
-              x1 += w1;
-              x2 += w2;
-              x3 += w3;
+              const float* mp = mail + ((size_t)((peer - 1) * rc + (g * 16 - c_lo)) * kEpiThreads + et);
+              float w[16];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const int c0 = g * 16 + 4 * j;
+                if (c0 >= c_lo && c0 < c_hi) {                  // live quad (warp-uniform)
+#pragma unroll
+                  for (int i = 0; i < 4; ++i) {
+                    w[4 * j + i] = (c0 + i < c_hi) ? mp[(size_t)(4 * j + i) * kEpiThreads] : 0.0f;
+                  }
+                } else {
+                  w[4 * j] = w[4 * j + 1] = w[4 * j + 2] = w[4 * j + 3] = 0.0f;
+                }
+              }
+#pragma unroll
+              for (int e = 0; e < 16; ++e) x[e] += w[e];
             }
-            float* sp = stage + (size_t)c0 * kMmaM + et;
-            sp[0] = x0;
-            if (c0 + 1 < ncols) sp[kMmaM] = x1;
-            if (c0 + 2 < ncols) sp[2 * kMmaM] = x2;
-            if (c0 + 3 < ncols) sp[3 * kMmaM] = x3;
+          }
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int col = g * 16 + e;
+            if (col >= c_lo && col < c_hi) stage[(size_t)col * kMmaM + et] = x[e];
           }
         }
       }
@@ -424,13 +442,21 @@ __global__ void __launch_bounds__(kThreads, 3)
 
   // ---- teardown
   if (warp == 2) {
-    waiter.wait<false>(bar_mma_done, 0u, kRoleTmemRelease, 0);
-    waiter.wait<false>(bar_tmem_empty, 0u, kRoleTmemRelease, 1);
+    waiter.wait<false>(bar_mma_done, 0u, kRoleTmemRelease, 0, 4);
+    waiter.wait<false>(bar_tmem_empty, 0u, kRoleTmemRelease, 1, 4);
     dev::tc_fence_after();
     __syncwarp();
     dev::tmem_dealloc(tmem_base, kTmemCols);
   }
-  if (split > 1) {
+  // With a dedicated mailbox and a single reduction round, rank 0 never
+  // addresses a peer's shared memory and its reduction wait proves every
+  // peer's bytes have landed: each CTA leaves as soon as it is done, so a
+  // peer's shared memory is free for the next kernel's CTAs while rank 0 is
+  // still reducing.  (A peer later than rank 0's whole wait limit would
+  // publish into a departed CTA; the limit is chosen so that never happens.)
+  const int tile_quads = (((p.M - m0) < MMA_N ? (p.M - m0) : MMA_N) + 3) >> 2;
+  const bool final_barrier = split > 1 && !(p.mailbox_dedicated && tile_quads <= p.mailbox_quads);
+  if (final_barrier) {
     // No CTA leaves while a peer may still address its shared memory.  The
     // arrival is relaxed (a release would wait for the tile's global
     // stores): rank 0's remote arrivals on the peers' barriers were observed
