@@ -157,6 +157,24 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def max_over_ranks(value: float, device=None) -> float:
+    """The largest `value` over all ranks (the job's time is its slowest
+    rank's); the value itself when no process group is running."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64,
+                     device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tbps(world: int, bytes_per_step: int, steps: int, elapsed_ms: float) -> float:
+    """Whole-job throughput: every rank moves bytes_per_step per step."""
+    return world * bytes_per_step * steps / (elapsed_ms * 1e-3) / 1e12
+
+
 def host_cores() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -321,16 +339,12 @@ def run_ours(args, w):
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize(dev)
-    elapsed_ms = start.elapsed_time(end)
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(start.elapsed_time(end), dev)
     if sk.splitk_get_status() != 0:
         raise SystemExit(f"kernel fault in the timed region: {sk.splitk_get_fault()}")
 
     ms_per_step = elapsed_ms / args.steps
-    value = world * w.bytes * args.steps / (elapsed_ms * 1e-3) / 1e12
+    value = job_tbps(world, w.bytes, args.steps, elapsed_ms)
     hbm, bf16, bf16s, src = peaks()
     achieved_gbs = w.bytes / (ms_per_step * 1e-3) / 1e9
     flops_tfs = w.flops / (ms_per_step * 1e-3) / 1e12
