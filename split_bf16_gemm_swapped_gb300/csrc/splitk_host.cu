@@ -67,14 +67,22 @@ uint32_t mailbox_round_bytes(int split, int quads, int ncols_max) {
   return (uint32_t)(split - 1) * (uint32_t)cols * kColumnBytes;
 }
 
-// Split-K choice without a measured table: the smallest split whose grid
-// covers every SM at least once; else the largest legal split.
-int auto_split(int K, long long tiles, int num_sms) {
-  int best = 0;
+// 128-wide K tiles covering K; the last one may be ragged (TMA reads zeros
+// past K).
+inline int total_k_tiles(int K) { return (K + kCtaK - 1) / kCtaK; }
+
+// Split-K choice from GB300 measurements (decode shapes and the long-K
+// sweep, back to back): rank 0's reduction costs more as the split and the
+// tile's token columns grow, so take the smallest split whose grid fills
+// about 3/4 of the SMs (1/2 for tiles of 64 or more tokens), with at least
+// one K tile per rank.
+int auto_split(int T, long long tiles, int num_sms, int mma_n) {
+  const double fill = (mma_n >= 64 ? 0.5 : 0.75) * (double)num_sms;
+  int best = 1;
   for (int s : {1, 2, 4, 8}) {
-    if (K % (kCtaK * s) != 0) continue;
+    if (s > T) break;
     best = s;
-    if (tiles * s >= num_sms) return s;
+    if ((double)(tiles * s) >= fill) return s;
   }
   return best;
 }
@@ -85,16 +93,18 @@ int plan_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t smem_
   if (M < 1 || N < 1 || K < 1 || L < 1) return SPLITK_ERR_INVALID_SHAPE;
   if (split_k != 0 && !valid_split(split_k)) return SPLITK_ERR_UNSUPPORTED_SPLIT;
   if (num_sms < 1 || smem_optin < 1 || smem_per_sm < 1) return SPLITK_ERR_UNSUPPORTED_DEVICE;
-  if (K % kCtaK != 0) return SPLITK_ERR_INVALID_SHAPE;
+  // K's row stride must be a multiple of 16 bytes (TMA).
+  if (K % 8 != 0) return SPLITK_ERR_INVALID_SHAPE;
+  const int T = total_k_tiles(K);
   const int mma_n = choose_mma_n(M);
   const long long m_tiles = (M + mma_n - 1) / mma_n;
   const long long n_tiles = ((long long)N + kMmaM - 1) / kMmaM;
   if (n_tiles > 65535 || L > 65535) return SPLITK_ERR_INVALID_SHAPE;
   int split = split_k;
-  if (split == 0) split = auto_split(K, m_tiles * n_tiles * L, num_sms);
-  if (split == 0 || K % (kCtaK * split) != 0) return SPLITK_ERR_INVALID_SHAPE;
+  if (split == 0) split = auto_split(T, m_tiles * n_tiles * L, num_sms, mma_n);
+  if (split > T) return SPLITK_ERR_INVALID_SHAPE;      // every rank owns a K tile
   if (m_tiles * split > 0x7FFFFFFFLL) return SPLITK_ERR_INVALID_SHAPE;
-  const int k_tiles = K / kCtaK / split;
+  const int k_tiles = (T + split - 1) / split;          // the most any rank owns
 
   // Shared memory is sized so the whole grid is resident at once (up to 2
   // CTAs per SM), with as deep a ring as that leaves.  Measured on GB300 for
@@ -156,8 +166,8 @@ int check_plan(const splitk_plan_t& pl, int M, int N, int K, int L, size_t smem_
   if (pl.mma_m != kMmaM) return SPLITK_ERR_BAD_PLAN;
   if (pl.mma_n != 16 && pl.mma_n != 32 && pl.mma_n != 64 && pl.mma_n != 128) return SPLITK_ERR_BAD_PLAN;
   if (!valid_split(pl.split_k)) return SPLITK_ERR_UNSUPPORTED_SPLIT;
-  if (K % (kCtaK * pl.split_k) != 0) return SPLITK_ERR_INVALID_SHAPE;
-  if (pl.k_tiles_per_cta != K / kCtaK / pl.split_k) return SPLITK_ERR_BAD_PLAN;
+  if (K % 8 != 0 || total_k_tiles(K) < pl.split_k) return SPLITK_ERR_INVALID_SHAPE;
+  if (pl.k_tiles_per_cta != (total_k_tiles(K) + pl.split_k - 1) / pl.split_k) return SPLITK_ERR_BAD_PLAN;
   if (pl.stages < 2 || pl.stages > kMaxStages) return SPLITK_ERR_BAD_PLAN;
   const long long m_tiles = (M + pl.mma_n - 1) / pl.mma_n;
   const long long n_tiles = ((long long)N + kMmaM - 1) / kMmaM;
@@ -386,7 +396,7 @@ int launch_locked(DeviceState& st, const void* a, const void* b, void* c, int M,
   p.L = L;
   p.split = pl.split_k;
   p.stages = pl.stages;
-  p.k_tiles = pl.k_tiles_per_cta;
+  p.k_tiles_total = total_k_tiles(K);
   p.mailbox_dedicated = pl.split_k > 1 ? pl.mailbox_dedicated : 0;
   p.mailbox_bytes = ded;
   p.mailbox_quads = pl.mailbox_quads;
@@ -546,7 +556,7 @@ SPLITK_API int splitk_gemm_bf16_noalloc(const void* a, const void* b, void* c, i
   p.L = L;
   p.split = pl.split_k;
   p.stages = pl.stages;
-  p.k_tiles = pl.k_tiles_per_cta;
+  p.k_tiles_total = total_k_tiles(K);
   p.mailbox_dedicated = pl.split_k > 1 ? pl.mailbox_dedicated : 0;
   p.mailbox_bytes = ded;
   p.mailbox_quads = pl.mailbox_quads;
@@ -641,7 +651,7 @@ SPLITK_API void splitk_release(void) {
 SPLITK_API const char* splitk_strerror(int code) {
   switch (code) {
     case SPLITK_OK: return "success";
-    case SPLITK_ERR_INVALID_SHAPE: return "invalid shape (M, N, K, L >= 1; K a multiple of 128*split_k)";
+    case SPLITK_ERR_INVALID_SHAPE: return "invalid shape (M, N, K, L >= 1; K a multiple of 8 with at least one 128-wide K tile per split rank)";
     case SPLITK_ERR_MISALIGNED: return "misaligned pointer (A and B need 16 bytes, C 2 bytes)";
     case SPLITK_ERR_UNSUPPORTED_SPLIT: return "split_k must be 0, 1, 2, 4 or 8";
     case SPLITK_ERR_NO_FIT: return "no tactic fits the shared-memory budget";

@@ -53,7 +53,7 @@ struct KernelParams {
   int M, N, K, L;
   int split;                  // cluster size along K
   int stages;                 // ring depth
-  int k_tiles;                // K tiles per CTA
+  int k_tiles_total;          // 128-wide K tiles over all of K (last may be ragged)
   int mailbox_dedicated;      // 1: own region after the ring, 0: rank 0's A ring
   uint32_t mailbox_bytes;     // size of the dedicated region (0 if aliased)
   int mailbox_quads;          // 4-column groups per reduction round: a multiple of 4, or all

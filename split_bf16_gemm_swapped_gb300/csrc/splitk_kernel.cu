@@ -145,8 +145,11 @@ __global__ void __launch_bounds__(kThreads, 3)
   const int n0 = (int)blockIdx.y * kMmaM;
   const int m0 = m_tile * MMA_N;
   const int l = (int)blockIdx.z;
-  const int k_tiles = p.k_tiles;
-  const int kt0 = rank * k_tiles;
+  // Contiguous K slices: ranks below T % split take one extra tile.
+  const int kt_base = p.k_tiles_total / split;
+  const int kt_extra = p.k_tiles_total % split;
+  const int k_tiles = kt_base + (rank < kt_extra ? 1 : 0);
+  const int kt0 = rank * kt_base + (rank < kt_extra ? rank : kt_extra);
 
   // Shared memory: [A ring][B ring][dedicated mailbox?][barriers].
   const uint32_t sA = base;

@@ -71,18 +71,28 @@ def test_decode_tactics_keep_the_grid_resident_with_three_stages():
         assert 2 * (p.smem_bytes + 1024) <= GB300["smem_per_sm"]
 
 
-def test_auto_split_covers_the_sms():
-    assert _plan(1, 7168, 2048).split_k == 4       # 56 tiles -> 224 CTAs
-    assert _plan(16, 4096, 7168).split_k == 8      # 32 tiles -> 256 CTAs
-    assert _plan(64, 18432, 7168).split_k == 2     # 144 tiles -> 288 CTAs
+def test_auto_split_fills_the_sms_with_the_smallest_split():
+    assert _plan(1, 7168, 2048).split_k == 4       # 56 tiles -> 224 CTAs >= 3/4 of 152
+    assert _plan(16, 4096, 7168).split_k == 4      # 32 tiles -> 128 CTAs
+    assert _plan(64, 18432, 7168).split_k == 1     # 144 tiles of 64 tokens: no reduction
+    assert _plan(8, 7168, 16384, 2).split_k == 2   # 112 tiles -> 224 CTAs
     assert _plan(1, 128, 128).split_k == 1         # K of one tile: no split
+    assert _plan(1, 128, 256).split_k == 2         # two K tiles, one tile: split 2
+
+
+@pytest.mark.parametrize("K,split,k_tiles", [(1000, 4, 2), (1032, 4, 3), (8, 1, 1), (136, 2, 1),
+                                             (7168, 8, 7), (7176, 8, 8)])
+def test_k_tails_take_ragged_tiles(K, split, k_tiles):
+    p = _plan(4, 256, K, 1, split)
+    assert p.k_tiles_per_cta == k_tiles
 
 
 @pytest.mark.parametrize("M", [1, 4, 16, 17, 32, 33, 64, 65, 128, 129, 1000])
 @pytest.mark.parametrize("split", [1, 2, 4, 8])
 def test_every_plan_fits_and_is_consistent(M, split):
-    K = 128 * 8 * 4
+    K = 128 * 8 * 4 - 8 * (M % 5)                  # some ragged K
     p = _plan(M, 7168, K, 2, split)
+    assert p.k_tiles_per_cta == -(-(-(-K // 128)) // split)
     assert p.mma_n >= min(M, 128) or p.mma_n == 128
     assert p.grid[0] == split * -(-M // p.mma_n)
     assert 2 <= p.stages <= 8
@@ -104,7 +114,8 @@ def test_every_plan_fits_and_is_consistent(M, split):
 @pytest.mark.parametrize("args,code", [
     ((0, 128, 128, 1, 1), -1), ((1, 0, 128, 1, 1), -1), ((1, 128, 0, 1, 1), -1),
     ((1, 128, 128, 0, 1), -1), ((1, 128, 100, 1, 1), -1), ((1, 128, 1024, 1, 3), -3),
-    ((1, 128, 1024, 1, 16), -3), ((1, 128, 384, 1, 2), -1), ((1, 128 * 70000, 128, 1, 1), -1),
+    ((1, 128, 1024, 1, 16), -3), ((1, 128, 128, 1, 2), -1), ((1, 128, 1004, 1, 1), -1),
+    ((1, 128 * 70000, 128, 1, 1), -1),
 ])
 def test_plan_rejects_bad_shapes(args, code):
     with pytest.raises(sk.SplitKError) as e:

@@ -41,9 +41,9 @@ def test_argument_errors_enqueue_nothing():
     tc = torch.full((4, 256), 7.0, dtype=torch.bfloat16, device=DEV)
     s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     a, b, c = ta.data_ptr(), tb.data_ptr(), tc.data_ptr()
-    assert lib.splitk_gemm_bf16(a, b, c, 4, 256, 1000, 1, 1, s) == -1      # K % 128
+    assert lib.splitk_gemm_bf16(a, b, c, 4, 256, 1004, 1, 1, s) == -1      # K % 8
     assert lib.splitk_gemm_bf16(a, b, c, 4, 256, 1024, 1, 3, s) == -3      # split 3
-    assert lib.splitk_gemm_bf16(a, b, c, 4, 256, 128 * 3, 1, 2, s) == -1   # K % (128*split)
+    assert lib.splitk_gemm_bf16(a, b, c, 4, 256, 128, 1, 2, s) == -1       # 1 K tile, 2 ranks
     assert lib.splitk_gemm_bf16(a + 2, b, c, 4, 256, 1024, 1, 1, s) == -2  # misaligned A
     assert lib.splitk_gemm_bf16(a, b, c, 0, 256, 1024, 1, 1, s) == -1
     p = sk.splitk_plan(4, 256, 1024, 1, 4)

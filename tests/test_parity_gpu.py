@@ -150,3 +150,24 @@ def test_no_pdl_flag_gives_identical_bits():
     c0 = gemm_gpu(a, b, plan=p)
     c1 = gemm_gpu(a, b, plan=p, flags=sk.FLAG_NO_PDL)
     assert np.array_equal(c0, c1)
+
+
+@pytest.mark.parametrize("K,split", [(8, 1), (136, 2), (1000, 4), (1032, 4), (1032, 8), (2040, 8),
+                                     (7176, 8), (520, 1)])
+def test_ragged_K_tails_and_uneven_slices(K, split):
+    """K not a multiple of 128*split: ranks own floor or ceil of the K tiles,
+    and TMA reads zeros past K (a whole box past K included)."""
+    L, M, N = 2, 5, 200
+    a, b = _draw(L, M, N, K, seed=800 + K)
+    c = gemm_gpu(a, b, split_k=split)
+    assert_parity(c, oracle_full(a, b), a, b, K)
+
+
+def test_ragged_K_all_ones_is_exact():
+    for K, split in [(1000, 4), (1032, 8), (264, 2)]:
+        L, M, N = 1, 3, 256
+        a = np.full((L, N, K), ONE, np.uint16)
+        b = np.full((L, M, K), ONE, np.uint16)
+        c = gemm_gpu(a, b, split_k=split)
+        expect = oracle.gemm(a[:, :1, :], b[:, :1, :])[0, 0, 0]     # bf16 of K
+        assert np.all(c == expect), (K, split)
