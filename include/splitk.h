@@ -107,6 +107,12 @@ typedef struct splitk_plan_t {
     int pdl_trigger;       /* when a CTA lets the next kernel on the stream
                               launch: 0 after its last weight TMA issue,
                               1 as soon as its set-up is done                  */
+    int reduce_scatter;    /* 0: rank 0 sums the whole tile and stores it (the
+                              page's design); 1: rank r sums and stores weight
+                              rows [r*128/split, (r+1)*128/split) -- same
+                              additions in the same order, same bits, 1/split
+                              of the DSMEM bytes per SM; needs split_k > 1 and
+                              a dedicated mailbox of min(M, mma_n) * 512 B     */
 } splitk_plan_t;
 
 /*

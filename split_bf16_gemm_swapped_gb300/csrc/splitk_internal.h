@@ -61,6 +61,7 @@ struct KernelParams {
   unsigned long long wait_limit_ns;
   unsigned inject;
   int pdl_trigger_early;      // launch_dependents at CTA start, not after the weights
+  int reduce_scatter;         // each rank sums and stores 128/split rows
   unsigned long long* trace;  // per-CTA %globaltimer stamps, or null
   unsigned trace_ctas;        // CTAs the trace buffer holds
 };

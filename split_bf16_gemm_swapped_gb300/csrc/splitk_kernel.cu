@@ -310,129 +310,83 @@ __global__ void __launch_bounds__(kThreads, 3)
     dev::tc_fence_after();
     if (et == 0) stamp(p, kTrMmaDone);
 
-    int round = 0;
-    for (int qb = 0; qb < nquads; qb += qr, ++round) {
-      const int q_end = (nquads - qb) < qr ? nquads : qb + qr;
-      const int c_lo = qb * 4;
-      // Mailbox of a round: [peer - 1][column - c_lo][row], f32; only the
-      // round's real token columns [c_lo, c_hi) travel.
-      const int c_hi = (ncols < q_end * 4) ? ncols : q_end * 4;
-      const int rc = c_hi - c_lo;
-      // The aliased mailbox (and any later round) waits for rank 0 to free it.
-      const bool need_ready = split > 1 && !(p.mailbox_dedicated && round == 0);
-      if (split > 1 && owner) {
-        if (et == 0) {
-          dev::mbar_arrive_expect_tx(bar_reduce, (uint32_t)(split - 1) * (uint32_t)rc * kColumnBytes);
-        }
-        // One thread per peer, in parallel: a release arrival waits for the
-        // issuing thread's earlier memory operations, so arrivals issued one
-        // after another from a single thread would serialise into round trips.
-        if (need_ready && et >= 1 && et < split) {
-          dev::mbar_arrive_remote(dev::mapa(bar_ready, (uint32_t)et));
-        }
+    if (p.reduce_scatter) {
+      // Scattered reduction: rank r sums and stores weight rows
+      // [r*R, (r+1)*R) of the tile, R = 128 / split.  Each rank's partial of
+      // those rows lands in rank r's mailbox [source rank][column][R rows]
+      // (its own by shared stores, the others' by st.async), and every
+      // element is summed over source ranks 0, 1, ... in order: the same
+      // additions in the same order as rank 0 makes in the gathered mode,
+      // with 1/split of the DSMEM bytes arriving at each SM.
+      const int R = kMmaM / split;
+      const int my_lo = rank * R;
+      float* const mb = reinterpret_cast<float*>(smem_raw + (sMail - raw));
+      if (et == 0) {
+        dev::mbar_arrive_expect_tx(bar_reduce, (uint32_t)((split - 1) * ncols * R) * 4u);
       }
-      const uint32_t r_bar = dev::mapa(bar_reduce, 0);
-      const uint32_t r_mail = dev::mapa(sMail, 0) + (uint32_t)((rank - 1) * rc) * kColumnBytes;
-      bool publish = split > 1 && !owner && !(p.inject & kInjectSkipPublish);
-      bool first_group = true;
-
-      // 16 token columns per TMEM load; quads of 4 columns within.
+      const int row0 = (warp & 3) * 32 + (lane & ~3);     // first row of this lane quad
+      const int dst_rank = row0 / R;                      // the rank that sums these rows
+      const bool publish = !(p.inject & kInjectSkipPublish);
+      const uint32_t slot = ((uint32_t)(rank * ncols) * (uint32_t)R + (uint32_t)(row0 - dst_rank * R)) * 4u;
+      const uint32_t r_bar = dev::mapa(bar_reduce, (uint32_t)dst_rank);
+      const uint32_t r_mail = dev::mapa(sMail, (uint32_t)dst_rank) + slot;
 #pragma unroll 1
-      for (int g = qb >> 2; g * 4 < q_end; ++g, first_group = false) {
+      for (int g = 0; g * 16 < ncols; ++g) {
         uint32_t v[16];
         __syncwarp();   // tcgen05.ld is warp-collective
         dev::tmem_ld_x16(t_row + (uint32_t)(g * 16), v);
         dev::tmem_wait_ld();
-        if (split > 1 && !owner) {
-          // 4x4 transpose within lane quads: lane 4g'+r will send column
-          // c0+r of rows 4g'..4g'+3 as one 16-byte st.async.  Done before
-          // waiting for rank 0, so it overlaps that wait.
-          float o[16];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int c0 = g * 16 + 4 * j;
-            if (c0 >= c_lo && c0 < c_hi) {                      // live quad (warp-uniform)
-              dev::quad_transpose(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                  __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]), lane,
-                                  &o[4 * j]);
+        for (int j = 0; j < 4; ++j) {
+          const int c0 = g * 16 + 4 * j;
+          if (c0 >= ncols) continue;                          // warp-uniform
+          // lane 4g'+r gets column c0+r of the quad's 4 rows
+          float o[4];
+          dev::quad_transpose(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                              __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]), lane, o);
+          const int col = c0 + (lane & 3);
+          if (col < ncols) {
+            if (dst_rank == rank) {
+              *reinterpret_cast<float4*>(reinterpret_cast<uint8_t*>(mb) + slot + (size_t)col * R * 4) =
+                  make_float4(o[0], o[1], o[2], o[3]);
+            } else if (publish) {
+              dev::st_async_v4(r_mail + (uint32_t)(col * R) * 4u, __float_as_uint(o[0]),
+                               __float_as_uint(o[1]), __float_as_uint(o[2]), __float_as_uint(o[3]),
+                               r_bar);
             }
-          }
-          if (first_group && publish && need_ready) {
-            publish = waiter.wait<true>(bar_ready,
-                                        (uint32_t)((round - (p.mailbox_dedicated ? 1 : 0)) & 1),
-                                        kRoleEpiReady, round);
-          }
-          if (publish) {
-            const uint32_t rows4 = (uint32_t)((warp & 3) * 32 + (lane & ~3)) * 4u;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int col = g * 16 + 4 * j + (lane & 3);
-              if (col >= c_lo && col < c_hi) {
-                dev::st_async_v4(r_mail + (uint32_t)(col - c_lo) * kColumnBytes + rows4,
-                                 __float_as_uint(o[4 * j]), __float_as_uint(o[4 * j + 1]),
-                                 __float_as_uint(o[4 * j + 2]), __float_as_uint(o[4 * j + 3]), r_bar);
-              }
-            }
-          }
-        } else {
-          float x[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) x[e] = __uint_as_float(v[e]);
-          if (split > 1) {
-            if (first_group) waiter.wait<true>(bar_reduce, (uint32_t)(round & 1), kRoleEpiReduce, round);
-            // rank 0's partial + peers 1, 2, ... in rank order; each peer's
-            // 16 columns are loaded together.
-#pragma unroll 1
-            for (int peer = 1; peer < split; ++peer) {
-              const float* mp = mail + ((size_t)((peer - 1) * rc + (g * 16 - c_lo)) * kEpiThreads + et);
-              float w[16];
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const int c0 = g * 16 + 4 * j;
-                if (c0 >= c_lo && c0 < c_hi) {                  // live quad (warp-uniform)
-#pragma unroll
-                  for (int i = 0; i < 4; ++i) {
-                    w[4 * j + i] = (c0 + i < c_hi) ? mp[(size_t)(4 * j + i) * kEpiThreads] : 0.0f;
-                  }
-                } else {
-                  w[4 * j] = w[4 * j + 1] = w[4 * j + 2] = w[4 * j + 3] = 0.0f;
-                }
-              }
-#pragma unroll
-              for (int e = 0; e < 16; ++e) x[e] += w[e];
-            }
-          }
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int col = g * 16 + e;
-            if (col >= c_lo && col < c_hi) stage[(size_t)col * kMmaM + et] = x[e];
           }
         }
       }
-      // Every rank-0 thread has read this round before the mailbox is reused.
-      if (split > 1 && owner && q_end < nquads) dev::named_bar_sync(1, kEpiThreads);
-    }
-    // TMEM reads are done: let warp 2 release it.
-    dev::tc_fence_before();
-    dev::mbar_arrive(bar_tmem_empty);
-    if (et == 0) stamp(p, kTrReduced);
-
-    if (owner) {
-      // Rank 0 stores the tile: 16 vectors of 8 bf16 per token row, packed in
-      // pairs (low half first) and coalesced along n.
-      dev::named_bar_sync(1, kEpiThreads);
-      const int total = ncols * (kMmaM / 8);
+      // TMEM reads are done: let warp 2 release it.
+      dev::tc_fence_before();
+      dev::mbar_arrive(bar_tmem_empty);
+      if (et == 0) stamp(p, kTrReduced);
+      dev::named_bar_sync(1, kEpiThreads);                  // own slot complete
+      waiter.wait<true>(bar_reduce, 0u, kRoleEpiReduce, 0);
+      // 8 weight rows of one token column per item: sum the sources in rank
+      // order, pack bf16 pairs, one 16-byte store.
+      const int chunks = R / 8;
+      const int items = ncols * chunks;
 #pragma unroll 1
-      for (int idx = et; idx < total; idx += kEpiThreads) {
-        const int row = idx >> 4;
-        const int c8 = (idx & 15) * 8;
-        const int n = n0 + c8;
+      for (int it = et; it < items; it += kEpiThreads) {
+        const int m = it / chunks;
+        const int c8 = (it - m * chunks) * 8;
+        const float* src = mb + (size_t)m * R + c8;
+        float4 x = *reinterpret_cast<const float4*>(src);
+        float4 y = *reinterpret_cast<const float4*>(src + 4);
+#pragma unroll 1
+        for (int sr = 1; sr < split; ++sr) {
+          const float* ps = src + (size_t)sr * ncols * R;
+          const float4 a4 = *reinterpret_cast<const float4*>(ps);
+          const float4 b4 = *reinterpret_cast<const float4*>(ps + 4);
+          x.x += a4.x; x.y += a4.y; x.z += a4.z; x.w += a4.w;
+          y.x += b4.x; y.y += b4.y; y.z += b4.z; y.w += b4.w;
+        }
+        const int n = n0 + my_lo + c8;
         if (n >= p.N) continue;
-        const float4 x = *reinterpret_cast<const float4*>(stage + row * kMmaM + c8);
-        const float4 y = *reinterpret_cast<const float4*>(stage + row * kMmaM + c8 + 4);
         const uint32_t q0 = dev::pack_bf16x2(x.x, x.y), q1 = dev::pack_bf16x2(x.z, x.w);
         const uint32_t q2 = dev::pack_bf16x2(y.x, y.y), q3 = dev::pack_bf16x2(y.z, y.w);
-        uint16_t* dst = p.c + ((size_t)((size_t)l * p.M + (size_t)(m0 + row)) * (size_t)p.N + (size_t)n);
+        uint16_t* dst = p.c + ((size_t)((size_t)l * p.M + (size_t)(m0 + m)) * (size_t)p.N + (size_t)n);
         if (p.vec_store && n + 8 <= p.N) {
           dev::st_global_v4(dst, q0, q1, q2, q3);
         } else {
@@ -440,6 +394,138 @@ __global__ void __launch_bounds__(kThreads, 3)
         }
       }
       if (et == 0) stamp(p, kTrStored);
+    } else {
+      int round = 0;
+      for (int qb = 0; qb < nquads; qb += qr, ++round) {
+        const int q_end = (nquads - qb) < qr ? nquads : qb + qr;
+        const int c_lo = qb * 4;
+        // Mailbox of a round: [peer - 1][column - c_lo][row], f32; only the
+        // round's real token columns [c_lo, c_hi) travel.
+        const int c_hi = (ncols < q_end * 4) ? ncols : q_end * 4;
+        const int rc = c_hi - c_lo;
+        // The aliased mailbox (and any later round) waits for rank 0 to free it.
+        const bool need_ready = split > 1 && !(p.mailbox_dedicated && round == 0);
+        if (split > 1 && owner) {
+          if (et == 0) {
+            dev::mbar_arrive_expect_tx(bar_reduce, (uint32_t)(split - 1) * (uint32_t)rc * kColumnBytes);
+          }
+          // One thread per peer, in parallel: a release arrival waits for the
+          // issuing thread's earlier memory operations, so arrivals issued one
+          // after another from a single thread would serialise into round trips.
+          if (need_ready && et >= 1 && et < split) {
+            dev::mbar_arrive_remote(dev::mapa(bar_ready, (uint32_t)et));
+          }
+        }
+        const uint32_t r_bar = dev::mapa(bar_reduce, 0);
+        const uint32_t r_mail = dev::mapa(sMail, 0) + (uint32_t)((rank - 1) * rc) * kColumnBytes;
+        bool publish = split > 1 && !owner && !(p.inject & kInjectSkipPublish);
+        bool first_group = true;
+
+        // 16 token columns per TMEM load; quads of 4 columns within.
+  #pragma unroll 1
+        for (int g = qb >> 2; g * 4 < q_end; ++g, first_group = false) {
+          uint32_t v[16];
+          __syncwarp();   // tcgen05.ld is warp-collective
+          dev::tmem_ld_x16(t_row + (uint32_t)(g * 16), v);
+          dev::tmem_wait_ld();
+          if (split > 1 && !owner) {
+            // 4x4 transpose within lane quads: lane 4g'+r will send column
+            // c0+r of rows 4g'..4g'+3 as one 16-byte st.async.  Done before
+            // waiting for rank 0, so it overlaps that wait.
+            float o[16];
+  #pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int c0 = g * 16 + 4 * j;
+              if (c0 >= c_lo && c0 < c_hi) {                      // live quad (warp-uniform)
+                dev::quad_transpose(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                    __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]), lane,
+                                    &o[4 * j]);
+              }
+            }
+            if (first_group && publish && need_ready) {
+              publish = waiter.wait<true>(bar_ready,
+                                          (uint32_t)((round - (p.mailbox_dedicated ? 1 : 0)) & 1),
+                                          kRoleEpiReady, round);
+            }
+            if (publish) {
+              const uint32_t rows4 = (uint32_t)((warp & 3) * 32 + (lane & ~3)) * 4u;
+  #pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const int col = g * 16 + 4 * j + (lane & 3);
+                if (col >= c_lo && col < c_hi) {
+                  dev::st_async_v4(r_mail + (uint32_t)(col - c_lo) * kColumnBytes + rows4,
+                                   __float_as_uint(o[4 * j]), __float_as_uint(o[4 * j + 1]),
+                                   __float_as_uint(o[4 * j + 2]), __float_as_uint(o[4 * j + 3]), r_bar);
+                }
+              }
+            }
+          } else {
+            float x[16];
+  #pragma unroll
+            for (int e = 0; e < 16; ++e) x[e] = __uint_as_float(v[e]);
+            if (split > 1) {
+              if (first_group) waiter.wait<true>(bar_reduce, (uint32_t)(round & 1), kRoleEpiReduce, round);
+              // rank 0's partial + peers 1, 2, ... in rank order; each peer's
+              // 16 columns are loaded together.
+  #pragma unroll 1
+              for (int peer = 1; peer < split; ++peer) {
+                const float* mp = mail + ((size_t)((peer - 1) * rc + (g * 16 - c_lo)) * kEpiThreads + et);
+                float w[16];
+  #pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  const int c0 = g * 16 + 4 * j;
+                  if (c0 >= c_lo && c0 < c_hi) {                  // live quad (warp-uniform)
+  #pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                      w[4 * j + i] = (c0 + i < c_hi) ? mp[(size_t)(4 * j + i) * kEpiThreads] : 0.0f;
+                    }
+                  } else {
+                    w[4 * j] = w[4 * j + 1] = w[4 * j + 2] = w[4 * j + 3] = 0.0f;
+                  }
+                }
+  #pragma unroll
+                for (int e = 0; e < 16; ++e) x[e] += w[e];
+              }
+            }
+  #pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int col = g * 16 + e;
+              if (col >= c_lo && col < c_hi) stage[(size_t)col * kMmaM + et] = x[e];
+            }
+          }
+        }
+        // Every rank-0 thread has read this round before the mailbox is reused.
+        if (split > 1 && owner && q_end < nquads) dev::named_bar_sync(1, kEpiThreads);
+      }
+      // TMEM reads are done: let warp 2 release it.
+      dev::tc_fence_before();
+      dev::mbar_arrive(bar_tmem_empty);
+      if (et == 0) stamp(p, kTrReduced);
+
+      if (owner) {
+        // Rank 0 stores the tile: 16 vectors of 8 bf16 per token row, packed in
+        // pairs (low half first) and coalesced along n.
+        dev::named_bar_sync(1, kEpiThreads);
+        const int total = ncols * (kMmaM / 8);
+  #pragma unroll 1
+        for (int idx = et; idx < total; idx += kEpiThreads) {
+          const int row = idx >> 4;
+          const int c8 = (idx & 15) * 8;
+          const int n = n0 + c8;
+          if (n >= p.N) continue;
+          const float4 x = *reinterpret_cast<const float4*>(stage + row * kMmaM + c8);
+          const float4 y = *reinterpret_cast<const float4*>(stage + row * kMmaM + c8 + 4);
+          const uint32_t q0 = dev::pack_bf16x2(x.x, x.y), q1 = dev::pack_bf16x2(x.z, x.w);
+          const uint32_t q2 = dev::pack_bf16x2(y.x, y.y), q3 = dev::pack_bf16x2(y.z, y.w);
+          uint16_t* dst = p.c + ((size_t)((size_t)l * p.M + (size_t)(m0 + row)) * (size_t)p.N + (size_t)n);
+          if (p.vec_store && n + 8 <= p.N) {
+            dev::st_global_v4(dst, q0, q1, q2, q3);
+          } else {
+            store8_clipped(dst, n, p.N, q0, q1, q2, q3);
+          }
+        }
+        if (et == 0) stamp(p, kTrStored);
+      }
     }
   }
 

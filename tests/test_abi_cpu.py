@@ -63,11 +63,15 @@ def test_plan_of_the_decode_workloads():
     assert p.reduce_rounds >= 1 and p.mailbox_quads % 4 == 0
 
 
-def test_decode_tactics_keep_the_grid_resident_with_three_stages():
-    """Two CTAs per SM hold the whole grid; three stages fit beside it."""
-    for M, N, K, split in [(1, 7168, 2048, 4), (16, 4096, 7168, 8)]:
-        p = _plan(M, N, K, 1, split)
-        assert p.ctas_per_sm == 2 and p.stages == 3
+def test_decode_tactics():
+    """M=1: rank 0 reduces, 3 stages at 2 CTAs per SM.  M=16, split 8: each
+    rank reduces 16 rows (scattered), 2 stages still at 2 CTAs per SM."""
+    p = _plan(1, 7168, 2048, 1, 4)
+    assert (p.ctas_per_sm, p.stages, p.reduce_scatter) == (2, 3, 0)
+    p = _plan(16, 4096, 7168, 1, 8)
+    assert (p.ctas_per_sm, p.stages, p.reduce_scatter, p.mailbox_dedicated) == (2, 2, 1, 1)
+    assert p.smem_bytes == 1024 + 2 * (32768 + 16 * 256) + 16 * 512 + 256
+    for p in (_plan(1, 7168, 2048, 1, 4), _plan(16, 4096, 7168, 1, 8)):
         assert 2 * (p.smem_bytes + 1024) <= GB300["smem_per_sm"]
 
 
@@ -98,7 +102,10 @@ def test_every_plan_fits_and_is_consistent(M, split):
     assert 2 <= p.stages <= 8
     assert p.smem_bytes <= GB300["smem_per_block_optin"]
     # the reduction's mailbox fits where it is placed
-    if split > 1:
+    if p.reduce_scatter:
+        assert split >= 4 and min(M, p.mma_n) >= 16 and p.mailbox_dedicated == 1
+        assert p.smem_bytes == 1024 + p.stages * (32768 + p.mma_n * 256) + min(M, p.mma_n) * 512 + 256
+    elif split > 1:
         cols = min(4 * p.mailbox_quads, M, p.mma_n)
         round_bytes = (split - 1) * cols * 128 * 4
         ded = round_bytes if p.mailbox_dedicated else 0

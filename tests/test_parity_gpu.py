@@ -112,12 +112,24 @@ def test_deterministic_run_to_run():
 
 
 def _variant(base, stages, dedicated, quads, M, trigger=0):
+    """A rank-0-reduction plan; `quads` is capped to what an aliased mailbox
+    (the drained weight ring) holds."""
     p = sk.Plan.from_buffer_copy(base)
+    p.reduce_scatter = 0
     p.stages = stages
     p.mailbox_dedicated = dedicated
-    p.mailbox_quads = quads
     p.pdl_trigger = trigger
     ncm = min(M, p.mma_n)
+    nq = -(-ncm // 4)
+    quads = min(quads, nq) if quads < 4 else min(quads, max(4, nq))
+    if not dedicated and p.split_k > 1:
+        fits = lambda q: (p.split_k - 1) * min(4 * q, ncm) * 512 <= stages * 32768
+        if not fits(quads):
+            quads = 4
+            while quads + 4 <= nq and fits(quads + 4):
+                quads += 4
+    p.mailbox_quads = quads
+    p.reduce_rounds = -(-nq // quads)
     cols = min(4 * quads, ncm)
     ded = (p.split_k - 1) * cols * 512 if (dedicated and p.split_k > 1) else 0
     p.smem_bytes = 1024 + stages * (32768 + p.mma_n * 256) + ded + 256
@@ -171,3 +183,33 @@ def test_ragged_K_all_ones_is_exact():
         c = gemm_gpu(a, b, split_k=split)
         expect = oracle.gemm(a[:, :1, :], b[:, :1, :])[0, 0, 0]     # bf16 of K
         assert np.all(c == expect), (K, split)
+
+
+def _scatter(base, M, stages=None):
+    p = sk.Plan.from_buffer_copy(base)
+    if stages is not None:
+        p.stages = stages
+    ncm = min(M, p.mma_n)
+    p.reduce_scatter = 1
+    p.mailbox_dedicated = 1
+    p.mailbox_quads = -(-ncm // 4)
+    p.reduce_rounds = 1
+    p.smem_bytes = 1024 + p.stages * (32768 + p.mma_n * 256) + ncm * 512 + 256
+    return p
+
+
+@pytest.mark.parametrize("split", [2, 4, 8])
+@pytest.mark.parametrize("M", [1, 5, 16, 33, 64, 100, 128])
+def test_scattered_reduction_matches_rank0_bit_for_bit(M, split):
+    """Each rank summing 128/split rows in rank order gives the bits rank 0
+    gives summing the whole tile (same additions, same order)."""
+    L, N, K = 2, 300, 2040
+    a, b = _draw(L, M, N, K, seed=900 + M + split)
+    base = sk.splitk_plan(M, N, K, L, split)
+    c0 = gemm_gpu(a, b, plan=base)
+    p = _scatter(base, M)
+    if p.smem_bytes > 232448:
+        p = _scatter(base, M, stages=2)
+    c1 = gemm_gpu(a, b, plan=p)
+    assert np.array_equal(c0, c1)
+    assert_parity(c1, oracle_full(a, b), a, b, K)
