@@ -146,6 +146,19 @@ SPLITK_API int splitk_gemm_bf16(const void *a, const void *b, void *c,
                                 splitk_stream_t stream);
 
 /*
+ * C = B * A^T + bias with the bias added per output feature n in FP32 before
+ * the one rounding to bf16: C[l][m][n] = bf16_rne(sum_k A B + bias[l][n]).
+ * This is the bias argument of the page's SplitKGemm launcher (left unused
+ * there).  bias is a device pointer to [L][N] bf16, 2-byte aligned.  Like A,
+ * the bias is read before the programmatic-dependent-launch wait, so it must
+ * not be written by the kernel immediately before the call on the stream.
+ * Otherwise as splitk_gemm_bf16().
+ */
+SPLITK_API int splitk_gemm_bf16_bias(const void *a, const void *b, const void *bias,
+                                     void *c, int M, int N, int K, int L,
+                                     int split_k, splitk_stream_t stream);
+
+/*
  * As splitk_gemm_bf16() with an explicit plan (from splitk_plan() or
  * splitk_plan_for(), possibly with stages / mailbox fields edited; the call
  * re-validates it) and flags (SPLITK_FLAG_NO_PDL).

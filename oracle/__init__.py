@@ -65,6 +65,8 @@ def _load():
     lib.oracle_gemm.restype = None
     lib.oracle_gemm_threaded.argtypes = [u16p, u16p, u16p, i64, i64, i64, i64,
                                          ctypes.c_int]
+    lib.oracle_gemm_bias.argtypes = [u16p, u16p, u16p, u16p, i64, i64, i64, i64]
+    lib.oracle_gemm_bias.restype = None
     lib.oracle_gemm_threaded.restype = ctypes.c_int
     _lib = lib
     return lib
@@ -113,6 +115,18 @@ def gemm(A: np.ndarray, B: np.ndarray, threads: int = 1) -> np.ndarray:
     else:
         _load().oracle_gemm_threaded(_ptr(A), _ptr(B), _ptr(C), M, N, K, L,
                                      int(threads))
+    return C[0] if squeeze else C
+
+
+def gemm_bias(A: np.ndarray, B: np.ndarray, bias: np.ndarray) -> np.ndarray:
+    """C[L, M, N] = RNE(sum_k A[l,n,k] B[l,m,k] + bias[l,n]), float64 then one rounding."""
+    squeeze = A.ndim == 2
+    A, B, M, N, K, L = _shape(_u16(A), _u16(B))
+    A = np.ascontiguousarray(A)
+    B = np.ascontiguousarray(B)
+    bias = np.ascontiguousarray(_u16(bias)).reshape(L, N)
+    C = np.empty((L, M, N), dtype=np.uint16)
+    _load().oracle_gemm_bias(_ptr(A), _ptr(B), _ptr(bias), _ptr(C), M, N, K, L)
     return C[0] if squeeze else C
 
 

@@ -206,3 +206,21 @@ int oracle_gemm_threaded(const uint16_t *A, const uint16_t *B, uint16_t *C,
     free(jobs);
     return started > 0 ? started : 1;
 }
+
+/*
+ * GEMM with a per-output-feature bias (the bias argument of SplitKGemm's
+ * launcher on the vLLM "splitk" page, unused there):
+ *     C[l][m][n] = RNE_bf16( sum_k f64(A[l][n][k]) * f64(B[l][m][k]) + f64(bias[l][n]) )
+ * bias is [L][N] bf16; the sum and the bias are added in float64 and rounded
+ * once.
+ */
+void oracle_gemm_bias(const uint16_t *A, const uint16_t *B, const uint16_t *bias,
+                      uint16_t *C, int64_t M, int64_t N, int64_t K, int64_t L)
+{
+    for (int64_t l = 0; l < L; ++l)
+        for (int64_t m = 0; m < M; ++m)
+            for (int64_t n = 0; n < N; ++n)
+                C[(l * M + m) * N + n] = oracle_f64_to_bf16(
+                    oracle_dot_f64(A, B, M, N, K, l, m, n) +
+                    oracle_bf16_to_f64(bias[l * N + n]));
+}

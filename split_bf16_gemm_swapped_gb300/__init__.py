@@ -22,7 +22,8 @@ from . import _build
 __all__ = [
     "SplitKError", "Plan", "Fault", "library_path", "load_library",
     "splitk_plan", "splitk_plan_for", "splitk_gemm_bf16", "splitk_gemm_bf16_planned",
-    "splitk_gemm_bf16_hostio", "splitk_gemm_bf16_noalloc", "splitk_get_fault",
+    "splitk_gemm_bf16_hostio", "splitk_gemm_bf16_noalloc", "splitk_gemm_bf16_bias",
+    "splitk_get_fault",
     "splitk_get_status",
     "splitk_set_wait_limit_ns", "splitk_debug_inject", "splitk_release",
     "splitk_strerror", "splitk_version", "splitk_set_trace", "FLAG_NO_PDL",
@@ -107,6 +108,8 @@ def load_library():
     lib.splitk_plan_for.restype = i
     lib.splitk_gemm_bf16.argtypes = [vp, vp, vp, i, i, i, i, i, vp]
     lib.splitk_gemm_bf16.restype = i
+    lib.splitk_gemm_bf16_bias.argtypes = [vp, vp, vp, vp, i, i, i, i, i, vp]
+    lib.splitk_gemm_bf16_bias.restype = i
     lib.splitk_gemm_bf16_planned.argtypes = [vp, vp, vp, i, i, i, i, ctypes.POINTER(Plan), u, vp]
     lib.splitk_gemm_bf16_planned.restype = i
     lib.splitk_gemm_bf16_hostio.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, vp]
@@ -206,6 +209,24 @@ def splitk_gemm_bf16(a, b, c=None, split_k: int = 0, stream=None):
             a.data_ptr(), b.data_ptr(), c.data_ptr(), M, N, K, L, int(split_k),
             _stream_handle(stream, a.device))
     _check(rc, "splitk_gemm_bf16")
+    return c
+
+
+def splitk_gemm_bf16_bias(a, b, bias, c=None, split_k: int = 0, stream=None):
+    """c = b @ a^T + bias (bias [L, N] or [N] bfloat16, added in FP32 before
+    the one rounding); returns c."""
+    import torch
+    M, N, K, L = _dims(a, b)
+    _require_cuda(a, b, bias)
+    if bias.dtype != torch.bfloat16 or bias.numel() != L * N:
+        raise ValueError("bias must be a bfloat16 tensor of L*N elements")
+    c = _out(c, a, M, N, L)
+    _require_cuda(c)
+    with torch.cuda.device(a.device):
+        rc = load_library().splitk_gemm_bf16_bias(
+            a.data_ptr(), b.data_ptr(), bias.data_ptr(), c.data_ptr(), M, N, K, L,
+            int(split_k), _stream_handle(stream, a.device))
+    _check(rc, "splitk_gemm_bf16_bias")
     return c
 
 

@@ -414,7 +414,8 @@ int check_pointers(const void* a, const void* b, const void* c) {
 
 // Caller holds g_mu.
 int launch_locked(DeviceState& st, const void* a, const void* b, void* c, int M, int N, int K, int L,
-                  const splitk_plan_t& pl, unsigned flags, cudaStream_t stream) {
+                  const splitk_plan_t& pl, unsigned flags, cudaStream_t stream,
+                  const void* bias = nullptr) {
   uint32_t ded = 0;
   int rc = check_plan(pl, M, N, K, L, st.smem_optin, &ded);
   if (rc != SPLITK_OK) return rc;
@@ -428,6 +429,7 @@ int launch_locked(DeviceState& st, const void* a, const void* b, void* c, int M,
   KernelParams p;
   p.a_map = a_map;
   p.c = static_cast<uint16_t*>(c);
+  p.bias = static_cast<const uint16_t*>(bias);
   p.M = M;
   p.N = N;
   p.K = K;
@@ -460,7 +462,7 @@ int launch_locked(DeviceState& st, const void* a, const void* b, void* c, int M,
 }
 
 int gemm_auto(const void* a, const void* b, void* c, int M, int N, int K, int L, int split_k,
-              unsigned flags, cudaStream_t stream) {
+              unsigned flags, cudaStream_t stream, const void* bias = nullptr) {
   int rc = check_pointers(a, b, c);
   if (rc != SPLITK_OK) return rc;
   std::lock_guard<std::mutex> lock(g_mu);
@@ -470,7 +472,7 @@ int gemm_auto(const void* a, const void* b, void* c, int M, int N, int K, int L,
   splitk_plan_t pl;
   rc = plan_impl(M, N, K, L, split_k, st->num_sms, st->smem_per_sm, st->smem_optin, &pl);
   if (rc != SPLITK_OK) return rc;
-  return launch_locked(*st, a, b, c, M, N, K, L, pl, flags, stream);
+  return launch_locked(*st, a, b, c, M, N, K, L, pl, flags, stream, bias);
 }
 
 }  // namespace
@@ -497,6 +499,13 @@ SPLITK_API int splitk_plan(int M, int N, int K, int L, int split_k, splitk_plan_
 SPLITK_API int splitk_gemm_bf16(const void* a, const void* b, void* c, int M, int N, int K, int L,
                                 int split_k, splitk_stream_t stream) {
   return gemm_auto(a, b, c, M, N, K, L, split_k, 0u, reinterpret_cast<cudaStream_t>(stream));
+}
+
+SPLITK_API int splitk_gemm_bf16_bias(const void* a, const void* b, const void* bias, void* c, int M,
+                                     int N, int K, int L, int split_k, splitk_stream_t stream) {
+  if (!bias) return SPLITK_ERR_NULL;
+  if ((uintptr_t)bias & 1u) return SPLITK_ERR_MISALIGNED;
+  return gemm_auto(a, b, c, M, N, K, L, split_k, 0u, reinterpret_cast<cudaStream_t>(stream), bias);
 }
 
 SPLITK_API int splitk_gemm_bf16_planned(const void* a, const void* b, void* c, int M, int N, int K,
@@ -589,6 +598,7 @@ SPLITK_API int splitk_gemm_bf16_noalloc(const void* a, const void* b, void* c, i
   KernelParams p;
   p.a_map = scratch_map;
   p.c = static_cast<uint16_t*>(c);
+  p.bias = nullptr;
   p.M = M;
   p.N = N;
   p.K = K;

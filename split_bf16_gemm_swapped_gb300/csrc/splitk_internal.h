@@ -50,6 +50,7 @@ constexpr unsigned kInjectSkipPublish = 0x1u;
 struct KernelParams {
   const CUtensorMap* a_map;   // device address of A's tensor map
   uint16_t* c;                // C[L][M][N] bf16 bits
+  const uint16_t* bias;       // [L][N] bf16 bits added before rounding, or null
   int M, N, K, L;
   int split;                  // cluster size along K
   int stages;                 // ring depth

@@ -305,6 +305,20 @@ __global__ void __launch_bounds__(kThreads, 3)
     float* const stage = reinterpret_cast<float*>(smem_raw + (sB - raw));
     const float* const mail = reinterpret_cast<const float*>(smem_raw + (sMail - raw));
 
+    // The bias of the 8 weight rows this thread will store (a parameter like
+    // A, read before the accumulator is complete).  Rank-0 stores: rows
+    // (et % 16) * 8 of the tile; scattered stores: rows of this rank's slice.
+    float bias8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (p.bias != nullptr) {
+      const int nb = n0 + (p.reduce_scatter ? rank * (kMmaM / split) + (et % (kMmaM / split / 8)) * 8
+                                            : (et & 15) * 8);
+      const uint16_t* bp = p.bias + (size_t)l * (size_t)p.N + (size_t)nb;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        if (nb + e < p.N) bias8[e] = __uint_as_float((uint32_t)__ldg(bp + e) << 16);
+      }
+    }
+
     waiter.wait<false>(bar_mma_done, 0u, kRoleEpiMma, 0);
     __syncwarp();
     dev::tc_fence_after();
@@ -384,6 +398,8 @@ __global__ void __launch_bounds__(kThreads, 3)
         }
         const int n = n0 + my_lo + c8;
         if (n >= p.N) continue;
+        x.x += bias8[0]; x.y += bias8[1]; x.z += bias8[2]; x.w += bias8[3];
+        y.x += bias8[4]; y.y += bias8[5]; y.z += bias8[6]; y.w += bias8[7];
         const uint32_t q0 = dev::pack_bf16x2(x.x, x.y), q1 = dev::pack_bf16x2(x.z, x.w);
         const uint32_t q2 = dev::pack_bf16x2(y.x, y.y), q3 = dev::pack_bf16x2(y.z, y.w);
         uint16_t* dst = p.c + ((size_t)((size_t)l * p.M + (size_t)(m0 + m)) * (size_t)p.N + (size_t)n);
@@ -513,8 +529,10 @@ __global__ void __launch_bounds__(kThreads, 3)
           const int c8 = (idx & 15) * 8;
           const int n = n0 + c8;
           if (n >= p.N) continue;
-          const float4 x = *reinterpret_cast<const float4*>(stage + row * kMmaM + c8);
-          const float4 y = *reinterpret_cast<const float4*>(stage + row * kMmaM + c8 + 4);
+          float4 x = *reinterpret_cast<const float4*>(stage + row * kMmaM + c8);
+          float4 y = *reinterpret_cast<const float4*>(stage + row * kMmaM + c8 + 4);
+          x.x += bias8[0]; x.y += bias8[1]; x.z += bias8[2]; x.w += bias8[3];
+          y.x += bias8[4]; y.y += bias8[5]; y.z += bias8[6]; y.w += bias8[7];
           const uint32_t q0 = dev::pack_bf16x2(x.x, x.y), q1 = dev::pack_bf16x2(x.z, x.w);
           const uint32_t q2 = dev::pack_bf16x2(y.x, y.y), q3 = dev::pack_bf16x2(y.z, y.w);
           uint16_t* dst = p.c + ((size_t)((size_t)l * p.M + (size_t)(m0 + row)) * (size_t)p.N + (size_t)n);

@@ -257,3 +257,52 @@ def test_pins_catch_planted_mistakes():
     }
     for name, out in planted.items():
         assert not np.array_equal(out, exact), name
+
+
+# --------------------------------------------------------------------------
+# The GEMM with a bias
+# --------------------------------------------------------------------------
+def test_bias_alone_passes_through_bit_exactly():
+    from split_bf16_gemm_swapped_gb300 import synthetic
+    L, M, N, K = 2, 3, 37, 16
+    A = np.zeros((L, N, K), np.uint16)
+    B = synthetic.normal_bf16((L, M, K), 51, 1, 1.0)
+    bias = synthetic.normal_bf16((L, N), 51, 0, 0.5)
+    C = oracle.gemm_bias(A, B, bias)
+    expect = np.broadcast_to(bias[:, None, :], (L, M, N)).copy()
+    expect[(expect & 0x7FFF) == 0] = 0
+    assert np.array_equal(C, expect)
+
+
+def test_bias_adds_before_the_single_rounding():
+    """All-ones A and B with K=3 and a bias of 1/4 give exactly 3.25 (a bf16
+    value); random small cases match the exact rational sum plus bias,
+    rounded once."""
+    rng = np.random.default_rng(3)
+    L, M, N, K = 1, 2, 5, 3
+    A = np.full((L, N, K), ONE, np.uint16)
+    B = np.full((L, M, K), ONE, np.uint16)
+    bias = np.full((L, N), _exact.round_bf16(Fraction(1, 4)), np.uint16)
+    C = oracle.gemm_bias(A, B, bias)
+    assert np.all(C == _exact.round_bf16(Fraction(13, 4)))          # 3.25 is a bf16
+    from split_bf16_gemm_swapped_gb300 import synthetic
+    for trial in range(4):
+        L, M, N, K = 2, 3, 4, 6
+        A = synthetic.normal_bf16((L, N, K), 60 + trial, 0, 0.02)
+        B = synthetic.normal_bf16((L, M, K), 60 + trial, 1, 1.0)
+        bias = synthetic.normal_bf16((L, N), 60 + trial, 2, 0.1)
+        C = oracle.gemm_bias(A, B, bias)
+        for l in range(L):
+            for m in range(M):
+                for n in range(N):
+                    s = sum(_exact.value(int(A[l, n, k])) * _exact.value(int(B[l, m, k]))
+                            for k in range(K)) + _exact.value(int(bias[l, n]))
+                    assert C[l, m, n] == _exact.round_bf16(s)
+
+
+def test_zero_bias_is_the_plain_gemm():
+    from split_bf16_gemm_swapped_gb300 import synthetic
+    L, M, N, K = 1, 4, 33, 64
+    A = synthetic.normal_bf16((L, N, K), 70, 0, 0.02)
+    B = synthetic.normal_bf16((L, M, K), 70, 1, 1.0)
+    assert np.array_equal(oracle.gemm_bias(A, B, np.zeros((L, N), np.uint16)), oracle.gemm(A, B))

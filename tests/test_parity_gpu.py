@@ -213,3 +213,28 @@ def test_scattered_reduction_matches_rank0_bit_for_bit(M, split):
     c1 = gemm_gpu(a, b, plan=p)
     assert np.array_equal(c0, c1)
     assert_parity(c1, oracle_full(a, b), a, b, K)
+
+
+@pytest.mark.parametrize("M,N,K,split", [(1, 7168, 2048, 4), (16, 4096, 7168, 8), (5, 300, 1000, 2),
+                                         (33, 203, 1032, 4), (64, 256, 2048, 1), (128, 384, 2048, 8)])
+def test_bias_epilogue(M, N, K, split):
+    """C = B A^T + bias, the bias added in FP32 before the one rounding; both
+    reduction modes (rank 0 and scattered) carry it."""
+    L = 2
+    a, b = _draw(L, M, N, K, seed=1100 + M)
+    bias = synthetic.normal_bf16((L, N), 1100 + M, synthetic.STREAM_OUTLIER, 0.5)
+    ta, tb = to_dev(a), to_dev(b)
+    tbias = to_dev(bias)
+    torch.cuda.synchronize()
+    tc = sk.splitk_gemm_bf16_bias(ta, tb, tbias, split_k=split)
+    torch.cuda.synchronize()
+    assert sk.splitk_get_status() == 0
+    ref = oracle.gemm_bias(a, b, bias)
+    from tests import _tol
+    ok, rep = _tol.check(to_host(tc), ref, K, _tol.max_abs_bf16(a), _tol.max_abs_bf16(b))
+    assert ok, rep
+    # a zero bias gives the plain GEMM's bits
+    tz = sk.splitk_gemm_bf16_bias(ta, tb, torch.zeros_like(tbias), split_k=split)
+    plain = sk.splitk_gemm_bf16(ta, tb, split_k=split)
+    torch.cuda.synchronize()
+    assert torch.equal(tz.view(torch.int16), plain.view(torch.int16))
