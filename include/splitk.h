@@ -106,13 +106,28 @@ typedef struct splitk_plan_t {
     int ctas_per_sm;       /* CTAs the smem budget was sized for               */
     int pdl_trigger;       /* when a CTA lets the next kernel on the stream
                               launch: 0 after its last weight TMA issue,
-                              1 as soon as its set-up is done                  */
+                              1 as soon as it holds its tensor memory          */
     int reduce_scatter;    /* 0: rank 0 sums the whole tile and stores it (the
                               page's design); 1: rank r sums and stores weight
                               rows [r*128/split, (r+1)*128/split) -- same
                               additions in the same order, same bits, 1/split
                               of the DSMEM bytes per SM; needs split_k > 1 and
                               a dedicated mailbox of min(M, mma_n) * 512 B     */
+    int b_resident;        /* 0: each activation K tile rides the weight ring
+                              stage it is multiplied with (the page's design);
+                              1: all of the CTA's activation K tiles have their
+                              own buffer and arrive at once after the
+                              programmatic-dependent-launch wait               */
+    int a_tmem_tiles;      /* 0..3 leading weight K tiles that the MMA warp
+                              copies from the ring into tensor memory
+                              (tcgen05.cp) before the activations exist, so
+                              their stages take further tiles; the MMAs then
+                              read those tiles from tensor memory.  Needs
+                              b_resident = 1                                   */
+    unsigned tmem_cols;    /* tensor-memory columns per CTA (derived: the
+                              accumulator, then 64 per staged tile, rounded
+                              up to a power of two); the CTAs that fit an SM
+                              by shared memory never need more than 512        */
 } splitk_plan_t;
 
 /*

@@ -59,7 +59,8 @@ class Plan(ctypes.Structure):
         ("reduce_rounds", ctypes.c_int), ("grid", ctypes.c_uint * 3),
         ("cluster", ctypes.c_uint * 3), ("smem_bytes", ctypes.c_size_t),
         ("ctas_per_sm", ctypes.c_int), ("pdl_trigger", ctypes.c_int),
-        ("reduce_scatter", ctypes.c_int),
+        ("reduce_scatter", ctypes.c_int), ("b_resident", ctypes.c_int),
+        ("a_tmem_tiles", ctypes.c_int), ("tmem_cols", ctypes.c_uint),
     ]
 
     def as_dict(self) -> dict:

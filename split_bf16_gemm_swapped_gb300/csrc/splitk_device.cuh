@@ -105,13 +105,10 @@ __device__ __forceinline__ void cluster_wait_acquire() {
 
 // 16-byte asynchronous store into a peer CTA's shared memory; completes
 // 16 transaction bytes on the peer's mbarrier.
-__device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, uint32_t a, uint32_t b,
-                                            uint32_t c, uint32_t d, uint32_t cluster_bar) {
-  asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::
-          "r"(cluster_addr),
-      "r"(a), "r"(b), "r"(c), "r"(d), "r"(cluster_bar)
-      : "memory");
+__device__ __forceinline__ void st_async_b32(uint32_t cluster_addr, uint32_t a, uint32_t cluster_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(cluster_addr),
+               "r"(a), "r"(cluster_bar)
+               : "memory");
 }
 
 // ---------------------------------------------------------------- PDL
@@ -189,6 +186,26 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem desc]^T: the A operand (128 lanes x 16 bf16
+// = 8 columns) is read from tensor memory instead of shared memory.
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Copies a 128-row x 32-byte matrix (one MMA's K slice of A) described by a
+// shared-memory matrix descriptor into tensor memory: lane i, 8 columns.
+// Asynchronous; ordered before later tcgen05.mma of the same thread, and
+// tracked by tcgen05.commit.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t s_desc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(s_desc) : "memory");
 }
 
 // Arrives once on the mbarrier when all tcgen05 ops issued so far by this
@@ -276,25 +293,6 @@ __device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
   float v;
   asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
   return v;
-}
-
-// 4x4 transpose across the four lanes 4g..4g+3 of a warp: lane 4g+r holds
-// x[0..3] on entry; on exit o[u] = x[r] of lane 4g+u.  All 32 lanes call it.
-__device__ __forceinline__ void quad_transpose(float x0, float x1, float x2, float x3, int lane,
-                                               float o[4]) {
-  const int r = lane & 3;
-  const int g4 = lane & ~3;
-#pragma unroll
-  for (int s = 0; s < 4; ++s) {
-    const int e = (r - s) & 3;   // the element the receiving lane wants from us
-    const float offer = e == 0 ? x0 : e == 1 ? x1 : e == 2 ? x2 : x3;
-    const int u = (r + s) & 3;   // the lane we receive from
-    const float got = __shfl_sync(0xffffffffu, offer, g4 | u);
-    o[0] = u == 0 ? got : o[0];
-    o[1] = u == 1 ? got : o[1];
-    o[2] = u == 2 ? got : o[2];
-    o[3] = u == 3 ? got : o[3];
-  }
 }
 
 __device__ __forceinline__ void st_shared_f32(uint32_t addr, float v) {

@@ -55,10 +55,21 @@ int choose_mma_n(int M) {
   return 128;
 }
 
-size_t smem_bytes_for(int mma_n, int stages, uint32_t dedicated_mailbox_bytes) {
-  return (size_t)kAlignSlack + (size_t)stages * (kAStageBytes + b_stage_bytes(mma_n)) +
-         dedicated_mailbox_bytes + kBarRegionBytes;
+// Activation tiles the B region holds: the ring's stages, or every K tile
+// of the CTA (at least as many as stages, so rank 0's f32 staging tile of
+// min(M, mma_n) x 128 always fits once the region is drained).
+int b_region_tiles_for(int stages, int b_resident, int k_tiles) {
+  return b_resident ? std::max(stages, k_tiles) : stages;
 }
+
+size_t smem_bytes_for(int mma_n, int stages, uint32_t dedicated_mailbox_bytes, int b_region_tiles) {
+  return (size_t)kAlignSlack + (size_t)stages * kAStageBytes +
+         (size_t)b_region_tiles * b_stage_bytes(mma_n) + dedicated_mailbox_bytes + kBarRegionBytes;
+}
+
+// CTAs of this kernel that shared memory lets onto one SM (each CTA also
+// reserves 1 KiB of the SM's shared memory).
+int resident_by_smem(size_t smem_per_sm, size_t smem) { return (int)(smem_per_sm / (smem + 1024)); }
 
 // Bytes of one reduction round: (split - 1) peers x the round's token
 // columns (at most 4 per quad, at most the tile's real columns) x 128 rows.
@@ -132,7 +143,7 @@ int plan_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t smem_
     const size_t budget = std::min(smem_optin, smem_per_sm / (size_t)per_sm - 1024);
     if (try_scatter) {
       for (int stages = stages_cap; stages >= 2; --stages) {
-        const size_t smem = smem_bytes_for(mma_n, stages, scatter_bytes);
+        const size_t smem = smem_bytes_for(mma_n, stages, scatter_bytes, stages);
         if (smem > budget) continue;
         out->mma_m = kMmaM;
         out->mma_n = mma_n;
@@ -152,12 +163,15 @@ int plan_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t smem_
         out->ctas_per_sm = per_sm;
         out->pdl_trigger = 0;
         out->reduce_scatter = 1;
+        out->b_resident = 0;
+        out->a_tmem_tiles = 0;
+        out->tmem_cols = tmem_cols_for(mma_n, 0);
         return SPLITK_OK;
       }
     }
     for (int stages = stages_cap; stages >= 2; --stages) {
       const uint32_t ded = prefer_dedicated ? ded_bytes : 0u;
-      const size_t smem = smem_bytes_for(mma_n, stages, ded);
+      const size_t smem = smem_bytes_for(mma_n, stages, ded, stages);
       if (smem > budget) continue;
       // One round when the partials fit, else rounds of whole 16-column
       // groups (4 quads; at least one group always fits a 2-stage ring).
@@ -187,6 +201,9 @@ int plan_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t smem_
       out->ctas_per_sm = per_sm;
       out->pdl_trigger = 0;
       out->reduce_scatter = 0;
+      out->b_resident = 0;
+      out->a_tmem_tiles = 0;
+      out->tmem_cols = tmem_cols_for(mma_n, 0);
       return SPLITK_OK;
     }
   }
@@ -195,7 +212,7 @@ int plan_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t smem_
 
 // Re-derives everything a plan implies and checks it against the shape.
 int check_plan(const splitk_plan_t& pl, int M, int N, int K, int L, size_t smem_optin,
-               uint32_t* dedicated_bytes) {
+               size_t smem_per_sm, uint32_t* dedicated_bytes) {
   if (pl.mma_m != kMmaM) return SPLITK_ERR_BAD_PLAN;
   if (pl.mma_n != 16 && pl.mma_n != 32 && pl.mma_n != 64 && pl.mma_n != 128) return SPLITK_ERR_BAD_PLAN;
   if (!valid_split(pl.split_k)) return SPLITK_ERR_UNSUPPORTED_SPLIT;
@@ -218,6 +235,12 @@ int check_plan(const splitk_plan_t& pl, int M, int N, int K, int L, size_t smem_
   }
   if (pl.pdl_trigger != 0 && pl.pdl_trigger != 1) return SPLITK_ERR_BAD_PLAN;
   if (pl.reduce_scatter != 0 && pl.reduce_scatter != 1) return SPLITK_ERR_BAD_PLAN;
+  if (pl.b_resident != 0 && pl.b_resident != 1) return SPLITK_ERR_BAD_PLAN;
+  if (pl.a_tmem_tiles < 0 || pl.a_tmem_tiles > kMaxTmemTiles || pl.a_tmem_tiles > pl.k_tiles_per_cta ||
+      (pl.a_tmem_tiles > 0 && !pl.b_resident)) {
+    return SPLITK_ERR_BAD_PLAN;
+  }
+  if (pl.tmem_cols != tmem_cols_for(pl.mma_n, pl.a_tmem_tiles)) return SPLITK_ERR_BAD_PLAN;
   uint32_t ded = 0;
   if (pl.reduce_scatter) {
     // every rank's slice of every source rank, one round, own region
@@ -231,9 +254,15 @@ int check_plan(const splitk_plan_t& pl, int M, int N, int K, int L, size_t smem_
       return SPLITK_ERR_BAD_PLAN;
     }
   }
-  const size_t smem = smem_bytes_for(pl.mma_n, pl.stages, ded);
+  const size_t smem =
+      smem_bytes_for(pl.mma_n, pl.stages, ded, b_region_tiles_for(pl.stages, pl.b_resident, pl.k_tiles_per_cta));
   if (smem != pl.smem_bytes) return SPLITK_ERR_BAD_PLAN;
   if (smem > smem_optin) return SPLITK_ERR_NO_FIT;
+  // tcgen05.alloc waits for free columns: however many CTAs fit an SM, their
+  // allocations together must fit its 512 columns, or a CTA could wait on
+  // one that waits on it (a cluster peer, or the next kernel's CTA that
+  // waits for this kernel to complete).
+  if ((size_t)resident_by_smem(smem_per_sm, smem) * pl.tmem_cols > 512u) return SPLITK_ERR_BAD_PLAN;
   *dedicated_bytes = ded;
   return SPLITK_OK;
 }
@@ -412,12 +441,51 @@ int check_pointers(const void* a, const void* b, const void* c) {
   return SPLITK_OK;
 }
 
+// The kernel's parameters for a checked plan.
+void fill_params(const splitk_plan_t& pl, int M, int N, int K, int L, uint32_t ded, const CUtensorMap* a_map,
+                 void* c, const void* bias, KernelParams* p) {
+  p->a_map = a_map;
+  p->c = static_cast<uint16_t*>(c);
+  p->bias = static_cast<const uint16_t*>(bias);
+  p->M = M;
+  p->N = N;
+  p->K = K;
+  p->L = L;
+  p->split = pl.split_k;
+  p->stages = pl.stages;
+  p->k_tiles_total = total_k_tiles(K);
+  p->mailbox_dedicated = pl.split_k > 1 ? pl.mailbox_dedicated : 0;
+  p->mailbox_bytes = ded;
+  p->mailbox_quads = pl.mailbox_quads;
+  p->vec_store = ((N % 8) == 0 && ((uintptr_t)c & 15u) == 0) ? 1 : 0;
+  p->wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+  p->inject = g_inject.load(std::memory_order_relaxed);
+  p->pdl_trigger_early = pl.pdl_trigger;
+  p->reduce_scatter = pl.reduce_scatter;
+  p->b_resident = pl.b_resident;
+  p->b_region_tiles = b_region_tiles_for(pl.stages, pl.b_resident, pl.k_tiles_per_cta);
+  p->a_tmem_tiles = pl.a_tmem_tiles;
+  p->tmem_cols = pl.tmem_cols;
+  p->trace = g_trace.load(std::memory_order_relaxed);
+  p->trace_ctas = p->trace ? g_trace_ctas.load(std::memory_order_relaxed) : 0u;
+}
+
+LaunchArgs launch_args(const splitk_plan_t& pl, bool pdl) {
+  LaunchArgs la;
+  la.mma_n = pl.mma_n;
+  la.grid = dim3(pl.grid[0], pl.grid[1], pl.grid[2]);
+  la.cluster_x = (unsigned)pl.split_k;
+  la.smem_bytes = pl.smem_bytes;
+  la.pdl = pdl;
+  return la;
+}
+
 // Caller holds g_mu.
 int launch_locked(DeviceState& st, const void* a, const void* b, void* c, int M, int N, int K, int L,
                   const splitk_plan_t& pl, unsigned flags, cudaStream_t stream,
                   const void* bias = nullptr) {
   uint32_t ded = 0;
-  int rc = check_plan(pl, M, N, K, L, st.smem_optin, &ded);
+  int rc = check_plan(pl, M, N, K, L, st.smem_optin, st.smem_per_sm, &ded);
   if (rc != SPLITK_OK) return rc;
   const CUtensorMap* a_map = nullptr;
   rc = a_map_for(st, a, N, K, L, stream, &a_map);
@@ -427,33 +495,8 @@ int launch_locked(DeviceState& st, const void* a, const void* b, void* c, int M,
   if (rc != SPLITK_OK) return rc;
 
   KernelParams p;
-  p.a_map = a_map;
-  p.c = static_cast<uint16_t*>(c);
-  p.bias = static_cast<const uint16_t*>(bias);
-  p.M = M;
-  p.N = N;
-  p.K = K;
-  p.L = L;
-  p.split = pl.split_k;
-  p.stages = pl.stages;
-  p.k_tiles_total = total_k_tiles(K);
-  p.mailbox_dedicated = pl.split_k > 1 ? pl.mailbox_dedicated : 0;
-  p.mailbox_bytes = ded;
-  p.mailbox_quads = pl.mailbox_quads;
-  p.vec_store = ((N % 8) == 0 && ((uintptr_t)c & 15u) == 0) ? 1 : 0;
-  p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
-  p.inject = g_inject.load(std::memory_order_relaxed);
-  p.pdl_trigger_early = pl.pdl_trigger;
-  p.reduce_scatter = pl.reduce_scatter;
-  p.trace = g_trace.load(std::memory_order_relaxed);
-  p.trace_ctas = p.trace ? g_trace_ctas.load(std::memory_order_relaxed) : 0u;
-
-  LaunchArgs la;
-  la.mma_n = pl.mma_n;
-  la.grid = dim3(pl.grid[0], pl.grid[1], pl.grid[2]);
-  la.cluster_x = (unsigned)pl.split_k;
-  la.smem_bytes = pl.smem_bytes;
-  la.pdl = (flags & SPLITK_FLAG_NO_PDL) == 0;
+  fill_params(pl, M, N, K, L, ded, a_map, c, bias, &p);
+  const LaunchArgs la = launch_args(pl, (flags & SPLITK_FLAG_NO_PDL) == 0);
   if (launch_kernel(la, b_map, p, stream) != cudaSuccess) {
     cudaGetLastError();
     return SPLITK_ERR_CUDA;
@@ -569,7 +612,7 @@ SPLITK_API int splitk_gemm_bf16_noalloc(const void* a, const void* b, void* c, i
   rc = plan_impl(M, N, K, L, split_k, st->num_sms, st->smem_per_sm, st->smem_optin, &pl);
   if (rc != SPLITK_OK) return rc;
   uint32_t ded = 0;
-  rc = check_plan(pl, M, N, K, L, st->smem_optin, &ded);
+  rc = check_plan(pl, M, N, K, L, st->smem_optin, st->smem_per_sm, &ded);
   if (rc != SPLITK_OK) return rc;
   // Set-up, once per device, with that device current: the device address of
   // the scratch array.
@@ -596,32 +639,8 @@ SPLITK_API int splitk_gemm_bf16_noalloc(const void* a, const void* b, void* c, i
     return SPLITK_ERR_CUDA;
   }
   KernelParams p;
-  p.a_map = scratch_map;
-  p.c = static_cast<uint16_t*>(c);
-  p.bias = nullptr;
-  p.M = M;
-  p.N = N;
-  p.K = K;
-  p.L = L;
-  p.split = pl.split_k;
-  p.stages = pl.stages;
-  p.k_tiles_total = total_k_tiles(K);
-  p.mailbox_dedicated = pl.split_k > 1 ? pl.mailbox_dedicated : 0;
-  p.mailbox_bytes = ded;
-  p.mailbox_quads = pl.mailbox_quads;
-  p.vec_store = ((N % 8) == 0 && ((uintptr_t)c & 15u) == 0) ? 1 : 0;
-  p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
-  p.inject = g_inject.load(std::memory_order_relaxed);
-  p.pdl_trigger_early = pl.pdl_trigger;
-  p.reduce_scatter = pl.reduce_scatter;
-  p.trace = g_trace.load(std::memory_order_relaxed);
-  p.trace_ctas = p.trace ? g_trace_ctas.load(std::memory_order_relaxed) : 0u;
-  LaunchArgs la;
-  la.mma_n = pl.mma_n;
-  la.grid = dim3(pl.grid[0], pl.grid[1], pl.grid[2]);
-  la.cluster_x = (unsigned)pl.split_k;
-  la.smem_bytes = pl.smem_bytes;
-  la.pdl = true;
+  fill_params(pl, M, N, K, L, ded, scratch_map, c, nullptr, &p);
+  const LaunchArgs la = launch_args(pl, true);
   if (launch_kernel(la, b_map, p, s) != cudaSuccess) {
     cudaGetLastError();
     return SPLITK_ERR_CUDA;

@@ -129,7 +129,7 @@ __global__ void __launch_bounds__(kThreads, 3)
     splitk_gemm_bf16_kernel(const __grid_constant__ CUtensorMap b_map, const KernelParams p) {
   constexpr uint32_t kBStage = b_stage_bytes(MMA_N);
   constexpr uint32_t kBBox = kBStage / 2;                   // MMA_N rows x 128 B
-  constexpr uint32_t kTmemCols = MMA_N < 32 ? 32u : (uint32_t)MMA_N;
+  constexpr uint32_t kTileCol0 = tmem_tile_col0(MMA_N);     // first TMEM column of staged weight tiles
   constexpr uint32_t kIdesc = dev::idesc_bf16_f32(kMmaM, MMA_N);
 
   extern __shared__ uint8_t smem_raw[];
@@ -151,10 +151,13 @@ __global__ void __launch_bounds__(kThreads, 3)
   const int k_tiles = kt_base + (rank < kt_extra ? 1 : 0);
   const int kt0 = rank * kt_base + (rank < kt_extra ? rank : kt_extra);
 
-  // Shared memory: [A ring][B ring][dedicated mailbox?][barriers].
+  const bool b_res = p.b_resident != 0;
+  const int tmem_tiles = p.a_tmem_tiles < k_tiles ? p.a_tmem_tiles : k_tiles;
+
+  // Shared memory: [A ring][B ring or all B tiles][dedicated mailbox?][barriers].
   const uint32_t sA = base;
   const uint32_t sB = sA + (uint32_t)stages * kAStageBytes;
-  const uint32_t ring_end = sB + (uint32_t)stages * kBStage;
+  const uint32_t ring_end = sB + (uint32_t)p.b_region_tiles * kBStage;
   const uint32_t sMail = p.mailbox_dedicated ? ring_end : sA;
   const uint32_t sBar = ring_end + (p.mailbox_dedicated ? p.mailbox_bytes : 0u);
   const uint32_t bar_full0 = sBar;                       // [kMaxStages], count 2
@@ -165,44 +168,58 @@ __global__ void __launch_bounds__(kThreads, 3)
   const uint32_t bar_ready = bar_mma_done + 24u;         // count 1 (rank 0 arrives)
   const uint32_t slot_tmem = bar_mma_done + 32u;
   const uint32_t slot_abort = bar_mma_done + 36u;
+  const uint32_t bar_b = bar_mma_done + 40u;             // count 1 + tx bytes (resident B)
 
   const Waiter waiter{slot_abort, p.wait_limit_ns};
 
-  // ---- set-up: barriers (thread 0), TMEM (warp 2), first weight loads.
+  // ---- set-up, three warps in parallel: warp 3 initialises the barriers,
+  // warp 2 allocates TMEM, and warp 0 acquires A's tensor map (a round trip
+  // to global memory) and then issues the first ring pass of weight loads.
   // Every thread arrives on the cluster barrier (a 1-CTA cluster when
   // split_k = 1) once its own set-up is published, and waits on it before
-  // touching shared state.  Thread 0 issues the first ring pass of weight
-  // loads between its arrival and its wait: an arrival with release
-  // semantics after those issues would hold the whole cluster until the
-  // loads have landed.
+  // touching shared state.  Warp 0 arrives before issuing its loads: an
+  // arrival with release semantics after those issues would hold the whole
+  // cluster until the loads have landed.
   int a_issued = 0;
   uint64_t a_policy = 0;
-  if (threadIdx.x == 0) {
-    stamp(p, kTrStart);
-    for (int s = 0; s < stages; ++s) {
-      dev::mbar_init(bar_full0 + 8u * s, 2);
-      dev::mbar_init(bar_empty0 + 8u * s, 1);
+  if (warp == 3) {
+    if (lane == 0) {
+      for (int s = 0; s < stages; ++s) {
+        dev::mbar_init(bar_full0 + 8u * s, b_res ? 1u : 2u);   // A (and B when it rides the ring)
+        dev::mbar_init(bar_empty0 + 8u * s, 1);
+      }
+      dev::mbar_init(bar_b, 1);
+      dev::mbar_init(bar_mma_done, 1);
+      dev::mbar_init(bar_tmem_empty, kEpiThreads);
+      dev::mbar_init(bar_reduce, 1);
+      dev::mbar_init(bar_ready, 1);
+      dev::st_shared_u32(slot_abort, 0u);
+      dev::fence_barrier_init();
+      stamp(p, kTrBarInit);
     }
-    dev::mbar_init(bar_mma_done, 1);
-    dev::mbar_init(bar_tmem_empty, kEpiThreads);
-    dev::mbar_init(bar_reduce, 1);
-    dev::mbar_init(bar_ready, 1);
-    dev::st_shared_u32(slot_abort, 0u);
-    dev::fence_barrier_init();
-    stamp(p, kTrBarInit);
-  }
-  if (warp == 2) {
-    dev::tmem_alloc(slot_tmem, kTmemCols);
+    dev::named_bar_sync(2, 64);          // barriers exist for warp 0's loads
+  } else if (warp == 0) {
+    if (lane == 0) {
+      stamp(p, kTrStart);
+      dev::tensormap_acquire(p.a_map);   // the weight stream does not depend on the previous kernel
+      stamp(p, kTrMapReady);
+      a_policy = dev::policy_evict_first();
+    }
+    dev::named_bar_sync(2, 64);
+  } else if (warp == 2) {
+    dev::tmem_alloc(slot_tmem, p.tmem_cols);
     dev::tmem_relinquish();
     dev::tc_fence_before();
-    if (lane == 0) stamp(p, kTrTmemAlloc);
+    if (lane == 0) {
+      stamp(p, kTrTmemAlloc);
+      // Early trigger: the next kernel may launch once every CTA holds its
+      // tensor memory.  (Not before: a CTA of the next kernel that took the
+      // columns first would wait for this kernel, which would wait for it.)
+      if (p.pdl_trigger_early) dev::griddep_launch_dependents();
+    }
   }
   dev::cluster_arrive_release();
   if (threadIdx.x == 0) {
-    // The weight stream does not depend on the previous kernel: start it now.
-    dev::tensormap_acquire(p.a_map);
-    stamp(p, kTrMapReady);
-    a_policy = dev::policy_evict_first();
     const int first = k_tiles < stages ? k_tiles : stages;
     for (; a_issued < first; ++a_issued) {
       const uint32_t full = bar_full0 + 8u * a_issued;
@@ -227,8 +244,6 @@ __global__ void __launch_bounds__(kThreads, 3)
             (unsigned long long)smid() | ((unsigned long long)rank << 32);
       }
     }
-    // Early trigger: the next kernel may launch once every CTA got here.
-    if (p.pdl_trigger_early) dev::griddep_launch_dependents();
   }
   if (threadIdx.x == 128) stamp(p, kTrEpiSynced);
 
@@ -254,7 +269,17 @@ __global__ void __launch_bounds__(kThreads, 3)
     if (lane == 0) {
       dev::griddep_wait();
       stamp(p, kTrActReady);
-      for (int kt = 0; kt < k_tiles; ++kt) {
+      if (b_res) {
+        // Every activation K tile of this CTA at once, on one barrier.
+        dev::mbar_arrive_expect_tx(bar_b, (uint32_t)k_tiles * kBStage);
+        for (int kt = 0; kt < k_tiles; ++kt) {
+          const uint32_t dst = sB + (uint32_t)kt * kBStage;
+          const int k = (kt0 + kt) * kCtaK;
+          dev::tma_load_3d(dst, &b_map, k, m0, l, bar_b);
+          dev::tma_load_3d(dst + kBBox, &b_map, k + kAtomK, m0, l, bar_b);
+        }
+      }
+      for (int kt = 0; kt < (b_res ? 0 : k_tiles); ++kt) {
         const int s = kt % stages;
         const int r = kt / stages;
         const uint32_t full = bar_full0 + 8u * s;
@@ -272,15 +297,53 @@ __global__ void __launch_bounds__(kThreads, 3)
   } else if (warp == 2) {
     // ---- MMA issuer: D[128 x MMA_N] += A[128 x 16] * B[MMA_N x 16]^T, 8 per K tile.
     if (lane == 0) {
-      for (int kt = 0; kt < k_tiles; ++kt) {
+      bool ok = true;
+      // Before the activations can exist: copy the first `tmem_tiles` weight
+      // K tiles from the ring into tensor memory as they land, so their
+      // stages take further tiles and more of the CTA's weights are on chip
+      // when the previous kernel completes.
+      for (int kt = 0; kt < tmem_tiles && ok; ++kt) {
         const int s = kt % stages;
         const int r = kt / stages;
-        if (!waiter.wait<false>(bar_full0 + 8u * s, (uint32_t)(r & 1), kRoleMma, kt)) break;
+        ok = waiter.wait<false>(bar_full0 + 8u * s, (uint32_t)(r & 1), kRoleMma, kt);
+        if (!ok) break;
+        dev::tc_fence_after();
+        const uint32_t a_st = sA + (uint32_t)s * kAStageBytes;
+        const uint32_t t_col = tmem_base + kTileCol0 + (uint32_t)kt * kTmemTileCols;
+#pragma unroll
+        for (int kk = 0; kk < kCtaK / kMmaK; ++kk) {
+          const uint32_t a_off = (uint32_t)(kk >> 2) * kABoxBytes + (uint32_t)(kk & 3) * 32u;
+          dev::tmem_cp_128x256b(t_col + (uint32_t)kk * 8u, dev::smem_desc_sw128(a_st + a_off));
+        }
+        dev::mma_commit(bar_empty0 + 8u * s);  // stage free once the copies have read it
+      }
+      if (ok && b_res) {
+        ok = waiter.wait<false>(bar_b, 0u, kRoleMma, -1);
+        dev::tc_fence_after();
+      }
+      for (int kt = 0; kt < k_tiles && ok; ++kt) {
+        const int s = kt % stages;
+        const int r = kt / stages;
+        const uint32_t b_st = sB + (uint32_t)(b_res ? kt : s) * kBStage;
+        if (kt < tmem_tiles) {
+          // A from tensor memory (copied above, ordered before these MMAs)
+          if (kt == 0) stamp(p, kTrFirstFull);
+          if (kt == k_tiles - 1) stamp(p, kTrLastFull);
+          const uint32_t t_col = tmem_base + kTileCol0 + (uint32_t)kt * kTmemTileCols;
+#pragma unroll
+          for (int kk = 0; kk < kCtaK / kMmaK; ++kk) {
+            const uint32_t b_off = (uint32_t)(kk >> 2) * kBBox + (uint32_t)(kk & 3) * 32u;
+            dev::mma_bf16_ts(tmem_base, t_col + (uint32_t)kk * 8u, dev::smem_desc_sw128(b_st + b_off),
+                             kIdesc, (kt | kk) != 0 ? 1u : 0u);
+          }
+          continue;
+        }
+        ok = waiter.wait<false>(bar_full0 + 8u * s, (uint32_t)(r & 1), kRoleMma, kt);
+        if (!ok) break;
         dev::tc_fence_after();
         if (kt == 0) stamp(p, kTrFirstFull);
         if (kt == k_tiles - 1) stamp(p, kTrLastFull);
         const uint32_t a_st = sA + (uint32_t)s * kAStageBytes;
-        const uint32_t b_st = sB + (uint32_t)s * kBStage;
 #pragma unroll
         for (int kk = 0; kk < kCtaK / kMmaK; ++kk) {
           const uint32_t a_off = (uint32_t)(kk >> 2) * kABoxBytes + (uint32_t)(kk & 3) * 32u;
@@ -308,8 +371,13 @@ __global__ void __launch_bounds__(kThreads, 3)
     // The bias of the 8 weight rows this thread will store (a parameter like
     // A, read before the accumulator is complete).  Rank-0 stores: rows
     // (et % 16) * 8 of the tile; scattered stores: rows of this rank's slice.
+    // Narrow tiles (at most 4 token columns) store each thread's own row:
+    // the bias of row n0 + et.
+    const bool narrow = !p.reduce_scatter && ncols <= 4;
     float bias8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    if (p.bias != nullptr) {
+    if (p.bias != nullptr && narrow) {
+      if (n0 + et < p.N) bias8[0] = __uint_as_float((uint32_t)__ldg(p.bias + (size_t)l * (size_t)p.N + (size_t)(n0 + et)) << 16);
+    } else if (p.bias != nullptr) {
       const int nb = n0 + (p.reduce_scatter ? rank * (kMmaM / split) + (et % (kMmaM / split / 8)) * 8
                                             : (et & 15) * 8);
       const uint16_t* bp = p.bias + (size_t)l * (size_t)p.N + (size_t)nb;
@@ -338,10 +406,12 @@ __global__ void __launch_bounds__(kThreads, 3)
       if (et == 0) {
         dev::mbar_arrive_expect_tx(bar_reduce, (uint32_t)((split - 1) * ncols * R) * 4u);
       }
-      const int row0 = (warp & 3) * 32 + (lane & ~3);     // first row of this lane quad
-      const int dst_rank = row0 / R;                      // the rank that sums these rows
+      // Thread et holds weight row et: its value of column c goes to
+      // [rank][c][et - dst_rank*R] of the rank that sums row et; a warp's 32
+      // rows of one column are 128 contiguous bytes.
+      const int dst_rank = et / R;
       const bool publish = !(p.inject & kInjectSkipPublish);
-      const uint32_t slot = ((uint32_t)(rank * ncols) * (uint32_t)R + (uint32_t)(row0 - dst_rank * R)) * 4u;
+      const uint32_t slot = ((uint32_t)(rank * ncols) * (uint32_t)R + (uint32_t)(et - dst_rank * R)) * 4u;
       const uint32_t r_bar = dev::mapa(bar_reduce, (uint32_t)dst_rank);
       const uint32_t r_mail = dev::mapa(sMail, (uint32_t)dst_rank) + slot;
 #pragma unroll 1
@@ -351,23 +421,13 @@ __global__ void __launch_bounds__(kThreads, 3)
         dev::tmem_ld_x16(t_row + (uint32_t)(g * 16), v);
         dev::tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int c0 = g * 16 + 4 * j;
-          if (c0 >= ncols) continue;                          // warp-uniform
-          // lane 4g'+r gets column c0+r of the quad's 4 rows
-          float o[4];
-          dev::quad_transpose(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                              __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]), lane, o);
-          const int col = c0 + (lane & 3);
-          if (col < ncols) {
-            if (dst_rank == rank) {
-              *reinterpret_cast<float4*>(reinterpret_cast<uint8_t*>(mb) + slot + (size_t)col * R * 4) =
-                  make_float4(o[0], o[1], o[2], o[3]);
-            } else if (publish) {
-              dev::st_async_v4(r_mail + (uint32_t)(col * R) * 4u, __float_as_uint(o[0]),
-                               __float_as_uint(o[1]), __float_as_uint(o[2]), __float_as_uint(o[3]),
-                               r_bar);
-            }
+        for (int e = 0; e < 16; ++e) {
+          const int col = g * 16 + e;
+          if (col >= ncols) break;                            // warp-uniform
+          if (dst_rank == rank) {
+            *reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(mb) + slot + (size_t)col * R * 4) = v[e];
+          } else if (publish) {
+            dev::st_async_b32(r_mail + (uint32_t)(col * R) * 4u, v[e], r_bar);
           }
         }
       }
@@ -410,6 +470,68 @@ __global__ void __launch_bounds__(kThreads, 3)
         }
       }
       if (et == 0) stamp(p, kTrStored);
+    } else if (narrow) {
+      // One round, each thread its own weight row: peers send each live
+      // column with a 4-byte st.async into rank 0's mailbox [peer-1][column]
+      // [row]; rank 0 adds peers 1, 2, ... in rank order (the same additions
+      // as the wide path) and stores its row's outputs itself.
+      uint32_t v[4];
+      __syncwarp();   // tcgen05.ld is warp-collective
+      dev::tmem_ld_x4(t_row, v[0], v[1], v[2], v[3]);
+      dev::tmem_wait_ld();
+      if (split > 1 && !owner) {
+        bool publish = !(p.inject & kInjectSkipPublish);
+        if (publish && !p.mailbox_dedicated) {
+          publish = waiter.wait<true>(bar_ready, 0u, kRoleEpiReady, 0);
+        }
+        dev::tc_fence_before();
+        dev::mbar_arrive(bar_tmem_empty);
+        if (publish) {
+          const uint32_t r_bar = dev::mapa(bar_reduce, 0);
+          const uint32_t r_mail =
+              dev::mapa(sMail, 0) + (uint32_t)((rank - 1) * ncols) * kColumnBytes + (uint32_t)et * 4u;
+#pragma unroll
+          for (int col = 0; col < 4; ++col) {
+            if (col < ncols) dev::st_async_b32(r_mail + (uint32_t)col * kColumnBytes, v[col], r_bar);
+          }
+        }
+        if (et == 0) stamp(p, kTrReduced);
+      } else {
+        if (split > 1) {
+          if (et == 0) {
+            dev::mbar_arrive_expect_tx(bar_reduce, (uint32_t)(split - 1) * (uint32_t)ncols * kColumnBytes);
+          }
+          if (!p.mailbox_dedicated && et >= 1 && et < split) {
+            dev::mbar_arrive_remote(dev::mapa(bar_ready, (uint32_t)et));
+          }
+        }
+        float x[4];
+#pragma unroll
+        for (int col = 0; col < 4; ++col) x[col] = __uint_as_float(v[col]);
+        dev::tc_fence_before();
+        dev::mbar_arrive(bar_tmem_empty);
+        if (split > 1) {
+          waiter.wait<true>(bar_reduce, 0u, kRoleEpiReduce, 0);
+#pragma unroll 1
+          for (int peer = 1; peer < split; ++peer) {
+            const float* mp = mail + (size_t)((peer - 1) * ncols) * kEpiThreads + et;
+#pragma unroll
+            for (int col = 0; col < 4; ++col) {
+              if (col < ncols) x[col] += mp[(size_t)col * kEpiThreads];
+            }
+          }
+        }
+        if (et == 0) stamp(p, kTrReduced);
+        const int n = n0 + et;
+        if (n < p.N) {
+          uint16_t* dst = p.c + ((size_t)l * p.M + (size_t)m0) * (size_t)p.N + (size_t)n;
+#pragma unroll
+          for (int col = 0; col < 4; ++col) {
+            if (col < ncols) dst[(size_t)col * p.N] = (uint16_t)(dev::pack_bf16x2(x[col] + bias8[0], 0.0f) & 0xFFFFu);
+          }
+        }
+        if (et == 0) stamp(p, kTrStored);
+      }
     } else {
       int round = 0;
       for (int qb = 0; qb < nquads; qb += qr, ++round) {
@@ -445,33 +567,20 @@ __global__ void __launch_bounds__(kThreads, 3)
           dev::tmem_ld_x16(t_row + (uint32_t)(g * 16), v);
           dev::tmem_wait_ld();
           if (split > 1 && !owner) {
-            // 4x4 transpose within lane quads: lane 4g'+r will send column
-            // c0+r of rows 4g'..4g'+3 as one 16-byte st.async.  Done before
-            // waiting for rank 0, so it overlaps that wait.
-            float o[16];
-  #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int c0 = g * 16 + 4 * j;
-              if (c0 >= c_lo && c0 < c_hi) {                      // live quad (warp-uniform)
-                dev::quad_transpose(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                    __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]), lane,
-                                    &o[4 * j]);
-              }
-            }
             if (first_group && publish && need_ready) {
               publish = waiter.wait<true>(bar_ready,
                                           (uint32_t)((round - (p.mailbox_dedicated ? 1 : 0)) & 1),
                                           kRoleEpiReady, round);
             }
             if (publish) {
-              const uint32_t rows4 = (uint32_t)((warp & 3) * 32 + (lane & ~3)) * 4u;
+              // Thread et sends row et of each live column; a warp's 32 rows
+              // of one column are 128 contiguous bytes of the mailbox.
   #pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const int col = g * 16 + 4 * j + (lane & 3);
-                if (col >= c_lo && col < c_hi) {
-                  dev::st_async_v4(r_mail + (uint32_t)(col - c_lo) * kColumnBytes + rows4,
-                                   __float_as_uint(o[4 * j]), __float_as_uint(o[4 * j + 1]),
-                                   __float_as_uint(o[4 * j + 2]), __float_as_uint(o[4 * j + 3]), r_bar);
+              for (int e = 0; e < 16; ++e) {
+                const int col = g * 16 + e;
+                if (col >= c_lo && col < c_hi) {                  // warp-uniform
+                  dev::st_async_b32(r_mail + (uint32_t)(col - c_lo) * kColumnBytes + (uint32_t)et * 4u, v[e],
+                                    r_bar);
                 }
               }
             }
@@ -553,7 +662,7 @@ __global__ void __launch_bounds__(kThreads, 3)
     waiter.wait<false>(bar_tmem_empty, 0u, kRoleTmemRelease, 1, 4);
     dev::tc_fence_after();
     __syncwarp();
-    dev::tmem_dealloc(tmem_base, kTmemCols);
+    dev::tmem_dealloc(tmem_base, p.tmem_cols);
   }
   // With a dedicated mailbox and a single reduction round, rank 0 never
   // addresses a peer's shared memory and its reduction wait proves every

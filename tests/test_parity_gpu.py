@@ -238,3 +238,52 @@ def test_bias_epilogue(M, N, K, split):
     plain = sk.splitk_gemm_bf16(ta, tb, split_k=split)
     torch.cuda.synchronize()
     assert torch.equal(tz.view(torch.int16), plain.view(torch.int16))
+
+
+def _tmem_cols(mma_n, tiles):
+    if tiles == 0:
+        return max(32, mma_n)
+    need = (64 if mma_n <= 64 else 128) + 64 * tiles
+    return next(c for c in (32, 64, 128, 256, 512) if c >= need)
+
+
+def _staged(base, stages, tmem_tiles):
+    """`base` with every activation K tile in its own buffer and the first
+    `tmem_tiles` weight K tiles staged in tensor memory; None if the plan
+    cannot hold (shared memory, or tensor memory of the CTAs an SM fits)."""
+    p = sk.Plan.from_buffer_copy(base)
+    ded = base.smem_bytes - (1024 + base.stages * (32768 + base.mma_n * 256) + 256)
+    if not base.mailbox_dedicated and base.split_k > 1:
+        round_bytes = (base.split_k - 1) * min(4 * base.mailbox_quads, base.mma_n) * 512
+        if round_bytes > stages * 32768:
+            return None
+    p.stages = stages
+    p.b_resident = 1
+    p.a_tmem_tiles = tmem_tiles
+    p.tmem_cols = _tmem_cols(p.mma_n, tmem_tiles)
+    p.smem_bytes = 1024 + stages * 32768 + max(stages, p.k_tiles_per_cta) * p.mma_n * 256 + ded + 256
+    if p.smem_bytes > 232448 or 233472 // (p.smem_bytes + 1024) * p.tmem_cols > 512:
+        return None
+    return p
+
+
+@pytest.mark.parametrize("M,split", [(1, 4), (4, 1), (16, 8), (16, 2), (33, 4), (64, 2), (128, 8), (100, 8)])
+def test_staged_weights_and_resident_activations_give_the_same_bits(M, split):
+    """Weight K tiles copied into tensor memory (tcgen05.cp) and read by the
+    MMA from there, and activation tiles loaded all at once, give the bits of
+    the plain ring: the same products accumulate in the same order."""
+    L, N, K = 2, 300, 2048 + 8 * split
+    a, b = _draw(L, M, N, K, seed=1200 + M + split)
+    base = sk.splitk_plan(M, N, K, L, split)
+    c0 = gemm_gpu(a, b, plan=base)
+    assert_parity(c0, oracle_full(a, b), a, b, K)
+    ran = 0
+    for stages in (2, 3):
+        for tiles in (0, 1, 2, 3):
+            p = _staged(base, stages, tiles)
+            if p is None:
+                continue
+            c1 = gemm_gpu(a, b, plan=p)
+            assert np.array_equal(c0, c1), (stages, tiles)
+            ran += 1
+    assert ran >= 1
