@@ -415,7 +415,8 @@ def run_ours(args, w):
             "config": config_block(w, rotation) | {
                 "plan": {k: v for k, v in plan.as_dict().items()
                          if k in ("mma_n", "stages", "split_k", "grid", "smem_bytes",
-                                  "mailbox_dedicated", "reduce_rounds")},
+                                  "mailbox_dedicated", "reduce_rounds", "reduce_scatter",
+                                  "b_resident", "a_tmem_tiles", "mma_issuers", "pdl_trigger")},
                 "launch": "CUDA graphs of back-to-back launches with programmatic dependent launch",
                 "isolated_launch_us": round(iso_us, 2),
                 "isolated_note": "one launch per graph replay, events around the replay"},
@@ -481,7 +482,9 @@ def run_sweep(args):
                           "hbm_frac": round(tb * 1e3 / hbm, 3), "peak_source": src,
                           "plan": {k: v for k, v in p.as_dict().items()
                                    if k in ("mma_n", "stages", "grid", "smem_bytes",
-                                            "mailbox_dedicated", "reduce_rounds", "ctas_per_sm")}}),
+                                            "mailbox_dedicated", "reduce_rounds", "ctas_per_sm",
+                                            "reduce_scatter", "b_resident", "a_tmem_tiles",
+                                            "mma_issuers", "pdl_trigger")}}),
               flush=True)
         del As, b, c, g
         torch.cuda.empty_cache()

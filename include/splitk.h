@@ -125,9 +125,16 @@ typedef struct splitk_plan_t {
                               read those tiles from tensor memory.  Needs
                               b_resident = 1                                   */
     unsigned tmem_cols;    /* tensor-memory columns per CTA (derived: the
-                              accumulator, then 64 per staged tile, rounded
-                              up to a power of two); the CTAs that fit an SM
-                              by shared memory never need more than 512        */
+                              accumulators, then 64 per staged tile from a
+                              64-column boundary, rounded up to a power of
+                              two); the CTAs that fit an SM by shared memory
+                              never need more than 512                         */
+    int mma_issuers;       /* 1: one thread issues every MMA (the page's
+                              design); 2: a second thread takes the odd K
+                              tiles into its own accumulator, the epilogue
+                              adds the two (one more FP32 addition per output,
+                              in a fixed order); stages must be a multiple of
+                              mma_issuers                                      */
 } splitk_plan_t;
 
 /*

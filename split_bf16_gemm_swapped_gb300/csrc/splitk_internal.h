@@ -31,19 +31,22 @@ constexpr uint32_t kWaitHintNs = 1000000u;
 
 __host__ __device__ constexpr uint32_t b_stage_bytes(int mma_n) { return (uint32_t)mma_n * kCtaK * 2; }
 
-// Tensor memory: the accumulator takes columns [0, max(32, mma_n)); weight K
-// tiles staged in tensor memory (64 columns each: 128 lanes x 128 bf16) start
-// at a 64-column boundary after it.  Allocations are powers of two.
+// Tensor memory: one accumulator per MMA issuer, max(32, mma_n) columns
+// each, from column 0; weight K tiles staged in tensor memory (64 columns
+// each: 128 lanes x 128 bf16) from the next 64-column boundary.  Allocations
+// are powers of two.
 constexpr int kMaxTmemTiles = 3;
 constexpr uint32_t kTmemTileCols = 64;
 __host__ __device__ constexpr uint32_t tmem_acc_cols(int mma_n) { return mma_n < 32 ? 32u : (uint32_t)mma_n; }
-__host__ __device__ constexpr uint32_t tmem_tile_col0(int mma_n) { return mma_n <= 64 ? 64u : 128u; }
+__host__ __device__ constexpr uint32_t tmem_tile_col0(int mma_n, int issuers) {
+  return (tmem_acc_cols(mma_n) * (uint32_t)issuers + 63u) & ~63u;
+}
 __host__ __device__ constexpr uint32_t pow2_at_least(uint32_t v) {
   return v <= 32u ? 32u : v <= 64u ? 64u : v <= 128u ? 128u : v <= 256u ? 256u : 512u;
 }
-__host__ __device__ constexpr uint32_t tmem_cols_for(int mma_n, int tmem_tiles) {
-  return tmem_tiles == 0 ? tmem_acc_cols(mma_n)
-                         : pow2_at_least(tmem_tile_col0(mma_n) + kTmemTileCols * (uint32_t)tmem_tiles);
+__host__ __device__ constexpr uint32_t tmem_cols_for(int mma_n, int tmem_tiles, int issuers) {
+  return pow2_at_least(tmem_tiles == 0 ? tmem_acc_cols(mma_n) * (uint32_t)issuers
+                                       : tmem_tile_col0(mma_n, issuers) + kTmemTileCols * (uint32_t)tmem_tiles);
 }
 
 // Fault record in device memory (one per device, see splitk_fault_t).
@@ -82,6 +85,8 @@ struct KernelParams {
   int b_region_tiles;         // activation tiles the B region holds (ring stages or all)
   int a_tmem_tiles;           // leading weight K tiles moved into TMEM before the PDL wait
   uint32_t tmem_cols;         // TMEM columns allocated per CTA
+  uint32_t tmem_tile_col0;    // TMEM column of the first staged weight tile
+  int mma_issuers;            // 1 or 2 threads issuing MMAs (2: even/odd K tiles)
   unsigned long long* trace;  // per-CTA %globaltimer stamps, or null
   unsigned trace_ctas;        // CTAs the trace buffer holds
 };

@@ -122,6 +122,35 @@ __device__ __noinline__ void store8_clipped(uint16_t* dst, int n, int N, uint32_
   }
 }
 
+// Accumulator columns [col, col + 16) (or + 4) of this thread's TMEM lane:
+// with two MMA issuers, the sum of both accumulators (`second` columns
+// apart), accumulator 0 first.
+__device__ __forceinline__ void load_acc16(uint32_t taddr, uint32_t second, bool two, uint32_t (&v)[16]) {
+  dev::tmem_ld_x16(taddr, v);
+  if (two) {
+    uint32_t w[16];
+    dev::tmem_ld_x16(taddr + second, w);
+    dev::tmem_wait_ld();
+#pragma unroll
+    for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) + __uint_as_float(w[e]));
+  } else {
+    dev::tmem_wait_ld();
+  }
+}
+
+__device__ __forceinline__ void load_acc4(uint32_t taddr, uint32_t second, bool two, uint32_t (&v)[4]) {
+  dev::tmem_ld_x4(taddr, v[0], v[1], v[2], v[3]);
+  if (two) {
+    uint32_t w[4];
+    dev::tmem_ld_x4(taddr + second, w[0], w[1], w[2], w[3]);
+    dev::tmem_wait_ld();
+#pragma unroll
+    for (int e = 0; e < 4; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) + __uint_as_float(w[e]));
+  } else {
+    dev::tmem_wait_ld();
+  }
+}
+
 }  // namespace
 
 template <int MMA_N>
@@ -129,7 +158,7 @@ __global__ void __launch_bounds__(kThreads, 3)
     splitk_gemm_bf16_kernel(const __grid_constant__ CUtensorMap b_map, const KernelParams p) {
   constexpr uint32_t kBStage = b_stage_bytes(MMA_N);
   constexpr uint32_t kBBox = kBStage / 2;                   // MMA_N rows x 128 B
-  constexpr uint32_t kTileCol0 = tmem_tile_col0(MMA_N);     // first TMEM column of staged weight tiles
+  constexpr uint32_t kAccCols = tmem_acc_cols(MMA_N);       // TMEM columns of one accumulator
   constexpr uint32_t kIdesc = dev::idesc_bf16_f32(kMmaM, MMA_N);
 
   extern __shared__ uint8_t smem_raw[];
@@ -189,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, 3)
         dev::mbar_init(bar_empty0 + 8u * s, 1);
       }
       dev::mbar_init(bar_b, 1);
-      dev::mbar_init(bar_mma_done, 1);
+      dev::mbar_init(bar_mma_done, (uint32_t)p.mma_issuers);
       dev::mbar_init(bar_tmem_empty, kEpiThreads);
       dev::mbar_init(bar_reduce, 1);
       dev::mbar_init(bar_ready, 1);
@@ -294,22 +323,29 @@ __global__ void __launch_bounds__(kThreads, 3)
         dev::tma_load_3d(dst + kBBox, &b_map, k + kAtomK, m0, l, full);
       }
     }
-  } else if (warp == 2) {
-    // ---- MMA issuer: D[128 x MMA_N] += A[128 x 16] * B[MMA_N x 16]^T, 8 per K tile.
-    if (lane == 0) {
+  } else if (warp == 2 || warp == 3) {
+    // ---- MMA issuers: D[128 x MMA_N] += A[128 x 16] * B[MMA_N x 16]^T, 8 per
+    // K tile.  With two issuers (one tcgen05.mma stream per thread is
+    // issue-bound at MMA_N <= 64), warp 2 takes the even K tiles into
+    // accumulator 0 and warp 3 the odd ones into accumulator 1; the epilogue
+    // adds the two.
+    const int issuer = warp - 2;
+    const int nis = p.mma_issuers;
+    if (lane == 0 && issuer < nis) {
+      const uint32_t d_acc = tmem_base + (uint32_t)issuer * kAccCols;
       bool ok = true;
-      // Before the activations can exist: copy the first `tmem_tiles` weight
-      // K tiles from the ring into tensor memory as they land, so their
-      // stages take further tiles and more of the CTA's weights are on chip
-      // when the previous kernel completes.
-      for (int kt = 0; kt < tmem_tiles && ok; ++kt) {
+      // Before the activations can exist: copy this issuer's share of the
+      // first `tmem_tiles` weight K tiles from the ring into tensor memory as
+      // they land, so their stages take further tiles and more of the CTA's
+      // weights are on chip when the previous kernel completes.
+      for (int kt = issuer; kt < tmem_tiles && ok; kt += nis) {
         const int s = kt % stages;
         const int r = kt / stages;
         ok = waiter.wait<false>(bar_full0 + 8u * s, (uint32_t)(r & 1), kRoleMma, kt);
         if (!ok) break;
         dev::tc_fence_after();
         const uint32_t a_st = sA + (uint32_t)s * kAStageBytes;
-        const uint32_t t_col = tmem_base + kTileCol0 + (uint32_t)kt * kTmemTileCols;
+        const uint32_t t_col = tmem_base + p.tmem_tile_col0 + (uint32_t)kt * kTmemTileCols;
 #pragma unroll
         for (int kk = 0; kk < kCtaK / kMmaK; ++kk) {
           const uint32_t a_off = (uint32_t)(kk >> 2) * kABoxBytes + (uint32_t)(kk & 3) * 32u;
@@ -321,39 +357,39 @@ __global__ void __launch_bounds__(kThreads, 3)
         ok = waiter.wait<false>(bar_b, 0u, kRoleMma, -1);
         dev::tc_fence_after();
       }
-      for (int kt = 0; kt < k_tiles && ok; ++kt) {
+      for (int kt = issuer; kt < k_tiles && ok; kt += nis) {
         const int s = kt % stages;
         const int r = kt / stages;
+        const uint32_t first = (uint32_t)(kt >= nis);          // 0: this accumulator's first tile
         const uint32_t b_st = sB + (uint32_t)(b_res ? kt : s) * kBStage;
+        if (kt == issuer) stamp(p, kTrFirstFull);
         if (kt < tmem_tiles) {
           // A from tensor memory (copied above, ordered before these MMAs)
-          if (kt == 0) stamp(p, kTrFirstFull);
           if (kt == k_tiles - 1) stamp(p, kTrLastFull);
-          const uint32_t t_col = tmem_base + kTileCol0 + (uint32_t)kt * kTmemTileCols;
+          const uint32_t t_col = tmem_base + p.tmem_tile_col0 + (uint32_t)kt * kTmemTileCols;
 #pragma unroll
           for (int kk = 0; kk < kCtaK / kMmaK; ++kk) {
             const uint32_t b_off = (uint32_t)(kk >> 2) * kBBox + (uint32_t)(kk & 3) * 32u;
-            dev::mma_bf16_ts(tmem_base, t_col + (uint32_t)kk * 8u, dev::smem_desc_sw128(b_st + b_off),
-                             kIdesc, (kt | kk) != 0 ? 1u : 0u);
+            dev::mma_bf16_ts(d_acc, t_col + (uint32_t)kk * 8u, dev::smem_desc_sw128(b_st + b_off), kIdesc,
+                             (first | (uint32_t)kk) != 0u ? 1u : 0u);
           }
           continue;
         }
         ok = waiter.wait<false>(bar_full0 + 8u * s, (uint32_t)(r & 1), kRoleMma, kt);
         if (!ok) break;
         dev::tc_fence_after();
-        if (kt == 0) stamp(p, kTrFirstFull);
         if (kt == k_tiles - 1) stamp(p, kTrLastFull);
         const uint32_t a_st = sA + (uint32_t)s * kAStageBytes;
 #pragma unroll
         for (int kk = 0; kk < kCtaK / kMmaK; ++kk) {
           const uint32_t a_off = (uint32_t)(kk >> 2) * kABoxBytes + (uint32_t)(kk & 3) * 32u;
           const uint32_t b_off = (uint32_t)(kk >> 2) * kBBox + (uint32_t)(kk & 3) * 32u;
-          dev::mma_bf16(tmem_base, dev::smem_desc_sw128(a_st + a_off),
-                        dev::smem_desc_sw128(b_st + b_off), kIdesc, (kt | kk) != 0 ? 1u : 0u);
+          dev::mma_bf16(d_acc, dev::smem_desc_sw128(a_st + a_off), dev::smem_desc_sw128(b_st + b_off), kIdesc,
+                        (first | (uint32_t)kk) != 0u ? 1u : 0u);
         }
         dev::mma_commit(bar_empty0 + 8u * s);  // stage free once these MMAs finish
       }
-      dev::mma_commit(bar_mma_done);           // accumulator complete
+      dev::mma_commit(bar_mma_done);           // this issuer's accumulator complete
     }
     __syncwarp();
   } else if (warp >= 4) {
@@ -361,6 +397,7 @@ __global__ void __launch_bounds__(kThreads, 3)
     const int et = (int)threadIdx.x - 128;
     const uint32_t t_row = tmem_base + ((uint32_t)((warp & 3) * 32) << 16);
     const int ncols = (p.M - m0) < MMA_N ? (p.M - m0) : MMA_N;    // real token columns
+    const bool two_acc = p.mma_issuers > 1 && k_tiles > 1;        // the odd K tiles' accumulator is in use
     const int nquads = (ncols + 3) >> 2;
     const int qr = p.mailbox_quads;                               // quads per round
     const bool owner = rank == 0;
@@ -418,8 +455,7 @@ __global__ void __launch_bounds__(kThreads, 3)
       for (int g = 0; g * 16 < ncols; ++g) {
         uint32_t v[16];
         __syncwarp();   // tcgen05.ld is warp-collective
-        dev::tmem_ld_x16(t_row + (uint32_t)(g * 16), v);
-        dev::tmem_wait_ld();
+        load_acc16(t_row + (uint32_t)(g * 16), kAccCols, two_acc, v);
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const int col = g * 16 + e;
@@ -477,8 +513,7 @@ __global__ void __launch_bounds__(kThreads, 3)
       // as the wide path) and stores its row's outputs itself.
       uint32_t v[4];
       __syncwarp();   // tcgen05.ld is warp-collective
-      dev::tmem_ld_x4(t_row, v[0], v[1], v[2], v[3]);
-      dev::tmem_wait_ld();
+      load_acc4(t_row, kAccCols, two_acc, v);
       if (split > 1 && !owner) {
         bool publish = !(p.inject & kInjectSkipPublish);
         if (publish && !p.mailbox_dedicated) {
@@ -564,8 +599,7 @@ __global__ void __launch_bounds__(kThreads, 3)
         for (int g = qb >> 2; g * 4 < q_end; ++g, first_group = false) {
           uint32_t v[16];
           __syncwarp();   // tcgen05.ld is warp-collective
-          dev::tmem_ld_x16(t_row + (uint32_t)(g * 16), v);
-          dev::tmem_wait_ld();
+          load_acc16(t_row + (uint32_t)(g * 16), kAccCols, two_acc, v);
           if (split > 1 && !owner) {
             if (first_group && publish && need_ready) {
               publish = waiter.wait<true>(bar_ready,

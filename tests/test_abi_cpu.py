@@ -64,15 +64,29 @@ def test_plan_of_the_decode_workloads():
 
 
 def test_decode_tactics():
-    """M=1: rank 0 reduces, 3 stages at 2 CTAs per SM.  M=16, split 8: each
-    rank reduces 16 rows (scattered), 2 stages still at 2 CTAs per SM."""
+    """The staged decode tactic: a 2-stage weight ring, all activation tiles
+    resident, the first min(3, k_tiles - 2) weight tiles staged in tensor
+    memory, two MMA issuers, early trigger, 2 CTAs per SM.  M=1: rank 0
+    reduces; M=16, split 8: each rank reduces 16 rows (scattered)."""
     p = _plan(1, 7168, 2048, 1, 4)
-    assert (p.ctas_per_sm, p.stages, p.reduce_scatter) == (2, 3, 0)
+    assert (p.ctas_per_sm, p.stages, p.reduce_scatter, p.mailbox_dedicated) == (2, 2, 0, 1)
+    assert (p.b_resident, p.a_tmem_tiles, p.mma_issuers, p.pdl_trigger, p.tmem_cols) == (1, 2, 2, 1, 256)
+    assert p.smem_bytes == 1024 + 2 * 32768 + 4 * 16 * 256 + 3 * 512 + 256
     p = _plan(16, 4096, 7168, 1, 8)
     assert (p.ctas_per_sm, p.stages, p.reduce_scatter, p.mailbox_dedicated) == (2, 2, 1, 1)
-    assert p.smem_bytes == 1024 + 2 * (32768 + 16 * 256) + 16 * 512 + 256
+    assert (p.b_resident, p.a_tmem_tiles, p.mma_issuers, p.pdl_trigger, p.tmem_cols) == (1, 3, 2, 1, 256)
+    assert p.smem_bytes == 1024 + 2 * 32768 + 7 * 16 * 256 + 16 * 512 + 256
     for p in (_plan(1, 7168, 2048, 1, 4), _plan(16, 4096, 7168, 1, 8)):
         assert 2 * (p.smem_bytes + 1024) <= GB300["smem_per_sm"]
+        assert GB300["smem_per_sm"] // (p.smem_bytes + 1024) * p.tmem_cols <= 512
+
+
+def test_long_k_and_wide_shapes_keep_the_ring():
+    """Where all activation tiles do not fit beside the ring at 2 CTAs per SM
+    (long K) or tiles are wide, the plan keeps the page's ring design."""
+    for args in [(1, 7168, 16384, 2, 4), (32, 7168, 16384, 2, 2), (64, 18432, 7168, 1, 2)]:
+        p = _plan(*args)
+        assert (p.b_resident, p.a_tmem_tiles, p.mma_issuers, p.pdl_trigger) == (0, 0, 1, 0), args
 
 
 def test_auto_split_fills_the_sms_with_the_smallest_split():
@@ -101,10 +115,17 @@ def test_every_plan_fits_and_is_consistent(M, split):
     assert p.grid[0] == split * -(-M // p.mma_n)
     assert 2 <= p.stages <= 8
     assert p.smem_bytes <= GB300["smem_per_block_optin"]
+    assert p.mma_issuers in (1, 2) and p.stages % p.mma_issuers == 0
+    assert 0 <= p.a_tmem_tiles <= 3 and (p.a_tmem_tiles == 0 or p.b_resident)
+    acc = max(32, p.mma_n) * p.mma_issuers
+    need = acc if p.a_tmem_tiles == 0 else (acc + 63) // 64 * 64 + 64 * p.a_tmem_tiles
+    assert p.tmem_cols == next(c for c in (32, 64, 128, 256, 512) if c >= need)
+    assert GB300["smem_per_sm"] // (p.smem_bytes + 1024) * p.tmem_cols <= 512
+    b_tiles = max(p.stages, p.k_tiles_per_cta) if p.b_resident else p.stages
     # the reduction's mailbox fits where it is placed
     if p.reduce_scatter:
         assert split >= 4 and min(M, p.mma_n) >= 16 and p.mailbox_dedicated == 1
-        assert p.smem_bytes == 1024 + p.stages * (32768 + p.mma_n * 256) + min(M, p.mma_n) * 512 + 256
+        assert p.smem_bytes == 1024 + p.stages * 32768 + b_tiles * p.mma_n * 256 + min(M, p.mma_n) * 512 + 256
     elif split > 1:
         cols = min(4 * p.mailbox_quads, M, p.mma_n)
         round_bytes = (split - 1) * cols * 128 * 4
@@ -113,9 +134,9 @@ def test_every_plan_fits_and_is_consistent(M, split):
             assert round_bytes <= p.stages * 32768
         nquads = -(-min(M, p.mma_n) // 4)
         assert p.reduce_rounds == -(-nquads // p.mailbox_quads)
-        assert p.smem_bytes == 1024 + p.stages * (32768 + p.mma_n * 256) + ded + 256
+        assert p.smem_bytes == 1024 + p.stages * 32768 + b_tiles * p.mma_n * 256 + ded + 256
     # the f32 staging tile of rank 0 fits in its drained activation ring
-    assert min(M, p.mma_n) * 128 * 4 <= p.stages * p.mma_n * 256
+    assert min(M, p.mma_n) * 128 * 4 <= b_tiles * p.mma_n * 256
 
 
 @pytest.mark.parametrize("args,code", [

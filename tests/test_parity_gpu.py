@@ -111,10 +111,33 @@ def test_deterministic_run_to_run():
         assert np.array_equal(c, first)
 
 
+def _mailbox_bytes(p, M):
+    """Bytes of the plan's dedicated mailbox region (0 when aliased)."""
+    ncm = min(M, p.mma_n)
+    if p.split_k == 1 or not p.mailbox_dedicated:
+        return 0
+    if p.reduce_scatter:
+        return ncm * 512
+    return (p.split_k - 1) * min(4 * p.mailbox_quads, ncm) * 512
+
+
+def _ring(base, M=None):
+    """`base` as the page's ring design: activations ride the weight ring,
+    no tensor-memory staging, one MMA issuer."""
+    p = sk.Plan.from_buffer_copy(base)
+    p.b_resident = 0
+    p.a_tmem_tiles = 0
+    p.mma_issuers = 1
+    p.tmem_cols = max(32, p.mma_n)
+    p.smem_bytes = (1024 + p.stages * (32768 + p.mma_n * 256)
+                    + _mailbox_bytes(p, M if M is not None else p.mma_n) + 256)
+    return p
+
+
 def _variant(base, stages, dedicated, quads, M, trigger=0):
     """A rank-0-reduction plan; `quads` is capped to what an aliased mailbox
     (the drained weight ring) holds."""
-    p = sk.Plan.from_buffer_copy(base)
+    p = _ring(base)
     p.reduce_scatter = 0
     p.stages = stages
     p.mailbox_dedicated = dedicated
@@ -186,7 +209,7 @@ def test_ragged_K_all_ones_is_exact():
 
 
 def _scatter(base, M, stages=None):
-    p = sk.Plan.from_buffer_copy(base)
+    p = _ring(base)
     if stages is not None:
         p.stages = stages
     ncm = min(M, p.mma_n)
@@ -205,7 +228,7 @@ def test_scattered_reduction_matches_rank0_bit_for_bit(M, split):
     gives summing the whole tile (same additions, same order)."""
     L, N, K = 2, 300, 2040
     a, b = _draw(L, M, N, K, seed=900 + M + split)
-    base = sk.splitk_plan(M, N, K, L, split)
+    base = _ring(sk.splitk_plan(M, N, K, L, split), M)
     c0 = gemm_gpu(a, b, plan=base)
     p = _scatter(base, M)
     if p.smem_bytes > 232448:
@@ -240,28 +263,32 @@ def test_bias_epilogue(M, N, K, split):
     assert torch.equal(tz.view(torch.int16), plain.view(torch.int16))
 
 
-def _tmem_cols(mma_n, tiles):
-    if tiles == 0:
-        return max(32, mma_n)
-    need = (64 if mma_n <= 64 else 128) + 64 * tiles
+def _tmem_cols(mma_n, tiles, issuers=1):
+    acc = max(32, mma_n) * issuers
+    need = acc if tiles == 0 else (acc + 63) // 64 * 64 + 64 * tiles
     return next(c for c in (32, 64, 128, 256, 512) if c >= need)
 
 
-def _staged(base, stages, tmem_tiles):
-    """`base` with every activation K tile in its own buffer and the first
-    `tmem_tiles` weight K tiles staged in tensor memory; None if the plan
-    cannot hold (shared memory, or tensor memory of the CTAs an SM fits)."""
+def _staged(base, stages, tmem_tiles, issuers=1, b_resident=1, M=None):
+    """`base` with every activation K tile in its own buffer, the first
+    `tmem_tiles` weight K tiles staged in tensor memory and `issuers` MMA
+    threads; None if the plan cannot hold (shared memory, or tensor memory of
+    the CTAs an SM fits)."""
+    if stages % issuers:
+        return None                   # a stage would have two consumers
     p = sk.Plan.from_buffer_copy(base)
-    ded = base.smem_bytes - (1024 + base.stages * (32768 + base.mma_n * 256) + 256)
+    ded = _mailbox_bytes(base, M if M is not None else base.mma_n)
     if not base.mailbox_dedicated and base.split_k > 1:
         round_bytes = (base.split_k - 1) * min(4 * base.mailbox_quads, base.mma_n) * 512
         if round_bytes > stages * 32768:
             return None
     p.stages = stages
-    p.b_resident = 1
+    p.b_resident = b_resident
     p.a_tmem_tiles = tmem_tiles
-    p.tmem_cols = _tmem_cols(p.mma_n, tmem_tiles)
-    p.smem_bytes = 1024 + stages * 32768 + max(stages, p.k_tiles_per_cta) * p.mma_n * 256 + ded + 256
+    p.mma_issuers = issuers
+    p.tmem_cols = _tmem_cols(p.mma_n, tmem_tiles, issuers)
+    b_tiles = max(stages, p.k_tiles_per_cta) if b_resident else stages
+    p.smem_bytes = 1024 + stages * 32768 + b_tiles * p.mma_n * 256 + ded + 256
     if p.smem_bytes > 232448 or 233472 // (p.smem_bytes + 1024) * p.tmem_cols > 512:
         return None
     return p
@@ -274,16 +301,57 @@ def test_staged_weights_and_resident_activations_give_the_same_bits(M, split):
     the plain ring: the same products accumulate in the same order."""
     L, N, K = 2, 300, 2048 + 8 * split
     a, b = _draw(L, M, N, K, seed=1200 + M + split)
-    base = sk.splitk_plan(M, N, K, L, split)
+    base = _ring(sk.splitk_plan(M, N, K, L, split), M)
     c0 = gemm_gpu(a, b, plan=base)
     assert_parity(c0, oracle_full(a, b), a, b, K)
     ran = 0
     for stages in (2, 3):
         for tiles in (0, 1, 2, 3):
-            p = _staged(base, stages, tiles)
+            p = _staged(base, stages, tiles, M=M)
             if p is None:
                 continue
             c1 = gemm_gpu(a, b, plan=p)
             assert np.array_equal(c0, c1), (stages, tiles)
             ran += 1
     assert ran >= 1
+
+
+@pytest.mark.parametrize("M,split", [(1, 4), (3, 1), (16, 8), (16, 2), (33, 4), (64, 2), (100, 8)])
+def test_two_mma_issuers(M, split):
+    """A second MMA thread takes the odd K tiles into its own accumulator:
+    parity with the oracle, exact closed forms, and every staging variant of
+    the two-issuer plan gives the same bits (same products, same order)."""
+    L, N, K = 2, 300, 2048 + 8 * split
+    a, b = _draw(L, M, N, K, seed=1300 + M + split)
+    base = sk.splitk_plan(M, N, K, L, split)
+    p2 = _staged(base, 2, 0, issuers=2, b_resident=0, M=M)
+    assert p2 is not None
+    c2 = gemm_gpu(a, b, plan=p2)
+    assert_parity(c2, oracle_full(a, b), a, b, K)
+    ran = 0
+    for stages in (2, 3):
+        for tiles in (0, 1, 2, 3):
+            p = _staged(base, stages, tiles, issuers=2, M=M)
+            if p is None:
+                continue
+            assert np.array_equal(gemm_gpu(a, b, plan=p), c2), (stages, tiles)
+            ran += 1
+    assert ran >= 1
+    ones = np.full((L, N, K), ONE, np.uint16)
+    c = gemm_gpu(ones, np.full((L, M, K), ONE, np.uint16), plan=p2)
+    assert np.all(c == oracle.gemm(ones[:1, :1, :], np.full((1, 1, K), ONE, np.uint16))[0, 0, 0])
+
+
+def test_two_issuers_need_an_even_ring():
+    """With an odd stage count a ring stage would have two consumers; the
+    library refuses such a plan before launching anything."""
+    base = _ring(sk.splitk_plan(1, 512, 2048, 1, 4), 1)
+    p = sk.Plan.from_buffer_copy(base)
+    p.stages = 3
+    p.mma_issuers = 2
+    p.tmem_cols = _tmem_cols(p.mma_n, 0, 2)
+    p.smem_bytes = 1024 + 3 * (32768 + p.mma_n * 256) + _mailbox_bytes(base, 1) + 256
+    a, b = _draw(1, 1, 512, 2048, seed=7)
+    with pytest.raises(sk.SplitKError) as e:
+        sk.splitk_gemm_bf16_planned(to_dev(a), to_dev(b), None, p)
+    assert e.value.name == "SPLITK_ERR_BAD_PLAN"
