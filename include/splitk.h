@@ -135,6 +135,10 @@ typedef struct splitk_plan_t {
                               adds the two (one more FP32 addition per output,
                               in a fixed order); stages must be a multiple of
                               mma_issuers                                      */
+    int b_loader;          /* with b_resident: 0 the activation warp loads the
+                              activation tiles by TMA; 1 the 128 epilogue
+                              threads load them with 16-byte loads and store
+                              them swizzled (for few rows: no TMA queue)       */
 } splitk_plan_t;
 
 /*

@@ -61,7 +61,7 @@ class Plan(ctypes.Structure):
         ("ctas_per_sm", ctypes.c_int), ("pdl_trigger", ctypes.c_int),
         ("reduce_scatter", ctypes.c_int), ("b_resident", ctypes.c_int),
         ("a_tmem_tiles", ctypes.c_int), ("tmem_cols", ctypes.c_uint),
-        ("mma_issuers", ctypes.c_int),
+        ("mma_issuers", ctypes.c_int), ("b_loader", ctypes.c_int),
     ]
 
     def as_dict(self) -> dict:

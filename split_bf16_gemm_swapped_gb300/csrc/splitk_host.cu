@@ -130,6 +130,10 @@ void stage_for_decode(splitk_plan_t* out, int ncols_max, long long ctas, int num
   out->pdl_trigger = 1;
   out->smem_bytes = smem;
   out->ctas_per_sm = 2;
+  // Few activation rows: the idle epilogue threads load them (at most 4
+  // 16-byte loads each) sooner than a TMA queued behind weight loads
+  // (single-token decode 5.8 -> 5.5 us; 16 rows x 7 tiles is slower).
+  out->b_loader = ncols_max * kt * (kCtaK / 8) <= 4 * kEpiThreads ? 1 : 0;
 }
 
 int plan_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t smem_per_sm,
@@ -201,6 +205,7 @@ int plan_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t smem_
         out->a_tmem_tiles = 0;
         out->tmem_cols = tmem_cols_for(mma_n, 0, 1);
         out->mma_issuers = 1;
+        out->b_loader = 0;
         stage_for_decode(out, ncols_max, ctas, num_sms, smem_per_sm, smem_optin, scatter_bytes);
         return SPLITK_OK;
       }
@@ -241,6 +246,7 @@ int plan_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t smem_
       out->a_tmem_tiles = 0;
       out->tmem_cols = tmem_cols_for(mma_n, 0, 1);
       out->mma_issuers = 1;
+      out->b_loader = 0;
       stage_for_decode(out, ncols_max, ctas, num_sms, smem_per_sm, smem_optin,
                        prefer_dedicated ? mailbox_round_bytes(split, quads, ncols_max) : 0u);
       return SPLITK_OK;
@@ -286,6 +292,7 @@ int check_plan(const splitk_plan_t& pl, int M, int N, int K, int L, size_t smem_
   // K tiles i, i + issuers, ..., so stage s belongs to issuer s % issuers
   // exactly when the stage count is a multiple of the issuer count.
   if (pl.stages % pl.mma_issuers != 0) return SPLITK_ERR_BAD_PLAN;
+  if (pl.b_loader != 0 && (pl.b_loader != 1 || !pl.b_resident)) return SPLITK_ERR_BAD_PLAN;
   if (pl.tmem_cols != tmem_cols_for(pl.mma_n, pl.a_tmem_tiles, pl.mma_issuers)) return SPLITK_ERR_BAD_PLAN;
   uint32_t ded = 0;
   if (pl.reduce_scatter) {
@@ -489,8 +496,9 @@ int check_pointers(const void* a, const void* b, const void* c) {
 
 // The kernel's parameters for a checked plan.
 void fill_params(const splitk_plan_t& pl, int M, int N, int K, int L, uint32_t ded, const CUtensorMap* a_map,
-                 void* c, const void* bias, KernelParams* p) {
+                 const void* b, void* c, const void* bias, KernelParams* p) {
   p->a_map = a_map;
+  p->b = static_cast<const uint16_t*>(b);
   p->c = static_cast<uint16_t*>(c);
   p->bias = static_cast<const uint16_t*>(bias);
   p->M = M;
@@ -514,6 +522,7 @@ void fill_params(const splitk_plan_t& pl, int M, int N, int K, int L, uint32_t d
   p->tmem_cols = pl.tmem_cols;
   p->tmem_tile_col0 = tmem_tile_col0(pl.mma_n, pl.mma_issuers);
   p->mma_issuers = pl.mma_issuers;
+  p->b_loader = pl.b_loader;
   p->trace = g_trace.load(std::memory_order_relaxed);
   p->trace_ctas = p->trace ? g_trace_ctas.load(std::memory_order_relaxed) : 0u;
 }
@@ -543,7 +552,7 @@ int launch_locked(DeviceState& st, const void* a, const void* b, void* c, int M,
   if (rc != SPLITK_OK) return rc;
 
   KernelParams p;
-  fill_params(pl, M, N, K, L, ded, a_map, c, bias, &p);
+  fill_params(pl, M, N, K, L, ded, a_map, b, c, bias, &p);
   const LaunchArgs la = launch_args(pl, (flags & SPLITK_FLAG_NO_PDL) == 0);
   if (launch_kernel(la, b_map, p, stream) != cudaSuccess) {
     cudaGetLastError();
@@ -687,7 +696,7 @@ SPLITK_API int splitk_gemm_bf16_noalloc(const void* a, const void* b, void* c, i
     return SPLITK_ERR_CUDA;
   }
   KernelParams p;
-  fill_params(pl, M, N, K, L, ded, scratch_map, c, nullptr, &p);
+  fill_params(pl, M, N, K, L, ded, scratch_map, b, c, nullptr, &p);
   const LaunchArgs la = launch_args(pl, true);
   if (launch_kernel(la, b_map, p, s) != cudaSuccess) {
     cudaGetLastError();

@@ -69,6 +69,7 @@ struct KernelParams {
   const CUtensorMap* a_map;   // device address of A's tensor map
   uint16_t* c;                // C[L][M][N] bf16 bits
   const uint16_t* bias;       // [L][N] bf16 bits added before rounding, or null
+  const uint16_t* b;          // activations B[L][M][K] (read directly when b_loader = 1)
   int M, N, K, L;
   int split;                  // cluster size along K
   int stages;                 // ring depth
@@ -87,6 +88,7 @@ struct KernelParams {
   uint32_t tmem_cols;         // TMEM columns allocated per CTA
   uint32_t tmem_tile_col0;    // TMEM column of the first staged weight tile
   int mma_issuers;            // 1 or 2 threads issuing MMAs (2: even/odd K tiles)
+  int b_loader;               // 0: TMA (activation warp); 1: epilogue threads
   unsigned long long* trace;  // per-CTA %globaltimer stamps, or null
   unsigned trace_ctas;        // CTAs the trace buffer holds
 };

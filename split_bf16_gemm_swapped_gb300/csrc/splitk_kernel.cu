@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 3)
         dev::mbar_init(bar_full0 + 8u * s, b_res ? 1u : 2u);   // A (and B when it rides the ring)
         dev::mbar_init(bar_empty0 + 8u * s, 1);
       }
-      dev::mbar_init(bar_b, 1);
+      dev::mbar_init(bar_b, p.b_loader ? (uint32_t)kEpiThreads : 1u);
       dev::mbar_init(bar_mma_done, (uint32_t)p.mma_issuers);
       dev::mbar_init(bar_tmem_empty, kEpiThreads);
       dev::mbar_init(bar_reduce, 1);
@@ -298,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 3)
     if (lane == 0) {
       dev::griddep_wait();
       stamp(p, kTrActReady);
-      if (b_res) {
+      if (b_res && !p.b_loader) {
         // Every activation K tile of this CTA at once, on one barrier.
         dev::mbar_arrive_expect_tx(bar_b, (uint32_t)k_tiles * kBStage);
         for (int kt = 0; kt < k_tiles; ++kt) {
@@ -422,6 +422,34 @@ __global__ void __launch_bounds__(kThreads, 3)
       for (int e = 0; e < 8; ++e) {
         if (nb + e < p.N) bias8[e] = __uint_as_float((uint32_t)__ldg(bp + e) << 16);
       }
+    }
+
+    if (p.b_loader) {
+      // The activations of all of the CTA's K tiles, loaded by the epilogue
+      // threads (idle until the accumulator is complete) with 16-byte loads
+      // through L2 and stored in the 128-byte-swizzled layout the MMA reads:
+      // 16-byte chunk c of row r of an 8-row atom lands at chunk c ^ (r % 8).
+      // Columns past K are zero (the weights there are zero-filled, and
+      // 0 * garbage could be NaN); rows past M are left unwritten -- they
+      // only feed accumulator columns that are never read.
+      dev::griddep_wait();
+      const int cpr = k_tiles * (kCtaK / 8);           // 16-byte chunks per row
+      for (int i = et; i < ncols * cpr; i += kEpiThreads) {
+        const int r = i / cpr;
+        const int ci = i - r * cpr;
+        const int kt = ci >> 4, half = (ci >> 3) & 1, c = ci & 7;
+        const int k = (kt0 + kt) * kCtaK + half * kAtomK + c * 8;
+        uint32_t x0 = 0, x1 = 0, x2 = 0, x3 = 0;
+        if (k < p.K) {
+          dev::ld_global_cg_v4(p.b + ((size_t)l * p.M + (size_t)(m0 + r)) * (size_t)p.K + (size_t)k, x0, x1, x2, x3);
+        }
+        dev::st_shared_v4(sB + (uint32_t)kt * kBStage + (uint32_t)half * kBBox + (uint32_t)(r >> 3) * 1024u +
+                              (uint32_t)(r & 7) * 128u + (uint32_t)((c ^ (r & 7)) * 16),
+                          x0, x1, x2, x3);
+      }
+      dev::fence_proxy_async_shared();   // generic-proxy stores, read by tcgen05.mma
+      dev::mbar_arrive(bar_b);
+      if (et == 0) stamp(p, kTrActReady);
     }
 
     waiter.wait<false>(bar_mma_done, 0u, kRoleEpiMma, 0);

@@ -126,6 +126,7 @@ def _ring(base, M=None):
     no tensor-memory staging, one MMA issuer."""
     p = sk.Plan.from_buffer_copy(base)
     p.b_resident = 0
+    p.b_loader = 0
     p.a_tmem_tiles = 0
     p.mma_issuers = 1
     p.tmem_cols = max(32, p.mma_n)
@@ -269,7 +270,7 @@ def _tmem_cols(mma_n, tiles, issuers=1):
     return next(c for c in (32, 64, 128, 256, 512) if c >= need)
 
 
-def _staged(base, stages, tmem_tiles, issuers=1, b_resident=1, M=None):
+def _staged(base, stages, tmem_tiles, issuers=1, b_resident=1, M=None, b_loader=0):
     """`base` with every activation K tile in its own buffer, the first
     `tmem_tiles` weight K tiles staged in tensor memory and `issuers` MMA
     threads; None if the plan cannot hold (shared memory, or tensor memory of
@@ -284,6 +285,7 @@ def _staged(base, stages, tmem_tiles, issuers=1, b_resident=1, M=None):
             return None
     p.stages = stages
     p.b_resident = b_resident
+    p.b_loader = b_loader
     p.a_tmem_tiles = tmem_tiles
     p.mma_issuers = issuers
     p.tmem_cols = _tmem_cols(p.mma_n, tmem_tiles, issuers)
@@ -307,12 +309,13 @@ def test_staged_weights_and_resident_activations_give_the_same_bits(M, split):
     ran = 0
     for stages in (2, 3):
         for tiles in (0, 1, 2, 3):
-            p = _staged(base, stages, tiles, M=M)
-            if p is None:
-                continue
-            c1 = gemm_gpu(a, b, plan=p)
-            assert np.array_equal(c0, c1), (stages, tiles)
-            ran += 1
+            for loader in (0, 1):
+                p = _staged(base, stages, tiles, M=M, b_loader=loader)
+                if p is None:
+                    continue
+                c1 = gemm_gpu(a, b, plan=p)
+                assert np.array_equal(c0, c1), (stages, tiles, loader)
+                ran += 1
     assert ran >= 1
 
 
@@ -331,7 +334,7 @@ def test_two_mma_issuers(M, split):
     ran = 0
     for stages in (2, 3):
         for tiles in (0, 1, 2, 3):
-            p = _staged(base, stages, tiles, issuers=2, M=M)
+            p = _staged(base, stages, tiles, issuers=2, M=M, b_loader=tiles % 2)
             if p is None:
                 continue
             assert np.array_equal(gemm_gpu(a, b, plan=p), c2), (stages, tiles)
@@ -355,3 +358,18 @@ def test_two_issuers_need_an_even_ring():
     with pytest.raises(sk.SplitKError) as e:
         sk.splitk_gemm_bf16_planned(to_dev(a), to_dev(b), None, p)
     assert e.value.name == "SPLITK_ERR_BAD_PLAN"
+
+
+@pytest.mark.parametrize("M,K", [(1, 1000), (3, 2056), (8, 1032), (16, 520)])
+def test_thread_loaded_activations_with_ragged_K_and_bias(M, K):
+    """Activations loaded by the epilogue threads (zeros past K, rows past M
+    left unwritten) give the bits of the TMA-loaded plan, with a bias too."""
+    L, N, split = 2, 200, 4
+    a, b = _draw(L, M, N, K, seed=1400 + M)
+    base = sk.splitk_plan(M, N, K, L, split)
+    p0 = _staged(base, 2, 0, issuers=2, M=M, b_loader=0)
+    p1 = _staged(base, 2, 0, issuers=2, M=M, b_loader=1)
+    assert p0 is not None and p1 is not None
+    c0 = gemm_gpu(a, b, plan=p0)
+    assert np.array_equal(gemm_gpu(a, b, plan=p1), c0)
+    assert_parity(c0, oracle_full(a, b), a, b, K)
