@@ -139,6 +139,10 @@ typedef struct splitk_plan_t {
                               activation tiles by TMA; 1 the 128 epilogue
                               threads load them with 16-byte loads and store
                               them swizzled (for few rows: no TMA queue)       */
+    int l2_prefetch;       /* 1: at CTA start, prefetch into L2 the weight K
+                              tiles that neither the ring nor tensor memory
+                              holds before the programmatic-dependent-launch
+                              wait returns                                     */
 } splitk_plan_t;
 
 /*

@@ -62,6 +62,7 @@ class Plan(ctypes.Structure):
         ("reduce_scatter", ctypes.c_int), ("b_resident", ctypes.c_int),
         ("a_tmem_tiles", ctypes.c_int), ("tmem_cols", ctypes.c_uint),
         ("mma_issuers", ctypes.c_int), ("b_loader", ctypes.c_int),
+        ("l2_prefetch", ctypes.c_int),
     ]
 
     def as_dict(self) -> dict:

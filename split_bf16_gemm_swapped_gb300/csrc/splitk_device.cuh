@@ -144,6 +144,13 @@ __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const void* map, 
       : "memory");
 }
 
+// L2 prefetch of one box of a 3-D tensor (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_3d(const void* map, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(map), "r"(c0),
+               "r"(c1), "r"(c2)
+               : "memory");
+}
+
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* map, int c0, int c1, int c2,
                                             uint32_t bar) {
   asm volatile(

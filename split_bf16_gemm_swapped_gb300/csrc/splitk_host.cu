@@ -102,8 +102,9 @@ int auto_split(int T, long long tiles, int num_sms, int mma_n) {
 // resident at 2 CTAs per SM with few K tiles per CTA: the activations of all
 // of a CTA's K tiles in their own buffer, loaded at once after the
 // programmatic-dependent-launch wait; a 2-stage weight ring whose first
-// min(3, k_tiles - 2) tiles are copied into tensor memory as they land, so
-// that up to 5 weight K tiles are on chip before the wait returns; two MMA
+// min(3, k_tiles - 2) tiles (both of 2) are copied into tensor memory as they
+// land, so that up to 5 weight K tiles are on chip before the wait returns,
+// the rest prefetched into L2; two MMA
 // issuers (a thread issues one tcgen05.mma about every 46 cycles at these
 // widths); and the early trigger.  Measured on GB300 (back to back, weights
 // rotated past L2): single-token decode 7.1 -> 5.8 us, small-batch decode
@@ -117,7 +118,9 @@ void stage_for_decode(splitk_plan_t* out, int ncols_max, long long ctas, int num
       mailbox_round_bytes(out->split_k, out->mailbox_quads, ncols_max) > 2u * kAStageBytes) {
     return;
   }
-  const int tiles = std::min(kMaxTmemTiles, std::max(0, kt - 2));
+  // All of them when the ring holds them anyway (2 tiles: measured faster),
+  // else as many as leave the 2 ring stages to the tiles after them.
+  const int tiles = kt <= 2 ? kt : std::min(kMaxTmemTiles, kt - 2);
   const uint32_t cols = tmem_cols_for(out->mma_n, tiles, 2);
   const size_t smem = smem_bytes_for(out->mma_n, 2, ded, b_region_tiles_for(2, 1, kt));
   const size_t budget = std::min(smem_optin, smem_per_sm / 2 - 1024);
@@ -134,6 +137,9 @@ void stage_for_decode(splitk_plan_t* out, int ncols_max, long long ctas, int num
   // 16-byte loads each) sooner than a TMA queued behind weight loads
   // (single-token decode 5.8 -> 5.5 us; 16 rows x 7 tiles is slower).
   out->b_loader = ncols_max * kt * (kCtaK / 8) <= 4 * kEpiThreads ? 1 : 0;
+  // Tiles that stay off chip until the wait go to L2 at CTA start
+  // (small-batch decode: 11.6 -> 11.1 us).
+  out->l2_prefetch = kt > 2 + tiles ? 1 : 0;
 }
 
 int plan_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t smem_per_sm,
@@ -206,6 +212,7 @@ int plan_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t smem_
         out->tmem_cols = tmem_cols_for(mma_n, 0, 1);
         out->mma_issuers = 1;
         out->b_loader = 0;
+        out->l2_prefetch = 0;
         stage_for_decode(out, ncols_max, ctas, num_sms, smem_per_sm, smem_optin, scatter_bytes);
         return SPLITK_OK;
       }
@@ -247,6 +254,7 @@ int plan_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t smem_
       out->tmem_cols = tmem_cols_for(mma_n, 0, 1);
       out->mma_issuers = 1;
       out->b_loader = 0;
+      out->l2_prefetch = 0;
       stage_for_decode(out, ncols_max, ctas, num_sms, smem_per_sm, smem_optin,
                        prefer_dedicated ? mailbox_round_bytes(split, quads, ncols_max) : 0u);
       return SPLITK_OK;
@@ -293,6 +301,7 @@ int check_plan(const splitk_plan_t& pl, int M, int N, int K, int L, size_t smem_
   // exactly when the stage count is a multiple of the issuer count.
   if (pl.stages % pl.mma_issuers != 0) return SPLITK_ERR_BAD_PLAN;
   if (pl.b_loader != 0 && (pl.b_loader != 1 || !pl.b_resident)) return SPLITK_ERR_BAD_PLAN;
+  if (pl.l2_prefetch != 0 && pl.l2_prefetch != 1) return SPLITK_ERR_BAD_PLAN;
   if (pl.tmem_cols != tmem_cols_for(pl.mma_n, pl.a_tmem_tiles, pl.mma_issuers)) return SPLITK_ERR_BAD_PLAN;
   uint32_t ded = 0;
   if (pl.reduce_scatter) {
@@ -523,6 +532,7 @@ void fill_params(const splitk_plan_t& pl, int M, int N, int K, int L, uint32_t d
   p->tmem_tile_col0 = tmem_tile_col0(pl.mma_n, pl.mma_issuers);
   p->mma_issuers = pl.mma_issuers;
   p->b_loader = pl.b_loader;
+  p->l2_prefetch = pl.l2_prefetch;
   p->trace = g_trace.load(std::memory_order_relaxed);
   p->trace_ctas = p->trace ? g_trace_ctas.load(std::memory_order_relaxed) : 0u;
 }

@@ -258,6 +258,16 @@ __global__ void __launch_bounds__(kThreads, 3)
       dev::tma_load_3d_hint(dst, p.a_map, k, n0, l, full, a_policy);
       dev::tma_load_3d_hint(dst + kABoxBytes, p.a_map, k + kAtomK, n0, l, full, a_policy);
     }
+    if (p.l2_prefetch) {
+      // The weight tiles that cannot be on chip before the PDL wait returns
+      // (past the ring and the tensor-memory tiles) go to L2 now, so their
+      // loads after the wait hit L2 instead of waiting for HBM.
+      for (int kt = stages + tmem_tiles; kt < k_tiles; ++kt) {
+        const int k = (kt0 + kt) * kCtaK;
+        dev::tma_prefetch_3d(p.a_map, k, n0, l);
+        dev::tma_prefetch_3d(p.a_map, k + kAtomK, n0, l);
+      }
+    }
     stamp(p, kTrPrefetched);
   }
   // Peers' barriers (and this CTA's TMEM address) exist past this point.

@@ -72,11 +72,13 @@ def test_decode_tactics():
     assert (p.ctas_per_sm, p.stages, p.reduce_scatter, p.mailbox_dedicated) == (2, 2, 0, 1)
     assert (p.b_resident, p.a_tmem_tiles, p.mma_issuers, p.pdl_trigger, p.tmem_cols) == (1, 2, 2, 1, 256)
     assert p.b_loader == 1                         # 1 row x 4 K tiles: 64 loads of 16 bytes
+    assert p.l2_prefetch == 0                      # all 4 weight tiles on chip
     assert p.smem_bytes == 1024 + 2 * 32768 + 4 * 16 * 256 + 3 * 512 + 256
     p = _plan(16, 4096, 7168, 1, 8)
     assert (p.ctas_per_sm, p.stages, p.reduce_scatter, p.mailbox_dedicated) == (2, 2, 1, 1)
     assert (p.b_resident, p.a_tmem_tiles, p.mma_issuers, p.pdl_trigger, p.tmem_cols) == (1, 3, 2, 1, 256)
     assert p.b_loader == 0                         # 16 rows x 7 K tiles: TMA
+    assert p.l2_prefetch == 1                      # 2 of 7 weight tiles off chip before the wait
     assert p.smem_bytes == 1024 + 2 * 32768 + 7 * 16 * 256 + 16 * 512 + 256
     for p in (_plan(1, 7168, 2048, 1, 4), _plan(16, 4096, 7168, 1, 8)):
         assert 2 * (p.smem_bytes + 1024) <= GB300["smem_per_sm"]
@@ -88,7 +90,8 @@ def test_long_k_and_wide_shapes_keep_the_ring():
     (long K) or tiles are wide, the plan keeps the page's ring design."""
     for args in [(1, 7168, 16384, 2, 4), (32, 7168, 16384, 2, 2), (64, 18432, 7168, 1, 2)]:
         p = _plan(*args)
-        assert (p.b_resident, p.a_tmem_tiles, p.mma_issuers, p.pdl_trigger, p.b_loader) == (0, 0, 1, 0, 0), args
+        assert (p.b_resident, p.a_tmem_tiles, p.mma_issuers, p.pdl_trigger, p.b_loader, p.l2_prefetch) == \
+            (0, 0, 1, 0, 0, 0), args
 
 
 def test_auto_split_fills_the_sms_with_the_smallest_split():

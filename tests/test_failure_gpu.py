@@ -41,8 +41,13 @@ def test_skipped_publish_times_out_and_the_context_survives(dedicated):
     assert sk.splitk_get_status() == 0
     plan = sk.splitk_plan(4, 256, 1024, 1, 4)
     if not dedicated and plan.mailbox_dedicated:
+        # the mailbox moves onto the drained weight ring; with the smaller
+        # shared memory 3 CTAs fit an SM, so no weight tiles stay in tensor
+        # memory (3 x 256 columns would not fit its 512)
         plan.mailbox_dedicated = 0
         plan.smem_bytes -= 3 * 4 * 512
+        plan.a_tmem_tiles = 0
+        plan.tmem_cols = max(32, plan.mma_n) * plan.mma_issuers
     try:
         sk.splitk_set_wait_limit_ns(50_000_000)          # 50 ms
         sk.splitk_debug_inject(sk.INJECT_SKIP_PUBLISH)

@@ -127,6 +127,7 @@ def _ring(base, M=None):
     p = sk.Plan.from_buffer_copy(base)
     p.b_resident = 0
     p.b_loader = 0
+    p.l2_prefetch = 0
     p.a_tmem_tiles = 0
     p.mma_issuers = 1
     p.tmem_cols = max(32, p.mma_n)
@@ -337,6 +338,7 @@ def test_two_mma_issuers(M, split):
             p = _staged(base, stages, tiles, issuers=2, M=M, b_loader=tiles % 2)
             if p is None:
                 continue
+            p.l2_prefetch = 1
             assert np.array_equal(gemm_gpu(a, b, plan=p), c2), (stages, tiles)
             ran += 1
     assert ran >= 1
