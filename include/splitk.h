@@ -176,6 +176,51 @@ SPLITK_API int splitk_gemm_bf16(const void *a, const void *b, void *c,
                                 splitk_stream_t stream);
 
 /*
+ * Checks a plan against a shape on a described device without touching CUDA
+ * (the check every launch makes): SPLITK_OK, or SPLITK_ERR_BAD_PLAN /
+ * INVALID_SHAPE / UNSUPPORTED_SPLIT / NO_FIT.  Useful before handing a
+ * hand-made plan to splitk_gemm_bf16_planned().
+ */
+SPLITK_API int splitk_plan_check_for(const splitk_plan_t *plan, int M, int N,
+                                     int K, int L, size_t smem_per_sm,
+                                     size_t smem_per_block_optin);
+
+/*
+ * Every valid tactic for a shape on a described device, without CUDA:
+ * splitk_plan_for()'s choice first, then the page's ring (2-4 stages, one or
+ * two MMA issuers, either PDL trigger) and the staged family (resident
+ * activations, 0-3 weight tiles in tensor memory, TMA or epilogue-thread
+ * activation loads, L2 prefetch), for each split (all valid ones when
+ * split_k = 0) and each reduction (rank 0 with its own or an aliased
+ * mailbox, scattered).  Writes up to max_out plans to out and returns how
+ * many exist (call with max_out = 0 to size the array), or a negative
+ * status.
+ */
+SPLITK_API int splitk_plan_candidates_for(int M, int N, int K, int L,
+                                          int split_k, int num_sms,
+                                          size_t smem_per_sm,
+                                          size_t smem_per_block_optin,
+                                          splitk_plan_t *out, int max_out);
+
+/*
+ * Measures every candidate of splitk_plan_candidates_for() on the current
+ * device and returns the fastest in *best (and its time per call in
+ * *best_us_per_call, if not null).  Each candidate runs `reps` back-to-back
+ * launches on `stream` (programmatic dependent launch on), cycling through
+ * the n_a weight tensors a_list[0..n_a-1] of identical shape -- a model's
+ * same-shape layers, or copies whose total exceeds the L2 cache, so that the
+ * weights stream from HBM as in decoding -- with the same activations b and
+ * output c.  Synchronises the stream.  Every launch is checked like
+ * splitk_gemm_bf16_planned(); waits that time out are recorded as usual
+ * (splitk_get_status()).  A setup-time call: it holds the library's lock
+ * for the whole measurement.
+ */
+SPLITK_API int splitk_tune(const void *const *a_list, int n_a, const void *b,
+                           void *c, int M, int N, int K, int L, int split_k,
+                           int reps, splitk_stream_t stream, splitk_plan_t *best,
+                           float *best_us_per_call);
+
+/*
  * C = B * A^T + bias with the bias added per output feature n in FP32 before
  * the one rounding to bf16: C[l][m][n] = bf16_rne(sum_k A B + bias[l][n]).
  * This is the bias argument of the page's SplitKGemm launcher (left unused

@@ -23,6 +23,7 @@ __all__ = [
     "SplitKError", "Plan", "Fault", "library_path", "load_library",
     "splitk_plan", "splitk_plan_for", "splitk_gemm_bf16", "splitk_gemm_bf16_planned",
     "splitk_gemm_bf16_hostio", "splitk_gemm_bf16_noalloc", "splitk_gemm_bf16_bias",
+    "splitk_plan_check_for", "splitk_plan_candidates_for", "splitk_tune",
     "splitk_get_fault",
     "splitk_get_status",
     "splitk_set_wait_limit_ns", "splitk_debug_inject", "splitk_release",
@@ -111,6 +112,13 @@ def load_library():
     lib.splitk_plan_for.restype = i
     lib.splitk_gemm_bf16.argtypes = [vp, vp, vp, i, i, i, i, i, vp]
     lib.splitk_gemm_bf16.restype = i
+    lib.splitk_plan_check_for.argtypes = [ctypes.POINTER(Plan), i, i, i, i, sz, sz]
+    lib.splitk_plan_check_for.restype = i
+    lib.splitk_plan_candidates_for.argtypes = [i, i, i, i, i, i, sz, sz, ctypes.POINTER(Plan), i]
+    lib.splitk_plan_candidates_for.restype = i
+    lib.splitk_tune.argtypes = [ctypes.POINTER(vp), i, vp, vp, i, i, i, i, i, i, vp, ctypes.POINTER(Plan),
+                                ctypes.POINTER(ctypes.c_float)]
+    lib.splitk_tune.restype = i
     lib.splitk_gemm_bf16_bias.argtypes = [vp, vp, vp, vp, i, i, i, i, i, vp]
     lib.splitk_gemm_bf16_bias.restype = i
     lib.splitk_gemm_bf16_planned.argtypes = [vp, vp, vp, i, i, i, i, ctypes.POINTER(Plan), u, vp]
@@ -213,6 +221,50 @@ def splitk_gemm_bf16(a, b, c=None, split_k: int = 0, stream=None):
             _stream_handle(stream, a.device))
     _check(rc, "splitk_gemm_bf16")
     return c
+
+
+def splitk_plan_check_for(plan: Plan, M: int, N: int, K: int, L: int, smem_per_sm: int,
+                          smem_per_block_optin: int) -> int:
+    """The launch-time plan check for a described device; returns the status."""
+    return load_library().splitk_plan_check_for(ctypes.byref(plan), M, N, K, L, smem_per_sm,
+                                                smem_per_block_optin)
+
+
+def splitk_plan_candidates_for(M: int, N: int, K: int, L: int, split_k: int, num_sms: int,
+                               smem_per_sm: int, smem_per_block_optin: int) -> list:
+    """Every valid tactic for the shape on a described device (the plan's
+    own choice first)."""
+    lib = load_library()
+    n = lib.splitk_plan_candidates_for(M, N, K, L, split_k, num_sms, smem_per_sm,
+                                       smem_per_block_optin, None, 0)
+    _check(n if n < 0 else 0, "splitk_plan_candidates_for")
+    arr = (Plan * max(n, 1))()
+    got = lib.splitk_plan_candidates_for(M, N, K, L, split_k, num_sms, smem_per_sm,
+                                         smem_per_block_optin, arr, n)
+    _check(got if got < 0 else 0, "splitk_plan_candidates_for")
+    return [Plan.from_buffer_copy(arr[k]) for k in range(n)]
+
+
+def splitk_tune(a_list, b, c=None, split_k: int = 0, reps: int = 64, stream=None):
+    """The fastest candidate tactic measured on this device, cycling through
+    the same-shape weight tensors `a_list`; returns (plan, us_per_call)."""
+    import torch
+    M, N, K, L = _dims(a_list[0], b)
+    for a in a_list:
+        _require_cuda(a)
+        if tuple(a.shape) != tuple(a_list[0].shape):
+            raise ValueError("the weight tensors must have one shape")
+    _require_cuda(b)
+    c = _out(c, a_list[0], M, N, L)
+    ptrs = (ctypes.c_void_p * len(a_list))(*[a.data_ptr() for a in a_list])
+    plan = Plan()
+    us = ctypes.c_float(0.0)
+    with torch.cuda.device(b.device):
+        rc = load_library().splitk_tune(ptrs, len(a_list), b.data_ptr(), c.data_ptr(), M, N, K, L,
+                                        int(split_k), int(reps), _stream_handle(stream, b.device),
+                                        ctypes.byref(plan), ctypes.byref(us))
+    _check(rc, "splitk_tune")
+    return plan, float(us.value)
 
 
 def splitk_gemm_bf16_bias(a, b, bias, c=None, split_k: int = 0, stream=None):

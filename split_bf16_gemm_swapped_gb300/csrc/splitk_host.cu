@@ -20,6 +20,7 @@
 #include <cstring>
 #include <mutex>
 #include <unordered_map>
+#include <vector>
 
 #include "splitk.h"
 #include "splitk_internal.h"
@@ -585,6 +586,106 @@ int gemm_auto(const void* a, const void* b, void* c, int M, int N, int K, int L,
   return launch_locked(*st, a, b, c, M, N, K, L, pl, flags, stream, bias);
 }
 
+// Every valid tactic for a shape on a described device: the plan's own
+// choice first, then the page's ring (2-4 stages, one or two MMA issuers,
+// either PDL trigger) and the staged family (2 stages, 0-3 weight tiles in
+// tensor memory, resident activations loaded by TMA or by the epilogue
+// threads, L2 prefetch of the tiles left off chip), for each split and each
+// reduction (rank 0 with its own or an aliased mailbox, scattered).  Each
+// candidate passes check_plan.
+int enumerate_plans(int M, int N, int K, int L, int split_k, int num_sms, size_t smem_per_sm,
+                    size_t smem_optin, std::vector<splitk_plan_t>* out) {
+  splitk_plan_t base;
+  std::memset(&base, 0, sizeof(base));
+  int rc = plan_impl(M, N, K, L, split_k, num_sms, smem_per_sm, smem_optin, &base);
+  if (rc != SPLITK_OK) return rc;
+  out->push_back(base);
+  const int T = total_k_tiles(K);
+  const int mma_n = base.mma_n;
+  const long long m_tiles = (M + mma_n - 1) / mma_n;
+  const long long n_tiles = ((long long)N + kMmaM - 1) / kMmaM;
+  const int ncols_max = std::min(M, mma_n);
+  const int nquads_max = (ncols_max + 3) / 4;
+  auto same = [](const splitk_plan_t& x, const splitk_plan_t& y) { return std::memcmp(&x, &y, sizeof(x)) == 0; };
+  for (int split : {1, 2, 4, 8}) {
+    if ((split_k != 0 && split != split_k) || split > T) continue;
+    const int kt = (T + split - 1) / split;
+    for (int mode = 0; mode < 3; ++mode) {               // 0 own mailbox, 1 aliased, 2 scattered
+      if (split == 1 && mode != 0) continue;
+      if (mode == 2 && ncols_max < 4) continue;
+      for (int b_res = 0; b_res <= 1; ++b_res) {
+        for (int stages = 2; stages <= (b_res ? 2 : 4); ++stages) {
+          if (stages > std::max(2, kt)) continue;
+          for (int tiles = 0; tiles <= (b_res ? std::min(kMaxTmemTiles, kt) : 0); ++tiles) {
+            for (int issuers = 1; issuers <= 2; ++issuers) {
+              if (stages % issuers) continue;
+              for (int trig = 0; trig <= 1; ++trig) {
+                for (int loader = 0; loader <= b_res; ++loader) {
+                  for (int pf = 0; pf <= (b_res && kt > stages + tiles ? 1 : 0); ++pf) {
+                    splitk_plan_t p;
+                    std::memset(&p, 0, sizeof(p));
+                    p.mma_m = kMmaM;
+                    p.mma_n = mma_n;
+                    p.stages = stages;
+                    p.split_k = split;
+                    p.k_tiles_per_cta = kt;
+                    p.grid[0] = (unsigned)(split * m_tiles);
+                    p.grid[1] = (unsigned)n_tiles;
+                    p.grid[2] = (unsigned)L;
+                    p.cluster[0] = (unsigned)split;
+                    p.cluster[1] = 1;
+                    p.cluster[2] = 1;
+                    p.pdl_trigger = trig;
+                    p.reduce_scatter = mode == 2 ? 1 : 0;
+                    p.b_resident = b_res;
+                    p.a_tmem_tiles = tiles;
+                    p.mma_issuers = issuers;
+                    p.tmem_cols = tmem_cols_for(mma_n, tiles, issuers);
+                    p.b_loader = loader;
+                    p.l2_prefetch = pf;
+                    uint32_t ded = 0;
+                    int quads = nquads_max;
+                    if (split == 1) {
+                      p.mailbox_dedicated = 0;
+                    } else if (mode == 0) {
+                      p.mailbox_dedicated = 1;
+                      ded = mailbox_round_bytes(split, quads, ncols_max);
+                    } else if (mode == 1) {
+                      p.mailbox_dedicated = 0;
+                      if (mailbox_round_bytes(split, quads, ncols_max) > (uint32_t)stages * kAStageBytes) {
+                        quads = 4;
+                        while (quads + 4 <= nquads_max &&
+                               mailbox_round_bytes(split, quads + 4, ncols_max) <= (uint32_t)stages * kAStageBytes) {
+                          quads += 4;
+                        }
+                      }
+                    } else {
+                      p.mailbox_dedicated = 1;
+                      ded = (uint32_t)ncols_max * kColumnBytes;
+                    }
+                    p.mailbox_quads = quads;
+                    p.reduce_rounds = split > 1 ? (nquads_max + quads - 1) / quads : 0;
+                    p.smem_bytes = smem_bytes_for(mma_n, stages, ded, b_region_tiles_for(stages, b_res, kt));
+                    p.ctas_per_sm = std::min(3, resident_by_smem(smem_per_sm, p.smem_bytes));
+                    uint32_t ded_check = 0;
+                    if (p.ctas_per_sm < 1 || check_plan(p, M, N, K, L, smem_optin, smem_per_sm, &ded_check) != SPLITK_OK) {
+                      continue;
+                    }
+                    bool dup = false;
+                    for (const auto& q : *out) dup = dup || same(p, q);
+                    if (!dup) out->push_back(p);
+                  }
+                }
+              }
+            }
+          }
+        }
+      }
+    }
+  }
+  return SPLITK_OK;
+}
+
 }  // namespace
 }  // namespace splitk
 
@@ -712,6 +813,78 @@ SPLITK_API int splitk_gemm_bf16_noalloc(const void* a, const void* b, void* c, i
     cudaGetLastError();
     return SPLITK_ERR_CUDA;
   }
+  return SPLITK_OK;
+}
+
+SPLITK_API int splitk_plan_check_for(const splitk_plan_t* plan, int M, int N, int K, int L,
+                                     size_t smem_per_sm, size_t smem_per_block_optin) {
+  if (!plan) return SPLITK_ERR_NULL;
+  if (M < 1 || N < 1 || K < 1 || L < 1) return SPLITK_ERR_INVALID_SHAPE;
+  uint32_t ded = 0;
+  return check_plan(*plan, M, N, K, L, smem_per_block_optin, smem_per_sm, &ded);
+}
+
+SPLITK_API int splitk_plan_candidates_for(int M, int N, int K, int L, int split_k, int num_sms,
+                                          size_t smem_per_sm, size_t smem_per_block_optin,
+                                          splitk_plan_t* out, int max_out) {
+  if (max_out > 0 && !out) return SPLITK_ERR_NULL;
+  std::vector<splitk_plan_t> all;
+  const int rc = enumerate_plans(M, N, K, L, split_k, num_sms, smem_per_sm, smem_per_block_optin, &all);
+  if (rc != SPLITK_OK) return rc;
+  for (int i = 0; i < (int)all.size() && i < max_out; ++i) out[i] = all[(size_t)i];
+  return (int)all.size();
+}
+
+SPLITK_API int splitk_tune(const void* const* a_list, int n_a, const void* b, void* c, int M, int N, int K,
+                           int L, int split_k, int reps, splitk_stream_t stream, splitk_plan_t* best,
+                           float* best_us_per_call) {
+  if (!a_list || n_a < 1 || !best) return SPLITK_ERR_NULL;
+  for (int i = 0; i < n_a; ++i) {
+    const int rc = check_pointers(a_list[i], b, c);
+    if (rc != SPLITK_OK) return rc;
+  }
+  if (M < 1 || N < 1 || K < 1 || L < 1) return SPLITK_ERR_INVALID_SHAPE;
+  if (reps < 1) reps = 64;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* st = nullptr;
+  int rc = current_device(&st, nullptr);
+  if (rc != SPLITK_OK) return rc;
+  std::vector<splitk_plan_t> cands;
+  rc = enumerate_plans(M, N, K, L, split_k, st->num_sms, st->smem_per_sm, st->smem_optin, &cands);
+  if (rc != SPLITK_OK) return rc;
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) {
+    if (e0) cudaEventDestroy(e0);
+    cudaGetLastError();
+    return SPLITK_ERR_CUDA;
+  }
+  float best_ms = -1.0f;
+  for (const splitk_plan_t& p : cands) {
+    // one pass over the weights to warm the tensor maps and the code
+    for (int i = 0; i < n_a && rc == SPLITK_OK; ++i) rc = launch_locked(*st, a_list[i], b, c, M, N, K, L, p, 0u, s);
+    if (rc == SPLITK_OK && cudaEventRecord(e0, s) != cudaSuccess) rc = SPLITK_ERR_CUDA;
+    for (int r = 0; r < reps && rc == SPLITK_OK; ++r) {
+      rc = launch_locked(*st, a_list[r % n_a], b, c, M, N, K, L, p, 0u, s);
+    }
+    float ms = 0.0f;
+    if (rc == SPLITK_OK && (cudaEventRecord(e1, s) != cudaSuccess || cudaEventSynchronize(e1) != cudaSuccess ||
+                            cudaEventElapsedTime(&ms, e0, e1) != cudaSuccess)) {
+      rc = SPLITK_ERR_CUDA;
+    }
+    if (rc != SPLITK_OK) break;
+    if (best_ms < 0.0f || ms < best_ms) {
+      best_ms = ms;
+      *best = p;
+    }
+  }
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  if (rc != SPLITK_OK) {
+    cudaGetLastError();
+    return rc;
+  }
+  if (best_us_per_call) *best_us_per_call = best_ms * 1000.0f / (float)reps;
   return SPLITK_OK;
 }
 

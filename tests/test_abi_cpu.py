@@ -179,3 +179,47 @@ def test_calls_needing_a_device_report_it_without_one():
 def test_settings_calls():
     assert sk.load_library().splitk_set_wait_limit_ns(0) == 0
     assert sk.load_library().splitk_debug_inject(0) == 0
+
+
+def _check(p, M, N, K, L):
+    return sk.splitk_plan_check_for(p, M, N, K, L, GB300["smem_per_sm"], GB300["smem_per_block_optin"])
+
+
+@pytest.mark.parametrize("args", [(1, 7168, 2048, 1, 4), (16, 4096, 7168, 1, 8), (4, 256, 1024, 1, 0),
+                                  (64, 18432, 7168, 1, 2), (128, 7168, 16384, 2, 0), (3, 200, 1000, 2, 0)])
+def test_candidates_are_valid_distinct_and_start_with_the_plan(args):
+    M, N, K, L, split = args
+    cands = sk.splitk_plan_candidates_for(M, N, K, L, split, **GB300)
+    assert len(cands) >= 2
+    assert cands[0].as_dict() == _plan(*args).as_dict()
+    seen = set()
+    for p in cands:
+        assert _check(p, M, N, K, L) == 0, p
+        assert split == 0 or p.split_k == split
+        assert p.stages % p.mma_issuers == 0
+        assert GB300["smem_per_sm"] // (p.smem_bytes + 1024) * p.tmem_cols <= 512
+        key = bytes(p)
+        assert key not in seen
+        seen.add(key)
+    # the page's ring always; the staged family where all activation tiles fit
+    assert any(not p.b_resident for p in cands)
+    if M <= 16 and K <= 8192:
+        assert any(p.b_resident and p.a_tmem_tiles for p in cands)
+    if split != 1 and min(M, cands[0].mma_n) >= 4:
+        assert any(p.reduce_scatter for p in cands)
+
+
+def test_plan_check_rejects_what_a_launch_would():
+    M, N, K, L = 1, 7168, 2048, 1
+    p = _plan(M, N, K, L, 4)
+    assert _check(p, M, N, K, L) == 0
+    bad = sk.Plan.from_buffer_copy(p)
+    bad.stages = 3                                      # odd ring with two issuers
+    assert _check(bad, M, N, K, L) == -10
+    bad = sk.Plan.from_buffer_copy(p)
+    bad.tmem_cols = 128                                 # not what the layout needs
+    assert _check(bad, M, N, K, L) == -10
+    bad = sk.Plan.from_buffer_copy(p)
+    bad.b_resident = 0                                  # staged tiles need resident activations
+    assert _check(bad, M, N, K, L) == -10
+    assert _check(p, M, N, K + 8, L) == -10             # another shape

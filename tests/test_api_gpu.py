@@ -139,3 +139,25 @@ def test_pdl_chain_matches_serialised_launches():
     assert torch.equal(c1.view(torch.int16), d1.view(torch.int16))
     assert torch.equal(c2.view(torch.int16), d2.view(torch.int16))
     assert_parity(to_host(c1), oracle.gemm(a1, b0), a1, b0, K1)
+
+
+def test_tune_measures_candidates_and_returns_a_plan_that_computes_the_product():
+    """splitk_tune times every candidate on this device over a few weight
+    copies and returns the fastest; that plan passes the launch check and
+    computes the product."""
+    M, N, K, L = 2, 1024, 2048, 1
+    a = synthetic.normal_bf16((L, N, K), 31, synthetic.STREAM_A, 0.02)
+    b = synthetic.normal_bf16((L, M, K), 31, synthetic.STREAM_B, 1.0)
+    ta = to_dev(a)
+    a_list = [ta] + [ta.clone() for _ in range(3)]
+    tb = to_dev(b)
+    plan, us = sk.splitk_tune(a_list, tb, split_k=4, reps=8)
+    torch.cuda.synchronize()
+    assert sk.splitk_get_status() == 0
+    assert us > 0 and plan.split_k == 4
+    props = torch.cuda.get_device_properties(DEV)
+    assert sk.splitk_plan_check_for(plan, M, N, K, L, props.shared_memory_per_multiprocessor,
+                                    props.shared_memory_per_block_optin) == 0
+    c = sk.splitk_gemm_bf16_planned(a_list[2], tb, None, plan)
+    torch.cuda.synchronize()
+    assert_parity(to_host(c), oracle.gemm(a, b), a, b, K)
