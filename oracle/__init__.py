@@ -68,6 +68,19 @@ def _load():
     lib.oracle_gemm_bias.argtypes = [u16p, u16p, u16p, u16p, i64, i64, i64, i64]
     lib.oracle_gemm_bias.restype = None
     lib.oracle_gemm_threaded.restype = ctypes.c_int
+    u8p = ctypes.POINTER(ctypes.c_uint8)
+    f64p = ctypes.POINTER(ctypes.c_double)
+    lib.oracle_e2m1_to_f64.argtypes = [ctypes.c_uint]
+    lib.oracle_e2m1_to_f64.restype = ctypes.c_double
+    lib.oracle_e8m0_to_f64.argtypes = [ctypes.c_uint]
+    lib.oracle_e8m0_to_f64.restype = ctypes.c_double
+    lib.oracle_w4_dequant.argtypes = [u8p, u8p, f64p, i64, i64, i64]
+    lib.oracle_w4_dequant.restype = None
+    lib.oracle_gemm_w4a16.argtypes = [u8p, u8p, u16p, u16p, i64, i64, i64, i64]
+    lib.oracle_gemm_w4a16.restype = None
+    lib.oracle_w4_elements.argtypes = [u8p, u8p, u16p, u16p, i64, i64, i64, i64,
+                                       ctypes.POINTER(ctypes.c_int64), i64]
+    lib.oracle_w4_elements.restype = None
     _lib = lib
     return lib
 
@@ -159,3 +172,62 @@ def dot_f64(A: np.ndarray, B: np.ndarray, l: int, m: int, n: int) -> float:
     A = np.ascontiguousarray(A)
     B = np.ascontiguousarray(B)
     return float(_load().oracle_dot_f64(_ptr(A), _ptr(B), M, N, K, l, m, n))
+
+
+# --------------------------------------------------------------------------
+# A16W4: E2M1 weights with E8M0 scales per 32 k, bf16 activations
+# --------------------------------------------------------------------------
+def e2m1_to_f64(code: int) -> float:
+    return _load().oracle_e2m1_to_f64(int(code) & 0xF)
+
+
+def e8m0_to_f64(code: int) -> float:
+    return _load().oracle_e8m0_to_f64(int(code) & 0xFF)
+
+
+def _w4_shape(Aq: np.ndarray, As: np.ndarray, B: np.ndarray):
+    Aq = np.ascontiguousarray(Aq, dtype=np.uint8)
+    As = np.ascontiguousarray(As, dtype=np.uint8)
+    B = _u16(B)
+    if Aq.ndim == 2:
+        Aq, As, B = Aq[None], As[None], B[None]
+    L, N, K2 = Aq.shape
+    K = 2 * K2
+    Lb, M, Kb = B.shape
+    if (Lb, Kb) != (L, K) or As.shape != (L, N, K // 32) or K % 32:
+        raise ValueError(f"shape mismatch Aq{Aq.shape} As{As.shape} B{B.shape}")
+    return Aq, As, np.ascontiguousarray(B), M, N, K, L
+
+
+def w4_dequant(Aq: np.ndarray, As: np.ndarray) -> np.ndarray:
+    """The float64 weights W[L, N, K] that A_q, A_s encode."""
+    squeeze = Aq.ndim == 2
+    Aq = np.ascontiguousarray(Aq, dtype=np.uint8)
+    As = np.ascontiguousarray(As, dtype=np.uint8)
+    if squeeze:
+        Aq, As = Aq[None], As[None]
+    L, N, K2 = Aq.shape
+    W = np.empty((L, N, 2 * K2), dtype=np.float64)
+    _load().oracle_w4_dequant(_ptr(Aq, ctypes.c_uint8), _ptr(As, ctypes.c_uint8),
+                              _ptr(W, ctypes.c_double), N, 2 * K2, L)
+    return W[0] if squeeze else W
+
+
+def gemm_w4a16(Aq: np.ndarray, As: np.ndarray, B: np.ndarray) -> np.ndarray:
+    """C[L, M, N] bf16 bits = RNE(sum_k w[l,n,k] * B[l,m,k]) in float64."""
+    squeeze = np.asarray(Aq).ndim == 2
+    Aq, As, B, M, N, K, L = _w4_shape(Aq, As, B)
+    C = np.empty((L, M, N), dtype=np.uint16)
+    _load().oracle_gemm_w4a16(_ptr(Aq, ctypes.c_uint8), _ptr(As, ctypes.c_uint8), _ptr(B), _ptr(C),
+                              M, N, K, L)
+    return C[0] if squeeze else C
+
+
+def w4_elements(Aq: np.ndarray, As: np.ndarray, B: np.ndarray, flat_idx) -> np.ndarray:
+    """Selected A16W4 outputs, flat index l*M*N + m*N + n, each computed alone."""
+    Aq, As, B, M, N, K, L = _w4_shape(Aq, As, B)
+    idx = np.ascontiguousarray(np.asarray(flat_idx, dtype=np.int64))
+    out = np.empty(idx.shape[0], dtype=np.uint16)
+    _load().oracle_w4_elements(_ptr(Aq, ctypes.c_uint8), _ptr(As, ctypes.c_uint8), _ptr(B), _ptr(out),
+                               M, N, K, L, _ptr(idx, ctypes.c_int64), idx.shape[0])
+    return out

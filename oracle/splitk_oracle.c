@@ -32,6 +32,10 @@
  * canonical quiet NaN 0x7FC0 (sign kept), overflow maps to +-Inf, subnormals
  * are kept (never flushed).
  *
+ * The A16W4 functions at the end (4-bit weights with 8-bit power-of-two
+ * scales, bf16 activations) follow the Muse Spark AMD dev page's e8m0_f32
+ * and fp4x8_bf16; see their block comment.
+ *
  * Every function here is pinned by tests/test_oracle_pins.py against values
  * fixed independently of this file (exact rational arithmetic, closed forms,
  * library conversions).
@@ -223,4 +227,84 @@ void oracle_gemm_bias(const uint16_t *A, const uint16_t *B, const uint16_t *bias
                 C[(l * M + m) * N + n] = oracle_f64_to_bf16(
                     oracle_dot_f64(A, B, M, N, K, l, m, n) +
                     oracle_bf16_to_f64(bias[l * N + n]));
+}
+
+/* ------------------------------------------------------------------------
+ * A16W4: 4-bit weights, bf16 activations (the Muse Spark AMD dev page,
+ * e8m0_f32 and fp4x8_bf16, "the aiter Muse a16w4 decode").
+ *
+ *   E2M1 code c (4 bits): sign = bit 3, exponent e = bits 2..1 (bias 1),
+ *   mantissa m = bit 0.  e = 0: (-1)^s * m * 2^-1;  e >= 1:
+ *   (-1)^s * (1 + m/2) * 2^(e-1).  Magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6.
+ *   E8M0 code x: the power of two 2^(x - 127) (the page's domain is 1..254,
+ *   where this is the f32 with exponent field x; 255 is not a number).
+ *
+ *   Weights: A_q[l][n][k/2] bytes, element k in the low nibble when k is
+ *   even ("low nibble first"); scales A_s[l][n][k/32], one code per 32
+ *   consecutive k of a weight row (the OCP microscaling block -- a reading:
+ *   the page decodes one dword of 8 codes with one scale but does not print
+ *   the block length).
+ *
+ *   C[l][m][n] = RNE_bf16( sum_k w(l,n,k) * f64(B[l][m][k]) ),
+ *   w(l,n,k) = e2m1(code of k) * e8m0(scale of k / 32), exact in float64.
+ * ------------------------------------------------------------------------ */
+double oracle_e2m1_to_f64(unsigned code)
+{
+    unsigned s = (code >> 3) & 1u, e = (code >> 1) & 3u, m = code & 1u;
+    double mag = e == 0 ? 0.5 * (double)m : (1.0 + 0.5 * (double)m) * ldexp(1.0, (int)e - 1);
+    return s ? -mag : mag;
+}
+
+double oracle_e8m0_to_f64(unsigned code)
+{
+    code &= 0xFFu;
+    if (code == 255u) return NAN;
+    return ldexp(1.0, (int)code - 127);
+}
+
+/* The dequantized weight w(l, n, k). */
+double oracle_w4_weight(const uint8_t *Aq, const uint8_t *As, int64_t N, int64_t K,
+                        int64_t l, int64_t n, int64_t k)
+{
+    const uint8_t byte = Aq[(l * N + n) * (K / 2) + k / 2];
+    const unsigned code = (k % 2 == 0) ? (byte & 0x0Fu) : (byte >> 4);
+    const uint8_t scale = As[(l * N + n) * (K / 32) + k / 32];
+    return oracle_e2m1_to_f64(code) * oracle_e8m0_to_f64(scale);
+}
+
+void oracle_w4_dequant(const uint8_t *Aq, const uint8_t *As, double *W, int64_t N, int64_t K, int64_t L)
+{
+    for (int64_t l = 0; l < L; ++l)
+        for (int64_t n = 0; n < N; ++n)
+            for (int64_t k = 0; k < K; ++k)
+                W[(l * N + n) * K + k] = oracle_w4_weight(Aq, As, N, K, l, n, k);
+}
+
+double oracle_w4_dot_f64(const uint8_t *Aq, const uint8_t *As, const uint16_t *B, int64_t M, int64_t N,
+                         int64_t K, int64_t l, int64_t m, int64_t n)
+{
+    double s = 0.0;
+    for (int64_t k = 0; k < K; ++k)
+        s += oracle_w4_weight(Aq, As, N, K, l, n, k) * oracle_bf16_to_f64(B[(l * M + m) * K + k]);
+    return s;
+}
+
+void oracle_gemm_w4a16(const uint8_t *Aq, const uint8_t *As, const uint16_t *B, uint16_t *C,
+                       int64_t M, int64_t N, int64_t K, int64_t L)
+{
+    for (int64_t l = 0; l < L; ++l)
+        for (int64_t m = 0; m < M; ++m)
+            for (int64_t n = 0; n < N; ++n)
+                C[(l * M + m) * N + n] = oracle_f64_to_bf16(oracle_w4_dot_f64(Aq, As, B, M, N, K, l, m, n));
+}
+
+void oracle_w4_elements(const uint8_t *Aq, const uint8_t *As, const uint16_t *B, uint16_t *out, int64_t M,
+                        int64_t N, int64_t K, int64_t L, const int64_t *flat, int64_t count)
+{
+    (void)L;
+    for (int64_t i = 0; i < count; ++i) {
+        const int64_t f = flat[i];
+        const int64_t l = f / (M * N), m = (f / N) % M, n = f % N;
+        out[i] = oracle_f64_to_bf16(oracle_w4_dot_f64(Aq, As, B, M, N, K, l, m, n));
+    }
 }

@@ -156,3 +156,19 @@ uint64_t synthetic_word(uint64_t seed, uint64_t stream, uint64_t i)
 {
     return word_at(stream_key(seed, stream), i);
 }
+
+/*
+ * Uniform bytes: out[i] = lo + (word i of (seed, stream)) mod span, for
+ * elements [offset, offset + count) -- random 4-bit weight codes (two per
+ * byte, span 256) and 8-bit scale codes (a range of exponents).  Single
+ * threaded: these tensors are a quarter and a 64th of the bf16 weights.
+ */
+void synthetic_bytes(uint8_t *out, uint64_t offset, uint64_t count, uint64_t seed, uint64_t stream,
+                     unsigned lo, unsigned span)
+{
+    const uint64_t key = stream_key(seed, stream);
+    if (span == 0u) span = 1u;
+    for (uint64_t i = 0; i < count; ++i) {
+        out[i] = (uint8_t)(lo + (unsigned)(word_at(key, offset + i) % (uint64_t)span));
+    }
+}

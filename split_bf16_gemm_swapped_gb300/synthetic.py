@@ -20,6 +20,8 @@ from . import _build
 STREAM_A = 0
 STREAM_B = 1
 STREAM_OUTLIER = 2
+STREAM_A_CODES = 3      # packed 4-bit weight codes (A16W4)
+STREAM_A_SCALES = 4     # 8-bit scale codes (A16W4)
 
 _lib = None
 
@@ -33,6 +35,10 @@ def _load():
             ctypes.c_uint64, ctypes.c_uint64, ctypes.c_double, ctypes.c_double,
             ctypes.c_double, ctypes.c_uint64, ctypes.c_int]
         lib.synthetic_normal_bf16.restype = ctypes.c_int
+        lib.synthetic_bytes.argtypes = [
+            ctypes.POINTER(ctypes.c_uint8), ctypes.c_uint64, ctypes.c_uint64,
+            ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint, ctypes.c_uint]
+        lib.synthetic_bytes.restype = None
         lib.synthetic_word.argtypes = [ctypes.c_uint64] * 3
         lib.synthetic_word.restype = ctypes.c_uint64
         _lib = lib
@@ -74,3 +80,31 @@ def normal_bf16(shape, seed: int, stream: int, sigma: float,
 def word(seed: int, stream: int, i: int) -> int:
     """The i-th raw 64-bit SplitMix64 word of (seed, stream)."""
     return int(_load().synthetic_word(int(seed), int(stream), int(i)))
+
+
+def uniform_bytes(shape, seed: int, stream: int, lo: int = 0, span: int = 256,
+                  offset: int = 0) -> np.ndarray:
+    """uint8 array: lo + (SplitMix64 word i of (seed, stream)) mod span."""
+    shape = tuple(int(s) for s in (shape if isinstance(shape, (tuple, list)) else (shape,)))
+    count = int(np.prod(shape)) if shape else 1
+    out = np.empty(shape, dtype=np.uint8)
+    if count:
+        _load().synthetic_bytes(out.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8)), int(offset),
+                                count, int(seed), int(stream), int(lo), int(span))
+    return out
+
+
+# Scale codes of the A16W4 weights: 2^-9 ... 2^-3, so that the 4-bit
+# magnitudes (0 ... 6) span the range of N(0, 0.02)-like weights.
+W4_SCALE_LO = 118
+W4_SCALE_SPAN = 7
+
+
+def w4_weights(L: int, N: int, K: int, seed: int):
+    """Seeded A16W4 weights: packed E2M1 codes A_q[L][N][K/2] (uniform over
+    the 16 codes) and E8M0 scale codes A_s[L][N][K/32]."""
+    if K % 32:
+        raise ValueError("K must be a multiple of 32 (the scale block)")
+    aq = uniform_bytes((L, N, K // 2), seed, STREAM_A_CODES)
+    a_s = uniform_bytes((L, N, K // 32), seed, STREAM_A_SCALES, W4_SCALE_LO, W4_SCALE_SPAN)
+    return aq, a_s

@@ -306,3 +306,123 @@ def test_zero_bias_is_the_plain_gemm():
     A = synthetic.normal_bf16((L, N, K), 70, 0, 0.02)
     B = synthetic.normal_bf16((L, M, K), 70, 1, 1.0)
     assert np.array_equal(oracle.gemm_bias(A, B, np.zeros((L, N), np.uint16)), oracle.gemm(A, B))
+
+
+# --------------------------------------------------------------------------
+# A16W4: E2M1 weight codes with E8M0 scales per 32 k (the Muse Spark AMD dev
+# page, e8m0_f32 and fp4x8_bf16)
+# --------------------------------------------------------------------------
+def _golden_e2m1():
+    rows = []
+    for line in (GOLDEN / "e2m1_values.txt").read_text().splitlines():
+        if line.strip() and not line.startswith("#"):
+            code, value = line.split()[:2]
+            rows.append((int(code, 16), float(value)))
+    return rows
+
+
+def test_e2m1_decoding_matches_the_hand_derived_table():
+    rows = _golden_e2m1()
+    assert [c for c, _ in rows] == list(range(16))
+    for code, value in rows:
+        got = oracle.e2m1_to_f64(code)
+        assert got == value and math.copysign(1.0, got) == math.copysign(1.0, value), code
+
+
+def test_e8m0_is_the_binary32_with_that_exponent_field():
+    """The page: code << 23, read as an f32, is the scale (codes 1..254)."""
+    codes = np.arange(1, 255, dtype=np.uint32)
+    ref = (codes << 23).view(np.float32).astype(np.float64)
+    got = np.array([oracle.e8m0_to_f64(int(c)) for c in codes])
+    assert np.array_equal(got, ref)
+    assert math.isnan(oracle.e8m0_to_f64(255))
+
+
+def _exact_w4(Aq, As, l, n, k):
+    byte = int(Aq[l, n, k // 2])
+    code = byte & 0xF if k % 2 == 0 else byte >> 4
+    value = Fraction(_golden_e2m1()[code][1])
+    return value * Fraction(2) ** (int(As[l, n, k // 32]) - 127)
+
+
+def test_nibble_order_and_scale_blocks_on_a_hand_made_row():
+    """Low nibble is the even k; the scale of k is byte k // 32 of its row.
+    One-hot activations pick single weights out of the product."""
+    K, N = 64, 2
+    Aq = np.zeros((1, N, K // 2), np.uint8)
+    As = np.full((1, N, K // 32), 127, np.uint8)
+    Aq[0, 0, 0] = 0x72          # k=0: code 2 (1.0), k=1: code 7 (6.0)
+    Aq[0, 0, 16] = 0xB5         # k=32: code 5 (3.0), k=33: code 0xB (-1.5)
+    As[0, 0, 1] = 130           # k = 32..63 of row 0 scaled by 2^3
+    Aq[0, 1, 31] = 0x10         # row 1, k=62: code 0, k=63: code 1 (0.5)
+    As[0, 1, 1] = 125           # ... scaled by 2^-2
+    W = oracle.w4_dequant(Aq, As)
+    assert (W[0, 0, 0], W[0, 0, 1], W[0, 0, 32], W[0, 0, 33]) == (1.0, 6.0, 24.0, -12.0)
+    assert (W[0, 1, 62], W[0, 1, 63]) == (0.0, 0.125)
+    M = 4
+    B = np.zeros((1, M, K), np.uint16)
+    for m, k in enumerate([0, 1, 33, 63]):
+        B[0, m, k] = 0x3F80     # 1.0
+    C = oracle.gemm_w4a16(Aq, As, B)
+    expect = [[1.0, 0.0], [6.0, 0.0], [-12.0, 0.0], [0.0, 0.125]]
+    for m in range(M):
+        for n in range(N):
+            assert oracle.bf16_to_f64(int(C[0, m, n])) == expect[m][n], (m, n)
+
+
+def test_w4a16_equals_the_bf16_gemm_of_its_exact_bf16_weights():
+    """Every weight the codes encode (in the scale range used) is a bf16
+    value, so the A16W4 product is the (separately pinned) bf16 oracle's."""
+    from split_bf16_gemm_swapped_gb300 import synthetic
+    L, M, N, K = 2, 3, 20, 256
+    Aq, As = synthetic.w4_weights(L, N, K, seed=51)
+    B = synthetic.normal_bf16((L, M, K), seed=51, stream=1, sigma=1.0)
+    W = oracle.w4_dequant(Aq, As)
+    Wb = np.vectorize(oracle.f64_to_bf16)(W).astype(np.uint16)
+    assert np.array_equal((Wb.astype(np.uint32) << 16).view(np.float32).astype(np.float64), W)
+    assert np.array_equal(oracle.gemm_w4a16(Aq, As, B), oracle.gemm(Wb, B))
+
+
+@pytest.mark.parametrize("L,M,N,K", [(1, 1, 1, 32), (1, 2, 3, 64), (2, 3, 2, 96)])
+def test_w4a16_brute_force_exact_rationals(L, M, N, K):
+    from split_bf16_gemm_swapped_gb300 import synthetic
+    Aq, As = synthetic.w4_weights(L, N, K, seed=61 + K)
+    B = synthetic.normal_bf16((L, M, K), seed=61 + K, stream=1, sigma=1.0)
+    C = oracle.gemm_w4a16(Aq, As, B)
+    for l in range(L):
+        for m in range(M):
+            for n in range(N):
+                s = sum(_exact_w4(Aq, As, l, n, k) * _exact.value(int(B[l, m, k])) for k in range(K))
+                assert C[l, m, n] == _exact.round_bf16(s), (l, m, n)
+
+
+@pytest.mark.parametrize("scale,expect", [(127, 1.0), (130, 8.0), (124, 0.125)])
+def test_w4a16_all_ones_closed_form(scale, expect):
+    """Every weight code 2 (1.0) with one scale, every activation 1.0:
+    C = K * 2^(scale - 127) exactly."""
+    L, M, N, K = 1, 2, 3, 1024
+    Aq = np.full((L, N, K // 2), 0x22, np.uint8)
+    As = np.full((L, N, K // 32), scale, np.uint8)
+    B = np.full((L, M, K), 0x3F80, np.uint16)
+    C = oracle.gemm_w4a16(Aq, As, B)
+    assert np.all(np.vectorize(oracle.bf16_to_f64)(C) == K * expect)
+
+
+def test_w4a16_pins_catch_planted_mistakes():
+    """Altered operands (the mistakes an oracle could make) change the exact
+    result: nibbles swapped, one scale per row, scale blocks out of order."""
+    from split_bf16_gemm_swapped_gb300 import synthetic
+    L, M, N, K = 1, 2, 3, 64
+    Aq, As = synthetic.w4_weights(L, N, K, seed=71)
+    B = synthetic.normal_bf16((L, M, K), seed=71, stream=1, sigma=1.0)
+    exact = np.array([[[_exact.round_bf16(sum(_exact_w4(Aq, As, 0, n, k) * _exact.value(int(B[0, m, k]))
+                                             for k in range(K))) for n in range(N)] for m in range(M)]],
+                     dtype=np.uint16)
+    assert np.array_equal(oracle.gemm_w4a16(Aq, As, B), exact)
+    swapped = ((Aq & 0x0F) << 4) | (Aq >> 4)            # high nibble read as the even k
+    one_scale = np.repeat(As[:, :, :1], K // 32, axis=2)  # the first block's scale for the whole row
+    reversed_blocks = np.ascontiguousarray(As[:, :, ::-1])  # block b scaled by block (nb - 1 - b)
+    assert np.any(As[:, :, 0] != As[:, :, 1])
+    for name, (q, s) in {"nibbles swapped": (swapped, As), "scale per row": (Aq, one_scale),
+                         "scale blocks": (Aq, reversed_blocks)}.items():
+        assert not np.array_equal(oracle.gemm_w4a16(q, s, B), exact), name
