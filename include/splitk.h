@@ -86,6 +86,10 @@ enum splitk_status {
 /* Flags of splitk_gemm_bf16_planned(). */
 #define SPLITK_FLAG_NO_PDL 0x1u
 
+/* Weight formats (splitk_plan_t.weight_format). */
+#define SPLITK_WEIGHTS_BF16 0        /* A[L][N][K] bf16                              */
+#define SPLITK_WEIGHTS_E2M1_E8M0 1   /* A16W4: codes A_q[L][N][K/2], scales A_s[L][N][K/32] */
+
 /*
  * A launch configuration ("tactic": the page's SplitKTactic fields mma_m,
  * mma_n, ab_stages, split_k, plus what the launcher derives from them).
@@ -143,6 +147,14 @@ typedef struct splitk_plan_t {
                               tiles that neither the ring nor tensor memory
                               holds before the programmatic-dependent-launch
                               wait returns                                     */
+    int weight_format;     /* SPLITK_WEIGHTS_BF16, or SPLITK_WEIGHTS_E2M1_E8M0
+                              (plans of splitk_plan_w4a16*): then `stages` is
+                              the CTA's K tiles (all their packed codes are
+                              loaded at once), `a_tmem_tiles` (1..3) the TMEM
+                              slots the epilogue threads decode tiles into,
+                              b_resident = 1, mma_issuers = 1; smem_bytes may
+                              exceed the layout's need, which caps how many
+                              CTAs share an SM (so the slots fit its TMEM)   */
 } splitk_plan_t;
 
 /*
@@ -174,6 +186,35 @@ SPLITK_API int splitk_plan_for(int M, int N, int K, int L, int split_k,
 SPLITK_API int splitk_gemm_bf16(const void *a, const void *b, void *c,
                                 int M, int N, int K, int L, int split_k,
                                 splitk_stream_t stream);
+
+/*
+ * A16W4: C[l][m][n] = bf16_rne( sum_k w(l,n,k) * B[l][m][k] ) with 4-bit
+ * weights: w = e2m1(code) * 2^(scale - 127), the Muse Spark AMD dev page's
+ * e8m0_f32 and fp4x8_bf16 ("a16w4 decode").
+ *   a_q      device, [L][N][K/2] bytes: element k of weight row n in the low
+ *            nibble of byte k/2 when k is even ("low nibble first"), 16-byte
+ *            aligned.  E2M1 code: sign bit 3, exponent bits 2..1 (bias 1),
+ *            mantissa bit 0.
+ *   a_scale  device, [L][N][K/32] bytes: one E8M0 code (1..252, 2^(x-127))
+ *            per 32 consecutive k of a row, 4-byte aligned.
+ *   b, c     as splitk_gemm_bf16().
+ * K must be a multiple of 128, M at most 32, and a CTA's K slice at most 8
+ * tiles of 128 (else SPLITK_ERR_INVALID_SHAPE / SPLITK_ERR_NO_FIT).  The
+ * weights are decoded to bf16 on chip, exactly, and multiplied by the same
+ * tcgen05 BF16 MMA as splitk_gemm_bf16().
+ */
+SPLITK_API int splitk_plan_w4a16_for(int M, int N, int K, int L, int split_k,
+                                     int num_sms, size_t smem_per_sm,
+                                     size_t smem_per_block_optin, splitk_plan_t *out);
+SPLITK_API int splitk_plan_w4a16(int M, int N, int K, int L, int split_k,
+                                 splitk_plan_t *out);
+SPLITK_API int splitk_gemm_w4a16(const void *a_q, const void *a_scale, const void *b,
+                                 void *c, int M, int N, int K, int L, int split_k,
+                                 splitk_stream_t stream);
+SPLITK_API int splitk_gemm_w4a16_planned(const void *a_q, const void *a_scale,
+                                         const void *b, void *c, int M, int N, int K,
+                                         int L, const splitk_plan_t *plan,
+                                         unsigned flags, splitk_stream_t stream);
 
 /*
  * Checks a plan against a shape on a described device without touching CUDA

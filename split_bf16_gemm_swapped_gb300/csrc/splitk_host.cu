@@ -68,16 +68,32 @@ size_t smem_bytes_for(int mma_n, int stages, uint32_t dedicated_mailbox_bytes, i
          (size_t)b_region_tiles * b_stage_bytes(mma_n) + dedicated_mailbox_bytes + kBarRegionBytes;
 }
 
-// CTAs of this kernel that shared memory lets onto one SM (each CTA also
-// reserves 1 KiB of the SM's shared memory).
-int resident_by_smem(size_t smem_per_sm, size_t smem) { return (int)(smem_per_sm / (smem + 1024)); }
-
 // Bytes of one reduction round: (split - 1) peers x the round's token
 // columns (at most 4 per quad, at most the tile's real columns) x 128 rows.
 uint32_t mailbox_round_bytes(int split, int quads, int ncols_max) {
   const int cols = std::min(quads * 4, ncols_max);
   return (uint32_t)(split - 1) * (uint32_t)cols * kColumnBytes;
 }
+
+// Shared memory of an A16W4 plan's layout: all packed weight tiles, all
+// activation tiles (at least 2: rank 0's f32 staging tile reuses them), the
+// mailbox, the barriers and the decode table.
+size_t smem_bytes_w4(int mma_n, int k_tiles, uint32_t dedicated_mailbox_bytes) {
+  return (size_t)kAlignSlack + (size_t)k_tiles * kW4TileBytes +
+         (size_t)std::max(2, k_tiles) * b_stage_bytes(mma_n) + dedicated_mailbox_bytes + kBarRegionBytes +
+         kW4TableBytes;
+}
+
+// Mailbox bytes of a dedicated single-round reduction (rank 0 or scattered).
+uint32_t w4_mailbox_bytes(int split, int reduce_scatter, int ncols_max) {
+  if (split == 1) return 0u;
+  if (reduce_scatter) return (uint32_t)ncols_max * kColumnBytes;
+  return mailbox_round_bytes(split, (ncols_max + 3) / 4, ncols_max);
+}
+
+// CTAs of this kernel that shared memory lets onto one SM (each CTA also
+// reserves 1 KiB of the SM's shared memory).
+int resident_by_smem(size_t smem_per_sm, size_t smem) { return (int)(smem_per_sm / (smem + 1024)); }
 
 // 128-wide K tiles covering K; the last one may be ragged (TMA reads zeros
 // past K).
@@ -214,6 +230,7 @@ int plan_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t smem_
         out->mma_issuers = 1;
         out->b_loader = 0;
         out->l2_prefetch = 0;
+        out->weight_format = SPLITK_WEIGHTS_BF16;
         stage_for_decode(out, ncols_max, ctas, num_sms, smem_per_sm, smem_optin, scatter_bytes);
         return SPLITK_OK;
       }
@@ -256,6 +273,7 @@ int plan_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t smem_
       out->mma_issuers = 1;
       out->b_loader = 0;
       out->l2_prefetch = 0;
+      out->weight_format = SPLITK_WEIGHTS_BF16;
       stage_for_decode(out, ncols_max, ctas, num_sms, smem_per_sm, smem_optin,
                        prefer_dedicated ? mailbox_round_bytes(split, quads, ncols_max) : 0u);
       return SPLITK_OK;
@@ -264,9 +282,108 @@ int plan_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t smem_
   return SPLITK_ERR_NO_FIT;
 }
 
+// The A16W4 plan: decode-sized tiles (mma_n 16 or 32), the split of the bf16
+// planner (raised until a CTA's K slice is at most 8 tiles, all of whose
+// packed codes are loaded at once), min(3, k_tiles) TMEM slots for decoded
+// tiles, resident activations (loaded by the epilogue threads when few), the
+// early trigger, and a dedicated single-round mailbox (scattered from split 4
+// and 16 token columns).  Shared memory is padded when needed so that the
+// CTAs fitting an SM can hold their TMEM.
+int plan_w4_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t smem_per_sm, size_t smem_optin,
+                 splitk_plan_t* out) {
+  if (!out) return SPLITK_ERR_NULL;
+  if (M < 1 || N < 1 || K < 1 || L < 1 || M > 32 || K % kCtaK != 0) return SPLITK_ERR_INVALID_SHAPE;
+  if (split_k != 0 && !valid_split(split_k)) return SPLITK_ERR_UNSUPPORTED_SPLIT;
+  if (num_sms < 1 || smem_optin < 1 || smem_per_sm < 1) return SPLITK_ERR_UNSUPPORTED_DEVICE;
+  const int T = K / kCtaK;
+  const int mma_n = choose_mma_n(M);
+  const long long m_tiles = (M + mma_n - 1) / mma_n;
+  const long long n_tiles = ((long long)N + kMmaM - 1) / kMmaM;
+  if (n_tiles > 65535 || L > 65535) return SPLITK_ERR_INVALID_SHAPE;
+  int split = split_k != 0 ? split_k : auto_split(T, m_tiles * n_tiles * L, num_sms, mma_n);
+  while (split_k == 0 && split < 8 && (T + split - 1) / split > kMaxStages && split * 2 <= T) split *= 2;
+  if (split > T) return SPLITK_ERR_INVALID_SHAPE;
+  const int kt = (T + split - 1) / split;
+  if (kt > kMaxStages) return SPLITK_ERR_NO_FIT;
+  const int ncols_max = std::min(M, mma_n);
+  splitk_plan_t p;
+  std::memset(&p, 0, sizeof(p));
+  p.mma_m = kMmaM;
+  p.mma_n = mma_n;
+  p.stages = kt;
+  p.split_k = split;
+  p.k_tiles_per_cta = kt;
+  p.mailbox_dedicated = split > 1 ? 1 : 0;
+  p.mailbox_quads = (ncols_max + 3) / 4;
+  p.reduce_rounds = split > 1 ? 1 : 0;
+  p.grid[0] = (unsigned)(split * m_tiles);
+  p.grid[1] = (unsigned)n_tiles;
+  p.grid[2] = (unsigned)L;
+  p.cluster[0] = (unsigned)split;
+  p.cluster[1] = 1;
+  p.cluster[2] = 1;
+  p.pdl_trigger = 1;
+  p.reduce_scatter = split >= 4 && ncols_max >= 16 ? 1 : 0;
+  p.b_resident = 1;
+  p.a_tmem_tiles = std::min(kMaxTmemTiles, kt);
+  p.mma_issuers = 1;
+  p.tmem_cols = tmem_cols_for(mma_n, p.a_tmem_tiles, 1);
+  p.b_loader = ncols_max * kt * (kCtaK / 8) <= 4 * kEpiThreads ? 1 : 0;
+  p.l2_prefetch = 0;
+  p.weight_format = SPLITK_WEIGHTS_E2M1_E8M0;
+  size_t smem = smem_bytes_w4(mma_n, kt, w4_mailbox_bytes(split, p.reduce_scatter, ncols_max));
+  const int per_sm_max = std::max(1, (int)(512u / p.tmem_cols));
+  if (resident_by_smem(smem_per_sm, smem) > per_sm_max) {
+    smem = std::max(smem, (smem_per_sm / (size_t)(per_sm_max + 1) + 16u) & ~(size_t)15u);
+    while (resident_by_smem(smem_per_sm, smem) > per_sm_max) smem += 16;
+  }
+  if (smem > smem_optin) return SPLITK_ERR_NO_FIT;
+  p.smem_bytes = smem;
+  p.ctas_per_sm = std::min(3, resident_by_smem(smem_per_sm, smem));
+  *out = p;
+  return SPLITK_OK;
+}
+
 // Re-derives everything a plan implies and checks it against the shape.
+int check_plan_w4(const splitk_plan_t& pl, int M, int N, int K, int L, size_t smem_optin, size_t smem_per_sm,
+                  uint32_t* dedicated_bytes) {
+  if (pl.mma_m != kMmaM || (pl.mma_n != 16 && pl.mma_n != 32)) return SPLITK_ERR_BAD_PLAN;
+  if (!valid_split(pl.split_k)) return SPLITK_ERR_UNSUPPORTED_SPLIT;
+  if (M > 32 || K % kCtaK != 0 || K / kCtaK < pl.split_k) return SPLITK_ERR_INVALID_SHAPE;
+  const int T = K / kCtaK;
+  const int kt = (T + pl.split_k - 1) / pl.split_k;
+  if (pl.k_tiles_per_cta != kt || pl.stages != kt) return SPLITK_ERR_BAD_PLAN;
+  if (kt > kMaxStages) return SPLITK_ERR_NO_FIT;
+  const long long m_tiles = (M + pl.mma_n - 1) / pl.mma_n;
+  const long long n_tiles = ((long long)N + kMmaM - 1) / kMmaM;
+  if (n_tiles > 65535 || L > 65535) return SPLITK_ERR_INVALID_SHAPE;
+  if (pl.grid[0] != (unsigned)(pl.split_k * m_tiles) || pl.grid[1] != (unsigned)n_tiles ||
+      pl.grid[2] != (unsigned)L || pl.cluster[0] != (unsigned)pl.split_k || pl.cluster[1] != 1 ||
+      pl.cluster[2] != 1) {
+    return SPLITK_ERR_BAD_PLAN;
+  }
+  const int ncols_max = std::min(M, pl.mma_n);
+  if (pl.split_k > 1 && (!pl.mailbox_dedicated || pl.mailbox_quads != (ncols_max + 3) / 4)) return SPLITK_ERR_BAD_PLAN;
+  if (pl.reduce_scatter != 0 && (pl.reduce_scatter != 1 || pl.split_k < 2)) return SPLITK_ERR_BAD_PLAN;
+  if (pl.b_resident != 1 || pl.mma_issuers != 1 || pl.l2_prefetch != 0) return SPLITK_ERR_BAD_PLAN;
+  if (pl.a_tmem_tiles < 1 || pl.a_tmem_tiles > kMaxTmemTiles) return SPLITK_ERR_BAD_PLAN;
+  if (pl.b_loader != 0 && pl.b_loader != 1) return SPLITK_ERR_BAD_PLAN;
+  if (pl.pdl_trigger != 0 && pl.pdl_trigger != 1) return SPLITK_ERR_BAD_PLAN;
+  if (pl.tmem_cols != tmem_cols_for(pl.mma_n, pl.a_tmem_tiles, 1)) return SPLITK_ERR_BAD_PLAN;
+  const uint32_t ded = w4_mailbox_bytes(pl.split_k, pl.reduce_scatter, ncols_max);
+  if (pl.smem_bytes < smem_bytes_w4(pl.mma_n, kt, ded) || pl.smem_bytes % 16 != 0) return SPLITK_ERR_BAD_PLAN;
+  if (pl.smem_bytes > smem_optin) return SPLITK_ERR_NO_FIT;
+  if ((size_t)resident_by_smem(smem_per_sm, pl.smem_bytes) * pl.tmem_cols > 512u) return SPLITK_ERR_BAD_PLAN;
+  *dedicated_bytes = ded;
+  return SPLITK_OK;
+}
+
 int check_plan(const splitk_plan_t& pl, int M, int N, int K, int L, size_t smem_optin,
                size_t smem_per_sm, uint32_t* dedicated_bytes) {
+  if (pl.weight_format == SPLITK_WEIGHTS_E2M1_E8M0) {
+    return check_plan_w4(pl, M, N, K, L, smem_optin, smem_per_sm, dedicated_bytes);
+  }
+  if (pl.weight_format != SPLITK_WEIGHTS_BF16) return SPLITK_ERR_BAD_PLAN;
   if (pl.mma_m != kMmaM) return SPLITK_ERR_BAD_PLAN;
   if (pl.mma_n != 16 && pl.mma_n != 32 && pl.mma_n != 64 && pl.mma_n != 128) return SPLITK_ERR_BAD_PLAN;
   if (!valid_split(pl.split_k)) return SPLITK_ERR_UNSUPPORTED_SPLIT;
@@ -362,10 +479,29 @@ bool encode_3d(CUtensorMap* map, const void* ptr, uint64_t d0, uint64_t d1, uint
   return r == CUDA_SUCCESS;
 }
 
+// A16W4 codes [L][N][K/2] bytes read in boxes of {64 B, 128 rows, 1} with
+// the 64-byte swizzle (each decoding thread reads its row conflict-free);
+// out-of-range rows read as zero codes.
+bool encode_3d_w4(CUtensorMap* map, const void* ptr, uint64_t row_bytes, uint64_t d1, uint64_t d2) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {row_bytes, d1, d2};
+  cuuint64_t strides[2] = {row_bytes, row_bytes * d1};
+  cuuint32_t box[3] = {kW4RowBytes, (cuuint32_t)kMmaM, 1u};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 struct AKey {
   uintptr_t ptr;
   int N, K, L;
-  bool operator==(const AKey& o) const { return ptr == o.ptr && N == o.N && K == o.K && L == o.L; }
+  int fmt;                    // SPLITK_WEIGHTS_*
+  bool operator==(const AKey& o) const {
+    return ptr == o.ptr && N == o.N && K == o.K && L == o.L && fmt == o.fmt;
+  }
 };
 struct BKey {
   uintptr_t ptr;
@@ -380,7 +516,7 @@ inline uint64_t mix(uint64_t h, uint64_t v) {
 }
 struct AKeyHash {
   size_t operator()(const AKey& k) const {
-    return (size_t)mix(mix(mix(mix(0, k.ptr), (uint64_t)k.N), (uint64_t)k.K), (uint64_t)k.L);
+    return (size_t)mix(mix(mix(mix(mix(0, k.ptr), (uint64_t)k.N), (uint64_t)k.K), (uint64_t)k.L), (uint64_t)k.fmt);
   }
 };
 struct BKeyHash {
@@ -445,8 +581,8 @@ int current_device(DeviceState** out, int* dev_out) {
 // Caller holds g_mu.  Device address of A's tensor map, encoding and
 // copying it on `stream` the first time.
 int a_map_for(DeviceState& st, const void* a, int N, int K, int L, cudaStream_t stream,
-              const CUtensorMap** out) {
-  AKey key{(uintptr_t)a, N, K, L};
+              const CUtensorMap** out, int fmt = SPLITK_WEIGHTS_BF16) {
+  AKey key{(uintptr_t)a, N, K, L, fmt};
   auto it = st.a_slots.find(key);
   if (it != st.a_slots.end()) {
     *out = st.d_pool + it->second;
@@ -469,9 +605,10 @@ int a_map_for(DeviceState& st, const void* a, int N, int K, int L, cudaStream_t 
   }
   if (st.used >= kMapPoolSlots) return SPLITK_ERR_CACHE_FULL;
   const int slot = st.used;
-  if (!encode_3d(&st.h_pool[slot], a, (uint64_t)K, (uint64_t)N, (uint64_t)L, (uint32_t)kMmaM)) {
-    return SPLITK_ERR_CUDA;
-  }
+  const bool encoded = fmt == SPLITK_WEIGHTS_E2M1_E8M0
+                           ? encode_3d_w4(&st.h_pool[slot], a, (uint64_t)K / 2u, (uint64_t)N, (uint64_t)L)
+                           : encode_3d(&st.h_pool[slot], a, (uint64_t)K, (uint64_t)N, (uint64_t)L, (uint32_t)kMmaM);
+  if (!encoded) return SPLITK_ERR_CUDA;
   if (cudaMemcpyAsync(st.d_pool + slot, st.h_pool + slot, sizeof(CUtensorMap), cudaMemcpyHostToDevice,
                       stream) != cudaSuccess) {
     cudaGetLastError();
@@ -506,8 +643,9 @@ int check_pointers(const void* a, const void* b, const void* c) {
 
 // The kernel's parameters for a checked plan.
 void fill_params(const splitk_plan_t& pl, int M, int N, int K, int L, uint32_t ded, const CUtensorMap* a_map,
-                 const void* b, void* c, const void* bias, KernelParams* p) {
+                 const void* b, void* c, const void* bias, KernelParams* p, const void* a_scale = nullptr) {
   p->a_map = a_map;
+  p->a_scale = static_cast<const uint8_t*>(a_scale);
   p->b = static_cast<const uint16_t*>(b);
   p->c = static_cast<uint16_t*>(c);
   p->bias = static_cast<const uint16_t*>(bias);
@@ -527,7 +665,9 @@ void fill_params(const splitk_plan_t& pl, int M, int N, int K, int L, uint32_t d
   p->pdl_trigger_early = pl.pdl_trigger;
   p->reduce_scatter = pl.reduce_scatter;
   p->b_resident = pl.b_resident;
-  p->b_region_tiles = b_region_tiles_for(pl.stages, pl.b_resident, pl.k_tiles_per_cta);
+  p->b_region_tiles = pl.weight_format == SPLITK_WEIGHTS_E2M1_E8M0
+                          ? std::max(2, pl.k_tiles_per_cta)
+                          : b_region_tiles_for(pl.stages, pl.b_resident, pl.k_tiles_per_cta);
   p->a_tmem_tiles = pl.a_tmem_tiles;
   p->tmem_cols = pl.tmem_cols;
   p->tmem_tile_col0 = tmem_tile_col0(pl.mma_n, pl.mma_issuers);
@@ -541,6 +681,7 @@ void fill_params(const splitk_plan_t& pl, int M, int N, int K, int L, uint32_t d
 LaunchArgs launch_args(const splitk_plan_t& pl, bool pdl) {
   LaunchArgs la;
   la.mma_n = pl.mma_n;
+  la.w4 = pl.weight_format == SPLITK_WEIGHTS_E2M1_E8M0;
   la.grid = dim3(pl.grid[0], pl.grid[1], pl.grid[2]);
   la.cluster_x = (unsigned)pl.split_k;
   la.smem_bytes = pl.smem_bytes;
@@ -551,19 +692,21 @@ LaunchArgs launch_args(const splitk_plan_t& pl, bool pdl) {
 // Caller holds g_mu.
 int launch_locked(DeviceState& st, const void* a, const void* b, void* c, int M, int N, int K, int L,
                   const splitk_plan_t& pl, unsigned flags, cudaStream_t stream,
-                  const void* bias = nullptr) {
+                  const void* bias = nullptr, const void* a_scale = nullptr) {
   uint32_t ded = 0;
   int rc = check_plan(pl, M, N, K, L, st.smem_optin, st.smem_per_sm, &ded);
   if (rc != SPLITK_OK) return rc;
+  // the A16W4 kernel needs its scales; the bf16 kernel takes none
+  if ((pl.weight_format == SPLITK_WEIGHTS_E2M1_E8M0) != (a_scale != nullptr)) return SPLITK_ERR_BAD_PLAN;
   const CUtensorMap* a_map = nullptr;
-  rc = a_map_for(st, a, N, K, L, stream, &a_map);
+  rc = a_map_for(st, a, N, K, L, stream, &a_map, pl.weight_format);
   if (rc != SPLITK_OK) return rc;
   CUtensorMap b_map;
   rc = b_map_for(st, b, M, K, L, pl.mma_n, &b_map);
   if (rc != SPLITK_OK) return rc;
 
   KernelParams p;
-  fill_params(pl, M, N, K, L, ded, a_map, b, c, bias, &p);
+  fill_params(pl, M, N, K, L, ded, a_map, b, c, bias, &p, a_scale);
   const LaunchArgs la = launch_args(pl, (flags & SPLITK_FLAG_NO_PDL) == 0);
   if (launch_kernel(la, b_map, p, stream) != cudaSuccess) {
     cudaGetLastError();
@@ -782,6 +925,7 @@ SPLITK_API int splitk_gemm_bf16_noalloc(const void* a, const void* b, void* c, i
   uint32_t ded = 0;
   rc = check_plan(pl, M, N, K, L, st->smem_optin, st->smem_per_sm, &ded);
   if (rc != SPLITK_OK) return rc;
+  if (pl.weight_format != SPLITK_WEIGHTS_BF16) return SPLITK_ERR_BAD_PLAN;
   // Set-up, once per device, with that device current: the device address of
   // the scratch array.
   if (g_noalloc_addr[dev] == nullptr) {
@@ -814,6 +958,54 @@ SPLITK_API int splitk_gemm_bf16_noalloc(const void* a, const void* b, void* c, i
     return SPLITK_ERR_CUDA;
   }
   return SPLITK_OK;
+}
+
+SPLITK_API int splitk_plan_w4a16_for(int M, int N, int K, int L, int split_k, int num_sms, size_t smem_per_sm,
+                                     size_t smem_per_block_optin, splitk_plan_t* out) {
+  return plan_w4_impl(M, N, K, L, split_k, num_sms, smem_per_sm, smem_per_block_optin, out);
+}
+
+SPLITK_API int splitk_plan_w4a16(int M, int N, int K, int L, int split_k, splitk_plan_t* out) {
+  if (!out) return SPLITK_ERR_NULL;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* st = nullptr;
+  int rc = current_device(&st, nullptr);
+  if (rc != SPLITK_OK) return rc;
+  return plan_w4_impl(M, N, K, L, split_k, st->num_sms, st->smem_per_sm, st->smem_optin, out);
+}
+
+SPLITK_API int splitk_gemm_w4a16_planned(const void* a_q, const void* a_scale, const void* b, void* c, int M,
+                                         int N, int K, int L, const splitk_plan_t* plan, unsigned flags,
+                                         splitk_stream_t stream) {
+  if (!plan || !a_scale) return SPLITK_ERR_NULL;
+  int rc = check_pointers(a_q, b, c);
+  if (rc != SPLITK_OK) return rc;
+  if ((uintptr_t)a_scale & 3u) return SPLITK_ERR_MISALIGNED;
+  if (M < 1 || N < 1 || K < 1 || L < 1) return SPLITK_ERR_INVALID_SHAPE;
+  if (plan->weight_format != SPLITK_WEIGHTS_E2M1_E8M0) return SPLITK_ERR_BAD_PLAN;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* st = nullptr;
+  rc = current_device(&st, nullptr);
+  if (rc != SPLITK_OK) return rc;
+  return launch_locked(*st, a_q, b, c, M, N, K, L, *plan, flags, reinterpret_cast<cudaStream_t>(stream), nullptr,
+                       a_scale);
+}
+
+SPLITK_API int splitk_gemm_w4a16(const void* a_q, const void* a_scale, const void* b, void* c, int M, int N,
+                                 int K, int L, int split_k, splitk_stream_t stream) {
+  if (!a_scale) return SPLITK_ERR_NULL;
+  int rc = check_pointers(a_q, b, c);
+  if (rc != SPLITK_OK) return rc;
+  if ((uintptr_t)a_scale & 3u) return SPLITK_ERR_MISALIGNED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* st = nullptr;
+  rc = current_device(&st, nullptr);
+  if (rc != SPLITK_OK) return rc;
+  splitk_plan_t pl;
+  rc = plan_w4_impl(M, N, K, L, split_k, st->num_sms, st->smem_per_sm, st->smem_optin, &pl);
+  if (rc != SPLITK_OK) return rc;
+  return launch_locked(*st, a_q, b, c, M, N, K, L, pl, 0u, reinterpret_cast<cudaStream_t>(stream), nullptr,
+                       a_scale);
 }
 
 SPLITK_API int splitk_plan_check_for(const splitk_plan_t* plan, int M, int N, int K, int L,

@@ -31,6 +31,14 @@ constexpr uint32_t kWaitHintNs = 1000000u;
 
 __host__ __device__ constexpr uint32_t b_stage_bytes(int mma_n) { return (uint32_t)mma_n * kCtaK * 2; }
 
+// A16W4 weights: a K tile of 128 rows x 128 four-bit codes is 128 rows of 64
+// bytes (one TMA box, 64-byte swizzle); its 4 scale codes per row (one per 32
+// k) are read by the decoding threads.  The decode table maps a byte (two
+// codes, low nibble first) to the two bf16 values it encodes.
+constexpr uint32_t kW4TileBytes = kMmaM * kCtaK / 2;       // 8 KiB
+constexpr uint32_t kW4RowBytes = kCtaK / 2;                 // 64
+constexpr uint32_t kW4TableBytes = 256 * 4;
+
 // Tensor memory: one accumulator per MMA issuer, max(32, mma_n) columns
 // each, from column 0; weight K tiles staged in tensor memory (64 columns
 // each: 128 lanes x 128 bf16) from the next 64-column boundary.  Allocations
@@ -61,6 +69,7 @@ enum Role : int {
   kRoleEpiMma = 4,
   kRoleEpiReduce = 5,
   kRoleEpiReady = 6,
+  kRoleEpiDecode = 7,
 };
 
 constexpr unsigned kInjectSkipPublish = 0x1u;
@@ -70,6 +79,7 @@ struct KernelParams {
   uint16_t* c;                // C[L][M][N] bf16 bits
   const uint16_t* bias;       // [L][N] bf16 bits added before rounding, or null
   const uint16_t* b;          // activations B[L][M][K] (read directly when b_loader = 1)
+  const uint8_t* a_scale;     // A16W4: scale codes [L][N][K/32] (null for bf16 weights)
   int M, N, K, L;
   int split;                  // cluster size along K
   int stages;                 // ring depth
@@ -117,6 +127,7 @@ enum TraceSlot : int {
 
 struct LaunchArgs {
   int mma_n;
+  bool w4;                    // A16W4 weights
   dim3 grid;
   unsigned cluster_x;
   size_t smem_bytes;

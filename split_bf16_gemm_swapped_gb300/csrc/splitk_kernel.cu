@@ -151,15 +151,25 @@ __device__ __forceinline__ void load_acc4(uint32_t taddr, uint32_t second, bool 
   }
 }
 
+// One E2M1 code (sign bit 3, exponent bits 2..1 with bias 1, mantissa bit
+// 0) as bf16 bits: exponent e >= 1 gives (1 + m/2) * 2^(e-1), i.e. the bf16
+// exponent field e + 126 with m as the top mantissa bit; e = 0 gives m * 0.5.
+__device__ __forceinline__ uint32_t e2m1_bf16_bits(uint32_t c) {
+  const uint32_t e = (c >> 1) & 3u, m = c & 1u;
+  const uint32_t mag = e != 0u ? (((e + 126u) << 7) | (m << 6)) : (m != 0u ? 0x3F00u : 0u);
+  return ((c & 8u) << 12) | mag;
+}
+
 }  // namespace
 
-template <int MMA_N>
+template <int MMA_N, bool kW4>
 __global__ void __launch_bounds__(kThreads, 3)
     splitk_gemm_bf16_kernel(const __grid_constant__ CUtensorMap b_map, const KernelParams p) {
   constexpr uint32_t kBStage = b_stage_bytes(MMA_N);
   constexpr uint32_t kBBox = kBStage / 2;                   // MMA_N rows x 128 B
   constexpr uint32_t kAccCols = tmem_acc_cols(MMA_N);       // TMEM columns of one accumulator
   constexpr uint32_t kIdesc = dev::idesc_bf16_f32(kMmaM, MMA_N);
+  constexpr uint32_t kAStage = kW4 ? kW4TileBytes : kAStageBytes;   // one weight K tile in shared memory
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = dev::smem_u32(smem_raw);
@@ -183,9 +193,10 @@ __global__ void __launch_bounds__(kThreads, 3)
   const bool b_res = p.b_resident != 0;
   const int tmem_tiles = p.a_tmem_tiles < k_tiles ? p.a_tmem_tiles : k_tiles;
 
-  // Shared memory: [A ring][B ring or all B tiles][dedicated mailbox?][barriers].
+  // Shared memory: [A ring (A16W4: all packed tiles)][B ring or all B tiles]
+  // [dedicated mailbox?][barriers][A16W4: decode table].
   const uint32_t sA = base;
-  const uint32_t sB = sA + (uint32_t)stages * kAStageBytes;
+  const uint32_t sB = sA + (uint32_t)stages * kAStage;
   const uint32_t ring_end = sB + (uint32_t)p.b_region_tiles * kBStage;
   const uint32_t sMail = p.mailbox_dedicated ? ring_end : sA;
   const uint32_t sBar = ring_end + (p.mailbox_dedicated ? p.mailbox_bytes : 0u);
@@ -198,6 +209,9 @@ __global__ void __launch_bounds__(kThreads, 3)
   const uint32_t slot_tmem = bar_mma_done + 32u;
   const uint32_t slot_abort = bar_mma_done + 36u;
   const uint32_t bar_b = bar_mma_done + 40u;             // count 1 + tx bytes (resident B)
+  const uint32_t bar_slot_full0 = bar_mma_done + 48u;    // A16W4 [3]: tile decoded into TMEM slot, count 128
+  const uint32_t bar_slot_empty0 = bar_mma_done + 72u;   // A16W4 [3]: slot read by the MMAs, count 1
+  const uint32_t sTab = sBar + kBarRegionBytes;          // A16W4 decode table, 256 x u32
 
   const Waiter waiter{slot_abort, p.wait_limit_ns};
 
@@ -222,6 +236,12 @@ __global__ void __launch_bounds__(kThreads, 3)
       dev::mbar_init(bar_tmem_empty, kEpiThreads);
       dev::mbar_init(bar_reduce, 1);
       dev::mbar_init(bar_ready, 1);
+      if (kW4) {
+        for (int i = 0; i < 3; ++i) {
+          dev::mbar_init(bar_slot_full0 + 8u * i, kEpiThreads);
+          dev::mbar_init(bar_slot_empty0 + 8u * i, 1);
+        }
+      }
       dev::st_shared_u32(slot_abort, 0u);
       dev::fence_barrier_init();
       stamp(p, kTrBarInit);
@@ -247,8 +267,24 @@ __global__ void __launch_bounds__(kThreads, 3)
       if (p.pdl_trigger_early) dev::griddep_launch_dependents();
     }
   }
+  if (kW4 && warp >= 4) {
+    // byte -> two bf16 (low nibble = lower k = low half)
+    for (int i = (int)threadIdx.x - 128; i < 256; i += kEpiThreads) {
+      dev::st_shared_u32(sTab + 4u * (uint32_t)i,
+                         e2m1_bf16_bits((uint32_t)i & 15u) | (e2m1_bf16_bits((uint32_t)i >> 4) << 16));
+    }
+  }
   dev::cluster_arrive_release();
-  if (threadIdx.x == 0) {
+  if (kW4 && threadIdx.x == 0) {
+    // every packed weight tile of the CTA at once: one 8 KiB box each
+    for (; a_issued < k_tiles; ++a_issued) {
+      const uint32_t full = bar_full0 + 8u * a_issued;
+      dev::mbar_arrive_expect_tx(full, kW4TileBytes);
+      dev::tma_load_3d_hint(sA + (uint32_t)a_issued * kW4TileBytes, p.a_map, (kt0 + a_issued) * (int)kW4RowBytes,
+                            n0, l, full, a_policy);
+    }
+    stamp(p, kTrPrefetched);
+  } else if (threadIdx.x == 0) {
     const int first = k_tiles < stages ? k_tiles : stages;
     for (; a_issued < first; ++a_issued) {
       const uint32_t full = bar_full0 + 8u * a_issued;
@@ -341,7 +377,32 @@ __global__ void __launch_bounds__(kThreads, 3)
     // adds the two.
     const int issuer = warp - 2;
     const int nis = p.mma_issuers;
-    if (lane == 0 && issuer < nis) {
+    if (kW4 && lane == 0 && issuer == 0) {
+      // A16W4: the epilogue threads decode each weight tile into a TMEM slot
+      // (tile kt in slot kt % slots); the MMAs read A from there.
+      const int slots = p.a_tmem_tiles;
+      bool ok = waiter.wait<false>(bar_b, 0u, kRoleMma, -1);
+      dev::tc_fence_after();
+      for (int kt = 0; kt < k_tiles && ok; ++kt) {
+        const int slot = kt % slots;
+        ok = waiter.wait<false>(bar_slot_full0 + 8u * slot, (uint32_t)((kt / slots) & 1), kRoleMma, kt);
+        if (!ok) break;
+        dev::tc_fence_after();
+        if (kt == 0) stamp(p, kTrFirstFull);
+        if (kt == k_tiles - 1) stamp(p, kTrLastFull);
+        const uint32_t b_st = sB + (uint32_t)kt * kBStage;
+        const uint32_t t_col = tmem_base + p.tmem_tile_col0 + (uint32_t)slot * kTmemTileCols;
+#pragma unroll
+        for (int kk = 0; kk < kCtaK / kMmaK; ++kk) {
+          const uint32_t b_off = (uint32_t)(kk >> 2) * kBBox + (uint32_t)(kk & 3) * 32u;
+          dev::mma_bf16_ts(tmem_base, t_col + (uint32_t)kk * 8u, dev::smem_desc_sw128(b_st + b_off), kIdesc,
+                           (kt | kk) != 0 ? 1u : 0u);
+        }
+        dev::mma_commit(bar_slot_empty0 + 8u * slot);   // slot free once these MMAs have read it
+      }
+      dev::mma_commit(bar_mma_done);
+    }
+    if (!kW4 && lane == 0 && issuer < nis) {
       const uint32_t d_acc = tmem_base + (uint32_t)issuer * kAccCols;
       bool ok = true;
       // Before the activations can exist: copy this issuer's share of the
@@ -434,14 +495,14 @@ __global__ void __launch_bounds__(kThreads, 3)
       }
     }
 
-    if (p.b_loader) {
-      // The activations of all of the CTA's K tiles, loaded by the epilogue
-      // threads (idle until the accumulator is complete) with 16-byte loads
-      // through L2 and stored in the 128-byte-swizzled layout the MMA reads:
-      // 16-byte chunk c of row r of an 8-row atom lands at chunk c ^ (r % 8).
-      // Columns past K are zero (the weights there are zero-filled, and
-      // 0 * garbage could be NaN); rows past M are left unwritten -- they
-      // only feed accumulator columns that are never read.
+    // The activations of all of the CTA's K tiles, loaded by the epilogue
+    // threads (idle until the accumulator is complete) with 16-byte loads
+    // through L2 and stored in the 128-byte-swizzled layout the MMA reads:
+    // 16-byte chunk c of row r of an 8-row atom lands at chunk c ^ (r % 8).
+    // Columns past K are zero (the weights there are zero-filled, and
+    // 0 * garbage could be NaN); rows past M are left unwritten -- they
+    // only feed accumulator columns that are never read.
+    auto load_activations = [&]() {
       dev::griddep_wait();
       const int cpr = k_tiles * (kCtaK / 8);           // 16-byte chunks per row
       for (int i = et; i < ncols * cpr; i += kEpiThreads) {
@@ -460,6 +521,52 @@ __global__ void __launch_bounds__(kThreads, 3)
       dev::fence_proxy_async_shared();   // generic-proxy stores, read by tcgen05.mma
       dev::mbar_arrive(bar_b);
       if (et == 0) stamp(p, kTrActReady);
+    };
+
+    if constexpr (kW4) {
+      // A16W4: thread et decodes weight row n0 + et of each K tile into TMEM
+      // lane et: 4 chunks of 32 codes (64 B of the tile's 64-byte-swizzled
+      // row: chunk j sits at 16-byte slot j ^ ((et >> 1) & 3)), each chunk
+      // one scale block; a byte becomes two bf16 by table, times the
+      // block's power of two (exact).  The first `slots` tiles are decoded
+      // before the previous kernel completes; with the epilogue loading the
+      // activations, that load comes next, then the remaining tiles as the
+      // MMAs free their slots.
+      const int slots = p.a_tmem_tiles;
+      const bool row_ok = n0 + et < p.N;
+      const uint8_t* srow =
+          p.a_scale + ((size_t)l * p.N + (size_t)(row_ok ? n0 + et : 0)) * (size_t)(p.K / 32) + (size_t)kt0 * 4;
+      for (int kt = 0; kt < k_tiles; ++kt) {
+        if (kt == slots && p.b_loader) load_activations();
+        const int slot = kt % slots;
+        const int round = kt / slots;
+        if (round > 0) waiter.wait<false>(bar_slot_empty0 + 8u * slot, (uint32_t)((round - 1) & 1), kRoleEpiDecode, kt);
+        waiter.wait<false>(bar_full0 + 8u * kt, 0u, kRoleEpiDecode, kt);
+        const uint32_t codes = row_ok ? __ldg(reinterpret_cast<const uint32_t*>(srow) + kt) : 0u;
+        const uint32_t row = sA + (uint32_t)kt * kW4TileBytes + (uint32_t)et * kW4RowBytes;
+        const uint32_t t_col = t_row + p.tmem_tile_col0 + (uint32_t)slot * kTmemTileCols;
+#pragma unroll 1
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t sc = (codes >> (8 * j)) & 0xFFu;
+          const uint32_t s2 = (sc << 7) | (sc << 23);         // the bf16 pair 2^(sc-127), 2^(sc-127)
+          uint32_t w[4];
+          dev::ld_shared_v4(row + (uint32_t)((j ^ ((et >> 1) & 3)) * 16), w[0], w[1], w[2], w[3]);
+          uint32_t r[16];
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            const uint32_t byte = (w[q >> 2] >> (8 * (q & 3))) & 0xFFu;
+            r[q] = dev::mul_bf16x2(dev::ld_shared_u32(sTab + 4u * byte), s2);
+          }
+          __syncwarp();   // tcgen05.st is warp-collective
+          dev::tmem_st_x16(t_col + (uint32_t)(j * 16), r);
+        }
+        dev::tmem_wait_st();
+        dev::tc_fence_before();
+        dev::mbar_arrive(bar_slot_full0 + 8u * slot);
+      }
+      if (p.b_loader && k_tiles <= slots) load_activations();
+    } else if (p.b_loader) {
+      load_activations();
     }
 
     waiter.wait<false>(bar_mma_done, 0u, kRoleEpiMma, 0);
@@ -762,7 +869,7 @@ __global__ void __launch_bounds__(kThreads, 3)
 // ---------------------------------------------------------------- host side
 namespace {
 
-template <int MMA_N>
+template <int MMA_N, bool kW4>
 cudaError_t launch_t(const LaunchArgs& la, const CUtensorMap& b_map, const KernelParams& p,
                      cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
@@ -784,12 +891,12 @@ cudaError_t launch_t(const LaunchArgs& la, const CUtensorMap& b_map, const Kerne
   }
   cfg.attrs = attrs;
   cfg.numAttrs = n;
-  return cudaLaunchKernelEx(&cfg, splitk_gemm_bf16_kernel<MMA_N>, b_map, p);
+  return cudaLaunchKernelEx(&cfg, splitk_gemm_bf16_kernel<MMA_N, kW4>, b_map, p);
 }
 
-template <int MMA_N>
+template <int MMA_N, bool kW4>
 cudaError_t prepare_t(int max_dynamic_smem) {
-  return cudaFuncSetAttribute(splitk_gemm_bf16_kernel<MMA_N>,
+  return cudaFuncSetAttribute(splitk_gemm_bf16_kernel<MMA_N, kW4>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, max_dynamic_smem);
 }
 
@@ -797,21 +904,31 @@ cudaError_t prepare_t(int max_dynamic_smem) {
 
 cudaError_t launch_kernel(const LaunchArgs& la, const CUtensorMap& b_map, const KernelParams& p,
                           cudaStream_t stream) {
+  if (la.w4) {
+    // A16W4 weights: decode-sized tiles only
+    switch (la.mma_n) {
+      case 16: return launch_t<16, true>(la, b_map, p, stream);
+      case 32: return launch_t<32, true>(la, b_map, p, stream);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (la.mma_n) {
-    case 16: return launch_t<16>(la, b_map, p, stream);
-    case 32: return launch_t<32>(la, b_map, p, stream);
-    case 64: return launch_t<64>(la, b_map, p, stream);
-    case 128: return launch_t<128>(la, b_map, p, stream);
+    case 16: return launch_t<16, false>(la, b_map, p, stream);
+    case 32: return launch_t<32, false>(la, b_map, p, stream);
+    case 64: return launch_t<64, false>(la, b_map, p, stream);
+    case 128: return launch_t<128, false>(la, b_map, p, stream);
     default: return cudaErrorInvalidValue;
   }
 }
 
 cudaError_t prepare_kernels(int max_dynamic_smem) {
   cudaError_t e;
-  if ((e = prepare_t<16>(max_dynamic_smem)) != cudaSuccess) return e;
-  if ((e = prepare_t<32>(max_dynamic_smem)) != cudaSuccess) return e;
-  if ((e = prepare_t<64>(max_dynamic_smem)) != cudaSuccess) return e;
-  return prepare_t<128>(max_dynamic_smem);
+  if ((e = prepare_t<16, false>(max_dynamic_smem)) != cudaSuccess) return e;
+  if ((e = prepare_t<32, false>(max_dynamic_smem)) != cudaSuccess) return e;
+  if ((e = prepare_t<64, false>(max_dynamic_smem)) != cudaSuccess) return e;
+  if ((e = prepare_t<128, false>(max_dynamic_smem)) != cudaSuccess) return e;
+  if ((e = prepare_t<16, true>(max_dynamic_smem)) != cudaSuccess) return e;
+  return prepare_t<32, true>(max_dynamic_smem);
 }
 
 cudaError_t read_and_clear_fault(int* out_words) {

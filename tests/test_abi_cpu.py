@@ -223,3 +223,33 @@ def test_plan_check_rejects_what_a_launch_would():
     bad.b_resident = 0                                  # staged tiles need resident activations
     assert _check(bad, M, N, K, L) == -10
     assert _check(p, M, N, K + 8, L) == -10             # another shape
+
+
+@pytest.mark.parametrize("args", [(1, 7168, 2048, 1, 4), (16, 4096, 7168, 1, 8), (4, 256, 1024, 1, 0),
+                                  (32, 1000, 4096, 2, 0), (3, 300, 512, 1, 2)])
+def test_w4a16_plans(args):
+    M, N, K, L, split = args
+    p = sk.splitk_plan_w4a16_for(*args, **GB300)
+    assert p.weight_format == sk.WEIGHTS_E2M1_E8M0
+    assert p.stages == p.k_tiles_per_cta <= 8 and p.b_resident == 1 and p.mma_issuers == 1
+    assert 1 <= p.a_tmem_tiles <= 3 and p.mma_n in (16, 32)
+    assert split == 0 or p.split_k == split
+    assert GB300["smem_per_sm"] // (p.smem_bytes + 1024) * p.tmem_cols <= 512
+    assert _check(p, M, N, K, L) == 0
+    bf = sk.Plan.from_buffer_copy(p)
+    bf.weight_format = sk.WEIGHTS_BF16          # an A16W4 layout is no bf16 plan
+    assert _check(bf, M, N, K, L) == -10
+
+
+def test_w4a16_plans_reject_what_the_kernel_cannot_do():
+    with pytest.raises(sk.SplitKError) as e:
+        sk.splitk_plan_w4a16_for(33, 256, 1024, 1, 0, **GB300)      # tiles of more than 32 tokens
+    assert e.value.code == -1
+    with pytest.raises(sk.SplitKError) as e:
+        sk.splitk_plan_w4a16_for(1, 256, 1000, 1, 0, **GB300)      # K not a multiple of 128
+    assert e.value.code == -1
+    with pytest.raises(sk.SplitKError) as e:
+        sk.splitk_plan_w4a16_for(1, 256, 128 * 20, 1, 2, **GB300)  # 10 K tiles per CTA
+    assert e.value.code == -4
+    p = sk.splitk_plan_w4a16_for(1, 256, 128 * 20, 1, 0, **GB300)  # the plan raises the split
+    assert p.k_tiles_per_cta <= 8

@@ -19,7 +19,8 @@ if not torch.cuda.is_available():  # pragma: no cover - CPU-only collection
 import oracle  # noqa: E402
 import split_bf16_gemm_swapped_gb300 as sk  # noqa: E402
 from split_bf16_gemm_swapped_gb300 import synthetic, workloads  # noqa: E402
-from tests._gpu import assert_parity, gemm_gpu, oracle_full, to_dev, to_host  # noqa: E402
+from tests import _tol  # noqa: E402
+from tests._gpu import DEV, assert_parity, gemm_gpu, oracle_full, to_dev, to_host  # noqa: E402
 
 ONE = 0x3F80
 
@@ -375,3 +376,83 @@ def test_thread_loaded_activations_with_ragged_K_and_bias(M, K):
     c0 = gemm_gpu(a, b, plan=p0)
     assert np.array_equal(gemm_gpu(a, b, plan=p1), c0)
     assert_parity(c0, oracle_full(a, b), a, b, K)
+
+
+# --------------------------------------------------------------------------
+# A16W4: 4-bit weights decoded on chip
+# --------------------------------------------------------------------------
+def _w4_draw(L, M, N, K, seed):
+    aq, a_s = synthetic.w4_weights(L, N, K, seed)
+    b = synthetic.normal_bf16((L, M, K), seed, synthetic.STREAM_B, 1.0)
+    return aq, a_s, b
+
+
+def _u8_dev(x):
+    return torch.from_numpy(np.ascontiguousarray(x)).to(DEV)
+
+
+@pytest.mark.parametrize("M,N,K,split", [(1, 300, 1024, 4), (4, 256, 1024, 1), (16, 200, 2048, 8),
+                                         (5, 384, 3072, 4), (32, 256, 1024, 2), (9, 130, 512, 2),
+                                         (17, 300, 896, 1)])
+def test_w4a16_matches_the_oracle(M, N, K, split):
+    L = 2
+    aq, a_s, b = _w4_draw(L, M, N, K, seed=1500 + M + K)
+    tc = sk.splitk_gemm_w4a16(_u8_dev(aq), _u8_dev(a_s), to_dev(b), split_k=split)
+    torch.cuda.synchronize()
+    assert sk.splitk_get_status() == 0, sk.splitk_get_fault()
+    ref = oracle.gemm_w4a16(aq, a_s, b)
+    w = oracle.w4_dequant(aq, a_s)
+    max_w = float(np.max(np.abs(w)))
+    ok, rep = _tol.check(to_host(tc), ref, K, max_w, _tol.max_abs_bf16(b))
+    assert ok, rep
+
+
+@pytest.mark.parametrize("M,split", [(1, 4), (8, 2), (16, 8), (32, 2)])
+def test_w4a16_equals_the_bf16_kernel_on_the_decoded_weights(M, split):
+    """The decoded weights are exact bf16 values, so the A16W4 product equals,
+    bit for bit, the bf16 kernel's on those weights with one MMA issuer (the
+    same products accumulated in the same order)."""
+    L, N, K = 1, 256, 2048
+    aq, a_s, b = _w4_draw(L, M, N, K, seed=1600 + M)
+    wb = np.vectorize(oracle.f64_to_bf16)(oracle.w4_dequant(aq, a_s)).astype(np.uint16)
+    c4 = to_host(sk.splitk_gemm_w4a16(_u8_dev(aq), _u8_dev(a_s), to_dev(b), split_k=split))
+    p = _ring(sk.splitk_plan(M, N, K, L, split), M)
+    cb = gemm_gpu(wb, b, plan=p)
+    assert np.array_equal(c4, cb)
+
+
+def test_w4a16_slot_counts_and_activation_loaders_agree():
+    """1, 2 or 3 TMEM slots (tiles decoded ahead), TMA- or thread-loaded
+    activations, and padded shared memory all give the same bits."""
+    L, M, N, K = 1, 3, 256, 1024 * 4
+    aq, a_s, b = _w4_draw(L, M, N, K, seed=1700)
+    base = sk.splitk_plan_w4a16(M, N, K, L, 4)
+    ta, ts, tb = _u8_dev(aq), _u8_dev(a_s), to_dev(b)
+    outs = []
+    for slots in (1, 2, 3):
+        for loader in (0, 1):
+            p = sk.Plan.from_buffer_copy(base)
+            p.a_tmem_tiles = slots
+            p.tmem_cols = _tmem_cols(p.mma_n, slots, 1)
+            p.b_loader = loader
+            p.smem_bytes = max(p.smem_bytes, 233472 // (512 // p.tmem_cols + 1) + 16) // 16 * 16
+            while 233472 // (p.smem_bytes + 1024) * p.tmem_cols > 512:
+                p.smem_bytes += 16
+            outs.append(to_host(sk.splitk_gemm_w4a16_planned(ta, ts, tb, None, p)))
+            torch.cuda.synchronize()
+            assert sk.splitk_get_status() == 0
+    for o in outs[1:]:
+        assert np.array_equal(o, outs[0])
+    ref = oracle.gemm_w4a16(aq, a_s, b)
+    ok, rep = _tol.check(outs[0], ref, K, float(np.max(np.abs(oracle.w4_dequant(aq, a_s)))), _tol.max_abs_bf16(b))
+    assert ok, rep
+
+
+def test_w4a16_all_ones_closed_form():
+    L, M, N, K = 1, 2, 256, 2048
+    aq = np.full((L, N, K // 2), 0x22, np.uint8)          # every weight 1.0 ...
+    a_s = np.full((L, N, K // 32), 129, np.uint8)         # ... times 4
+    b = np.full((L, M, K), ONE, np.uint16)
+    c = to_host(sk.splitk_gemm_w4a16(_u8_dev(aq), _u8_dev(a_s), to_dev(b), split_k=4))
+    torch.cuda.synchronize()
+    assert np.all(c == oracle.f64_to_bf16(4.0 * K))
