@@ -428,6 +428,74 @@ def run_ours(args, w):
         dist.destroy_process_group()
 
 
+def run_sweep_w4(args):
+    """Extra lines for the A16W4 variant (4-bit E2M1 weights with E8M0 scales
+    per 32 k, bf16 activations) on the decode shapes: HBM TB/s of the bytes
+    it moves (codes, scales, activations, output) and the step time next to
+    the bf16 kernel's on the same shape."""
+    import torch
+
+    import split_bf16_gemm_swapped_gb300 as sk
+    from split_bf16_gemm_swapped_gb300 import synthetic
+    from split_bf16_gemm_swapped_gb300 import workloads as W
+    dev = torch.device("cuda:0")
+    hbm, bf16, bf16s, src = peaks()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+
+    def timed(launch, R):
+        s = torch.cuda.Stream(dev)
+        with torch.cuda.stream(s):
+            for i in range(R + 3):
+                launch(i % R, s)
+        s.synchronize()
+        n = max(R, 240 // R * R)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for i in range(n):
+                launch(i % R, s)
+        with torch.cuda.stream(s):
+            g.replay()
+        s.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 10
+        with torch.cuda.stream(s):
+            e0.record(s)
+            for _ in range(reps):
+                g.replay()
+            e1.record(s)
+        e1.synchronize()
+        return e0.elapsed_time(e1) / (reps * n) * 1e-3
+
+    for w in (W.DECODE_M1, W.DECODE_M16, W.TINY, W.DECODE_M1.with_(M=8), W.DECODE_M1.with_(M=32),
+              W.DECODE_M1.with_(L=8), W.DECODE_M16.with_(L=4)):
+        aq, a_s = synthetic.w4_weights(w.L, w.N, w.K, w.seed)
+        q0 = torch.from_numpy(aq).to(dev)
+        s0 = torch.from_numpy(a_s).to(dev)
+        w4_bytes = w.L * (w.N * w.K // 2 + w.N * w.K // 32 + 2 * w.M * w.K + 2 * w.M * w.N)
+        R = max(2, min(64, math.ceil(4 * l2 / (aq.nbytes + a_s.nbytes))))
+        Qs = [q0] + [q0.clone() for _ in range(R - 1)]
+        Ss = [s0] + [s0.clone() for _ in range(R - 1)]
+        b = to_dev(w.make_b(), dev)
+        c = torch.empty((w.L, w.M, w.N), dtype=torch.bfloat16, device=dev)
+        t4 = timed(lambda i, st: sk.splitk_gemm_w4a16(Qs[i], Ss[i], b, c, split_k=w.split_k, stream=st), R)
+        a0 = to_dev(w.make_a(), dev)
+        Rb = max(2, min(20, math.ceil(4 * l2 / (a0.numel() * 2))))
+        As = [a0] + [a0.clone() for _ in range(Rb - 1)]
+        tb = timed(lambda i, st: sk.splitk_gemm_bf16(As[i], b, c, split_k=w.split_k, stream=st), Rb)
+        p = sk.splitk_plan_w4a16(w.M, w.N, w.K, w.L, w.split_k)
+        print(json.dumps({"sweep": "A16W4 " + describe(w), "us": round(t4 * 1e6, 2),
+                          "TB/s": round(w4_bytes / t4 / 1e12, 3), "bytes_per_call": w4_bytes,
+                          "hbm_frac": round(w4_bytes / t4 / 1e9 / hbm, 3), "peak_source": src,
+                          "bf16_us": round(tb * 1e6, 2), "speedup_vs_bf16": round(tb / t4, 2),
+                          "plan": {k: v for k, v in p.as_dict().items()
+                                   if k in ("mma_n", "split_k", "stages", "a_tmem_tiles", "smem_bytes",
+                                            "ctas_per_sm", "reduce_scatter", "b_loader")}}), flush=True)
+        del Qs, Ss, As, b, c
+        torch.cuda.empty_cache()
+    if sk.splitk_get_status() != 0:
+        raise SystemExit(f"kernel fault during the sweep: {sk.splitk_get_fault()}")
+
+
 def run_sweep(args):
     """Extra lines, one per workload (not the contract line): TB/s, TFLOP/s and
     roofline fraction vs M and split."""
@@ -499,7 +567,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=100)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode_m1")
-    ap.add_argument("--sweep", choices=["sweep", "all"], default=None)
+    ap.add_argument("--sweep", choices=["sweep", "all", "w4a16"], default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--rotate", type=int, default=0,
                     help="weight copies to rotate (default: enough for 4x the L2 cache)")
@@ -515,6 +583,8 @@ def main():
     w = workload_by_name(args.workload)
     if args.impl == "reference":
         run_reference(args, w)
+    elif args.sweep == "w4a16":
+        run_sweep_w4(args)
     elif args.sweep:
         run_sweep(args)
     else:

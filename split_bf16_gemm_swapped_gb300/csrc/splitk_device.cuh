@@ -258,12 +258,22 @@ __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// Two bf16 products, each rounded to nearest even (exact for a power-of-two
-// factor whose result stays in range).
-__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
+// One byte of two E2M1 codes (low nibble = first element) -> two bf16 values
+// times the power of two `scale` (binary32 bits), packed with the first in
+// the low half.  The hardware conversion to f16x2 is exact (E2M1 values are
+// f16 values), widening to f32 is exact, the power-of-two product is exact
+// in range, and the final rounding to bf16 is exact because the value has
+// at most 2 significant bits.
+__device__ __forceinline__ uint32_t e2m1x2_scaled_bf16x2(uint32_t byte, float scale) {
+  uint32_t h2;
+  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(h2) : "r"(byte));
+  float lo, hi;
+  asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(h2));
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi * scale), "f"(lo * scale));
+  return r;
 }
 
 __device__ __forceinline__ void tmem_wait_ld() {

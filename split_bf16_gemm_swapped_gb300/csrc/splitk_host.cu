@@ -77,11 +77,10 @@ uint32_t mailbox_round_bytes(int split, int quads, int ncols_max) {
 
 // Shared memory of an A16W4 plan's layout: all packed weight tiles, all
 // activation tiles (at least 2: rank 0's f32 staging tile reuses them), the
-// mailbox, the barriers and the decode table.
+// mailbox and the barriers.
 size_t smem_bytes_w4(int mma_n, int k_tiles, uint32_t dedicated_mailbox_bytes) {
   return (size_t)kAlignSlack + (size_t)k_tiles * kW4TileBytes +
-         (size_t)std::max(2, k_tiles) * b_stage_bytes(mma_n) + dedicated_mailbox_bytes + kBarRegionBytes +
-         kW4TableBytes;
+         (size_t)std::max(2, k_tiles) * b_stage_bytes(mma_n) + dedicated_mailbox_bytes + kBarRegionBytes;
 }
 
 // Mailbox bytes of a dedicated single-round reduction (rank 0 or scattered).
@@ -285,9 +284,10 @@ int plan_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t smem_
 // The A16W4 plan: decode-sized tiles (mma_n 16 or 32), the split of the bf16
 // planner (raised until a CTA's K slice is at most 8 tiles, all of whose
 // packed codes are loaded at once), min(3, k_tiles) TMEM slots for decoded
-// tiles, resident activations (loaded by the epilogue threads when few), the
-// early trigger, and a dedicated single-round mailbox (scattered from split 4
-// and 16 token columns).  Shared memory is padded when needed so that the
+// tiles (measured: more slots, decoded before the PDL wait, beat more CTAs
+// per SM), resident activations loaded by TMA, the early trigger, and a
+// dedicated single-round mailbox (scattered from split 4 and 16 token
+// columns).  Shared memory is padded when needed so that the
 // CTAs fitting an SM can hold their TMEM.
 int plan_w4_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t smem_per_sm, size_t smem_optin,
                  splitk_plan_t* out) {
@@ -328,7 +328,7 @@ int plan_w4_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t sm
   p.a_tmem_tiles = std::min(kMaxTmemTiles, kt);
   p.mma_issuers = 1;
   p.tmem_cols = tmem_cols_for(mma_n, p.a_tmem_tiles, 1);
-  p.b_loader = ncols_max * kt * (kCtaK / 8) <= 4 * kEpiThreads ? 1 : 0;
+  p.b_loader = 0;             // the epilogue threads are busy decoding (measured: TMA is faster here)
   p.l2_prefetch = 0;
   p.weight_format = SPLITK_WEIGHTS_E2M1_E8M0;
   size_t smem = smem_bytes_w4(mma_n, kt, w4_mailbox_bytes(split, p.reduce_scatter, ncols_max));

@@ -33,11 +33,9 @@ __host__ __device__ constexpr uint32_t b_stage_bytes(int mma_n) { return (uint32
 
 // A16W4 weights: a K tile of 128 rows x 128 four-bit codes is 128 rows of 64
 // bytes (one TMA box, 64-byte swizzle); its 4 scale codes per row (one per 32
-// k) are read by the decoding threads.  The decode table maps a byte (two
-// codes, low nibble first) to the two bf16 values it encodes.
+// k) are read by the decoding threads.
 constexpr uint32_t kW4TileBytes = kMmaM * kCtaK / 2;       // 8 KiB
 constexpr uint32_t kW4RowBytes = kCtaK / 2;                 // 64
-constexpr uint32_t kW4TableBytes = 256 * 4;
 
 // Tensor memory: one accumulator per MMA issuer, max(32, mma_n) columns
 // each, from column 0; weight K tiles staged in tensor memory (64 columns

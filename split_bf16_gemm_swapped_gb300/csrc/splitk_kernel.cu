@@ -151,15 +151,6 @@ __device__ __forceinline__ void load_acc4(uint32_t taddr, uint32_t second, bool 
   }
 }
 
-// One E2M1 code (sign bit 3, exponent bits 2..1 with bias 1, mantissa bit
-// 0) as bf16 bits: exponent e >= 1 gives (1 + m/2) * 2^(e-1), i.e. the bf16
-// exponent field e + 126 with m as the top mantissa bit; e = 0 gives m * 0.5.
-__device__ __forceinline__ uint32_t e2m1_bf16_bits(uint32_t c) {
-  const uint32_t e = (c >> 1) & 3u, m = c & 1u;
-  const uint32_t mag = e != 0u ? (((e + 126u) << 7) | (m << 6)) : (m != 0u ? 0x3F00u : 0u);
-  return ((c & 8u) << 12) | mag;
-}
-
 }  // namespace
 
 template <int MMA_N, bool kW4>
@@ -194,7 +185,7 @@ __global__ void __launch_bounds__(kThreads, 3)
   const int tmem_tiles = p.a_tmem_tiles < k_tiles ? p.a_tmem_tiles : k_tiles;
 
   // Shared memory: [A ring (A16W4: all packed tiles)][B ring or all B tiles]
-  // [dedicated mailbox?][barriers][A16W4: decode table].
+  // [dedicated mailbox?][barriers].
   const uint32_t sA = base;
   const uint32_t sB = sA + (uint32_t)stages * kAStage;
   const uint32_t ring_end = sB + (uint32_t)p.b_region_tiles * kBStage;
@@ -211,7 +202,6 @@ __global__ void __launch_bounds__(kThreads, 3)
   const uint32_t bar_b = bar_mma_done + 40u;             // count 1 + tx bytes (resident B)
   const uint32_t bar_slot_full0 = bar_mma_done + 48u;    // A16W4 [3]: tile decoded into TMEM slot, count 128
   const uint32_t bar_slot_empty0 = bar_mma_done + 72u;   // A16W4 [3]: slot read by the MMAs, count 1
-  const uint32_t sTab = sBar + kBarRegionBytes;          // A16W4 decode table, 256 x u32
 
   const Waiter waiter{slot_abort, p.wait_limit_ns};
 
@@ -265,13 +255,6 @@ __global__ void __launch_bounds__(kThreads, 3)
       // tensor memory.  (Not before: a CTA of the next kernel that took the
       // columns first would wait for this kernel, which would wait for it.)
       if (p.pdl_trigger_early) dev::griddep_launch_dependents();
-    }
-  }
-  if (kW4 && warp >= 4) {
-    // byte -> two bf16 (low nibble = lower k = low half)
-    for (int i = (int)threadIdx.x - 128; i < 256; i += kEpiThreads) {
-      dev::st_shared_u32(sTab + 4u * (uint32_t)i,
-                         e2m1_bf16_bits((uint32_t)i & 15u) | (e2m1_bf16_bits((uint32_t)i >> 4) << 16));
     }
   }
   dev::cluster_arrive_release();
@@ -527,8 +510,9 @@ __global__ void __launch_bounds__(kThreads, 3)
       // A16W4: thread et decodes weight row n0 + et of each K tile into TMEM
       // lane et: 4 chunks of 32 codes (64 B of the tile's 64-byte-swizzled
       // row: chunk j sits at 16-byte slot j ^ ((et >> 1) & 3)), each chunk
-      // one scale block; a byte becomes two bf16 by table, times the
-      // block's power of two (exact).  The first `slots` tiles are decoded
+      // one scale block; a byte becomes two bf16 through the hardware
+      // E2M1 -> f16 conversion and an exact binary32 product with the
+      // block's power of two.  The first `slots` tiles are decoded
       // before the previous kernel completes; with the epilogue loading the
       // activations, that load comes next, then the remaining tiles as the
       // MMAs free their slots.
@@ -547,15 +531,13 @@ __global__ void __launch_bounds__(kThreads, 3)
         const uint32_t t_col = t_row + p.tmem_tile_col0 + (uint32_t)slot * kTmemTileCols;
 #pragma unroll 1
         for (int j = 0; j < 4; ++j) {
-          const uint32_t sc = (codes >> (8 * j)) & 0xFFu;
-          const uint32_t s2 = (sc << 7) | (sc << 23);         // the bf16 pair 2^(sc-127), 2^(sc-127)
+          const float scale = __uint_as_float(((codes >> (8 * j)) & 0xFFu) << 23);   // 2^(code - 127)
           uint32_t w[4];
           dev::ld_shared_v4(row + (uint32_t)((j ^ ((et >> 1) & 3)) * 16), w[0], w[1], w[2], w[3]);
           uint32_t r[16];
 #pragma unroll
           for (int q = 0; q < 16; ++q) {
-            const uint32_t byte = (w[q >> 2] >> (8 * (q & 3))) & 0xFFu;
-            r[q] = dev::mul_bf16x2(dev::ld_shared_u32(sTab + 4u * byte), s2);
+            r[q] = dev::e2m1x2_scaled_bf16x2(w[q >> 2] >> (8 * (q & 3)), scale);
           }
           __syncwarp();   // tcgen05.st is warp-collective
           dev::tmem_st_x16(t_col + (uint32_t)(j * 16), r);
