@@ -83,6 +83,18 @@ __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, uint32_t a
   }
 }
 
+// After a failure: waits, bounded by `limit_ns` and regardless of the CTA's
+// failure flag, for the phase of `bar` with `parity` -- the landing of copies
+// this CTA issued into its own shared memory -- so that it does not leave
+// with a copy still writing there.  Returns whether the phase completed.
+__device__ __noinline__ bool drain_wait(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
+  const uint64_t t0 = dev::globaltimer_ns();
+  while (!dev::mbar_try_wait(bar, parity, 10000u)) {
+    if (dev::globaltimer_ns() - t0 > limit_ns) return false;
+  }
+  return true;
+}
+
 struct Waiter {
   uint32_t abort_flag;            // shared-memory u32, sticky per CTA
   unsigned long long limit_ns;
@@ -213,7 +225,8 @@ __global__ void __launch_bounds__(kThreads, 3)
   // touching shared state.  Warp 0 arrives before issuing its loads: an
   // arrival with release semantics after those issues would hold the whole
   // cluster until the loads have landed.
-  int a_issued = 0;
+  int a_issued = 0;          // weight tiles thread 0 has issued (for the drain after a failure)
+  bool b_issued = false;     // activation tiles issued onto bar_b (resident activations)
   uint64_t a_policy = 0;
   if (warp == 3) {
     if (lane == 0) {
@@ -318,6 +331,7 @@ __global__ void __launch_bounds__(kThreads, 3)
         dev::mbar_arrive_expect_tx(full, kAStageBytes);
         dev::tma_load_3d_hint(dst, p.a_map, k, n0, l, full, a_policy);
         dev::tma_load_3d_hint(dst + kABoxBytes, p.a_map, k + kAtomK, n0, l, full, a_policy);
+        a_issued = kt + 1;
       }
       stamp(p, kTrWeightsIssued);
       if (!p.pdl_trigger_early) dev::griddep_launch_dependents();
@@ -330,6 +344,7 @@ __global__ void __launch_bounds__(kThreads, 3)
       if (b_res && !p.b_loader) {
         // Every activation K tile of this CTA at once, on one barrier.
         dev::mbar_arrive_expect_tx(bar_b, (uint32_t)k_tiles * kBStage);
+        b_issued = true;
         for (int kt = 0; kt < k_tiles; ++kt) {
           const uint32_t dst = sB + (uint32_t)kt * kBStage;
           const int k = (kt0 + kt) * kCtaK;
@@ -818,6 +833,33 @@ __global__ void __launch_bounds__(kThreads, 3)
   }
 
   // ---- teardown
+  if (dev::ld_shared_u32(slot_abort) != 0u) {
+    // A wait failed somewhere in this CTA, so consumers may have stopped
+    // waiting for copies that are still landing in this CTA's shared memory:
+    // let them land (bounded) before the CTA leaves.  For each ring stage
+    // the last round issued is the one to wait for; earlier rounds completed
+    // before the stage was refilled.
+    const unsigned long long drain_ns = 10000000ull;   // 10 ms
+    if (threadIdx.x == 0) {
+      if (kW4) {
+        // one barrier per packed tile, used once
+        for (int kt = 0; kt < a_issued; ++kt) drain_wait(bar_full0 + 8u * kt, 0u, drain_ns);
+      } else {
+        for (int s = 0; s < a_issued && s < stages; ++s) {
+          const int round = (a_issued - 1 - s) / stages;   // of the last tile issued to stage s
+          drain_wait(bar_full0 + 8u * s, (uint32_t)(round & 1), drain_ns);
+        }
+      }
+    }
+    if (warp == 1 && lane == 0 && b_issued) drain_wait(bar_b, 0u, drain_ns);
+    // the peers' partials of a dedicated single-round (or scattered) reduction,
+    // which no final cluster barrier covers
+    const int tq = (((p.M - m0) < MMA_N ? (p.M - m0) : MMA_N) + 3) >> 2;
+    if (threadIdx.x == 128 && split > 1 && p.mailbox_dedicated && tq <= p.mailbox_quads &&
+        (p.reduce_scatter || rank == 0)) {
+      drain_wait(bar_reduce, 0u, drain_ns);
+    }
+  }
   if (warp == 2) {
     waiter.wait<false>(bar_mma_done, 0u, kRoleTmemRelease, 0, 4);
     waiter.wait<false>(bar_tmem_empty, 0u, kRoleTmemRelease, 1, 4);
