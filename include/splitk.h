@@ -155,6 +155,11 @@ typedef struct splitk_plan_t {
                               b_resident = 1, mma_issuers = 1; smem_bytes may
                               exceed the layout's need, which caps how many
                               CTAs share an SM (so the slots fit its TMEM)   */
+    int w4_smem_tiles;     /* A16W4 only: 1 = the one K tile after the TMEM
+                              slots (k_tiles_per_cta = a_tmem_tiles + 1) is
+                              decoded into a 32 KiB bf16 stage in shared
+                              memory, so that every tile is decoded before the
+                              programmatic-dependent-launch wait returns     */
 } splitk_plan_t;
 
 /*

@@ -78,9 +78,10 @@ uint32_t mailbox_round_bytes(int split, int quads, int ncols_max) {
 // Shared memory of an A16W4 plan's layout: all packed weight tiles, all
 // activation tiles (at least 2: rank 0's f32 staging tile reuses them), the
 // mailbox and the barriers.
-size_t smem_bytes_w4(int mma_n, int k_tiles, uint32_t dedicated_mailbox_bytes) {
+size_t smem_bytes_w4(int mma_n, int k_tiles, uint32_t dedicated_mailbox_bytes, int smem_tiles) {
   return (size_t)kAlignSlack + (size_t)k_tiles * kW4TileBytes +
-         (size_t)std::max(2, k_tiles) * b_stage_bytes(mma_n) + dedicated_mailbox_bytes + kBarRegionBytes;
+         (size_t)std::max(2, k_tiles) * b_stage_bytes(mma_n) + (size_t)smem_tiles * kAStageBytes +
+         dedicated_mailbox_bytes + kBarRegionBytes;
 }
 
 // Mailbox bytes of a dedicated single-round reduction (rank 0 or scattered).
@@ -161,6 +162,7 @@ void stage_for_decode(splitk_plan_t* out, int ncols_max, long long ctas, int num
 int plan_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t smem_per_sm,
               size_t smem_optin, splitk_plan_t* out) {
   if (!out) return SPLITK_ERR_NULL;
+  std::memset(out, 0, sizeof(*out));   // fields a bf16 plan does not use stay 0
   if (M < 1 || N < 1 || K < 1 || L < 1) return SPLITK_ERR_INVALID_SHAPE;
   if (split_k != 0 && !valid_split(split_k)) return SPLITK_ERR_UNSUPPORTED_SPLIT;
   if (num_sms < 1 || smem_optin < 1 || smem_per_sm < 1) return SPLITK_ERR_UNSUPPORTED_DEVICE;
@@ -331,7 +333,15 @@ int plan_w4_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t sm
   p.b_loader = 0;             // the epilogue threads are busy decoding (measured: TMA is faster here)
   p.l2_prefetch = 0;
   p.weight_format = SPLITK_WEIGHTS_E2M1_E8M0;
-  size_t smem = smem_bytes_w4(mma_n, kt, w4_mailbox_bytes(split, p.reduce_scatter, ncols_max));
+  const uint32_t ded = w4_mailbox_bytes(split, p.reduce_scatter, ncols_max);
+  // One tile past the TMEM slots: decode it into a bf16 stage in shared
+  // memory, before the PDL wait, if that still fits 2 CTAs per SM
+  // (the single-token decode case: 4 K tiles per CTA, 3 slots).
+  p.w4_smem_tiles = kt == p.a_tmem_tiles + 1 &&
+                            smem_bytes_w4(mma_n, kt, ded, 1) + 1024 <= smem_per_sm / 2
+                        ? 1
+                        : 0;
+  size_t smem = smem_bytes_w4(mma_n, kt, ded, p.w4_smem_tiles);
   const int per_sm_max = std::max(1, (int)(512u / p.tmem_cols));
   if (resident_by_smem(smem_per_sm, smem) > per_sm_max) {
     smem = std::max(smem, (smem_per_sm / (size_t)(per_sm_max + 1) + 16u) & ~(size_t)15u);
@@ -370,8 +380,14 @@ int check_plan_w4(const splitk_plan_t& pl, int M, int N, int K, int L, size_t sm
   if (pl.b_loader != 0 && pl.b_loader != 1) return SPLITK_ERR_BAD_PLAN;
   if (pl.pdl_trigger != 0 && pl.pdl_trigger != 1) return SPLITK_ERR_BAD_PLAN;
   if (pl.tmem_cols != tmem_cols_for(pl.mma_n, pl.a_tmem_tiles, 1)) return SPLITK_ERR_BAD_PLAN;
+  // the bf16 stage takes exactly the tile after the TMEM slots, which are
+  // then each used once (a slot reused after the stage would be waited on a
+  // round it never had)
+  if (pl.w4_smem_tiles != 0 && (pl.w4_smem_tiles != 1 || kt != pl.a_tmem_tiles + 1)) return SPLITK_ERR_BAD_PLAN;
   const uint32_t ded = w4_mailbox_bytes(pl.split_k, pl.reduce_scatter, ncols_max);
-  if (pl.smem_bytes < smem_bytes_w4(pl.mma_n, kt, ded) || pl.smem_bytes % 16 != 0) return SPLITK_ERR_BAD_PLAN;
+  if (pl.smem_bytes < smem_bytes_w4(pl.mma_n, kt, ded, pl.w4_smem_tiles) || pl.smem_bytes % 16 != 0) {
+    return SPLITK_ERR_BAD_PLAN;
+  }
   if (pl.smem_bytes > smem_optin) return SPLITK_ERR_NO_FIT;
   if ((size_t)resident_by_smem(smem_per_sm, pl.smem_bytes) * pl.tmem_cols > 512u) return SPLITK_ERR_BAD_PLAN;
   *dedicated_bytes = ded;
@@ -383,7 +399,7 @@ int check_plan(const splitk_plan_t& pl, int M, int N, int K, int L, size_t smem_
   if (pl.weight_format == SPLITK_WEIGHTS_E2M1_E8M0) {
     return check_plan_w4(pl, M, N, K, L, smem_optin, smem_per_sm, dedicated_bytes);
   }
-  if (pl.weight_format != SPLITK_WEIGHTS_BF16) return SPLITK_ERR_BAD_PLAN;
+  if (pl.weight_format != SPLITK_WEIGHTS_BF16 || pl.w4_smem_tiles != 0) return SPLITK_ERR_BAD_PLAN;
   if (pl.mma_m != kMmaM) return SPLITK_ERR_BAD_PLAN;
   if (pl.mma_n != 16 && pl.mma_n != 32 && pl.mma_n != 64 && pl.mma_n != 128) return SPLITK_ERR_BAD_PLAN;
   if (!valid_split(pl.split_k)) return SPLITK_ERR_UNSUPPORTED_SPLIT;
@@ -673,6 +689,7 @@ void fill_params(const splitk_plan_t& pl, int M, int N, int K, int L, uint32_t d
   p->tmem_tile_col0 = tmem_tile_col0(pl.mma_n, pl.mma_issuers);
   p->mma_issuers = pl.mma_issuers;
   p->b_loader = pl.b_loader;
+  p->w4_smem_tiles = pl.w4_smem_tiles;
   p->l2_prefetch = pl.l2_prefetch;
   p->trace = g_trace.load(std::memory_order_relaxed);
   p->trace_ctas = p->trace ? g_trace_ctas.load(std::memory_order_relaxed) : 0u;

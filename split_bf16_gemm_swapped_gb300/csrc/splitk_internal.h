@@ -97,6 +97,7 @@ struct KernelParams {
   uint32_t tmem_tile_col0;    // TMEM column of the first staged weight tile
   int mma_issuers;            // 1 or 2 threads issuing MMAs (2: even/odd K tiles)
   int b_loader;               // 0: TMA (activation warp); 1: epilogue threads
+  int w4_smem_tiles;          // A16W4: 1 = the tile after the TMEM slots is decoded into a bf16 stage in shared memory
   int l2_prefetch;            // 1: weight tiles not on chip before the PDL wait prefetched to L2
   unsigned long long* trace;  // per-CTA %globaltimer stamps, or null
   unsigned trace_ctas;        // CTAs the trace buffer holds

@@ -200,7 +200,8 @@ __global__ void __launch_bounds__(kThreads, 3)
   // [dedicated mailbox?][barriers].
   const uint32_t sA = base;
   const uint32_t sB = sA + (uint32_t)stages * kAStage;
-  const uint32_t ring_end = sB + (uint32_t)p.b_region_tiles * kBStage;
+  const uint32_t sW4Stage = sB + (uint32_t)p.b_region_tiles * kBStage;   // A16W4 bf16 stage (if any)
+  const uint32_t ring_end = sW4Stage + (kW4 ? (uint32_t)p.w4_smem_tiles * kAStageBytes : 0u);
   const uint32_t sMail = p.mailbox_dedicated ? ring_end : sA;
   const uint32_t sBar = ring_end + (p.mailbox_dedicated ? p.mailbox_bytes : 0u);
   const uint32_t bar_full0 = sBar;                       // [kMaxStages], count 2
@@ -214,6 +215,7 @@ __global__ void __launch_bounds__(kThreads, 3)
   const uint32_t bar_b = bar_mma_done + 40u;             // count 1 + tx bytes (resident B)
   const uint32_t bar_slot_full0 = bar_mma_done + 48u;    // A16W4 [3]: tile decoded into TMEM slot, count 128
   const uint32_t bar_slot_empty0 = bar_mma_done + 72u;   // A16W4 [3]: slot read by the MMAs, count 1
+  const uint32_t bar_w4_stage = bar_mma_done + 96u;      // A16W4: the bf16 stage decoded, count 128
 
   const Waiter waiter{slot_abort, p.wait_limit_ns};
 
@@ -244,6 +246,7 @@ __global__ void __launch_bounds__(kThreads, 3)
           dev::mbar_init(bar_slot_full0 + 8u * i, kEpiThreads);
           dev::mbar_init(bar_slot_empty0 + 8u * i, 1);
         }
+        dev::mbar_init(bar_w4_stage, kEpiThreads);
       }
       dev::st_shared_u32(slot_abort, 0u);
       dev::fence_barrier_init();
@@ -382,13 +385,28 @@ __global__ void __launch_bounds__(kThreads, 3)
       bool ok = waiter.wait<false>(bar_b, 0u, kRoleMma, -1);
       dev::tc_fence_after();
       for (int kt = 0; kt < k_tiles && ok; ++kt) {
+        const uint32_t b_st = sB + (uint32_t)kt * kBStage;
+        if (p.w4_smem_tiles && kt == slots) {
+          // the tile decoded into the bf16 stage in shared memory
+          ok = waiter.wait<false>(bar_w4_stage, 0u, kRoleMma, kt);
+          if (!ok) break;
+          dev::tc_fence_after();
+          if (kt == k_tiles - 1) stamp(p, kTrLastFull);
+#pragma unroll
+          for (int kk = 0; kk < kCtaK / kMmaK; ++kk) {
+            const uint32_t a_off = (uint32_t)(kk >> 2) * kABoxBytes + (uint32_t)(kk & 3) * 32u;
+            const uint32_t b_off = (uint32_t)(kk >> 2) * kBBox + (uint32_t)(kk & 3) * 32u;
+            dev::mma_bf16(tmem_base, dev::smem_desc_sw128(sW4Stage + a_off), dev::smem_desc_sw128(b_st + b_off),
+                          kIdesc, (kt | kk) != 0 ? 1u : 0u);
+          }
+          continue;
+        }
         const int slot = kt % slots;
         ok = waiter.wait<false>(bar_slot_full0 + 8u * slot, (uint32_t)((kt / slots) & 1), kRoleMma, kt);
         if (!ok) break;
         dev::tc_fence_after();
         if (kt == 0) stamp(p, kTrFirstFull);
         if (kt == k_tiles - 1) stamp(p, kTrLastFull);
-        const uint32_t b_st = sB + (uint32_t)kt * kBStage;
         const uint32_t t_col = tmem_base + p.tmem_tile_col0 + (uint32_t)slot * kTmemTileCols;
 #pragma unroll
         for (int kk = 0; kk < kCtaK / kMmaK; ++kk) {
@@ -536,7 +554,38 @@ __global__ void __launch_bounds__(kThreads, 3)
       const uint8_t* srow =
           p.a_scale + ((size_t)l * p.N + (size_t)(row_ok ? n0 + et : 0)) * (size_t)(p.K / 32) + (size_t)kt0 * 4;
       for (int kt = 0; kt < k_tiles; ++kt) {
-        if (kt == slots && p.b_loader) load_activations();
+        if (kt == slots && p.b_loader && !p.w4_smem_tiles) load_activations();
+        if (p.w4_smem_tiles && kt == slots) {
+          // the tile after the TMEM slots: decoded before the wait into a bf16
+          // stage in the 128-byte-swizzled layout (two boxes of 64 k; 16-byte
+          // chunk c of row r of an 8-row atom at chunk c ^ (r % 8)), read by
+          // the MMA from shared memory
+          waiter.wait<false>(bar_full0 + 8u * kt, 0u, kRoleEpiDecode, kt);
+          const uint32_t codes = row_ok ? __ldg(reinterpret_cast<const uint32_t*>(srow) + kt) : 0u;
+          const uint32_t row = sA + (uint32_t)kt * kW4TileBytes + (uint32_t)et * kW4RowBytes;
+          const uint32_t atom = sW4Stage + (uint32_t)(et >> 3) * 1024u + (uint32_t)(et & 7) * 128u;
+#pragma unroll 1
+          for (int j = 0; j < 4; ++j) {
+            const float scale = __uint_as_float(((codes >> (8 * j)) & 0xFFu) << 23);
+            uint32_t w[4];
+            dev::ld_shared_v4(row + (uint32_t)((j ^ ((et >> 1) & 3)) * 16), w[0], w[1], w[2], w[3]);
+            uint32_t r[16];
+#pragma unroll
+            for (int q = 0; q < 16; ++q) r[q] = dev::e2m1x2_scaled_bf16x2(w[q >> 2] >> (8 * (q & 3)), scale);
+            // k = 32 j .. 32 j + 31: box j / 2, chunks 4 (j % 2) .. + 3
+            const uint32_t box = atom + (uint32_t)(j >> 1) * kABoxBytes;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const int chunk = 4 * (j & 1) + c;
+              dev::st_shared_v4(box + (uint32_t)((chunk ^ (et & 7)) * 16), r[4 * c], r[4 * c + 1], r[4 * c + 2],
+                                r[4 * c + 3]);
+            }
+          }
+          dev::fence_proxy_async_shared();   // generic-proxy stores, read by tcgen05.mma
+          dev::mbar_arrive(bar_w4_stage);
+          if (p.b_loader) load_activations();   // the stage is the last tile
+          continue;
+        }
         const int slot = kt % slots;
         const int round = kt / slots;
         if (round > 0) waiter.wait<false>(bar_slot_empty0 + 8u * slot, (uint32_t)((round - 1) & 1), kRoleEpiDecode, kt);

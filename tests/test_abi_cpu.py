@@ -209,6 +209,20 @@ def test_candidates_are_valid_distinct_and_start_with_the_plan(args):
         assert any(p.reduce_scatter for p in cands)
 
 
+def test_the_planner_writes_every_field():
+    """A plan written over stale memory is the same plan (the one-shot GEMM
+    calls plan into an uninitialised struct on the stack)."""
+    import ctypes
+    for args in [(1, 7168, 2048, 1, 4), (16, 4096, 7168, 1, 8), (3, 200, 1000, 2, 0)]:
+        stale = sk.Plan()
+        ctypes.memset(ctypes.byref(stale), 0xA5, ctypes.sizeof(stale))
+        rc = sk.load_library().splitk_plan_for(*args, GB300["num_sms"], GB300["smem_per_sm"],
+                                               GB300["smem_per_block_optin"], ctypes.byref(stale))
+        assert rc == 0
+        assert bytes(stale) == bytes(_plan(*args))
+        assert _check(stale, *args[:4]) == 0
+
+
 def test_plan_check_rejects_what_a_launch_would():
     M, N, K, L = 1, 7168, 2048, 1
     p = _plan(M, N, K, L, 4)
@@ -221,6 +235,10 @@ def test_plan_check_rejects_what_a_launch_would():
     assert _check(bad, M, N, K, L) == -10
     bad = sk.Plan.from_buffer_copy(p)
     bad.b_resident = 0                                  # staged tiles need resident activations
+    assert _check(bad, M, N, K, L) == -10
+    bad = sk.Plan.from_buffer_copy(p)
+    bad.w4_smem_tiles = 1                               # a bf16 stage of decoded 4-bit weights
+    bad.smem_bytes += 32768
     assert _check(bad, M, N, K, L) == -10
     assert _check(p, M, N, K + 8, L) == -10             # another shape
 
@@ -239,6 +257,16 @@ def test_w4a16_plans(args):
     bf = sk.Plan.from_buffer_copy(p)
     bf.weight_format = sk.WEIGHTS_BF16          # an A16W4 layout is no bf16 plan
     assert _check(bf, M, N, K, L) == -10
+    # the bf16 stage takes the one tile after the TMEM slots, and only that
+    assert p.w4_smem_tiles == (1 if p.k_tiles_per_cta == p.a_tmem_tiles + 1 and M <= 16 else 0)
+    st = sk.Plan.from_buffer_copy(p)
+    st.w4_smem_tiles = 1 - p.w4_smem_tiles
+    st.smem_bytes += 32768
+    assert _check(st, M, N, K, L) == (0 if p.k_tiles_per_cta == p.a_tmem_tiles + 1 else -10)
+    if p.w4_smem_tiles:
+        small = sk.Plan.from_buffer_copy(p)
+        small.smem_bytes -= 32768               # no room for the stage
+        assert _check(small, M, N, K, L) == -10
 
 
 def test_w4a16_plans_reject_what_the_kernel_cannot_do():

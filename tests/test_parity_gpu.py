@@ -407,7 +407,7 @@ def test_w4a16_matches_the_oracle(M, N, K, split):
     assert ok, rep
 
 
-@pytest.mark.parametrize("M,split", [(1, 4), (8, 2), (16, 8), (32, 2)])
+@pytest.mark.parametrize("M,split", [(1, 4), (8, 2), (8, 4), (16, 8), (32, 2)])
 def test_w4a16_equals_the_bf16_kernel_on_the_decoded_weights(M, split):
     """The decoded weights are exact bf16 values, so the A16W4 product equals,
     bit for bit, the bf16 kernel's on those weights with one MMA issuer (the
@@ -421,26 +421,42 @@ def test_w4a16_equals_the_bf16_kernel_on_the_decoded_weights(M, split):
     assert np.array_equal(c4, cb)
 
 
-def test_w4a16_slot_counts_and_activation_loaders_agree():
-    """1, 2 or 3 TMEM slots (tiles decoded ahead), TMA- or thread-loaded
-    activations, and padded shared memory all give the same bits."""
-    L, M, N, K = 1, 3, 256, 1024 * 4
-    aq, a_s, b = _w4_draw(L, M, N, K, seed=1700)
+def _w4_variant(base, slots, stage, loader):
+    """`base` with `slots` TMEM slots, the bf16 shared-memory stage on or
+    off and the given activation loader; shared memory grown for the stage
+    and padded until the slots of the CTAs sharing an SM fit its TMEM."""
+    p = sk.Plan.from_buffer_copy(base)
+    p.a_tmem_tiles = slots
+    p.tmem_cols = _tmem_cols(p.mma_n, slots, 1)
+    p.b_loader = loader
+    p.smem_bytes += max(0, stage - base.w4_smem_tiles) * 32768
+    p.w4_smem_tiles = stage
+    p.smem_bytes = max(p.smem_bytes, 233472 // (512 // p.tmem_cols + 1) + 16) // 16 * 16
+    while 233472 // (p.smem_bytes + 1024) * p.tmem_cols > 512:
+        p.smem_bytes += 16
+    return p
+
+
+@pytest.mark.parametrize("M,K,variants", [
+    (3, 1024 * 4, [(s, 0, ld) for s in (1, 2, 3) for ld in (0, 1)]),
+    (3, 512 * 4, [(s, st, ld) for s, st in ((3, 1), (3, 0), (2, 0), (1, 0)) for ld in (0, 1)]),
+    (1, 256 * 4, [(s, st, ld) for s, st in ((1, 1), (1, 0), (2, 0)) for ld in (0, 1)]),
+])
+def test_w4a16_slot_counts_and_activation_loaders_agree(M, K, variants):
+    """1, 2 or 3 TMEM slots (tiles decoded ahead), the last tile decoded into
+    a bf16 stage in shared memory or into a reused slot, TMA- or
+    thread-loaded activations, and padded shared memory all give the same
+    bits."""
+    L, N = 1, 256
+    aq, a_s, b = _w4_draw(L, M, N, K, seed=1700 + K)
     base = sk.splitk_plan_w4a16(M, N, K, L, 4)
     ta, ts, tb = _u8_dev(aq), _u8_dev(a_s), to_dev(b)
     outs = []
-    for slots in (1, 2, 3):
-        for loader in (0, 1):
-            p = sk.Plan.from_buffer_copy(base)
-            p.a_tmem_tiles = slots
-            p.tmem_cols = _tmem_cols(p.mma_n, slots, 1)
-            p.b_loader = loader
-            p.smem_bytes = max(p.smem_bytes, 233472 // (512 // p.tmem_cols + 1) + 16) // 16 * 16
-            while 233472 // (p.smem_bytes + 1024) * p.tmem_cols > 512:
-                p.smem_bytes += 16
-            outs.append(to_host(sk.splitk_gemm_w4a16_planned(ta, ts, tb, None, p)))
-            torch.cuda.synchronize()
-            assert sk.splitk_get_status() == 0
+    for slots, stage, loader in variants:
+        p = _w4_variant(base, slots, stage, loader)
+        outs.append(to_host(sk.splitk_gemm_w4a16_planned(ta, ts, tb, None, p)))
+        torch.cuda.synchronize()
+        assert sk.splitk_get_status() == 0
     for o in outs[1:]:
         assert np.array_equal(o, outs[0])
     ref = oracle.gemm_w4a16(aq, a_s, b)
