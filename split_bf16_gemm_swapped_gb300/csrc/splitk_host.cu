@@ -328,8 +328,10 @@ int plan_w4_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t sm
   p.reduce_scatter = split >= 4 && ncols_max >= 16 ? 1 : 0;
   p.b_resident = 1;
   p.a_tmem_tiles = std::min(kMaxTmemTiles, kt);
-  p.mma_issuers = 1;
-  p.tmem_cols = tmem_cols_for(mma_n, p.a_tmem_tiles, 1);
+  // two MMA issuers (even and odd K tiles into two accumulators) where
+  // there are two slots: a lone issuer's tcgen05.mma stream is issue-bound
+  p.mma_issuers = p.a_tmem_tiles >= 2 ? 2 : 1;
+  p.tmem_cols = tmem_cols_for(mma_n, p.a_tmem_tiles, p.mma_issuers);
   p.b_loader = 0;             // the epilogue threads are busy decoding (measured: TMA is faster here)
   p.l2_prefetch = 0;
   p.weight_format = SPLITK_WEIGHTS_E2M1_E8M0;
@@ -375,11 +377,16 @@ int check_plan_w4(const splitk_plan_t& pl, int M, int N, int K, int L, size_t sm
   const int ncols_max = std::min(M, pl.mma_n);
   if (pl.split_k > 1 && (!pl.mailbox_dedicated || pl.mailbox_quads != (ncols_max + 3) / 4)) return SPLITK_ERR_BAD_PLAN;
   if (pl.reduce_scatter != 0 && (pl.reduce_scatter != 1 || pl.split_k < 2)) return SPLITK_ERR_BAD_PLAN;
-  if (pl.b_resident != 1 || pl.mma_issuers != 1 || pl.l2_prefetch != 0) return SPLITK_ERR_BAD_PLAN;
+  if (pl.b_resident != 1 || pl.l2_prefetch != 0) return SPLITK_ERR_BAD_PLAN;
   if (pl.a_tmem_tiles < 1 || pl.a_tmem_tiles > kMaxTmemTiles) return SPLITK_ERR_BAD_PLAN;
+  // An issuer waits on a slot's next round only after its own previous tile
+  // (nis tiles back) is full, which orders it after the slot's previous
+  // round when the slots are at least as many as the issuers; otherwise a
+  // phase-parity wait could return a round early.
+  if (pl.mma_issuers < 1 || pl.mma_issuers > 2 || pl.mma_issuers > pl.a_tmem_tiles) return SPLITK_ERR_BAD_PLAN;
   if (pl.b_loader != 0 && pl.b_loader != 1) return SPLITK_ERR_BAD_PLAN;
   if (pl.pdl_trigger != 0 && pl.pdl_trigger != 1) return SPLITK_ERR_BAD_PLAN;
-  if (pl.tmem_cols != tmem_cols_for(pl.mma_n, pl.a_tmem_tiles, 1)) return SPLITK_ERR_BAD_PLAN;
+  if (pl.tmem_cols != tmem_cols_for(pl.mma_n, pl.a_tmem_tiles, pl.mma_issuers)) return SPLITK_ERR_BAD_PLAN;
   // the bf16 stage takes exactly the tile after the TMEM slots, which are
   // then each used once (a slot reused after the stage would be waited on a
   // round it never had)

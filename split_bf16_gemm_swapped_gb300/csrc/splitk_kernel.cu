@@ -378,13 +378,18 @@ __global__ void __launch_bounds__(kThreads, 3)
     // adds the two.
     const int issuer = warp - 2;
     const int nis = p.mma_issuers;
-    if (kW4 && lane == 0 && issuer == 0) {
+    if (kW4 && lane == 0 && issuer < nis) {
       // A16W4: the epilogue threads decode each weight tile into a TMEM slot
-      // (tile kt in slot kt % slots); the MMAs read A from there.
+      // (tile kt in slot kt % slots); the MMAs read A from there.  Issuer i
+      // takes tiles i, i + nis, ... into its own accumulator.  The decoders
+      // finish tiles in order, so an issuer that saw tile kt - nis full also
+      // saw every earlier round of tile kt's slot complete (nis <= slots).
       const int slots = p.a_tmem_tiles;
+      const uint32_t d_acc = tmem_base + (uint32_t)issuer * kAccCols;
       bool ok = waiter.wait<false>(bar_b, 0u, kRoleMma, -1);
       dev::tc_fence_after();
-      for (int kt = 0; kt < k_tiles && ok; ++kt) {
+      for (int kt = issuer; kt < k_tiles && ok; kt += nis) {
+        const uint32_t first = (uint32_t)(kt >= nis);          // 0: this accumulator's first tile
         const uint32_t b_st = sB + (uint32_t)kt * kBStage;
         if (p.w4_smem_tiles && kt == slots) {
           // the tile decoded into the bf16 stage in shared memory
@@ -396,8 +401,8 @@ __global__ void __launch_bounds__(kThreads, 3)
           for (int kk = 0; kk < kCtaK / kMmaK; ++kk) {
             const uint32_t a_off = (uint32_t)(kk >> 2) * kABoxBytes + (uint32_t)(kk & 3) * 32u;
             const uint32_t b_off = (uint32_t)(kk >> 2) * kBBox + (uint32_t)(kk & 3) * 32u;
-            dev::mma_bf16(tmem_base, dev::smem_desc_sw128(sW4Stage + a_off), dev::smem_desc_sw128(b_st + b_off),
-                          kIdesc, (kt | kk) != 0 ? 1u : 0u);
+            dev::mma_bf16(d_acc, dev::smem_desc_sw128(sW4Stage + a_off), dev::smem_desc_sw128(b_st + b_off),
+                          kIdesc, (first | (uint32_t)kk) != 0u ? 1u : 0u);
           }
           continue;
         }
@@ -411,8 +416,8 @@ __global__ void __launch_bounds__(kThreads, 3)
 #pragma unroll
         for (int kk = 0; kk < kCtaK / kMmaK; ++kk) {
           const uint32_t b_off = (uint32_t)(kk >> 2) * kBBox + (uint32_t)(kk & 3) * 32u;
-          dev::mma_bf16_ts(tmem_base, t_col + (uint32_t)kk * 8u, dev::smem_desc_sw128(b_st + b_off), kIdesc,
-                           (kt | kk) != 0 ? 1u : 0u);
+          dev::mma_bf16_ts(d_acc, t_col + (uint32_t)kk * 8u, dev::smem_desc_sw128(b_st + b_off), kIdesc,
+                           (first | (uint32_t)kk) != 0u ? 1u : 0u);
         }
         dev::mma_commit(bar_slot_empty0 + 8u * slot);   // slot free once these MMAs have read it
       }

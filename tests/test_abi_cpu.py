@@ -249,7 +249,8 @@ def test_w4a16_plans(args):
     M, N, K, L, split = args
     p = sk.splitk_plan_w4a16_for(*args, **GB300)
     assert p.weight_format == sk.WEIGHTS_E2M1_E8M0
-    assert p.stages == p.k_tiles_per_cta <= 8 and p.b_resident == 1 and p.mma_issuers == 1
+    assert p.stages == p.k_tiles_per_cta <= 8 and p.b_resident == 1
+    assert p.mma_issuers == (2 if p.a_tmem_tiles >= 2 else 1)
     assert 1 <= p.a_tmem_tiles <= 3 and p.mma_n in (16, 32)
     assert split == 0 or p.split_k == split
     assert GB300["smem_per_sm"] // (p.smem_bytes + 1024) * p.tmem_cols <= 512
@@ -257,6 +258,14 @@ def test_w4a16_plans(args):
     bf = sk.Plan.from_buffer_copy(p)
     bf.weight_format = sk.WEIGHTS_BF16          # an A16W4 layout is no bf16 plan
     assert _check(bf, M, N, K, L) == -10
+    if p.mma_issuers == 2:
+        one = sk.Plan.from_buffer_copy(p)
+        one.mma_issuers = 1                     # one issuer fits the same TMEM columns
+        assert _check(one, M, N, K, L) == 0
+        few = sk.Plan.from_buffer_copy(p)
+        few.a_tmem_tiles = 1                    # two issuers need two slots
+        few.tmem_cols = 128
+        assert _check(few, M, N, K, L) == -10
     # the bf16 stage takes the one tile after the TMEM slots, and only that
     assert p.w4_smem_tiles == (1 if p.k_tiles_per_cta == p.a_tmem_tiles + 1 and M <= 16 else 0)
     st = sk.Plan.from_buffer_copy(p)

@@ -410,24 +410,34 @@ def test_w4a16_matches_the_oracle(M, N, K, split):
 @pytest.mark.parametrize("M,split", [(1, 4), (8, 2), (8, 4), (16, 8), (32, 2)])
 def test_w4a16_equals_the_bf16_kernel_on_the_decoded_weights(M, split):
     """The decoded weights are exact bf16 values, so the A16W4 product equals,
-    bit for bit, the bf16 kernel's on those weights with one MMA issuer (the
-    same products accumulated in the same order)."""
+    bit for bit, the bf16 kernel's on those weights with as many MMA issuers
+    (the same products accumulated in the same order: with two, the even and
+    odd K tiles in two accumulators added at the end)."""
     L, N, K = 1, 256, 2048
     aq, a_s, b = _w4_draw(L, M, N, K, seed=1600 + M)
     wb = np.vectorize(oracle.f64_to_bf16)(oracle.w4_dequant(aq, a_s)).astype(np.uint16)
-    c4 = to_host(sk.splitk_gemm_w4a16(_u8_dev(aq), _u8_dev(a_s), to_dev(b), split_k=split))
-    p = _ring(sk.splitk_plan(M, N, K, L, split), M)
-    cb = gemm_gpu(wb, b, plan=p)
-    assert np.array_equal(c4, cb)
+    ta, ts, tb = _u8_dev(aq), _u8_dev(a_s), to_dev(b)
+    w4 = sk.splitk_plan_w4a16(M, N, K, L, split)
+    for issuers in (1, 2):
+        if issuers > w4.a_tmem_tiles:
+            continue
+        p4 = sk.Plan.from_buffer_copy(w4)
+        p4.mma_issuers = issuers
+        p4.tmem_cols = _tmem_cols(p4.mma_n, p4.a_tmem_tiles, issuers)
+        c4 = to_host(sk.splitk_gemm_w4a16_planned(ta, ts, tb, None, p4))
+        cb = gemm_gpu(wb, b, plan=_bf16_plan_like(p4, M, N, K, L, split))
+        assert np.array_equal(c4, cb), issuers
 
 
-def _w4_variant(base, slots, stage, loader):
+def _w4_variant(base, slots, stage, loader, issuers=1):
     """`base` with `slots` TMEM slots, the bf16 shared-memory stage on or
-    off and the given activation loader; shared memory grown for the stage
-    and padded until the slots of the CTAs sharing an SM fit its TMEM."""
+    off, the given activation loader and MMA issuers; shared memory grown
+    for the stage and padded until the slots of the CTAs sharing an SM fit
+    its TMEM."""
     p = sk.Plan.from_buffer_copy(base)
     p.a_tmem_tiles = slots
-    p.tmem_cols = _tmem_cols(p.mma_n, slots, 1)
+    p.mma_issuers = issuers
+    p.tmem_cols = _tmem_cols(p.mma_n, slots, issuers)
     p.b_loader = loader
     p.smem_bytes += max(0, stage - base.w4_smem_tiles) * 32768
     p.w4_smem_tiles = stage
@@ -438,30 +448,108 @@ def _w4_variant(base, slots, stage, loader):
 
 
 @pytest.mark.parametrize("M,K,variants", [
-    (3, 1024 * 4, [(s, 0, ld) for s in (1, 2, 3) for ld in (0, 1)]),
-    (3, 512 * 4, [(s, st, ld) for s, st in ((3, 1), (3, 0), (2, 0), (1, 0)) for ld in (0, 1)]),
-    (1, 256 * 4, [(s, st, ld) for s, st in ((1, 1), (1, 0), (2, 0)) for ld in (0, 1)]),
+    (3, 1024 * 4, [(s, 0, ld, i) for s in (1, 2, 3) for ld in (0, 1) for i in (1, 2) if i <= s]),
+    (3, 512 * 4, [(s, st, ld, i) for s, st in ((3, 1), (3, 0), (2, 0), (1, 0)) for ld in (0, 1) for i in (1, 2)
+                  if i <= s]),
+    (1, 256 * 4, [(s, st, ld, i) for s, st in ((1, 1), (1, 0), (2, 0)) for ld in (0, 1) for i in (1, 2) if i <= s]),
 ])
 def test_w4a16_slot_counts_and_activation_loaders_agree(M, K, variants):
     """1, 2 or 3 TMEM slots (tiles decoded ahead), the last tile decoded into
     a bf16 stage in shared memory or into a reused slot, TMA- or
     thread-loaded activations, and padded shared memory all give the same
-    bits."""
+    bits for a given number of MMA issuers (one or two accumulators)."""
     L, N = 1, 256
     aq, a_s, b = _w4_draw(L, M, N, K, seed=1700 + K)
     base = sk.splitk_plan_w4a16(M, N, K, L, 4)
     ta, ts, tb = _u8_dev(aq), _u8_dev(a_s), to_dev(b)
-    outs = []
-    for slots, stage, loader in variants:
-        p = _w4_variant(base, slots, stage, loader)
-        outs.append(to_host(sk.splitk_gemm_w4a16_planned(ta, ts, tb, None, p)))
+    outs = {1: [], 2: []}
+    for slots, stage, loader, issuers in variants:
+        p = _w4_variant(base, slots, stage, loader, issuers)
+        for _ in range(3):                 # repeated: a race shows as a difference
+            outs[issuers].append(to_host(sk.splitk_gemm_w4a16_planned(ta, ts, tb, None, p)))
         torch.cuda.synchronize()
         assert sk.splitk_get_status() == 0
-    for o in outs[1:]:
-        assert np.array_equal(o, outs[0])
     ref = oracle.gemm_w4a16(aq, a_s, b)
-    ok, rep = _tol.check(outs[0], ref, K, float(np.max(np.abs(oracle.w4_dequant(aq, a_s)))), _tol.max_abs_bf16(b))
-    assert ok, rep
+    max_w = float(np.max(np.abs(oracle.w4_dequant(aq, a_s))))
+    for group in outs.values():
+        for o in group[1:]:
+            assert np.array_equal(o, group[0])
+        if group:
+            ok, rep = _tol.check(group[0], ref, K, max_w, _tol.max_abs_bf16(b))
+            assert ok, rep
+
+
+def test_w4a16_one_hot_activations_read_out_every_decoded_weight():
+    """With one-hot activations (token m reads k = 32 m + o), C[m][n] is the
+    decoded weight w(n, 32 m + o) itself; 32 offsets read out every weight of
+    a shape holding all 16 codes and scale codes 2..252 (2 is the smallest
+    whose products stay normal), compared bit for bit with the oracle's exact
+    dequantisation."""
+    L, M, N, K = 1, 32, 256, 1024
+    rng = np.random.default_rng(1800)
+    aq = rng.integers(0, 256, size=(L, N, K // 2), dtype=np.uint8)
+    a_s = rng.integers(2, 253, size=(L, N, K // 32), dtype=np.uint8)
+    a_s[0, :, 0] = 2
+    a_s[0, :, 1] = 127
+    a_s[0, :, 3] = 252                     # largest documented code
+    want = np.vectorize(oracle.f64_to_bf16)(oracle.w4_dequant(aq, a_s)).astype(np.uint16)
+    want[want == 0x8000] = 0               # a sum holding +0 terms reads a -0 weight as +0
+    ta, ts = _u8_dev(aq), _u8_dev(a_s)
+    for o in range(32):
+        b = np.zeros((L, M, K), np.uint16)
+        b[0, np.arange(M), 32 * np.arange(M) + o] = ONE
+        c = to_host(sk.splitk_gemm_w4a16(ta, ts, to_dev(b), split_k=2))
+        assert np.array_equal(c[0], want[0][:, 32 * np.arange(M) + o].T), o
+    torch.cuda.synchronize()
+    assert sk.splitk_get_status() == 0
+
+
+def _bf16_plan_like(w4, M, N, K, L, split):
+    """A bf16 plan accumulating like the A16W4 plan `w4`: the page's ring with
+    one issuer, or with two (even and odd K tiles in two accumulators)."""
+    ring = _ring(sk.splitk_plan(M, N, K, L, split), M)
+    if w4.mma_issuers == 1:
+        return ring
+    pb = _staged(ring, 2, 0, issuers=2, M=M) or _staged(ring, 4, 0, issuers=2, M=M)
+    assert pb is not None
+    return pb
+
+
+def test_w4a16_extreme_scales_equal_the_bf16_kernel():
+    """Scale codes from 1 (products of 0.5 that are bf16 subnormals) to 252,
+    small activations keeping the sums finite: the A16W4 GEMM equals the bf16
+    kernel on the exactly dequantised weights, bit for bit."""
+    L, M, N, K, split = 1, 4, 256, 2048, 4
+    rng = np.random.default_rng(1900)
+    aq = rng.integers(0, 256, size=(L, N, K // 2), dtype=np.uint8)
+    codes = np.array([1, 2, 100, 127, 142, 143, 200, 252], np.uint8)
+    a_s = codes[rng.integers(0, len(codes), size=(L, N, K // 32))]
+    b = synthetic.normal_bf16((L, M, K), 1900, synthetic.STREAM_B, 2.0 ** -20)
+    wb = np.vectorize(oracle.f64_to_bf16)(oracle.w4_dequant(aq, a_s)).astype(np.uint16)
+    w4 = sk.splitk_plan_w4a16(M, N, K, L, split)
+    c4 = to_host(sk.splitk_gemm_w4a16_planned(_u8_dev(aq), _u8_dev(a_s), to_dev(b), None, w4))
+    cb = gemm_gpu(wb, b, plan=_bf16_plan_like(w4, M, N, K, L, split))
+    assert np.array_equal(c4, cb)
+
+
+def test_w4a16_activations_of_any_magnitude_equal_the_bf16_kernel():
+    """Tokens of 2^100, of 2^-100, beyond f16's range, and one spanning 30
+    binades: the A16W4 GEMM equals the bf16 kernel on the dequantised
+    weights, bit for bit (every product normal in both)."""
+    L, M, N, K, split = 1, 5, 256, 2048, 4
+    aq, a_s, _ = _w4_draw(L, M, N, K, seed=1950)
+    rng = np.random.default_rng(1950)
+    vals = rng.standard_normal((L, M, K))
+    vals[0, 0] *= 2.0 ** 100
+    vals[0, 1] *= 2.0 ** -100
+    vals[0, 2] *= 1e6
+    vals[0, 3] *= np.exp2(rng.integers(-10, 20, size=K))
+    b = np.vectorize(oracle.f64_to_bf16)(vals).astype(np.uint16)
+    wb = np.vectorize(oracle.f64_to_bf16)(oracle.w4_dequant(aq, a_s)).astype(np.uint16)
+    w4 = sk.splitk_plan_w4a16(M, N, K, L, split)
+    c4 = to_host(sk.splitk_gemm_w4a16_planned(_u8_dev(aq), _u8_dev(a_s), to_dev(b), None, w4))
+    cb = gemm_gpu(wb, b, plan=_bf16_plan_like(w4, M, N, K, L, split))
+    assert np.array_equal(c4, cb)
 
 
 def test_w4a16_all_ones_closed_form():
