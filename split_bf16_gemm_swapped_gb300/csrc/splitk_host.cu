@@ -126,14 +126,14 @@ int auto_split(int T, long long tiles, int num_sms, int mma_n) {
 // widths); and the early trigger.  Measured on GB300 (back to back, weights
 // rotated past L2): single-token decode 7.1 -> 5.8 us, small-batch decode
 // 12.0 -> 11.8 us.  `ded` is the mailbox region the ring plan chose.
-void stage_for_decode(splitk_plan_t* out, int ncols_max, long long ctas, int num_sms, size_t smem_per_sm,
+bool stage_for_decode(splitk_plan_t* out, int ncols_max, long long ctas, int num_sms, size_t smem_per_sm,
                       size_t smem_optin, uint32_t ded) {
   const int kt = out->k_tiles_per_cta;
-  if (out->mma_n > 32 || kt < 2 || ctas > 2LL * num_sms) return;
+  if (out->mma_n > 32 || kt < 2 || ctas > 2LL * num_sms) return false;
   // an aliased mailbox round must fit the 2-stage ring
   if (!out->reduce_scatter && out->split_k > 1 && !out->mailbox_dedicated &&
       mailbox_round_bytes(out->split_k, out->mailbox_quads, ncols_max) > 2u * kAStageBytes) {
-    return;
+    return false;
   }
   // All of them when the ring holds them anyway (2 tiles: measured faster),
   // else as many as leave the 2 ring stages to the tiles after them.
@@ -141,7 +141,7 @@ void stage_for_decode(splitk_plan_t* out, int ncols_max, long long ctas, int num
   const uint32_t cols = tmem_cols_for(out->mma_n, tiles, 2);
   const size_t smem = smem_bytes_for(out->mma_n, 2, ded, b_region_tiles_for(2, 1, kt));
   const size_t budget = std::min(smem_optin, smem_per_sm / 2 - 1024);
-  if (smem > budget || (size_t)resident_by_smem(smem_per_sm, smem) * cols > 512u) return;
+  if (smem > budget || (size_t)resident_by_smem(smem_per_sm, smem) * cols > 512u) return false;
   out->stages = 2;
   out->b_resident = 1;
   out->a_tmem_tiles = tiles;
@@ -157,6 +157,7 @@ void stage_for_decode(splitk_plan_t* out, int ncols_max, long long ctas, int num
   // Tiles that stay off chip until the wait go to L2 at CTA start
   // (small-batch decode: 11.6 -> 11.1 us).
   out->l2_prefetch = kt > 2 + tiles ? 1 : 0;
+  return true;
 }
 
 int plan_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t smem_per_sm,
@@ -192,7 +193,6 @@ int plan_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t smem_
   const uint32_t ded_bytes =
       split > 1 ? mailbox_round_bytes(split, nquads_max, ncols_max) : 0u;
   const bool prefer_dedicated = split > 1 && ded_bytes <= 16u * 1024u;
-  const int stages_cap = std::min(kMaxStages, std::max(2, std::min(k_tiles, 4)));
 
   // Scattered reduction (each rank sums 128/split rows) moves 1/split of the
   // DSMEM bytes into each SM; measured on GB300 it wins from split 4 and 16
@@ -201,84 +201,103 @@ int plan_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t smem_
   const bool try_scatter = split >= 4 && ncols_max >= 16;
   const uint32_t scatter_bytes = (uint32_t)ncols_max * kColumnBytes;
 
+  // A ring plan: `stages` deep, mailbox `mode` (2 scattered, 1 dedicated,
+  // 0 aliased on rank 0's drained ring, or none without a split).
+  auto fill = [&](int stages, int mode, int per_sm_v, int issuers) {
+    // Aliased: one round when the partials fit the drained ring, else rounds
+    // of whole 16-column groups (4 quads; at least one group always fits a
+    // 2-stage ring).
+    int quads = nquads_max;
+    if (split > 1 && mode == 0 && mailbox_round_bytes(split, quads, ncols_max) > (uint32_t)stages * kAStageBytes) {
+      quads = 4;
+      while (mailbox_round_bytes(split, quads + 4, ncols_max) <= (uint32_t)stages * kAStageBytes) quads += 4;
+    }
+    const uint32_t ded = mode == 2 ? scatter_bytes : mode == 1 ? ded_bytes : 0u;
+    out->mma_m = kMmaM;
+    out->mma_n = mma_n;
+    out->stages = stages;
+    out->split_k = split;
+    out->k_tiles_per_cta = k_tiles;
+    out->mailbox_dedicated = split > 1 && mode != 0 ? 1 : 0;
+    out->mailbox_quads = quads;
+    out->reduce_rounds = split > 1 ? (nquads_max + quads - 1) / quads : 0;
+    out->grid[0] = (unsigned)(split * m_tiles);
+    out->grid[1] = (unsigned)n_tiles;
+    out->grid[2] = (unsigned)L;
+    out->cluster[0] = (unsigned)split;
+    out->cluster[1] = 1;
+    out->cluster[2] = 1;
+    out->smem_bytes = smem_bytes_for(mma_n, stages, ded, stages);
+    out->ctas_per_sm = per_sm_v;
+    out->pdl_trigger = 0;
+    out->reduce_scatter = mode == 2 ? 1 : 0;
+    out->b_resident = 0;
+    out->a_tmem_tiles = 0;
+    out->mma_issuers = issuers;
+    out->tmem_cols = tmem_cols_for(mma_n, 0, issuers);
+    out->b_loader = 0;
+    out->l2_prefetch = 0;
+    out->weight_format = SPLITK_WEIGHTS_BF16;
+    return ded;
+  };
+  const int split_mode = split == 1 ? 0 : try_scatter ? 2 : prefer_dedicated ? 1 : 0;
+
+  // Short K slices of narrow tiles: the staged decode tactic
+  // (stage_for_decode), with the mailbox measured best for it: scattered from
+  // 16 token columns and split 4, else a dedicated one when small.
+  {
+    const uint32_t ded = fill(2, split_mode, 2, 1);
+    if (stage_for_decode(out, ncols_max, ctas, num_sms, smem_per_sm, smem_optin, ded)) return SPLITK_OK;
+  }
+
   for (; per_sm >= 1; --per_sm) {
     const size_t budget = std::min(smem_optin, smem_per_sm / (size_t)per_sm - 1024);
-    if (try_scatter) {
-      for (int stages = stages_cap; stages >= 2; --stages) {
-        const size_t smem = smem_bytes_for(mma_n, stages, scatter_bytes, stages);
-        if (smem > budget) continue;
-        out->mma_m = kMmaM;
-        out->mma_n = mma_n;
-        out->stages = stages;
-        out->split_k = split;
-        out->k_tiles_per_cta = k_tiles;
-        out->mailbox_dedicated = 1;
-        out->mailbox_quads = nquads_max;
-        out->reduce_rounds = 1;
-        out->grid[0] = (unsigned)(split * m_tiles);
-        out->grid[1] = (unsigned)n_tiles;
-        out->grid[2] = (unsigned)L;
-        out->cluster[0] = (unsigned)split;
-        out->cluster[1] = 1;
-        out->cluster[2] = 1;
-        out->smem_bytes = smem;
-        out->ctas_per_sm = per_sm;
-        out->pdl_trigger = 0;
-        out->reduce_scatter = 1;
-        out->b_resident = 0;
-        out->a_tmem_tiles = 0;
-        out->tmem_cols = tmem_cols_for(mma_n, 0, 1);
-        out->mma_issuers = 1;
-        out->b_loader = 0;
-        out->l2_prefetch = 0;
-        out->weight_format = SPLITK_WEIGHTS_BF16;
-        stage_for_decode(out, ncols_max, ctas, num_sms, smem_per_sm, smem_optin, scatter_bytes);
-        return SPLITK_OK;
-      }
-    }
-    for (int stages = stages_cap; stages >= 2; --stages) {
-      const uint32_t ded = prefer_dedicated ? ded_bytes : 0u;
-      const size_t smem = smem_bytes_for(mma_n, stages, ded, stages);
-      if (smem > budget) continue;
-      // One round when the partials fit, else rounds of whole 16-column
-      // groups (4 quads; at least one group always fits a 2-stage ring).
-      int quads = nquads_max;
-      if (split > 1 && !prefer_dedicated &&
-          mailbox_round_bytes(split, quads, ncols_max) > (uint32_t)stages * kAStageBytes) {
-        quads = 4;
-        while (mailbox_round_bytes(split, quads + 4, ncols_max) <= (uint32_t)stages * kAStageBytes) {
-          quads += 4;
+    // A CTA alone on its SM (a grid of at most one CTA per SM) keeps as many
+    // weight tiles in flight as its shared memory holds, with two MMA issuers
+    // on an even ring where one issuer's tcgen05.mma stream is issue-bound
+    // (mma_n <= 64).  Measured on GB300, the split-1 sweep (112 CTAs, K 16384):
+    // M=1 0.86 -> 0.95 of the HBM copy bandwidth with 6 stages, M=16
+    // 0.85 -> 0.92, M=64 0.85 -> 0.88 (4 stages, all that fit).
+    const bool deep = per_sm == 1 && ctas <= num_sms;
+    const bool deep_two = deep && mma_n <= 64;
+    const int stages_cap = std::min(kMaxStages, std::max(2, deep ? k_tiles : std::min(k_tiles, 4)));
+    // Mailbox modes in order of preference (measured on the decode shapes):
+    // scattered, dedicated, aliased.  On short K slices the first mode that
+    // fits at any depth wins; on long ones (32 K tiles a CTA and more) the
+    // deepest ring does, with the first mode that fits at that depth: a stage
+    // more in flight outweighs the mailbox placement there (K = 16384 sweep
+    // at 2 CTAs/SM: M=8, split 2 0.93 -> 0.99 and M=16, split 4 0.91 -> 0.93
+    // of the HBM copy bandwidth with 3 aliased stages instead of 2 with
+    // their own mailbox).
+    int modes[3];
+    int n_modes = 0;
+    if (split_mode == 2) modes[n_modes++] = 2;
+    if (split > 1 && prefer_dedicated) modes[n_modes++] = 1;
+    modes[n_modes++] = 0;
+    auto fits = [&](int mode, int stages) {
+      if (deep_two && stages % 2 != 0) return false;
+      const uint32_t ded = mode == 2 ? scatter_bytes : mode == 1 ? ded_bytes : 0u;
+      return smem_bytes_for(mma_n, stages, ded, stages) <= budget;
+    };
+    auto choose = [&](bool depth_first) {
+      for (int i = 0; i < (depth_first ? stages_cap - 1 : n_modes); ++i) {
+        for (int j = 0; j < (depth_first ? n_modes : stages_cap - 1); ++j) {
+          const int stages = stages_cap - (depth_first ? i : j);
+          const int mode = modes[depth_first ? j : i];
+          if (!fits(mode, stages)) continue;
+          // ... but not into an aliased mailbox that needs more than one
+          // reduction round (M=128, split 4: 0.55 -> 0.52 that way)
+          if (depth_first && mode == 0 && split > 1 && mode != modes[0] &&
+              mailbox_round_bytes(split, nquads_max, ncols_max) > (uint32_t)stages * kAStageBytes) {
+            continue;
+          }
+          fill(stages, mode, per_sm, deep_two ? 2 : 1);
+          return true;
         }
       }
-      out->mma_m = kMmaM;
-      out->mma_n = mma_n;
-      out->stages = stages;
-      out->split_k = split;
-      out->k_tiles_per_cta = k_tiles;
-      out->mailbox_dedicated = prefer_dedicated ? 1 : 0;
-      out->mailbox_quads = quads;
-      out->reduce_rounds = split > 1 ? (nquads_max + quads - 1) / quads : 0;
-      out->grid[0] = (unsigned)(split * m_tiles);
-      out->grid[1] = (unsigned)n_tiles;
-      out->grid[2] = (unsigned)L;
-      out->cluster[0] = (unsigned)split;
-      out->cluster[1] = 1;
-      out->cluster[2] = 1;
-      out->smem_bytes = smem;
-      out->ctas_per_sm = per_sm;
-      out->pdl_trigger = 0;
-      out->reduce_scatter = 0;
-      out->b_resident = 0;
-      out->a_tmem_tiles = 0;
-      out->tmem_cols = tmem_cols_for(mma_n, 0, 1);
-      out->mma_issuers = 1;
-      out->b_loader = 0;
-      out->l2_prefetch = 0;
-      out->weight_format = SPLITK_WEIGHTS_BF16;
-      stage_for_decode(out, ncols_max, ctas, num_sms, smem_per_sm, smem_optin,
-                       prefer_dedicated ? mailbox_round_bytes(split, quads, ncols_max) : 0u);
-      return SPLITK_OK;
-    }
+      return false;
+    };
+    if ((k_tiles >= 32 && choose(true)) || choose(false)) return SPLITK_OK;
   }
   return SPLITK_ERR_NO_FIT;
 }
@@ -781,7 +800,7 @@ int enumerate_plans(int M, int N, int K, int L, int split_k, int num_sms, size_t
       if (split == 1 && mode != 0) continue;
       if (mode == 2 && ncols_max < 4) continue;
       for (int b_res = 0; b_res <= 1; ++b_res) {
-        for (int stages = 2; stages <= (b_res ? 2 : 4); ++stages) {
+        for (int stages = 2; stages <= (b_res ? 2 : kMaxStages); ++stages) {
           if (stages > std::max(2, kt)) continue;
           for (int tiles = 0; tiles <= (b_res ? std::min(kMaxTmemTiles, kt) : 0); ++tiles) {
             for (int issuers = 1; issuers <= 2; ++issuers) {

@@ -209,6 +209,37 @@ def test_candidates_are_valid_distinct_and_start_with_the_plan(args):
         assert any(p.reduce_scatter for p in cands)
 
 
+def test_a_cta_alone_on_its_sm_gets_a_deep_ring_and_two_issuers():
+    """Grids of at most one CTA per SM (the split-1 sweep: 112 CTAs) keep as
+    many weight tiles in flight as shared memory holds, on an even ring with
+    two MMA issuers where mma_n <= 64; fuller grids keep the shallow ring."""
+    p = _plan(1, 7168, 16384, 2, 1)
+    assert (p.stages, p.mma_issuers, p.ctas_per_sm) == (6, 2, 1)
+    assert p.smem_bytes <= GB300["smem_per_block_optin"]
+    assert _check(p, 1, 7168, 16384, 2) == 0
+    p = _plan(64, 7168, 16384, 2, 1)
+    assert (p.stages, p.mma_issuers) == (4, 2)
+    p = _plan(128, 7168, 16384, 2, 1)                   # mma_n 128: one issuer
+    assert p.mma_issuers == 1
+    p = _plan(1, 7168, 16384, 2, 2)                     # 224 CTAs share SMs
+    assert p.stages <= 4 and p.ctas_per_sm == 2
+
+
+def test_long_k_slices_prefer_a_deeper_ring_over_their_own_mailbox():
+    """32 K tiles a CTA and more: 3 ring stages with the mailbox aliased on the
+    drained ring beat 2 with a dedicated or scattered one at 2 CTAs/SM; not
+    when the aliased partials would need more than one reduction round, and
+    not on short slices."""
+    for M, split in ((8, 2), (16, 2), (16, 4)):
+        p = _plan(M, 7168, 16384, 2, split)
+        assert (p.stages, p.mailbox_dedicated, p.reduce_scatter, p.reduce_rounds, p.ctas_per_sm) == (3, 0, 0, 1, 2)
+        assert _check(p, M, 7168, 16384, 2) == 0
+    p = _plan(128, 7168, 16384, 2, 4)                   # 96 KB of partials: keep the scattered mailbox
+    assert (p.stages, p.reduce_scatter) == (2, 1)
+    p = _plan(8, 7168, 4096, 4, 2)                      # 16 K tiles a CTA: the dedicated mailbox stays
+    assert (p.stages, p.mailbox_dedicated) == (2, 1)
+
+
 def test_the_planner_writes_every_field():
     """A plan written over stale memory is the same plan (the one-shot GEMM
     calls plan into an uninitialised struct on the stack)."""
