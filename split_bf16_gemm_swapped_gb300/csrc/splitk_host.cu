@@ -263,12 +263,12 @@ int plan_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t smem_
     const int stages_cap = std::min(kMaxStages, std::max(2, deep ? k_tiles : std::min(k_tiles, 4)));
     // Mailbox modes in order of preference (measured on the decode shapes):
     // scattered, dedicated, aliased.  On short K slices the first mode that
-    // fits at any depth wins; on long ones (32 K tiles a CTA and more) the
+    // fits at any depth wins; on long ones (16 K tiles a CTA and more) the
     // deepest ring does, with the first mode that fits at that depth: a stage
     // more in flight outweighs the mailbox placement there (K = 16384 sweep
-    // at 2 CTAs/SM: M=8, split 2 0.93 -> 0.99 and M=16, split 4 0.91 -> 0.93
-    // of the HBM copy bandwidth with 3 aliased stages instead of 2 with
-    // their own mailbox).
+    // at 2 CTAs/SM: M=8, split 2 0.93 -> 0.99, M=16, split 4 0.91 -> 0.93 and
+    // M=2, split 8 0.87 -> 0.92 of the HBM copy bandwidth with 3 aliased
+    // stages instead of 2 with their own mailbox).
     int modes[3];
     int n_modes = 0;
     if (split_mode == 2) modes[n_modes++] = 2;
@@ -297,7 +297,7 @@ int plan_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t smem_
       }
       return false;
     };
-    if ((k_tiles >= 32 && choose(true)) || choose(false)) return SPLITK_OK;
+    if ((k_tiles >= 16 && choose(true)) || choose(false)) return SPLITK_OK;
   }
   return SPLITK_ERR_NO_FIT;
 }

@@ -226,7 +226,7 @@ def test_a_cta_alone_on_its_sm_gets_a_deep_ring_and_two_issuers():
 
 
 def test_long_k_slices_prefer_a_deeper_ring_over_their_own_mailbox():
-    """32 K tiles a CTA and more: 3 ring stages with the mailbox aliased on the
+    """16 K tiles a CTA and more: 3 ring stages with the mailbox aliased on the
     drained ring beat 2 with a dedicated or scattered one at 2 CTAs/SM; not
     when the aliased partials would need more than one reduction round, and
     not on short slices."""
@@ -236,7 +236,9 @@ def test_long_k_slices_prefer_a_deeper_ring_over_their_own_mailbox():
         assert _check(p, M, 7168, 16384, 2) == 0
     p = _plan(128, 7168, 16384, 2, 4)                   # 96 KB of partials: keep the scattered mailbox
     assert (p.stages, p.reduce_scatter) == (2, 1)
-    p = _plan(8, 7168, 4096, 4, 2)                      # 16 K tiles a CTA: the dedicated mailbox stays
+    p = _plan(2, 7168, 16384, 2, 8)                     # 16 K tiles a CTA
+    assert (p.stages, p.mailbox_dedicated) == (3, 0)
+    p = _plan(8, 7168, 2048, 4, 2)                      # 8 K tiles a CTA: the dedicated mailbox stays
     assert (p.stages, p.mailbox_dedicated) == (2, 1)
 
 
