@@ -202,7 +202,7 @@ def cpu_oracle_rate(w, budget_s: float, threads: int):
         _, used = oracle.gemm_threaded(a_s, b, threads)
         elapsed += time.perf_counter() - t0
         reps += 1
-        if elapsed >= budget_s * 0.5 or reps >= 1000:
+        if elapsed >= budget_s or reps >= 100000:
             break
     sample_bytes = 2 * w.L * (n * w.K + w.M * w.K + w.M * n)
     rate = sample_bytes * reps / elapsed / 1e12
