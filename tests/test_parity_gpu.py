@@ -47,6 +47,24 @@ def test_every_split_and_token_tail(split, M):
     assert_parity(c, oracle_full(a, b), a, b, K)
 
 
+@pytest.mark.parametrize("M,N,K,L,split,kind", [
+    (3, 300, 8192, 1, 1, (6, 2, 0, 1)),     # CTAs alone on their SMs: 6 stages, two issuers
+    (5, 1000, 4096, 8, 2, (6, 2, 1, 1)),    # the same with a dedicated mailbox
+    (8, 2560, 4096, 8, 2, (3, 1, 0, 2)),    # 16 K tiles a CTA: 3 stages, mailbox aliased on the ring
+    (16, 1280, 8192, 4, 4, (3, 1, 0, 2)),
+])
+def test_deep_rings_and_depth_first_mailboxes(M, N, K, L, split, kind):
+    """The plans of grids of lone CTAs (deep even rings, two issuers) and of
+    long K slices at 2 CTAs/SM (a third stage before a mailbox of their own)
+    against the oracle."""
+    p = sk.splitk_plan(M, N, K, L, split)
+    assert (p.stages, p.mma_issuers, p.mailbox_dedicated, p.ctas_per_sm) == kind
+    a, b = _draw(L, M, N, K, seed=2100 + M)
+    c = gemm_gpu(a, b, split_k=split)
+    assert_parity(c, oracle_full(a, b), a, b, K)
+    assert np.array_equal(c, gemm_gpu(a, b, plan=p))
+
+
 @pytest.mark.parametrize("split", [1, 4])
 def test_batched_L_and_ragged_N(split):
     L, M, N, K = 3, 7, 200, 2048
