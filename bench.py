@@ -384,22 +384,69 @@ def run_ours(args, w):
         b_pin = torch.from_numpy(b_host.view(np.int16)).view(torch.bfloat16).pin_memory()
         c_pin = torch.empty((w.L, w.M, w.N), dtype=torch.bfloat16).pin_memory()
         n_e2e = min(args.steps, args.e2e_steps)
-        with torch.cuda.stream(stream):
-            for i in range(min(args.warmup, 10)):
-                sk.splitk_gemm_bf16_hostio(As[i % R], b_pin, c_pin, b, c, w.split_k, stream)
-            stream.synchronize()
+
+        def timed_calls(call, graph_steps):
+            """ms per call: eager (one host call per step), or captured in a
+            CUDA graph of `graph_steps` calls (how a decode loop issues them)."""
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for i in range(n_e2e):
-                sk.splitk_gemm_bf16_hostio(As[i % R], b_pin, c_pin, b, c, w.split_k, stream)
-            e1.record(stream)
-            e1.synchronize()
-        e2e_ms = e0.elapsed_time(e1) / n_e2e
-        e2e = {"value": world * w.bytes / (e2e_ms * 1e-3) / 1e12, "unit": "TB/s",
+            with torch.cuda.stream(stream):
+                for i in range(min(args.warmup, 10)):
+                    call(i)
+                stream.synchronize()
+                if graph_steps == 0:
+                    e0.record(stream)
+                    for i in range(n_e2e):
+                        call(i)
+                    e1.record(stream)
+                    e1.synchronize()
+                    return e0.elapsed_time(e1) / n_e2e, n_e2e
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    for i in range(graph_steps):
+                        call(i)
+                g.replay()
+                stream.synchronize()
+                reps = max(1, n_e2e // graph_steps)
+                e0.record(stream)
+                for _ in range(reps):
+                    g.replay()
+                e1.record(stream)
+                e1.synchronize()
+                return e0.elapsed_time(e1) / (reps * graph_steps), reps * graph_steps
+
+        def copies(i):      # copy engines: b_pin -> b, GEMM, c -> c_pin
+            sk.splitk_gemm_bf16_hostio(As[i % R], b_pin, c_pin, b, c, w.split_k, stream)
+
+        def zero_copy(i):   # the kernel reads b_pin and writes c_pin itself
+            sk.splitk_gemm_bf16_zerocopy(As[i % R], b_pin, c_pin, w.split_k, stream)
+
+        G = 50
+        copy_eager_ms, _ = timed_calls(copies, 0)
+        try:
+            zero_copy(0)
+            zc = True
+        except sk.SplitKError:
+            zc = False      # shape without thread-loaded activations
+        stream.synchronize()
+        if zc:
+            zc_eager_ms, _ = timed_calls(zero_copy, 0)
+            e2e_ms, steps_e2e = timed_calls(zero_copy, G)
+        else:
+            e2e_ms, steps_e2e = timed_calls(copies, G)
+        tbps = lambda ms: world * w.bytes / (ms * 1e-3) / 1e12
+        e2e = {"value": tbps(e2e_ms), "unit": "TB/s",
                "h2d_bytes_per_step": int(b_host.nbytes), "d2h_bytes_per_step": int(w.L * w.M * w.N * 2),
-               "steps": n_e2e, "ms_per_step": e2e_ms,
-               "note": "weights resident; activations copied in and the output copied out every step"}
+               "steps": steps_e2e, "ms_per_step": e2e_ms,
+               "path": "splitk_gemm_bf16_zerocopy" if zc else "splitk_gemm_bf16_hostio",
+               "copy_engine_eager_ms_per_step": copy_eager_ms,
+               "zero_copy_eager_ms_per_step": zc_eager_ms if zc else None,
+               "note": ("weights resident in HBM; every step the activations cross from pinned host memory "
+                        "and the output back to pinned host memory; value: "
+                        + ("the kernel loads and stores them itself (splitk_gemm_bf16_zerocopy), "
+                           if zc else "copy engines around the kernel (splitk_gemm_bf16_hostio), ")
+                        + f"calls captured in a CUDA graph of {G} steps; *_eager_*: one host call per step, "
+                        "copy_engine: splitk_gemm_bf16_hostio")}
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:

@@ -80,7 +80,10 @@ enum splitk_status {
     SPLITK_ERR_BAD_PLAN = -10,
     /* splitk_gemm_bf16_noalloc(): the call needs more scratch than its
        static array holds. */
-    SPLITK_ERR_SCRATCH = -11
+    SPLITK_ERR_SCRATCH = -11,
+    /* splitk_gemm_bf16_zerocopy(): a host buffer is not page-locked and
+       mapped into the device address space. */
+    SPLITK_ERR_NOT_MAPPED = -12
 };
 
 /* Flags of splitk_gemm_bf16_planned(). */
@@ -301,6 +304,24 @@ SPLITK_API int splitk_gemm_bf16_hostio(const void *a, const void *b_host,
                                        void *c_host, void *b_dev, void *c_dev,
                                        int M, int N, int K, int L, int split_k,
                                        splitk_stream_t stream);
+
+/*
+ * End-to-end call without copy engines: the GEMM reads the activations
+ * straight from pinned host memory `b_host` (B[L][M][K] bf16) and writes C
+ * straight into pinned host memory `c_host` (C[L][M][N] bf16), both through
+ * their device mappings (on a coherent CPU-GPU link, the epilogue threads'
+ * loads and stores cross it within the kernel).  Both buffers must be
+ * page-locked and mapped into the device address space (cudaHostAlloc /
+ * cudaMallocHost, or registered with cudaHostRegister and the mapped flag):
+ * otherwise SPLITK_ERR_NOT_MAPPED, with nothing enqueued.  Only plans whose
+ * activations the epilogue threads load (the staged decode tactic: narrow
+ * tiles, short K slices) can do this; other shapes return
+ * SPLITK_ERR_NO_FIT (use splitk_gemm_bf16_hostio).  The caller synchronizes
+ * `stream` before reading c_host and keeps b_host unchanged until then.
+ */
+SPLITK_API int splitk_gemm_bf16_zerocopy(const void *a, const void *b_host, void *c_host,
+                                         int M, int N, int K, int L, int split_k,
+                                         splitk_stream_t stream);
 
 /*
  * splitk_gemm_bf16() for callers that must not allocate device memory.

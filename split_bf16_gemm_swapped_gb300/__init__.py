@@ -22,7 +22,8 @@ from . import _build
 __all__ = [
     "SplitKError", "Plan", "Fault", "library_path", "load_library",
     "splitk_plan", "splitk_plan_for", "splitk_gemm_bf16", "splitk_gemm_bf16_planned",
-    "splitk_gemm_bf16_hostio", "splitk_gemm_bf16_noalloc", "splitk_gemm_bf16_bias",
+    "splitk_gemm_bf16_hostio", "splitk_gemm_bf16_zerocopy", "splitk_gemm_bf16_noalloc",
+    "splitk_gemm_bf16_bias",
     "splitk_plan_check_for", "splitk_plan_candidates_for", "splitk_tune",
     "splitk_plan_w4a16", "splitk_plan_w4a16_for", "splitk_gemm_w4a16", "splitk_gemm_w4a16_planned",
     "splitk_get_fault",
@@ -41,7 +42,7 @@ STATUS = {
     -3: "SPLITK_ERR_UNSUPPORTED_SPLIT", -4: "SPLITK_ERR_NO_FIT", -5: "SPLITK_ERR_CUDA",
     -6: "SPLITK_ERR_TIMEOUT", -7: "SPLITK_ERR_NULL", -8: "SPLITK_ERR_CACHE_FULL",
     -9: "SPLITK_ERR_UNSUPPORTED_DEVICE", -10: "SPLITK_ERR_BAD_PLAN",
-    -11: "SPLITK_ERR_SCRATCH",
+    -11: "SPLITK_ERR_SCRATCH", -12: "SPLITK_ERR_NOT_MAPPED",
 }
 
 
@@ -135,6 +136,8 @@ def load_library():
     lib.splitk_gemm_bf16_planned.restype = i
     lib.splitk_gemm_bf16_hostio.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, vp]
     lib.splitk_gemm_bf16_hostio.restype = i
+    lib.splitk_gemm_bf16_zerocopy.argtypes = [vp, vp, vp, i, i, i, i, i, vp]
+    lib.splitk_gemm_bf16_zerocopy.restype = i
     lib.splitk_gemm_bf16_noalloc.argtypes = [vp, vp, vp, i, i, i, i, i, vp]
     lib.splitk_gemm_bf16_noalloc.restype = i
     lib.splitk_get_fault.argtypes = [ctypes.POINTER(Fault)]
@@ -409,6 +412,35 @@ def splitk_gemm_bf16_hostio(a, b_host, c_host, b_dev, c_dev, split_k: int = 0, s
             a.data_ptr(), b_host.data_ptr(), c_host.data_ptr(), b_dev.data_ptr(),
             c_dev.data_ptr(), M, N, K, L, int(split_k), _stream_handle(stream, a.device))
     _check(rc, "splitk_gemm_bf16_hostio")
+    return c_host
+
+
+def splitk_gemm_bf16_zerocopy(a, b_host, c_host, split_k: int = 0, stream=None):
+    """c_host = b_host @ a^T with the activations read from, and the output
+    written to, pinned host memory by the kernel itself (no copy engines);
+    returns c_host.  Synchronize the stream before reading it."""
+    import torch
+    if b_host.is_cuda or c_host.is_cuda:
+        raise ValueError("b_host and c_host must be host tensors")
+    _require_cuda(a)
+    if a.dtype != torch.bfloat16 or b_host.dtype != torch.bfloat16 or c_host.dtype != torch.bfloat16:
+        raise TypeError("a, b_host and c_host must be bfloat16")
+    if a.dim() != b_host.dim() or a.dim() not in (2, 3) or not (a.is_contiguous() and b_host.is_contiguous()
+                                                                and c_host.is_contiguous()):
+        raise ValueError("a and b_host must be contiguous [N, K] and [M, K] (or batched [L, ...])")
+    a3 = a if a.dim() == 3 else a.unsqueeze(0)
+    b3 = b_host if b_host.dim() == 3 else b_host.unsqueeze(0)
+    L, N, K = a3.shape
+    if b3.shape[0] != L or b3.shape[2] != K:
+        raise ValueError("a and b_host disagree on L or K")
+    M = b3.shape[1]
+    if c_host.numel() != L * M * N:
+        raise ValueError("c_host must hold L * M * N values")
+    with torch.cuda.device(a.device):
+        rc = load_library().splitk_gemm_bf16_zerocopy(
+            a.data_ptr(), b_host.data_ptr(), c_host.data_ptr(), M, N, K, L, int(split_k),
+            _stream_handle(stream, a.device))
+    _check(rc, "splitk_gemm_bf16_zerocopy")
     return c_host
 
 

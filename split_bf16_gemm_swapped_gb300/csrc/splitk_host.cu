@@ -949,6 +949,39 @@ SPLITK_API int splitk_gemm_bf16_hostio(const void* a, const void* b_host, void* 
   return SPLITK_OK;
 }
 
+// The device address of page-locked, device-mapped host memory, or null.
+void* mapped_device_pointer(const void* host) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, host) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (at.type != cudaMemoryTypeHost || at.devicePointer == nullptr) return nullptr;
+  return at.devicePointer;
+}
+
+SPLITK_API int splitk_gemm_bf16_zerocopy(const void* a, const void* b_host, void* c_host, int M, int N, int K,
+                                         int L, int split_k, splitk_stream_t stream) {
+  if (!a || !b_host || !c_host) return SPLITK_ERR_NULL;
+  if (M < 1 || N < 1 || K < 1 || L < 1) return SPLITK_ERR_INVALID_SHAPE;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* st = nullptr;
+  int rc = current_device(&st, nullptr);
+  if (rc != SPLITK_OK) return rc;
+  void* b_dev = mapped_device_pointer(b_host);
+  void* c_dev = mapped_device_pointer(c_host);
+  if (!b_dev || !c_dev) return SPLITK_ERR_NOT_MAPPED;
+  rc = check_pointers(a, b_dev, c_dev);
+  if (rc != SPLITK_OK) return rc;
+  splitk_plan_t pl;
+  rc = plan_impl(M, N, K, L, split_k, st->num_sms, st->smem_per_sm, st->smem_optin, &pl);
+  if (rc != SPLITK_OK) return rc;
+  // the epilogue threads' loads read the host memory; TMA is not used on it
+  if (!pl.b_resident) return SPLITK_ERR_NO_FIT;
+  pl.b_loader = 1;
+  return launch_locked(*st, a, b_dev, c_dev, M, N, K, L, pl, 0u, reinterpret_cast<cudaStream_t>(stream));
+}
+
 SPLITK_API int splitk_gemm_bf16_noalloc(const void* a, const void* b, void* c, int M, int N, int K,
                                         int L, int split_k, splitk_stream_t stream) {
   int rc = check_pointers(a, b, c);
@@ -1206,6 +1239,7 @@ SPLITK_API const char* splitk_strerror(int code) {
     case SPLITK_ERR_UNSUPPORTED_DEVICE: return "no CUDA device of compute capability 10.3";
     case SPLITK_ERR_BAD_PLAN: return "plan does not match the shape";
     case SPLITK_ERR_SCRATCH: return "the call needs more scratch than the allocation-free array holds";
+    case SPLITK_ERR_NOT_MAPPED: return "host buffer is not page-locked and mapped into the device address space";
     default: return "unknown status code";
   }
 }

@@ -16,7 +16,7 @@ if not torch.cuda.is_available():  # pragma: no cover
 import oracle  # noqa: E402
 import split_bf16_gemm_swapped_gb300 as sk  # noqa: E402
 from split_bf16_gemm_swapped_gb300 import synthetic, workloads  # noqa: E402
-from tests._gpu import DEV, assert_parity, to_dev, to_host  # noqa: E402
+from tests._gpu import DEV, assert_parity, gemm_gpu, to_dev, to_host  # noqa: E402
 
 
 def _draw(L, M, N, K, seed):
@@ -98,6 +98,45 @@ def test_host_io_entry_point_matches_the_device_path():
     sk.splitk_gemm_bf16_hostio(ta, b_pin, c_pin, b_dev, c_dev, w.split_k)
     torch.cuda.synchronize()
     assert torch.equal(c_pin.view(torch.int16), ref.cpu().view(torch.int16))
+
+
+@pytest.mark.parametrize("M,N,K,L,split", [(1, 7168, 2048, 1, 4), (4, 300, 1024, 2, 2), (16, 4096, 7168, 1, 8)])
+def test_zero_copy_entry_point_matches_the_device_path(M, N, K, L, split):
+    """Activations read from, and the output written to, pinned host memory
+    by the kernel itself: the device path's bits."""
+    a, b = _draw(L, M, N, K, seed=2200 + M)
+    want = gemm_gpu(a, b, split_k=split)
+    ta = to_dev(a)
+    b_pin = torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).pin_memory()
+    c_pin = torch.full((L, M, N), float("nan"), dtype=torch.bfloat16).pin_memory()
+    for _ in range(2):
+        sk.splitk_gemm_bf16_zerocopy(ta, b_pin, c_pin, split_k=split)
+        torch.cuda.synchronize()
+        assert sk.splitk_get_status() == 0
+        assert np.array_equal(c_pin.view(torch.int16).numpy().view(np.uint16), want)
+
+
+def test_zero_copy_refuses_unmapped_buffers_and_unstaged_shapes():
+    L, M, N, K = 1, 1, 256, 1024
+    a, b = _draw(L, M, N, K, seed=2300)
+    ta = to_dev(a)
+    b_pin = torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).pin_memory()
+    c_pin = torch.empty((L, M, N), dtype=torch.bfloat16).pin_memory()
+    pageable_b = torch.from_numpy(b.view(np.int16).copy()).view(torch.bfloat16)
+    pageable_c = torch.empty((L, M, N), dtype=torch.bfloat16)
+    for bb, cc in ((pageable_b, c_pin), (b_pin, pageable_c)):
+        with pytest.raises(sk.SplitKError) as e:
+            sk.splitk_gemm_bf16_zerocopy(ta, bb, cc, split_k=2)
+        assert e.value.code == -12
+    # a shape whose activations the epilogue threads do not load (wide tiles)
+    a2, b2 = _draw(1, 64, 256, 8192, seed=2301)
+    b2_pin = torch.from_numpy(b2.view(np.int16)).view(torch.bfloat16).pin_memory()
+    c2_pin = torch.empty((1, 64, 256), dtype=torch.bfloat16).pin_memory()
+    with pytest.raises(sk.SplitKError) as e:
+        sk.splitk_gemm_bf16_zerocopy(to_dev(a2), b2_pin, c2_pin, split_k=1)
+    assert e.value.code == -4
+    torch.cuda.synchronize()
+    assert sk.splitk_get_status() == 0
 
 
 def test_calls_captured_in_a_cuda_graph_replay_identically():
