@@ -236,7 +236,7 @@ SPLITK_API int splitk_plan_check_for(const splitk_plan_t *plan, int M, int N,
 
 /*
  * Every valid tactic for a shape on a described device, without CUDA:
- * splitk_plan_for()'s choice first, then the page's ring (2-4 stages, one or
+ * splitk_plan_for()'s choice first, then the page's ring (2-8 stages, one or
  * two MMA issuers, either PDL trigger) and the staged family (resident
  * activations, 0-3 weight tiles in tensor memory, TMA or epilogue-thread
  * activation loads, L2 prefetch), for each split (all valid ones when

@@ -773,7 +773,7 @@ int gemm_auto(const void* a, const void* b, void* c, int M, int N, int K, int L,
 }
 
 // Every valid tactic for a shape on a described device: the plan's own
-// choice first, then the page's ring (2-4 stages, one or two MMA issuers,
+// choice first, then the page's ring (2-8 stages, one or two MMA issuers,
 // either PDL trigger) and the staged family (2 stages, 0-3 weight tiles in
 // tensor memory, resident activations loaded by TMA or by the epilogue
 // threads, L2 prefetch of the tiles left off chip), for each split and each
