@@ -273,6 +273,11 @@ int plan_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t smem_
     int n_modes = 0;
     if (split_mode == 2) modes[n_modes++] = 2;
     if (split > 1 && prefer_dedicated) modes[n_modes++] = 1;
+    // A few token columns (2-15): the scattered mailbox before the aliased
+    // one when the dedicated one does not fit (K = 16384 sweep at 3 stages,
+    // split 8: M=2 0.90 -> 0.92, M=4 0.89 -> 0.91; a single column keeps the
+    // dedicated mailbox, measured best).
+    if (split_mode != 2 && split >= 4 && ncols_max >= 2) modes[n_modes++] = 2;
     modes[n_modes++] = 0;
     auto fits = [&](int mode, int stages) {
       if (deep_two && stages % 2 != 0) return false;

@@ -236,8 +236,15 @@ def test_long_k_slices_prefer_a_deeper_ring_over_their_own_mailbox():
         assert _check(p, M, 7168, 16384, 2) == 0
     p = _plan(128, 7168, 16384, 2, 4)                   # 96 KB of partials: keep the scattered mailbox
     assert (p.stages, p.reduce_scatter) == (2, 1)
-    p = _plan(2, 7168, 16384, 2, 8)                     # 16 K tiles a CTA
+    p = _plan(8, 7168, 16384, 2, 8)                     # 16 K tiles a CTA
     assert (p.stages, p.mailbox_dedicated) == (3, 0)
+    # a few token columns: the scattered mailbox when the dedicated one does
+    # not fit beside the third stage; a single column keeps the dedicated one
+    for M in (2, 4):
+        p = _plan(M, 7168, 16384, 2, 8)
+        assert (p.stages, p.mailbox_dedicated, p.reduce_scatter, p.ctas_per_sm) == (3, 1, 1, 2)
+    p = _plan(1, 7168, 16384, 2, 8)
+    assert (p.stages, p.mailbox_dedicated, p.reduce_scatter) == (3, 1, 0)
     p = _plan(8, 7168, 2048, 4, 2)                      # 8 K tiles a CTA: the dedicated mailbox stays
     assert (p.stages, p.mailbox_dedicated) == (2, 1)
 
