@@ -130,7 +130,7 @@ def test_every_plan_fits_and_is_consistent(M, split):
     b_tiles = max(p.stages, p.k_tiles_per_cta) if p.b_resident else p.stages
     # the reduction's mailbox fits where it is placed
     if p.reduce_scatter:
-        assert split >= 4 and min(M, p.mma_n) >= 16 and p.mailbox_dedicated == 1
+        assert split >= 4 and min(M, p.mma_n) >= 2 and p.mailbox_dedicated == 1
         assert p.smem_bytes == 1024 + p.stages * 32768 + b_tiles * p.mma_n * 256 + min(M, p.mma_n) * 512 + 256
     elif split > 1:
         cols = min(4 * p.mailbox_quads, M, p.mma_n)
@@ -143,6 +143,35 @@ def test_every_plan_fits_and_is_consistent(M, split):
         assert p.smem_bytes == 1024 + p.stages * 32768 + b_tiles * p.mma_n * 256 + ded + 256
     # the f32 staging tile of rank 0 fits in its drained activation ring
     assert min(M, p.mma_n) * 128 * 4 <= b_tiles * p.mma_n * 256
+
+
+def test_every_plan_of_a_broad_shape_grid_passes_the_launch_check():
+    """Whatever the planners write for ~5,000 shapes, the launch-time check
+    accepts, within the shared-memory and TMEM budgets of the SM."""
+    n = 0
+    for M in (1, 2, 3, 5, 8, 13, 16, 24, 32, 48, 64, 100, 128, 200):
+        for N in (128, 300, 1000, 7168, 18432):
+            for K in (8, 136, 1000, 2048, 7168, 16384, 32768):
+                for L in (1, 3):
+                    for split in (0, 1, 2, 4, 8):
+                        try:
+                            p = _plan(M, N, K, L, split)
+                        except sk.SplitKError as e:
+                            assert e.code in (-1, -4), (M, N, K, L, split, e.code)
+                            continue
+                        assert _check(p, M, N, K, L) == 0, (M, N, K, L, split, p.as_dict())
+                        assert p.smem_bytes <= GB300["smem_per_block_optin"]
+                        assert GB300["smem_per_sm"] // (p.smem_bytes + 1024) * p.tmem_cols <= 512
+                        n += 1
+                        if M <= 32 and K % 128 == 0:
+                            try:
+                                q = sk.splitk_plan_w4a16_for(M, N, K, L, split, **GB300)
+                            except sk.SplitKError as e:
+                                assert e.code in (-1, -4), (M, N, K, L, split, e.code)
+                                continue
+                            assert _check(q, M, N, K, L) == 0, (M, N, K, L, split, q.as_dict())
+                            assert GB300["smem_per_sm"] // (q.smem_bytes + 1024) * q.tmem_cols <= 512
+    assert n > 3000
 
 
 @pytest.mark.parametrize("args,code", [
