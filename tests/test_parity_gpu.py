@@ -65,6 +65,28 @@ def test_deep_rings_and_depth_first_mailboxes(M, N, K, L, split, kind):
     assert np.array_equal(c, gemm_gpu(a, b, plan=p))
 
 
+def test_seeded_random_shapes_match_the_oracle():
+    """40 seeded shapes (ragged K multiples of 8, ragged N, batches, every
+    split and the planner's own), each through whatever plan the planner
+    picks, against the oracle."""
+    rng = np.random.default_rng(2400)
+    kinds = set()
+    for i in range(40):
+        M = int(rng.choice([1, 2, 3, 4, 6, 8, 12, 16, 20, 32, 40, 64]))
+        N = int(rng.integers(1, 9)) * 128 - int(rng.choice([0, 0, 8, 40]))
+        K = int(rng.integers(1, 65)) * 128 - 8 * int(rng.integers(0, 3))
+        L = int(rng.choice([1, 1, 2]))
+        split = int(rng.choice([0, 1, 2, 4, 8]))
+        if split and -(-K // 128) < split:
+            split = 1
+        a, b = _draw(L, M, N, K, seed=2400 + i)
+        p = sk.splitk_plan(M, N, K, L, split)
+        kinds.add((p.stages, p.mma_issuers, p.mailbox_dedicated, p.reduce_scatter, p.b_resident, p.a_tmem_tiles))
+        c = gemm_gpu(a, b, split_k=split)
+        assert_parity(c, oracle_full(a, b), a, b, K)
+    assert len(kinds) >= 8                  # the draw reaches many plan families
+
+
 @pytest.mark.parametrize("split", [1, 4])
 def test_batched_L_and_ragged_N(split):
     L, M, N, K = 3, 7, 200, 2048
