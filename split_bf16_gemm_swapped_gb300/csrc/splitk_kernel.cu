@@ -182,7 +182,15 @@ __global__ void __launch_bounds__(kThreads, 3)
   const int lane = (int)(threadIdx.x & 31);
   const int split = p.split;
   const int stages = p.stages;
-  const int rank = split > 1 ? (int)dev::cluster_ctarank() : 0;
+  // The cluster is (split, mc): x the K ranks of one output tile, y the mc
+  // tiles of an N-group that share each activation tile by multicast.
+  const int mc = p.mc;
+  const int crank = (split > 1 || mc > 1) ? (int)dev::cluster_ctarank() : 0;
+  const int rank = crank % split;                  // K rank
+  const int yc = crank / split;                    // place in the N-group
+  const uint32_t peer0 = (uint32_t)(yc * split);   // cluster rank of K rank 0 of this tile
+  uint16_t mc_mask = 0;                            // the N-group's CTAs of this K rank
+  for (int j = 0; j < mc; ++j) mc_mask |= (uint16_t)(1u << (rank + split * j));
   const int m_tile = (int)blockIdx.x / split;
   const int n0 = (int)blockIdx.y * kMmaM;
   const int m0 = m_tile * MMA_N;
@@ -234,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 3)
     if (lane == 0) {
       for (int s = 0; s < stages; ++s) {
         dev::mbar_init(bar_full0 + 8u * s, b_res ? 1u : 2u);   // A (and B when it rides the ring)
-        dev::mbar_init(bar_empty0 + 8u * s, 1);
+        dev::mbar_init(bar_empty0 + 8u * s, (uint32_t)mc);   // every consumer of the N-group
       }
       dev::mbar_init(bar_b, p.b_loader ? (uint32_t)kEpiThreads : 1u);
       dev::mbar_init(bar_mma_done, (uint32_t)p.mma_issuers);
@@ -366,8 +374,16 @@ __global__ void __launch_bounds__(kThreads, 3)
         const uint32_t dst = sB + (uint32_t)s * kBStage;
         const int k = (kt0 + kt) * kCtaK;
         dev::mbar_arrive_expect_tx(full, kBStage);
-        dev::tma_load_3d(dst, &b_map, k, m0, l, full);
-        dev::tma_load_3d(dst + kBBox, &b_map, k + kAtomK, m0, l, full);
+        if (mc == 1) {
+          dev::tma_load_3d(dst, &b_map, k, m0, l, full);
+          dev::tma_load_3d(dst + kBBox, &b_map, k + kAtomK, m0, l, full);
+        } else if (kt % mc == yc) {
+          // this CTA's turn: the tile goes to the whole N-group (the stage is
+          // free in all of them: each CTA's empty barrier counts every
+          // group member's release)
+          dev::tma_load_3d_multicast(dst, &b_map, k, m0, l, full, mc_mask);
+          dev::tma_load_3d_multicast(dst + kBBox, &b_map, k + kAtomK, m0, l, full, mc_mask);
+        }
       }
     }
   } else if (warp == 2 || warp == 3) {
@@ -479,7 +495,11 @@ __global__ void __launch_bounds__(kThreads, 3)
           dev::mma_bf16(d_acc, dev::smem_desc_sw128(a_st + a_off), dev::smem_desc_sw128(b_st + b_off), kIdesc,
                         (first | (uint32_t)kk) != 0u ? 1u : 0u);
         }
-        dev::mma_commit(bar_empty0 + 8u * s);  // stage free once these MMAs finish
+        if (mc == 1) {
+          dev::mma_commit(bar_empty0 + 8u * s);  // stage free once these MMAs finish
+        } else {
+          dev::mma_commit_multicast(bar_empty0 + 8u * s, mc_mask);   // ... in every CTA of the N-group
+        }
       }
       dev::mma_commit(bar_mma_done);           // this issuer's accumulator complete
     }
@@ -645,8 +665,8 @@ __global__ void __launch_bounds__(kThreads, 3)
       const int dst_rank = et / R;
       const bool publish = !(p.inject & kInjectSkipPublish);
       const uint32_t slot = ((uint32_t)(rank * ncols) * (uint32_t)R + (uint32_t)(et - dst_rank * R)) * 4u;
-      const uint32_t r_bar = dev::mapa(bar_reduce, (uint32_t)dst_rank);
-      const uint32_t r_mail = dev::mapa(sMail, (uint32_t)dst_rank) + slot;
+      const uint32_t r_bar = dev::mapa(bar_reduce, peer0 + (uint32_t)dst_rank);
+      const uint32_t r_mail = dev::mapa(sMail, peer0 + (uint32_t)dst_rank) + slot;
 #pragma unroll 1
       for (int g = 0; g * 16 < ncols; ++g) {
         uint32_t v[16];
@@ -718,9 +738,9 @@ __global__ void __launch_bounds__(kThreads, 3)
         dev::tc_fence_before();
         dev::mbar_arrive(bar_tmem_empty);
         if (publish) {
-          const uint32_t r_bar = dev::mapa(bar_reduce, 0);
+          const uint32_t r_bar = dev::mapa(bar_reduce, peer0);
           const uint32_t r_mail =
-              dev::mapa(sMail, 0) + (uint32_t)((rank - 1) * ncols) * kColumnBytes + (uint32_t)et * 4u;
+              dev::mapa(sMail, peer0) + (uint32_t)((rank - 1) * ncols) * kColumnBytes + (uint32_t)et * 4u;
 #pragma unroll
           for (int col = 0; col < 4; ++col) {
             if (col < ncols) dev::st_async_b32(r_mail + (uint32_t)col * kColumnBytes, v[col], r_bar);
@@ -733,7 +753,7 @@ __global__ void __launch_bounds__(kThreads, 3)
             dev::mbar_arrive_expect_tx(bar_reduce, (uint32_t)(split - 1) * (uint32_t)ncols * kColumnBytes);
           }
           if (!p.mailbox_dedicated && et >= 1 && et < split) {
-            dev::mbar_arrive_remote(dev::mapa(bar_ready, (uint32_t)et));
+            dev::mbar_arrive_remote(dev::mapa(bar_ready, peer0 + (uint32_t)et));
           }
         }
         float x[4];
@@ -782,11 +802,11 @@ __global__ void __launch_bounds__(kThreads, 3)
           // issuing thread's earlier memory operations, so arrivals issued one
           // after another from a single thread would serialise into round trips.
           if (need_ready && et >= 1 && et < split) {
-            dev::mbar_arrive_remote(dev::mapa(bar_ready, (uint32_t)et));
+            dev::mbar_arrive_remote(dev::mapa(bar_ready, peer0 + (uint32_t)et));
           }
         }
-        const uint32_t r_bar = dev::mapa(bar_reduce, 0);
-        const uint32_t r_mail = dev::mapa(sMail, 0) + (uint32_t)((rank - 1) * rc) * kColumnBytes;
+        const uint32_t r_bar = dev::mapa(bar_reduce, peer0);
+        const uint32_t r_mail = dev::mapa(sMail, peer0) + (uint32_t)((rank - 1) * rc) * kColumnBytes;
         bool publish = split > 1 && !owner && !(p.inject & kInjectSkipPublish);
         bool first_group = true;
 
@@ -928,7 +948,10 @@ __global__ void __launch_bounds__(kThreads, 3)
   // still reducing.  (A peer later than rank 0's whole wait limit would
   // publish into a departed CTA; the limit is chosen so that never happens.)
   const int tile_quads = (((p.M - m0) < MMA_N ? (p.M - m0) : MMA_N) + 3) >> 2;
-  const bool final_barrier = split > 1 && !(p.mailbox_dedicated && tile_quads <= p.mailbox_quads);
+  // (With multicast every CTA stays: its releases arrive on the group's
+  // barriers and the group's activation tiles land in its shared memory.)
+  const bool final_barrier =
+      mc > 1 || (split > 1 && !(p.mailbox_dedicated && tile_quads <= p.mailbox_quads));
   if (final_barrier) {
     // No CTA leaves while a peer may still address its shared memory.  The
     // arrival is relaxed (a release would wait for the tile's global
@@ -959,7 +982,7 @@ cudaError_t launch_t(const LaunchArgs& la, const CUtensorMap& b_map, const Kerne
   int n = 0;
   attrs[n].id = cudaLaunchAttributeClusterDimension;
   attrs[n].val.clusterDim.x = la.cluster_x;
-  attrs[n].val.clusterDim.y = 1;
+  attrs[n].val.clusterDim.y = la.cluster_y;
   attrs[n].val.clusterDim.z = 1;
   ++n;
   if (la.pdl) {
