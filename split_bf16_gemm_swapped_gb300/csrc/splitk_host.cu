@@ -367,11 +367,31 @@ int plan_w4_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t sm
                             smem_bytes_w4(mma_n, kt, ded, 1) + 1024 <= smem_per_sm / 2
                         ? 1
                         : 0;
-  size_t smem = smem_bytes_w4(mma_n, kt, ded, p.w4_smem_tiles);
-  const int per_sm_max = std::max(1, (int)(512u / p.tmem_cols));
-  if (resident_by_smem(smem_per_sm, smem) > per_sm_max) {
-    smem = std::max(smem, (smem_per_sm / (size_t)(per_sm_max + 1) + 16u) & ~(size_t)15u);
-    while (resident_by_smem(smem_per_sm, smem) > per_sm_max) smem += 16;
+  // Shared memory padded when needed so that the CTAs fitting an SM can
+  // hold their TMEM.
+  auto padded_smem = [&](size_t smem, uint32_t tmem_cols) {
+    const int per_sm_max = std::max(1, (int)(512u / tmem_cols));
+    if (resident_by_smem(smem_per_sm, smem) > per_sm_max) {
+      smem = std::max(smem, (smem_per_sm / (size_t)(per_sm_max + 1) + 16u) & ~(size_t)15u);
+      while (resident_by_smem(smem_per_sm, smem) > per_sm_max) smem += 16;
+    }
+    return smem;
+  };
+  size_t smem = padded_smem(smem_bytes_w4(mma_n, kt, ded, p.w4_smem_tiles), p.tmem_cols);
+  // Grids of more than two waves: one TMEM slot and one issuer when that lets
+  // more CTAs share an SM (at most 3 by registers), so that their decodes
+  // overlap (single-token decode, L=8: 49.1 -> 46.2 us).
+  const long long ctas = (long long)split * m_tiles * n_tiles * L;
+  if (ctas > 2LL * num_sms && p.a_tmem_tiles > 1) {
+    const uint32_t cols1 = tmem_cols_for(mma_n, 1, 1);
+    const size_t smem1 = padded_smem(smem_bytes_w4(mma_n, kt, ded, 0), cols1);
+    if (std::min(3, resident_by_smem(smem_per_sm, smem1)) > std::min(3, resident_by_smem(smem_per_sm, smem))) {
+      p.a_tmem_tiles = 1;
+      p.mma_issuers = 1;
+      p.tmem_cols = cols1;
+      p.w4_smem_tiles = 0;
+      smem = smem1;
+    }
   }
   if (smem > smem_optin) return SPLITK_ERR_NO_FIT;
   p.smem_bytes = smem;

@@ -313,7 +313,7 @@ def test_plan_check_rejects_what_a_launch_would():
 
 
 @pytest.mark.parametrize("args", [(1, 7168, 2048, 1, 4), (16, 4096, 7168, 1, 8), (4, 256, 1024, 1, 0),
-                                  (32, 1000, 4096, 2, 0), (3, 300, 512, 1, 2)])
+                                  (32, 1000, 4096, 2, 0), (3, 300, 512, 1, 2), (1, 7168, 2048, 8, 4)])
 def test_w4a16_plans(args):
     M, N, K, L, split = args
     p = sk.splitk_plan_w4a16_for(*args, **GB300)
@@ -345,6 +345,17 @@ def test_w4a16_plans(args):
         small = sk.Plan.from_buffer_copy(p)
         small.smem_bytes -= 32768               # no room for the stage
         assert _check(small, M, N, K, L) == -10
+
+
+def test_w4a16_grids_of_several_waves_trade_tmem_slots_for_residency():
+    one = sk.splitk_plan_w4a16_for(1, 7168, 2048, 1, 4, **GB300)    # 224 CTAs: under two waves
+    assert one.a_tmem_tiles == 3 and one.ctas_per_sm == 2
+    many = sk.splitk_plan_w4a16_for(1, 7168, 2048, 8, 4, **GB300)   # 1792 CTAs
+    assert (many.a_tmem_tiles, many.mma_issuers, many.w4_smem_tiles) == (1, 1, 0)
+    assert many.ctas_per_sm == 3 and many.ctas_per_sm * many.tmem_cols <= 512
+    assert _check(many, 1, 7168, 2048, 8) == 0
+    wide = sk.splitk_plan_w4a16_for(16, 4096, 7168, 4, 8, **GB300)  # one slot would not raise residency
+    assert wide.a_tmem_tiles == 3 and wide.ctas_per_sm == 2
 
 
 def test_w4a16_plans_reject_what_the_kernel_cannot_do():

@@ -474,6 +474,22 @@ def test_w4a16_matches_the_oracle(M, N, K, split):
     assert ok, rep
 
 
+@pytest.mark.parametrize("M", [3, 9])
+def test_w4a16_grids_of_several_waves_match_the_oracle(M):
+    """512 CTAs: the planner trades TMEM slots for a third CTA per SM."""
+    L, N, K, split = 8, 2048, 2048, 4
+    aq, a_s, b = _w4_draw(L, M, N, K, seed=1550 + M)
+    p = sk.splitk_plan_w4a16(M, N, K, L, split)
+    assert (p.a_tmem_tiles, p.mma_issuers, p.ctas_per_sm) == (1, 1, 3)
+    tc = sk.splitk_gemm_w4a16_planned(_u8_dev(aq), _u8_dev(a_s), to_dev(b), None, p)
+    torch.cuda.synchronize()
+    assert sk.splitk_get_status() == 0, sk.splitk_get_fault()
+    ref = oracle.gemm_w4a16(aq, a_s, b)
+    max_w = float(np.max(np.abs(oracle.w4_dequant(aq, a_s))))
+    ok, rep = _tol.check(to_host(tc), ref, K, max_w, _tol.max_abs_bf16(b))
+    assert ok, rep
+
+
 @pytest.mark.parametrize("M,split", [(1, 4), (8, 2), (8, 4), (16, 8), (32, 2)])
 def test_w4a16_equals_the_bf16_kernel_on_the_decoded_weights(M, split):
     """The decoded weights are exact bf16 values, so the A16W4 product equals,
