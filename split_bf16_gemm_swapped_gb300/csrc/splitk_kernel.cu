@@ -17,17 +17,26 @@
 //               L2 evict_first, issued before the programmatic-dependent-launch
 //               wait; then launch_dependents (SplitKGemm.weight_warp)
 //   warp 1      activation (B) producer: griddepcontrol.wait, then TMA
-//               (SplitKGemm.activation_warp)
-//   warp 2      TMEM allocation, tcgen05.mma issue, TMEM release (mma_warp)
-//   warp 3      idle (keeps warps 4..7 on TMEM lane quadrants 0..3)
-//   warps 4..7  epilogue: TMEM -> registers, DSMEM publish / rank-0 reduce,
+//               (SplitKGemm.activation_warp); with a cluster multicast group,
+//               the group's CTAs take turns loading each tile for all of them
+//   warp 2      TMEM allocation, tcgen05.mma issue (even K tiles when there
+//               are two issuers), TMEM release (mma_warp)
+//   warp 3      second MMA issuer (odd K tiles, own accumulator) or idle; it
+//               keeps warps 4..7 on TMEM lane quadrants 0..3
+//   warps 4..7  weight tiles copied into TMEM before the wait (staged tiles)
+//               or, for 4-bit weights, decoded to bf16 into TMEM or a
+//               shared-memory stage; activation loads for few rows; then the
+//               epilogue: TMEM -> registers, DSMEM publish / rank-0 reduce,
 //               BF16 packing, 16-byte stores (epilog_warp)
 //
 // Every mbarrier wait is bounded by %globaltimer (the Muse Spark AMD dev
 // page's _spin_bounded: a timeout records a diagnostic, sets a sticky failed
-// flag, and the CTA's later waits give up at once); TMEM is always released
-// and every CTA of a cluster meets at a final cluster barrier, so a failed
-// launch ends with no copy in flight into a departed CTA.
+// flag, and the CTA's later waits give up at once); TMEM is always released.
+// A CTA whose shared memory a peer may still address (aliased or multi-round
+// mailboxes, multicast groups) leaves only after a final cluster barrier; a
+// CTA whose wait failed first drains (bounded) the copies it issued and the
+// partials addressed to it, so a failed launch leaves no copy in flight into
+// a departed CTA.
 
 #include <cuda.h>
 #include <cuda_runtime.h>
