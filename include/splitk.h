@@ -194,9 +194,12 @@ SPLITK_API int splitk_plan_for(int M, int N, int K, int L, int split_k,
  * a, b, c are device pointers (layouts above); a and b 16-byte aligned.
  * C is written once (not accumulated); rows m >= M and columns n >= N of the
  * padded tiles are never written.  The first call for a given A pointer and
- * shape encodes A's tensor map and copies it to the device on `stream`
- * (allocating the pool on the first call of all), so make that first call
- * outside any CUDA graph capture.
+ * shape encodes A's tensor map and copies it to the device (allocating the
+ * pool on the first call of all).  Outside a graph capture that copy is
+ * synchronous, so later calls on any stream may use the map; inside a
+ * capture it is a node of the graph, and calls on other streams must then
+ * wait until the graph has run once.  Make that first call outside any
+ * capture.
  */
 SPLITK_API int splitk_gemm_bf16(const void *a, const void *b, void *c,
                                 int M, int N, int K, int L, int split_k,

@@ -684,8 +684,20 @@ int a_map_for(DeviceState& st, const void* a, int N, int K, int L, cudaStream_t 
                            ? encode_3d_w4(&st.h_pool[slot], a, (uint64_t)K / 2u, (uint64_t)N, (uint64_t)L)
                            : encode_3d(&st.h_pool[slot], a, (uint64_t)K, (uint64_t)N, (uint64_t)L, (uint32_t)kMmaM);
   if (!encoded) return SPLITK_ERR_CUDA;
-  if (cudaMemcpyAsync(st.d_pool + slot, st.h_pool + slot, sizeof(CUtensorMap), cudaMemcpyHostToDevice,
-                      stream) != cudaSuccess) {
+  // Outside a graph capture the copy completes before this returns, so a
+  // launch on any stream may use the slot from now on; inside a capture it
+  // becomes a node of the graph, ordered before the kernel on `stream`.
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) {
+    cudaGetLastError();
+    return SPLITK_ERR_CUDA;
+  }
+  const cudaError_t copied =
+      cap == cudaStreamCaptureStatusNone
+          ? cudaMemcpy(st.d_pool + slot, st.h_pool + slot, sizeof(CUtensorMap), cudaMemcpyHostToDevice)
+          : cudaMemcpyAsync(st.d_pool + slot, st.h_pool + slot, sizeof(CUtensorMap),
+                            cudaMemcpyHostToDevice, stream);
+  if (copied != cudaSuccess) {
     cudaGetLastError();
     return SPLITK_ERR_CUDA;
   }
