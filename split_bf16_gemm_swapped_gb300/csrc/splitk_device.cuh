@@ -103,8 +103,8 @@ __device__ __forceinline__ void cluster_wait_acquire() {
   asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
 }
 
-// 16-byte asynchronous store into a peer CTA's shared memory; completes
-// 16 transaction bytes on the peer's mbarrier.
+// 4-byte asynchronous store into a peer CTA's shared memory; completes
+// 4 transaction bytes on the peer's mbarrier.
 __device__ __forceinline__ void st_async_b32(uint32_t cluster_addr, uint32_t a, uint32_t cluster_bar) {
   asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(cluster_addr),
                "r"(a), "r"(cluster_bar)
