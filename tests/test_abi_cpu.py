@@ -178,12 +178,19 @@ def test_every_plan_of_a_broad_shape_grid_passes_the_launch_check():
     ((0, 128, 128, 1, 1), -1), ((1, 0, 128, 1, 1), -1), ((1, 128, 0, 1, 1), -1),
     ((1, 128, 128, 0, 1), -1), ((1, 128, 100, 1, 1), -1), ((1, 128, 1024, 1, 3), -3),
     ((1, 128, 1024, 1, 16), -3), ((1, 128, 128, 1, 2), -1), ((1, 128, 1004, 1, 1), -1),
-    ((1, 128 * 70000, 128, 1, 1), -1),
+    ((1, 128 * 70000, 128, 1, 1), -1), ((1, 128 * 65535 + 1, 128, 1, 1), -1), ((1, 128, 128, 65536, 1), -1),
 ])
 def test_plan_rejects_bad_shapes(args, code):
     with pytest.raises(sk.SplitKError) as e:
         sk.splitk_plan_for(*args, **GB300)
     assert e.value.code == code
+
+
+def test_the_largest_grid_dimensions_are_planned():
+    p = sk.splitk_plan_for(1, 128 * 65535, 128, 1, 0, **GB300)
+    assert tuple(p.grid) == (1, 65535, 1)
+    p = sk.splitk_plan_for(1, 128, 128, 65535, 0, **GB300)
+    assert tuple(p.grid) == (1, 1, 65535)
 
 
 def test_gemm_rejects_null_and_misaligned_pointers_before_cuda():

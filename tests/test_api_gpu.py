@@ -60,6 +60,30 @@ def test_argument_errors_enqueue_nothing():
     assert bool((tc == 7.0).all())
 
 
+@pytest.mark.parametrize("L,N", [(65535, 128), (1, 65535 * 128)])
+def test_the_largest_grid_dimensions_index_correctly(L, N):
+    """The grid's limits of 65,535 matrices (z) and 65,535 weight tiles (y).
+    Weight row n of matrix l has one nonzero, s = (l + n) % 7 - 3, at k = 0,
+    so C[l][m][n] = s * B[l][m][0] exactly: B holds multiples of 1/4 in
+    [-1.5, 1.5], and every product is a bf16 value.  2.1 GB of weights."""
+    M, K = 2, 128
+    s = ((np.arange(L)[:, None] + np.arange(N)[None, :]) % 7 - 3).astype(np.float32)     # [L, N]
+    b = (((np.arange(L * M * K) % 13) - 6) * 0.25).astype(np.float32).reshape(L, M, K)
+    b_bits = (b.view(np.uint32) >> 16).astype(np.uint16)                                  # exact
+    expect = s[:, None, :].astype(np.float64) * b[:, :, 0:1].astype(np.float64)          # [L, M, N]
+    a = torch.zeros((L, N, K), dtype=torch.bfloat16, device=DEV)
+    a[:, :, 0] = torch.from_numpy(s).to(DEV).to(torch.bfloat16)
+    p = sk.splitk_plan(M, N, K, L, 0)
+    assert tuple(p.grid)[1:] == ((N + 127) // 128, L)
+    c = sk.splitk_gemm_bf16(a, to_dev(b_bits), split_k=0)
+    torch.cuda.synchronize()
+    assert sk.splitk_get_status() == 0, sk.splitk_get_fault()
+    got = to_host(c).astype(np.uint32) << 16
+    assert np.array_equal(got.view(np.float32).astype(np.float64), expect)
+    del a, c
+    torch.cuda.empty_cache()
+
+
 @pytest.mark.parametrize("M,N,split", [(1, 300, 4), (5, 129, 2), (40, 200, 8), (128, 384, 1)])
 def test_guard_bands_around_C_are_untouched(M, N, split):
     L, K = 2, 1024
