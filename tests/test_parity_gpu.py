@@ -643,3 +643,26 @@ def test_w4a16_all_ones_closed_form():
     c = to_host(sk.splitk_gemm_w4a16(_u8_dev(aq), _u8_dev(a_s), to_dev(b), split_k=4))
     torch.cuda.synchronize()
     assert np.all(c == oracle.f64_to_bf16(4.0 * K))
+
+
+@pytest.mark.parametrize("L,N", [(65535, 128), (1, 65535 * 128)])
+def test_w4a16_the_largest_grid_dimensions_index_correctly(L, N):
+    """As the bf16 case: weight row n of matrix l has one nonzero 4-bit code,
+    s = (l + n) % 7 - 3 (E2M1 holds 0, +-1, +-2, +-3 exactly), at k = 0, with
+    scale code 127 (x1), so C[l][m][n] = s * B[l][m][0] exactly."""
+    M, K = 2, 128
+    s = (np.arange(L)[:, None] + np.arange(N)[None, :]) % 7 - 3                   # [L, N]
+    e2m1 = np.array([0xD, 0xC, 0xA, 0x0, 0x2, 0x4, 0x5], np.uint8)                 # -3 .. 3
+    aq = np.zeros((L, N, K // 2), np.uint8)
+    aq[:, :, 0] = e2m1[s + 3]                                                        # low nibble: k = 0
+    a_s = np.full((L, N, K // 32), 127, np.uint8)
+    b = (((np.arange(L * M * K) % 13) - 6) * 0.25).astype(np.float32).reshape(L, M, K)
+    b_bits = (b.view(np.uint32) >> 16).astype(np.uint16)                            # exact
+    expect = s[:, None, :].astype(np.float64) * b[:, :, 0:1].astype(np.float64)    # [L, M, N]
+    c = sk.splitk_gemm_w4a16(_u8_dev(aq), _u8_dev(a_s), to_dev(b_bits), split_k=0)
+    torch.cuda.synchronize()
+    assert sk.splitk_get_status() == 0, sk.splitk_get_fault()
+    got = to_host(c).astype(np.uint32) << 16
+    assert np.array_equal(got.view(np.float32).astype(np.float64), expect)
+    del c
+    torch.cuda.empty_cache()
