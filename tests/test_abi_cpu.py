@@ -37,6 +37,43 @@ def test_every_declared_symbol_is_exported():
     assert not missing, missing
 
 
+_C_CONSUMER = r"""
+#include <stdio.h>
+#include "splitk.h"
+int main(void) {
+    splitk_plan_t p;
+    int rc = splitk_plan_for(16, 4096, 7168, 1, 8, 152, 233472, 232448, &p);
+    printf("%d %d %d %d %d %d %u %u %u %zu\n", rc, p.mma_n, p.stages, p.split_k, p.a_tmem_tiles,
+           p.reduce_scatter, p.grid[0], p.grid[1], p.grid[2], p.smem_bytes);
+    printf("%d\n", splitk_gemm_bf16(NULL, NULL, NULL, 1, 128, 128, 1, 1, NULL));
+    return 0;
+}
+"""
+
+
+def test_the_header_is_plain_c_and_a_c_program_links_the_library(tmp_path):
+    """A C11 consumer compiles against include/splitk.h with every warning an
+    error, links the library, and plans what the Python binding plans."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "consumer.c"
+    src.write_text(_C_CONSUMER)
+    lib = sk.library_path()
+    exe = tmp_path / "consumer"
+    subprocess.run([gcc, "-std=c11", "-Wall", "-Wextra", "-pedantic", "-Werror", f"-I{ROOT / 'include'}",
+                    str(src), "-o", str(exe), f"-L{lib.parent}", f"-l:{lib.name}", f"-Wl,-rpath,{lib.parent}"],
+                   check=True, capture_output=True, text=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split("\n")
+    p = sk.splitk_plan_for(16, 4096, 7168, 1, 8, **GB300)
+    expect = (f"0 {p.mma_n} {p.stages} {p.split_k} {p.a_tmem_tiles} {p.reduce_scatter} "
+              f"{p.grid[0]} {p.grid[1]} {p.grid[2]} {p.smem_bytes}")
+    assert out[0] == expect
+    assert int(out[1]) == -7                           # SPLITK_ERR_NULL, before any CUDA call
+
+
 def test_version_and_strerror():
     assert sk.splitk_version() >= 10000
     for code, name in sk.STATUS.items():
