@@ -74,6 +74,16 @@ def test_the_header_is_plain_c_and_a_c_program_links_the_library(tmp_path):
     assert int(out[1]) == -7                           # SPLITK_ERR_NULL, before any CUDA call
 
 
+def test_a_missing_library_raises_instead_of_falling_back(monkeypatch, tmp_path):
+    """No CPU fallback: without the built library every entry point raises."""
+    monkeypatch.setattr(_build, "SPLITK_LIB", tmp_path / "libmissing.so")
+    monkeypatch.setattr(sk, "_lib", None)
+    with pytest.raises(RuntimeError, match="missing"):
+        sk.load_library()
+    with pytest.raises(RuntimeError, match="missing"):
+        sk.splitk_plan_for(1, 7168, 2048, 1, 4, **GB300)
+
+
 def test_version_and_strerror():
     assert sk.splitk_version() >= 10000
     for code, name in sk.STATUS.items():
