@@ -279,22 +279,28 @@ __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// The power of two of E8M0 scale code x, 2^(x - 127) (code 0: zero), as a
+// bf16 pair: the bf16 bits are x << 7.
+__device__ __forceinline__ uint32_t e8m0_bf16x2(uint32_t code) { return (code << 7) | (code << 23); }
+
 // One byte of two E2M1 codes (low nibble = first element) -> two bf16 values
-// times the power of two `scale` (binary32 bits), packed with the first in
-// the low half.  The hardware conversion to f16x2 is exact (E2M1 values are
-// f16 values), widening to f32 is exact, the power-of-two product is exact
-// in range, and the final rounding to bf16 is exact because the value has
-// at most 2 significant bits.
-__device__ __forceinline__ uint32_t e2m1x2_scaled_bf16x2(uint32_t byte, float scale) {
+// times the power of two `scale2` (a bf16 pair, e8m0_bf16x2), packed with
+// the first in the low half.  The hardware conversion to f16x2 is exact
+// (E2M1 values are f16 values), widening to f32 and rounding to bf16 are
+// exact (at most 2 significant bits), and the bf16 product by a power of two
+// is exact wherever the result is a finite bf16 value, subnormals included
+// (the smallest, 0.5 * 2^-126, is one).
+__device__ __forceinline__ uint32_t e2m1x2_scaled_bf16x2(uint32_t byte, uint32_t scale2) {
   uint32_t h2;
   asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(h2) : "r"(byte));
   float lo, hi;
   asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
       : "=f"(lo), "=f"(hi)
       : "r"(h2));
-  uint32_t r;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi * scale), "f"(lo * scale));
-  return r;
+  uint32_t r, d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(r), "r"(scale2));
+  return d;
 }
 
 __device__ __forceinline__ void tmem_wait_ld() {

@@ -578,8 +578,8 @@ __global__ void __launch_bounds__(kThreads, 3)
       // lane et: 4 chunks of 32 codes (64 B of the tile's 64-byte-swizzled
       // row: chunk j sits at 16-byte slot j ^ ((et >> 1) & 3)), each chunk
       // one scale block; a byte becomes two bf16 through the hardware
-      // E2M1 -> f16 conversion and an exact binary32 product with the
-      // block's power of two.  The first `slots` tiles are decoded
+      // E2M1 -> f16 conversion, an exact rounding to bf16 and an exact bf16
+      // product with the block's power of two.  The first `slots` tiles are decoded
       // before the previous kernel completes; with the epilogue loading the
       // activations, that load comes next, then the remaining tiles as the
       // MMAs free their slots.
@@ -600,7 +600,7 @@ __global__ void __launch_bounds__(kThreads, 3)
           const uint32_t atom = sW4Stage + (uint32_t)(et >> 3) * 1024u + (uint32_t)(et & 7) * 128u;
 #pragma unroll 1
           for (int j = 0; j < 4; ++j) {
-            const float scale = __uint_as_float(((codes >> (8 * j)) & 0xFFu) << 23);
+            const uint32_t scale = dev::e8m0_bf16x2((codes >> (8 * j)) & 0xFFu);
             uint32_t w[4];
             dev::ld_shared_v4(row + (uint32_t)((j ^ ((et >> 1) & 3)) * 16), w[0], w[1], w[2], w[3]);
             uint32_t r[16];
@@ -629,7 +629,7 @@ __global__ void __launch_bounds__(kThreads, 3)
         const uint32_t t_col = t_row + p.tmem_tile_col0 + (uint32_t)slot * kTmemTileCols;
 #pragma unroll 1
         for (int j = 0; j < 4; ++j) {
-          const float scale = __uint_as_float(((codes >> (8 * j)) & 0xFFu) << 23);   // 2^(code - 127)
+          const uint32_t scale = dev::e8m0_bf16x2((codes >> (8 * j)) & 0xFFu);   // 2^(code - 127)
           uint32_t w[4];
           dev::ld_shared_v4(row + (uint32_t)((j ^ ((et >> 1) & 3)) * 16), w[0], w[1], w[2], w[3]);
           uint32_t r[16];
