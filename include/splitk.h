@@ -57,8 +57,10 @@ typedef struct CUstream_st *splitk_stream_t;
 
 enum splitk_status {
     SPLITK_OK = 0,
-    /* M, N, K or L < 1, a size past a hardware limit, K not a multiple of
-       8 (TMA row stride), or fewer 128-wide K tiles than split ranks. */
+    /* M, N, K or L < 1, a size past a hardware limit (N > 65535 * 128,
+       L > 65535, K > 2^31 - 128, or more than 2^31 - 1 CTAs along the
+       grid's x), K not a multiple of 8 (TMA row stride), or fewer 128-wide
+       K tiles than split ranks. */
     SPLITK_ERR_INVALID_SHAPE = -1,
     /* A or B not 16-byte aligned (TMA), or C not 2-byte aligned. */
     SPLITK_ERR_MISALIGNED = -2,

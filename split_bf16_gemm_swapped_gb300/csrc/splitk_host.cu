@@ -97,7 +97,14 @@ int resident_by_smem(size_t smem_per_sm, size_t smem) { return (int)(smem_per_sm
 
 // 128-wide K tiles covering K; the last one may be ragged (TMA reads zeros
 // past K).
-inline int total_k_tiles(int K) { return (K + kCtaK - 1) / kCtaK; }
+inline int total_k_tiles(int K) { return (int)(((long long)K + kCtaK - 1) / kCtaK); }
+
+// The largest K: the kernel's K coordinates (TMA takes signed 32-bit ones)
+// reach the end of the last 128-wide tile.
+constexpr int kMaxK = 0x7FFFFFFF - kCtaK + 1;
+
+// Tiles of `tile` rows covering `rows` (64-bit: rows may be near INT_MAX).
+inline long long tiles_of(int rows, int tile) { return ((long long)rows + tile - 1) / tile; }
 
 // Split-K choice from GB300 measurements (decode shapes and the long-K
 // sweep, back to back): rank 0's reduction costs more as the split and the
@@ -168,10 +175,10 @@ int plan_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t smem_
   if (split_k != 0 && !valid_split(split_k)) return SPLITK_ERR_UNSUPPORTED_SPLIT;
   if (num_sms < 1 || smem_optin < 1 || smem_per_sm < 1) return SPLITK_ERR_UNSUPPORTED_DEVICE;
   // K's row stride must be a multiple of 16 bytes (TMA).
-  if (K % 8 != 0) return SPLITK_ERR_INVALID_SHAPE;
+  if (K % 8 != 0 || K > kMaxK) return SPLITK_ERR_INVALID_SHAPE;
   const int T = total_k_tiles(K);
   const int mma_n = choose_mma_n(M);
-  const long long m_tiles = (M + mma_n - 1) / mma_n;
+  const long long m_tiles = tiles_of(M, mma_n);
   const long long n_tiles = ((long long)N + kMmaM - 1) / kMmaM;
   if (n_tiles > 65535 || L > 65535) return SPLITK_ERR_INVALID_SHAPE;
   int split = split_k;
@@ -318,12 +325,12 @@ int plan_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t smem_
 int plan_w4_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t smem_per_sm, size_t smem_optin,
                  splitk_plan_t* out) {
   if (!out) return SPLITK_ERR_NULL;
-  if (M < 1 || N < 1 || K < 1 || L < 1 || M > 32 || K % kCtaK != 0) return SPLITK_ERR_INVALID_SHAPE;
+  if (M < 1 || N < 1 || K < 1 || L < 1 || M > 32 || K % kCtaK != 0 || K > kMaxK) return SPLITK_ERR_INVALID_SHAPE;
   if (split_k != 0 && !valid_split(split_k)) return SPLITK_ERR_UNSUPPORTED_SPLIT;
   if (num_sms < 1 || smem_optin < 1 || smem_per_sm < 1) return SPLITK_ERR_UNSUPPORTED_DEVICE;
   const int T = K / kCtaK;
   const int mma_n = choose_mma_n(M);
-  const long long m_tiles = (M + mma_n - 1) / mma_n;
+  const long long m_tiles = tiles_of(M, mma_n);
   const long long n_tiles = ((long long)N + kMmaM - 1) / kMmaM;
   if (n_tiles > 65535 || L > 65535) return SPLITK_ERR_INVALID_SHAPE;
   int split = split_k != 0 ? split_k : auto_split(T, m_tiles * n_tiles * L, num_sms, mma_n);
@@ -405,13 +412,13 @@ int check_plan_w4(const splitk_plan_t& pl, int M, int N, int K, int L, size_t sm
                   uint32_t* dedicated_bytes) {
   if (pl.mma_m != kMmaM || (pl.mma_n != 16 && pl.mma_n != 32)) return SPLITK_ERR_BAD_PLAN;
   if (!valid_split(pl.split_k)) return SPLITK_ERR_UNSUPPORTED_SPLIT;
-  if (M > 32 || K % kCtaK != 0 || K / kCtaK < pl.split_k) return SPLITK_ERR_INVALID_SHAPE;
+  if (M > 32 || K % kCtaK != 0 || K > kMaxK || K / kCtaK < pl.split_k) return SPLITK_ERR_INVALID_SHAPE;
   const int T = K / kCtaK;
   const int kt = (T + pl.split_k - 1) / pl.split_k;
   if (pl.k_tiles_per_cta != kt || pl.stages != kt) return SPLITK_ERR_BAD_PLAN;
   if (kt > kMaxStages) return SPLITK_ERR_NO_FIT;
   if (pl.b_multicast > 1) return SPLITK_ERR_BAD_PLAN;
-  const long long m_tiles = (M + pl.mma_n - 1) / pl.mma_n;
+  const long long m_tiles = tiles_of(M, pl.mma_n);
   const long long n_tiles = ((long long)N + kMmaM - 1) / kMmaM;
   if (n_tiles > 65535 || L > 65535) return SPLITK_ERR_INVALID_SHAPE;
   if (pl.grid[0] != (unsigned)(pl.split_k * m_tiles) || pl.grid[1] != (unsigned)n_tiles ||
@@ -455,11 +462,12 @@ int check_plan(const splitk_plan_t& pl, int M, int N, int K, int L, size_t smem_
   if (pl.mma_m != kMmaM) return SPLITK_ERR_BAD_PLAN;
   if (pl.mma_n != 16 && pl.mma_n != 32 && pl.mma_n != 64 && pl.mma_n != 128) return SPLITK_ERR_BAD_PLAN;
   if (!valid_split(pl.split_k)) return SPLITK_ERR_UNSUPPORTED_SPLIT;
-  if (K % 8 != 0 || total_k_tiles(K) < pl.split_k) return SPLITK_ERR_INVALID_SHAPE;
+  if (K % 8 != 0 || K > kMaxK || total_k_tiles(K) < pl.split_k) return SPLITK_ERR_INVALID_SHAPE;
   if (pl.k_tiles_per_cta != (total_k_tiles(K) + pl.split_k - 1) / pl.split_k) return SPLITK_ERR_BAD_PLAN;
   if (pl.stages < 2 || pl.stages > kMaxStages) return SPLITK_ERR_BAD_PLAN;
-  const long long m_tiles = (M + pl.mma_n - 1) / pl.mma_n;
+  const long long m_tiles = tiles_of(M, pl.mma_n);
   const long long n_tiles = ((long long)N + kMmaM - 1) / kMmaM;
+  if (m_tiles * pl.split_k > 0x7FFFFFFFLL) return SPLITK_ERR_INVALID_SHAPE;
   // Multicast N-groups of mc tiles (the grid padded to whole groups; padded
   // tiles read zeros and store nothing): the page's ring only, and a
   // cluster of at most 8 CTAs.
@@ -835,7 +843,7 @@ int enumerate_plans(int M, int N, int K, int L, int split_k, int num_sms, size_t
   out->push_back(base);
   const int T = total_k_tiles(K);
   const int mma_n = base.mma_n;
-  const long long m_tiles = (M + mma_n - 1) / mma_n;
+  const long long m_tiles = tiles_of(M, mma_n);
   const long long n_tiles = ((long long)N + kMmaM - 1) / kMmaM;
   const int ncols_max = std::min(M, mma_n);
   const int nquads_max = (ncols_max + 3) / 4;

@@ -226,11 +226,24 @@ def test_every_plan_of_a_broad_shape_grid_passes_the_launch_check():
     ((1, 128, 128, 0, 1), -1), ((1, 128, 100, 1, 1), -1), ((1, 128, 1024, 1, 3), -3),
     ((1, 128, 1024, 1, 16), -3), ((1, 128, 128, 1, 2), -1), ((1, 128, 1004, 1, 1), -1),
     ((1, 128 * 70000, 128, 1, 1), -1), ((1, 128 * 65535 + 1, 128, 1, 1), -1), ((1, 128, 128, 65536, 1), -1),
+    ((1, 128, 2**31 - 120, 1, 0), -1),                 # K past the last signed 32-bit tile coordinate
 ])
 def test_plan_rejects_bad_shapes(args, code):
     with pytest.raises(sk.SplitKError) as e:
         sk.splitk_plan_for(*args, **GB300)
     assert e.value.code == code
+
+
+def test_sizes_near_int_max_plan_without_overflow():
+    M = 2**31 - 1
+    p = sk.splitk_plan_for(M, 128, 128, 1, 1, **GB300)
+    assert tuple(p.grid) == ((M + 127) // 128, 1, 1)
+    assert _check(p, M, 128, 128, 1) == 0
+    K = 2**31 - 128                                    # the largest K
+    p = sk.splitk_plan_for(1, 128, K, 1, 8, **GB300)
+    assert p.k_tiles_per_cta == -(-(K // 128) // 8)       # the most any rank owns
+    assert _check(p, 1, 128, K, 1) == 0
+    assert _check(p, 1, 128, K + 8, 1) == -1
 
 
 def test_the_largest_grid_dimensions_are_planned():
