@@ -212,6 +212,8 @@ def _out(c, a, M, N, L):
         return torch.empty(shape, dtype=torch.bfloat16, device=a.device)
     if tuple(c.shape) != shape or c.dtype != torch.bfloat16 or not c.is_contiguous():
         raise ValueError(f"c must be a contiguous bfloat16 tensor of shape {shape}")
+    if c.device != a.device:
+        raise ValueError(f"c must be on {a.device}, the operands' device")
     return c
 
 
@@ -219,6 +221,8 @@ def _require_cuda(*ts):
     for t in ts:
         if not t.is_cuda or not t.is_contiguous():
             raise ValueError("operands must be contiguous CUDA tensors")
+    if len({str(t.device) for t in ts}) > 1:
+        raise ValueError("operands must be on one device")
 
 
 def splitk_gemm_bf16(a, b, c=None, split_k: int = 0, stream=None):

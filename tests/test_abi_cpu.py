@@ -84,6 +84,14 @@ def test_a_missing_library_raises_instead_of_falling_back(monkeypatch, tmp_path)
         sk.splitk_plan_for(1, 7168, 2048, 1, 4, **GB300)
 
 
+def test_an_output_on_another_device_is_refused():
+    import torch
+    a = torch.empty((128, 256), dtype=torch.bfloat16, device="meta")
+    with pytest.raises(ValueError, match="device"):
+        sk._out(torch.empty((4, 128), dtype=torch.bfloat16), a, 4, 128, 1)
+    assert sk._out(None, a, 4, 128, 1).device == a.device
+
+
 def test_version_and_strerror():
     assert sk.splitk_version() >= 10000
     for code, name in sk.STATUS.items():

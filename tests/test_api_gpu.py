@@ -60,6 +60,19 @@ def test_argument_errors_enqueue_nothing():
     assert bool((tc == 7.0).all())
 
 
+def test_a_host_output_tensor_is_refused_before_any_launch():
+    a = torch.zeros((256, 1024), dtype=torch.bfloat16, device=DEV)
+    b = torch.zeros((4, 1024), dtype=torch.bfloat16, device=DEV)
+    host_c = torch.full((4, 256), 7.0, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="device"):
+        sk.splitk_gemm_bf16(a, b, host_c)
+    aq = torch.zeros((256, 512), dtype=torch.uint8, device=DEV)
+    a_s = torch.full((256, 32), 127, dtype=torch.uint8, device=DEV)
+    with pytest.raises(ValueError, match="device"):
+        sk.splitk_gemm_w4a16(aq, a_s, b, host_c)
+    assert bool((host_c == 7.0).all())
+
+
 @pytest.mark.parametrize("L,N", [(65535, 128), (1, 65535 * 128)])
 def test_the_largest_grid_dimensions_index_correctly(L, N):
     """The grid's limits of 65,535 matrices (z) and 65,535 weight tiles (y).
