@@ -264,6 +264,10 @@ def _w4_dims(a_q, a_s, b):
     import torch
     if a_q.dtype != torch.uint8 or a_s.dtype != torch.uint8:
         raise TypeError("A16W4 codes and scales are uint8 tensors")
+    if b.dtype != torch.bfloat16:
+        raise TypeError("b must be bfloat16")
+    if a_q.dim() not in (2, 3) or a_s.dim() != a_q.dim() or b.dim() != a_q.dim():
+        raise ValueError("a_q is [L, N, K/2] or [N, K/2], a_s [L, N, K/32] or [N, K/32], b [L, M, K] or [M, K]")
     if a_q.dim() == 2:
         a_q, a_s = a_q.unsqueeze(0), a_s.unsqueeze(0)
     if b.dim() == 2:
@@ -332,10 +336,9 @@ def splitk_tune(a_list, b, c=None, split_k: int = 0, reps: int = 64, stream=None
     import torch
     M, N, K, L = _dims(a_list[0], b)
     for a in a_list:
-        _require_cuda(a)
-        if tuple(a.shape) != tuple(a_list[0].shape):
-            raise ValueError("the weight tensors must have one shape")
-    _require_cuda(b)
+        if tuple(a.shape) != tuple(a_list[0].shape) or a.dtype != a_list[0].dtype:
+            raise ValueError("the weight tensors must have one shape and dtype")
+    _require_cuda(*a_list, b)
     c = _out(c, a_list[0], M, N, L)
     ptrs = (ctypes.c_void_p * len(a_list))(*[a.data_ptr() for a in a_list])
     plan = Plan()

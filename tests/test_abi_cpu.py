@@ -92,6 +92,20 @@ def test_an_output_on_another_device_is_refused():
     assert sk._out(None, a, 4, 128, 1).device == a.device
 
 
+def test_a16w4_operands_are_checked_before_the_library():
+    import torch
+    aq = torch.empty((256, 512), dtype=torch.uint8, device="meta")
+    a_s = torch.empty((256, 32), dtype=torch.uint8, device="meta")
+    b = torch.empty((4, 1024), dtype=torch.bfloat16, device="meta")
+    assert sk._w4_dims(aq, a_s, b) == (4, 256, 1024, 1)
+    with pytest.raises(TypeError):
+        sk._w4_dims(aq, a_s, b.float())                 # activations are bf16
+    with pytest.raises(ValueError):
+        sk._w4_dims(aq, a_s, b.unsqueeze(0))            # mixed ranks
+    with pytest.raises(ValueError):
+        sk._w4_dims(aq, a_s[:, :16], b)                 # one scale per 32 k
+
+
 def test_version_and_strerror():
     assert sk.splitk_version() >= 10000
     for code, name in sk.STATUS.items():
