@@ -85,7 +85,9 @@ enum splitk_status {
     SPLITK_ERR_SCRATCH = -11,
     /* splitk_gemm_bf16_zerocopy(): a host buffer is not page-locked and
        mapped into the device address space. */
-    SPLITK_ERR_NOT_MAPPED = -12
+    SPLITK_ERR_NOT_MAPPED = -12,
+    /* splitk_gemm_bf16_noalloc(): the stream is capturing a CUDA graph. */
+    SPLITK_ERR_CAPTURE = -13
 };
 
 /* Flags of splitk_gemm_bf16_planned(). */
@@ -357,10 +359,13 @@ SPLITK_API int splitk_gemm_bf16_zerocopy(const void *a, const void *b_host, void
  * (with one 128-byte map per call, no valid call does).
  *
  * The first call on a device (with that device current) looks up the
- * array's device address once (cudaGetSymbolAddress); make that first call
- * before any stream capture.  Every call rewrites the whole map on `stream`
- * with a host-to-device copy ahead of its kernel, so nothing in the array
- * has to start at zero and the array keeps the last call's map.  All calls
+ * array's device address once (cudaGetSymbolAddress).  Every call rewrites
+ * the whole map on `stream` with a host-to-device copy ahead of its kernel,
+ * so nothing in the array has to start at zero and the array keeps the last
+ * call's map.  That copy reads a host buffer that lives only during the
+ * call, so a call on a stream that is capturing a CUDA graph is refused
+ * with SPLITK_ERR_CAPTURE, with nothing enqueued (a captured copy would
+ * read that buffer again at every replay).  All calls
  * on a device share that one array (each device has its own copy): calls
  * that overlap on the GPU, such as calls on two streams of one device,
  * race on it.  Calls issued in order on one stream do not overlap.

@@ -42,7 +42,7 @@ STATUS = {
     -3: "SPLITK_ERR_UNSUPPORTED_SPLIT", -4: "SPLITK_ERR_NO_FIT", -5: "SPLITK_ERR_CUDA",
     -6: "SPLITK_ERR_TIMEOUT", -7: "SPLITK_ERR_NULL", -8: "SPLITK_ERR_CACHE_FULL",
     -9: "SPLITK_ERR_UNSUPPORTED_DEVICE", -10: "SPLITK_ERR_BAD_PLAN",
-    -11: "SPLITK_ERR_SCRATCH", -12: "SPLITK_ERR_NOT_MAPPED",
+    -11: "SPLITK_ERR_SCRATCH", -12: "SPLITK_ERR_NOT_MAPPED", -13: "SPLITK_ERR_CAPTURE",
 }
 
 

@@ -1050,6 +1050,14 @@ SPLITK_API int splitk_gemm_bf16_noalloc(const void* a, const void* b, void* c, i
   int dev = -1;
   rc = current_device(&st, &dev);
   if (rc != SPLITK_OK) return rc;
+  // The tensor map is copied from a host variable of this call: a graph
+  // would copy it again at every replay, after the call has returned.
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) {
+    cudaGetLastError();
+    return SPLITK_ERR_CUDA;
+  }
+  if (cap != cudaStreamCaptureStatusNone) return SPLITK_ERR_CAPTURE;
   splitk_plan_t pl;
   rc = plan_impl(M, N, K, L, split_k, st->num_sms, st->smem_per_sm, st->smem_optin, &pl);
   if (rc != SPLITK_OK) return rc;
@@ -1295,6 +1303,7 @@ SPLITK_API const char* splitk_strerror(int code) {
     case SPLITK_ERR_BAD_PLAN: return "plan does not match the shape";
     case SPLITK_ERR_SCRATCH: return "the call needs more scratch than the allocation-free array holds";
     case SPLITK_ERR_NOT_MAPPED: return "host buffer is not page-locked and mapped into the device address space";
+    case SPLITK_ERR_CAPTURE: return "the allocation-free entry point cannot run inside a CUDA graph capture";
     default: return "unknown status code";
   }
 }

@@ -109,8 +109,16 @@ def test_a16w4_operands_are_checked_before_the_library():
 def test_version_and_strerror():
     assert sk.splitk_version() >= 10000
     for code, name in sk.STATUS.items():
-        assert sk.splitk_strerror(code)
+        assert sk.splitk_strerror(code) != "unknown status code", name
     assert sk.splitk_strerror(12345) == "unknown status code"
+
+
+def test_the_binding_knows_every_status_the_header_declares():
+    text = (ROOT / "include" / "splitk.h").read_text()
+    enum = text[text.index("enum splitk_status"):]
+    enum = enum[:enum.index("};")]
+    declared = {int(v): k for k, v in re.findall(r"(SPLITK_\w+)\s*=\s*(-?\d+)", enum)}
+    assert declared == sk.STATUS
 
 
 def _plan(M, N, K, L=1, split=0):

@@ -47,3 +47,23 @@ def test_two_calls_in_a_row_match_the_regular_entry_point():
     assert sk.splitk_get_status() == 0
     for a, b, ta, tb, ref, out, K, split in inputs:
         assert_parity(to_host(out), to_host(ref), a, b, K)
+
+
+def test_a_capturing_stream_is_refused_with_nothing_enqueued():
+    a, b = _case(73, 1, 4, 256, 1024)
+    ta, tb = to_dev(a), to_dev(b)
+    out = torch.full((1, 4, 256), 7.0, dtype=torch.bfloat16, device=ta.device)
+    sk.splitk_gemm_bf16_noalloc(ta, tb, out, split_k=4)          # the device's set-up, outside capture
+    torch.cuda.synchronize()
+    out.fill_(7.0)
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        with pytest.raises(sk.SplitKError) as e:
+            sk.splitk_gemm_bf16_noalloc(ta, tb, out, split_k=4)
+        out.mul_(1)                                              # the graph's one node
+    assert e.value.code == -13
+    g.replay()
+    torch.cuda.synchronize()
+    assert bool((out == 7.0).all())
+    assert sk.splitk_get_status() == 0
