@@ -436,7 +436,9 @@ SPLITK_API int splitk_debug_inject(unsigned flags);
  */
 SPLITK_API int splitk_set_trace(void *device_buffer, size_t bytes);
 
-/* Synchronizes every device the library used, then frees its caches. */
+/* Synchronizes every device the library used, then frees its caches.  A
+ * CUDA graph that captured calls of this library holds addresses of the freed
+ * tensor maps: do not replay it after this call (capture it again). */
 SPLITK_API void splitk_release(void);
 
 /* A static description of a status code. */

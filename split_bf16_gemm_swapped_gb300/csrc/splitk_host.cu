@@ -1291,7 +1291,7 @@ SPLITK_API void splitk_release(void) {
 SPLITK_API const char* splitk_strerror(int code) {
   switch (code) {
     case SPLITK_OK: return "success";
-    case SPLITK_ERR_INVALID_SHAPE: return "invalid shape (M, N, K, L >= 1; K a multiple of 8 with at least one 128-wide K tile per split rank)";
+    case SPLITK_ERR_INVALID_SHAPE: return "invalid shape (M, N, K, L >= 1; K a multiple of 8 with at least one 128-wide K tile per split rank; N, K, L and the grid within their limits)";
     case SPLITK_ERR_MISALIGNED: return "misaligned pointer (A and B need 16 bytes, C 2 bytes)";
     case SPLITK_ERR_UNSUPPORTED_SPLIT: return "split_k must be 0, 1, 2, 4 or 8";
     case SPLITK_ERR_NO_FIT: return "no tactic fits the shared-memory budget";
