@@ -231,6 +231,23 @@ def cpu_oracle_rate(w, budget_s: float, threads: int):
     return rate, sample, used
 
 
+def run_cpu_table(args):
+    """Extra lines, no GPU: the oracle on the host cores, all of them and one,
+    for the tiny, decode and sweep (M = 1, 16, 128) workloads, each a bounded
+    sample (a prefix of the weight rows when a pass would exceed the budget)."""
+    from split_bf16_gemm_swapped_gb300 import workloads as W
+    sweep = {w.M: w for w in W.all_sweep() if w.split_k == 1}
+    cases = [W.TINY, W.DECODE_M1, W.DECODE_M16, sweep[1], sweep[16], sweep[128]]
+    budget = max(1.0, args.cpu_budget / 4)
+    cores = host_cores()
+    for w in cases:
+        for threads in (cores, 1):
+            rate, sample, used = cpu_oracle_rate(w, budget, threads)
+            print(json.dumps({"cpu_table": describe(w), "impl": "oracle", "TB/s": rate,
+                              "GFLOP/s": rate * 1e3 * w.flops / w.bytes, "cores": used,
+                              "cpu": host_cpu_name(), "sample": sample}), flush=True)
+
+
 def run_reference(args, w):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -681,13 +698,17 @@ def main():
                     help="steps of the end-to-end host-I/O measurement (0 skips it)")
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of host time for the CPU oracle baseline")
+    ap.add_argument("--cpu-table", action="store_true",
+                    help="time the oracle alone (all host cores and one) on the fixed and sweep workloads")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
     if args.steps < 1:
         raise SystemExit("--steps must be >= 1")
     w = workload_by_name(args.workload)
-    if args.impl == "reference":
+    if args.cpu_table:
+        run_cpu_table(args)
+    elif args.impl == "reference":
         run_reference(args, w)
     elif args.sweep == "w4a16":
         run_sweep_w4(args)
