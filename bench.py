@@ -157,6 +157,29 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def clock_verdict(summary: dict) -> str:
+    """Whether a timed region's clock record makes its number acceptable:
+    thermal or hardware slowdown, or an SM clock well below its maximum with
+    no reason given (a leftover clock lock), rejects it; a power cap is
+    noted (normal for a long dense run on this part)."""
+    reasons = summary.get("reasons") or []
+    bad = [r for r in reasons if r in ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")]
+    if bad:
+        return "rejected: " + ", ".join(bad)
+    sm, smax = summary.get("sm_mhz"), summary.get("sm_max_mhz")
+    if sm is None or smax is None:
+        return "unsampled"
+    if "sw_power_cap" in reasons:
+        return "ok (sw_power_cap noted)"
+    if sm < 0.8 * smax:
+        return f"rejected: SM clock {sm:.0f} of {smax:.0f} MHz with no reason"
+    return "ok"
+
+
+def with_verdict(summary: dict) -> dict:
+    return dict(summary, verdict=clock_verdict(summary))
+
+
 def max_over_ranks(value: float, device=None) -> float:
     """The largest `value` over all ranks (the job's time is its slowest
     rank's); the value itself when no process group is running."""
@@ -539,7 +562,7 @@ def run_ours(args, w):
                 "isolated_launch_us": round(iso_us, 2),
                 "isolated_note": "one launch per graph replay, events around the replay"},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": args.steps, "clocks": clocks.summary(),
+            "gpu_launches": args.steps, "clocks": with_verdict(clocks.summary()),
             "parts": {"tbps": part_tbps, "median": statistics.median(part_tbps),
                       "note": f"the timed region in {parts} consecutive parts; value covers all of it"},
             "hot_l2": {"value": round(w.bytes / (hot_ms * 1e-3) / 1e12, 3), "unit": "TB/s",
