@@ -708,13 +708,17 @@ def run_sweep(args):
 
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200000)
-    ap.add_argument("--warmup", type=int, default=100)
-    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="decode_m1")
-    ap.add_argument("--sweep", choices=["sweep", "all", "w4a16"], default=None)
-    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--gpus", type=int, default=1,
+                    help="GPUs (one rank each under torch.distributed.run; each runs a replica)")
+    ap.add_argument("--steps", type=int, default=200000, help="timed steps (one GEMM call each)")
+    ap.add_argument("--warmup", type=int, default=100, help="untimed steps first (at least 3)")
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours",
+                    help="reference: the float64 CPU oracle on the host cores")
+    ap.add_argument("--workload", default="decode_m1",
+                    help="decode_m1 (the default line), decode_m16, tiny, wide_s2, wide_s4, sweep_m<M>_s<split>")
+    ap.add_argument("--sweep", choices=["sweep", "all", "w4a16"], default=None,
+                    help="extra lines: the M x split sweep, that plus the fixed workloads, or A16W4")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the timed oracle leg")
     ap.add_argument("--rotate", type=int, default=0,
                     help="weight copies to rotate (default: enough for 4x the L2 cache)")
     ap.add_argument("--e2e-steps", type=int, default=2000,
