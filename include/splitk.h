@@ -167,13 +167,7 @@ typedef struct splitk_plan_t {
                               decoded into a 32 KiB bf16 stage in shared
                               memory, so that every tile is decoded before the
                               programmatic-dependent-launch wait returns     */
-    int b_multicast;       /* 0 or 1: off.  2, 4 or 8 (the page's ring only,
-                              split_k * b_multicast <= 8): that many output
-                              tiles along N form an N-group (cluster
-                              (split_k, b_multicast, 1), grid[1] padded to
-                              whole groups) whose CTAs take turns loading
-                              each activation K tile once and multicasting it
-                              to the group                                   */
+    int reserved;          /* must be 0                                      */
 } splitk_plan_t;
 
 /*

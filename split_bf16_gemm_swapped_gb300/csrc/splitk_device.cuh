@@ -160,17 +160,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* map, int c
       : "memory");
 }
 
-// The same box written to the same shared-memory offset of every CTA of the
-// cluster in `cta_mask`, completing bytes on each one's mbarrier at `bar`.
-__device__ __forceinline__ void tma_load_3d_multicast(uint32_t dst, const void* map, int c0, int c1, int c2,
-                                                      uint32_t bar, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
-      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "h"(cta_mask)
-      : "memory");
-}
-
 // ---------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
@@ -231,16 +220,6 @@ __device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t s_desc
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                : "memory");
-}
-
-// The same, arriving on the mbarrier at offset `bar` of every CTA of the
-// cluster in `cta_mask`.
-__device__ __forceinline__ void mma_commit_multicast(uint32_t bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-          bar),
-      "h"(cta_mask)
-      : "memory");
 }
 
 // Four consecutive 32-bit TMEM columns of this thread's lane.

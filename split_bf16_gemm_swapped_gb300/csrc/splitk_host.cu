@@ -417,7 +417,7 @@ int check_plan_w4(const splitk_plan_t& pl, int M, int N, int K, int L, size_t sm
   const int kt = (T + pl.split_k - 1) / pl.split_k;
   if (pl.k_tiles_per_cta != kt || pl.stages != kt) return SPLITK_ERR_BAD_PLAN;
   if (kt > kMaxStages) return SPLITK_ERR_NO_FIT;
-  if (pl.b_multicast > 1) return SPLITK_ERR_BAD_PLAN;
+  if (pl.reserved != 0) return SPLITK_ERR_BAD_PLAN;
   const long long m_tiles = tiles_of(M, pl.mma_n);
   const long long n_tiles = ((long long)N + kMmaM - 1) / kMmaM;
   if (n_tiles > 65535 || L > 65535) return SPLITK_ERR_INVALID_SHAPE;
@@ -468,16 +468,10 @@ int check_plan(const splitk_plan_t& pl, int M, int N, int K, int L, size_t smem_
   const long long m_tiles = tiles_of(M, pl.mma_n);
   const long long n_tiles = ((long long)N + kMmaM - 1) / kMmaM;
   if (m_tiles * pl.split_k > 0x7FFFFFFFLL) return SPLITK_ERR_INVALID_SHAPE;
-  // Multicast N-groups of mc tiles (the grid padded to whole groups; padded
-  // tiles read zeros and store nothing): the page's ring only, and a
-  // cluster of at most 8 CTAs.
-  const int mcg = pl.b_multicast > 1 ? pl.b_multicast : 1;
-  if (pl.b_multicast < 0 || (mcg != 1 && mcg != 2 && mcg != 4 && mcg != 8)) return SPLITK_ERR_BAD_PLAN;
-  if (mcg > 1 && (pl.b_resident != 0 || pl.split_k * mcg > 8)) return SPLITK_ERR_BAD_PLAN;
-  const long long n_grid = (n_tiles + mcg - 1) / mcg * mcg;
-  if (n_grid > 65535 || L > 65535) return SPLITK_ERR_INVALID_SHAPE;
-  if (pl.grid[0] != (unsigned)(pl.split_k * m_tiles) || pl.grid[1] != (unsigned)n_grid ||
-      pl.grid[2] != (unsigned)L || pl.cluster[0] != (unsigned)pl.split_k || pl.cluster[1] != (unsigned)mcg ||
+  if (pl.reserved != 0) return SPLITK_ERR_BAD_PLAN;
+  if (n_tiles > 65535 || L > 65535) return SPLITK_ERR_INVALID_SHAPE;
+  if (pl.grid[0] != (unsigned)(pl.split_k * m_tiles) || pl.grid[1] != (unsigned)n_tiles ||
+      pl.grid[2] != (unsigned)L || pl.cluster[0] != (unsigned)pl.split_k || pl.cluster[1] != 1 ||
       pl.cluster[2] != 1) {
     return SPLITK_ERR_BAD_PLAN;
   }
@@ -768,7 +762,6 @@ void fill_params(const splitk_plan_t& pl, int M, int N, int K, int L, uint32_t d
   p->tmem_tile_col0 = tmem_tile_col0(pl.mma_n, pl.mma_issuers);
   p->mma_issuers = pl.mma_issuers;
   p->b_loader = pl.b_loader;
-  p->mc = pl.b_multicast > 1 ? pl.b_multicast : 1;
   p->w4_smem_tiles = pl.w4_smem_tiles;
   p->l2_prefetch = pl.l2_prefetch;
   p->trace = g_trace.load(std::memory_order_relaxed);
@@ -781,7 +774,6 @@ LaunchArgs launch_args(const splitk_plan_t& pl, bool pdl) {
   la.w4 = pl.weight_format == SPLITK_WEIGHTS_E2M1_E8M0;
   la.grid = dim3(pl.grid[0], pl.grid[1], pl.grid[2]);
   la.cluster_x = (unsigned)pl.split_k;
-  la.cluster_y = pl.b_multicast > 1 ? (unsigned)pl.b_multicast : 1u;
   la.smem_bytes = pl.smem_bytes;
   la.pdl = pdl;
   return la;

@@ -99,7 +99,6 @@ struct KernelParams {
   int b_loader;               // 0: TMA (activation warp); 1: epilogue threads
   int w4_smem_tiles;          // A16W4: 1 = the tile after the TMEM slots is decoded into a bf16 stage in shared memory
   int l2_prefetch;            // 1: weight tiles not on chip before the PDL wait prefetched to L2
-  int mc;                     // CTAs of an N-group sharing each activation tile by multicast (1: none)
   unsigned long long* trace;  // per-CTA %globaltimer stamps, or null
   unsigned trace_ctas;        // CTAs the trace buffer holds
 };
@@ -130,7 +129,6 @@ struct LaunchArgs {
   bool w4;                    // A16W4 weights
   dim3 grid;
   unsigned cluster_x;
-  unsigned cluster_y;         // the multicast N-group
   size_t smem_bytes;
   bool pdl;
 };

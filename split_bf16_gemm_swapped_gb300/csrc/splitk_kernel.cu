@@ -17,8 +17,7 @@
 //               L2 evict_first, issued before the programmatic-dependent-launch
 //               wait; then launch_dependents (SplitKGemm.weight_warp)
 //   warp 1      activation (B) producer: griddepcontrol.wait, then TMA
-//               (SplitKGemm.activation_warp); with a cluster multicast group,
-//               the group's CTAs take turns loading each tile for all of them
+//               (SplitKGemm.activation_warp)
 //   warp 2      TMEM allocation, tcgen05.mma issue (even K tiles when there
 //               are two issuers), TMEM release (mma_warp)
 //   warp 3      second MMA issuer (odd K tiles, own accumulator) or idle; it
@@ -33,7 +32,7 @@
 // page's _spin_bounded: a timeout records a diagnostic, sets a sticky failed
 // flag, and the CTA's later waits give up at once); TMEM is always released.
 // A CTA whose shared memory a peer may still address (aliased or multi-round
-// mailboxes, multicast groups) leaves only after a final cluster barrier; a
+// mailboxes) leaves only after a final cluster barrier; a
 // CTA whose wait failed first drains (bounded) the copies it issued and the
 // partials addressed to it, so a failed launch leaves no copy in flight into
 // a departed CTA.
@@ -191,15 +190,8 @@ __global__ void __launch_bounds__(kThreads, 3)
   const int lane = (int)(threadIdx.x & 31);
   const int split = p.split;
   const int stages = p.stages;
-  // The cluster is (split, mc): x the K ranks of one output tile, y the mc
-  // tiles of an N-group that share each activation tile by multicast.
-  const int mc = p.mc;
-  const int crank = (split > 1 || mc > 1) ? (int)dev::cluster_ctarank() : 0;
-  const int rank = crank % split;                  // K rank
-  const int yc = crank / split;                    // place in the N-group
-  const uint32_t peer0 = (uint32_t)(yc * split);   // cluster rank of K rank 0 of this tile
-  uint16_t mc_mask = 0;                            // the N-group's CTAs of this K rank
-  for (int j = 0; j < mc; ++j) mc_mask |= (uint16_t)(1u << (rank + split * j));
+  // The cluster is the split K ranks of one output tile; rank 0 owns the tile.
+  const int rank = split > 1 ? (int)dev::cluster_ctarank() : 0;
   const int m_tile = (int)blockIdx.x / split;
   const int n0 = (int)blockIdx.y * kMmaM;
   const int m0 = m_tile * MMA_N;
@@ -251,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 3)
     if (lane == 0) {
       for (int s = 0; s < stages; ++s) {
         dev::mbar_init(bar_full0 + 8u * s, b_res ? 1u : 2u);   // A (and B when it rides the ring)
-        dev::mbar_init(bar_empty0 + 8u * s, (uint32_t)mc);   // every consumer of the N-group
+        dev::mbar_init(bar_empty0 + 8u * s, 1u);             // the stage's MMA commit
       }
       dev::mbar_init(bar_b, p.b_loader ? (uint32_t)kEpiThreads : 1u);
       dev::mbar_init(bar_mma_done, (uint32_t)p.mma_issuers);
@@ -383,16 +375,8 @@ __global__ void __launch_bounds__(kThreads, 3)
         const uint32_t dst = sB + (uint32_t)s * kBStage;
         const int k = (kt0 + kt) * kCtaK;
         dev::mbar_arrive_expect_tx(full, kBStage);
-        if (mc == 1) {
-          dev::tma_load_3d(dst, &b_map, k, m0, l, full);
-          dev::tma_load_3d(dst + kBBox, &b_map, k + kAtomK, m0, l, full);
-        } else if (kt % mc == yc) {
-          // this CTA's turn: the tile goes to the whole N-group (the stage is
-          // free in all of them: each CTA's empty barrier counts every
-          // group member's release)
-          dev::tma_load_3d_multicast(dst, &b_map, k, m0, l, full, mc_mask);
-          dev::tma_load_3d_multicast(dst + kBBox, &b_map, k + kAtomK, m0, l, full, mc_mask);
-        }
+        dev::tma_load_3d(dst, &b_map, k, m0, l, full);
+        dev::tma_load_3d(dst + kBBox, &b_map, k + kAtomK, m0, l, full);
       }
     }
   } else if (warp == 2 || warp == 3) {
@@ -504,11 +488,7 @@ __global__ void __launch_bounds__(kThreads, 3)
           dev::mma_bf16(d_acc, dev::smem_desc_sw128(a_st + a_off), dev::smem_desc_sw128(b_st + b_off), kIdesc,
                         (first | (uint32_t)kk) != 0u ? 1u : 0u);
         }
-        if (mc == 1) {
-          dev::mma_commit(bar_empty0 + 8u * s);  // stage free once these MMAs finish
-        } else {
-          dev::mma_commit_multicast(bar_empty0 + 8u * s, mc_mask);   // ... in every CTA of the N-group
-        }
+        dev::mma_commit(bar_empty0 + 8u * s);  // stage free once these MMAs finish
       }
       dev::mma_commit(bar_mma_done);           // this issuer's accumulator complete
     }
@@ -674,8 +654,8 @@ __global__ void __launch_bounds__(kThreads, 3)
       const int dst_rank = et / R;
       const bool publish = !(p.inject & kInjectSkipPublish);
       const uint32_t slot = ((uint32_t)(rank * ncols) * (uint32_t)R + (uint32_t)(et - dst_rank * R)) * 4u;
-      const uint32_t r_bar = dev::mapa(bar_reduce, peer0 + (uint32_t)dst_rank);
-      const uint32_t r_mail = dev::mapa(sMail, peer0 + (uint32_t)dst_rank) + slot;
+      const uint32_t r_bar = dev::mapa(bar_reduce, (uint32_t)dst_rank);
+      const uint32_t r_mail = dev::mapa(sMail, (uint32_t)dst_rank) + slot;
 #pragma unroll 1
       for (int g = 0; g * 16 < ncols; ++g) {
         uint32_t v[16];
@@ -747,9 +727,9 @@ __global__ void __launch_bounds__(kThreads, 3)
         dev::tc_fence_before();
         dev::mbar_arrive(bar_tmem_empty);
         if (publish) {
-          const uint32_t r_bar = dev::mapa(bar_reduce, peer0);
+          const uint32_t r_bar = dev::mapa(bar_reduce, 0u);
           const uint32_t r_mail =
-              dev::mapa(sMail, peer0) + (uint32_t)((rank - 1) * ncols) * kColumnBytes + (uint32_t)et * 4u;
+              dev::mapa(sMail, 0u) + (uint32_t)((rank - 1) * ncols) * kColumnBytes + (uint32_t)et * 4u;
 #pragma unroll
           for (int col = 0; col < 4; ++col) {
             if (col < ncols) dev::st_async_b32(r_mail + (uint32_t)col * kColumnBytes, v[col], r_bar);
@@ -762,7 +742,7 @@ __global__ void __launch_bounds__(kThreads, 3)
             dev::mbar_arrive_expect_tx(bar_reduce, (uint32_t)(split - 1) * (uint32_t)ncols * kColumnBytes);
           }
           if (!p.mailbox_dedicated && et >= 1 && et < split) {
-            dev::mbar_arrive_remote(dev::mapa(bar_ready, peer0 + (uint32_t)et));
+            dev::mbar_arrive_remote(dev::mapa(bar_ready, (uint32_t)et));
           }
         }
         float x[4];
@@ -811,11 +791,11 @@ __global__ void __launch_bounds__(kThreads, 3)
           // issuing thread's earlier memory operations, so arrivals issued one
           // after another from a single thread would serialise into round trips.
           if (need_ready && et >= 1 && et < split) {
-            dev::mbar_arrive_remote(dev::mapa(bar_ready, peer0 + (uint32_t)et));
+            dev::mbar_arrive_remote(dev::mapa(bar_ready, (uint32_t)et));
           }
         }
-        const uint32_t r_bar = dev::mapa(bar_reduce, peer0);
-        const uint32_t r_mail = dev::mapa(sMail, peer0) + (uint32_t)((rank - 1) * rc) * kColumnBytes;
+        const uint32_t r_bar = dev::mapa(bar_reduce, 0u);
+        const uint32_t r_mail = dev::mapa(sMail, 0u) + (uint32_t)((rank - 1) * rc) * kColumnBytes;
         bool publish = split > 1 && !owner && !(p.inject & kInjectSkipPublish);
         bool first_group = true;
 
@@ -957,10 +937,7 @@ __global__ void __launch_bounds__(kThreads, 3)
   // still reducing.  (A peer later than rank 0's whole wait limit would
   // publish into a departed CTA; the limit is chosen so that never happens.)
   const int tile_quads = (((p.M - m0) < MMA_N ? (p.M - m0) : MMA_N) + 3) >> 2;
-  // (With multicast every CTA stays: its releases arrive on the group's
-  // barriers and the group's activation tiles land in its shared memory.)
-  const bool final_barrier =
-      mc > 1 || (split > 1 && !(p.mailbox_dedicated && tile_quads <= p.mailbox_quads));
+  const bool final_barrier = split > 1 && !(p.mailbox_dedicated && tile_quads <= p.mailbox_quads);
   if (final_barrier) {
     // No CTA leaves while a peer may still address its shared memory.  The
     // arrival is relaxed (a release would wait for the tile's global
@@ -991,7 +968,7 @@ cudaError_t launch_t(const LaunchArgs& la, const CUtensorMap& b_map, const Kerne
   int n = 0;
   attrs[n].id = cudaLaunchAttributeClusterDimension;
   attrs[n].val.clusterDim.x = la.cluster_x;
-  attrs[n].val.clusterDim.y = la.cluster_y;
+  attrs[n].val.clusterDim.y = 1;
   attrs[n].val.clusterDim.z = 1;
   ++n;
   if (la.pdl) {

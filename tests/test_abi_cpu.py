@@ -407,6 +407,12 @@ def test_plan_check_rejects_what_a_launch_would():
     bad.smem_bytes += 32768
     assert _check(bad, M, N, K, L) == -10
     assert _check(p, M, N, K + 8, L) == -10             # another shape
+    bad = sk.Plan.from_buffer_copy(p)
+    bad.reserved = 2                                    # the reserved field must stay 0
+    assert _check(bad, M, N, K, L) == -10
+    bad = sk.Plan.from_buffer_copy(p)
+    bad.cluster[1] = 2                                  # clusters span the K ranks of one tile only
+    assert _check(bad, M, N, K, L) == -10
 
 
 @pytest.mark.parametrize("args", [(1, 7168, 2048, 1, 4), (16, 4096, 7168, 1, 8), (4, 256, 1024, 1, 0),

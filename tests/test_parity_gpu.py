@@ -87,33 +87,6 @@ def test_seeded_random_shapes_match_the_oracle():
     assert len(kinds) >= 8                  # the draw reaches many plan families
 
 
-def _multicast(base, N, g):
-    """`base` (a ring plan) with N-groups of g tiles sharing each activation
-    tile by multicast; the grid padded to whole groups."""
-    p = sk.Plan.from_buffer_copy(base)
-    n_tiles = -(-N // 128)
-    p.b_multicast = g
-    p.grid[1] = -(-n_tiles // g) * g
-    p.cluster[1] = g
-    return p
-
-
-@pytest.mark.parametrize("M,N,K,L,split,g", [
-    (64, 2048, 4096, 1, 1, 2), (64, 2048, 4096, 1, 2, 4), (128, 600, 2048, 2, 2, 4),
-    (33, 1000, 3000, 1, 1, 8), (100, 900, 2048, 2, 4, 2), (16, 700, 4096, 1, 2, 2),
-])
-def test_activation_multicast_gives_the_same_bits(M, N, K, L, split, g):
-    """N-groups of g tiles loading each activation tile once and multicasting
-    it (grid padded to whole groups when N is not) give the bits of the same
-    ring without multicast, and match the oracle."""
-    a, b = _draw(L, M, N, K, seed=2500 + M + g)
-    ring = _ring(sk.splitk_plan(M, N, K, L, split), M)
-    want = gemm_gpu(a, b, plan=ring)
-    got = gemm_gpu(a, b, plan=_multicast(ring, N, g))
-    assert np.array_equal(got, want)
-    assert_parity(got, oracle_full(a, b), a, b, K)
-
-
 @pytest.mark.parametrize("split", [1, 4])
 def test_batched_L_and_ragged_N(split):
     L, M, N, K = 3, 7, 200, 2048
