@@ -18,8 +18,8 @@
  *   value       x = sigma * z, times `outlier_scale` where the uniform drawn
  *               from stream `outlier_stream` at the same index is below
  *               `outlier_p`.
- *   bf16        x is rounded to binary32 (C cast, nearest-even), then to bf16
- *               (nearest-even on the binary32 bits).
+ *   bf16        x is rounded once, directly from binary64 to bf16, to
+ *               nearest with ties to even (no intermediate binary32).
  */
 #include <math.h>
 #include <pthread.h>
@@ -56,13 +56,32 @@ static inline double uniform_closed0(uint64_t w)  /* [0, 1) */
     return (double)(w >> 11) * 0x1p-53;
 }
 
+/*
+ * binary64 -> bf16 bits, one rounding to nearest-even.  A bf16 number keeps 8
+ * significant bits, a binary64 53: for |x| in bf16's normal range the 45 low
+ * significand bits of x are rounded away on its bit pattern (adding half an
+ * ulp minus one, plus the kept lsb, carries into the exponent when needed),
+ * which leaves a binary64 that binary32 holds exactly.  Below 2^-126 the
+ * spacing is the fixed 2^-133, so x * 2^133 is rounded to an integer with the
+ * default (nearest-even) mode.  Past the largest finite bf16: infinity.
+ */
 static inline uint16_t to_bf16_bits(double x)
 {
-    float f = (float)x;
-    uint32_t u;
-    memcpy(&u, &f, sizeof u);
-    u += 0x7FFFu + ((u >> 16) & 1u);
-    return (uint16_t)(u >> 16);
+    const double ax = fabs(x);
+    double r;
+    if (ax < 0x1p-126) {
+        r = nearbyint(x * 0x1p133) * 0x1p-133;
+    } else {
+        uint64_t u;
+        memcpy(&u, &x, sizeof u);
+        u += 0x00000FFFFFFFFFFFULL + ((u >> 45) & 1u);
+        u &= ~0x00001FFFFFFFFFFFULL;
+        memcpy(&r, &u, sizeof r);
+    }
+    float f = fabs(r) >= 0x1p128 ? copysignf(INFINITY, (float)x) : (float)r;
+    uint32_t b;
+    memcpy(&b, &f, sizeof b);
+    return (uint16_t)(b >> 16);
 }
 
 struct syn_job {

@@ -2,8 +2,8 @@
 
 Holds no GEMM arithmetic: it only draws normal numbers and rounds them to
 bf16 bit patterns (see ``csrc/synthetic.c`` for the exact generator:
-SplitMix64 counter stream + Box-Muller, rounded f64 -> f32 -> bf16, each
-step to nearest-even).
+SplitMix64 counter stream + Box-Muller, rounded once from f64 to bf16,
+nearest-even).
 
 Streams: A (weights) draws from stream 0, B (activations) from stream 1, the
 outlier mask of B from stream 2, all under the workload's seed.

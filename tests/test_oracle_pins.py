@@ -426,3 +426,30 @@ def test_w4a16_pins_catch_planted_mistakes():
     for name, (q, s) in {"nibbles swapped": (swapped, As), "scale per row": (Aq, one_scale),
                          "scale blocks": (Aq, reversed_blocks)}.items():
         assert not np.array_equal(oracle.gemm_w4a16(q, s, B), exact), name
+
+
+def test_w4_elements_equal_exact_rationals_one_by_one():
+    """The per-element A16W4 path, pinned directly: every output of a small
+    batched shape against the exact rational sum rounded once, and on a
+    larger shape against the whole-GEMM path (itself pinned above) at the
+    first, last and scattered flat indices l*M*N + m*N + n."""
+    from split_bf16_gemm_swapped_gb300 import synthetic
+    L, M, N, K = 2, 3, 4, 64
+    Aq, As = synthetic.w4_weights(L, N, K, seed=81)
+    B = synthetic.normal_bf16((L, M, K), seed=81, stream=1, sigma=1.0)
+    idx = np.arange(L * M * N)
+    got = oracle.w4_elements(Aq, As, B, idx)
+    for i in idx:
+        l, m, n = i // (M * N), (i // N) % M, i % N
+        s = sum(_exact_w4(Aq, As, l, n, k) * _exact.value(int(B[l, m, k])) for k in range(K))
+        assert got[i] == _exact.round_bf16(s), (l, m, n)
+    L, M, N, K = 2, 5, 300, 512
+    Aq, As = synthetic.w4_weights(L, N, K, seed=82)
+    B = synthetic.normal_bf16((L, M, K), seed=82, stream=1, sigma=1.0)
+    full = oracle.gemm_w4a16(Aq, As, B).reshape(-1)
+    idx = np.unique(np.concatenate([[0, 1, N - 1, N, M * N, L * M * N - 1],
+                                    np.random.default_rng(5).integers(0, L * M * N, 400)]))
+    assert np.array_equal(oracle.w4_elements(Aq, As, B, idx), full[idx])
+    # an index read with M and N exchanged would pick other outputs
+    swapped = (idx // (M * N)) * M * N + (idx % N) * M + (idx // N) % M
+    assert not np.array_equal(full[swapped], full[idx])

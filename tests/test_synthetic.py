@@ -1,6 +1,6 @@
 """The seeded input generator: a numpy restatement of its published recipe
-(SplitMix64, Box-Muller, f64 -> f32 -> bf16 nearest-even), independence from
-the thread count and offset, and the drawn distributions."""
+(SplitMix64, Box-Muller, one f64 -> bf16 nearest-even rounding), independence
+from the thread count and offset, and the drawn distributions."""
 from __future__ import annotations
 
 import numpy as np
@@ -35,9 +35,33 @@ def _numpy_draw(count, seed, stream, sigma, p=0.0, scale=1.0, offset=0):
     if p > 0:
         uo = (_words(seed, synthetic.STREAM_OUTLIER, i) >> np.uint64(11)).astype(np.float64) * 2.0 ** -53
         x = np.where(uo < p, x * scale, x)
-    f = x.astype(np.float32).view(np.uint32).astype(np.uint64)
-    f = (f + np.uint64(0x7FFF) + ((f >> np.uint64(16)) & np.uint64(1))) >> np.uint64(16)
-    return f.astype(np.uint16)
+    return _f64_to_bf16_exact(x)
+
+
+def _f64_to_bf16_exact(x):
+    """One nearest-even rounding of float64 values to bf16 bits, by exact
+    rational arithmetic (only for the normal range these draws reach)."""
+    from fractions import Fraction
+    out = np.empty(x.shape, dtype=np.uint16)
+    for i, v in enumerate(x.ravel()):
+        f = Fraction(float(v))
+        if f == 0:
+            out.flat[i] = 0x8000 if np.signbit(v) else 0
+            continue
+        mag = abs(f)
+        e = mag.numerator.bit_length() - mag.denominator.bit_length()
+        if Fraction(2) ** e > mag:
+            e -= 1                                   # 2^e <= |v| < 2^(e+1)
+        q = Fraction(2) ** (e - 7)                   # bf16 spacing in that binade
+        n = mag / q
+        k = n.numerator // n.denominator
+        rem = n - k
+        if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and k % 2 == 1):
+            k += 1
+        r = float(k * q)
+        bits = np.array([r], dtype=np.float32).view(np.uint32)[0] >> 16
+        out.flat[i] = int(bits) | (0x8000 if v < 0 else 0)
+    return out
 
 
 def test_splitmix64_reference_words():
@@ -53,8 +77,8 @@ def test_splitmix64_reference_words():
 def test_c_generator_matches_numpy_restatement():
     for (seed, stream, sigma, p, sc, off) in [(0, 0, 0.02, 0, 1, 0), (2, 1, 1.0, 0.01, 30.0, 0),
                                               (3, 1, 1.0, 0.0, 1.0, 12345)]:
-        got = synthetic.normal_bf16(20001, seed, stream, sigma, p, sc, offset=off, threads=1)
-        ref = _numpy_draw(20001, seed, stream, sigma, p, sc, offset=off)
+        got = synthetic.normal_bf16(4001, seed, stream, sigma, p, sc, offset=off, threads=1)
+        ref = _numpy_draw(4001, seed, stream, sigma, p, sc, offset=off)
         # libm may differ from numpy's log/sin/cos in the last bit; that can flip a
         # bf16 rounding only at an exact binary32 tie, i.e. essentially never.
         assert np.mean(got != ref) < 1e-4
@@ -78,3 +102,16 @@ def test_distributions():
     frac_big = np.mean(np.abs(vb) > 8.0)     # ~1% scaled by 30 lands mostly beyond 8
     assert 0.006 < frac_big < 0.011
     assert vb.max() > 60.0
+
+
+def test_the_restatement_rounds_once_from_float64():
+    """A value just above the midpoint of two bf16 numbers, which binary32
+    rounds onto the midpoint itself: one rounding goes up; a detour through
+    binary32 would then tie to even and go down.  The C generator is held to
+    this restatement above."""
+    x = 1.0 + 2.0 ** -8 + 2.0 ** -40            # midpoint of 1 and 1 + 2^-7, plus a little
+    assert np.float32(x) == np.float32(1.0 + 2.0 ** -8)
+    assert _f64_to_bf16_exact(np.array([x]))[0] == 0x3F81
+    assert _f64_to_bf16_exact(np.array([-x]))[0] == 0xBF81
+    ties = np.array([1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8])   # exact ties: to the even neighbour
+    assert _f64_to_bf16_exact(ties).tolist() == [0x3F80, 0x3F82]
