@@ -363,6 +363,10 @@ SPLITK_API int splitk_gemm_bf16_zerocopy(const void *a, const void *b_host, void
  * on a device share that one array (each device has its own copy): calls
  * that overlap on the GPU, such as calls on two streams of one device,
  * race on it.  Calls issued in order on one stream do not overlap.
+ *
+ * The array's device address is looked up once per device and kept for the
+ * life of the process (as are the plan's device properties): a
+ * cudaDeviceReset() after the first call on a device is not supported.
  */
 SPLITK_API int splitk_gemm_bf16_noalloc(const void *a, const void *b, void *c,
                                         int M, int N, int K, int L, int split_k,
@@ -429,6 +433,18 @@ SPLITK_API int splitk_debug_inject(unsigned flags);
  * reached stay as they were.  NULL (or bytes = 0) turns tracing off.
  */
 SPLITK_API int splitk_set_trace(void *device_buffer, size_t bytes);
+
+/*
+ * The memory the library owns on the current device (no counterpart on the
+ * method's pages; a library accounting call): *device_bytes of device memory
+ * (the tensor-map pool of A, 0 until the first call that needs it),
+ * *host_bytes of page-locked host memory (the pool's mirror) and *maps
+ * tensor maps of A in the pool.  Any of the pointers may be NULL.  Reads the
+ * library's own bookkeeping only: no allocation, no synchronisation, and no
+ * CUDA call but the lookup of the current device
+ * (SPLITK_ERR_UNSUPPORTED_DEVICE if there is none).
+ */
+SPLITK_API int splitk_cache_info(size_t *device_bytes, size_t *host_bytes, int *maps);
 
 /* Synchronizes every device the library used, then frees its caches.  A
  * CUDA graph that captured calls of this library holds addresses of the freed

@@ -28,7 +28,7 @@ __all__ = [
     "splitk_plan_w4a16", "splitk_plan_w4a16_for", "splitk_gemm_w4a16", "splitk_gemm_w4a16_planned",
     "splitk_get_fault",
     "splitk_get_status",
-    "splitk_set_wait_limit_ns", "splitk_debug_inject", "splitk_release",
+    "splitk_set_wait_limit_ns", "splitk_debug_inject", "splitk_release", "splitk_cache_info",
     "splitk_strerror", "splitk_version", "splitk_set_trace", "FLAG_NO_PDL",
     "INJECT_SKIP_PUBLISH", "TRACE_SLOTS", "TRACE_FIELDS",
     "STATUS",
@@ -152,6 +152,8 @@ def load_library():
     lib.splitk_set_trace.restype = i
     lib.splitk_release.argtypes = []
     lib.splitk_release.restype = None
+    lib.splitk_cache_info.argtypes = [ctypes.POINTER(sz), ctypes.POINTER(sz), ctypes.POINTER(i)]
+    lib.splitk_cache_info.restype = i
     lib.splitk_strerror.argtypes = [i]
     lib.splitk_strerror.restype = ctypes.c_char_p
     lib.splitk_version.argtypes = []
@@ -491,6 +493,15 @@ TRACE_FIELDS = ("sm_rank", "start", "synced", "weights_issued", "act_ready", "fi
 
 def splitk_release() -> None:
     load_library().splitk_release()
+
+
+def splitk_cache_info() -> dict:
+    """The memory the library owns on the current CUDA device: device and
+    page-locked host bytes of its tensor-map pool, and the maps in it."""
+    dev_b, host_b, maps = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_int()
+    _check(load_library().splitk_cache_info(ctypes.byref(dev_b), ctypes.byref(host_b), ctypes.byref(maps)),
+           "splitk_cache_info")
+    return {"device_bytes": dev_b.value, "host_bytes": host_b.value, "maps": maps.value}
 
 
 def splitk_strerror(code: int) -> str:

@@ -1076,6 +1076,11 @@ SPLITK_API int splitk_gemm_bf16_noalloc(const void* a, const void* b, void* c, i
       !encode_3d(&b_map, b, (uint64_t)K, (uint64_t)M, (uint64_t)L, (uint32_t)pl.mma_n)) {
     return SPLITK_ERR_CUDA;
   }
+  // The source is a pageable local: cudaMemcpyAsync returns only once it has
+  // been staged, so it may go out of scope afterwards.  The same device
+  // address is rewritten by every call; the kernel orders this generic-proxy
+  // write before its TMA loads with fence.proxy.tensormap::generic.acquire at
+  // its start, which the copy precedes in stream order.
   if (cudaMemcpyAsync(scratch_map, &a_map, sizeof(CUtensorMap), cudaMemcpyHostToDevice, s) !=
       cudaSuccess) {
     cudaGetLastError();
@@ -1255,6 +1260,21 @@ SPLITK_API int splitk_set_trace(void* device_buffer, size_t bytes) {
   const size_t ctas = device_buffer ? bytes / (sizeof(unsigned long long) * kTraceSlots) : 0;
   g_trace_ctas.store((unsigned)std::min<size_t>(ctas, 0xFFFFFFFFu));
   g_trace.store(ctas ? static_cast<unsigned long long*>(device_buffer) : nullptr);
+  return SPLITK_OK;
+}
+
+SPLITK_API int splitk_cache_info(size_t* device_bytes, size_t* host_bytes, int* maps) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return SPLITK_ERR_UNSUPPORTED_DEVICE;
+  }
+  const DeviceState& st = g_dev[dev];
+  const size_t pool = sizeof(CUtensorMap) * (size_t)kMapPoolSlots;
+  if (device_bytes) *device_bytes = st.d_pool ? pool : 0u;
+  if (host_bytes) *host_bytes = st.h_pool ? pool : 0u;
+  if (maps) *maps = st.d_pool ? st.used : 0;
   return SPLITK_OK;
 }
 

@@ -237,3 +237,74 @@ def test_tune_measures_candidates_and_returns_a_plan_that_computes_the_product()
     c = sk.splitk_gemm_bf16_planned(a_list[2], tb, None, plan)
     torch.cuda.synchronize()
     assert_parity(to_host(c), oracle.gemm(a, b), a, b, K)
+
+
+def test_trace_stamps_stay_in_their_buffer_are_ordered_and_stop_when_off():
+    """splitk_set_trace: a buffer for fewer CTAs than the grid receives the
+    stamps of the first CTAs only; a CTA's stamps taken by one thread are in
+    time order, stamps a CTA never reaches stay as they were, words past the
+    buffer's CTAs are untouched; tracing off stops every write."""
+    w = workloads.DECODE_M1                             # 224 CTAs: 56 tiles x split 4
+    a, b = w.make_a(), w.make_b()
+    ta, tb = to_dev(a), to_dev(b)
+    plan = sk.splitk_plan(w.M, w.N, w.K, w.L, w.split_k)
+    grid = plan.grid[0] * plan.grid[1] * plan.grid[2]
+    traced = 100                                        # CTAs the buffer holds
+    SENT = 0x5A5A5A5A5A5A5A5A
+    buf = torch.full(((grid + 8) * sk.TRACE_SLOTS,), SENT, dtype=torch.int64, device=DEV)
+    torch.cuda.synchronize()
+    sk.splitk_set_trace(buf[: traced * sk.TRACE_SLOTS])
+    try:
+        c = sk.splitk_gemm_bf16(ta, tb, split_k=w.split_k)
+        torch.cuda.synchronize()
+    finally:
+        sk.splitk_set_trace(None)
+    assert sk.splitk_get_status() == 0
+    assert_parity(to_host(c), oracle.gemm(a, b, threads=8), a, b, w.K)
+    t = buf.cpu().numpy().view(np.uint64).reshape(grid + 8, sk.TRACE_SLOTS)
+    assert np.all(t[traced:] == SENT)                  # past the buffer: untouched
+    f = {name: i for i, name in enumerate(sk.TRACE_FIELDS)}
+    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
+    for cta in range(traced):
+        r = t[cta]
+        sm, rank = int(r[f["sm_rank"]]) & 0xFFFFFFFF, int(r[f["sm_rank"]]) >> 32
+        assert sm < sms and rank == cta % w.split_k     # the cluster runs along grid x
+        # thread 0: start, map acquired, first ring pass issued, set-up passed,
+        # last weight issued, end
+        chain = [r[f[k]] for k in ("start", "map_ready", "prefetched", "synced", "weights_issued", "end")]
+        assert all(x != SENT for x in chain) and chain == sorted(chain), (cta, chain)
+        # epilogue thread 0: accumulator complete, then partials published or summed
+        assert r[f["mma_done"]] != SENT and r[f["mma_done"]] <= r[f["reduced"]] != SENT
+        if rank == 0:
+            assert r[f["reduced"]] <= r[f["stored"]] != SENT
+        else:
+            assert r[f["stored"]] == SENT               # only rank 0 stores
+        assert r[f["start"]] <= r[f["mma_done"]]
+    # tracing off: a second call writes nothing
+    buf.fill_(SENT)
+    c2 = sk.splitk_gemm_bf16(ta, tb, split_k=w.split_k)
+    torch.cuda.synchronize()
+    assert bool((buf == SENT).all())
+    assert torch.equal(c.view(torch.int16), c2.view(torch.int16))
+
+
+def test_release_frees_the_cache_and_later_calls_rebuild_it():
+    """splitk_release frees the device tensor-map pool (and its host mirror);
+    the next call encodes the maps again and computes the same bits."""
+    a, b = _draw(1, 3, 700, 2048, 91)
+    ta, tb = to_dev(a), to_dev(b)
+    c1 = sk.splitk_gemm_bf16(ta, tb, split_k=4)
+    torch.cuda.synchronize()
+    info = sk.splitk_cache_info()
+    assert info["device_bytes"] > 0 and info["host_bytes"] > 0 and info["maps"] >= 1
+    sk.splitk_release()
+    assert sk.splitk_cache_info() == {"device_bytes": 0, "host_bytes": 0, "maps": 0}
+    c2 = sk.splitk_gemm_bf16(ta, tb, split_k=4)
+    c3 = sk.splitk_gemm_bf16(ta, tb, split_k=2)          # another plan, the same weight map
+    torch.cuda.synchronize()
+    assert sk.splitk_get_status() == 0
+    assert sk.splitk_cache_info()["maps"] == 1
+    assert torch.equal(c1.view(torch.int16), c2.view(torch.int16))
+    ref = oracle.gemm(a, b)
+    assert_parity(to_host(c2), ref, a, b, 2048)
+    assert_parity(to_host(c3), ref, a, b, 2048)

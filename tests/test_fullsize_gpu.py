@@ -1,11 +1,13 @@
 """Parity at the full workload sizes, in the launch configuration the
 benchmark times (the workload's split_k, the library's plan, PDL on).
 
-The oracle checks sampled outputs one by one (every element of the first
-and last token row of the first and last weight tile, plus random ones);
-two closed forms check every output exactly at full size: all-ones inputs
-give C = K, and weights with one 1.0 per row at column n mod K give
-C[l, m, n] = B[l, m, n mod K] bit for bit.
+The tiny and the two decode workloads are compared with the oracle on every
+output element (the threaded oracle takes seconds there).  The wide
+projection and the sweep points are checked on sampled outputs one by one
+(every element of the first and last token row of the first and last weight
+tile, plus random ones); two closed forms check every output exactly at full
+size: all-ones inputs give C = K, and weights with one 1.0 per row at column
+n mod K give C[l, m, n] = B[l, m, n mod K] bit for bit.
 """
 from __future__ import annotations
 
@@ -17,6 +19,8 @@ pytestmark = pytest.mark.gpu
 
 if not torch.cuda.is_available():  # pragma: no cover
     pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import os  # noqa: E402
 
 import oracle  # noqa: E402
 import split_bf16_gemm_swapped_gb300 as sk  # noqa: E402
@@ -68,8 +72,21 @@ def _check_sampled(w):
     assert torch.equal(tc.view(torch.int16), tc2.view(torch.int16))
 
 
-@pytest.mark.parametrize("w", FIXED, ids=lambda w: f"{w.name.split()[0]}-M{w.M}-s{w.split_k}")
-def test_fixed_workloads_sampled_against_oracle(w):
+@pytest.mark.parametrize("w", [workloads.TINY, workloads.DECODE_M1, workloads.DECODE_M16],
+                         ids=lambda w: f"{w.name.split()[0]}-M{w.M}-s{w.split_k}")
+def test_decode_workloads_every_output_against_oracle(w):
+    a, ta = _weights(w)
+    b = w.make_b()
+    tc = sk.splitk_gemm_bf16(ta, to_dev(b), split_k=w.split_k)
+    torch.cuda.synchronize()
+    assert sk.splitk_get_status() == 0
+    ref = oracle.gemm(a, b, threads=max(1, min(32, os.cpu_count() or 1)))
+    ok, rep = _tol.check(to_host(tc), ref, w.K, _tol.max_abs_bf16(a), _tol.max_abs_bf16(b))
+    assert ok, f"{w.name}: {rep}"
+
+
+@pytest.mark.parametrize("w", FIXED[2:], ids=lambda w: f"{w.name.split()[0]}-M{w.M}-s{w.split_k}")
+def test_wide_workloads_sampled_against_oracle(w):
     _check_sampled(w)
 
 
