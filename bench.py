@@ -1,24 +1,34 @@
 #!/usr/bin/env python3
 """Benchmark of the split-K BF16 decode GEMM on GB300.
 
-Default workload: the single-token decode projection, M=1 token, N=7168
-weight rows, K=2048, L=1, split_k=4 (29 MB of bf16 weights, pure weight
-streaming).  Metric: achieved HBM TB/s of algorithmic bytes
-2*L*(N*K + M*K + M*N) per step; the roofline fraction is reported beside it.
+Default workload: the M x split sweep, M in {1, 2, 4, 8, 16, 32, 64, 128}
+tokens x split_k in {1, 2, 4, 8}, N=7168 weight rows, K=16384, L=2
+independent weight sets (470 MB of bf16 weights per call).  Metric: achieved
+HBM TB/s of algorithmic bytes 2*L*(N*K + M*K + M*N) per call, with the
+roofline fraction beside it, at every point.  The line's `value` is the
+lowest TB/s over the points with M <= 16 (the decode shapes that the 75 %
+HBM target covers); every point is listed under `per_point`, and the two
+fixed decode workloads (M=1, N=7168, K=2048, split 4; M=16, N=4096, K=7168,
+split 8) under `decode`.
 
-A step is one call of the GEMM on one batch of activations.  Timed steps run
-back to back on one stream (captured in CUDA graphs, programmatic dependent
-launch between steps, as a decode model chains its projections), each step
-reading the next of R weight copies whose total exceeds 4x the L2 cache, so
-every step streams its weights from HBM.
+A step is one call of the GEMM on one batch of activations.  For each point,
+`--steps` calls run back to back on one stream (captured in a CUDA graph,
+programmatic dependent launch between calls, as a decode model chains its
+projections), each reading the next of R weight copies whose total exceeds
+4x the L2 cache, so every call streams its weights from HBM.  The graph is
+replayed back to back at least 5 times and for at least `--min-ms` per
+point, each replay bracketed by CUDA events; the point's time is the median
+replay / steps.  All points are captured first and timed in one block, so
+the clock sampler sees the GPU under load.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload decode_m1|...] [--sweep]
+                  [--workload sweep|decode_m1|...] [--sweep fixed|w4a16]
 
 Under torchrun (N > 1) every rank runs an independent replica of the
 workload on its own GPU (weak scaling, no data exchange); rank 0 prints the
-JSON line with the max-over-ranks time.  `--impl reference` times the CPU
-oracle (float64, all host cores) on a bounded sample of the same workload.
+JSON line with the max-over-ranks time of each point.  `--impl reference`
+times the CPU oracle (float64, all host cores) on bounded samples of the
+same workload.
 """
 from __future__ import annotations
 
@@ -44,9 +54,25 @@ FALLBACK_BF16_TFLOPS = 1900.0
 KERNEL_SOURCES = ["split_bf16_gemm_swapped_gb300/csrc/splitk_kernel.cu",
                   "split_bf16_gemm_swapped_gb300/csrc/splitk_device.cuh",
                   "split_bf16_gemm_swapped_gb300/csrc/splitk_internal.h"]
+TRAFFIC_TABLE = ROOT / "profiles" / "splitk_dram_traffic.txt"
+SWEEP_DESC = ("sweep: M in {1,2,4,8,16,32,64,128} x split_k in {1,2,4,8}, N=7168, K=16384, L=2 "
+              "independent weight sets")
+VALUE_RULE = "lowest TB/s over the points with M <= 16 (the decode shapes the 75 % HBM target covers)"
 
 
 # ----------------------------------------------------------------- helpers
+def workload_key(w) -> str:
+    """The name bench.py and the traffic table use for a workload."""
+    from split_bf16_gemm_swapped_gb300 import workloads as W
+    fixed = {W.TINY: "tiny", W.DECODE_M1: "decode_m1", W.DECODE_M16: "decode_m16",
+             W.WIDE_S2: "wide_s2", W.WIDE_S4: "wide_s4"}
+    if w in fixed:
+        return fixed[w]
+    if w.name == "sweep":
+        return f"sweep_m{w.M}_s{w.split_k}"
+    return f"{w.name}_m{w.M}_n{w.N}_k{w.K}_l{w.L}_s{w.split_k}"
+
+
 def workload_by_name(name: str):
     from split_bf16_gemm_swapped_gb300 import workloads as W
     table = {"tiny": W.TINY, "decode_m1": W.DECODE_M1, "decode_m16": W.DECODE_M16,
@@ -85,23 +111,26 @@ def kernel_sha() -> str:
     return h.hexdigest()[:16]
 
 
-def committed_traffic(workload_key: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source."""
-    path = ROOT / "profiles" / f"splitk_{workload_key}_traffic.txt"
-    if not path.exists():
-        return None
-    kv = {}
-    for line in path.read_text().splitlines():
-        if ":" in line and not line.startswith("#"):
-            k, v = line.split(":", 1)
-            kv[k.strip()] = v.strip()
-    if kv.get("kernel_sha256") != kernel_sha():
-        return None
-    try:
-        return int(float(kv["traffic_bytes_per_launch"]))
-    except (KeyError, ValueError):
-        return None
+def traffic_table() -> dict:
+    """DRAM bytes per launch by workload key, from the committed ncu table,
+    if it was taken on the current kernel sources (else empty)."""
+    if not TRAFFIC_TABLE.exists():
+        return {}
+    sha, rows = None, {}
+    for line in TRAFFIC_TABLE.read_text().splitlines():
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        k, _, v = line.partition(":")
+        k, v = k.strip(), v.strip()
+        if k == "kernel_sha256":
+            sha = v
+        elif k.startswith("traffic "):
+            try:
+                rows[k[len("traffic "):]] = int(float(v.split()[0]))
+            except (ValueError, IndexError):
+                pass
+    return rows if sha == kernel_sha() else {}
 
 
 class ClockSampler:
@@ -198,6 +227,21 @@ def job_tbps(world: int, bytes_per_step: int, steps: int, elapsed_ms: float) -> 
     return world * bytes_per_step * steps / (elapsed_ms * 1e-3) / 1e12
 
 
+def repeats_for(one_replay_ms: float, min_ms: float, at_least: int = 5, at_most: int = 100000) -> int:
+    """Back-to-back replays of a graph to time: at least `at_least`, and
+    enough to cover `min_ms` of GPU time."""
+    if one_replay_ms <= 0:
+        return at_least
+    return int(min(at_most, max(at_least, math.ceil(min_ms / one_replay_ms))))
+
+
+def headline(points: list) -> dict:
+    """The point the line's value is quoted on: the lowest TB/s among the
+    points with M <= 16 (all points when none has)."""
+    small = [p for p in points if p["M"] <= 16] or points
+    return min(small, key=lambda p: p["tbps"])
+
+
 def host_cores() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -223,6 +267,16 @@ def host_cpu_name() -> str:
         return (f"{platform.machine()} implementer {fields.get('CPU implementer', '?')} "
                 f"part {fields['CPU part']}")
     return platform.machine() or "unknown"
+
+
+def sweep_config(ws):
+    return {"workload": SWEEP_DESC, "M": sorted({w.M for w in ws}), "N": ws[0].N, "K": ws[0].K,
+            "L": ws[0].L, "split_k": sorted({w.split_k for w in ws}), "value_rule": VALUE_RULE}
+
+
+def single_config(w):
+    return {"workload": describe(w), "M": w.M, "N": w.N, "K": w.K, "L": w.L,
+            "split_k": w.split_k, "bytes_per_step": w.bytes, "flops_per_step": w.flops}
 
 
 # ----------------------------------------------------------------- CPU arms
@@ -271,51 +325,63 @@ def run_cpu_table(args):
                               "cpu": host_cpu_name(), "sample": sample}), flush=True)
 
 
-def run_reference(args, w):
+def run_reference(args):
+    """The reference arm: the float64 CPU oracle on the host cores, on the
+    same workload and metric.  Each step is a bounded sample (a prefix of the
+    weight rows) of every timed point; the oracle has no split, so the sweep
+    is timed once per M (M <= 16, the points the value is quoted on)."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     import oracle
+    from split_bf16_gemm_swapped_gb300 import workloads as W
     threads = host_cores()
-    a = w.make_a()
-    b = w.make_b()
+    if args.workload == "sweep":
+        ws = [W.sweep(m, 1) for m in W.SWEEP_M if m <= 16]
+        config = sweep_config(W.all_sweep())
+    else:
+        ws = [workload_by_name(args.workload)]
+        config = single_config(ws[0])
     total_steps = args.steps + args.warmup
-    per_step_budget = max(1e-3, min(1.0, 120.0 / max(1, total_steps)))
-    rows = min(w.N, 128)
-    t0 = time.perf_counter()
-    oracle.gemm_threaded(np.ascontiguousarray(a[:, :rows]), b, threads)
-    per_row = (time.perf_counter() - t0) / rows
-    n = max(1, min(w.N, int(per_step_budget / max(per_row, 1e-9))))
-    a_s = np.ascontiguousarray(a[:, :n])
-    for _ in range(args.warmup):
-        oracle.gemm_threaded(a_s, b, threads)
-    used = 1
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        _, used = oracle.gemm_threaded(a_s, b, threads)
-    elapsed = time.perf_counter() - t0
-    sample_bytes = 2 * w.L * (n * w.K + w.M * w.K + w.M * n)
-    value = sample_bytes * args.steps / elapsed / 1e12
-    sample = f"first {n} of {w.N} weight rows per step" if n < w.N else "whole workload per step"
+    per_step_budget = max(1e-3, min(1.0, 60.0 / max(1, total_steps * len(ws))))
+    points, used, a_cache = [], 1, {}
+    for w in ws:
+        key = (w.N, w.K, w.L, w.seed)
+        if key not in a_cache:
+            a_cache.clear()
+            a_cache[key] = w.make_a()
+        a = a_cache[key]
+        b = w.make_b()
+        rows = min(w.N, 128)
+        t0 = time.perf_counter()
+        oracle.gemm_threaded(np.ascontiguousarray(a[:, :rows]), b, threads)
+        per_row = (time.perf_counter() - t0) / rows
+        n = max(1, min(w.N, int(per_step_budget / max(per_row, 1e-9))))
+        a_s = np.ascontiguousarray(a[:, :n])
+        for _ in range(args.warmup):
+            oracle.gemm_threaded(a_s, b, threads)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            _, used = oracle.gemm_threaded(a_s, b, threads)
+        elapsed = time.perf_counter() - t0
+        sample_bytes = 2 * w.L * (n * w.K + w.M * w.K + w.M * n)
+        points.append({"M": w.M, "tbps": sample_bytes * args.steps / elapsed / 1e12,
+                       "ms_per_step": elapsed / args.steps * 1e3,
+                       "sample": f"first {n} of {w.N} weight rows per step" if n < w.N else "whole workload per step"})
+    top = headline(points)
+    value = top["tbps"]
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TB/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": elapsed / args.steps * 1e3, "higher_is_better": True,
+        "ms_per_step": top["ms_per_step"], "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": config_block(w, None),
+        "config": config | {"value_point": f"M={top['M']}"},
+        "per_point": points,
         "cpu_baseline": {"value": value, "unit": "TB/s", "cores": used, "kind": "oracle",
-                         "sample": sample, "cpu": host_cpu_name()},
+                         "sample": top["sample"], "cpu": host_cpu_name()},
         "e2e": {"value": value, "unit": "TB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
-
-
-def config_block(w, rotation):
-    c = {"workload": describe(w), "M": w.M, "N": w.N, "K": w.K, "L": w.L,
-         "split_k": w.split_k, "bytes_per_step": w.bytes, "flops_per_step": w.flops}
-    if rotation is not None:
-        c["l2"] = rotation
-    return c
 
 
 # ----------------------------------------------------------------- GPU arm
@@ -324,11 +390,149 @@ def to_dev(bits: np.ndarray, device):
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
 
 
-def run_ours(args, w):
+class Point:
+    """One workload prepared for timing: its weight copies, activations,
+    output and the CUDA graph of `steps` back-to-back calls."""
+
+    def __init__(self, w, weights, dev, stream, steps, warmup):
+        import torch
+        import split_bf16_gemm_swapped_gb300 as sk
+        self.w = w
+        self.As = weights
+        self.R = len(weights)
+        self.b = to_dev(w.make_b(), dev)
+        self.c = torch.empty((w.L, w.M, w.N), dtype=torch.bfloat16, device=dev)
+        self.stream = stream
+        self.steps = steps
+        self.plan = sk.splitk_plan(w.M, w.N, w.K, w.L, w.split_k)
+        with torch.cuda.stream(stream):
+            for i in range(max(warmup, self.R)):        # also builds every tensor map
+                self.step(i)
+        stream.synchronize()
+        if sk.splitk_get_status() != 0:
+            raise SystemExit(f"kernel fault during warm-up of {describe(w)}: {sk.splitk_get_fault()}")
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=stream):
+            for i in range(steps):
+                self.step(i)
+        # one untimed replay: settles the graph and estimates a replay's time
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            self.graph.replay()
+            e0.record(stream)
+            self.graph.replay()
+            e1.record(stream)
+        e1.synchronize()
+        self.replay_ms_estimate = e0.elapsed_time(e1)
+
+    def step(self, i):
+        import split_bf16_gemm_swapped_gb300 as sk
+        sk.splitk_gemm_bf16(self.As[i % self.R], self.b, self.c, split_k=self.w.split_k, stream=self.stream)
+
+
+def time_replays(graph, stream, reps):
+    """Per-replay ms of `reps` back-to-back replays, each between two events."""
+    import torch
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+    with torch.cuda.stream(stream):
+        ev[0].record(stream)
+        for j in range(reps):
+            graph.replay()
+            ev[j + 1].record(stream)
+    ev[-1].synchronize()
+    return [ev[j].elapsed_time(ev[j + 1]) for j in range(reps)]
+
+
+def point_record(w, ms_per_step, reps, steps, plan, traffic, world):
+    hbm, bf16, bf16s, src = peaks()
+    t = ms_per_step * 1e-3
+    tb = world * w.bytes / t / 1e12
+    t_roof = max(w.bytes / (hbm * 1e9), w.flops / (bf16s * 1e12))
+    return {"M": w.M, "split_k": w.split_k, "N": w.N, "K": w.K, "L": w.L, "key": workload_key(w),
+            "us": round(ms_per_step * 1e3, 3), "tbps": tb, "tflops": round(world * w.flops / t / 1e12, 2),
+            "hbm_frac": round(w.bytes / t / 1e9 / hbm, 4), "roofline_frac": round(t_roof / t, 4),
+            "repeats": reps, "launches": reps * steps,
+            "traffic": traffic.get(workload_key(w)),
+            "plan": {k: v for k, v in plan.as_dict().items()
+                     if k in ("mma_n", "stages", "grid", "smem_bytes", "ctas_per_sm", "mailbox_dedicated",
+                              "reduce_rounds", "reduce_scatter", "b_resident", "a_tmem_tiles",
+                              "mma_issuers", "b_loader", "pdl_trigger")}}
+
+
+def e2e_point(w, weights, dev, stream, steps, reps, warmup, world):
+    """The same metric end to end through the C ABI: every step copies its
+    activations in from pinned host memory and its output back to pinned host
+    memory -- the kernel itself through the buffers' device mappings
+    (splitk_gemm_bf16_zerocopy) where the plan loads activations with its
+    threads, else the copy engines around the kernel (splitk_gemm_bf16_hostio).
+    Timed like the device-resident value: a graph of `steps` calls replayed
+    `reps` times back to back, median replay / steps."""
+    import torch
+    import split_bf16_gemm_swapped_gb300 as sk
+    R = len(weights)
+    b_host = w.make_b()
+    b_pin = torch.from_numpy(b_host.view(np.int16)).view(torch.bfloat16).pin_memory()
+    c_pin = torch.empty((w.L, w.M, w.N), dtype=torch.bfloat16).pin_memory()
+    b_dev = torch.empty((w.L, w.M, w.K), dtype=torch.bfloat16, device=dev)
+    c_dev = torch.empty((w.L, w.M, w.N), dtype=torch.bfloat16, device=dev)
+    plan = sk.splitk_plan(w.M, w.N, w.K, w.L, w.split_k)
+    zc = bool(plan.b_resident)
+
+    def call(i):
+        if zc:
+            sk.splitk_gemm_bf16_zerocopy(weights[i % R], b_pin, c_pin, w.split_k, stream)
+        else:
+            sk.splitk_gemm_bf16_hostio(weights[i % R], b_pin, c_pin, b_dev, c_dev, w.split_k, stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(max(warmup, R)):
+            call(i)
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(steps):
+            call(i)
+    with torch.cuda.stream(stream):
+        g.replay()
+    stream.synchronize()
+    ms = statistics.median(time_replays(g, stream, reps)) / steps
+    if sk.splitk_get_status() != 0:
+        raise SystemExit(f"kernel fault in the end-to-end run: {sk.splitk_get_fault()}")
+    ms = max_over_ranks(ms, dev)
+    del g
+    return {"value": world * w.bytes / (ms * 1e-3) / 1e12, "unit": "TB/s",
+            "h2d_bytes_per_step": int(b_host.nbytes), "d2h_bytes_per_step": int(w.L * w.M * w.N * 2),
+            "ms_per_step": ms, "steps": steps, "repeats": reps, "workload": describe(w),
+            "path": "splitk_gemm_bf16_zerocopy" if zc else "splitk_gemm_bf16_hostio",
+            "note": ("weights resident in HBM; every step the activations cross from pinned host memory and "
+                     "the output back to pinned host memory, inside the timed region; "
+                     + ("the kernel loads and stores them itself through their device mappings"
+                        if zc else "copy engines around the kernel")
+                     + f"; graph of {steps} calls replayed {reps} times, median replay / steps")}
+
+
+def weight_copies(w, dev, l2, rotate, cache):
+    """R device copies of the workload's weights (R * bytes >= 4x L2 unless
+    `rotate` fixes R), shared by the workloads with the same weights."""
+    key = (w.N, w.K, w.L, w.seed)
+    a_bytes = 2 * w.L * w.N * w.K
+    R = rotate if rotate else max(2, math.ceil(4 * l2 / a_bytes))
+    if key not in cache:
+        a0 = to_dev(w.make_a(), dev)
+        cache[key] = [a0]
+    copies = cache[key]
+    while len(copies) < R:
+        copies.append(copies[0].clone())
+    return copies[:R], (f"rotating {R} weight copies ({R * a_bytes / 1e6:.0f} MB, "
+                        f"{R * a_bytes / l2:.1f}x the {l2 / 2**20:.0f} MiB L2)")
+
+
+def run_ours(args):
     import torch
     import torch.distributed as dist
 
     import split_bf16_gemm_swapped_gb300 as sk
+    from split_bf16_gemm_swapped_gb300 import workloads as W
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -338,247 +542,170 @@ def run_ours(args, w):
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
     sk.load_library()
-
-    a_host = w.make_a()
-    b_host = w.make_b()
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 0) or 0) or 126 * 1024 * 1024
-    a_bytes = a_host.nbytes
-    R = args.rotate if args.rotate else max(2, math.ceil(4 * l2 / a_bytes))
-    a0 = to_dev(a_host, dev)
-    As = [a0] + [a0.clone() for _ in range(R - 1)]
-    b = to_dev(b_host, dev)
-    c = torch.empty((w.L, w.M, w.N), dtype=torch.bfloat16, device=dev)
-    plan = sk.splitk_plan(w.M, w.N, w.K, w.L, w.split_k)
-    rotation = (f"rotating {R} weight copies ({R * a_bytes / 1e6:.0f} MB, "
-                f"{R * a_bytes / l2:.1f}x the {l2 / 2**20:.0f} MiB L2)")
-
     stream = torch.cuda.Stream(dev)
+    traffic = traffic_table()
+
+    sweep_mode = args.workload == "sweep"
+    main_ws = W.all_sweep() if sweep_mode else [workload_by_name(args.workload)]
+    extra_ws = [W.DECODE_M1, W.DECODE_M16] if sweep_mode and not args.no_extras else []
+
+    # prepare every point (weights, activations, graph) before timing any
+    cache, rotations, prepared = {}, {}, []
+    for w in main_ws + extra_ws:
+        copies, rot = weight_copies(w, dev, l2, args.rotate, cache)
+        rotations[workload_key(w)] = rot
+        prepared.append(Point(w, copies, dev, stream, args.steps, args.warmup))
     torch.cuda.synchronize(dev)
 
-    def step(i):
-        sk.splitk_gemm_bf16(As[i % R], b, c, split_k=w.split_k, stream=stream)
-
-    # warm-up: eager launches (also builds every tensor map before capture)
-    with torch.cuda.stream(stream):
-        for i in range(max(args.warmup, R)):
-            step(i)
-    stream.synchronize()
-    if sk.splitk_get_status() != 0:
-        raise SystemExit(f"kernel fault during warm-up: {sk.splitk_get_fault()}")
-
-    # graphs of G steps (and a tail graph) so the host never limits the rate
-    G = min(args.steps, R * max(1, 1024 // R))
-    def capture(n):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for i in range(n):
-                step(i)
-        return g
-    g_main = capture(G) if G > 0 else None
-    reps, tail = divmod(args.steps, G)
-    g_tail = capture(tail) if tail else None
-    with torch.cuda.stream(stream):
-        g_main.replay()
-    stream.synchronize()
-
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
-    # the timed region in 5 consecutive parts (events between graph replays)
-    parts = 5 if reps >= 5 else 1
-    bounds = [reps * j // parts for j in range(parts + 1)]
-    marks = [torch.cuda.Event(enable_timing=True) for _ in range(parts)]
+    # time every point in one block: barrier + synchronize on both sides of
+    # each point's replays, median replay / steps, max over ranks
+    results = []
+    launches = 0
     with ClockSampler(local) as clocks:
-        with torch.cuda.stream(stream):
-            start.record(stream)
-            for j in range(parts):
-                for _ in range(bounds[j + 1] - bounds[j]):
-                    g_main.replay()
-                marks[j].record(stream)
-            if g_tail is not None:
-                g_tail.replay()
-            end.record(stream)
-        end.synchronize()
-        if world > 1:
-            dist.barrier()
-        torch.cuda.synchronize(dev)
-    elapsed_ms = max_over_ranks(start.elapsed_time(end), dev)
+        for pt in prepared:
+            reps = repeats_for(pt.replay_ms_estimate, args.min_ms)
+            if world > 1:
+                dist.barrier()
+            torch.cuda.synchronize(dev)
+            per_rep = time_replays(pt.graph, stream, reps)
+            torch.cuda.synchronize(dev)
+            if world > 1:
+                dist.barrier()
+            ms = max_over_ranks(statistics.median(per_rep) / args.steps, dev)
+            launches += reps * args.steps
+            results.append((pt, ms, reps))
     if sk.splitk_get_status() != 0:
         raise SystemExit(f"kernel fault in the timed region: {sk.splitk_get_fault()}")
 
-    ms_per_step = elapsed_ms / args.steps
-    value = job_tbps(world, w.bytes, args.steps, elapsed_ms)
+    records = [point_record(pt.w, ms, reps, args.steps, pt.plan, traffic, world) for pt, ms, reps in results]
+    main_recs = records[:len(main_ws)]
+    extra_recs = records[len(main_ws):]
+    top = headline(main_recs)
+    top_i = main_recs.index(top)
+    top_pt, top_ms, top_reps = results[top_i]
+    w = top_pt.w
+
     hbm, bf16, bf16s, src = peaks()
-    achieved_gbs = w.bytes / (ms_per_step * 1e-3) / 1e9
-    flops_tfs = w.flops / (ms_per_step * 1e-3) / 1e12
+    achieved_gbs = w.bytes / (top_ms * 1e-3) / 1e9
     t_roof = max(w.bytes / (hbm * 1e9), w.flops / (bf16s * 1e12))
-    bound = "hbm" if w.bytes / (hbm * 1e9) >= w.flops / (bf16s * 1e12) else "tensor"
-    key = args.workload
-    roofline = {"bound": bound, "achieved": round(achieved_gbs, 1), "peak": hbm,
-                "unit": "GB/s", "frac": round(achieved_gbs / hbm, 4),
-                "traffic": committed_traffic(key), "peak_source": src,
-                "roofline_time_frac": round(t_roof / (ms_per_step * 1e-3), 4),
-                "tflops": round(flops_tfs, 2),
-                "note": f"frac of {src} HBM copy bandwidth; launch duration = timed region / steps"}
-    if bound == "tensor":
-        roofline.update({"achieved": round(flops_tfs, 2), "peak": bf16s, "unit": "TFLOP/s",
-                         "frac": round(flops_tfs / bf16s, 4)})
+    roofline = {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved_gbs / hbm, 4), "traffic": top["traffic"], "peak_source": src,
+                "kernel": f"splitk_gemm_bf16_kernel<{top['plan']['mma_n']}, false>",
+                "roofline_time_frac": round(t_roof / (top_ms * 1e-3), 4), "tflops": top["tflops"],
+                "note": (f"frac of {src} HBM copy bandwidth ({hbm:.0f} GB/s) at the value's point; launch "
+                         "duration = median graph replay / steps, CUDA events on the launching stream")}
 
-    # isolated single-launch time: one launch per graph replay, so no
-    # neighbour overlaps it and host launch overhead is not on the GPU clock
-    g_one = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_one, stream=stream):
-        step(0)
-    iso = []
-    with torch.cuda.stream(stream):
-        for i in range(20):
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            g_one.replay()
-            e1.record(stream)
-            e1.synchronize()
-            iso.append(e0.elapsed_time(e1))
-    iso_us = statistics.median(iso) * 1e3
-
-    # the parts of the timed region, and a hot-L2 figure (one weight copy
-    # that stays in L2; labelled, not the metric)
-    part_tbps = []
-    prev = start
-    for j in range(parts):
-        n = (bounds[j + 1] - bounds[j]) * G
-        part_tbps.append(round(w.bytes * n / (prev.elapsed_time(marks[j]) * 1e-3) / 1e12, 3))
-        prev = marks[j]
-    g_hot = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_hot, stream=stream):
-        for _ in range(G):
-            sk.splitk_gemm_bf16(As[0], b, c, split_k=w.split_k, stream=stream)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        g_hot.replay()
-        e0.record(stream)
-        for _ in range(5):
-            g_hot.replay()
-        e1.record(stream)
-    e1.synchronize()
-    hot_ms = e0.elapsed_time(e1) / (5 * G)
-    del g_hot
-    if sk.splitk_get_status() != 0:
-        raise SystemExit(f"kernel fault in the hot-L2 run: {sk.splitk_get_fault()}")
-
-    # end to end through the C ABI: pinned host activations in, host output out
+    # end to end on the value's point (and on the decode workloads)
     e2e = None
-    if args.e2e_steps > 0:
-        b_pin = torch.from_numpy(b_host.view(np.int16)).view(torch.bfloat16).pin_memory()
-        c_pin = torch.empty((w.L, w.M, w.N), dtype=torch.bfloat16).pin_memory()
-        n_e2e = min(args.steps, args.e2e_steps)
+    e2e_decode = {}
+    if args.e2e:
+        for pt, ms, reps in [results[top_i]] + results[len(main_ws):]:
+            rec = e2e_point(pt.w, pt.As, dev, stream, args.steps, reps, args.warmup, world)
+            if pt is top_pt:
+                e2e = rec
+            else:
+                e2e_decode[workload_key(pt.w)] = rec
 
-        def timed_calls(call, graph_steps):
-            """ms per call: eager (one host call per step), or captured in a
-            CUDA graph of `graph_steps` calls (how a decode loop issues them)."""
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            with torch.cuda.stream(stream):
-                for i in range(min(args.warmup, 10)):
-                    call(i)
-                stream.synchronize()
-                if graph_steps == 0:
-                    e0.record(stream)
-                    for i in range(n_e2e):
-                        call(i)
-                    e1.record(stream)
-                    e1.synchronize()
-                    return e0.elapsed_time(e1) / n_e2e, n_e2e
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g, stream=stream):
-                    for i in range(graph_steps):
-                        call(i)
-                g.replay()
-                stream.synchronize()
-                reps = max(1, n_e2e // graph_steps)
-                e0.record(stream)
-                for _ in range(reps):
-                    g.replay()
-                e1.record(stream)
-                e1.synchronize()
-                return e0.elapsed_time(e1) / (reps * graph_steps), reps * graph_steps
-
-        def copies(i):      # copy engines: b_pin -> b, GEMM, c -> c_pin
-            sk.splitk_gemm_bf16_hostio(As[i % R], b_pin, c_pin, b, c, w.split_k, stream)
-
-        def zero_copy(i):   # the kernel reads b_pin and writes c_pin itself
-            sk.splitk_gemm_bf16_zerocopy(As[i % R], b_pin, c_pin, w.split_k, stream)
-
-        G = 50
-        copy_eager_ms, _ = timed_calls(copies, 0)
-        try:
-            zero_copy(0)
-            zc = True
-        except sk.SplitKError:
-            zc = False      # shape without thread-loaded activations
+    # the hot-L2 figure of the single-workload mode: one weight copy that
+    # stays in L2 (labelled, not the metric)
+    hot = None
+    if not sweep_mode:
+        g_hot = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_hot, stream=stream):
+            for _ in range(args.steps):
+                sk.splitk_gemm_bf16(top_pt.As[0], top_pt.b, top_pt.c, split_k=w.split_k, stream=stream)
+        with torch.cuda.stream(stream):
+            g_hot.replay()
         stream.synchronize()
-        if zc:
-            zc_eager_ms, _ = timed_calls(zero_copy, 0)
-            e2e_ms, steps_e2e = timed_calls(zero_copy, G)
-        else:
-            e2e_ms, steps_e2e = timed_calls(copies, G)
-        tbps = lambda ms: world * w.bytes / (ms * 1e-3) / 1e12
-        e2e = {"value": tbps(e2e_ms), "unit": "TB/s",
-               "h2d_bytes_per_step": int(b_host.nbytes), "d2h_bytes_per_step": int(w.L * w.M * w.N * 2),
-               "steps": steps_e2e, "ms_per_step": e2e_ms,
-               "path": "splitk_gemm_bf16_zerocopy" if zc else "splitk_gemm_bf16_hostio",
-               "copy_engine_eager_ms_per_step": copy_eager_ms,
-               "zero_copy_eager_ms_per_step": zc_eager_ms if zc else None,
-               "note": ("weights resident in HBM; every step the activations cross from pinned host memory "
-                        "and the output back to pinned host memory; value: "
-                        + ("the kernel loads and stores them itself (splitk_gemm_bf16_zerocopy), "
-                           if zc else "copy engines around the kernel (splitk_gemm_bf16_hostio), ")
-                        + f"calls captured in a CUDA graph of {G} steps; *_eager_*: one host call per step, "
-                        "copy_engine: splitk_gemm_bf16_hostio")}
+        hot_ms = statistics.median(time_replays(g_hot, stream, top_reps)) / args.steps
+        hot = {"value": round(w.bytes / (hot_ms * 1e-3) / 1e12, 3), "unit": "TB/s", "ms_per_step": hot_ms,
+               "note": "one weight copy, L2-resident after the first pass; not the metric"}
+        del g_hot
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         rate, sample, used = cpu_oracle_rate(w, args.cpu_budget, host_cores())
-        cpu = {"value": rate, "unit": "TB/s", "cores": used, "kind": "oracle", "sample": sample,
-               "cpu": host_cpu_name()}
+        cpu = {"value": rate, "unit": "TB/s", "cores": used, "kind": "oracle",
+               "sample": f"{describe(w)}: {sample}", "cpu": host_cpu_name()}
         one, one_sample, _ = cpu_oracle_rate(w, max(1.0, args.cpu_budget / 4), 1)
         cpu["single_core"] = {"value": one, "unit": "TB/s", "sample": one_sample}
 
     if rank == 0:
+        if sweep_mode:
+            config = sweep_config(main_ws) | {
+                "value_point": f"M={w.M} split_k={w.split_k}", "bytes_per_step": w.bytes,
+                "flops_per_step": w.flops, "l2": rotations[workload_key(w)]}
+        else:
+            config = single_config(w) | {"l2": rotations[workload_key(w)], "plan": top["plan"]}
+        config["launch"] = ("CUDA graph of --steps back-to-back calls with programmatic dependent launch, "
+                            f"replayed back to back at least 5 times and for at least {args.min_ms:g} ms "
+                            "per point; the median replay / steps is the point's time")
         line = {
-            "metric": METRIC, "value": value, "unit": "TB/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "metric": METRIC, "value": top["tbps"], "unit": "TB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": top_ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16", "data": "synthetic",
-            "config": config_block(w, rotation) | {
-                "plan": {k: v for k, v in plan.as_dict().items()
-                         if k in ("mma_n", "stages", "split_k", "grid", "smem_bytes",
-                                  "mailbox_dedicated", "reduce_rounds", "reduce_scatter",
-                                  "b_resident", "a_tmem_tiles", "mma_issuers", "pdl_trigger")},
-                "launch": "CUDA graphs of back-to-back launches with programmatic dependent launch",
-                "isolated_launch_us": round(iso_us, 2),
-                "isolated_note": "one launch per graph replay, events around the replay"},
+            "dtype": "bf16", "data": "synthetic", "config": config,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": args.steps, "clocks": with_verdict(clocks.summary()),
-            "parts": {"tbps": part_tbps, "median": statistics.median(part_tbps),
-                      "note": f"the timed region in {parts} consecutive parts; value covers all of it"},
-            "hot_l2": {"value": round(w.bytes / (hot_ms * 1e-3) / 1e12, 3), "unit": "TB/s",
-                       "ms_per_step": hot_ms,
-                       "note": "one weight copy, L2-resident after the first pass; not the metric"},
+            "gpu_launches": launches, "clocks": with_verdict(clocks.summary()),
+            "per_point": main_recs,
         }
+        if extra_recs:
+            line["decode"] = {r["key"]: r | ({"e2e": e2e_decode[r["key"]]} if r["key"] in e2e_decode else {})
+                              for r in extra_recs}
+        if hot is not None:
+            line["hot_l2"] = hot
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def run_profile_case(args):
+    """A short eager run for ncu: for one workload (or, with `all`, every
+    fixed and sweep workload in turn), one weight copy (so ncu's memory save
+    and restore stays small), `--warmup` launches, then `--steps` launches;
+    no graphs, no CPU oracle.  `--w4` runs the A16W4 kernel on the same
+    shapes (4-bit codes with their scales)."""
+    import torch
+
+    import split_bf16_gemm_swapped_gb300 as sk
+    from split_bf16_gemm_swapped_gb300 import synthetic
+    from split_bf16_gemm_swapped_gb300 import workloads as W
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    ws = list(W.ALL_FIXED) + W.all_sweep() if args.profile_case == "all" else [workload_by_name(args.profile_case)]
+    a_cache = {}
+    for w in ws:
+        b = to_dev(w.make_b(), dev)
+        c = torch.empty((w.L, w.M, w.N), dtype=torch.bfloat16, device=dev)
+        if args.w4:
+            aq, a_s = synthetic.w4_weights(w.L, w.N, w.K, w.seed)
+            q, s = torch.from_numpy(aq).to(dev), torch.from_numpy(a_s).to(dev)
+            call = lambda: sk.splitk_gemm_w4a16(q, s, b, c, split_k=w.split_k)  # noqa: E731
+        else:
+            key = (w.N, w.K, w.L, w.seed)
+            if key not in a_cache:
+                a_cache.clear()
+                torch.cuda.empty_cache()
+                a_cache[key] = to_dev(w.make_a(), dev)
+            a = a_cache[key]
+            call = lambda: sk.splitk_gemm_bf16(a, b, c, split_k=w.split_k)  # noqa: E731
+        for _ in range(args.warmup + args.steps):
+            call()
+        torch.cuda.synchronize(dev)
+        rc = sk.splitk_get_status()
+        print(json.dumps({"profile_case": describe(w), "key": workload_key(w), "w4": bool(args.w4),
+                          "launches": args.warmup + args.steps, "status": rc}), flush=True)
+        if rc != 0:
+            raise SystemExit(1)
 
 
 def run_sweep_w4(args):
     """Extra lines for the A16W4 variant (4-bit E2M1 weights with E8M0 scales
     per 32 k, bf16 activations) on the decode shapes: HBM TB/s of the bytes
     it moves (codes, scales, activations, output) and the step time next to
-    the bf16 kernel's on the same shape."""
+    the bf16 kernel's on the same shape, both timed like the main line."""
     import torch
 
     import split_bf16_gemm_swapped_gb300 as sk
@@ -587,14 +714,14 @@ def run_sweep_w4(args):
     dev = torch.device("cuda:0")
     hbm, bf16, bf16s, src = peaks()
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    s = torch.cuda.Stream(dev)
 
     def timed(launch, R):
-        s = torch.cuda.Stream(dev)
         with torch.cuda.stream(s):
-            for i in range(R + 3):
+            for i in range(R + args.warmup):
                 launch(i % R, s)
         s.synchronize()
-        n = max(R, 240 // R * R)
+        n = max(args.steps, R)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=s):
             for i in range(n):
@@ -602,15 +729,9 @@ def run_sweep_w4(args):
         with torch.cuda.stream(s):
             g.replay()
         s.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        reps = 10
-        with torch.cuda.stream(s):
-            e0.record(s)
-            for _ in range(reps):
-                g.replay()
-            e1.record(s)
-        e1.synchronize()
-        return e0.elapsed_time(e1) / (reps * n) * 1e-3
+        one = time_replays(g, s, 1)[0]
+        per = time_replays(g, s, repeats_for(one, args.min_ms))
+        return statistics.median(per) / n * 1e-3
 
     for w in (W.DECODE_M1, W.DECODE_M16, W.TINY, W.DECODE_M1.with_(M=8), W.DECODE_M1.with_(M=32),
               W.DECODE_M1.with_(L=8), W.DECODE_M16.with_(L=4)):
@@ -632,75 +753,39 @@ def run_sweep_w4(args):
         print(json.dumps({"sweep": "A16W4 " + describe(w), "us": round(t4 * 1e6, 2),
                           "TB/s": round(w4_bytes / t4 / 1e12, 3), "bytes_per_call": w4_bytes,
                           "hbm_frac": round(w4_bytes / t4 / 1e9 / hbm, 3), "peak_source": src,
-                          "bf16_us": round(tb * 1e6, 2), "speedup_vs_bf16": round(tb / t4, 2),
+                          "bf16_us": round(tb * 1e6, 2), "speedup_vs_bf16": round(tb / t4, 3),
                           "plan": {k: v for k, v in p.as_dict().items()
                                    if k in ("mma_n", "split_k", "stages", "a_tmem_tiles", "smem_bytes",
-                                            "ctas_per_sm", "reduce_scatter", "b_loader")}}), flush=True)
+                                            "ctas_per_sm", "reduce_scatter", "b_loader", "mma_issuers",
+                                            "w4_smem_tiles")}}), flush=True)
         del Qs, Ss, As, b, c
         torch.cuda.empty_cache()
     if sk.splitk_get_status() != 0:
         raise SystemExit(f"kernel fault during the sweep: {sk.splitk_get_fault()}")
 
 
-def run_sweep(args):
-    """Extra lines, one per workload (not the contract line): TB/s, TFLOP/s and
-    roofline fraction vs M and split."""
+def run_sweep_fixed(args):
+    """Extra lines, one per fixed workload (tiny, the two decode shapes, the
+    wide projection at both splits), timed like the main line."""
     import torch
 
     import split_bf16_gemm_swapped_gb300 as sk
     from split_bf16_gemm_swapped_gb300 import workloads as W
     dev = torch.device("cuda:0")
-    hbm, bf16, bf16s, src = peaks()
-    ws = list(W.ALL_FIXED) + W.all_sweep() if args.sweep == "all" else W.all_sweep()
+    torch.cuda.set_device(dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    stream = torch.cuda.Stream(dev)
+    traffic = traffic_table()
     cache = {}
-    for w in ws:
-        key = (w.N, w.K, w.L, w.seed)
-        if key not in cache:
-            cache.clear()
-            cache[key] = to_dev(w.make_a(), dev)
-        a0 = cache[key]
-        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-        R = max(2, math.ceil(3 * l2 / a0.numel() / 2))
-        As = [a0] + [a0.clone() for _ in range(R - 1)] if R * a0.numel() * 2 < 8e9 else [a0]
-        R = len(As)
-        b = to_dev(w.make_b(), dev)
-        c = torch.empty((w.L, w.M, w.N), dtype=torch.bfloat16, device=dev)
-        s = torch.cuda.Stream(dev)
-        with torch.cuda.stream(s):
-            for i in range(R + 3):
-                sk.splitk_gemm_bf16(As[i % R], b, c, split_k=w.split_k, stream=s)
-        s.synchronize()
-        n = max(R, 64 // R * R)
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=s):
-            for i in range(n):
-                sk.splitk_gemm_bf16(As[i % R], b, c, split_k=w.split_k, stream=s)
-        with torch.cuda.stream(s):
-            g.replay()
-        s.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        reps = 5
-        with torch.cuda.stream(s):
-            e0.record(s)
-            for _ in range(reps):
-                g.replay()
-            e1.record(s)
-        e1.synchronize()
-        t = e0.elapsed_time(e1) / (reps * n) * 1e-3
-        tb = w.bytes / t / 1e12
-        tf = w.flops / t / 1e12
-        t_roof = max(w.bytes / (hbm * 1e9), w.flops / (bf16s * 1e12))
-        p = sk.splitk_plan(w.M, w.N, w.K, w.L, w.split_k)
-        print(json.dumps({"sweep": describe(w), "us": round(t * 1e6, 2), "TB/s": round(tb, 3),
-                          "TFLOP/s": round(tf, 1), "roofline_frac": round(t_roof / t, 3),
-                          "hbm_frac": round(tb * 1e3 / hbm, 3), "peak_source": src,
-                          "plan": {k: v for k, v in p.as_dict().items()
-                                   if k in ("mma_n", "stages", "grid", "smem_bytes",
-                                            "mailbox_dedicated", "reduce_rounds", "ctas_per_sm",
-                                            "reduce_scatter", "b_resident", "a_tmem_tiles",
-                                            "mma_issuers", "pdl_trigger")}}),
-              flush=True)
-        del As, b, c, g
+    for w in W.ALL_FIXED:
+        copies, rot = weight_copies(w, dev, l2, args.rotate, cache)
+        pt = Point(w, copies, dev, stream, args.steps, args.warmup)
+        reps = repeats_for(pt.replay_ms_estimate, args.min_ms)
+        ms = statistics.median(time_replays(pt.graph, stream, reps)) / args.steps
+        rec = point_record(w, ms, reps, args.steps, pt.plan, traffic, 1)
+        print(json.dumps({"sweep": describe(w), "l2": rot} | rec), flush=True)
+        del pt
+        cache.clear()
         torch.cuda.empty_cache()
     if sk.splitk_get_status() != 0:
         raise SystemExit(f"kernel fault during the sweep: {sk.splitk_get_fault()}")
@@ -710,39 +795,51 @@ def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1,
                     help="GPUs (one rank each under torch.distributed.run; each runs a replica)")
-    ap.add_argument("--steps", type=int, default=200000, help="timed steps (one GEMM call each)")
-    ap.add_argument("--warmup", type=int, default=100, help="untimed steps first (at least 3)")
+    ap.add_argument("--steps", type=int, default=200, help="calls per timed graph (one GEMM call each)")
+    ap.add_argument("--warmup", type=int, default=10, help="untimed calls first, per point (at least 3)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours",
                     help="reference: the float64 CPU oracle on the host cores")
-    ap.add_argument("--workload", default="decode_m1",
-                    help="decode_m1 (the default line), decode_m16, tiny, wide_s2, wide_s4, sweep_m<M>_s<split>")
-    ap.add_argument("--sweep", choices=["sweep", "all", "w4a16"], default=None,
-                    help="extra lines: the M x split sweep, that plus the fixed workloads, or A16W4")
+    ap.add_argument("--workload", default="sweep",
+                    help="sweep (the default line), decode_m1, decode_m16, tiny, wide_s2, wide_s4, "
+                         "sweep_m<M>_s<split>")
+    ap.add_argument("--min-ms", type=float, default=40.0,
+                    help="GPU time each point's back-to-back replays cover at least")
+    ap.add_argument("--sweep", choices=["fixed", "w4a16"], default=None,
+                    help="extra lines instead of the contract line: the fixed workloads, or A16W4")
+    ap.add_argument("--no-extras", action="store_true", help="skip the decode workloads of the sweep line")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the timed oracle leg")
+    ap.add_argument("--no-e2e", dest="e2e", action="store_false", help="skip the end-to-end measurement")
     ap.add_argument("--rotate", type=int, default=0,
                     help="weight copies to rotate (default: enough for 4x the L2 cache)")
-    ap.add_argument("--e2e-steps", type=int, default=2000,
-                    help="steps of the end-to-end host-I/O measurement (0 skips it)")
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of host time for the CPU oracle baseline")
     ap.add_argument("--cpu-table", action="store_true",
                     help="time the oracle alone (all host cores and one) on the fixed and sweep workloads")
+    ap.add_argument("--profile-case", default=None,
+                    help="a short eager run for ncu of one workload, or `all` of them in turn "
+                         "(no graphs, one weight copy)")
+    ap.add_argument("--w4", action="store_true", help="with --profile-case: the A16W4 kernel")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
     if args.steps < 1:
         raise SystemExit("--steps must be >= 1")
-    w = workload_by_name(args.workload)
+    if args.workload != "sweep":
+        workload_by_name(args.workload)
+    if args.profile_case not in (None, "all"):
+        workload_by_name(args.profile_case)
     if args.cpu_table:
         run_cpu_table(args)
     elif args.impl == "reference":
-        run_reference(args, w)
+        run_reference(args)
+    elif args.profile_case:
+        run_profile_case(args)
     elif args.sweep == "w4a16":
         run_sweep_w4(args)
-    elif args.sweep:
-        run_sweep(args)
+    elif args.sweep == "fixed":
+        run_sweep_fixed(args)
     else:
-        run_ours(args, w)
+        run_ours(args)
 
 
 if __name__ == "__main__":

@@ -31,3 +31,32 @@ def test_clock_sampler_parses_nvidia_smi_lines():
 def test_host_cpu_name_is_a_nonempty_string():
     name = bench.host_cpu_name()
     assert isinstance(name, str) and name
+
+
+def test_the_value_is_the_slowest_point_with_at_most_16_tokens():
+    pts = [{"M": 1, "tbps": 6.0}, {"M": 16, "tbps": 5.5}, {"M": 8, "tbps": 5.7}, {"M": 128, "tbps": 2.7}]
+    assert bench.headline(pts) == {"M": 16, "tbps": 5.5}
+    assert bench.headline([{"M": 64, "tbps": 4.0}, {"M": 32, "tbps": 5.0}]) == {"M": 64, "tbps": 4.0}
+
+
+def test_repeats_cover_the_minimum_time_and_at_least_five():
+    assert bench.repeats_for(15.0, 40.0) == 5
+    assert bench.repeats_for(1.6, 40.0) == 25
+    assert bench.repeats_for(0.11, 40.0) == 364
+    assert bench.repeats_for(0.0, 40.0) == 5
+
+
+def test_workload_keys_name_the_workloads_the_bench_accepts():
+    from split_bf16_gemm_swapped_gb300 import workloads as W
+    for w in list(W.ALL_FIXED) + W.all_sweep():
+        assert bench.workload_by_name(bench.workload_key(w)) == w
+
+
+def test_the_traffic_table_is_read_only_for_the_current_kernel(tmp_path, monkeypatch):
+    table = tmp_path / "t.txt"
+    table.write_text("# comment\nkernel_sha256: %s\ntraffic sweep_m16_s8: 470900000 B\n"
+                     "traffic decode_m1: 29438208\n" % bench.kernel_sha())
+    monkeypatch.setattr(bench, "TRAFFIC_TABLE", table)
+    assert bench.traffic_table() == {"sweep_m16_s8": 470900000, "decode_m1": 29438208}
+    table.write_text("kernel_sha256: 0000\ntraffic decode_m1: 29438208\n")
+    assert bench.traffic_table() == {}
