@@ -701,6 +701,46 @@ def run_profile_case(args):
             raise SystemExit(1)
 
 
+def ncu_traffic_table(csv_path: str, log_path: str, use_last: int) -> str:
+    """The committed DRAM-traffic table from an ncu CSV of `--profile-case`
+    runs (metrics dram__bytes_read.sum, dram__bytes_write.sum and
+    gpu__time_duration.sum) and the run's own log, which names the workloads
+    in launch order: per workload, the mean over its last `use_last`
+    launches (the earlier ones are warm-up)."""
+    import csv
+    keys, per = [], []
+    for line in Path(log_path).read_text().splitlines():
+        if line.startswith("{"):
+            d = json.loads(line)
+            keys.append(d["key"])
+            per.append(int(d["launches"]))
+    launches = {}
+    with open(csv_path) as f:
+        rows = [r for r in csv.reader(f) if len(r) > 14]
+    head = rows[0]
+    col = {n: head.index(n) for n in ("ID", "Kernel Name", "Metric Name", "Metric Value")}
+    for r in rows[1:]:
+        i = int(r[col["ID"]])
+        d = launches.setdefault(i, {"kernel": r[col["Kernel Name"]]})
+        d[r[col["Metric Name"]]] = float(r[col["Metric Value"]].replace(",", ""))
+    from split_bf16_gemm_swapped_gb300 import workloads as W  # noqa: F401
+    out = []
+    first = 0
+    for key, n in zip(keys, per):
+        ids = list(range(first + n - use_last, first + n))
+        first += n
+        got = [launches[i] for i in ids if i in launches]
+        if not got:
+            continue
+        traffic = statistics.mean(g["dram__bytes_read.sum"] + g["dram__bytes_write.sum"] for g in got)
+        dur = statistics.mean(g.get("gpu__time_duration.sum", 0.0) for g in got)
+        w = workload_by_name(key)
+        name = got[-1]["kernel"].replace("void ", "").split("(")[0]
+        out.append(f"traffic {key}: {traffic:.0f} B  (algorithmic {w.bytes} B, {traffic / w.bytes:.3f}x; "
+                   f"{name}; ncu duration {dur / 1e3:.1f} us, serialised)")
+    return "\n".join(out)
+
+
 def run_sweep_w4(args):
     """Extra lines for the A16W4 variant (4-bit E2M1 weights with E8M0 scales
     per 32 k, bf16 activations) on the decode shapes: HBM TB/s of the bytes
@@ -819,6 +859,8 @@ def main():
                     help="a short eager run for ncu of one workload, or `all` of them in turn "
                          "(no graphs, one weight copy)")
     ap.add_argument("--w4", action="store_true", help="with --profile-case: the A16W4 kernel")
+    ap.add_argument("--ncu-table", nargs=2, metavar=("CSV", "LOG"), default=None,
+                    help="print the DRAM-traffic table from an ncu CSV of a --profile-case run and its log")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
@@ -828,7 +870,9 @@ def main():
         workload_by_name(args.workload)
     if args.profile_case not in (None, "all"):
         workload_by_name(args.profile_case)
-    if args.cpu_table:
+    if args.ncu_table:
+        print(ncu_traffic_table(args.ncu_table[0], args.ncu_table[1], args.steps))
+    elif args.cpu_table:
         run_cpu_table(args)
     elif args.impl == "reference":
         run_reference(args)
