@@ -70,7 +70,7 @@ def workload_key(w) -> str:
         return fixed[w]
     if w.name == "sweep":
         return f"sweep_m{w.M}_s{w.split_k}"
-    return f"{w.name}_m{w.M}_n{w.N}_k{w.K}_l{w.L}_s{w.split_k}"
+    return f"shape_m{w.M}_n{w.N}_k{w.K}_l{w.L}_s{w.split_k}"
 
 
 def workload_by_name(name: str):
@@ -82,6 +82,10 @@ def workload_by_name(name: str):
     if name.startswith("sweep_m"):
         m, s = name[len("sweep_m"):].split("_s")
         return W.sweep(int(m), int(s))
+    if name.startswith("shape_"):
+        # shape_m<M>_n<N>_k<K>_l<L>_s<split>: decode-like inputs (seed 1) of any shape
+        f = dict((part[0], int(part[1:])) for part in name[len("shape_"):].split("_"))
+        return W.DECODE_M1.with_(name="shape", M=f["m"], N=f["n"], K=f["k"], L=f["l"], split_k=f["s"])
     raise SystemExit(f"unknown workload {name}")
 
 
