@@ -52,6 +52,8 @@ METRIC = "achieved HBM TB/s (and % of roofline) vs M for BF16 split-K decode GEM
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 KERNEL_SOURCES = ["split_bf16_gemm_swapped_gb300/csrc/splitk_kernel.cu",
+                  "split_bf16_gemm_swapped_gb300/csrc/splitk_persistent.cu",
+                  "split_bf16_gemm_swapped_gb300/csrc/splitk_kernel_common.cuh",
                   "split_bf16_gemm_swapped_gb300/csrc/splitk_device.cuh",
                   "split_bf16_gemm_swapped_gb300/csrc/splitk_internal.h"]
 TRAFFIC_TABLE = ROOT / "profiles" / "splitk_dram_traffic.txt"
@@ -808,6 +810,61 @@ def run_sweep_w4(args):
         raise SystemExit(f"kernel fault during the sweep: {sk.splitk_get_fault()}")
 
 
+def run_sweep_persistent(args):
+    """Extra lines: for every sweep point with split >= 2 and the wide
+    projection, the per-tile kernel's plan against the persistent kernel at
+    each ring depth, each timed like the main line (a graph of --steps calls,
+    median of back-to-back replays)."""
+    import torch
+
+    import split_bf16_gemm_swapped_gb300 as sk
+    from split_bf16_gemm_swapped_gb300 import workloads as W
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = props.L2_cache_size
+    stream = torch.cuda.Stream(dev)
+    cache = {}
+    ws = [w for w in W.all_sweep() if w.split_k >= 2] + [W.WIDE_S2, W.WIDE_S4]
+    for w in ws:
+        copies, _ = weight_copies(w, dev, l2, args.rotate, cache)
+        R = len(copies)
+        b = to_dev(w.make_b(), dev)
+        c = torch.empty((w.L, w.M, w.N), dtype=torch.bfloat16, device=dev)
+        cands = sk.splitk_plan_candidates_for(w.M, w.N, w.K, w.L, w.split_k, props.multi_processor_count,
+                                              props.shared_memory_per_multiprocessor,
+                                              props.shared_memory_per_block_optin)
+        ring = next(p for p in cands if not p.persistent)
+        plans = [("per-tile", ring)] + [(f"persistent s{p.stages}", p) for p in cands if p.persistent]
+        out = {}
+        for name, plan in plans:
+            def call(i, plan=plan):
+                sk.splitk_gemm_bf16_planned(copies[i % R], b, c, plan, 0, stream)
+            with torch.cuda.stream(stream):
+                for i in range(max(args.warmup, R)):
+                    call(i)
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(args.steps):
+                    call(i)
+            with torch.cuda.stream(stream):
+                g.replay()
+            stream.synchronize()
+            one = time_replays(g, stream, 1)[0]
+            ms = statistics.median(time_replays(g, stream, repeats_for(one, args.min_ms))) / args.steps
+            out[name] = round(ms * 1e3, 2)
+            del g
+        best = min(out, key=out.get)
+        hbm = peaks()[0]
+        print(json.dumps({"sweep": "persistent vs per-tile " + describe(w), "us": out, "best": best,
+                          "best_hbm_frac": round(w.bytes / (out[best] * 1e-6) / 1e9 / hbm, 3),
+                          "planner": "persistent" if cands[0].persistent else "per-tile"}), flush=True)
+        del b, c
+    if sk.splitk_get_status() != 0:
+        raise SystemExit(f"kernel fault during the sweep: {sk.splitk_get_fault()}")
+
+
 def run_sweep_fixed(args):
     """Extra lines, one per fixed workload (tiny, the two decode shapes, the
     wide projection at both splits), timed like the main line."""
@@ -848,8 +905,9 @@ def main():
                          "sweep_m<M>_s<split>")
     ap.add_argument("--min-ms", type=float, default=40.0,
                     help="GPU time each point's back-to-back replays cover at least")
-    ap.add_argument("--sweep", choices=["fixed", "w4a16"], default=None,
-                    help="extra lines instead of the contract line: the fixed workloads, or A16W4")
+    ap.add_argument("--sweep", choices=["fixed", "w4a16", "persistent"], default=None,
+                    help="extra lines instead of the contract line: the fixed workloads, A16W4, or the "
+                         "per-tile against the persistent kernel")
     ap.add_argument("--no-extras", action="store_true", help="skip the decode workloads of the sweep line")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the timed oracle leg")
     ap.add_argument("--no-e2e", dest="e2e", action="store_false", help="skip the end-to-end measurement")
@@ -886,6 +944,8 @@ def main():
         run_sweep_w4(args)
     elif args.sweep == "fixed":
         run_sweep_fixed(args)
+    elif args.sweep == "persistent":
+        run_sweep_persistent(args)
     else:
         run_ours(args)
 

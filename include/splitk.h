@@ -168,6 +168,20 @@ typedef struct splitk_plan_t {
                               memory, so that every tile is decoded before the
                               programmatic-dependent-launch wait returns     */
     int reserved;          /* must be 0                                      */
+    int persistent;        /* 0: one CTA per (output tile, K rank), the grid
+                              above.  1: the persistent kernel: grid
+                              (split_k, clusters, 1), each cluster of split_k
+                              CTAs (one per SM) walking the output tiles
+                              `clusters` apart, its ring running on from tile
+                              to tile and its accumulator alternating between
+                              two TMEM buffers, so that a tile's reduction
+                              overlaps the next tile's loads and MMAs.  Needs
+                              split_k >= 2 and the scattered reduction
+                              (reduce_scatter = 1, mailbox_dedicated = 1,
+                              b_resident = 0, a_tmem_tiles = 0,
+                              mma_issuers = 1).  grid[1] is an upper bound: a
+                              launch uses at most as many clusters as the
+                              device holds at once and as there are tiles   */
 } splitk_plan_t;
 
 /*
@@ -244,12 +258,14 @@ SPLITK_API int splitk_plan_check_for(const splitk_plan_t *plan, int M, int N,
 
 /*
  * Every valid tactic for a shape on a described device, without CUDA:
- * splitk_plan_for()'s choice first, then the page's ring (2-8 stages, one or
+ * splitk_plan_for()'s choice first (followed, when that is a persistent plan,
+ * by the per-tile kernel's own choice), then the page's ring (2-8 stages, one or
  * two MMA issuers, either PDL trigger) and the staged family (resident
  * activations, 0-3 weight tiles in tensor memory, TMA or epilogue-thread
  * activation loads, L2 prefetch), for each split (all valid ones when
  * split_k = 0) and each reduction (rank 0 with its own or an aliased
- * mailbox, scattered).  Writes up to max_out plans to out and returns how
+ * mailbox, scattered), then the persistent kernel at each ring depth that
+ * fits (split_k >= 2).  Writes up to max_out plans to out and returns how
  * many exist (call with max_out = 0 to size the array), or a negative
  * status.
  */
@@ -382,7 +398,8 @@ typedef struct splitk_fault_t {
     int code;        /* SPLITK_OK or SPLITK_ERR_TIMEOUT                        */
     int role;        /* 0 weight TMA, 1 activation TMA, 2 MMA, 3 TMEM release,
                         4 epilogue: MMA completion, 5 epilogue: partials
-                        (rank 0), 6 epilogue: mailbox free (peer)              */
+                        (rank 0), 6 epilogue: mailbox free (peer), 7 A16W4
+                        decode, 8 MMA: accumulator free (persistent plans)   */
     int index;       /* K tile or reduction round being waited for             */
     int parity;      /* mbarrier phase parity waited for                       */
     int block[3];    /* blockIdx of the CTA                                    */

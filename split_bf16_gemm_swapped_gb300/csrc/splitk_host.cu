@@ -95,6 +95,14 @@ uint32_t w4_mailbox_bytes(int split, int reduce_scatter, int ncols_max) {
 // reserves 1 KiB of the SM's shared memory).
 int resident_by_smem(size_t smem_per_sm, size_t smem) { return (int)(smem_per_sm / (smem + 1024)); }
 
+// Shared memory of a persistent plan: the ring (a weight and an activation K
+// tile per stage), the scattered mailbox of min(M, mma_n) token columns and
+// the barriers.
+size_t smem_bytes_persistent(int mma_n, int stages, int ncols_max) {
+  return (size_t)kAlignSlack + (size_t)stages * (kAStageBytes + b_stage_bytes(mma_n)) +
+         (size_t)ncols_max * kColumnBytes + kBarRegionBytes;
+}
+
 // 128-wide K tiles covering K; the last one may be ragged (TMA reads zeros
 // past K).
 inline int total_k_tiles(int K) { return (int)(((long long)K + kCtaK - 1) / kCtaK); }
@@ -167,8 +175,71 @@ bool stage_for_decode(splitk_plan_t* out, int ncols_max, long long ctas, int num
   return true;
 }
 
+// The persistent plan for a shape and a split of 2 or more: one CTA per SM
+// with the deepest ring (2 to 8 stages, or exactly `stages` when that is
+// given) that fits beside the scattered mailbox, two accumulators in TMEM,
+// and one cluster per `split` SMs (at most one per output tile).
+bool persistent_plan(int M, int N, int K, int L, int split, int stages, int num_sms, size_t smem_per_sm,
+                     size_t smem_optin, splitk_plan_t* out) {
+  if (split < 2 || !valid_split(split)) return false;
+  const int T = total_k_tiles(K);
+  if (T < split) return false;
+  const int mma_n = choose_mma_n(M);
+  const int ncols_max = std::min(M, mma_n);
+  const size_t budget = std::min(smem_optin, smem_per_sm - 1024);
+  int st = stages;
+  if (st == 0) {
+    for (st = kMaxStages; st > 2 && smem_bytes_persistent(mma_n, st, ncols_max) > budget; --st) {
+    }
+  }
+  if (st < 2 || st > kMaxStages || smem_bytes_persistent(mma_n, st, ncols_max) > budget) return false;
+  const long long tiles = tiles_of(M, mma_n) * tiles_of(N, kMmaM) * L;
+  const long long clusters = std::max<long long>(1, std::min<long long>(tiles, num_sms / split));
+  std::memset(out, 0, sizeof(*out));
+  out->mma_m = kMmaM;
+  out->mma_n = mma_n;
+  out->stages = st;
+  out->split_k = split;
+  out->k_tiles_per_cta = (T + split - 1) / split;
+  out->mailbox_dedicated = 1;
+  out->mailbox_quads = (ncols_max + 3) / 4;
+  out->reduce_rounds = 1;
+  out->grid[0] = (unsigned)split;
+  out->grid[1] = (unsigned)std::min<long long>(clusters, 65535);
+  out->grid[2] = 1;
+  out->cluster[0] = (unsigned)split;
+  out->cluster[1] = 1;
+  out->cluster[2] = 1;
+  out->smem_bytes = smem_bytes_persistent(mma_n, st, ncols_max);
+  out->ctas_per_sm = 1;
+  out->reduce_scatter = 1;
+  out->mma_issuers = 1;
+  out->tmem_cols = pow2_at_least(2u * tmem_acc_cols(mma_n));
+  out->weight_format = SPLITK_WEIGHTS_BF16;
+  out->persistent = 1;
+  return true;
+}
+
+int plan_ring_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t smem_per_sm,
+                   size_t smem_optin, splitk_plan_t* out);
+
+// The plan: the per-tile kernel's (plan_ring_impl), or, for wide tiles
+// (mma_n >= 64) at splits of 4 and 8 whose grid exceeds one CTA per SM, the
+// persistent kernel, whose reduction overlaps the next tile's stream.
 int plan_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t smem_per_sm,
               size_t smem_optin, splitk_plan_t* out) {
+  const int rc = plan_ring_impl(M, N, K, L, split_k, num_sms, smem_per_sm, smem_optin, out);
+  if (rc != SPLITK_OK) return rc;
+  const long long tiles = tiles_of(M, out->mma_n) * tiles_of(N, kMmaM) * L;
+  if (out->split_k >= 4 && out->mma_n >= 64 && tiles * out->split_k > num_sms) {
+    splitk_plan_t p;
+    if (persistent_plan(M, N, K, L, out->split_k, 0, num_sms, smem_per_sm, smem_optin, &p)) *out = p;
+  }
+  return SPLITK_OK;
+}
+
+int plan_ring_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t smem_per_sm,
+                   size_t smem_optin, splitk_plan_t* out) {
   if (!out) return SPLITK_ERR_NULL;
   std::memset(out, 0, sizeof(*out));   // fields a bf16 plan does not use stay 0
   if (M < 1 || N < 1 || K < 1 || L < 1) return SPLITK_ERR_INVALID_SHAPE;
@@ -417,7 +488,7 @@ int check_plan_w4(const splitk_plan_t& pl, int M, int N, int K, int L, size_t sm
   const int kt = (T + pl.split_k - 1) / pl.split_k;
   if (pl.k_tiles_per_cta != kt || pl.stages != kt) return SPLITK_ERR_BAD_PLAN;
   if (kt > kMaxStages) return SPLITK_ERR_NO_FIT;
-  if (pl.reserved != 0) return SPLITK_ERR_BAD_PLAN;
+  if (pl.reserved != 0 || pl.persistent != 0) return SPLITK_ERR_BAD_PLAN;
   const long long m_tiles = tiles_of(M, pl.mma_n);
   const long long n_tiles = ((long long)N + kMmaM - 1) / kMmaM;
   if (n_tiles > 65535 || L > 65535) return SPLITK_ERR_INVALID_SHAPE;
@@ -453,12 +524,43 @@ int check_plan_w4(const splitk_plan_t& pl, int M, int N, int K, int L, size_t sm
   return SPLITK_OK;
 }
 
+// Re-derives everything a persistent plan implies and checks it.
+int check_plan_persistent(const splitk_plan_t& pl, int M, int N, int K, int L, size_t smem_optin,
+                          size_t smem_per_sm, uint32_t* dedicated_bytes) {
+  if (pl.persistent != 1 || pl.mma_m != kMmaM) return SPLITK_ERR_BAD_PLAN;
+  if (pl.mma_n != 16 && pl.mma_n != 32 && pl.mma_n != 64 && pl.mma_n != 128) return SPLITK_ERR_BAD_PLAN;
+  if (!valid_split(pl.split_k)) return SPLITK_ERR_UNSUPPORTED_SPLIT;
+  if (pl.split_k < 2) return SPLITK_ERR_BAD_PLAN;
+  if (K % 8 != 0 || K > kMaxK || total_k_tiles(K) < pl.split_k) return SPLITK_ERR_INVALID_SHAPE;
+  if (pl.k_tiles_per_cta != (total_k_tiles(K) + pl.split_k - 1) / pl.split_k) return SPLITK_ERR_BAD_PLAN;
+  if (pl.stages < 2 || pl.stages > kMaxStages) return SPLITK_ERR_BAD_PLAN;
+  if (L > 65535) return SPLITK_ERR_INVALID_SHAPE;
+  if (pl.grid[0] != (unsigned)pl.split_k || pl.grid[1] < 1 || pl.grid[1] > 65535 || pl.grid[2] != 1 ||
+      pl.cluster[0] != (unsigned)pl.split_k || pl.cluster[1] != 1 || pl.cluster[2] != 1) {
+    return SPLITK_ERR_BAD_PLAN;
+  }
+  const int ncols_max = std::min(M, pl.mma_n);
+  if (pl.reduce_scatter != 1 || pl.mailbox_dedicated != 1 || pl.mailbox_quads != (ncols_max + 3) / 4 ||
+      pl.b_resident != 0 || pl.a_tmem_tiles != 0 || pl.mma_issuers != 1 || pl.b_loader != 0 ||
+      pl.l2_prefetch != 0 || pl.pdl_trigger != 0 || pl.reserved != 0) {
+    return SPLITK_ERR_BAD_PLAN;
+  }
+  if (pl.tmem_cols != pow2_at_least(2u * tmem_acc_cols(pl.mma_n))) return SPLITK_ERR_BAD_PLAN;
+  const size_t smem = smem_bytes_persistent(pl.mma_n, pl.stages, ncols_max);
+  if (smem != pl.smem_bytes) return SPLITK_ERR_BAD_PLAN;
+  if (smem > smem_optin) return SPLITK_ERR_NO_FIT;
+  if ((size_t)resident_by_smem(smem_per_sm, smem) * pl.tmem_cols > 512u) return SPLITK_ERR_BAD_PLAN;
+  *dedicated_bytes = (uint32_t)ncols_max * kColumnBytes;
+  return SPLITK_OK;
+}
+
 int check_plan(const splitk_plan_t& pl, int M, int N, int K, int L, size_t smem_optin,
                size_t smem_per_sm, uint32_t* dedicated_bytes) {
   if (pl.weight_format == SPLITK_WEIGHTS_E2M1_E8M0) {
     return check_plan_w4(pl, M, N, K, L, smem_optin, smem_per_sm, dedicated_bytes);
   }
   if (pl.weight_format != SPLITK_WEIGHTS_BF16 || pl.w4_smem_tiles != 0) return SPLITK_ERR_BAD_PLAN;
+  if (pl.persistent != 0) return check_plan_persistent(pl, M, N, K, L, smem_optin, smem_per_sm, dedicated_bytes);
   if (pl.mma_m != kMmaM) return SPLITK_ERR_BAD_PLAN;
   if (pl.mma_n != 16 && pl.mma_n != 32 && pl.mma_n != 64 && pl.mma_n != 128) return SPLITK_ERR_BAD_PLAN;
   if (!valid_split(pl.split_k)) return SPLITK_ERR_UNSUPPORTED_SPLIT;
@@ -613,6 +715,7 @@ struct DeviceState {
   int used = 0;
   std::unordered_map<AKey, int, AKeyHash> a_slots;
   std::unordered_map<BKey, CUtensorMap, BKeyHash> b_maps;
+  std::unordered_map<uint64_t, int> max_clusters;   // persistent kernel: clusters resident at once
 };
 
 std::mutex g_mu;
@@ -641,7 +744,7 @@ int current_device(DeviceState** out, int* dev_out) {
     }
     if (major != 10 || minor != 3) return SPLITK_ERR_UNSUPPORTED_DEVICE;
     if (!encode_fn()) return SPLITK_ERR_CUDA;
-    if (prepare_kernels(optin) != cudaSuccess) {
+    if (prepare_kernels(optin) != cudaSuccess || prepare_persistent(optin) != cudaSuccess) {
       cudaGetLastError();
       return SPLITK_ERR_CUDA;
     }
@@ -772,11 +875,37 @@ LaunchArgs launch_args(const splitk_plan_t& pl, bool pdl) {
   LaunchArgs la;
   la.mma_n = pl.mma_n;
   la.w4 = pl.weight_format == SPLITK_WEIGHTS_E2M1_E8M0;
+  la.persistent = pl.persistent != 0;
   la.grid = dim3(pl.grid[0], pl.grid[1], pl.grid[2]);
   la.cluster_x = (unsigned)pl.split_k;
   la.smem_bytes = pl.smem_bytes;
   la.pdl = pdl;
   return la;
+}
+
+// Caller holds g_mu.  Launches a checked plan: the per-tile kernel, or the
+// persistent one with as many clusters as the device holds at once (at most
+// the plan's grid[1] and the output tiles; the kernel is correct for any
+// number, as each cluster walks the tiles that many apart).
+cudaError_t launch_plan(DeviceState& st, const splitk_plan_t& pl, const LaunchArgs& la0, const CUtensorMap& b_map,
+                        const KernelParams& p, int M, int N, int L, cudaStream_t stream) {
+  if (!la0.persistent) return launch_kernel(la0, b_map, p, stream);
+  LaunchArgs la = la0;
+  const uint64_t key = ((uint64_t)pl.mma_n << 48) | ((uint64_t)pl.split_k << 40) | (uint64_t)pl.smem_bytes;
+  auto it = st.max_clusters.find(key);
+  if (it == st.max_clusters.end()) {
+    int fit = 0;
+    if (max_active_clusters_persistent(pl.mma_n, (unsigned)pl.split_k, pl.smem_bytes, &fit) != cudaSuccess) {
+      cudaGetLastError();
+      fit = 0;                                   // unknown: the plan's own bound
+    }
+    it = st.max_clusters.emplace(key, fit).first;
+  }
+  const long long tiles = tiles_of(M, pl.mma_n) * tiles_of(N, kMmaM) * L;
+  long long g = std::min<long long>((long long)pl.grid[1], tiles);
+  if (it->second > 0) g = std::min<long long>(g, it->second);
+  la.grid = dim3((unsigned)pl.split_k, (unsigned)std::max<long long>(1, g), 1u);
+  return launch_persistent(la, b_map, p, stream);
 }
 
 // Caller holds g_mu.
@@ -798,7 +927,7 @@ int launch_locked(DeviceState& st, const void* a, const void* b, void* c, int M,
   KernelParams p;
   fill_params(pl, M, N, K, L, ded, a_map, b, c, bias, &p, a_scale);
   const LaunchArgs la = launch_args(pl, (flags & SPLITK_FLAG_NO_PDL) == 0);
-  if (launch_kernel(la, b_map, p, stream) != cudaSuccess) {
+  if (launch_plan(st, pl, la, b_map, p, M, N, L, stream) != cudaSuccess) {
     cudaGetLastError();
     return SPLITK_ERR_CUDA;
   }
@@ -833,6 +962,13 @@ int enumerate_plans(int M, int N, int K, int L, int split_k, int num_sms, size_t
   int rc = plan_impl(M, N, K, L, split_k, num_sms, smem_per_sm, smem_optin, &base);
   if (rc != SPLITK_OK) return rc;
   out->push_back(base);
+  if (base.persistent) {
+    // the per-tile kernel's own choice next, for comparison
+    splitk_plan_t ring;
+    if (plan_ring_impl(M, N, K, L, split_k, num_sms, smem_per_sm, smem_optin, &ring) == SPLITK_OK) {
+      out->push_back(ring);
+    }
+  }
   const int T = total_k_tiles(K);
   const int mma_n = base.mma_n;
   const long long m_tiles = tiles_of(M, mma_n);
@@ -914,6 +1050,18 @@ int enumerate_plans(int M, int N, int K, int L, int split_k, int num_sms, size_t
           }
         }
       }
+    }
+    // the persistent kernel at every ring depth that fits
+    for (int stages = 2; split >= 2 && stages <= kMaxStages; ++stages) {
+      splitk_plan_t p;
+      uint32_t ded_check = 0;
+      if (!persistent_plan(M, N, K, L, split, stages, num_sms, smem_per_sm, smem_optin, &p) ||
+          check_plan(p, M, N, K, L, smem_optin, smem_per_sm, &ded_check) != SPLITK_OK) {
+        continue;
+      }
+      bool dup = false;
+      for (const auto& q : *out) dup = dup || same(p, q);
+      if (!dup) out->push_back(p);
     }
   }
   return SPLITK_OK;
@@ -1089,7 +1237,7 @@ SPLITK_API int splitk_gemm_bf16_noalloc(const void* a, const void* b, void* c, i
   KernelParams p;
   fill_params(pl, M, N, K, L, ded, scratch_map, b, c, nullptr, &p);
   const LaunchArgs la = launch_args(pl, true);
-  if (launch_kernel(la, b_map, p, s) != cudaSuccess) {
+  if (launch_plan(*st, pl, la, b_map, p, M, N, L, s) != cudaSuccess) {
     cudaGetLastError();
     return SPLITK_ERR_CUDA;
   }
@@ -1225,10 +1373,12 @@ SPLITK_API int splitk_get_fault(splitk_fault_t* out) {
       cudaGetLastError();
       return SPLITK_ERR_UNSUPPORTED_DEVICE;
     }
-    if (read_and_clear_fault(words) != cudaSuccess) {
+    int words_p[kFaultWords] = {0};
+    if (read_and_clear_fault(words) != cudaSuccess || read_and_clear_fault_persistent(words_p) != cudaSuccess) {
       cudaGetLastError();
       return SPLITK_ERR_CUDA;
     }
+    if (words[0] == 0) std::memcpy(words, words_p, sizeof(words));
   }
   if (out) {
     out->code = words[0];

@@ -68,6 +68,7 @@ enum Role : int {
   kRoleEpiReduce = 5,
   kRoleEpiReady = 6,
   kRoleEpiDecode = 7,
+  kRoleMmaAccFree = 8,   // persistent kernel: MMA issuer waiting for an accumulator to be read
 };
 
 constexpr unsigned kInjectSkipPublish = 0x1u;
@@ -127,6 +128,7 @@ enum TraceSlot : int {
 struct LaunchArgs {
   int mma_n;
   bool w4;                    // A16W4 weights
+  bool persistent;            // the persistent kernel (grid = (split, clusters, 1))
   dim3 grid;
   unsigned cluster_x;
   size_t smem_bytes;
@@ -138,5 +140,12 @@ cudaError_t launch_kernel(const LaunchArgs& la, const CUtensorMap& b_map,
                           const KernelParams& p, cudaStream_t stream);
 cudaError_t prepare_kernels(int max_dynamic_smem);
 cudaError_t read_and_clear_fault(int* out_words);
+
+// Defined in splitk_persistent.cu.
+cudaError_t launch_persistent(const LaunchArgs& la, const CUtensorMap& b_map,
+                              const KernelParams& p, cudaStream_t stream);
+cudaError_t max_active_clusters_persistent(int mma_n, unsigned cluster_x, size_t smem, int* out);
+cudaError_t prepare_persistent(int max_dynamic_smem);
+cudaError_t read_and_clear_fault_persistent(int* out_words);
 
 }  // namespace splitk

@@ -135,8 +135,8 @@ def test_plan_of_the_decode_workloads():
     assert list(p.grid) == [8, 32, 1]
     p = _plan(64, 18432, 7168, 1, 2)
     assert (p.mma_n, list(p.grid)) == (64, [2, 144, 1])
-    p = _plan(128, 7168, 16384, 2, 8)
-    assert (p.mma_n, list(p.grid), p.k_tiles_per_cta) == (128, [8, 56, 2], 16)
+    p = _plan(128, 7168, 16384, 2, 8)              # persistent: 152 SMs / 8 = 19 clusters
+    assert (p.mma_n, list(p.grid), p.k_tiles_per_cta, p.persistent) == (128, [8, 19, 1], 16, 1)
     assert p.reduce_rounds >= 1 and p.mailbox_quads % 4 == 0
 
 
@@ -187,6 +187,25 @@ def test_k_tails_take_ragged_tiles(K, split, k_tiles):
     assert p.k_tiles_per_cta == k_tiles
 
 
+def _check_persistent(p, M, N, K, L, split):
+    """The invariants of a persistent plan: a cluster of split CTAs per
+    `split` SMs (at most one per output tile), one CTA per SM, two
+    accumulators, the scattered mailbox beside a ring of weight and
+    activation stages."""
+    tiles = -(-M // p.mma_n) * -(-N // 128) * L
+    assert split >= 2 and p.split_k == split
+    assert list(p.grid) == [split, max(1, min(tiles, GB300["num_sms"] // split)), 1]
+    assert list(p.cluster) == [split, 1, 1]
+    assert (p.reduce_scatter, p.mailbox_dedicated, p.reduce_rounds, p.b_resident, p.a_tmem_tiles,
+            p.mma_issuers, p.b_loader, p.l2_prefetch, p.ctas_per_sm) == (1, 1, 1, 0, 0, 1, 0, 0, 1)
+    assert p.tmem_cols == next(c for c in (32, 64, 128, 256, 512) if c >= 2 * max(32, p.mma_n))
+    assert 2 <= p.stages <= 8
+    assert p.smem_bytes == 1024 + p.stages * (32768 + p.mma_n * 256) + min(M, p.mma_n) * 512 + 256
+    assert p.smem_bytes <= min(GB300["smem_per_block_optin"], GB300["smem_per_sm"] - 1024)
+    if p.stages < 8:   # the deepest ring that fits
+        assert p.smem_bytes + 32768 + p.mma_n * 256 > min(GB300["smem_per_block_optin"], GB300["smem_per_sm"] - 1024)
+
+
 @pytest.mark.parametrize("M", [1, 4, 16, 17, 32, 33, 64, 65, 128, 129, 1000])
 @pytest.mark.parametrize("split", [1, 2, 4, 8])
 def test_every_plan_fits_and_is_consistent(M, split):
@@ -194,6 +213,9 @@ def test_every_plan_fits_and_is_consistent(M, split):
     p = _plan(M, 7168, K, 2, split)
     assert p.k_tiles_per_cta == -(-(-(-K // 128)) // split)
     assert p.mma_n >= min(M, 128) or p.mma_n == 128
+    if p.persistent:
+        _check_persistent(p, M, 7168, K, 2, split)
+        return
     assert p.grid[0] == split * -(-M // p.mma_n)
     assert 2 <= p.stages <= 8
     assert p.smem_bytes <= GB300["smem_per_block_optin"]

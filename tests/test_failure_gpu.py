@@ -75,3 +75,35 @@ def test_no_fault_recorded_in_normal_operation():
         sk.splitk_gemm_bf16(ta, tb, split_k=split)
     torch.cuda.synchronize()
     assert sk.splitk_get_fault()["code"] == 0
+
+
+def test_persistent_plan_skipped_publish_times_out_and_the_context_survives():
+    """The persistent kernel's bounded waits: with the peers' partials
+    withheld every rank's reduction wait runs out, the launch ends, and a
+    normal call afterwards is correct."""
+    M, N, K, L, split = 64, 1000, 4096, 1, 4
+    a = synthetic.normal_bf16((L, N, K), 901, synthetic.STREAM_A, 0.02)
+    b = synthetic.normal_bf16((L, M, K), 901, synthetic.STREAM_B, 1.0)
+    ta, tb = to_dev(a), to_dev(b)
+    props = torch.cuda.get_device_properties(0)
+    plan = next(p for p in sk.splitk_plan_candidates_for(M, N, K, L, split, props.multi_processor_count,
+                                                          props.shared_memory_per_multiprocessor,
+                                                          props.shared_memory_per_block_optin)
+                if p.persistent)
+    plan.grid[1] = 2                                     # each cluster walks several tiles
+    try:
+        sk.splitk_set_wait_limit_ns(50_000_000)          # 50 ms
+        sk.splitk_debug_inject(sk.INJECT_SKIP_PUBLISH)
+        sk.splitk_gemm_bf16_planned(ta, tb, None, plan)
+        torch.cuda.synchronize()
+    finally:
+        sk.splitk_debug_inject(0)
+        sk.splitk_set_wait_limit_ns(0)
+    fault = sk.splitk_get_fault()
+    assert fault["code"] == -6, fault
+    assert fault["role"] == ROLE_EPI_REDUCE, fault
+    assert sk.splitk_get_status() == 0
+    c = to_host(sk.splitk_gemm_bf16_planned(ta, tb, None, plan))
+    torch.cuda.synchronize()
+    assert sk.splitk_get_status() == 0
+    assert_parity(c, oracle.gemm(a, b), a, b, K)

@@ -639,3 +639,79 @@ def test_w4a16_the_largest_grid_dimensions_index_correctly(L, N):
     assert np.array_equal(got.view(np.float32).astype(np.float64), expect)
     del c
     torch.cuda.empty_cache()
+
+
+# ---------------------------------------------------------------- persistent plans
+def _persistent(M, N, K, L, split, clusters=None, stages=None):
+    """The persistent plan of the shape at `split` (the deepest ring unless
+    `stages` is given), with `clusters` as its grid bound if given."""
+    props = torch.cuda.get_device_properties(DEV)
+    cands = sk.splitk_plan_candidates_for(M, N, K, L, split, props.multi_processor_count,
+                                          props.shared_memory_per_multiprocessor,
+                                          props.shared_memory_per_block_optin)
+    ps = [p for p in cands if p.persistent]
+    assert ps, "no persistent candidate"
+    p = max(ps, key=lambda q: q.stages) if stages is None else next(q for q in ps if q.stages == stages)
+    p = sk.Plan.from_buffer_copy(p)
+    if clusters is not None:
+        p.grid[1] = clusters
+    return p
+
+
+@pytest.mark.parametrize("M,N,K,L,split,clusters", [
+    (64, 1000, 4096, 2, 4, 3),      # a ragged weight tile; 3 clusters walk 16 tiles
+    (128, 384, 2048, 3, 8, 2),
+    (100, 700, 3000, 1, 2, 1),      # ragged K and a ragged token tile; one cluster walks all tiles
+    (129, 300, 2040, 2, 4, None),   # two token tiles, the second with one column
+    (33, 520, 1024, 2, 8, 4),
+    (16, 1024, 8192, 2, 4, 5),
+    (1, 640, 2048, 1, 2, 2),
+])
+def test_persistent_kernel_matches_the_oracle(M, N, K, L, split, clusters):
+    """Clusters that each walk several output tiles, with the ring running on
+    across tiles and two accumulators, against the oracle."""
+    a, b = _draw(L, M, N, K, seed=2700 + M + split)
+    p = _persistent(M, N, K, L, split, clusters)
+    c = gemm_gpu(a, b, plan=p)
+    assert_parity(c, oracle_full(a, b), a, b, K)
+    assert np.array_equal(c, gemm_gpu(a, b, plan=p))          # run to run
+
+
+@pytest.mark.parametrize("split", [2, 4, 8])
+@pytest.mark.parametrize("M", [5, 64, 128])
+def test_persistent_kernel_equals_the_scattered_per_tile_kernel_bit_for_bit(M, split):
+    """The same partials (one issuer, the same K slices) summed over ranks in
+    the same order: the persistent and the per-tile scattered kernels give
+    the same bits, at every ring depth and cluster count."""
+    L, N, K = 2, 640, 4096
+    a, b = _draw(L, M, N, K, seed=2800 + M + split)
+    base = _ring(sk.splitk_plan(M, N, K, L, split), M)
+    ref_plan = _scatter(base, M)
+    if ref_plan.smem_bytes > 232448:
+        ref_plan = _scatter(base, M, stages=2)
+    want = gemm_gpu(a, b, plan=ref_plan)
+    for stages, clusters in [(None, None), (2, 1), (3, 7)]:
+        try:
+            p = _persistent(M, N, K, L, split, clusters, stages)
+        except StopIteration:
+            continue                                          # that depth does not fit
+        assert np.array_equal(gemm_gpu(a, b, plan=p), want), (stages, clusters)
+
+
+def test_persistent_kernel_closed_forms_and_bias():
+    """All-ones inputs give C = K exactly; the bias is added before the one
+    rounding, as by the oracle."""
+    L, M, N, K, split = 2, 64, 1000, 4096, 4
+    p = _persistent(M, N, K, L, split, clusters=5)
+    ones = np.full((L, N, K), ONE, np.uint16)
+    c = gemm_gpu(ones, np.full((L, M, K), ONE, np.uint16), plan=p)
+    assert np.all(c == oracle.f64_to_bf16(float(K)))
+    # a shape whose plan is persistent (more CTAs than SMs), through the bias entry point
+    L, M, N, K = 1, 64, 5000, 2048
+    assert sk.splitk_plan(M, N, K, L, split).persistent == 1
+    a, b = _draw(L, M, N, K, seed=2900)
+    bias = synthetic.normal_bf16((L, N), 2900, synthetic.STREAM_OUTLIER, 0.5)
+    tc = sk.splitk_gemm_bf16_bias(to_dev(a), to_dev(b), to_dev(bias), split_k=split)
+    torch.cuda.synchronize()
+    assert sk.splitk_get_status() == 0
+    assert_parity(to_host(tc), oracle.gemm_bias(a, b, bias), a, b, K)
