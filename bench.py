@@ -747,6 +747,65 @@ def ncu_traffic_table(csv_path: str, log_path: str, use_last: int) -> str:
     return "\n".join(out)
 
 
+NCU_SUMMARY_METRICS = [
+    ("gpu__time_duration.sum", "duration (serialised, cold caches)"),
+    ("dram__bytes_read.sum", "DRAM read"),
+    ("dram__bytes_write.sum", "DRAM write"),
+    ("gpu__dram_throughput.avg.pct_of_peak_sustained_elapsed", "DRAM throughput, % of peak"),
+    ("lts__throughput.avg.pct_of_peak_sustained_elapsed", "L2 throughput, % of peak"),
+    ("sm__pipe_tensor_cycles_active.avg.pct_of_peak_sustained_elapsed", "tensor pipe active, % of elapsed"),
+    ("sm__pipe_tensor_cycles_active.avg.pct_of_peak_sustained_active", "tensor pipe active, % of SM-active"),
+    ("sm__issue_active.avg.pct_of_peak_sustained_elapsed", "SM issue active, %"),
+    ("sm__warps_active.avg.pct_of_peak_sustained_active", "warps active, % of peak"),
+    ("launch__registers_per_thread", "registers per thread"),
+    ("launch__shared_mem_per_block_dynamic", "dynamic shared memory per CTA"),
+    ("launch__grid_size", "CTAs"),
+    ("launch__cluster_size", "cluster size"),
+    ("launch__cluster_max_active", "clusters resident at once (max)"),
+]
+
+
+def ncu_summary(rep: str, key: str, w4: bool = False) -> str:
+    """A markdown summary of one `ncu --set full` report: the kernel, its
+    launch shape, duration, DRAM bytes against the algorithmic bytes of the
+    workload `key`, DRAM / L2 / tensor-pipe utilisation and the top warp
+    stall reasons."""
+    import csv
+    import io
+    out = subprocess.run(["ncu", "-i", rep, "--page", "raw", "--csv"], capture_output=True, text=True,
+                         check=True).stdout
+    rows = list(csv.reader(io.StringIO(out)))
+    head, units, vals = rows[0], rows[1], rows[2]
+    get = {h: (u, v) for h, u, v in zip(head, units, vals)}
+    w = workload_by_name(key)
+    alg = w.bytes if not w4 else w.L * (w.N * w.K // 2 + w.N * w.K // 32 + 2 * w.M * w.K + 2 * w.M * w.N)
+    lines = [f"kernel: `{get.get('Kernel Name', ('', '?'))[1]}`",
+             f"workload: {describe(w)}{' (A16W4 weights)' if w4 else ''}; algorithmic bytes per launch {alg}", "",
+             "| metric | value |", "|---|---|"]
+    for m, label in NCU_SUMMARY_METRICS:
+        if m in get and get[m][1] != "":
+            u, v = get[m]
+            lines.append(f"| {label} (`{m}`) | {v} {u} |")
+    def to_bytes(m):
+        u, v = get.get(m, ("", "0"))
+        f = float(v.replace(",", "") or 0)
+        return f * {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}.get(u, 1)
+    traffic = to_bytes("dram__bytes_read.sum") + to_bytes("dram__bytes_write.sum")
+    lines.append(f"| DRAM traffic / algorithmic bytes | {traffic / alg:.3f} |")
+    stalls = []
+    for h, (u, v) in get.items():
+        if h.startswith("smsp__average_warps_issue_stalled_") and h.endswith("_per_issue_active.ratio"):
+            try:
+                stalls.append((float(v), h[len("smsp__average_warps_issue_stalled_"):-len("_per_issue_active.ratio")]))
+            except ValueError:
+                pass
+    stalls.sort(reverse=True)
+    lines.append("")
+    lines.append("top warp stall reasons (warps stalled per issued instruction): " +
+                 ", ".join(f"{n} {v:.2f}" for v, n in stalls[:5]))
+    return "\n".join(lines)
+
+
 def run_sweep_w4(args):
     """Extra lines for the A16W4 variant (4-bit E2M1 weights with E8M0 scales
     per 32 k, bf16 activations) on the decode shapes: HBM TB/s of the bytes
@@ -921,6 +980,8 @@ def main():
                     help="a short eager run for ncu of one workload, or `all` of them in turn "
                          "(no graphs, one weight copy)")
     ap.add_argument("--w4", action="store_true", help="with --profile-case: the A16W4 kernel")
+    ap.add_argument("--ncu-summary", nargs=2, metavar=("REPORT", "WORKLOAD"), default=None,
+                    help="print a markdown summary of an ncu --set full report of WORKLOAD (with --w4: A16W4)")
     ap.add_argument("--ncu-table", nargs=2, metavar=("CSV", "LOG"), default=None,
                     help="print the DRAM-traffic table from an ncu CSV of a --profile-case run and its log")
     args = ap.parse_args()
@@ -932,7 +993,9 @@ def main():
         workload_by_name(args.workload)
     if args.profile_case not in (None, "all"):
         workload_by_name(args.profile_case)
-    if args.ncu_table:
+    if args.ncu_summary:
+        print(ncu_summary(args.ncu_summary[0], args.ncu_summary[1], args.w4))
+    elif args.ncu_table:
         print(ncu_traffic_table(args.ncu_table[0], args.ncu_table[1], args.steps))
     elif args.cpu_table:
         run_cpu_table(args)
