@@ -649,6 +649,10 @@ __global__ void __launch_bounds__(kThreads, 3)
       }
     } else {
       int round = 0;
+      // A round whose reduction wait failed leaves its barrier phase open:
+      // rank 0 then arms no further round (an arrival on a phase with no
+      // pending arrivals is undefined).
+      bool reduce_ok = true;
       for (int qb = 0; qb < nquads; qb += qr, ++round) {
         const int q_end = (nquads - qb) < qr ? nquads : qb + qr;
         const int c_lo = qb * 4;
@@ -659,7 +663,7 @@ __global__ void __launch_bounds__(kThreads, 3)
         // The aliased mailbox (and any later round) waits for rank 0 to free it.
         const bool need_ready = split > 1 && !(p.mailbox_dedicated && round == 0);
         if (split > 1 && owner) {
-          if (et == 0) {
+          if (et == 0 && reduce_ok) {
             dev::mbar_arrive_expect_tx(bar_reduce, (uint32_t)(split - 1) * (uint32_t)rc * kColumnBytes);
           }
           // One thread per peer, in parallel: a release arrival waits for the
@@ -703,7 +707,9 @@ __global__ void __launch_bounds__(kThreads, 3)
   #pragma unroll
             for (int e = 0; e < 16; ++e) x[e] = __uint_as_float(v[e]);
             if (split > 1) {
-              if (first_group) waiter.wait<true>(bar_reduce, (uint32_t)(round & 1), kRoleEpiReduce, round);
+              if (first_group && reduce_ok) {
+                reduce_ok = waiter.wait<true>(bar_reduce, (uint32_t)(round & 1), kRoleEpiReduce, round);
+              }
               // rank 0's partial + peers 1, 2, ... in rank order; each peer's
               // 16 columns are loaded together.
   #pragma unroll 1

@@ -264,9 +264,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp >= 4) {
     // ---- epilogue: thread et owns TMEM lane et = weight row n0 + et of each tile.
-    // After a failed wait the loop still runs to the end (later waits give up
-    // at once) so that all 128 threads meet every named barrier; the output
-    // is then undefined.
+    // After a failed wait (or once the CTA's failure flag is set) a thread
+    // goes quiet: it arms, waits for and addresses no barrier or mailbox any
+    // more -- re-arming the reduction barrier while its phase is still open
+    // would arrive on a phase with no pending arrivals -- but it still runs
+    // the loop to the end, so that all 128 threads meet every named barrier.
+    // The output is then undefined.
+    bool quiet = false;
     const int et = (int)threadIdx.x - 128;
     const uint32_t t_row = tmem_base + ((uint32_t)((warp & 3) * 32) << 16);
     const int R = kMmaM / split;
@@ -291,17 +295,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (nb + e < p.N) bias8[e] = __uint_as_float((uint32_t)__ldg(bp + e) << 16);
         }
       }
-      waiter.wait<false>(bar_acc_full0 + 8u * buf, (uint32_t)((j >> 1) & 1), kRoleEpiMma, j);
+      if (dev::ld_shared_u32(slot_abort) != 0u) quiet = true;
+      if (!quiet && !waiter.wait<false>(bar_acc_full0 + 8u * buf, (uint32_t)((j >> 1) & 1), kRoleEpiMma, j)) {
+        quiet = true;
+      }
       __syncwarp();
       dev::tc_fence_after();
       if (j == 0 && et == 0) stamp(p, kTrMmaDone);
-      if (et == 0) {
+      if (et == 0 && !quiet) {
         dev::mbar_arrive_expect_tx(bar_reduce, (uint32_t)((split - 1) * ncols * R) * 4u);
         reduce_armed = j & 1;
       }
       // The peers' mailboxes hold tile j - 1 until each peer has read it.
-      bool send = publish;
-      if (j > 0 && send) send = waiter.wait<true>(bar_ready, (uint32_t)((j - 1) & 1), kRoleEpiReady, j);
+      if (j > 0 && publish && !quiet && !waiter.wait<true>(bar_ready, (uint32_t)((j - 1) & 1), kRoleEpiReady, j)) {
+        quiet = true;
+      }
+      const bool send = publish && !quiet;
       // Thread et's value of column c goes to [rank][c][et - dst_rank*R] of
       // the rank that sums row et; a warp's rows of one column are contiguous.
       const uint32_t slot = ((uint32_t)(rank * ncols) * (uint32_t)R + (uint32_t)(et - dst_rank * R)) * 4u;
@@ -325,7 +334,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       dev::tc_fence_before();
       dev::mbar_arrive(bar_acc_empty0 + 8u * buf);
       dev::named_bar_sync(1, kEpiThreads);                  // own slot complete
-      if (waiter.wait<true>(bar_reduce, (uint32_t)(j & 1), kRoleEpiReduce, j) && et == 0) reduce_armed = -1;
+      if (!quiet) {
+        if (waiter.wait<true>(bar_reduce, (uint32_t)(j & 1), kRoleEpiReduce, j)) {
+          if (et == 0) reduce_armed = -1;
+        } else {
+          quiet = true;
+        }
+      }
       // 8 weight rows of one token column per item: sum the sources in rank
       // order, pack bf16 pairs, one 16-byte store.
       const int chunks = R / 8;
@@ -360,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // Every thread has read the mailbox: the peers may publish tile j + 1.
       dev::named_bar_sync(1, kEpiThreads);
-      if (j + 1 < my_tiles && et >= 1 && et < split) {
+      if (j + 1 < my_tiles && et >= 1 && et < split && !quiet) {
         dev::mbar_arrive_remote(dev::mapa(bar_ready, (uint32_t)((rank + et) % split)));
       }
       if (j == my_tiles - 1 && et == 0) stamp(p, kTrStored);
