@@ -226,7 +226,12 @@ SPLITK_API int splitk_gemm_bf16(const void *a, const void *b, void *c,
  *            aligned.  E2M1 code: sign bit 3, exponent bits 2..1 (bias 1),
  *            mantissa bit 0.
  *   a_scale  device, [L][N][K/32] bytes: one E8M0 code (1..252, 2^(x-127))
- *            per 32 consecutive k of a row, 4-byte aligned.
+ *            per 32 consecutive k of a row, 4-byte aligned.  Codes outside
+ *            1..252 are outside the contract and decode as follows: 0 as a
+ *            zero scale (the format's value, 2^-127, is not applied), 253
+ *            and 254 as 2^126 and 2^127 (weights past bf16's largest finite
+ *            value become +-Inf), 255 (not a number in the format) as +Inf
+ *            (a zero weight times it is NaN).
  *   b, c     as splitk_gemm_bf16().
  * K must be a multiple of 128, M at most 32, and a CTA's K slice at most 8
  * tiles of 128 (else SPLITK_ERR_INVALID_SHAPE / SPLITK_ERR_NO_FIT).  The

@@ -95,12 +95,16 @@ uint32_t w4_mailbox_bytes(int split, int reduce_scatter, int ncols_max) {
 // reserves 1 KiB of the SM's shared memory).
 int resident_by_smem(size_t smem_per_sm, size_t smem) { return (int)(smem_per_sm / (smem + 1024)); }
 
+// Token columns one reduction round of a persistent plan moves: all of a
+// tile's, or `quads` 4-column groups.
+int persistent_round_cols(int ncols_max, int quads) { return std::min(ncols_max, 4 * quads); }
+
 // Shared memory of a persistent plan: the ring (a weight and an activation K
-// tile per stage), the scattered mailbox of min(M, mma_n) token columns and
-// the barriers.
-size_t smem_bytes_persistent(int mma_n, int stages, int ncols_max) {
+// tile per stage), the scattered mailbox of one reduction round's token
+// columns and the barriers.
+size_t smem_bytes_persistent(int mma_n, int stages, int round_cols) {
   return (size_t)kAlignSlack + (size_t)stages * (kAStageBytes + b_stage_bytes(mma_n)) +
-         (size_t)ncols_max * kColumnBytes + kBarRegionBytes;
+         (size_t)round_cols * kColumnBytes + kBarRegionBytes;
 }
 
 // 128-wide K tiles covering K; the last one may be ragged (TMA reads zeros
@@ -176,23 +180,38 @@ bool stage_for_decode(splitk_plan_t* out, int ncols_max, long long ctas, int num
 }
 
 // The persistent plan for a shape and a split of 2 or more: one CTA per SM
-// with the deepest ring (2 to 8 stages, or exactly `stages` when that is
-// given) that fits beside the scattered mailbox, two accumulators in TMEM,
-// and one cluster per `split` SMs (at most one per output tile).
-bool persistent_plan(int M, int N, int K, int L, int split, int stages, int num_sms, size_t smem_per_sm,
-                     size_t smem_optin, splitk_plan_t* out) {
+// with the deepest ring (2 to 8 stages) that fits beside the scattered
+// mailbox, the mailbox holding a whole tile's columns or, when a smaller one
+// leaves room for a deeper ring, reduction rounds of 16, 8 or 4 4-column
+// groups; two accumulators in TMEM; one cluster per `split` SMs (at most one
+// per output tile).  Nonzero `stages` / `quads` fix the ring depth / round.
+bool persistent_plan(int M, int N, int K, int L, int split, int stages, int quads, int num_sms,
+                     size_t smem_per_sm, size_t smem_optin, splitk_plan_t* out) {
   if (split < 2 || !valid_split(split)) return false;
   const int T = total_k_tiles(K);
   if (T < split) return false;
   const int mma_n = choose_mma_n(M);
   const int ncols_max = std::min(M, mma_n);
+  const int nquads_max = (ncols_max + 3) / 4;
   const size_t budget = std::min(smem_optin, smem_per_sm - 1024);
-  int st = stages;
-  if (st == 0) {
-    for (st = kMaxStages; st > 2 && smem_bytes_persistent(mma_n, st, ncols_max) > budget; --st) {
+  auto deepest = [&](int qr) {
+    int st = kMaxStages;
+    while (st > 2 && smem_bytes_persistent(mma_n, st, persistent_round_cols(ncols_max, qr)) > budget) --st;
+    return st;
+  };
+  int qr = quads;
+  if (qr == 0) {
+    // one round a tile unless fewer columns a round buy a deeper ring
+    qr = nquads_max;
+    for (int q : {16, 8, 4}) {
+      if (q < nquads_max && (stages == 0 ? deepest(q) > deepest(qr) : false)) qr = q;
     }
   }
-  if (st < 2 || st > kMaxStages || smem_bytes_persistent(mma_n, st, ncols_max) > budget) return false;
+  if (qr < 1 || qr > mma_n / 4 || (qr % 4 != 0 && qr < nquads_max)) return false;
+  qr = std::min(qr, nquads_max);
+  const int round_cols = persistent_round_cols(ncols_max, qr);
+  const int st = stages != 0 ? stages : deepest(qr);
+  if (st < 2 || st > kMaxStages || smem_bytes_persistent(mma_n, st, round_cols) > budget) return false;
   const long long tiles = tiles_of(M, mma_n) * tiles_of(N, kMmaM) * L;
   const long long clusters = std::max<long long>(1, std::min<long long>(tiles, num_sms / split));
   std::memset(out, 0, sizeof(*out));
@@ -202,15 +221,15 @@ bool persistent_plan(int M, int N, int K, int L, int split, int stages, int num_
   out->split_k = split;
   out->k_tiles_per_cta = (T + split - 1) / split;
   out->mailbox_dedicated = 1;
-  out->mailbox_quads = (ncols_max + 3) / 4;
-  out->reduce_rounds = 1;
+  out->mailbox_quads = qr;
+  out->reduce_rounds = (nquads_max + qr - 1) / qr;
   out->grid[0] = (unsigned)split;
   out->grid[1] = (unsigned)std::min<long long>(clusters, 65535);
   out->grid[2] = 1;
   out->cluster[0] = (unsigned)split;
   out->cluster[1] = 1;
   out->cluster[2] = 1;
-  out->smem_bytes = smem_bytes_persistent(mma_n, st, ncols_max);
+  out->smem_bytes = smem_bytes_persistent(mma_n, st, round_cols);
   out->ctas_per_sm = 1;
   out->reduce_scatter = 1;
   out->mma_issuers = 1;
@@ -223,17 +242,26 @@ bool persistent_plan(int M, int N, int K, int L, int split, int stages, int num_
 int plan_ring_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t smem_per_sm,
                    size_t smem_optin, splitk_plan_t* out);
 
-// The plan: the per-tile kernel's (plan_ring_impl), or, for wide tiles
-// (mma_n >= 64) at splits of 4 and 8 whose grid exceeds one CTA per SM, the
-// persistent kernel, whose reduction overlaps the next tile's stream.
+// The plan: the per-tile kernel's (plan_ring_impl), or the persistent kernel,
+// whose reduction overlaps the next tile's stream, where that measured
+// faster on GB300 (the K = 16384 sweep, back to back, the same box): split 8
+// at every tile width (M = 1..16: 0.82-0.95 -> 0.97-0.99 of the HBM copy
+// bandwidth; M = 64: 0.55 -> 0.87), and split 4 for tiles of 64 and 128
+// tokens (M = 64: 0.80 -> 0.82; the wide projection 0.68 -> 0.88), when the
+// grid exceeds one CTA per SM and the output tiles deal out evenly (at least
+// 90 %) over one cluster per `split` SMs.
 int plan_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t smem_per_sm,
               size_t smem_optin, splitk_plan_t* out) {
   const int rc = plan_ring_impl(M, N, K, L, split_k, num_sms, smem_per_sm, smem_optin, out);
   if (rc != SPLITK_OK) return rc;
+  const int split = out->split_k;
   const long long tiles = tiles_of(M, out->mma_n) * tiles_of(N, kMmaM) * L;
-  if (out->split_k >= 4 && out->mma_n >= 64 && tiles * out->split_k > num_sms) {
+  const long long clusters = std::max(1, num_sms / split);
+  const long long rounds = (tiles + clusters - 1) / clusters;
+  const bool balanced = (double)tiles >= 0.9 * (double)(rounds * clusters);
+  if ((split == 8 || (split == 4 && out->mma_n >= 64)) && tiles * split > num_sms && balanced) {
     splitk_plan_t p;
-    if (persistent_plan(M, N, K, L, out->split_k, 0, num_sms, smem_per_sm, smem_optin, &p)) *out = p;
+    if (persistent_plan(M, N, K, L, split, 0, 0, num_sms, smem_per_sm, smem_optin, &p)) *out = p;
   }
   return SPLITK_OK;
 }
@@ -540,17 +568,24 @@ int check_plan_persistent(const splitk_plan_t& pl, int M, int N, int K, int L, s
     return SPLITK_ERR_BAD_PLAN;
   }
   const int ncols_max = std::min(M, pl.mma_n);
-  if (pl.reduce_scatter != 1 || pl.mailbox_dedicated != 1 || pl.mailbox_quads != (ncols_max + 3) / 4 ||
-      pl.b_resident != 0 || pl.a_tmem_tiles != 0 || pl.mma_issuers != 1 || pl.b_loader != 0 ||
-      pl.l2_prefetch != 0 || pl.pdl_trigger != 0 || pl.reserved != 0) {
+  const int nquads_max = (ncols_max + 3) / 4;
+  // rounds of whole 16-column groups (or all of a tile's columns at once)
+  if (pl.mailbox_quads < 1 || pl.mailbox_quads > nquads_max ||
+      (pl.mailbox_quads % 4 != 0 && pl.mailbox_quads != nquads_max) ||
+      pl.reduce_rounds != (nquads_max + pl.mailbox_quads - 1) / pl.mailbox_quads) {
+    return SPLITK_ERR_BAD_PLAN;
+  }
+  if (pl.reduce_scatter != 1 || pl.mailbox_dedicated != 1 || pl.b_resident != 0 || pl.a_tmem_tiles != 0 ||
+      pl.mma_issuers != 1 || pl.b_loader != 0 || pl.l2_prefetch != 0 || pl.pdl_trigger != 0 || pl.reserved != 0) {
     return SPLITK_ERR_BAD_PLAN;
   }
   if (pl.tmem_cols != pow2_at_least(2u * tmem_acc_cols(pl.mma_n))) return SPLITK_ERR_BAD_PLAN;
-  const size_t smem = smem_bytes_persistent(pl.mma_n, pl.stages, ncols_max);
+  const int round_cols = persistent_round_cols(ncols_max, pl.mailbox_quads);
+  const size_t smem = smem_bytes_persistent(pl.mma_n, pl.stages, round_cols);
   if (smem != pl.smem_bytes) return SPLITK_ERR_BAD_PLAN;
   if (smem > smem_optin) return SPLITK_ERR_NO_FIT;
   if ((size_t)resident_by_smem(smem_per_sm, smem) * pl.tmem_cols > 512u) return SPLITK_ERR_BAD_PLAN;
-  *dedicated_bytes = (uint32_t)ncols_max * kColumnBytes;
+  *dedicated_bytes = (uint32_t)round_cols * kColumnBytes;
   return SPLITK_OK;
 }
 
@@ -1051,17 +1086,20 @@ int enumerate_plans(int M, int N, int K, int L, int split_k, int num_sms, size_t
         }
       }
     }
-    // the persistent kernel at every ring depth that fits
+    // the persistent kernel at every ring depth and reduction round that fit
     for (int stages = 2; split >= 2 && stages <= kMaxStages; ++stages) {
-      splitk_plan_t p;
-      uint32_t ded_check = 0;
-      if (!persistent_plan(M, N, K, L, split, stages, num_sms, smem_per_sm, smem_optin, &p) ||
-          check_plan(p, M, N, K, L, smem_optin, smem_per_sm, &ded_check) != SPLITK_OK) {
-        continue;
+      for (int quads : {nquads_max, 16, 8, 4}) {
+        if (quads > nquads_max || (quads != nquads_max && quads % 4 != 0)) continue;
+        splitk_plan_t p;
+        uint32_t ded_check = 0;
+        if (!persistent_plan(M, N, K, L, split, stages, quads, num_sms, smem_per_sm, smem_optin, &p) ||
+            check_plan(p, M, N, K, L, smem_optin, smem_per_sm, &ded_check) != SPLITK_OK) {
+          continue;
+        }
+        bool dup = false;
+        for (const auto& q : *out) dup = dup || same(p, q);
+        if (!dup) out->push_back(p);
       }
-      bool dup = false;
-      for (const auto& q : *out) dup = dup || same(p, q);
-      if (!dup) out->push_back(p);
     }
   }
   return SPLITK_OK;

@@ -17,9 +17,11 @@
 // reduce_scatter mode -- rank r sums weight rows [r*R, (r+1)*R), R = 128 /
 // split, over source ranks 0, 1, ..., split-1 in that order (the same FP32
 // additions as rank 0 makes in the gathered mode, so the same bits).  Each
-// rank has one mailbox [source][column][R rows]; before publishing tile
-// j + 1 into a peer's mailbox a rank waits until every peer has signalled
-// (a remote mbarrier arrival) that it has read its mailbox of tile j.
+// rank has one mailbox [source][column][R rows] holding the columns of one
+// reduction round (a whole tile, or a group of its columns when the mailbox
+// is smaller); before publishing a round into a peer's mailbox a rank waits
+// until every peer has signalled (a remote mbarrier arrival) that it has
+// read its mailbox of the previous round.
 //
 // CTA roles (256 threads):
 //   warp 0      weight producer: TMA, L2 evict_first, the first ring pass
@@ -264,6 +266,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp >= 4) {
     // ---- epilogue: thread et owns TMEM lane et = weight row n0 + et of each tile.
+    // A tile is reduced in rounds of p.mailbox_quads 4-column groups (one
+    // round when the mailbox holds all of a tile's columns): each round the
+    // ranks publish those columns, sum and store them, and signal the peers
+    // that the mailbox is free for the next round (of this tile or the next).
     // After a failed wait (or once the CTA's failure flag is set) a thread
     // goes quiet: it arms, waits for and addresses no barrier or mailbox any
     // more -- re-arming the reduction barrier while its phase is still open
@@ -276,15 +282,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int R = kMmaM / split;
     const int my_lo = rank * R;
     const int dst_rank = et / R;
+    const int qr = p.mailbox_quads;                          // 4-column groups per round
     const bool publish = !(p.inject & kInjectSkipPublish);
     float* const mb = reinterpret_cast<float*>(smem_raw + (sMail - raw));
     const uint32_t r_bar = dev::mapa(bar_reduce, (uint32_t)dst_rank);
     const uint32_t r_mail0 = dev::mapa(sMail, (uint32_t)dst_rank);
+    int gr = 0;                                              // reduction rounds so far (all tiles)
     for (int j = 0; j < my_tiles; ++j) {
       const int buf = j & 1;
       int n0, m0, l;
       tile_coords(j, &n0, &m0, &l);
       const int ncols = (p.M - m0) < MMA_N ? (p.M - m0) : MMA_N;
+      const int nquads = (ncols + 3) >> 2;
       // the bias of the 8 weight rows this thread will store
       float bias8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       if (p.bias != nullptr) {
@@ -302,81 +311,92 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       dev::tc_fence_after();
       if (j == 0 && et == 0) stamp(p, kTrMmaDone);
-      if (et == 0 && !quiet) {
-        dev::mbar_arrive_expect_tx(bar_reduce, (uint32_t)((split - 1) * ncols * R) * 4u);
-        reduce_armed = j & 1;
-      }
-      // The peers' mailboxes hold tile j - 1 until each peer has read it.
-      if (j > 0 && publish && !quiet && !waiter.wait<true>(bar_ready, (uint32_t)((j - 1) & 1), kRoleEpiReady, j)) {
-        quiet = true;
-      }
-      const bool send = publish && !quiet;
-      // Thread et's value of column c goes to [rank][c][et - dst_rank*R] of
-      // the rank that sums row et; a warp's rows of one column are contiguous.
-      const uint32_t slot = ((uint32_t)(rank * ncols) * (uint32_t)R + (uint32_t)(et - dst_rank * R)) * 4u;
-#pragma unroll 1
-      for (int g = 0; g * 16 < ncols; ++g) {
-        uint32_t v[16];
-        __syncwarp();   // tcgen05.ld is warp-collective
-        load_acc16(t_row + (uint32_t)buf * kAccCols + (uint32_t)(g * 16), 0u, false, v);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int col = g * 16 + e;
-          if (col >= ncols) break;                            // warp-uniform
-          if (dst_rank == rank) {
-            *reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(mb) + slot + (size_t)col * R * 4) = v[e];
-          } else if (send) {
-            dev::st_async_b32(r_mail0 + slot + (uint32_t)(col * R) * 4u, v[e], r_bar);
-          }
+      for (int qb = 0; qb < nquads; qb += qr, ++gr) {
+        const int c_lo = qb * 4;
+        const int c_hi = ncols < (qb + qr) * 4 ? ncols : (qb + qr) * 4;
+        const int rc = c_hi - c_lo;
+        const bool last_round_of_tile = qb + qr >= nquads;
+        if (et == 0 && !quiet) {
+          dev::mbar_arrive_expect_tx(bar_reduce, (uint32_t)((split - 1) * rc * R) * 4u);
+          reduce_armed = gr & 1;
         }
-      }
-      // this buffer's TMEM reads are done: the MMAs of tile j + 2 may use it
-      dev::tc_fence_before();
-      dev::mbar_arrive(bar_acc_empty0 + 8u * buf);
-      dev::named_bar_sync(1, kEpiThreads);                  // own slot complete
-      if (!quiet) {
-        if (waiter.wait<true>(bar_reduce, (uint32_t)(j & 1), kRoleEpiReduce, j)) {
-          if (et == 0) reduce_armed = -1;
-        } else {
+        // The peers' mailboxes hold the previous round until each peer has read it.
+        if (gr > 0 && publish && !quiet &&
+            !waiter.wait<true>(bar_ready, (uint32_t)((gr - 1) & 1), kRoleEpiReady, gr)) {
           quiet = true;
         }
-      }
-      // 8 weight rows of one token column per item: sum the sources in rank
-      // order, pack bf16 pairs, one 16-byte store.
-      const int chunks = R / 8;
-      const int items = ncols * chunks;
+        const bool send = publish && !quiet;
+        // Thread et's value of column c goes to [rank][c - c_lo][et - dst_rank*R]
+        // of the rank that sums row et; a warp's rows of one column are contiguous.
+        const uint32_t slot = ((uint32_t)(rank * rc) * (uint32_t)R + (uint32_t)(et - dst_rank * R)) * 4u;
 #pragma unroll 1
-      for (int it = et; it < items; it += kEpiThreads) {
-        const int m = it / chunks;
-        const int c8 = (it - m * chunks) * 8;
-        const float* src = mb + (size_t)m * R + c8;
-        float4 x = *reinterpret_cast<const float4*>(src);
-        float4 y = *reinterpret_cast<const float4*>(src + 4);
+        for (int g = c_lo >> 4; g * 16 < c_hi; ++g) {
+          uint32_t v[16];
+          __syncwarp();   // tcgen05.ld is warp-collective
+          load_acc16(t_row + (uint32_t)buf * kAccCols + (uint32_t)(g * 16), 0u, false, v);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int col = g * 16 + e;
+            if (col < c_lo || col >= c_hi) continue;             // warp-uniform
+            const uint32_t off = slot + (uint32_t)((col - c_lo) * R) * 4u;
+            if (dst_rank == rank) {
+              *reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(mb) + off) = v[e];
+            } else if (send) {
+              dev::st_async_b32(r_mail0 + off, v[e], r_bar);
+            }
+          }
+        }
+        if (last_round_of_tile) {
+          // this buffer's TMEM reads are done: the MMAs of tile j + 2 may use it
+          dev::tc_fence_before();
+          dev::mbar_arrive(bar_acc_empty0 + 8u * buf);
+        }
+        dev::named_bar_sync(1, kEpiThreads);                // own slot complete
+        if (!quiet) {
+          if (waiter.wait<true>(bar_reduce, (uint32_t)(gr & 1), kRoleEpiReduce, gr)) {
+            if (et == 0) reduce_armed = -1;
+          } else {
+            quiet = true;
+          }
+        }
+        // 8 weight rows of one token column per item: sum the sources in rank
+        // order, pack bf16 pairs, one 16-byte store.
+        const int chunks = R / 8;
+        const int items = rc * chunks;
 #pragma unroll 1
-        for (int sr = 1; sr < split; ++sr) {
-          const float* ps = src + (size_t)sr * ncols * R;
-          const float4 a4 = *reinterpret_cast<const float4*>(ps);
-          const float4 b4 = *reinterpret_cast<const float4*>(ps + 4);
-          x.x += a4.x; x.y += a4.y; x.z += a4.z; x.w += a4.w;
-          y.x += b4.x; y.y += b4.y; y.z += b4.z; y.w += b4.w;
+        for (int it = et; it < items; it += kEpiThreads) {
+          const int mc = it / chunks;
+          const int c8 = (it - mc * chunks) * 8;
+          const float* src = mb + (size_t)mc * R + c8;
+          float4 x = *reinterpret_cast<const float4*>(src);
+          float4 y = *reinterpret_cast<const float4*>(src + 4);
+#pragma unroll 1
+          for (int sr = 1; sr < split; ++sr) {
+            const float* ps = src + (size_t)sr * rc * R;
+            const float4 a4 = *reinterpret_cast<const float4*>(ps);
+            const float4 b4 = *reinterpret_cast<const float4*>(ps + 4);
+            x.x += a4.x; x.y += a4.y; x.z += a4.z; x.w += a4.w;
+            y.x += b4.x; y.y += b4.y; y.z += b4.z; y.w += b4.w;
+          }
+          const int n = n0 + my_lo + c8;
+          if (n >= p.N) continue;
+          x.x += bias8[0]; x.y += bias8[1]; x.z += bias8[2]; x.w += bias8[3];
+          y.x += bias8[4]; y.y += bias8[5]; y.z += bias8[6]; y.w += bias8[7];
+          const uint32_t q0 = dev::pack_bf16x2(x.x, x.y), q1 = dev::pack_bf16x2(x.z, x.w);
+          const uint32_t q2 = dev::pack_bf16x2(y.x, y.y), q3 = dev::pack_bf16x2(y.z, y.w);
+          uint16_t* dst = p.c + ((size_t)((size_t)l * p.M + (size_t)(m0 + c_lo + mc)) * (size_t)p.N + (size_t)n);
+          if (p.vec_store && n + 8 <= p.N) {
+            dev::st_global_v4(dst, q0, q1, q2, q3);
+          } else {
+            store8_clipped(dst, n, p.N, q0, q1, q2, q3);
+          }
         }
-        const int n = n0 + my_lo + c8;
-        if (n >= p.N) continue;
-        x.x += bias8[0]; x.y += bias8[1]; x.z += bias8[2]; x.w += bias8[3];
-        y.x += bias8[4]; y.y += bias8[5]; y.z += bias8[6]; y.w += bias8[7];
-        const uint32_t q0 = dev::pack_bf16x2(x.x, x.y), q1 = dev::pack_bf16x2(x.z, x.w);
-        const uint32_t q2 = dev::pack_bf16x2(y.x, y.y), q3 = dev::pack_bf16x2(y.z, y.w);
-        uint16_t* dst = p.c + ((size_t)((size_t)l * p.M + (size_t)(m0 + m)) * (size_t)p.N + (size_t)n);
-        if (p.vec_store && n + 8 <= p.N) {
-          dev::st_global_v4(dst, q0, q1, q2, q3);
-        } else {
-          store8_clipped(dst, n, p.N, q0, q1, q2, q3);
+        // Every thread has read the mailbox: the peers may publish the next round.
+        dev::named_bar_sync(1, kEpiThreads);
+        const bool more = !(j == my_tiles - 1 && last_round_of_tile);
+        if (more && et >= 1 && et < split && !quiet) {
+          dev::mbar_arrive_remote(dev::mapa(bar_ready, (uint32_t)((rank + et) % split)));
         }
-      }
-      // Every thread has read the mailbox: the peers may publish tile j + 1.
-      dev::named_bar_sync(1, kEpiThreads);
-      if (j + 1 < my_tiles && et >= 1 && et < split && !quiet) {
-        dev::mbar_arrive_remote(dev::mapa(bar_ready, (uint32_t)((rank + et) % split)));
       }
       if (j == my_tiles - 1 && et == 0) stamp(p, kTrStored);
     }

@@ -125,6 +125,13 @@ def _plan(M, N, K, L=1, split=0):
     return sk.splitk_plan_for(M, N, K, L, split, **GB300)
 
 
+def _per_tile(M, N, K, L=1, split=0):
+    """The per-tile kernel's own choice (the second candidate when the plan
+    is persistent)."""
+    c = sk.splitk_plan_candidates_for(M, N, K, L, split, **GB300)
+    return c[1] if c[0].persistent else c[0]
+
+
 def test_plan_of_the_decode_workloads():
     p = _plan(1, 7168, 2048, 1, 4)
     assert (p.mma_m, p.mma_n, p.split_k, p.k_tiles_per_cta) == (128, 16, 4, 4)
@@ -137,6 +144,11 @@ def test_plan_of_the_decode_workloads():
     assert (p.mma_n, list(p.grid)) == (64, [2, 144, 1])
     p = _plan(128, 7168, 16384, 2, 8)              # persistent: 152 SMs / 8 = 19 clusters
     assert (p.mma_n, list(p.grid), p.k_tiles_per_cta, p.persistent) == (128, [8, 19, 1], 16, 1)
+    assert (p.stages, p.mailbox_quads, p.reduce_rounds) == (3, 16, 2)   # two rounds buy a third stage
+    assert _plan(16, 4096, 7168, 1, 8).persistent == 0   # 32 tiles deal out unevenly over 19 clusters
+    assert _plan(16, 7168, 16384, 2, 8).persistent == 1
+    assert _plan(16, 7168, 16384, 2, 4).persistent == 0  # narrow tiles at split 4: the per-tile kernel
+    assert _plan(64, 7168, 16384, 2, 4).persistent == 1
     assert p.reduce_rounds >= 1 and p.mailbox_quads % 4 == 0
 
 
@@ -196,14 +208,21 @@ def _check_persistent(p, M, N, K, L, split):
     assert split >= 2 and p.split_k == split
     assert list(p.grid) == [split, max(1, min(tiles, GB300["num_sms"] // split)), 1]
     assert list(p.cluster) == [split, 1, 1]
-    assert (p.reduce_scatter, p.mailbox_dedicated, p.reduce_rounds, p.b_resident, p.a_tmem_tiles,
-            p.mma_issuers, p.b_loader, p.l2_prefetch, p.ctas_per_sm) == (1, 1, 1, 0, 0, 1, 0, 0, 1)
+    assert (p.reduce_scatter, p.mailbox_dedicated, p.b_resident, p.a_tmem_tiles,
+            p.mma_issuers, p.b_loader, p.l2_prefetch, p.ctas_per_sm) == (1, 1, 0, 0, 1, 0, 0, 1)
     assert p.tmem_cols == next(c for c in (32, 64, 128, 256, 512) if c >= 2 * max(32, p.mma_n))
     assert 2 <= p.stages <= 8
-    assert p.smem_bytes == 1024 + p.stages * (32768 + p.mma_n * 256) + min(M, p.mma_n) * 512 + 256
-    assert p.smem_bytes <= min(GB300["smem_per_block_optin"], GB300["smem_per_sm"] - 1024)
+    nquads = -(-min(M, p.mma_n) // 4)
+    assert p.mailbox_quads == nquads or (p.mailbox_quads % 4 == 0 and p.mailbox_quads < nquads)
+    assert p.reduce_rounds == -(-nquads // p.mailbox_quads)
+    round_cols = min(min(M, p.mma_n), 4 * p.mailbox_quads)
+    budget = min(GB300["smem_per_block_optin"], GB300["smem_per_sm"] - 1024)
+    assert p.smem_bytes == 1024 + p.stages * (32768 + p.mma_n * 256) + round_cols * 512 + 256
+    assert p.smem_bytes <= budget
     if p.stages < 8:   # the deepest ring that fits
-        assert p.smem_bytes + 32768 + p.mma_n * 256 > min(GB300["smem_per_block_optin"], GB300["smem_per_sm"] - 1024)
+        assert p.smem_bytes + 32768 + p.mma_n * 256 > budget
+    if p.reduce_rounds > 1:   # rounds only where they buy a deeper ring than one round a tile
+        assert 1024 + p.stages * (32768 + p.mma_n * 256) + min(M, p.mma_n) * 512 + 256 > budget
 
 
 @pytest.mark.parametrize("M", [1, 4, 16, 17, 32, 33, 64, 65, 128, 129, 1000])
@@ -379,21 +398,21 @@ def test_long_k_slices_prefer_a_deeper_ring_over_their_own_mailbox():
     when the aliased partials would need more than one reduction round, and
     not on short slices."""
     for M, split in ((8, 2), (16, 2), (16, 4)):
-        p = _plan(M, 7168, 16384, 2, split)
+        p = _per_tile(M, 7168, 16384, 2, split)
         assert (p.stages, p.mailbox_dedicated, p.reduce_scatter, p.reduce_rounds, p.ctas_per_sm) == (3, 0, 0, 1, 2)
         assert _check(p, M, 7168, 16384, 2) == 0
-    p = _plan(128, 7168, 16384, 2, 4)                   # 96 KB of partials: keep the scattered mailbox
+    p = _per_tile(128, 7168, 16384, 2, 4)                   # 96 KB of partials: keep the scattered mailbox
     assert (p.stages, p.reduce_scatter) == (2, 1)
-    p = _plan(8, 7168, 16384, 2, 8)                     # 16 K tiles a CTA
+    p = _per_tile(8, 7168, 16384, 2, 8)                     # 16 K tiles a CTA
     assert (p.stages, p.mailbox_dedicated) == (3, 0)
     # a few token columns: the scattered mailbox when the dedicated one does
     # not fit beside the third stage; a single column keeps the dedicated one
     for M in (2, 4):
-        p = _plan(M, 7168, 16384, 2, 8)
+        p = _per_tile(M, 7168, 16384, 2, 8)
         assert (p.stages, p.mailbox_dedicated, p.reduce_scatter, p.ctas_per_sm) == (3, 1, 1, 2)
-    p = _plan(1, 7168, 16384, 2, 8)
+    p = _per_tile(1, 7168, 16384, 2, 8)
     assert (p.stages, p.mailbox_dedicated, p.reduce_scatter) == (3, 1, 0)
-    p = _plan(8, 7168, 2048, 4, 2)                      # 8 K tiles a CTA: the dedicated mailbox stays
+    p = _per_tile(8, 7168, 2048, 4, 2)                      # 8 K tiles a CTA: the dedicated mailbox stays
     assert (p.stages, p.mailbox_dedicated) == (2, 1)
 
 

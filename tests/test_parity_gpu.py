@@ -642,14 +642,15 @@ def test_w4a16_the_largest_grid_dimensions_index_correctly(L, N):
 
 
 # ---------------------------------------------------------------- persistent plans
-def _persistent(M, N, K, L, split, clusters=None, stages=None):
+def _persistent(M, N, K, L, split, clusters=None, stages=None, quads=None):
     """The persistent plan of the shape at `split` (the deepest ring unless
-    `stages` is given), with `clusters` as its grid bound if given."""
+    `stages` is given, reduction rounds of `quads` 4-column groups if given),
+    with `clusters` as its grid bound if given."""
     props = torch.cuda.get_device_properties(DEV)
     cands = sk.splitk_plan_candidates_for(M, N, K, L, split, props.multi_processor_count,
                                           props.shared_memory_per_multiprocessor,
                                           props.shared_memory_per_block_optin)
-    ps = [p for p in cands if p.persistent]
+    ps = [p for p in cands if p.persistent and (quads is None or p.mailbox_quads == quads)]
     assert ps, "no persistent candidate"
     p = max(ps, key=lambda q: q.stages) if stages is None else next(q for q in ps if q.stages == stages)
     p = sk.Plan.from_buffer_copy(p)
@@ -698,6 +699,21 @@ def test_persistent_kernel_equals_the_scattered_per_tile_kernel_bit_for_bit(M, s
         assert np.array_equal(gemm_gpu(a, b, plan=p), want), (stages, clusters)
 
 
+@pytest.mark.parametrize("M,quads", [(100, 4), (128, 16), (64, 8), (37, 4)])
+def test_persistent_reduction_rounds(M, quads):
+    """A tile reduced in rounds of a few 4-column groups through a smaller
+    mailbox (the last round ragged when M is): the same bits as one round a
+    tile, and the oracle's values."""
+    L, N, K, split = 2, 520, 2048, 4
+    a, b = _draw(L, M, N, K, seed=3000 + M)
+    p = _persistent(M, N, K, L, split, clusters=3, quads=quads)
+    assert p.reduce_rounds > 1
+    c = gemm_gpu(a, b, plan=p)
+    one = _persistent(M, N, K, L, split, clusters=3, quads=-(-min(M, p.mma_n) // 4), stages=2)
+    assert np.array_equal(c, gemm_gpu(a, b, plan=one))
+    assert_parity(c, oracle_full(a, b), a, b, K)
+
+
 def test_persistent_kernel_closed_forms_and_bias():
     """All-ones inputs give C = K exactly; the bias is added before the one
     rounding, as by the oracle."""
@@ -715,3 +731,37 @@ def test_persistent_kernel_closed_forms_and_bias():
     torch.cuda.synchronize()
     assert sk.splitk_get_status() == 0
     assert_parity(to_host(tc), oracle.gemm_bias(a, b, bias), a, b, K)
+
+
+def test_w4a16_scale_codes_outside_the_contract_decode_as_documented():
+    """Scale codes 0, 253, 254 and 255 (outside the documented 1..252): a
+    block of 32 k with that code, every activation of the block 2^-10 and
+    the rest zero, so C[n] = 32 * 2^-10 * w decoded.  Code 0 decodes as a
+    zero scale, 253 and 254 as 2^126 and 2^127 (decoded weights past bf16's
+    largest finite value are +-Inf), 255 as +Inf (NaN for the zero code)."""
+    L, M, N, K = 1, 1, 256, 1024
+    aq = np.zeros((L, N, K // 2), np.uint8)
+    for n in range(N):                         # row n: every k holds e2m1 code n % 16
+        aq[0, n, :] = (n % 16) * 0x11
+    e2m1 = np.array([0, .5, 1, 1.5, 2, 3, 4, 6, -0., -.5, -1, -1.5, -2, -3, -4, -6])
+    b = np.zeros((L, M, K), np.uint16)
+    b[0, 0, 32:64] = 0x3A80                    # 2^-10 on block 1
+    for code in (0, 253, 254, 255):
+        a_s = np.full((L, N, K // 32), 127, np.uint8)
+        a_s[0, :, 1] = code
+        c = to_host(sk.splitk_gemm_w4a16(_u8_dev(aq), _u8_dev(a_s), to_dev(b), split_k=2))
+        torch.cuda.synchronize()
+        assert sk.splitk_get_status() == 0
+        got = (c.astype(np.uint32) << 16).view(np.float32)[0, 0].astype(np.float64)
+        for n in range(N):
+            w = e2m1[n % 16]
+            if code == 0:
+                assert got[n] == 0.0, (code, n)
+                continue
+            dec = w * np.inf if code == 255 else w * 2.0 ** (code - 127)
+            if np.isfinite(dec) and abs(dec) >= 2.0 ** 128:
+                dec = np.copysign(np.inf, w)
+            if w == 0 and code == 255:
+                assert np.isnan(got[n]), (code, n)
+            else:
+                assert got[n] == dec * 32 * 2.0 ** -10, (code, n, got[n], dec)
