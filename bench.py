@@ -839,7 +839,7 @@ def run_sweep_w4(args):
         return statistics.median(per) / n * 1e-3
 
     for w in (W.DECODE_M1, W.DECODE_M16, W.TINY, W.DECODE_M1.with_(M=8), W.DECODE_M1.with_(M=32),
-              W.DECODE_M1.with_(L=8), W.DECODE_M16.with_(L=4)):
+              W.DECODE_M1.with_(L=8), W.DECODE_M16.with_(L=4), W.DECODE_M1.with_(split_k=8)):
         aq, a_s = synthetic.w4_weights(w.L, w.N, w.K, w.seed)
         q0 = torch.from_numpy(aq).to(dev)
         s0 = torch.from_numpy(a_s).to(dev)
@@ -850,6 +850,13 @@ def run_sweep_w4(args):
         b = to_dev(w.make_b(), dev)
         c = torch.empty((w.L, w.M, w.N), dtype=torch.bfloat16, device=dev)
         t4 = timed(lambda i, st: sk.splitk_gemm_w4a16(Qs[i], Ss[i], b, c, split_k=w.split_k, stream=st), R)
+        # the other decoder count, for comparison
+        p_alt = sk.splitk_plan_w4a16(w.M, w.N, w.K, w.L, w.split_k)
+        p_alt.w4_decoders = 3 - p_alt.w4_decoders
+        try:
+            t4_alt = timed(lambda i, st: sk.splitk_gemm_w4a16_planned(Qs[i], Ss[i], b, c, p_alt, 0, st), R)
+        except sk.SplitKError:
+            t4_alt = None
         a0 = to_dev(w.make_a(), dev)
         Rb = max(2, min(20, math.ceil(4 * l2 / (a0.numel() * 2))))
         As = [a0] + [a0.clone() for _ in range(Rb - 1)]
@@ -859,10 +866,11 @@ def run_sweep_w4(args):
                           "TB/s": round(w4_bytes / t4 / 1e12, 3), "bytes_per_call": w4_bytes,
                           "hbm_frac": round(w4_bytes / t4 / 1e9 / hbm, 3), "peak_source": src,
                           "bf16_us": round(tb * 1e6, 2), "speedup_vs_bf16": round(tb / t4, 3),
+                          f"us_with_{p_alt.w4_decoders}_decoders": round(t4_alt * 1e6, 2) if t4_alt else None,
                           "plan": {k: v for k, v in p.as_dict().items()
                                    if k in ("mma_n", "split_k", "stages", "a_tmem_tiles", "smem_bytes",
                                             "ctas_per_sm", "reduce_scatter", "b_loader", "mma_issuers",
-                                            "w4_smem_tiles")}}), flush=True)
+                                            "w4_smem_tiles", "w4_decoders")}}), flush=True)
         del Qs, Ss, As, b, c
         torch.cuda.empty_cache()
     if sk.splitk_get_status() != 0:

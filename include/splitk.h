@@ -182,6 +182,11 @@ typedef struct splitk_plan_t {
                               mma_issuers = 1).  grid[1] is an upper bound: a
                               launch uses at most as many clusters as the
                               device holds at once and as there are tiles   */
+    int w4_decoders;       /* A16W4 only (0 for bf16 plans): 1 = the four
+                              epilogue warps decode the weight tiles; 2 = four
+                              more warps (384 threads a CTA, at most 2 CTAs
+                              an SM) decode the second half of every tile's K
+                              beside them                                   */
 } splitk_plan_t;
 
 /*

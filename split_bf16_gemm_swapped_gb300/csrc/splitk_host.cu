@@ -473,6 +473,9 @@ int plan_w4_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t sm
                             smem_bytes_w4(mma_n, kt, ded, 1) + 1024 <= smem_per_sm / 2
                         ? 1
                         : 0;
+  // A second decoding warpgroup halves every tile's decode (384 threads a
+  // CTA: at most 2 CTAs an SM by registers).
+  p.w4_decoders = 2;
   // Shared memory padded when needed so that the CTAs fitting an SM can
   // hold their TMEM.
   auto padded_smem = [&](size_t smem, uint32_t tmem_cols) {
@@ -491,17 +494,18 @@ int plan_w4_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t sm
   if (ctas > 2LL * num_sms && p.a_tmem_tiles > 1) {
     const uint32_t cols1 = tmem_cols_for(mma_n, 1, 1);
     const size_t smem1 = padded_smem(smem_bytes_w4(mma_n, kt, ded, 0), cols1);
-    if (std::min(3, resident_by_smem(smem_per_sm, smem1)) > std::min(3, resident_by_smem(smem_per_sm, smem))) {
+    if (std::min(3, resident_by_smem(smem_per_sm, smem1)) > std::min(2, resident_by_smem(smem_per_sm, smem))) {
       p.a_tmem_tiles = 1;
       p.mma_issuers = 1;
       p.tmem_cols = cols1;
       p.w4_smem_tiles = 0;
+      p.w4_decoders = 1;        // 256 threads: a third CTA fits an SM's registers
       smem = smem1;
     }
   }
   if (smem > smem_optin) return SPLITK_ERR_NO_FIT;
   p.smem_bytes = smem;
-  p.ctas_per_sm = std::min(3, resident_by_smem(smem_per_sm, smem));
+  p.ctas_per_sm = std::min(p.w4_decoders == 2 ? 2 : 3, resident_by_smem(smem_per_sm, smem));
   *out = p;
   return SPLITK_OK;
 }
@@ -517,6 +521,7 @@ int check_plan_w4(const splitk_plan_t& pl, int M, int N, int K, int L, size_t sm
   if (pl.k_tiles_per_cta != kt || pl.stages != kt) return SPLITK_ERR_BAD_PLAN;
   if (kt > kMaxStages) return SPLITK_ERR_NO_FIT;
   if (pl.reserved != 0 || pl.persistent != 0) return SPLITK_ERR_BAD_PLAN;
+  if (pl.w4_decoders != 1 && pl.w4_decoders != 2) return SPLITK_ERR_BAD_PLAN;
   const long long m_tiles = tiles_of(M, pl.mma_n);
   const long long n_tiles = ((long long)N + kMmaM - 1) / kMmaM;
   if (n_tiles > 65535 || L > 65535) return SPLITK_ERR_INVALID_SHAPE;
@@ -594,7 +599,9 @@ int check_plan(const splitk_plan_t& pl, int M, int N, int K, int L, size_t smem_
   if (pl.weight_format == SPLITK_WEIGHTS_E2M1_E8M0) {
     return check_plan_w4(pl, M, N, K, L, smem_optin, smem_per_sm, dedicated_bytes);
   }
-  if (pl.weight_format != SPLITK_WEIGHTS_BF16 || pl.w4_smem_tiles != 0) return SPLITK_ERR_BAD_PLAN;
+  if (pl.weight_format != SPLITK_WEIGHTS_BF16 || pl.w4_smem_tiles != 0 || pl.w4_decoders != 0) {
+    return SPLITK_ERR_BAD_PLAN;
+  }
   if (pl.persistent != 0) return check_plan_persistent(pl, M, N, K, L, smem_optin, smem_per_sm, dedicated_bytes);
   if (pl.mma_m != kMmaM) return SPLITK_ERR_BAD_PLAN;
   if (pl.mma_n != 16 && pl.mma_n != 32 && pl.mma_n != 64 && pl.mma_n != 128) return SPLITK_ERR_BAD_PLAN;
@@ -911,6 +918,7 @@ LaunchArgs launch_args(const splitk_plan_t& pl, bool pdl) {
   la.mma_n = pl.mma_n;
   la.w4 = pl.weight_format == SPLITK_WEIGHTS_E2M1_E8M0;
   la.persistent = pl.persistent != 0;
+  la.w4_decoders = pl.w4_decoders == 2 ? 2 : 1;
   la.grid = dim3(pl.grid[0], pl.grid[1], pl.grid[2]);
   la.cluster_x = (unsigned)pl.split_k;
   la.smem_bytes = pl.smem_bytes;

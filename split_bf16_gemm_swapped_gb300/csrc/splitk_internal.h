@@ -17,6 +17,7 @@ constexpr int kCtaK = 128;
 constexpr int kAtomK = 64;
 constexpr int kMmaK = 16;
 constexpr int kThreads = 256;      // warps 0..7
+constexpr int kThreadsW4Wide = 384;   // A16W4 with a second decoding warpgroup (warps 8..11)
 constexpr int kEpiThreads = 128;   // warps 4..7, one per TMEM lane / weight row
 constexpr int kMaxStages = 8;
 constexpr uint32_t kAStageBytes = kMmaM * kCtaK * 2;        // 32 KiB
@@ -129,6 +130,7 @@ struct LaunchArgs {
   int mma_n;
   bool w4;                    // A16W4 weights
   bool persistent;            // the persistent kernel (grid = (split, clusters, 1))
+  int w4_decoders;            // A16W4: decoding warpgroups (1 or 2)
   dim3 grid;
   unsigned cluster_x;
   size_t smem_bytes;

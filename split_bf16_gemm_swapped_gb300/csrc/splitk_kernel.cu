@@ -48,8 +48,10 @@
 
 namespace splitk {
 
-template <int MMA_N, bool kW4>
-__global__ void __launch_bounds__(kThreads, 3)
+// kDecWG: warpgroups decoding A16W4 weight tiles (1: warps 4..7, the
+// epilogue; 2: also warps 8..11, each group decoding half of every tile's K).
+template <int MMA_N, bool kW4, int kDecWG>
+__global__ void __launch_bounds__(kDecWG == 2 ? kThreadsW4Wide : kThreads, kDecWG == 2 ? 2 : 3)
     splitk_gemm_bf16_kernel(const __grid_constant__ CUtensorMap b_map, const KernelParams p) {
   constexpr uint32_t kBStage = b_stage_bytes(MMA_N);
   constexpr uint32_t kBBox = kBStage / 2;                   // MMA_N rows x 128 B
@@ -127,10 +129,10 @@ __global__ void __launch_bounds__(kThreads, 3)
       dev::mbar_init(bar_ready, 1);
       if (kW4) {
         for (int i = 0; i < 3; ++i) {
-          dev::mbar_init(bar_slot_full0 + 8u * i, kEpiThreads);
+          dev::mbar_init(bar_slot_full0 + 8u * i, (uint32_t)(kEpiThreads * kDecWG));
           dev::mbar_init(bar_slot_empty0 + 8u * i, 1);
         }
-        dev::mbar_init(bar_w4_stage, kEpiThreads);
+        dev::mbar_init(bar_w4_stage, (uint32_t)(kEpiThreads * kDecWG));
       }
       dev::st_shared_u32(slot_abort, 0u);
       dev::fence_barrier_init();
@@ -204,6 +206,53 @@ __global__ void __launch_bounds__(kThreads, 3)
     }
   }
   if (threadIdx.x == 128) stamp(p, kTrEpiSynced);
+
+  // A16W4 decode of the 32-k chunks [j0, j1) of weight row `row` of packed
+  // tile kt (64 B of the tile's 64-byte-swizzled row: chunk j sits at 16-byte
+  // slot j ^ ((row >> 1) & 3)), each chunk one scale block (scale code byte j
+  // of `codes`): a byte becomes two bf16 through the hardware E2M1 -> f16
+  // conversion, an exact rounding to bf16 and an exact bf16 product with the
+  // block's power of two.  Into TMEM columns t_col + 16 j of the thread's
+  // lane, or into the bf16 stage in shared memory in the 128-byte-swizzled
+  // layout of the bf16 path (two boxes of 64 k; 16-byte chunk c of row r of
+  // an 8-row atom at chunk c ^ (r % 8)), read by the MMA from there.
+  auto w4_decode_tmem = [&](int kt, int row, uint32_t codes, uint32_t t_col, int j0, int j1) {
+    const uint32_t src = sA + (uint32_t)kt * kW4TileBytes + (uint32_t)row * kW4RowBytes;
+#pragma unroll 1
+    for (int j = j0; j < j1; ++j) {
+      const uint32_t scale = dev::e8m0_bf16x2((codes >> (8 * j)) & 0xFFu);   // 2^(code - 127)
+      uint32_t w[4];
+      dev::ld_shared_v4(src + (uint32_t)((j ^ ((row >> 1) & 3)) * 16), w[0], w[1], w[2], w[3]);
+      uint32_t r[16];
+#pragma unroll
+      for (int q = 0; q < 16; ++q) r[q] = dev::e2m1x2_scaled_bf16x2(w[q >> 2] >> (8 * (q & 3)), scale);
+      __syncwarp();   // tcgen05.st is warp-collective
+      dev::tmem_st_x16(t_col + (uint32_t)(j * 16), r);
+    }
+  };
+  auto w4_decode_stage = [&](int kt, int row, uint32_t codes, int j0, int j1) {
+    const uint32_t src = sA + (uint32_t)kt * kW4TileBytes + (uint32_t)row * kW4RowBytes;
+    const uint32_t atom = sW4Stage + (uint32_t)(row >> 3) * 1024u + (uint32_t)(row & 7) * 128u;
+#pragma unroll 1
+    for (int j = j0; j < j1; ++j) {
+      const uint32_t scale = dev::e8m0_bf16x2((codes >> (8 * j)) & 0xFFu);
+      uint32_t w[4];
+      dev::ld_shared_v4(src + (uint32_t)((j ^ ((row >> 1) & 3)) * 16), w[0], w[1], w[2], w[3]);
+      uint32_t r[16];
+#pragma unroll
+      for (int q = 0; q < 16; ++q) r[q] = dev::e2m1x2_scaled_bf16x2(w[q >> 2] >> (8 * (q & 3)), scale);
+      // k = 32 j .. 32 j + 31: box j / 2, chunks 4 (j % 2) .. + 3
+      const uint32_t box = atom + (uint32_t)(j >> 1) * kABoxBytes;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int chunk = 4 * (j & 1) + c;
+        dev::st_shared_v4(box + (uint32_t)((chunk ^ (row & 7)) * 16), r[4 * c], r[4 * c + 1], r[4 * c + 2],
+                          r[4 * c + 3]);
+      }
+    }
+  };
+  // the chunks of each tile the epilogue warpgroup decodes (the rest: warps 8..11)
+  constexpr int kEpiJ1 = kDecWG == 2 ? 2 : 4;
 
   if (warp == 0) {
     // ---- weight producer
@@ -368,6 +417,34 @@ __global__ void __launch_bounds__(kThreads, 3)
       dev::mma_commit(bar_mma_done);           // this issuer's accumulator complete
     }
     __syncwarp();
+  } else if (kDecWG == 2 && warp >= 8) {
+    // ---- second A16W4 decoding warpgroup: chunks 2 and 3 (k 64..127) of
+    // every tile's rows, into the same TMEM slots or bf16 stage
+    const int row = (int)threadIdx.x - 256;
+    const uint32_t t_row2 = tmem_base + ((uint32_t)((warp & 3) * 32) << 16);
+    const int slots = p.a_tmem_tiles;
+    const bool row_ok = n0 + row < p.N;
+    const uint8_t* srow =
+        p.a_scale + ((size_t)l * p.N + (size_t)(row_ok ? n0 + row : 0)) * (size_t)(p.K / 32) + (size_t)kt0 * 4;
+    for (int kt = 0; kt < k_tiles; ++kt) {
+      if (p.w4_smem_tiles && kt == slots) {
+        waiter.wait<false>(bar_full0 + 8u * kt, 0u, kRoleEpiDecode, kt);
+        const uint32_t codes = row_ok ? __ldg(reinterpret_cast<const uint32_t*>(srow) + kt) : 0u;
+        w4_decode_stage(kt, row, codes, kEpiJ1, 4);
+        dev::fence_proxy_async_shared();
+        dev::mbar_arrive(bar_w4_stage);
+        continue;
+      }
+      const int slot = kt % slots;
+      const int round = kt / slots;
+      if (round > 0) waiter.wait<false>(bar_slot_empty0 + 8u * slot, (uint32_t)((round - 1) & 1), kRoleEpiDecode, kt);
+      waiter.wait<false>(bar_full0 + 8u * kt, 0u, kRoleEpiDecode, kt);
+      const uint32_t codes = row_ok ? __ldg(reinterpret_cast<const uint32_t*>(srow) + kt) : 0u;
+      w4_decode_tmem(kt, row, codes, t_row2 + p.tmem_tile_col0 + (uint32_t)slot * kTmemTileCols, kEpiJ1, 4);
+      dev::tmem_wait_st();
+      dev::tc_fence_before();
+      dev::mbar_arrive(bar_slot_full0 + 8u * slot);
+    }
   } else if (warp >= 4) {
     // ---- epilogue: thread et owns TMEM lane et = weight row n0 + et.
     const int et = (int)threadIdx.x - 128;
@@ -430,14 +507,11 @@ __global__ void __launch_bounds__(kThreads, 3)
 
     if constexpr (kW4) {
       // A16W4: thread et decodes weight row n0 + et of each K tile into TMEM
-      // lane et: 4 chunks of 32 codes (64 B of the tile's 64-byte-swizzled
-      // row: chunk j sits at 16-byte slot j ^ ((et >> 1) & 3)), each chunk
-      // one scale block; a byte becomes two bf16 through the hardware
-      // E2M1 -> f16 conversion, an exact rounding to bf16 and an exact bf16
-      // product with the block's power of two.  The first `slots` tiles are decoded
-      // before the previous kernel completes; with the epilogue loading the
-      // activations, that load comes next, then the remaining tiles as the
-      // MMAs free their slots.
+      // lane et (with a second decoding warpgroup: chunks 0 and 1 of each
+      // tile, the other group chunks 2 and 3).  The first `slots` tiles are
+      // decoded before the previous kernel completes; with the epilogue
+      // loading the activations, that load comes next, then the remaining
+      // tiles as the MMAs free their slots.
       const int slots = p.a_tmem_tiles;
       const bool row_ok = n0 + et < p.N;
       const uint8_t* srow =
@@ -445,31 +519,11 @@ __global__ void __launch_bounds__(kThreads, 3)
       for (int kt = 0; kt < k_tiles; ++kt) {
         if (kt == slots && p.b_loader && !p.w4_smem_tiles) load_activations();
         if (p.w4_smem_tiles && kt == slots) {
-          // the tile after the TMEM slots: decoded before the wait into a bf16
-          // stage in the 128-byte-swizzled layout (two boxes of 64 k; 16-byte
-          // chunk c of row r of an 8-row atom at chunk c ^ (r % 8)), read by
-          // the MMA from shared memory
+          // the tile after the TMEM slots: decoded before the wait into the
+          // bf16 stage in shared memory
           waiter.wait<false>(bar_full0 + 8u * kt, 0u, kRoleEpiDecode, kt);
           const uint32_t codes = row_ok ? __ldg(reinterpret_cast<const uint32_t*>(srow) + kt) : 0u;
-          const uint32_t row = sA + (uint32_t)kt * kW4TileBytes + (uint32_t)et * kW4RowBytes;
-          const uint32_t atom = sW4Stage + (uint32_t)(et >> 3) * 1024u + (uint32_t)(et & 7) * 128u;
-#pragma unroll 1
-          for (int j = 0; j < 4; ++j) {
-            const uint32_t scale = dev::e8m0_bf16x2((codes >> (8 * j)) & 0xFFu);
-            uint32_t w[4];
-            dev::ld_shared_v4(row + (uint32_t)((j ^ ((et >> 1) & 3)) * 16), w[0], w[1], w[2], w[3]);
-            uint32_t r[16];
-#pragma unroll
-            for (int q = 0; q < 16; ++q) r[q] = dev::e2m1x2_scaled_bf16x2(w[q >> 2] >> (8 * (q & 3)), scale);
-            // k = 32 j .. 32 j + 31: box j / 2, chunks 4 (j % 2) .. + 3
-            const uint32_t box = atom + (uint32_t)(j >> 1) * kABoxBytes;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              const int chunk = 4 * (j & 1) + c;
-              dev::st_shared_v4(box + (uint32_t)((chunk ^ (et & 7)) * 16), r[4 * c], r[4 * c + 1], r[4 * c + 2],
-                                r[4 * c + 3]);
-            }
-          }
+          w4_decode_stage(kt, et, codes, 0, kEpiJ1);
           dev::fence_proxy_async_shared();   // generic-proxy stores, read by tcgen05.mma
           dev::mbar_arrive(bar_w4_stage);
           if (p.b_loader) load_activations();   // the stage is the last tile
@@ -480,21 +534,7 @@ __global__ void __launch_bounds__(kThreads, 3)
         if (round > 0) waiter.wait<false>(bar_slot_empty0 + 8u * slot, (uint32_t)((round - 1) & 1), kRoleEpiDecode, kt);
         waiter.wait<false>(bar_full0 + 8u * kt, 0u, kRoleEpiDecode, kt);
         const uint32_t codes = row_ok ? __ldg(reinterpret_cast<const uint32_t*>(srow) + kt) : 0u;
-        const uint32_t row = sA + (uint32_t)kt * kW4TileBytes + (uint32_t)et * kW4RowBytes;
-        const uint32_t t_col = t_row + p.tmem_tile_col0 + (uint32_t)slot * kTmemTileCols;
-#pragma unroll 1
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t scale = dev::e8m0_bf16x2((codes >> (8 * j)) & 0xFFu);   // 2^(code - 127)
-          uint32_t w[4];
-          dev::ld_shared_v4(row + (uint32_t)((j ^ ((et >> 1) & 3)) * 16), w[0], w[1], w[2], w[3]);
-          uint32_t r[16];
-#pragma unroll
-          for (int q = 0; q < 16; ++q) {
-            r[q] = dev::e2m1x2_scaled_bf16x2(w[q >> 2] >> (8 * (q & 3)), scale);
-          }
-          __syncwarp();   // tcgen05.st is warp-collective
-          dev::tmem_st_x16(t_col + (uint32_t)(j * 16), r);
-        }
+        w4_decode_tmem(kt, et, codes, t_row + p.tmem_tile_col0 + (uint32_t)slot * kTmemTileCols, 0, kEpiJ1);
         dev::tmem_wait_st();
         dev::tc_fence_before();
         dev::mbar_arrive(bar_slot_full0 + 8u * slot);
@@ -837,12 +877,12 @@ __global__ void __launch_bounds__(kThreads, 3)
 // ---------------------------------------------------------------- host side
 namespace {
 
-template <int MMA_N, bool kW4>
+template <int MMA_N, bool kW4, int kDecWG = 1>
 cudaError_t launch_t(const LaunchArgs& la, const CUtensorMap& b_map, const KernelParams& p,
                      cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = la.grid;
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(kDecWG == 2 ? kThreadsW4Wide : kThreads, 1, 1);
   cfg.dynamicSmemBytes = la.smem_bytes;
   cfg.stream = stream;
   cudaLaunchAttribute attrs[2];
@@ -859,12 +899,12 @@ cudaError_t launch_t(const LaunchArgs& la, const CUtensorMap& b_map, const Kerne
   }
   cfg.attrs = attrs;
   cfg.numAttrs = n;
-  return cudaLaunchKernelEx(&cfg, splitk_gemm_bf16_kernel<MMA_N, kW4>, b_map, p);
+  return cudaLaunchKernelEx(&cfg, splitk_gemm_bf16_kernel<MMA_N, kW4, kDecWG>, b_map, p);
 }
 
-template <int MMA_N, bool kW4>
+template <int MMA_N, bool kW4, int kDecWG = 1>
 cudaError_t prepare_t(int max_dynamic_smem) {
-  return cudaFuncSetAttribute(splitk_gemm_bf16_kernel<MMA_N, kW4>,
+  return cudaFuncSetAttribute(splitk_gemm_bf16_kernel<MMA_N, kW4, kDecWG>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, max_dynamic_smem);
 }
 
@@ -874,6 +914,13 @@ cudaError_t launch_kernel(const LaunchArgs& la, const CUtensorMap& b_map, const 
                           cudaStream_t stream) {
   if (la.w4) {
     // A16W4 weights: decode-sized tiles only
+    if (la.w4_decoders == 2) {
+      switch (la.mma_n) {
+        case 16: return launch_t<16, true, 2>(la, b_map, p, stream);
+        case 32: return launch_t<32, true, 2>(la, b_map, p, stream);
+        default: return cudaErrorInvalidValue;
+      }
+    }
     switch (la.mma_n) {
       case 16: return launch_t<16, true>(la, b_map, p, stream);
       case 32: return launch_t<32, true>(la, b_map, p, stream);
@@ -896,7 +943,9 @@ cudaError_t prepare_kernels(int max_dynamic_smem) {
   if ((e = prepare_t<64, false>(max_dynamic_smem)) != cudaSuccess) return e;
   if ((e = prepare_t<128, false>(max_dynamic_smem)) != cudaSuccess) return e;
   if ((e = prepare_t<16, true>(max_dynamic_smem)) != cudaSuccess) return e;
-  return prepare_t<32, true>(max_dynamic_smem);
+  if ((e = prepare_t<32, true>(max_dynamic_smem)) != cudaSuccess) return e;
+  if ((e = prepare_t<16, true, 2>(max_dynamic_smem)) != cudaSuccess) return e;
+  return prepare_t<32, true, 2>(max_dynamic_smem);
 }
 
 cudaError_t read_and_clear_fault(int* out_words) {

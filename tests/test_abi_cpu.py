@@ -452,6 +452,15 @@ def test_plan_check_rejects_what_a_launch_would():
     bad.reserved = 2                                    # the reserved field must stay 0
     assert _check(bad, M, N, K, L) == -10
     bad = sk.Plan.from_buffer_copy(p)
+    bad.w4_decoders = 1                                 # a bf16 plan decodes nothing
+    assert _check(bad, M, N, K, L) == -10
+    w4 = sk.splitk_plan_w4a16_for(M, N, K, L, 4, **GB300)
+    assert _check(w4, M, N, K, L) == 0
+    for dec in (0, 3):
+        bad = sk.Plan.from_buffer_copy(w4)
+        bad.w4_decoders = dec
+        assert _check(bad, M, N, K, L) == -10
+    bad = sk.Plan.from_buffer_copy(p)
     bad.cluster[1] = 2                                  # clusters span the K ranks of one tile only
     assert _check(bad, M, N, K, L) == -10
 
@@ -494,8 +503,9 @@ def test_w4a16_plans(args):
 def test_w4a16_grids_of_several_waves_trade_tmem_slots_for_residency():
     one = sk.splitk_plan_w4a16_for(1, 7168, 2048, 1, 4, **GB300)    # 224 CTAs: under two waves
     assert one.a_tmem_tiles == 3 and one.ctas_per_sm == 2
+    assert one.w4_decoders == 2                                      # 384 threads: two decoding warpgroups
     many = sk.splitk_plan_w4a16_for(1, 7168, 2048, 8, 4, **GB300)   # 1792 CTAs
-    assert (many.a_tmem_tiles, many.mma_issuers, many.w4_smem_tiles) == (1, 1, 0)
+    assert (many.a_tmem_tiles, many.mma_issuers, many.w4_smem_tiles, many.w4_decoders) == (1, 1, 0, 1)
     assert many.ctas_per_sm == 3 and many.ctas_per_sm * many.tmem_cols <= 512
     assert _check(many, 1, 7168, 2048, 8) == 0
     wide = sk.splitk_plan_w4a16_for(16, 4096, 7168, 4, 8, **GB300)  # one slot would not raise residency

@@ -485,12 +485,14 @@ def test_w4a16_equals_the_bf16_kernel_on_the_decoded_weights(M, split):
         assert np.array_equal(c4, cb), issuers
 
 
-def _w4_variant(base, slots, stage, loader, issuers=1):
+def _w4_variant(base, slots, stage, loader, issuers=1, decoders=None):
     """`base` with `slots` TMEM slots, the bf16 shared-memory stage on or
-    off, the given activation loader and MMA issuers; shared memory grown
-    for the stage and padded until the slots of the CTAs sharing an SM fit
-    its TMEM."""
+    off, the given activation loader, MMA issuers and decoding warpgroups;
+    shared memory grown for the stage and padded until the slots of the CTAs
+    sharing an SM fit its TMEM."""
     p = sk.Plan.from_buffer_copy(base)
+    if decoders is not None:
+        p.w4_decoders = decoders
     p.a_tmem_tiles = slots
     p.mma_issuers = issuers
     p.tmem_cols = _tmem_cols(p.mma_n, slots, issuers)
@@ -520,9 +522,10 @@ def test_w4a16_slot_counts_and_activation_loaders_agree(M, K, variants):
     ta, ts, tb = _u8_dev(aq), _u8_dev(a_s), to_dev(b)
     outs = {1: [], 2: []}
     for slots, stage, loader, issuers in variants:
-        p = _w4_variant(base, slots, stage, loader, issuers)
-        for _ in range(3):                 # repeated: a race shows as a difference
-            outs[issuers].append(to_host(sk.splitk_gemm_w4a16_planned(ta, ts, tb, None, p)))
+        for decoders in (1, 2):            # one or two decoding warpgroups: the same bits
+            p = _w4_variant(base, slots, stage, loader, issuers, decoders)
+            for _ in range(3):             # repeated: a race shows as a difference
+                outs[issuers].append(to_host(sk.splitk_gemm_w4a16_planned(ta, ts, tb, None, p)))
         torch.cuda.synchronize()
         assert sk.splitk_get_status() == 0
     ref = oracle.gemm_w4a16(aq, a_s, b)
@@ -722,8 +725,8 @@ def test_persistent_kernel_closed_forms_and_bias():
     ones = np.full((L, N, K), ONE, np.uint16)
     c = gemm_gpu(ones, np.full((L, M, K), ONE, np.uint16), plan=p)
     assert np.all(c == oracle.f64_to_bf16(float(K)))
-    # a shape whose plan is persistent (more CTAs than SMs), through the bias entry point
-    L, M, N, K = 1, 64, 5000, 2048
+    # a shape whose plan is persistent (76 tiles: two rounds of 38 clusters), through the bias entry point
+    L, M, N, K = 1, 64, 9728 - 100, 1024
     assert sk.splitk_plan(M, N, K, L, split).persistent == 1
     a, b = _draw(L, M, N, K, seed=2900)
     bias = synthetic.normal_bf16((L, N), 2900, synthetic.STREAM_OUTLIER, 0.5)
