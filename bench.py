@@ -902,7 +902,8 @@ def run_sweep_persistent(args):
                                               props.shared_memory_per_multiprocessor,
                                               props.shared_memory_per_block_optin)
         ring = next(p for p in cands if not p.persistent)
-        plans = [("per-tile", ring)] + [(f"persistent s{p.stages}", p) for p in cands if p.persistent]
+        plans = [("per-tile", ring)] + [(f"persistent s{p.stages} r{p.reduce_rounds}", p)
+                                        for p in cands if p.persistent]
         out = {}
         for name, plan in plans:
             def call(i, plan=plan):

@@ -474,8 +474,11 @@ int plan_w4_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t sm
                         ? 1
                         : 0;
   // A second decoding warpgroup halves every tile's decode (384 threads a
-  // CTA: at most 2 CTAs an SM by registers).
-  p.w4_decoders = 2;
+  // CTA: at most 2 CTAs an SM by registers).  Measured on GB300 it pays from
+  // 5 K tiles a CTA (small-batch decode, 7 tiles: 12.17 -> 11.76 us; M=16,
+  // L=4: 48.1 -> 45.9 us) and costs at 4 (single-token decode: 6.56 ->
+  // 6.67 us), where the next kernel's CTAs find fewer free registers.
+  p.w4_decoders = kt >= 5 ? 2 : 1;
   // Shared memory padded when needed so that the CTAs fitting an SM can
   // hold their TMEM.
   auto padded_smem = [&](size_t smem, uint32_t tmem_cols) {
