@@ -914,7 +914,7 @@ def run_sweep_persistent(args):
                                               props.shared_memory_per_multiprocessor,
                                               props.shared_memory_per_block_optin)
         ring = next(p for p in cands if not p.persistent)
-        plans = [("per-tile", ring)] + [(f"persistent s{p.stages} r{p.reduce_rounds}", p)
+        plans = [("per-tile", ring)] + [(f"persistent n{p.mma_n} s{p.stages} r{p.reduce_rounds}", p)
                                         for p in cands if p.persistent]
         out = {}
         for name, plan in plans:

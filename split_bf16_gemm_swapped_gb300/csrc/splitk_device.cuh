@@ -125,6 +125,12 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return pol;
 }
 
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
 // The tensor map lives in global memory, written through the generic proxy
 // (a copy from the host); make it visible to the tensormap proxy.
 __device__ __forceinline__ void tensormap_acquire(const void* map) {

@@ -186,11 +186,12 @@ bool stage_for_decode(splitk_plan_t* out, int ncols_max, long long ctas, int num
 // groups; two accumulators in TMEM; one cluster per `split` SMs (at most one
 // per output tile).  Nonzero `stages` / `quads` fix the ring depth / round.
 bool persistent_plan(int M, int N, int K, int L, int split, int stages, int quads, int num_sms,
-                     size_t smem_per_sm, size_t smem_optin, splitk_plan_t* out) {
+                     size_t smem_per_sm, size_t smem_optin, splitk_plan_t* out, int mma_n_want = 0) {
   if (split < 2 || !valid_split(split)) return false;
   const int T = total_k_tiles(K);
   if (T < split) return false;
-  const int mma_n = choose_mma_n(M);
+  const int mma_n = mma_n_want != 0 ? mma_n_want : choose_mma_n(M);
+  if (mma_n != 16 && mma_n != 32 && mma_n != 64 && mma_n != 128) return false;
   const int ncols_max = std::min(M, mma_n);
   const int nquads_max = (ncols_max + 3) / 4;
   const size_t budget = std::min(smem_optin, smem_per_sm - 1024);
@@ -1097,19 +1098,25 @@ int enumerate_plans(int M, int N, int K, int L, int split_k, int num_sms, size_t
         }
       }
     }
-    // the persistent kernel at every ring depth and reduction round that fit
-    for (int stages = 2; split >= 2 && stages <= kMaxStages; ++stages) {
-      for (int quads : {nquads_max, 16, 8, 4}) {
-        if (quads > nquads_max || (quads != nquads_max && quads % 4 != 0)) continue;
-        splitk_plan_t p;
-        uint32_t ded_check = 0;
-        if (!persistent_plan(M, N, K, L, split, stages, quads, num_sms, smem_per_sm, smem_optin, &p) ||
-            check_plan(p, M, N, K, L, smem_optin, smem_per_sm, &ded_check) != SPLITK_OK) {
-          continue;
+    // the persistent kernel at every ring depth and reduction round that
+    // fit, at the shape's token tile and (for more than 64 tokens) at
+    // 64-token tiles, several of which share each weight tile
+    for (int tile_n : {mma_n, 64}) {
+      if (tile_n != mma_n && M <= 64) continue;
+      const int nq = (std::min(M, tile_n) + 3) / 4;
+      for (int stages = 2; split >= 2 && stages <= kMaxStages; ++stages) {
+        for (int quads : {nq, 16, 8, 4}) {
+          if (quads > nq || (quads != nq && quads % 4 != 0)) continue;
+          splitk_plan_t p;
+          uint32_t ded_check = 0;
+          if (!persistent_plan(M, N, K, L, split, stages, quads, num_sms, smem_per_sm, smem_optin, &p, tile_n) ||
+              check_plan(p, M, N, K, L, smem_optin, smem_per_sm, &ded_check) != SPLITK_OK) {
+            continue;
+          }
+          bool dup = false;
+          for (const auto& q : *out) dup = dup || same(p, q);
+          if (!dup) out->push_back(p);
         }
-        bool dup = false;
-        for (const auto& q : *out) dup = dup || same(p, q);
-        if (!dup) out->push_back(p);
       }
     }
   }

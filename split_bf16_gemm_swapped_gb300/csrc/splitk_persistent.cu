@@ -66,8 +66,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int split = p.split;
   const int stages = p.stages;
   const int rank = (int)dev::cluster_ctarank();
-  // Output tiles: n fastest, then m, then l, so that the clusters working at
-  // the same time share activation tiles in L2.
+  // Output tiles: m (token tiles) fastest, then n, then l.  The clusters
+  // working at the same time then share each weight tile's reads when there
+  // are several token tiles (the later reads hit L2), and activation tiles
+  // in L2 either way.
   const int m_tiles = (p.M + MMA_N - 1) / MMA_N;
   const int n_tiles = (p.N + kMmaM - 1) / kMmaM;
   const long long tiles = (long long)m_tiles * n_tiles * p.L;
@@ -99,10 +101,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   auto tile_coords = [&](int j, int* n0, int* m0, int* l) {
     const long long t = (long long)cy + (long long)j * clusters;
-    const long long r = t / n_tiles;
-    *n0 = (int)(t - r * n_tiles) * kMmaM;
-    *m0 = (int)(r % m_tiles) * MMA_N;
-    *l = (int)(r / m_tiles);
+    const long long r = t / m_tiles;
+    *m0 = (int)(t - r * m_tiles) * MMA_N;
+    *n0 = (int)(r % n_tiles) * kMmaM;
+    *l = (int)(r / n_tiles);
   };
 
   // ---- set-up: warp 3 initialises the barriers, warp 2 allocates TMEM,
@@ -135,7 +137,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       stamp(p, kTrStart);
       dev::tensormap_acquire(p.a_map);
       stamp(p, kTrMapReady);
-      a_policy = dev::policy_evict_first();
+      // Weights are read once (evict first), or once per token tile by
+      // clusters working side by side (kept for the later reads).
+      a_policy = m_tiles == 1 ? dev::policy_evict_first() : dev::policy_evict_normal();
     }
     dev::named_bar_sync(2, 64);
   } else if (warp == 2) {

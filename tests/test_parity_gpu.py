@@ -645,7 +645,7 @@ def test_w4a16_the_largest_grid_dimensions_index_correctly(L, N):
 
 
 # ---------------------------------------------------------------- persistent plans
-def _persistent(M, N, K, L, split, clusters=None, stages=None, quads=None):
+def _persistent(M, N, K, L, split, clusters=None, stages=None, quads=None, mma_n=None):
     """The persistent plan of the shape at `split` (the deepest ring unless
     `stages` is given, reduction rounds of `quads` 4-column groups if given),
     with `clusters` as its grid bound if given."""
@@ -653,7 +653,8 @@ def _persistent(M, N, K, L, split, clusters=None, stages=None, quads=None):
     cands = sk.splitk_plan_candidates_for(M, N, K, L, split, props.multi_processor_count,
                                           props.shared_memory_per_multiprocessor,
                                           props.shared_memory_per_block_optin)
-    ps = [p for p in cands if p.persistent and (quads is None or p.mailbox_quads == quads)]
+    ps = [p for p in cands if p.persistent and (quads is None or p.mailbox_quads == quads)
+          and (mma_n is None or p.mma_n == mma_n)]
     assert ps, "no persistent candidate"
     p = max(ps, key=lambda q: q.stages) if stages is None else next(q for q in ps if q.stages == stages)
     p = sk.Plan.from_buffer_copy(p)
@@ -714,6 +715,20 @@ def test_persistent_reduction_rounds(M, quads):
     c = gemm_gpu(a, b, plan=p)
     one = _persistent(M, N, K, L, split, clusters=3, quads=-(-min(M, p.mma_n) // 4), stages=2)
     assert np.array_equal(c, gemm_gpu(a, b, plan=one))
+    assert_parity(c, oracle_full(a, b), a, b, K)
+
+
+@pytest.mark.parametrize("M", [100, 128, 129])
+def test_persistent_64_token_tiles_share_weight_tiles(M):
+    """More than 64 tokens as several 64-token tiles per weight tile (the
+    clusters working side by side read each weight tile in turn): the same
+    bits as the shape's own token tile, and the oracle's values."""
+    L, N, K, split = 2, 520, 2048, 8
+    a, b = _draw(L, M, N, K, seed=3100 + M)
+    p64 = _persistent(M, N, K, L, split, clusters=5, mma_n=64)
+    c = gemm_gpu(a, b, plan=p64)
+    own = _persistent(M, N, K, L, split, clusters=3, mma_n=128)
+    assert np.array_equal(c, gemm_gpu(a, b, plan=own))
     assert_parity(c, oracle_full(a, b), a, b, K)
 
 
