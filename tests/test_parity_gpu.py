@@ -710,10 +710,11 @@ def test_persistent_reduction_rounds(M, quads):
     tile, and the oracle's values."""
     L, N, K, split = 2, 520, 2048, 4
     a, b = _draw(L, M, N, K, seed=3000 + M)
-    p = _persistent(M, N, K, L, split, clusters=3, quads=quads)
+    tile = next(t for t in (16, 32, 64, 128) if t >= min(M, 128))      # the shape's own token tile
+    p = _persistent(M, N, K, L, split, clusters=3, quads=quads, mma_n=tile)
     assert p.reduce_rounds > 1
     c = gemm_gpu(a, b, plan=p)
-    one = _persistent(M, N, K, L, split, clusters=3, quads=-(-min(M, p.mma_n) // 4), stages=2)
+    one = _persistent(M, N, K, L, split, clusters=3, quads=-(-min(M, tile) // 4), stages=2, mma_n=tile)
     assert np.array_equal(c, gemm_gpu(a, b, plan=one))
     assert_parity(c, oracle_full(a, b), a, b, K)
 
