@@ -761,7 +761,7 @@ struct DeviceState {
   int used = 0;
   std::unordered_map<AKey, int, AKeyHash> a_slots;
   std::unordered_map<BKey, CUtensorMap, BKeyHash> b_maps;
-  std::unordered_map<uint64_t, int> max_clusters;   // persistent kernel: clusters resident at once
+  int max_clusters[9] = {};        // persistent kernel: clusters of 2, 4, 8 resident at once (0: unknown)
 };
 
 std::mutex g_mu;
@@ -797,6 +797,17 @@ int current_device(DeviceState** out, int* dev_out) {
     st.num_sms = sms;
     st.smem_optin = (size_t)optin;
     st.smem_per_sm = (size_t)per_sm;
+    // Clusters of the persistent kernel that fit the device at once, one CTA
+    // an SM (the shared memory of its plans), queried here rather than at a
+    // launch that may be part of a graph capture.
+    for (int split : {2, 4, 8}) {
+      int fit = 0;
+      if (max_active_clusters_persistent(128, (unsigned)split, (size_t)optin, &fit) != cudaSuccess) {
+        cudaGetLastError();
+        fit = 0;
+      }
+      st.max_clusters[split] = fit;
+    }
     st.ready = true;
   }
   *out = &st;
@@ -938,19 +949,10 @@ cudaError_t launch_plan(DeviceState& st, const splitk_plan_t& pl, const LaunchAr
                         const KernelParams& p, int M, int N, int L, cudaStream_t stream) {
   if (!la0.persistent) return launch_kernel(la0, b_map, p, stream);
   LaunchArgs la = la0;
-  const uint64_t key = ((uint64_t)pl.mma_n << 48) | ((uint64_t)pl.split_k << 40) | (uint64_t)pl.smem_bytes;
-  auto it = st.max_clusters.find(key);
-  if (it == st.max_clusters.end()) {
-    int fit = 0;
-    if (max_active_clusters_persistent(pl.mma_n, (unsigned)pl.split_k, pl.smem_bytes, &fit) != cudaSuccess) {
-      cudaGetLastError();
-      fit = 0;                                   // unknown: the plan's own bound
-    }
-    it = st.max_clusters.emplace(key, fit).first;
-  }
+  const int fit = pl.split_k >= 2 && pl.split_k <= 8 ? st.max_clusters[pl.split_k] : 0;
   const long long tiles = tiles_of(M, pl.mma_n) * tiles_of(N, kMmaM) * L;
   long long g = std::min<long long>((long long)pl.grid[1], tiles);
-  if (it->second > 0) g = std::min<long long>(g, it->second);
+  if (fit > 0) g = std::min<long long>(g, fit);       // 0: unknown, the plan's own bound
   la.grid = dim3((unsigned)pl.split_k, (unsigned)std::max<long long>(1, g), 1u);
   return launch_persistent(la, b_map, p, stream);
 }

@@ -308,3 +308,42 @@ def test_release_frees_the_cache_and_later_calls_rebuild_it():
     ref = oracle.gemm(a, b)
     assert_parity(to_host(c2), ref, a, b, 2048)
     assert_parity(to_host(c3), ref, a, b, 2048)
+
+
+def test_persistent_plans_chain_with_pdl_and_replay_in_a_graph():
+    """Persistent plans (the planner's choice at split 8 for long streams):
+    a call whose activations are the previous call's output waits for it
+    (programmatic dependent launch), and calls captured in a CUDA graph --
+    the first one of the shape inside the capture -- replay bit for bit."""
+    M, N1, K1, N2 = 16, 4864, 4096, 4864
+    a1 = synthetic.normal_bf16((N1, K1), 71, synthetic.STREAM_A, 0.02)
+    a2 = synthetic.normal_bf16((N2, N1), 72, synthetic.STREAM_A, 0.02)
+    b0 = synthetic.normal_bf16((M, K1), 71, synthetic.STREAM_B, 1.0)
+    ta1, ta2, tb0 = to_dev(a1), to_dev(a2), to_dev(b0)
+    p1 = sk.splitk_plan(M, N1, K1, 1, 8)
+    p2 = sk.splitk_plan(M, N2, N1, 1, 8)
+    assert p1.persistent == 1 and p2.persistent == 1
+    torch.cuda.synchronize()
+    c1 = sk.splitk_gemm_bf16(ta1, tb0, split_k=8)
+    c2 = sk.splitk_gemm_bf16(ta2, c1, split_k=8)               # PDL on
+    torch.cuda.synchronize()
+    d1 = sk.splitk_gemm_bf16_planned(ta1, tb0, None, p1, sk.FLAG_NO_PDL)
+    torch.cuda.synchronize()
+    d2 = sk.splitk_gemm_bf16_planned(ta2, d1, None, p2, sk.FLAG_NO_PDL)
+    torch.cuda.synchronize()
+    assert torch.equal(c1.view(torch.int16), d1.view(torch.int16))
+    assert torch.equal(c2.view(torch.int16), d2.view(torch.int16))
+    assert_parity(to_host(c1), oracle.gemm(a1, b0), a1, b0, K1)
+    # capture: a new weight pointer, so its tensor map is first made inside the capture
+    ta3 = ta1.clone()
+    out = torch.empty_like(c1)
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(3):
+            sk.splitk_gemm_bf16(ta3, tb0, out, split_k=8, stream=s)
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert sk.splitk_get_status() == 0
+    assert torch.equal(out.view(torch.int16), c1.view(torch.int16))
