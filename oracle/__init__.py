@@ -81,6 +81,12 @@ def _load():
     lib.oracle_w4_elements.argtypes = [u8p, u8p, u16p, u16p, i64, i64, i64, i64,
                                        ctypes.POINTER(ctypes.c_int64), i64]
     lib.oracle_w4_elements.restype = None
+    lib.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint]
+    lib.oracle_e4m3_to_f64.restype = ctypes.c_double
+    lib.oracle_w8_dequant.argtypes = [u8p, u8p, f64p, i64, i64, i64]
+    lib.oracle_w8_dequant.restype = None
+    lib.oracle_gemm_w8a16.argtypes = [u8p, u8p, u16p, u16p, i64, i64, i64, i64]
+    lib.oracle_gemm_w8a16.restype = None
     _lib = lib
     return lib
 
@@ -231,3 +237,47 @@ def w4_elements(Aq: np.ndarray, As: np.ndarray, B: np.ndarray, flat_idx) -> np.n
     _load().oracle_w4_elements(_ptr(Aq, ctypes.c_uint8), _ptr(As, ctypes.c_uint8), _ptr(B), _ptr(out),
                                M, N, K, L, _ptr(idx, ctypes.c_int64), idx.shape[0])
     return out
+
+
+# --------------------------------------------------------------------------
+# A16W8: E4M3 weights with E8M0 scales per 32 k, bf16 activations
+# --------------------------------------------------------------------------
+def e4m3_to_f64(code: int) -> float:
+    return _load().oracle_e4m3_to_f64(int(code) & 0xFF)
+
+
+def _w8_shape(Aq: np.ndarray, As: np.ndarray, B: np.ndarray):
+    Aq = np.ascontiguousarray(Aq, dtype=np.uint8)
+    As = np.ascontiguousarray(As, dtype=np.uint8)
+    B = _u16(B)
+    if Aq.ndim == 2:
+        Aq, As, B = Aq[None], As[None], B[None]
+    L, N, K = Aq.shape
+    Lb, M, Kb = B.shape
+    if (Lb, Kb) != (L, K) or As.shape != (L, N, K // 32) or K % 32:
+        raise ValueError(f"shape mismatch Aq{Aq.shape} As{As.shape} B{B.shape}")
+    return Aq, As, np.ascontiguousarray(B), M, N, K, L
+
+
+def w8_dequant(Aq: np.ndarray, As: np.ndarray) -> np.ndarray:
+    """The float64 weights W[L, N, K] that the E4M3 codes A_q and scales A_s encode."""
+    squeeze = Aq.ndim == 2
+    Aq = np.ascontiguousarray(Aq, dtype=np.uint8)
+    As = np.ascontiguousarray(As, dtype=np.uint8)
+    if squeeze:
+        Aq, As = Aq[None], As[None]
+    L, N, K = Aq.shape
+    W = np.empty((L, N, K), dtype=np.float64)
+    _load().oracle_w8_dequant(_ptr(Aq, ctypes.c_uint8), _ptr(As, ctypes.c_uint8),
+                              _ptr(W, ctypes.c_double), N, K, L)
+    return W[0] if squeeze else W
+
+
+def gemm_w8a16(Aq: np.ndarray, As: np.ndarray, B: np.ndarray) -> np.ndarray:
+    """C[L, M, N] bf16 bits = RNE(sum_k w[l,n,k] * B[l,m,k]) in float64, 8-bit weights."""
+    squeeze = np.asarray(Aq).ndim == 2
+    Aq, As, B, M, N, K, L = _w8_shape(Aq, As, B)
+    C = np.empty((L, M, N), dtype=np.uint16)
+    _load().oracle_gemm_w8a16(_ptr(Aq, ctypes.c_uint8), _ptr(As, ctypes.c_uint8), _ptr(B), _ptr(C),
+                              M, N, K, L)
+    return C[0] if squeeze else C

@@ -308,3 +308,61 @@ void oracle_w4_elements(const uint8_t *Aq, const uint8_t *As, const uint16_t *B,
         out[i] = oracle_f64_to_bf16(oracle_w4_dot_f64(Aq, As, B, M, N, K, l, m, n));
     }
 }
+
+/* ------------------------------------------------------------------------
+ * A16W8: 8-bit E4M3 weights with E8M0 scales per 32 k, bf16 activations.
+ *
+ *   E4M3 (the DeepSeek-V4.1 AMD mono ops page's fp8_pack4 packs four f32 into
+ *   "four E4M3 bytes, RNE"; the bit layout is the OCP 8-bit floating-point
+ *   E4M3 definition, a reading: the page names the format, not its fields):
+ *   sign bit 7, exponent bits 6..3 with bias 7, mantissa bits 2..0.
+ *   Exponent 0 is subnormal, m * 2^-9; exponent field 15 with mantissa 7 is
+ *   not a number (no infinities; largest finite 448).
+ *
+ *   Weights: A_q[l][n][k] bytes, one code per k; scales A_s[l][n][k/32], one
+ *   E8M0 code per 32 consecutive k of a weight row, as for the 4-bit weights
+ *   above (the OCP microscaling block -- a reading: the pages give no block
+ *   scale for 8-bit weights; this is the plainest one that matches the 4-bit
+ *   path).
+ *
+ *   C[l][m][n] = RNE_bf16( sum_k w(l,n,k) * f64(B[l][m][k]) ),
+ *   w(l,n,k) = e4m3(A_q[l][n][k]) * e8m0(A_s[l][n][k/32]), exact in float64.
+ * ------------------------------------------------------------------------ */
+double oracle_e4m3_to_f64(unsigned code)
+{
+    code &= 0xFFu;
+    const unsigned s = code >> 7, e = (code >> 3) & 15u, m = code & 7u;
+    if (e == 15u && m == 7u) return NAN;
+    double mag = e == 0 ? (double)m * ldexp(1.0, -9) : (1.0 + (double)m / 8.0) * ldexp(1.0, (int)e - 7);
+    return s ? -mag : mag;
+}
+
+/* The dequantized 8-bit weight w(l, n, k). */
+double oracle_w8_weight(const uint8_t *Aq, const uint8_t *As, int64_t N, int64_t K,
+                        int64_t l, int64_t n, int64_t k)
+{
+    const uint8_t code = Aq[(l * N + n) * K + k];
+    const uint8_t scale = As[(l * N + n) * (K / 32) + k / 32];
+    return oracle_e4m3_to_f64(code) * oracle_e8m0_to_f64(scale);
+}
+
+void oracle_w8_dequant(const uint8_t *Aq, const uint8_t *As, double *W, int64_t N, int64_t K, int64_t L)
+{
+    for (int64_t l = 0; l < L; ++l)
+        for (int64_t n = 0; n < N; ++n)
+            for (int64_t k = 0; k < K; ++k)
+                W[(l * N + n) * K + k] = oracle_w8_weight(Aq, As, N, K, l, n, k);
+}
+
+void oracle_gemm_w8a16(const uint8_t *Aq, const uint8_t *As, const uint16_t *B, uint16_t *C,
+                       int64_t M, int64_t N, int64_t K, int64_t L)
+{
+    for (int64_t l = 0; l < L; ++l)
+        for (int64_t m = 0; m < M; ++m)
+            for (int64_t n = 0; n < N; ++n) {
+                double s = 0.0;
+                for (int64_t k = 0; k < K; ++k)
+                    s += oracle_w8_weight(Aq, As, N, K, l, n, k) * oracle_bf16_to_f64(B[(l * M + m) * K + k]);
+                C[(l * M + m) * N + n] = oracle_f64_to_bf16(s);
+            }
+}

@@ -22,6 +22,8 @@ STREAM_B = 1
 STREAM_OUTLIER = 2
 STREAM_A_CODES = 3      # packed 4-bit weight codes (A16W4)
 STREAM_A_SCALES = 4     # 8-bit scale codes (A16W4)
+STREAM_A_CODES8 = 5     # 8-bit E4M3 weight codes (A16W8)
+STREAM_A_SCALES8 = 6    # their scale codes
 
 _lib = None
 
@@ -107,4 +109,22 @@ def w4_weights(L: int, N: int, K: int, seed: int):
         raise ValueError("K must be a multiple of 32 (the scale block)")
     aq = uniform_bytes((L, N, K // 2), seed, STREAM_A_CODES)
     a_s = uniform_bytes((L, N, K // 32), seed, STREAM_A_SCALES, W4_SCALE_LO, W4_SCALE_SPAN)
+    return aq, a_s
+
+
+# Scale codes of the A16W8 weights: 2^-13 ... 2^-7, so that E4M3 magnitudes
+# (2^-9 ... 448) land in the range of N(0, 0.02)-like weights.
+W8_SCALE_LO = 114
+W8_SCALE_SPAN = 7
+
+
+def w8_weights(L: int, N: int, K: int, seed: int):
+    """Seeded A16W8 weights: E4M3 codes A_q[L][N][K] (uniform over the 254
+    finite codes: the two not-a-number codes 0x7F and 0xFF become 0x7E and
+    0xFE) and E8M0 scale codes A_s[L][N][K/32]."""
+    if K % 32:
+        raise ValueError("K must be a multiple of 32 (the scale block)")
+    aq = uniform_bytes((L, N, K), seed, STREAM_A_CODES8)
+    aq[(aq & 0x7F) == 0x7F] ^= 1
+    a_s = uniform_bytes((L, N, K // 32), seed, STREAM_A_SCALES8, W8_SCALE_LO, W8_SCALE_SPAN)
     return aq, a_s

@@ -453,3 +453,126 @@ def test_w4_elements_equal_exact_rationals_one_by_one():
     # an index read with M and N exchanged would pick other outputs
     swapped = (idx // (M * N)) * M * N + (idx % N) * M + (idx // N) % M
     assert not np.array_equal(full[swapped], full[idx])
+
+
+# --------------------------------------------------------------------------
+# A16W8: E4M3 weights with E8M0 scales per 32 k
+# --------------------------------------------------------------------------
+def _golden_e4m3():
+    rows = []
+    for line in (GOLDEN / "e4m3_values.txt").read_text().splitlines():
+        if line.startswith("0x"):
+            code, value = line.split()[:2]
+            rows.append((int(code, 16), float(value)))
+    return rows
+
+
+def test_e4m3_decoding_matches_the_hand_derived_table():
+    rows = _golden_e4m3()
+    assert len(rows) >= 18
+    for code, value in rows:
+        got = oracle.e4m3_to_f64(code)
+        assert got == value and math.copysign(1.0, got) == math.copysign(1.0, value), hex(code)
+
+
+def test_e4m3_decoding_matches_torch_on_all_256_codes():
+    """Every code against PyTorch's float8_e4m3fn (a library conversion):
+    the same value, sign of zero included, and not-a-number for 0x7F, 0xFF."""
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([oracle.e4m3_to_f64(c) for c in range(256)])
+    nan = np.isnan(ref)
+    assert nan.sum() == 2 and np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(ref[~nan]))
+
+
+_E4M3_TORCH = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).tolist()
+
+
+def _exact_w8(Aq, As, l, n, k):
+    """The weight from PyTorch's E4M3 conversion (independent of the oracle)
+    and the scale's power of two, as an exact rational."""
+    value = Fraction(_E4M3_TORCH[int(Aq[l, n, k])])
+    return value * Fraction(2) ** (int(As[l, n, k // 32]) - 127)
+
+
+def test_w8_byte_order_and_scale_blocks_on_a_hand_made_row():
+    """Code k of a row is byte k; the scale of k is byte k // 32 of the row's
+    scales.  One-hot activations pick single weights out of the product."""
+    K, N = 64, 2
+    Aq = np.zeros((1, N, K), np.uint8)
+    As = np.full((1, N, K // 32), 127, np.uint8)
+    Aq[0, 0, 0], Aq[0, 0, 1] = 0x38, 0x4B     # 1.0, 5.5
+    Aq[0, 0, 33] = 0xBC                        # -1.5, in the second scale block
+    As[0, 0, 1] = 130                          # x 2^3
+    Aq[0, 1, 63] = 0x01                        # 2^-9
+    As[0, 1, 1] = 120                          # x 2^-7
+    W = oracle.w8_dequant(Aq, As)
+    assert (W[0, 0, 0], W[0, 0, 1], W[0, 0, 33], W[0, 1, 63]) == (1.0, 5.5, -12.0, 2.0 ** -16)
+    M = 4
+    B = np.zeros((1, M, K), np.uint16)
+    for m, k in enumerate([0, 1, 33, 63]):
+        B[0, m, k] = 0x3F80
+    C = oracle.gemm_w8a16(Aq, As, B)
+    expect = [[1.0, 0.0], [5.5, 0.0], [-12.0, 0.0], [0.0, 2.0 ** -16]]
+    for m in range(M):
+        for n in range(N):
+            assert oracle.bf16_to_f64(int(C[0, m, n])) == expect[m][n], (m, n)
+
+
+@pytest.mark.parametrize("L,M,N,K", [(1, 1, 1, 32), (1, 2, 3, 64), (2, 3, 2, 96)])
+def test_w8a16_brute_force_exact_rationals(L, M, N, K):
+    from split_bf16_gemm_swapped_gb300 import synthetic
+    Aq, As = synthetic.w8_weights(L, N, K, seed=91 + K)
+    B = synthetic.normal_bf16((L, M, K), seed=91 + K, stream=1, sigma=1.0)
+    C = oracle.gemm_w8a16(Aq, As, B)
+    for l in range(L):
+        for m in range(M):
+            for n in range(N):
+                s = sum(_exact_w8(Aq, As, l, n, k) * _exact.value(int(B[l, m, k])) for k in range(K))
+                assert C[l, m, n] == _exact.round_bf16(s), (l, m, n)
+
+
+def test_w8a16_equals_the_bf16_gemm_of_its_exact_bf16_weights():
+    """Every weight the 8-bit codes encode (in the scale range used) is a
+    bf16 value (4 significant bits), so the A16W8 product is the bf16
+    oracle's on those weights."""
+    from split_bf16_gemm_swapped_gb300 import synthetic
+    L, M, N, K = 2, 3, 20, 256
+    Aq, As = synthetic.w8_weights(L, N, K, seed=95)
+    B = synthetic.normal_bf16((L, M, K), seed=95, stream=1, sigma=1.0)
+    W = oracle.w8_dequant(Aq, As)
+    Wb = np.vectorize(oracle.f64_to_bf16)(W).astype(np.uint16)
+    assert np.array_equal((Wb.astype(np.uint32) << 16).view(np.float32).astype(np.float64), W)
+    assert np.array_equal(oracle.gemm_w8a16(Aq, As, B), oracle.gemm(Wb, B))
+
+
+def test_w8a16_all_ones_closed_form():
+    """Every weight code 0x38 (1.0) with scale 2^2, every activation 1.0:
+    C = 4 K exactly."""
+    L, M, N, K = 1, 2, 3, 1024
+    Aq = np.full((L, N, K), 0x38, np.uint8)
+    As = np.full((L, N, K // 32), 129, np.uint8)
+    B = np.full((L, M, K), 0x3F80, np.uint16)
+    assert np.all(np.vectorize(oracle.bf16_to_f64)(oracle.gemm_w8a16(Aq, As, B)) == 4.0 * K)
+
+
+def test_w8a16_pins_catch_planted_mistakes():
+    """Altered operands (the mistakes an oracle could make) change the exact
+    result: bytes swapped in pairs, one scale per row, scale blocks reversed."""
+    from split_bf16_gemm_swapped_gb300 import synthetic
+    L, M, N, K = 1, 2, 3, 64
+    Aq, As = synthetic.w8_weights(L, N, K, seed=97)
+    B = synthetic.normal_bf16((L, M, K), seed=97, stream=1, sigma=1.0)
+    exact = np.array([[[_exact.round_bf16(sum(_exact_w8(Aq, As, 0, n, k) * _exact.value(int(B[0, m, k]))
+                                             for k in range(K))) for n in range(N)] for m in range(M)]],
+                     dtype=np.uint16)
+    assert np.array_equal(oracle.gemm_w8a16(Aq, As, B), exact)
+    swapped = np.ascontiguousarray(Aq.reshape(L, N, K // 2, 2)[..., ::-1].reshape(L, N, K))
+    one_scale = np.repeat(As[:, :, :1], K // 32, axis=2)
+    reversed_blocks = np.ascontiguousarray(As[:, :, ::-1])
+    assert np.any(As[:, :, 0] != As[:, :, 1])
+    for name, (q, s) in {"bytes swapped": (swapped, As), "scale per row": (Aq, one_scale),
+                         "scale blocks": (Aq, reversed_blocks)}.items():
+        assert not np.array_equal(oracle.gemm_w8a16(q, s, B), exact), name
