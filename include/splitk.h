@@ -96,6 +96,7 @@ enum splitk_status {
 /* Weight formats (splitk_plan_t.weight_format). */
 #define SPLITK_WEIGHTS_BF16 0        /* A[L][N][K] bf16                              */
 #define SPLITK_WEIGHTS_E2M1_E8M0 1   /* A16W4: codes A_q[L][N][K/2], scales A_s[L][N][K/32] */
+#define SPLITK_WEIGHTS_E4M3_E8M0 2   /* A16W8: codes A_q[L][N][K], scales A_s[L][N][K/32]   */
 
 /*
  * A launch configuration ("tactic": the page's SplitKTactic fields mma_m,
@@ -252,6 +253,39 @@ SPLITK_API int splitk_gemm_w4a16(const void *a_q, const void *a_scale, const voi
                                  void *c, int M, int N, int K, int L, int split_k,
                                  splitk_stream_t stream);
 SPLITK_API int splitk_gemm_w4a16_planned(const void *a_q, const void *a_scale,
+                                         const void *b, void *c, int M, int N, int K,
+                                         int L, const splitk_plan_t *plan,
+                                         unsigned flags, splitk_stream_t stream);
+
+/*
+ * A16W8: C[l][m][n] = bf16_rne( sum_k w(l,n,k) * B[l][m][k] ) with 8-bit
+ * weights: w = e4m3(code) * 2^(scale - 127).  The element format is E4M3,
+ * as the DeepSeek-V4.1 AMD mono ops page's fp8_pack4 packs it ("four E4M3
+ * bytes, RNE"): sign bit 7, exponent bits 6..3 (bias 7), mantissa bits 2..0,
+ * no infinities, 0x7F / 0xFF not a number, largest finite 448.  The block
+ * scale is the one of the 4-bit weights above: one E8M0 code per 32
+ * consecutive k of a row.
+ *   a_q      device, [L][N][K] bytes, one code per k, 16-byte aligned.
+ *   a_scale  device, [L][N][K/32] bytes, 4-byte aligned.  Codes 3..246 keep
+ *            every decoded weight a finite bf16 value with no bits below
+ *            2^-133 (exact); outside that range the decode saturates or
+ *            rounds as bf16 arithmetic does, and the not-a-number codes give
+ *            not-a-number weights.
+ *   b, c     as splitk_gemm_bf16().
+ * K must be a multiple of 128, M at most 32, and a CTA's K slice at most 8
+ * tiles of 128 (else SPLITK_ERR_INVALID_SHAPE / SPLITK_ERR_NO_FIT).  The
+ * plan carries weight_format = SPLITK_WEIGHTS_E4M3_E8M0; otherwise the plan
+ * fields, kernel and tactics are those of the 4-bit weights.
+ */
+SPLITK_API int splitk_plan_w8a16_for(int M, int N, int K, int L, int split_k,
+                                     int num_sms, size_t smem_per_sm,
+                                     size_t smem_per_block_optin, splitk_plan_t *out);
+SPLITK_API int splitk_plan_w8a16(int M, int N, int K, int L, int split_k,
+                                 splitk_plan_t *out);
+SPLITK_API int splitk_gemm_w8a16(const void *a_q, const void *a_scale, const void *b,
+                                 void *c, int M, int N, int K, int L, int split_k,
+                                 splitk_stream_t stream);
+SPLITK_API int splitk_gemm_w8a16_planned(const void *a_q, const void *a_scale,
                                          const void *b, void *c, int M, int N, int K,
                                          int L, const splitk_plan_t *plan,
                                          unsigned flags, splitk_stream_t stream);

@@ -26,6 +26,7 @@ __all__ = [
     "splitk_gemm_bf16_bias",
     "splitk_plan_check_for", "splitk_plan_candidates_for", "splitk_tune",
     "splitk_plan_w4a16", "splitk_plan_w4a16_for", "splitk_gemm_w4a16", "splitk_gemm_w4a16_planned",
+    "splitk_plan_w8a16", "splitk_plan_w8a16_for", "splitk_gemm_w8a16", "splitk_gemm_w8a16_planned",
     "splitk_get_fault",
     "splitk_get_status",
     "splitk_set_wait_limit_ns", "splitk_debug_inject", "splitk_release", "splitk_cache_info",
@@ -124,6 +125,14 @@ def load_library():
     lib.splitk_gemm_w4a16.restype = i
     lib.splitk_gemm_w4a16_planned.argtypes = [vp, vp, vp, vp, i, i, i, i, ctypes.POINTER(Plan), u, vp]
     lib.splitk_gemm_w4a16_planned.restype = i
+    lib.splitk_plan_w8a16_for.argtypes = [i, i, i, i, i, i, sz, sz, ctypes.POINTER(Plan)]
+    lib.splitk_plan_w8a16_for.restype = i
+    lib.splitk_plan_w8a16.argtypes = [i, i, i, i, i, ctypes.POINTER(Plan)]
+    lib.splitk_plan_w8a16.restype = i
+    lib.splitk_gemm_w8a16.argtypes = [vp, vp, vp, vp, i, i, i, i, i, vp]
+    lib.splitk_gemm_w8a16.restype = i
+    lib.splitk_gemm_w8a16_planned.argtypes = [vp, vp, vp, vp, i, i, i, i, ctypes.POINTER(Plan), u, vp]
+    lib.splitk_gemm_w8a16_planned.restype = i
     lib.splitk_plan_check_for.argtypes = [ctypes.POINTER(Plan), i, i, i, i, sz, sz]
     lib.splitk_plan_check_for.restype = i
     lib.splitk_plan_candidates_for.argtypes = [i, i, i, i, i, i, sz, sz, ctypes.POINTER(Plan), i]
@@ -245,6 +254,7 @@ def splitk_gemm_bf16(a, b, c=None, split_k: int = 0, stream=None):
 
 WEIGHTS_BF16 = 0
 WEIGHTS_E2M1_E8M0 = 1
+WEIGHTS_E4M3_E8M0 = 2
 
 
 def splitk_plan_w4a16_for(M: int, N: int, K: int, L: int, split_k: int, num_sms: int,
@@ -308,6 +318,70 @@ def splitk_gemm_w4a16_planned(a_q, a_s, b, c, plan: Plan, flags: int = 0, stream
                                                       c.data_ptr(), M, N, K, L, ctypes.byref(plan),
                                                       int(flags), _stream_handle(stream, b.device))
     _check(rc, "splitk_gemm_w4a16_planned")
+    return c
+
+
+# ---------------------------------------------------------------- A16W8
+def splitk_plan_w8a16_for(M: int, N: int, K: int, L: int, split_k: int, num_sms: int,
+                          smem_per_sm: int, smem_per_block_optin: int) -> Plan:
+    """The A16W8 plan for a described device (no CUDA)."""
+    p = Plan()
+    _check(load_library().splitk_plan_w8a16_for(M, N, K, L, split_k, num_sms, smem_per_sm,
+                                                smem_per_block_optin, ctypes.byref(p)),
+           "splitk_plan_w8a16_for")
+    return p
+
+
+def splitk_plan_w8a16(M: int, N: int, K: int, L: int = 1, split_k: int = 0) -> Plan:
+    p = Plan()
+    _check(load_library().splitk_plan_w8a16(M, N, K, L, split_k, ctypes.byref(p)), "splitk_plan_w8a16")
+    return p
+
+
+def _w8_dims(a_q, a_s, b):
+    import torch
+    if a_q.dtype != torch.uint8 or a_s.dtype != torch.uint8:
+        raise TypeError("A16W8 codes and scales are uint8 tensors")
+    if b.dtype != torch.bfloat16:
+        raise TypeError("b must be bfloat16")
+    if a_q.dim() not in (2, 3) or a_s.dim() != a_q.dim() or b.dim() != a_q.dim():
+        raise ValueError("a_q is [L, N, K] or [N, K], a_s [L, N, K/32] or [N, K/32], b [L, M, K] or [M, K]")
+    if a_q.dim() == 2:
+        a_q, a_s = a_q.unsqueeze(0), a_s.unsqueeze(0)
+    if b.dim() == 2:
+        b = b.unsqueeze(0)
+    L, N, K = a_q.shape
+    if tuple(a_s.shape) != (L, N, K // 32) or b.shape[0] != L or b.shape[2] != K:
+        raise ValueError(f"shape mismatch a_q{tuple(a_q.shape)} a_s{tuple(a_s.shape)} b{tuple(b.shape)}")
+    for t in (a_q, a_s, b):
+        if not t.is_contiguous():
+            raise ValueError("operands must be contiguous")
+    return int(b.shape[1]), N, K, L
+
+
+def splitk_gemm_w8a16(a_q, a_s, b, c=None, split_k: int = 0, stream=None):
+    """c = b @ dequant(a_q, a_s)^T (8-bit E4M3 codes, E8M0 scales per 32 k)."""
+    import torch
+    M, N, K, L = _w8_dims(a_q, a_s, b)
+    _require_cuda(a_q, a_s, b)
+    c = _out(c, b, M, N, L)
+    with torch.cuda.device(b.device):
+        rc = load_library().splitk_gemm_w8a16(a_q.data_ptr(), a_s.data_ptr(), b.data_ptr(), c.data_ptr(),
+                                              M, N, K, L, int(split_k), _stream_handle(stream, b.device))
+    _check(rc, "splitk_gemm_w8a16")
+    return c
+
+
+def splitk_gemm_w8a16_planned(a_q, a_s, b, c, plan: Plan, flags: int = 0, stream=None):
+    import torch
+    M, N, K, L = _w8_dims(a_q, a_s, b)
+    _require_cuda(a_q, a_s, b)
+    c = _out(c, b, M, N, L)
+    with torch.cuda.device(b.device):
+        rc = load_library().splitk_gemm_w8a16_planned(a_q.data_ptr(), a_s.data_ptr(), b.data_ptr(),
+                                                      c.data_ptr(), M, N, K, L, ctypes.byref(plan),
+                                                      int(flags), _stream_handle(stream, b.device))
+    _check(rc, "splitk_gemm_w8a16_planned")
     return c
 
 

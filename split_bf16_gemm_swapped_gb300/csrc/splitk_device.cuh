@@ -288,6 +288,26 @@ __device__ __forceinline__ uint32_t e2m1x2_scaled_bf16x2(uint32_t byte, uint32_t
   return d;
 }
 
+// Two E4M3 codes (the low 16 bits of `pair`; the lower byte is the first
+// element) -> two bf16 values times the power of two `scale2` (a bf16 pair,
+// e8m0_bf16x2), packed with the first in the low half.  The hardware
+// conversion to f16x2 is exact (E4M3 values are f16 values), widening to f32
+// and rounding to bf16 are exact (at most 4 significant bits), and the bf16
+// product by a power of two is exact wherever the result is a finite bf16
+// value with no bits below 2^-133.
+__device__ __forceinline__ uint32_t e4m3x2_scaled_bf16x2(uint32_t pair, uint32_t scale2) {
+  uint32_t h2;
+  asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(h2) : "r"(pair));
+  float lo, hi;
+  asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(h2));
+  uint32_t r, d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(r), "r"(scale2));
+  return d;
+}
+
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }

@@ -75,11 +75,16 @@ uint32_t mailbox_round_bytes(int split, int quads, int ncols_max) {
   return (uint32_t)(split - 1) * (uint32_t)cols * kColumnBytes;
 }
 
-// Shared memory of an A16W4 plan's layout: all packed weight tiles, all
-// activation tiles (at least 2: rank 0's f32 staging tile reuses them), the
-// mailbox and the barriers.
-size_t smem_bytes_w4(int mma_n, int k_tiles, uint32_t dedicated_mailbox_bytes, int smem_tiles) {
-  return (size_t)kAlignSlack + (size_t)k_tiles * kW4TileBytes +
+// Bytes of one packed K tile of quantized weights (E2M1: 8 KiB, E4M3: 16 KiB).
+inline uint32_t q_tile_bytes(int fmt) { return fmt == SPLITK_WEIGHTS_E4M3_E8M0 ? kW8TileBytes : kW4TileBytes; }
+inline bool is_quantized(int fmt) { return fmt == SPLITK_WEIGHTS_E2M1_E8M0 || fmt == SPLITK_WEIGHTS_E4M3_E8M0; }
+
+// Shared memory of a quantized-weight plan's layout: all packed weight
+// tiles, all activation tiles (at least 2: rank 0's f32 staging tile reuses
+// them), the mailbox and the barriers.
+size_t smem_bytes_w4(int mma_n, int k_tiles, uint32_t dedicated_mailbox_bytes, int smem_tiles,
+                     int fmt = SPLITK_WEIGHTS_E2M1_E8M0) {
+  return (size_t)kAlignSlack + (size_t)k_tiles * q_tile_bytes(fmt) +
          (size_t)std::max(2, k_tiles) * b_stage_bytes(mma_n) + (size_t)smem_tiles * kAStageBytes +
          dedicated_mailbox_bytes + kBarRegionBytes;
 }
@@ -423,7 +428,7 @@ int plan_ring_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t 
 // columns).  Shared memory is padded when needed so that the
 // CTAs fitting an SM can hold their TMEM.
 int plan_w4_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t smem_per_sm, size_t smem_optin,
-                 splitk_plan_t* out) {
+                 splitk_plan_t* out, int fmt = SPLITK_WEIGHTS_E2M1_E8M0) {
   if (!out) return SPLITK_ERR_NULL;
   if (M < 1 || N < 1 || K < 1 || L < 1 || M > 32 || K % kCtaK != 0 || K > kMaxK) return SPLITK_ERR_INVALID_SHAPE;
   if (split_k != 0 && !valid_split(split_k)) return SPLITK_ERR_UNSUPPORTED_SPLIT;
@@ -465,13 +470,13 @@ int plan_w4_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t sm
   p.tmem_cols = tmem_cols_for(mma_n, p.a_tmem_tiles, p.mma_issuers);
   p.b_loader = 0;             // the epilogue threads are busy decoding (measured: TMA is faster here)
   p.l2_prefetch = 0;
-  p.weight_format = SPLITK_WEIGHTS_E2M1_E8M0;
+  p.weight_format = fmt;
   const uint32_t ded = w4_mailbox_bytes(split, p.reduce_scatter, ncols_max);
   // One tile past the TMEM slots: decode it into a bf16 stage in shared
   // memory, before the PDL wait, if that still fits 2 CTAs per SM
   // (the single-token decode case: 4 K tiles per CTA, 3 slots).
   p.w4_smem_tiles = kt == p.a_tmem_tiles + 1 &&
-                            smem_bytes_w4(mma_n, kt, ded, 1) + 1024 <= smem_per_sm / 2
+                            smem_bytes_w4(mma_n, kt, ded, 1, fmt) + 1024 <= smem_per_sm / 2
                         ? 1
                         : 0;
   // A second decoding warpgroup halves every tile's decode (384 threads a
@@ -490,14 +495,14 @@ int plan_w4_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t sm
     }
     return smem;
   };
-  size_t smem = padded_smem(smem_bytes_w4(mma_n, kt, ded, p.w4_smem_tiles), p.tmem_cols);
+  size_t smem = padded_smem(smem_bytes_w4(mma_n, kt, ded, p.w4_smem_tiles, fmt), p.tmem_cols);
   // Grids of more than two waves: one TMEM slot and one issuer when that lets
   // more CTAs share an SM (at most 3 by registers), so that their decodes
   // overlap (single-token decode, L=8: 49.1 -> 46.2 us).
   const long long ctas = (long long)split * m_tiles * n_tiles * L;
   if (ctas > 2LL * num_sms && p.a_tmem_tiles > 1) {
     const uint32_t cols1 = tmem_cols_for(mma_n, 1, 1);
-    const size_t smem1 = padded_smem(smem_bytes_w4(mma_n, kt, ded, 0), cols1);
+    const size_t smem1 = padded_smem(smem_bytes_w4(mma_n, kt, ded, 0, fmt), cols1);
     if (std::min(3, resident_by_smem(smem_per_sm, smem1)) > std::min(2, resident_by_smem(smem_per_sm, smem))) {
       p.a_tmem_tiles = 1;
       p.mma_issuers = 1;
@@ -552,7 +557,7 @@ int check_plan_w4(const splitk_plan_t& pl, int M, int N, int K, int L, size_t sm
   // round it never had)
   if (pl.w4_smem_tiles != 0 && (pl.w4_smem_tiles != 1 || kt != pl.a_tmem_tiles + 1)) return SPLITK_ERR_BAD_PLAN;
   const uint32_t ded = w4_mailbox_bytes(pl.split_k, pl.reduce_scatter, ncols_max);
-  if (pl.smem_bytes < smem_bytes_w4(pl.mma_n, kt, ded, pl.w4_smem_tiles) || pl.smem_bytes % 16 != 0) {
+  if (pl.smem_bytes < smem_bytes_w4(pl.mma_n, kt, ded, pl.w4_smem_tiles, pl.weight_format) || pl.smem_bytes % 16 != 0) {
     return SPLITK_ERR_BAD_PLAN;
   }
   if (pl.smem_bytes > smem_optin) return SPLITK_ERR_NO_FIT;
@@ -600,7 +605,7 @@ int check_plan_persistent(const splitk_plan_t& pl, int M, int N, int K, int L, s
 
 int check_plan(const splitk_plan_t& pl, int M, int N, int K, int L, size_t smem_optin,
                size_t smem_per_sm, uint32_t* dedicated_bytes) {
-  if (pl.weight_format == SPLITK_WEIGHTS_E2M1_E8M0) {
+  if (is_quantized(pl.weight_format)) {
     return check_plan_w4(pl, M, N, K, L, smem_optin, smem_per_sm, dedicated_bytes);
   }
   if (pl.weight_format != SPLITK_WEIGHTS_BF16 || pl.w4_smem_tiles != 0 || pl.w4_decoders != 0) {
@@ -704,19 +709,22 @@ bool encode_3d(CUtensorMap* map, const void* ptr, uint64_t d0, uint64_t d1, uint
   return r == CUDA_SUCCESS;
 }
 
-// A16W4 codes [L][N][K/2] bytes read in boxes of {64 B, 128 rows, 1} with
-// the 64-byte swizzle (each decoding thread reads its row conflict-free);
-// out-of-range rows read as zero codes.
-bool encode_3d_w4(CUtensorMap* map, const void* ptr, uint64_t row_bytes, uint64_t d1, uint64_t d2) {
+// Quantized weight codes [L][N][row_bytes] read in boxes of one packed K
+// tile by 128 rows: A16W4 {64 B, 128, 1} with the 64-byte swizzle, A16W8
+// {128 B, 128, 1} with the 128-byte swizzle (each decoding thread reads its
+// row conflict-free); out-of-range rows read as zero codes.
+bool encode_3d_w4(CUtensorMap* map, const void* ptr, uint64_t row_bytes, uint64_t d1, uint64_t d2,
+                  int fmt = SPLITK_WEIGHTS_E2M1_E8M0) {
   auto fn = encode_fn();
   if (!fn) return false;
+  const bool w8 = fmt == SPLITK_WEIGHTS_E4M3_E8M0;
   cuuint64_t dims[3] = {row_bytes, d1, d2};
   cuuint64_t strides[2] = {row_bytes, row_bytes * d1};
-  cuuint32_t box[3] = {kW4RowBytes, (cuuint32_t)kMmaM, 1u};
+  cuuint32_t box[3] = {w8 ? kW8RowBytes : kW4RowBytes, (cuuint32_t)kMmaM, 1u};
   cuuint32_t estr[3] = {1u, 1u, 1u};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, w8 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -842,9 +850,11 @@ int a_map_for(DeviceState& st, const void* a, int N, int K, int L, cudaStream_t 
   }
   if (st.used >= kMapPoolSlots) return SPLITK_ERR_CACHE_FULL;
   const int slot = st.used;
-  const bool encoded = fmt == SPLITK_WEIGHTS_E2M1_E8M0
-                           ? encode_3d_w4(&st.h_pool[slot], a, (uint64_t)K / 2u, (uint64_t)N, (uint64_t)L)
-                           : encode_3d(&st.h_pool[slot], a, (uint64_t)K, (uint64_t)N, (uint64_t)L, (uint32_t)kMmaM);
+  const bool encoded =
+      fmt == SPLITK_WEIGHTS_E2M1_E8M0   ? encode_3d_w4(&st.h_pool[slot], a, (uint64_t)K / 2u, (uint64_t)N, (uint64_t)L)
+      : fmt == SPLITK_WEIGHTS_E4M3_E8M0 ? encode_3d_w4(&st.h_pool[slot], a, (uint64_t)K, (uint64_t)N, (uint64_t)L, fmt)
+                                        : encode_3d(&st.h_pool[slot], a, (uint64_t)K, (uint64_t)N, (uint64_t)L,
+                                                    (uint32_t)kMmaM);
   if (!encoded) return SPLITK_ERR_CUDA;
   // Outside a graph capture the copy completes before this returns, so a
   // launch on any stream may use the slot from now on; inside a capture it
@@ -914,7 +924,7 @@ void fill_params(const splitk_plan_t& pl, int M, int N, int K, int L, uint32_t d
   p->pdl_trigger_early = pl.pdl_trigger;
   p->reduce_scatter = pl.reduce_scatter;
   p->b_resident = pl.b_resident;
-  p->b_region_tiles = pl.weight_format == SPLITK_WEIGHTS_E2M1_E8M0
+  p->b_region_tiles = is_quantized(pl.weight_format)
                           ? std::max(2, pl.k_tiles_per_cta)
                           : b_region_tiles_for(pl.stages, pl.b_resident, pl.k_tiles_per_cta);
   p->a_tmem_tiles = pl.a_tmem_tiles;
@@ -931,7 +941,7 @@ void fill_params(const splitk_plan_t& pl, int M, int N, int K, int L, uint32_t d
 LaunchArgs launch_args(const splitk_plan_t& pl, bool pdl) {
   LaunchArgs la;
   la.mma_n = pl.mma_n;
-  la.w4 = pl.weight_format == SPLITK_WEIGHTS_E2M1_E8M0;
+  la.fmt = pl.weight_format == SPLITK_WEIGHTS_E2M1_E8M0 ? 1 : pl.weight_format == SPLITK_WEIGHTS_E4M3_E8M0 ? 2 : 0;
   la.persistent = pl.persistent != 0;
   la.w4_decoders = pl.w4_decoders == 2 ? 2 : 1;
   la.grid = dim3(pl.grid[0], pl.grid[1], pl.grid[2]);
@@ -965,7 +975,7 @@ int launch_locked(DeviceState& st, const void* a, const void* b, void* c, int M,
   int rc = check_plan(pl, M, N, K, L, st.smem_optin, st.smem_per_sm, &ded);
   if (rc != SPLITK_OK) return rc;
   // the A16W4 kernel needs its scales; the bf16 kernel takes none
-  if ((pl.weight_format == SPLITK_WEIGHTS_E2M1_E8M0) != (a_scale != nullptr)) return SPLITK_ERR_BAD_PLAN;
+  if (is_quantized(pl.weight_format) != (a_scale != nullptr)) return SPLITK_ERR_BAD_PLAN;
   const CUtensorMap* a_map = nullptr;
   rc = a_map_for(st, a, N, K, L, stream, &a_map, pl.weight_format);
   if (rc != SPLITK_OK) return rc;
@@ -1345,6 +1355,56 @@ SPLITK_API int splitk_gemm_w4a16(const void* a_q, const void* a_scale, const voi
   if (rc != SPLITK_OK) return rc;
   splitk_plan_t pl;
   rc = plan_w4_impl(M, N, K, L, split_k, st->num_sms, st->smem_per_sm, st->smem_optin, &pl);
+  if (rc != SPLITK_OK) return rc;
+  return launch_locked(*st, a_q, b, c, M, N, K, L, pl, 0u, reinterpret_cast<cudaStream_t>(stream), nullptr,
+                       a_scale);
+}
+
+SPLITK_API int splitk_plan_w8a16_for(int M, int N, int K, int L, int split_k, int num_sms, size_t smem_per_sm,
+                                     size_t smem_per_block_optin, splitk_plan_t* out) {
+  return plan_w4_impl(M, N, K, L, split_k, num_sms, smem_per_sm, smem_per_block_optin, out, SPLITK_WEIGHTS_E4M3_E8M0);
+}
+
+SPLITK_API int splitk_plan_w8a16(int M, int N, int K, int L, int split_k, splitk_plan_t* out) {
+  if (!out) return SPLITK_ERR_NULL;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* st = nullptr;
+  int rc = current_device(&st, nullptr);
+  if (rc != SPLITK_OK) return rc;
+  return plan_w4_impl(M, N, K, L, split_k, st->num_sms, st->smem_per_sm, st->smem_optin, out,
+                      SPLITK_WEIGHTS_E4M3_E8M0);
+}
+
+SPLITK_API int splitk_gemm_w8a16_planned(const void* a_q, const void* a_scale, const void* b, void* c, int M,
+                                         int N, int K, int L, const splitk_plan_t* plan, unsigned flags,
+                                         splitk_stream_t stream) {
+  if (!plan || !a_scale) return SPLITK_ERR_NULL;
+  int rc = check_pointers(a_q, b, c);
+  if (rc != SPLITK_OK) return rc;
+  if ((uintptr_t)a_scale & 3u) return SPLITK_ERR_MISALIGNED;
+  if (M < 1 || N < 1 || K < 1 || L < 1) return SPLITK_ERR_INVALID_SHAPE;
+  if (plan->weight_format != SPLITK_WEIGHTS_E4M3_E8M0) return SPLITK_ERR_BAD_PLAN;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* st = nullptr;
+  rc = current_device(&st, nullptr);
+  if (rc != SPLITK_OK) return rc;
+  return launch_locked(*st, a_q, b, c, M, N, K, L, *plan, flags, reinterpret_cast<cudaStream_t>(stream), nullptr,
+                       a_scale);
+}
+
+SPLITK_API int splitk_gemm_w8a16(const void* a_q, const void* a_scale, const void* b, void* c, int M, int N,
+                                 int K, int L, int split_k, splitk_stream_t stream) {
+  if (!a_scale) return SPLITK_ERR_NULL;
+  int rc = check_pointers(a_q, b, c);
+  if (rc != SPLITK_OK) return rc;
+  if ((uintptr_t)a_scale & 3u) return SPLITK_ERR_MISALIGNED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* st = nullptr;
+  rc = current_device(&st, nullptr);
+  if (rc != SPLITK_OK) return rc;
+  splitk_plan_t pl;
+  rc = plan_w4_impl(M, N, K, L, split_k, st->num_sms, st->smem_per_sm, st->smem_optin, &pl,
+                    SPLITK_WEIGHTS_E4M3_E8M0);
   if (rc != SPLITK_OK) return rc;
   return launch_locked(*st, a_q, b, c, M, N, K, L, pl, 0u, reinterpret_cast<cudaStream_t>(stream), nullptr,
                        a_scale);

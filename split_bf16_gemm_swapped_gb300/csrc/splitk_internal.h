@@ -37,6 +37,10 @@ __host__ __device__ constexpr uint32_t b_stage_bytes(int mma_n) { return (uint32
 // k) are read by the decoding threads.
 constexpr uint32_t kW4TileBytes = kMmaM * kCtaK / 2;       // 8 KiB
 constexpr uint32_t kW4RowBytes = kCtaK / 2;                 // 64
+// A16W8 weights: 128 rows x 128 E4M3 codes = 128 rows of 128 bytes (one TMA
+// box, 128-byte swizzle), the same 4 scale codes per row and K tile.
+constexpr uint32_t kW8TileBytes = kMmaM * kCtaK;           // 16 KiB
+constexpr uint32_t kW8RowBytes = kCtaK;                     // 128
 
 // Tensor memory: one accumulator per MMA issuer, max(32, mma_n) columns
 // each, from column 0; weight K tiles staged in tensor memory (64 columns
@@ -128,7 +132,7 @@ enum TraceSlot : int {
 
 struct LaunchArgs {
   int mma_n;
-  bool w4;                    // A16W4 weights
+  int fmt;                    // 0 bf16 weights, 1 E2M1 codes, 2 E4M3 codes (with E8M0 scales)
   bool persistent;            // the persistent kernel (grid = (split, clusters, 1))
   int w4_decoders;            // A16W4: decoding warpgroups (1 or 2)
   dim3 grid;

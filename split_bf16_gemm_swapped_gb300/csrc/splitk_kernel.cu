@@ -48,16 +48,21 @@
 
 namespace splitk {
 
-// kDecWG: warpgroups decoding A16W4 weight tiles (1: warps 4..7, the
-// epilogue; 2: also warps 8..11, each group decoding half of every tile's K).
-template <int MMA_N, bool kW4, int kDecWG>
+// kFmt: the weight format (0 bf16; 1 E2M1 codes, 2 E4M3 codes, each with
+// E8M0 scales per 32 k, decoded on chip).  kDecWG: warpgroups decoding
+// quantized weight tiles (1: warps 4..7, the epilogue; 2: also warps 8..11,
+// each group decoding half of every tile's K).
+template <int MMA_N, int kFmt, int kDecWG>
 __global__ void __launch_bounds__(kDecWG == 2 ? kThreadsW4Wide : kThreads, kDecWG == 2 ? 2 : 3)
     splitk_gemm_bf16_kernel(const __grid_constant__ CUtensorMap b_map, const KernelParams p) {
+  constexpr bool kW4 = kFmt != 0;                           // quantized weights, decoded on chip
+  constexpr uint32_t kQTileBytes = kFmt == 2 ? kW8TileBytes : kW4TileBytes;   // one packed K tile
+  constexpr uint32_t kQRowBytes = kFmt == 2 ? kW8RowBytes : kW4RowBytes;      // one row of it
   constexpr uint32_t kBStage = b_stage_bytes(MMA_N);
   constexpr uint32_t kBBox = kBStage / 2;                   // MMA_N rows x 128 B
   constexpr uint32_t kAccCols = tmem_acc_cols(MMA_N);       // TMEM columns of one accumulator
   constexpr uint32_t kIdesc = dev::idesc_bf16_f32(kMmaM, MMA_N);
-  constexpr uint32_t kAStage = kW4 ? kW4TileBytes : kAStageBytes;   // one weight K tile in shared memory
+  constexpr uint32_t kAStage = kW4 ? kQTileBytes : kAStageBytes;   // one weight K tile in shared memory
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = dev::smem_u32(smem_raw);
@@ -161,11 +166,12 @@ __global__ void __launch_bounds__(kDecWG == 2 ? kThreadsW4Wide : kThreads, kDecW
   }
   dev::cluster_arrive_release();
   if (kW4 && threadIdx.x == 0) {
-    // every packed weight tile of the CTA at once: one 8 KiB box each
+    // every packed weight tile of the CTA at once: one box each (8 KiB of
+    // 4-bit codes or 16 KiB of 8-bit ones)
     for (; a_issued < k_tiles; ++a_issued) {
       const uint32_t full = bar_full0 + 8u * a_issued;
-      dev::mbar_arrive_expect_tx(full, kW4TileBytes);
-      dev::tma_load_3d_hint(sA + (uint32_t)a_issued * kW4TileBytes, p.a_map, (kt0 + a_issued) * (int)kW4RowBytes,
+      dev::mbar_arrive_expect_tx(full, kQTileBytes);
+      dev::tma_load_3d_hint(sA + (uint32_t)a_issued * kQTileBytes, p.a_map, (kt0 + a_issued) * (int)kQRowBytes,
                             n0, l, full, a_policy);
     }
     stamp(p, kTrPrefetched);
@@ -207,40 +213,51 @@ __global__ void __launch_bounds__(kDecWG == 2 ? kThreadsW4Wide : kThreads, kDecW
   }
   if (threadIdx.x == 128) stamp(p, kTrEpiSynced);
 
-  // A16W4 decode of the 32-k chunks [j0, j1) of weight row `row` of packed
-  // tile kt (64 B of the tile's 64-byte-swizzled row: chunk j sits at 16-byte
-  // slot j ^ ((row >> 1) & 3)), each chunk one scale block (scale code byte j
-  // of `codes`): a byte becomes two bf16 through the hardware E2M1 -> f16
-  // conversion, an exact rounding to bf16 and an exact bf16 product with the
-  // block's power of two.  Into TMEM columns t_col + 16 j of the thread's
-  // lane, or into the bf16 stage in shared memory in the 128-byte-swizzled
-  // layout of the bf16 path (two boxes of 64 k; 16-byte chunk c of row r of
-  // an 8-row atom at chunk c ^ (r % 8)), read by the MMA from there.
+  // Decode of the 32-k steps [j0, j1) of weight row `row` of packed tile kt,
+  // each step one scale block (scale code byte j of `codes`), into 16 words
+  // of bf16 pairs: E2M1 codes are 64 B a row in the 64-byte swizzle (step j
+  // is the 16-byte chunk at slot j ^ ((row >> 1) & 3)), a byte -> two bf16;
+  // E4M3 codes are 128 B a row in the 128-byte swizzle (step j is chunks 2j
+  // and 2j + 1 at slots c ^ (row & 7)), two bytes -> two bf16.  Both go
+  // through the hardware conversion to f16 (exact), an exact rounding to
+  // bf16 and an exact bf16 product with the block's power of two.
+  auto q_decode_step = [&](uint32_t src, int j, int row, uint32_t scale, uint32_t (&r)[16]) {
+    if constexpr (kFmt == 2) {
+      uint32_t w[8];
+      dev::ld_shared_v4(src + (uint32_t)(((2 * j) ^ (row & 7)) * 16), w[0], w[1], w[2], w[3]);
+      dev::ld_shared_v4(src + (uint32_t)(((2 * j + 1) ^ (row & 7)) * 16), w[4], w[5], w[6], w[7]);
+#pragma unroll
+      for (int q = 0; q < 16; ++q) r[q] = dev::e4m3x2_scaled_bf16x2(w[q >> 1] >> (16 * (q & 1)), scale);
+    } else {
+      uint32_t w[4];
+      dev::ld_shared_v4(src + (uint32_t)((j ^ ((row >> 1) & 3)) * 16), w[0], w[1], w[2], w[3]);
+#pragma unroll
+      for (int q = 0; q < 16; ++q) r[q] = dev::e2m1x2_scaled_bf16x2(w[q >> 2] >> (8 * (q & 3)), scale);
+    }
+  };
+  // Into TMEM columns t_col + 16 j of the thread's lane, or into the bf16
+  // stage in shared memory in the 128-byte-swizzled layout of the bf16 path
+  // (two boxes of 64 k; 16-byte chunk c of row r of an 8-row atom at chunk
+  // c ^ (r % 8)), read by the MMA from there.
   auto w4_decode_tmem = [&](int kt, int row, uint32_t codes, uint32_t t_col, int j0, int j1) {
-    const uint32_t src = sA + (uint32_t)kt * kW4TileBytes + (uint32_t)row * kW4RowBytes;
+    const uint32_t src = sA + (uint32_t)kt * kQTileBytes + (uint32_t)row * kQRowBytes;
 #pragma unroll 1
     for (int j = j0; j < j1; ++j) {
       const uint32_t scale = dev::e8m0_bf16x2((codes >> (8 * j)) & 0xFFu);   // 2^(code - 127)
-      uint32_t w[4];
-      dev::ld_shared_v4(src + (uint32_t)((j ^ ((row >> 1) & 3)) * 16), w[0], w[1], w[2], w[3]);
       uint32_t r[16];
-#pragma unroll
-      for (int q = 0; q < 16; ++q) r[q] = dev::e2m1x2_scaled_bf16x2(w[q >> 2] >> (8 * (q & 3)), scale);
+      q_decode_step(src, j, row, scale, r);
       __syncwarp();   // tcgen05.st is warp-collective
       dev::tmem_st_x16(t_col + (uint32_t)(j * 16), r);
     }
   };
   auto w4_decode_stage = [&](int kt, int row, uint32_t codes, int j0, int j1) {
-    const uint32_t src = sA + (uint32_t)kt * kW4TileBytes + (uint32_t)row * kW4RowBytes;
+    const uint32_t src = sA + (uint32_t)kt * kQTileBytes + (uint32_t)row * kQRowBytes;
     const uint32_t atom = sW4Stage + (uint32_t)(row >> 3) * 1024u + (uint32_t)(row & 7) * 128u;
 #pragma unroll 1
     for (int j = j0; j < j1; ++j) {
       const uint32_t scale = dev::e8m0_bf16x2((codes >> (8 * j)) & 0xFFu);
-      uint32_t w[4];
-      dev::ld_shared_v4(src + (uint32_t)((j ^ ((row >> 1) & 3)) * 16), w[0], w[1], w[2], w[3]);
       uint32_t r[16];
-#pragma unroll
-      for (int q = 0; q < 16; ++q) r[q] = dev::e2m1x2_scaled_bf16x2(w[q >> 2] >> (8 * (q & 3)), scale);
+      q_decode_step(src, j, row, scale, r);
       // k = 32 j .. 32 j + 31: box j / 2, chunks 4 (j % 2) .. + 3
       const uint32_t box = atom + (uint32_t)(j >> 1) * kABoxBytes;
 #pragma unroll
@@ -877,7 +894,7 @@ __global__ void __launch_bounds__(kDecWG == 2 ? kThreadsW4Wide : kThreads, kDecW
 // ---------------------------------------------------------------- host side
 namespace {
 
-template <int MMA_N, bool kW4, int kDecWG = 1>
+template <int MMA_N, int kFmt, int kDecWG = 1>
 cudaError_t launch_t(const LaunchArgs& la, const CUtensorMap& b_map, const KernelParams& p,
                      cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
@@ -899,53 +916,65 @@ cudaError_t launch_t(const LaunchArgs& la, const CUtensorMap& b_map, const Kerne
   }
   cfg.attrs = attrs;
   cfg.numAttrs = n;
-  return cudaLaunchKernelEx(&cfg, splitk_gemm_bf16_kernel<MMA_N, kW4, kDecWG>, b_map, p);
+  return cudaLaunchKernelEx(&cfg, splitk_gemm_bf16_kernel<MMA_N, kFmt, kDecWG>, b_map, p);
 }
 
-template <int MMA_N, bool kW4, int kDecWG = 1>
+template <int MMA_N, int kFmt, int kDecWG = 1>
 cudaError_t prepare_t(int max_dynamic_smem) {
-  return cudaFuncSetAttribute(splitk_gemm_bf16_kernel<MMA_N, kW4, kDecWG>,
+  return cudaFuncSetAttribute(splitk_gemm_bf16_kernel<MMA_N, kFmt, kDecWG>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, max_dynamic_smem);
+}
+
+template <int kFmt>
+cudaError_t launch_quantized(const LaunchArgs& la, const CUtensorMap& b_map, const KernelParams& p,
+                             cudaStream_t stream) {
+  // quantized weights: decode-sized tiles only
+  if (la.w4_decoders == 2) {
+    switch (la.mma_n) {
+      case 16: return launch_t<16, kFmt, 2>(la, b_map, p, stream);
+      case 32: return launch_t<32, kFmt, 2>(la, b_map, p, stream);
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  switch (la.mma_n) {
+    case 16: return launch_t<16, kFmt>(la, b_map, p, stream);
+    case 32: return launch_t<32, kFmt>(la, b_map, p, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <int kFmt>
+cudaError_t prepare_quantized(int max_dynamic_smem) {
+  cudaError_t e;
+  if ((e = prepare_t<16, kFmt>(max_dynamic_smem)) != cudaSuccess) return e;
+  if ((e = prepare_t<32, kFmt>(max_dynamic_smem)) != cudaSuccess) return e;
+  if ((e = prepare_t<16, kFmt, 2>(max_dynamic_smem)) != cudaSuccess) return e;
+  return prepare_t<32, kFmt, 2>(max_dynamic_smem);
 }
 
 }  // namespace
 
 cudaError_t launch_kernel(const LaunchArgs& la, const CUtensorMap& b_map, const KernelParams& p,
                           cudaStream_t stream) {
-  if (la.w4) {
-    // A16W4 weights: decode-sized tiles only
-    if (la.w4_decoders == 2) {
-      switch (la.mma_n) {
-        case 16: return launch_t<16, true, 2>(la, b_map, p, stream);
-        case 32: return launch_t<32, true, 2>(la, b_map, p, stream);
-        default: return cudaErrorInvalidValue;
-      }
-    }
-    switch (la.mma_n) {
-      case 16: return launch_t<16, true>(la, b_map, p, stream);
-      case 32: return launch_t<32, true>(la, b_map, p, stream);
-      default: return cudaErrorInvalidValue;
-    }
-  }
+  if (la.fmt == 1) return launch_quantized<1>(la, b_map, p, stream);
+  if (la.fmt == 2) return launch_quantized<2>(la, b_map, p, stream);
   switch (la.mma_n) {
-    case 16: return launch_t<16, false>(la, b_map, p, stream);
-    case 32: return launch_t<32, false>(la, b_map, p, stream);
-    case 64: return launch_t<64, false>(la, b_map, p, stream);
-    case 128: return launch_t<128, false>(la, b_map, p, stream);
+    case 16: return launch_t<16, 0>(la, b_map, p, stream);
+    case 32: return launch_t<32, 0>(la, b_map, p, stream);
+    case 64: return launch_t<64, 0>(la, b_map, p, stream);
+    case 128: return launch_t<128, 0>(la, b_map, p, stream);
     default: return cudaErrorInvalidValue;
   }
 }
 
 cudaError_t prepare_kernels(int max_dynamic_smem) {
   cudaError_t e;
-  if ((e = prepare_t<16, false>(max_dynamic_smem)) != cudaSuccess) return e;
-  if ((e = prepare_t<32, false>(max_dynamic_smem)) != cudaSuccess) return e;
-  if ((e = prepare_t<64, false>(max_dynamic_smem)) != cudaSuccess) return e;
-  if ((e = prepare_t<128, false>(max_dynamic_smem)) != cudaSuccess) return e;
-  if ((e = prepare_t<16, true>(max_dynamic_smem)) != cudaSuccess) return e;
-  if ((e = prepare_t<32, true>(max_dynamic_smem)) != cudaSuccess) return e;
-  if ((e = prepare_t<16, true, 2>(max_dynamic_smem)) != cudaSuccess) return e;
-  return prepare_t<32, true, 2>(max_dynamic_smem);
+  if ((e = prepare_t<16, 0>(max_dynamic_smem)) != cudaSuccess) return e;
+  if ((e = prepare_t<32, 0>(max_dynamic_smem)) != cudaSuccess) return e;
+  if ((e = prepare_t<64, 0>(max_dynamic_smem)) != cudaSuccess) return e;
+  if ((e = prepare_t<128, 0>(max_dynamic_smem)) != cudaSuccess) return e;
+  if ((e = prepare_quantized<1>(max_dynamic_smem)) != cudaSuccess) return e;
+  return prepare_quantized<2>(max_dynamic_smem);
 }
 
 cudaError_t read_and_clear_fault(int* out_words) {

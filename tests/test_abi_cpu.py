@@ -526,3 +526,24 @@ def test_w4a16_plans_reject_what_the_kernel_cannot_do():
     assert e.value.code == -4
     p = sk.splitk_plan_w4a16_for(1, 256, 128 * 20, 1, 0, **GB300)  # the plan raises the split
     assert p.k_tiles_per_cta <= 8
+
+
+@pytest.mark.parametrize("args", [(1, 7168, 2048, 1, 4), (16, 4096, 7168, 1, 8), (4, 256, 1024, 1, 0),
+                                  (32, 1000, 4096, 2, 0)])
+def test_w8a16_plans(args):
+    M, N, K, L, split = args
+    p = sk.splitk_plan_w8a16_for(*args, **GB300)
+    assert p.weight_format == sk.WEIGHTS_E4M3_E8M0
+    assert p.stages == p.k_tiles_per_cta <= 8 and p.b_resident == 1
+    assert 1 <= p.a_tmem_tiles <= 3 and p.mma_n in (16, 32) and p.w4_decoders in (1, 2)
+    assert _check(p, M, N, K, L) == 0
+    # 16 KiB of codes a K tile: the layout holds them all
+    b_tiles = max(2, p.k_tiles_per_cta)
+    assert p.smem_bytes >= 1024 + p.k_tiles_per_cta * 16384 + b_tiles * p.mma_n * 256 + p.w4_smem_tiles * 32768
+    # a 4-bit plan of the same shape is not an 8-bit one
+    w4 = sk.splitk_plan_w4a16_for(*args, **GB300)
+    bad = sk.Plan.from_buffer_copy(w4)
+    bad.weight_format = sk.WEIGHTS_E4M3_E8M0
+    assert _check(bad, M, N, K, L) in (0, -10)     # accepted only if its shared memory holds 8-bit tiles
+    if w4.smem_bytes < p.smem_bytes - 32768:
+        assert _check(bad, M, N, K, L) == -10

@@ -784,3 +784,113 @@ def test_w4a16_scale_codes_outside_the_contract_decode_as_documented():
                 assert np.isnan(got[n]), (code, n)
             else:
                 assert got[n] == dec * 32 * 2.0 ** -10, (code, n, got[n], dec)
+
+
+# ---------------------------------------------------------------- A16W8 (E4M3 weights)
+def _w8_draw(L, M, N, K, seed):
+    aq, a_s = synthetic.w8_weights(L, N, K, seed)
+    b = synthetic.normal_bf16((L, M, K), seed, synthetic.STREAM_B, 1.0)
+    return aq, a_s, b
+
+
+@pytest.mark.parametrize("M,N,K,split", [(1, 300, 1024, 4), (4, 256, 1024, 1), (16, 200, 2048, 8),
+                                         (5, 384, 3072, 4), (32, 256, 1024, 2), (17, 300, 896, 1),
+                                         (1, 7168, 2048, 4), (16, 4096, 7168, 8)])
+def test_w8a16_matches_the_oracle(M, N, K, split):
+    L = 2 if N < 1000 else 1
+    aq, a_s, b = _w8_draw(L, M, N, K, seed=3200 + M + K)
+    tc = sk.splitk_gemm_w8a16(_u8_dev(aq), _u8_dev(a_s), to_dev(b), split_k=split)
+    torch.cuda.synchronize()
+    assert sk.splitk_get_status() == 0, sk.splitk_get_fault()
+    ref = oracle.gemm_w8a16(aq, a_s, b)
+    max_w = float(np.max(np.abs(oracle.w8_dequant(aq, a_s))))
+    ok, rep = _tol.check(to_host(tc), ref, K, max_w, _tol.max_abs_bf16(b))
+    assert ok, rep
+
+
+@pytest.mark.parametrize("M,split", [(1, 4), (8, 2), (16, 8), (32, 2)])
+def test_w8a16_equals_the_bf16_kernel_on_the_decoded_weights(M, split):
+    """Every E4M3 weight times its power of two is an exact bf16 value, so
+    the A16W8 product equals, bit for bit, the bf16 kernel's on the decoded
+    weights with as many MMA issuers, and with one or two decoding
+    warpgroups."""
+    L, N, K = 1, 256, 2048
+    aq, a_s, b = _w8_draw(L, M, N, K, seed=3300 + M)
+    wb = np.vectorize(oracle.f64_to_bf16)(oracle.w8_dequant(aq, a_s)).astype(np.uint16)
+    ta, ts, tb = _u8_dev(aq), _u8_dev(a_s), to_dev(b)
+    w8 = sk.splitk_plan_w8a16(M, N, K, L, split)
+    assert w8.weight_format == sk.WEIGHTS_E4M3_E8M0
+    for issuers in (1, 2):
+        if issuers > w8.a_tmem_tiles:
+            continue
+        for decoders in (1, 2):
+            p8 = _w4_variant(w8, w8.a_tmem_tiles, w8.w4_smem_tiles, w8.b_loader, issuers, decoders)
+            c8 = to_host(sk.splitk_gemm_w8a16_planned(ta, ts, tb, None, p8))
+            cb = gemm_gpu(wb, b, plan=_bf16_plan_like(p8, M, N, K, L, split))
+            assert np.array_equal(c8, cb), (issuers, decoders)
+
+
+def test_w8a16_one_hot_activations_read_out_every_decoded_weight():
+    """One-hot activations (token m reads k = 32 m + o) make C[m][n] the
+    decoded weight w(n, 32 m + o); 32 offsets read out every weight of a
+    shape holding all 254 finite codes and scale codes 3..246, compared bit
+    for bit with the oracle's exact dequantisation."""
+    L, M, N, K = 1, 32, 256, 1024
+    rng = np.random.default_rng(3400)
+    aq = rng.integers(0, 256, size=(L, N, K), dtype=np.uint8)
+    aq[(aq & 0x7F) == 0x7F] ^= 1                   # no not-a-number codes
+    aq[0, 0, :254] = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], np.uint8)
+    a_s = rng.integers(3, 247, size=(L, N, K // 32), dtype=np.uint8)
+    a_s[0, :, 0] = 3                               # smallest exact scale
+    a_s[0, :, 1] = 127
+    a_s[0, :, 3] = 246                             # largest exact scale
+    want = np.vectorize(oracle.f64_to_bf16)(oracle.w8_dequant(aq, a_s)).astype(np.uint16)
+    want[want == 0x8000] = 0                       # a sum holding +0 terms reads a -0 weight as +0
+    ta, ts = _u8_dev(aq), _u8_dev(a_s)
+    for o in range(32):
+        b = np.zeros((L, M, K), np.uint16)
+        b[0, np.arange(M), 32 * np.arange(M) + o] = ONE
+        c = to_host(sk.splitk_gemm_w8a16(ta, ts, to_dev(b), split_k=2))
+        assert np.array_equal(c[0], want[0][:, 32 * np.arange(M) + o].T), o
+    torch.cuda.synchronize()
+    assert sk.splitk_get_status() == 0
+
+
+def test_w8a16_slots_stage_and_decoders_agree():
+    """1, 2 or 3 TMEM slots, the bf16 stage, the activation loaders and one
+    or two decoding warpgroups: the same bits, run three times each."""
+    L, M, N, K = 1, 3, 256, 512 * 4
+    aq, a_s, b = _w8_draw(L, M, N, K, seed=3500)
+    base = sk.splitk_plan_w8a16(M, N, K, L, 4)
+    ta, ts, tb = _u8_dev(aq), _u8_dev(a_s), to_dev(b)
+    outs = {1: [], 2: []}
+    for slots, stage in ((3, 1), (3, 0), (2, 0), (1, 0)):
+        for loader in (0, 1):
+            for issuers in (1, 2):
+                if issuers > slots:
+                    continue
+                for decoders in (1, 2):
+                    p = _w4_variant(base, slots, stage, loader, issuers, decoders)
+                    for _ in range(3):
+                        outs[issuers].append(to_host(sk.splitk_gemm_w8a16_planned(ta, ts, tb, None, p)))
+    torch.cuda.synchronize()
+    assert sk.splitk_get_status() == 0
+    ref = oracle.gemm_w8a16(aq, a_s, b)
+    max_w = float(np.max(np.abs(oracle.w8_dequant(aq, a_s))))
+    for group in outs.values():
+        for o in group[1:]:
+            assert np.array_equal(o, group[0])
+        ok, rep = _tol.check(group[0], ref, K, max_w, _tol.max_abs_bf16(b))
+        assert ok, rep
+
+
+def test_w8a16_all_ones_closed_form():
+    """Every weight code 0x38 (1.0) with scale 2^2 and every activation 1.0:
+    C = 4 K exactly."""
+    L, M, N, K = 1, 4, 300, 2048
+    aq = np.full((L, N, K), 0x38, np.uint8)
+    a_s = np.full((L, N, K // 32), 129, np.uint8)
+    b = np.full((L, M, K), ONE, np.uint16)
+    c = to_host(sk.splitk_gemm_w8a16(_u8_dev(aq), _u8_dev(a_s), to_dev(b), split_k=4))
+    torch.cuda.synchronize()
+    assert np.all(c == oracle.f64_to_bf16(4.0 * K))
