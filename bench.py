@@ -22,7 +22,7 @@ replay / steps.  All points are captured first and timed in one block, so
 the clock sampler sees the GPU under load.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload sweep|decode_m1|...] [--sweep fixed|w4a16]
+                  [--workload sweep|decode_m1|...] [--sweep fixed|w4a16|w8a16|persistent]
 
 Under torchrun (N > 1) every rank runs an independent replica of the
 workload on its own GPU (weak scaling, no data exchange); rank 0 prints the
@@ -683,8 +683,8 @@ def run_profile_case(args):
     """A short eager run for ncu: for one workload (or, with `all`, every
     fixed and sweep workload in turn), one weight copy (so ncu's memory save
     and restore stays small), `--warmup` launches, then `--steps` launches;
-    no graphs, no CPU oracle.  `--w4` runs the A16W4 kernel on the same
-    shapes (4-bit codes with their scales)."""
+    no graphs, no CPU oracle.  `--w4` (`--w8`) runs the A16W4 (A16W8)
+    kernel on the same shapes: 4-bit (8-bit) codes with their scales."""
     import torch
 
     import split_bf16_gemm_swapped_gb300 as sk
@@ -697,10 +697,11 @@ def run_profile_case(args):
     for w in ws:
         b = to_dev(w.make_b(), dev)
         c = torch.empty((w.L, w.M, w.N), dtype=torch.bfloat16, device=dev)
-        if args.w4:
-            aq, a_s = synthetic.w4_weights(w.L, w.N, w.K, w.seed)
+        if args.w4 or args.w8:
+            aq, a_s = (synthetic.w4_weights if args.w4 else synthetic.w8_weights)(w.L, w.N, w.K, w.seed)
             q, s = torch.from_numpy(aq).to(dev), torch.from_numpy(a_s).to(dev)
-            call = lambda: sk.splitk_gemm_w4a16(q, s, b, c, split_k=w.split_k)  # noqa: E731
+            gemm = sk.splitk_gemm_w4a16 if args.w4 else sk.splitk_gemm_w8a16
+            call = lambda: gemm(q, s, b, c, split_k=w.split_k)  # noqa: E731
         else:
             key = (w.N, w.K, w.L, w.seed)
             if key not in a_cache:
@@ -713,7 +714,7 @@ def run_profile_case(args):
             call()
         torch.cuda.synchronize(dev)
         rc = sk.splitk_get_status()
-        print(json.dumps({"profile_case": describe(w), "key": workload_key(w), "w4": bool(args.w4),
+        print(json.dumps({"profile_case": describe(w), "key": workload_key(w), "w4": bool(args.w4), "w8": bool(args.w8),
                           "launches": args.warmup + args.steps, "status": rc}), flush=True)
         if rc != 0:
             raise SystemExit(1)
@@ -777,7 +778,13 @@ NCU_SUMMARY_METRICS = [
 ]
 
 
-def ncu_summary(rep: str, key: str, w4: bool = False) -> str:
+def quant_bytes(w, bits: int) -> int:
+    """Bytes one quantized-weight call moves: the codes (`bits` a weight),
+    the E8M0 scales (one byte per 32 weights), activations and output."""
+    return w.L * (w.N * w.K * bits // 8 + w.N * w.K // 32 + 2 * w.M * w.K + 2 * w.M * w.N)
+
+
+def ncu_summary(rep: str, key: str, w4: bool = False, w8: bool = False) -> str:
     """A markdown summary of one `ncu --set full` report: the kernel, its
     launch shape, duration, DRAM bytes against the algorithmic bytes of the
     workload `key`, DRAM / L2 / tensor-pipe utilisation and the top warp
@@ -790,9 +797,9 @@ def ncu_summary(rep: str, key: str, w4: bool = False) -> str:
     head, units, vals = rows[0], rows[1], rows[2]
     get = {h: (u, v) for h, u, v in zip(head, units, vals)}
     w = workload_by_name(key)
-    alg = w.bytes if not w4 else w.L * (w.N * w.K // 2 + w.N * w.K // 32 + 2 * w.M * w.K + 2 * w.M * w.N)
+    alg = quant_bytes(w, 4) if w4 else quant_bytes(w, 8) if w8 else w.bytes
     lines = [f"kernel: `{get.get('Kernel Name', ('', '?'))[1]}`",
-             f"workload: {describe(w)}{' (A16W4 weights)' if w4 else ''}; algorithmic bytes per launch {alg}", "",
+             f"workload: {describe(w)}{' (A16W4 weights)' if w4 else ' (A16W8 weights)' if w8 else ''}; algorithmic bytes per launch {alg}", "",
              "| metric | value |", "|---|---|"]
     for m, label in NCU_SUMMARY_METRICS:
         if m in get and get[m][1] != "":
@@ -818,11 +825,12 @@ def ncu_summary(rep: str, key: str, w4: bool = False) -> str:
     return "\n".join(lines)
 
 
-def run_sweep_w4(args):
-    """Extra lines for the A16W4 variant (4-bit E2M1 weights with E8M0 scales
-    per 32 k, bf16 activations) on the decode shapes: HBM TB/s of the bytes
-    it moves (codes, scales, activations, output) and the step time next to
-    the bf16 kernel's on the same shape, both timed like the main line."""
+def run_sweep_quant(args, bits: int):
+    """Extra lines for the quantized-weight variants (A16W4: 4-bit E2M1
+    weights, A16W8: 8-bit E4M3 weights, both with E8M0 scales per 32 k and
+    bf16 activations) on the decode shapes: HBM TB/s of the bytes it moves
+    (codes, scales, activations, output) and the step time next to the bf16
+    kernel's on the same shape, both timed like the main line."""
     import torch
 
     import split_bf16_gemm_swapped_gb300 as sk
@@ -852,29 +860,32 @@ def run_sweep_w4(args):
 
     for w in (W.DECODE_M1, W.DECODE_M16, W.TINY, W.DECODE_M1.with_(M=8), W.DECODE_M1.with_(M=32),
               W.DECODE_M1.with_(L=8), W.DECODE_M16.with_(L=4), W.DECODE_M1.with_(split_k=8)):
-        aq, a_s = synthetic.w4_weights(w.L, w.N, w.K, w.seed)
+        aq, a_s = (synthetic.w4_weights if bits == 4 else synthetic.w8_weights)(w.L, w.N, w.K, w.seed)
         q0 = torch.from_numpy(aq).to(dev)
         s0 = torch.from_numpy(a_s).to(dev)
-        w4_bytes = w.L * (w.N * w.K // 2 + w.N * w.K // 32 + 2 * w.M * w.K + 2 * w.M * w.N)
+        w4_bytes = quant_bytes(w, bits)
         R = max(2, min(64, math.ceil(4 * l2 / (aq.nbytes + a_s.nbytes))))
         Qs = [q0] + [q0.clone() for _ in range(R - 1)]
         Ss = [s0] + [s0.clone() for _ in range(R - 1)]
         b = to_dev(w.make_b(), dev)
         c = torch.empty((w.L, w.M, w.N), dtype=torch.bfloat16, device=dev)
-        t4 = timed(lambda i, st: sk.splitk_gemm_w4a16(Qs[i], Ss[i], b, c, split_k=w.split_k, stream=st), R)
+        gemm = sk.splitk_gemm_w4a16 if bits == 4 else sk.splitk_gemm_w8a16
+        gemm_planned = sk.splitk_gemm_w4a16_planned if bits == 4 else sk.splitk_gemm_w8a16_planned
+        plan = sk.splitk_plan_w4a16 if bits == 4 else sk.splitk_plan_w8a16
+        t4 = timed(lambda i, st: gemm(Qs[i], Ss[i], b, c, split_k=w.split_k, stream=st), R)
         # the other decoder count, for comparison
-        p_alt = sk.splitk_plan_w4a16(w.M, w.N, w.K, w.L, w.split_k)
+        p_alt = plan(w.M, w.N, w.K, w.L, w.split_k)
         p_alt.w4_decoders = 3 - p_alt.w4_decoders
         try:
-            t4_alt = timed(lambda i, st: sk.splitk_gemm_w4a16_planned(Qs[i], Ss[i], b, c, p_alt, 0, st), R)
+            t4_alt = timed(lambda i, st: gemm_planned(Qs[i], Ss[i], b, c, p_alt, 0, st), R)
         except sk.SplitKError:
             t4_alt = None
         a0 = to_dev(w.make_a(), dev)
         Rb = max(2, min(20, math.ceil(4 * l2 / (a0.numel() * 2))))
         As = [a0] + [a0.clone() for _ in range(Rb - 1)]
         tb = timed(lambda i, st: sk.splitk_gemm_bf16(As[i], b, c, split_k=w.split_k, stream=st), Rb)
-        p = sk.splitk_plan_w4a16(w.M, w.N, w.K, w.L, w.split_k)
-        print(json.dumps({"sweep": "A16W4 " + describe(w), "us": round(t4 * 1e6, 2),
+        p = plan(w.M, w.N, w.K, w.L, w.split_k)
+        print(json.dumps({"sweep": f"A16W{bits} " + describe(w), "us": round(t4 * 1e6, 2),
                           "TB/s": round(w4_bytes / t4 / 1e12, 3), "bytes_per_call": w4_bytes,
                           "hbm_frac": round(w4_bytes / t4 / 1e9 / hbm, 3), "peak_source": src,
                           "bf16_us": round(tb * 1e6, 2), "speedup_vs_bf16": round(tb / t4, 3),
@@ -985,9 +996,9 @@ def main():
                          "sweep_m<M>_s<split>")
     ap.add_argument("--min-ms", type=float, default=40.0,
                     help="GPU time each point's back-to-back replays cover at least")
-    ap.add_argument("--sweep", choices=["fixed", "w4a16", "persistent"], default=None,
-                    help="extra lines instead of the contract line: the fixed workloads, A16W4, or the "
-                         "per-tile against the persistent kernel")
+    ap.add_argument("--sweep", choices=["fixed", "w4a16", "w8a16", "persistent"], default=None,
+                    help="extra lines instead of the contract line: the fixed workloads, A16W4, A16W8, or "
+                         "the per-tile against the persistent kernel")
     ap.add_argument("--no-extras", action="store_true", help="skip the decode workloads of the sweep line")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the timed oracle leg")
     ap.add_argument("--no-e2e", dest="e2e", action="store_false", help="skip the end-to-end measurement")
@@ -1001,8 +1012,10 @@ def main():
                     help="a short eager run for ncu of one workload, or `all` of them in turn "
                          "(no graphs, one weight copy)")
     ap.add_argument("--w4", action="store_true", help="with --profile-case: the A16W4 kernel")
+    ap.add_argument("--w8", action="store_true", help="with --profile-case: the A16W8 kernel")
     ap.add_argument("--ncu-summary", nargs=2, metavar=("REPORT", "WORKLOAD"), default=None,
-                    help="print a markdown summary of an ncu --set full report of WORKLOAD (with --w4: A16W4)")
+                    help="print a markdown summary of an ncu --set full report of WORKLOAD (with --w4 / --w8: "
+                         "A16W4 / A16W8)")
     ap.add_argument("--ncu-table", nargs=2, metavar=("CSV", "LOG"), default=None,
                     help="print the DRAM-traffic table from an ncu CSV of a --profile-case run and its log")
     args = ap.parse_args()
@@ -1010,12 +1023,14 @@ def main():
         raise SystemExit("--warmup must be >= 3")
     if args.steps < 1:
         raise SystemExit("--steps must be >= 1")
+    if args.w4 and args.w8:
+        raise SystemExit("--w4 and --w8 exclude each other")
     if args.workload != "sweep":
         workload_by_name(args.workload)
     if args.profile_case not in (None, "all"):
         workload_by_name(args.profile_case)
     if args.ncu_summary:
-        print(ncu_summary(args.ncu_summary[0], args.ncu_summary[1], args.w4))
+        print(ncu_summary(args.ncu_summary[0], args.ncu_summary[1], args.w4, args.w8))
     elif args.ncu_table:
         print(ncu_traffic_table(args.ncu_table[0], args.ncu_table[1], args.steps))
     elif args.cpu_table:
@@ -1024,8 +1039,8 @@ def main():
         run_reference(args)
     elif args.profile_case:
         run_profile_case(args)
-    elif args.sweep == "w4a16":
-        run_sweep_w4(args)
+    elif args.sweep in ("w4a16", "w8a16"):
+        run_sweep_quant(args, 4 if args.sweep == "w4a16" else 8)
     elif args.sweep == "fixed":
         run_sweep_fixed(args)
     elif args.sweep == "persistent":

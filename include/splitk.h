@@ -156,9 +156,11 @@ typedef struct splitk_plan_t {
                               holds before the programmatic-dependent-launch
                               wait returns                                     */
     int weight_format;     /* SPLITK_WEIGHTS_BF16, or SPLITK_WEIGHTS_E2M1_E8M0
-                              (plans of splitk_plan_w4a16*): then `stages` is
-                              the CTA's K tiles (all their packed codes are
-                              loaded at once), `a_tmem_tiles` (1..3) the TMEM
+                              (plans of splitk_plan_w4a16*), or
+                              SPLITK_WEIGHTS_E4M3_E8M0 (splitk_plan_w8a16*):
+                              then `stages` (1..k_tiles_per_cta) is the ring
+                              of packed code tiles (all of the CTA's at once
+                              when equal), `a_tmem_tiles` (1..3) the TMEM
                               slots the epilogue threads decode tiles into,
                               b_resident = 1, mma_issuers = 1; smem_bytes may
                               exceed the layout's need, which caps how many

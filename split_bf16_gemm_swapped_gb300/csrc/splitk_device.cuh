@@ -264,49 +264,72 @@ __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// The power of two of E8M0 scale code x, 2^(x - 127) (code 0: zero), as a
-// bf16 pair: the bf16 bits are x << 7.
-__device__ __forceinline__ uint32_t e8m0_bf16x2(uint32_t code) { return (code << 7) | (code << 23); }
-
-// One byte of two E2M1 codes (low nibble = first element) -> two bf16 values
-// times the power of two `scale2` (a bf16 pair, e8m0_bf16x2), packed with
-// the first in the low half.  The hardware conversion to f16x2 is exact
-// (E2M1 values are f16 values), widening to f32 and rounding to bf16 are
-// exact (at most 2 significant bits), and the bf16 product by a power of two
-// is exact wherever the result is a finite bf16 value, subnormals included
-// (the smallest, 0.5 * 2^-126, is one).
-__device__ __forceinline__ uint32_t e2m1x2_scaled_bf16x2(uint32_t byte, uint32_t scale2) {
-  uint32_t h2;
-  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(h2) : "r"(byte));
-  float lo, hi;
-  asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
-      : "=f"(lo), "=f"(hi)
-      : "r"(h2));
-  uint32_t r, d;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(r), "r"(scale2));
+// Quantized codes to bf16, two at a time, by placing bits (no conversion
+// instructions).  A byte permute copies each code byte into one 16-bit lane
+// and fills the byte above it with the code's sign (the permute's
+// sign-replicate mode); a shift and a mask then leave the sign at bit 15 and
+// the code's exponent and mantissa fields at bf16's exponent low bits and
+// mantissa high bits.  The lane is then the bf16 of x * 2^-126 (E2M1) or
+// x * 2^-120 (E4M3) exactly: a code with a zero exponent field lands on a
+// bf16 subnormal of the same significand, which is the code's own
+// subnormal scaled the same way.  One product by a power of two restores x
+// times the block scale.
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
   return d;
 }
 
-// Two E4M3 codes (the low 16 bits of `pair`; the lower byte is the first
-// element) -> two bf16 values times the power of two `scale2` (a bf16 pair,
-// e8m0_bf16x2), packed with the first in the low half.  The hardware
-// conversion to f16x2 is exact (E4M3 values are f16 values), widening to f32
-// and rounding to bf16 are exact (at most 4 significant bits), and the bf16
-// product by a power of two is exact wherever the result is a finite bf16
-// value with no bits below 2^-133.
-__device__ __forceinline__ uint32_t e4m3x2_scaled_bf16x2(uint32_t pair, uint32_t scale2) {
-  uint32_t h2;
-  asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(h2) : "r"(pair));
-  float lo, hi;
-  asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
-      : "=f"(lo), "=f"(hi)
-      : "r"(h2));
-  uint32_t r, d;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(r), "r"(scale2));
-  return d;
+// The codes of byte `kByte` of `w` (low nibble first) as bf16 x * 2^-126,
+// packed with the first in the low half; `w4` = w << 4, whose byte kByte has
+// the low nibble's code in its high half.  Lane 0 takes byte kByte of w4,
+// lane 1 byte kByte of w, each over its sign-replicated copy; shifted left
+// by 2, bits 6..4 of the byte (sign-free magnitude) land at 8..6 and the sign
+// at 15.
+template <int kByte>
+__device__ __forceinline__ uint32_t e2m1x2_placed(uint32_t w, uint32_t w4) {
+  constexpr uint32_t sel = (uint32_t)(4 + kByte) | ((uint32_t)(12 + kByte) << 4) | ((uint32_t)kByte << 8) |
+                           ((uint32_t)(8 + kByte) << 12);
+  return (prmt(w, w4, sel) << 2) & 0x81C081C0u;
 }
+
+// The E4M3 codes of bytes 2 kPair and 2 kPair + 1 of `w` as bf16
+// x * 2^-120, packed with the first in the low half: each byte over its
+// sign-replicated copy, shifted left by 4, bits 6..0 land at 10..4 and the
+// sign at 15.
+template <int kPair>
+__device__ __forceinline__ uint32_t e4m3x2_placed(uint32_t w) {
+  constexpr uint32_t sel = kPair == 0 ? 0x9180u : 0xB3A2u;
+  return (prmt(w, 0u, sel) << 4) & 0x87F087F0u;
+}
+
+// The multipliers of one 32-k block with E8M0 scale code `code`, for placed
+// codes worth x * 2^-kShift: one product by 2^(code - 127 + kShift) when
+// that is a normal bf16 (code in 1 .. 254 - kShift), else two, by 2^kShift
+// (exact: the placed value times it is x) and by the scale as a bf16
+// (code 0: zero; 255: infinity).  Either way the result is x times the
+// scale rounded once, the value of the exact product.
+template <int kShift>
+struct BlockScale {
+  uint32_t m1, m2;
+  bool two;
+  __device__ __forceinline__ explicit BlockScale(uint32_t code) {
+    two = code - 1u >= (uint32_t)(254 - kShift);
+    const uint32_t f = two ? (uint32_t)(127 + kShift) : code + (uint32_t)kShift;   // bf16 exponent field
+    m1 = (f << 7) | (f << 23);
+    m2 = (code << 7) | (code << 23);
+  }
+  template <bool kTwo>
+  __device__ __forceinline__ uint32_t apply(uint32_t placed) const {
+    const uint32_t y = bf16x2_mul(placed, m1);
+    return kTwo ? bf16x2_mul(y, m2) : y;
+  }
+};
 
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");

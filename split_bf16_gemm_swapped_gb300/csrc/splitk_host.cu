@@ -82,9 +82,10 @@ inline bool is_quantized(int fmt) { return fmt == SPLITK_WEIGHTS_E2M1_E8M0 || fm
 // Shared memory of a quantized-weight plan's layout: all packed weight
 // tiles, all activation tiles (at least 2: rank 0's f32 staging tile reuses
 // them), the mailbox and the barriers.
-size_t smem_bytes_w4(int mma_n, int k_tiles, uint32_t dedicated_mailbox_bytes, int smem_tiles,
-                     int fmt = SPLITK_WEIGHTS_E2M1_E8M0) {
-  return (size_t)kAlignSlack + (size_t)k_tiles * q_tile_bytes(fmt) +
+// code_stages: the ring of packed weight tiles (at most k_tiles)
+size_t smem_bytes_w4(int mma_n, int k_tiles, int code_stages, uint32_t dedicated_mailbox_bytes, int smem_tiles,
+                     int fmt) {
+  return (size_t)kAlignSlack + (size_t)code_stages * q_tile_bytes(fmt) +
          (size_t)std::max(2, k_tiles) * b_stage_bytes(mma_n) + (size_t)smem_tiles * kAStageBytes +
          dedicated_mailbox_bytes + kBarRegionBytes;
 }
@@ -475,8 +476,17 @@ int plan_w4_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t sm
   // One tile past the TMEM slots: decode it into a bf16 stage in shared
   // memory, before the PDL wait, if that still fits 2 CTAs per SM
   // (the single-token decode case: 4 K tiles per CTA, 3 slots).
+  // The ring of packed tiles: all of the CTA's at once, unless fewer let two
+  // CTAs share an SM (8-bit codes: 16 KiB a tile; small-batch decode, 7
+  // tiles a CTA, would otherwise run one CTA per SM, its 32 clusters of 8
+  // in three waves).
+  int code_stages = kt;
+  while (code_stages > 2 && smem_bytes_w4(mma_n, kt, code_stages, ded, 0, fmt) + 1024 > smem_per_sm / 2) {
+    --code_stages;
+  }
+  p.stages = code_stages;
   p.w4_smem_tiles = kt == p.a_tmem_tiles + 1 &&
-                            smem_bytes_w4(mma_n, kt, ded, 1, fmt) + 1024 <= smem_per_sm / 2
+                            smem_bytes_w4(mma_n, kt, code_stages, ded, 1, fmt) + 1024 <= smem_per_sm / 2
                         ? 1
                         : 0;
   // A second decoding warpgroup halves every tile's decode (384 threads a
@@ -495,14 +505,14 @@ int plan_w4_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t sm
     }
     return smem;
   };
-  size_t smem = padded_smem(smem_bytes_w4(mma_n, kt, ded, p.w4_smem_tiles, fmt), p.tmem_cols);
+  size_t smem = padded_smem(smem_bytes_w4(mma_n, kt, code_stages, ded, p.w4_smem_tiles, fmt), p.tmem_cols);
   // Grids of more than two waves: one TMEM slot and one issuer when that lets
   // more CTAs share an SM (at most 3 by registers), so that their decodes
   // overlap (single-token decode, L=8: 49.1 -> 46.2 us).
   const long long ctas = (long long)split * m_tiles * n_tiles * L;
   if (ctas > 2LL * num_sms && p.a_tmem_tiles > 1) {
     const uint32_t cols1 = tmem_cols_for(mma_n, 1, 1);
-    const size_t smem1 = padded_smem(smem_bytes_w4(mma_n, kt, ded, 0, fmt), cols1);
+    const size_t smem1 = padded_smem(smem_bytes_w4(mma_n, kt, code_stages, ded, 0, fmt), cols1);
     if (std::min(3, resident_by_smem(smem_per_sm, smem1)) > std::min(2, resident_by_smem(smem_per_sm, smem))) {
       p.a_tmem_tiles = 1;
       p.mma_issuers = 1;
@@ -527,7 +537,7 @@ int check_plan_w4(const splitk_plan_t& pl, int M, int N, int K, int L, size_t sm
   if (M > 32 || K % kCtaK != 0 || K > kMaxK || K / kCtaK < pl.split_k) return SPLITK_ERR_INVALID_SHAPE;
   const int T = K / kCtaK;
   const int kt = (T + pl.split_k - 1) / pl.split_k;
-  if (pl.k_tiles_per_cta != kt || pl.stages != kt) return SPLITK_ERR_BAD_PLAN;
+  if (pl.k_tiles_per_cta != kt || pl.stages < 1 || pl.stages > kt) return SPLITK_ERR_BAD_PLAN;
   if (kt > kMaxStages) return SPLITK_ERR_NO_FIT;
   if (pl.reserved != 0 || pl.persistent != 0) return SPLITK_ERR_BAD_PLAN;
   if (pl.w4_decoders != 1 && pl.w4_decoders != 2) return SPLITK_ERR_BAD_PLAN;
@@ -557,7 +567,8 @@ int check_plan_w4(const splitk_plan_t& pl, int M, int N, int K, int L, size_t sm
   // round it never had)
   if (pl.w4_smem_tiles != 0 && (pl.w4_smem_tiles != 1 || kt != pl.a_tmem_tiles + 1)) return SPLITK_ERR_BAD_PLAN;
   const uint32_t ded = w4_mailbox_bytes(pl.split_k, pl.reduce_scatter, ncols_max);
-  if (pl.smem_bytes < smem_bytes_w4(pl.mma_n, kt, ded, pl.w4_smem_tiles, pl.weight_format) || pl.smem_bytes % 16 != 0) {
+  if (pl.smem_bytes < smem_bytes_w4(pl.mma_n, kt, pl.stages, ded, pl.w4_smem_tiles, pl.weight_format) ||
+      pl.smem_bytes % 16 != 0) {
     return SPLITK_ERR_BAD_PLAN;
   }
   if (pl.smem_bytes > smem_optin) return SPLITK_ERR_NO_FIT;

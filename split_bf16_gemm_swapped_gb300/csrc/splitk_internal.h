@@ -19,6 +19,7 @@ constexpr int kMmaK = 16;
 constexpr int kThreads = 256;      // warps 0..7
 constexpr int kThreadsW4Wide = 384;   // A16W4 with a second decoding warpgroup (warps 8..11)
 constexpr int kEpiThreads = 128;   // warps 4..7, one per TMEM lane / weight row
+constexpr int kEpiWarps = kEpiThreads / 32;
 constexpr int kMaxStages = 8;
 constexpr uint32_t kAStageBytes = kMmaM * kCtaK * 2;        // 32 KiB
 constexpr uint32_t kABoxBytes = kMmaM * kAtomK * 2;         // 16 KiB

@@ -23,7 +23,7 @@
 //   warp 3      second MMA issuer (odd K tiles, own accumulator) or idle; it
 //               keeps warps 4..7 on TMEM lane quadrants 0..3
 //   warps 4..7  weight tiles copied into TMEM before the wait (staged tiles)
-//               or, for 4-bit weights, decoded to bf16 into TMEM or a
+//               or, for 4- and 8-bit weights, decoded to bf16 into TMEM or a
 //               shared-memory stage; activation loads for few rows; then the
 //               epilogue: TMEM -> registers, DSMEM publish / rank-0 reduce,
 //               BF16 packing, 16-byte stores (epilog_warp)
@@ -41,12 +41,32 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "splitk.h"
 #include "splitk_device.cuh"
 #include "splitk_internal.h"
 #include "splitk_kernel_common.cuh"
 
 namespace splitk {
+
+// The E8M0 scale words of one weight row's K tiles (four codes a tile, one
+// per 32 k), all loaded when the decoder starts, so that no tile's decode
+// waits on a global load; taken in order, each take shifting the rest down
+// (indices stay compile-time: the words stay in registers).
+struct ScaleWords {
+  uint32_t w[kMaxStages];
+  __device__ __forceinline__ void load(const uint32_t* src, bool row_ok, int k_tiles) {
+#pragma unroll
+    for (int i = 0; i < kMaxStages; ++i) w[i] = (row_ok && i < k_tiles) ? __ldg(src + i) : 0u;
+  }
+  __device__ __forceinline__ uint32_t take() {
+    const uint32_t x = w[0];
+#pragma unroll
+    for (int i = 0; i + 1 < kMaxStages; ++i) w[i] = w[i + 1];
+    return x;
+  }
+};
 
 // kFmt: the weight format (0 bf16; 1 E2M1 codes, 2 E4M3 codes, each with
 // E8M0 scales per 32 k, decoded on chip).  kDecWG: warpgroups decoding
@@ -87,7 +107,7 @@ __global__ void __launch_bounds__(kDecWG == 2 ? kThreadsW4Wide : kThreads, kDecW
   const bool b_res = p.b_resident != 0;
   const int tmem_tiles = p.a_tmem_tiles < k_tiles ? p.a_tmem_tiles : k_tiles;
 
-  // Shared memory: [A ring (A16W4: all packed tiles)][B ring or all B tiles]
+  // Shared memory: [A ring (quantized weights: a ring of packed tiles)][B ring or all B tiles]
   // [dedicated mailbox?][barriers].
   const uint32_t sA = base;
   const uint32_t sB = sA + (uint32_t)stages * kAStage;
@@ -96,7 +116,7 @@ __global__ void __launch_bounds__(kDecWG == 2 ? kThreadsW4Wide : kThreads, kDecW
   const uint32_t sMail = p.mailbox_dedicated ? ring_end : sA;
   const uint32_t sBar = ring_end + (p.mailbox_dedicated ? p.mailbox_bytes : 0u);
   const uint32_t bar_full0 = sBar;                       // [kMaxStages], count 2
-  const uint32_t bar_empty0 = sBar + 8u * kMaxStages;    // [kMaxStages], count 1
+  const uint32_t bar_empty0 = sBar + 8u * kMaxStages;    // [kMaxStages], count 1 (quantized: the decoders)
   const uint32_t bar_mma_done = sBar + 16u * kMaxStages; // count 1
   const uint32_t bar_tmem_empty = bar_mma_done + 8u;     // count 128
   const uint32_t bar_reduce = bar_mma_done + 16u;        // count 1 + tx bytes
@@ -104,9 +124,9 @@ __global__ void __launch_bounds__(kDecWG == 2 ? kThreadsW4Wide : kThreads, kDecW
   const uint32_t slot_tmem = bar_mma_done + 32u;
   const uint32_t slot_abort = bar_mma_done + 36u;
   const uint32_t bar_b = bar_mma_done + 40u;             // count 1 + tx bytes (resident B)
-  const uint32_t bar_slot_full0 = bar_mma_done + 48u;    // A16W4 [3]: tile decoded into TMEM slot, count 128
-  const uint32_t bar_slot_empty0 = bar_mma_done + 72u;   // A16W4 [3]: slot read by the MMAs, count 1
-  const uint32_t bar_w4_stage = bar_mma_done + 96u;      // A16W4: the bf16 stage decoded, count 128
+  const uint32_t bar_slot_full0 = bar_mma_done + 48u;    // quantized [3]: tile decoded into TMEM slot (a warp each)
+  const uint32_t bar_slot_empty0 = bar_mma_done + 72u;   // quantized [3]: slot read by the MMAs, count 1
+  const uint32_t bar_w4_stage = bar_mma_done + 96u;      // quantized: the bf16 stage decoded (a warp each)
 
   const Waiter waiter{slot_abort, p.wait_limit_ns};
 
@@ -125,7 +145,9 @@ __global__ void __launch_bounds__(kDecWG == 2 ? kThreadsW4Wide : kThreads, kDecW
     if (lane == 0) {
       for (int s = 0; s < stages; ++s) {
         dev::mbar_init(bar_full0 + 8u * s, b_res ? 1u : 2u);   // A (and B when it rides the ring)
-        dev::mbar_init(bar_empty0 + 8u * s, 1u);             // the stage's MMA commit
+        // the stage's MMA commit; quantized weights: every decoding warp,
+        // once it has read the stage's codes
+        dev::mbar_init(bar_empty0 + 8u * s, kW4 ? (uint32_t)(kEpiWarps * kDecWG) : 1u);
       }
       dev::mbar_init(bar_b, p.b_loader ? (uint32_t)kEpiThreads : 1u);
       dev::mbar_init(bar_mma_done, (uint32_t)p.mma_issuers);
@@ -134,10 +156,10 @@ __global__ void __launch_bounds__(kDecWG == 2 ? kThreadsW4Wide : kThreads, kDecW
       dev::mbar_init(bar_ready, 1);
       if (kW4) {
         for (int i = 0; i < 3; ++i) {
-          dev::mbar_init(bar_slot_full0 + 8u * i, (uint32_t)(kEpiThreads * kDecWG));
+          dev::mbar_init(bar_slot_full0 + 8u * i, (uint32_t)(kEpiWarps * kDecWG));
           dev::mbar_init(bar_slot_empty0 + 8u * i, 1);
         }
-        dev::mbar_init(bar_w4_stage, (uint32_t)(kEpiThreads * kDecWG));
+        dev::mbar_init(bar_w4_stage, (uint32_t)(kEpiWarps * kDecWG));
       }
       dev::st_shared_u32(slot_abort, 0u);
       dev::fence_barrier_init();
@@ -166,9 +188,10 @@ __global__ void __launch_bounds__(kDecWG == 2 ? kThreadsW4Wide : kThreads, kDecW
   }
   dev::cluster_arrive_release();
   if (kW4 && threadIdx.x == 0) {
-    // every packed weight tile of the CTA at once: one box each (8 KiB of
-    // 4-bit codes or 16 KiB of 8-bit ones)
-    for (; a_issued < k_tiles; ++a_issued) {
+    // the first ring pass of packed weight tiles (usually all of the CTA's):
+    // one box each, 8 KiB of 4-bit codes or 16 KiB of 8-bit ones
+    const int first = k_tiles < stages ? k_tiles : stages;
+    for (; a_issued < first; ++a_issued) {
       const uint32_t full = bar_full0 + 8u * a_issued;
       dev::mbar_arrive_expect_tx(full, kQTileBytes);
       dev::tma_load_3d_hint(sA + (uint32_t)a_issued * kQTileBytes, p.a_map, (kt0 + a_issued) * (int)kQRowBytes,
@@ -218,46 +241,85 @@ __global__ void __launch_bounds__(kDecWG == 2 ? kThreadsW4Wide : kThreads, kDecW
   // of bf16 pairs: E2M1 codes are 64 B a row in the 64-byte swizzle (step j
   // is the 16-byte chunk at slot j ^ ((row >> 1) & 3)), a byte -> two bf16;
   // E4M3 codes are 128 B a row in the 128-byte swizzle (step j is chunks 2j
-  // and 2j + 1 at slots c ^ (row & 7)), two bytes -> two bf16.  Both go
-  // through the hardware conversion to f16 (exact), an exact rounding to
-  // bf16 and an exact bf16 product with the block's power of two.
-  auto q_decode_step = [&](uint32_t src, int j, int row, uint32_t scale, uint32_t (&r)[16]) {
+  // and 2j + 1 at slots c ^ (row & 7)), two bytes -> two bf16.  Both place
+  // the code bits in bf16 lanes (exact, a constant power of two apart from
+  // the code's value) and take one bf16 product by a power of two (two for
+  // scale codes out of that product's range), exact wherever the scaled
+  // weight is a bf16 value.
+  //
+  // The loop is software-pipelined: step j + 1's codes are loaded from
+  // shared memory before step j is converted, so the load latency overlaps
+  // the conversions instead of stalling each step (the loads and the TMEM or
+  // shared-memory stores are ordered accesses the compiler keeps in program
+  // order).
+  constexpr int kCodeWords = kFmt == 2 ? 8 : 4;   // 32-bit words of codes a step
+  auto q_load = [&](uint32_t src, int j, int row, uint32_t (&w)[kCodeWords]) {
     if constexpr (kFmt == 2) {
-      uint32_t w[8];
       dev::ld_shared_v4(src + (uint32_t)(((2 * j) ^ (row & 7)) * 16), w[0], w[1], w[2], w[3]);
-      dev::ld_shared_v4(src + (uint32_t)(((2 * j + 1) ^ (row & 7)) * 16), w[4], w[5], w[6], w[7]);
-#pragma unroll
-      for (int q = 0; q < 16; ++q) r[q] = dev::e4m3x2_scaled_bf16x2(w[q >> 1] >> (16 * (q & 1)), scale);
+      dev::ld_shared_v4(src + (uint32_t)(((2 * j + 1) ^ (row & 7)) * 16), w[kCodeWords - 4], w[kCodeWords - 3],
+                        w[kCodeWords - 2], w[kCodeWords - 1]);
     } else {
-      uint32_t w[4];
       dev::ld_shared_v4(src + (uint32_t)((j ^ ((row >> 1) & 3)) * 16), w[0], w[1], w[2], w[3]);
+    }
+  };
+  // One step's 16 pairs; scale code `code`.  The one-or-two-product choice
+  // is taken once a step (a branch, not a select per pair).
+  auto q_convert = [&](const uint32_t (&w)[kCodeWords], uint32_t code, uint32_t (&r)[16]) {
+    auto pairs = [&](auto two, const auto& bs) {
+      constexpr bool kTwo = decltype(two)::value;
+      if constexpr (kFmt == 2) {
 #pragma unroll
-      for (int q = 0; q < 16; ++q) r[q] = dev::e2m1x2_scaled_bf16x2(w[q >> 2] >> (8 * (q & 3)), scale);
+        for (int i = 0; i < 8; ++i) {
+          r[2 * i] = bs.template apply<kTwo>(dev::e4m3x2_placed<0>(w[i]));
+          r[2 * i + 1] = bs.template apply<kTwo>(dev::e4m3x2_placed<1>(w[i]));
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t w4 = w[i] << 4;
+          r[4 * i + 0] = bs.template apply<kTwo>(dev::e2m1x2_placed<0>(w[i], w4));
+          r[4 * i + 1] = bs.template apply<kTwo>(dev::e2m1x2_placed<1>(w[i], w4));
+          r[4 * i + 2] = bs.template apply<kTwo>(dev::e2m1x2_placed<2>(w[i], w4));
+          r[4 * i + 3] = bs.template apply<kTwo>(dev::e2m1x2_placed<3>(w[i], w4));
+        }
+      }
+    };
+    const dev::BlockScale<kFmt == 2 ? 120 : 126> bs(code);
+    if (bs.two) {
+      pairs(std::true_type{}, bs);
+    } else {
+      pairs(std::false_type{}, bs);
+    }
+  };
+  // Steps [j0, j1) of one row: `emit(j, r)` stores step j's 16 words.
+  auto q_decode_row = [&](int stage, int row, uint32_t codes, int j0, int j1, auto&& emit) {
+    const uint32_t src = sA + (uint32_t)stage * kQTileBytes + (uint32_t)row * kQRowBytes;
+    uint32_t next[kCodeWords];
+    q_load(src, j0, row, next);
+#pragma unroll 1
+    for (int j = j0; j < j1; ++j) {
+      uint32_t cur[kCodeWords];
+#pragma unroll
+      for (int i = 0; i < kCodeWords; ++i) cur[i] = next[i];
+      if (j + 1 < j1) q_load(src, j + 1, row, next);
+      uint32_t r[16];
+      q_convert(cur, (codes >> (8 * j)) & 0xFFu, r);
+      emit(j, r);
     }
   };
   // Into TMEM columns t_col + 16 j of the thread's lane, or into the bf16
   // stage in shared memory in the 128-byte-swizzled layout of the bf16 path
   // (two boxes of 64 k; 16-byte chunk c of row r of an 8-row atom at chunk
   // c ^ (r % 8)), read by the MMA from there.
-  auto w4_decode_tmem = [&](int kt, int row, uint32_t codes, uint32_t t_col, int j0, int j1) {
-    const uint32_t src = sA + (uint32_t)kt * kQTileBytes + (uint32_t)row * kQRowBytes;
-#pragma unroll 1
-    for (int j = j0; j < j1; ++j) {
-      const uint32_t scale = dev::e8m0_bf16x2((codes >> (8 * j)) & 0xFFu);   // 2^(code - 127)
-      uint32_t r[16];
-      q_decode_step(src, j, row, scale, r);
+  auto w4_decode_tmem = [&](int stage, int row, uint32_t codes, uint32_t t_col, int j0, int j1) {
+    q_decode_row(stage, row, codes, j0, j1, [&](int j, const uint32_t (&r)[16]) {
       __syncwarp();   // tcgen05.st is warp-collective
       dev::tmem_st_x16(t_col + (uint32_t)(j * 16), r);
-    }
+    });
   };
-  auto w4_decode_stage = [&](int kt, int row, uint32_t codes, int j0, int j1) {
-    const uint32_t src = sA + (uint32_t)kt * kQTileBytes + (uint32_t)row * kQRowBytes;
+  auto w4_decode_stage = [&](int stage, int row, uint32_t codes, int j0, int j1) {
     const uint32_t atom = sW4Stage + (uint32_t)(row >> 3) * 1024u + (uint32_t)(row & 7) * 128u;
-#pragma unroll 1
-    for (int j = j0; j < j1; ++j) {
-      const uint32_t scale = dev::e8m0_bf16x2((codes >> (8 * j)) & 0xFFu);
-      uint32_t r[16];
-      q_decode_step(src, j, row, scale, r);
+    q_decode_row(stage, row, codes, j0, j1, [&](int j, const uint32_t (&r)[16]) {
       // k = 32 j .. 32 j + 31: box j / 2, chunks 4 (j % 2) .. + 3
       const uint32_t box = atom + (uint32_t)(j >> 1) * kABoxBytes;
 #pragma unroll
@@ -266,24 +328,50 @@ __global__ void __launch_bounds__(kDecWG == 2 ? kThreadsW4Wide : kThreads, kDecW
         dev::st_shared_v4(box + (uint32_t)((chunk ^ (row & 7)) * 16), r[4 * c], r[4 * c + 1], r[4 * c + 2],
                           r[4 * c + 3]);
       }
-    }
+    });
   };
   // the chunks of each tile the epilogue warpgroup decodes (the rest: warps 8..11)
   constexpr int kEpiJ1 = kDecWG == 2 ? 2 : 4;
+  // A decoder's wait for packed tile kt at code-ring position `cp`.
+  auto code_wait = [&](const RingPos& cp, int kt) {
+    waiter.wait<false>(bar_full0 + 8u * (uint32_t)cp.index, cp.phase, kRoleEpiDecode, kt);
+  };
+  // The decoders' signals, one arrival a warp (a thread arrival each would
+  // queue 128 or 256 shared-memory atomics on one barrier per tile): after a
+  // warp synchronisation, which orders every lane's prior accesses (and,
+  // after each lane's tcgen05 fence or proxy fence, its TMEM or shared-memory
+  // stores) before lane 0's release.
+  auto warp_arrive = [&](uint32_t bar) {
+    __syncwarp();
+    if (lane == 0) dev::mbar_arrive(bar);
+  };
+  // Tile kt's codes (ring stage `stage`) read into registers: the stage may
+  // take tile kt + stages (no arrival when there is none).
+  auto code_free = [&](int kt, int stage) {
+    if (kt + stages < k_tiles) warp_arrive(bar_empty0 + 8u * (uint32_t)stage);
+  };
 
   if (warp == 0) {
     // ---- weight producer
     if (lane == 0) {
-      for (int kt = a_issued; kt < k_tiles; ++kt) {
-        const int s = kt % stages;
-        const int r = kt / stages;
+      RingPos pos = RingPos::at(a_issued, stages);
+      for (int kt = a_issued; kt < k_tiles; ++kt, pos.advance(1, stages)) {
+        const int s = pos.index;
         const uint32_t full = bar_full0 + 8u * s;
-        if (!waiter.wait<false>(bar_empty0 + 8u * s, (uint32_t)((r - 1) & 1), kRoleWeightTma, kt)) break;
-        const uint32_t dst = sA + (uint32_t)s * kAStageBytes;
-        const int k = (kt0 + kt) * kCtaK;
-        dev::mbar_arrive_expect_tx(full, kAStageBytes);
-        dev::tma_load_3d_hint(dst, p.a_map, k, n0, l, full, a_policy);
-        dev::tma_load_3d_hint(dst + kABoxBytes, p.a_map, k + kAtomK, n0, l, full, a_policy);
+        // the stage's previous round (kt - stages) consumed
+        if (!waiter.wait<false>(bar_empty0 + 8u * s, pos.phase ^ 1u, kRoleWeightTma, kt)) break;
+        if constexpr (kW4) {
+          // packed codes: the stage is free once every decoder has read it
+          dev::mbar_arrive_expect_tx(full, kQTileBytes);
+          dev::tma_load_3d_hint(sA + (uint32_t)s * kQTileBytes, p.a_map, (kt0 + kt) * (int)kQRowBytes, n0, l,
+                                full, a_policy);
+        } else {
+          const uint32_t dst = sA + (uint32_t)s * kAStageBytes;
+          const int k = (kt0 + kt) * kCtaK;
+          dev::mbar_arrive_expect_tx(full, kAStageBytes);
+          dev::tma_load_3d_hint(dst, p.a_map, k, n0, l, full, a_policy);
+          dev::tma_load_3d_hint(dst + kABoxBytes, p.a_map, k + kAtomK, n0, l, full, a_policy);
+        }
         a_issued = kt + 1;
       }
       stamp(p, kTrWeightsIssued);
@@ -305,12 +393,11 @@ __global__ void __launch_bounds__(kDecWG == 2 ? kThreadsW4Wide : kThreads, kDecW
           dev::tma_load_3d(dst + kBBox, &b_map, k + kAtomK, m0, l, bar_b);
         }
       }
-      for (int kt = 0; kt < (b_res ? 0 : k_tiles); ++kt) {
-        const int s = kt % stages;
-        const int r = kt / stages;
+      RingPos pos{0, 0u};
+      for (int kt = 0; kt < (b_res ? 0 : k_tiles); ++kt, pos.advance(1, stages)) {
+        const int s = pos.index;
         const uint32_t full = bar_full0 + 8u * s;
-        if (kt >= stages &&
-            !waiter.wait<false>(bar_empty0 + 8u * s, (uint32_t)((r - 1) & 1), kRoleActTma, kt)) {
+        if (kt >= stages && !waiter.wait<false>(bar_empty0 + 8u * s, pos.phase ^ 1u, kRoleActTma, kt)) {
           break;
         }
         const uint32_t dst = sB + (uint32_t)s * kBStage;
@@ -338,7 +425,8 @@ __global__ void __launch_bounds__(kDecWG == 2 ? kThreadsW4Wide : kThreads, kDecW
       const uint32_t d_acc = tmem_base + (uint32_t)issuer * kAccCols;
       bool ok = waiter.wait<false>(bar_b, 0u, kRoleMma, -1);
       dev::tc_fence_after();
-      for (int kt = issuer; kt < k_tiles && ok; kt += nis) {
+      RingPos sp = RingPos::at(issuer, slots);                  // TMEM slot of tile kt
+      for (int kt = issuer; kt < k_tiles && ok; kt += nis, sp.advance(nis, slots)) {
         const uint32_t first = (uint32_t)(kt >= nis);          // 0: this accumulator's first tile
         const uint32_t b_st = sB + (uint32_t)kt * kBStage;
         if (p.w4_smem_tiles && kt == slots) {
@@ -356,8 +444,8 @@ __global__ void __launch_bounds__(kDecWG == 2 ? kThreadsW4Wide : kThreads, kDecW
           }
           continue;
         }
-        const int slot = kt % slots;
-        ok = waiter.wait<false>(bar_slot_full0 + 8u * slot, (uint32_t)((kt / slots) & 1), kRoleMma, kt);
+        const int slot = sp.index;
+        ok = waiter.wait<false>(bar_slot_full0 + 8u * slot, sp.phase, kRoleMma, kt);
         if (!ok) break;
         dev::tc_fence_after();
         if (kt == 0) stamp(p, kTrFirstFull);
@@ -380,10 +468,10 @@ __global__ void __launch_bounds__(kDecWG == 2 ? kThreadsW4Wide : kThreads, kDecW
       // first `tmem_tiles` weight K tiles from the ring into tensor memory as
       // they land, so their stages take further tiles and more of the CTA's
       // weights are on chip when the previous kernel completes.
-      for (int kt = issuer; kt < tmem_tiles && ok; kt += nis) {
-        const int s = kt % stages;
-        const int r = kt / stages;
-        ok = waiter.wait<false>(bar_full0 + 8u * s, (uint32_t)(r & 1), kRoleMma, kt);
+      RingPos cpos = RingPos::at(issuer, stages);
+      for (int kt = issuer; kt < tmem_tiles && ok; kt += nis, cpos.advance(nis, stages)) {
+        const int s = cpos.index;
+        ok = waiter.wait<false>(bar_full0 + 8u * s, cpos.phase, kRoleMma, kt);
         if (!ok) break;
         dev::tc_fence_after();
         const uint32_t a_st = sA + (uint32_t)s * kAStageBytes;
@@ -399,9 +487,9 @@ __global__ void __launch_bounds__(kDecWG == 2 ? kThreadsW4Wide : kThreads, kDecW
         ok = waiter.wait<false>(bar_b, 0u, kRoleMma, -1);
         dev::tc_fence_after();
       }
-      for (int kt = issuer; kt < k_tiles && ok; kt += nis) {
-        const int s = kt % stages;
-        const int r = kt / stages;
+      RingPos pos = RingPos::at(issuer, stages);
+      for (int kt = issuer; kt < k_tiles && ok; kt += nis, pos.advance(nis, stages)) {
+        const int s = pos.index;
         const uint32_t first = (uint32_t)(kt >= nis);          // 0: this accumulator's first tile
         const uint32_t b_st = sB + (uint32_t)(b_res ? kt : s) * kBStage;
         if (kt == issuer) stamp(p, kTrFirstFull);
@@ -417,7 +505,7 @@ __global__ void __launch_bounds__(kDecWG == 2 ? kThreadsW4Wide : kThreads, kDecW
           }
           continue;
         }
-        ok = waiter.wait<false>(bar_full0 + 8u * s, (uint32_t)(r & 1), kRoleMma, kt);
+        ok = waiter.wait<false>(bar_full0 + 8u * s, pos.phase, kRoleMma, kt);
         if (!ok) break;
         dev::tc_fence_after();
         if (kt == k_tiles - 1) stamp(p, kTrLastFull);
@@ -443,24 +531,29 @@ __global__ void __launch_bounds__(kDecWG == 2 ? kThreadsW4Wide : kThreads, kDecW
     const bool row_ok = n0 + row < p.N;
     const uint8_t* srow =
         p.a_scale + ((size_t)l * p.N + (size_t)(row_ok ? n0 + row : 0)) * (size_t)(p.K / 32) + (size_t)kt0 * 4;
-    for (int kt = 0; kt < k_tiles; ++kt) {
+    ScaleWords scales;
+    scales.load(reinterpret_cast<const uint32_t*>(srow), row_ok, k_tiles);
+    RingPos cp{0, 0u}, sp{0, 0u};   // code-ring stage and TMEM slot of tile kt
+    for (int kt = 0; kt < k_tiles; ++kt, cp.advance(1, stages), sp.advance(1, slots)) {
       if (p.w4_smem_tiles && kt == slots) {
-        waiter.wait<false>(bar_full0 + 8u * kt, 0u, kRoleEpiDecode, kt);
-        const uint32_t codes = row_ok ? __ldg(reinterpret_cast<const uint32_t*>(srow) + kt) : 0u;
-        w4_decode_stage(kt, row, codes, kEpiJ1, 4);
+        code_wait(cp, kt);
+        const uint32_t codes = scales.take();
+        w4_decode_stage(cp.index, row, codes, kEpiJ1, 4);
+        code_free(kt, cp.index);
         dev::fence_proxy_async_shared();
-        dev::mbar_arrive(bar_w4_stage);
+        warp_arrive(bar_w4_stage);
         continue;
       }
-      const int slot = kt % slots;
-      const int round = kt / slots;
-      if (round > 0) waiter.wait<false>(bar_slot_empty0 + 8u * slot, (uint32_t)((round - 1) & 1), kRoleEpiDecode, kt);
-      waiter.wait<false>(bar_full0 + 8u * kt, 0u, kRoleEpiDecode, kt);
-      const uint32_t codes = row_ok ? __ldg(reinterpret_cast<const uint32_t*>(srow) + kt) : 0u;
-      w4_decode_tmem(kt, row, codes, t_row2 + p.tmem_tile_col0 + (uint32_t)slot * kTmemTileCols, kEpiJ1, 4);
+      const int slot = sp.index;
+      // the slot's previous tile (kt - slots) read by the MMAs
+      if (kt >= slots) waiter.wait<false>(bar_slot_empty0 + 8u * slot, sp.phase ^ 1u, kRoleEpiDecode, kt);
+      code_wait(cp, kt);
+      const uint32_t codes = scales.take();
+      w4_decode_tmem(cp.index, row, codes, t_row2 + p.tmem_tile_col0 + (uint32_t)slot * kTmemTileCols, kEpiJ1, 4);
+      code_free(kt, cp.index);
       dev::tmem_wait_st();
       dev::tc_fence_before();
-      dev::mbar_arrive(bar_slot_full0 + 8u * slot);
+      warp_arrive(bar_slot_full0 + 8u * slot);
     }
   } else if (warp >= 4) {
     // ---- epilogue: thread et owns TMEM lane et = weight row n0 + et.
@@ -533,28 +626,33 @@ __global__ void __launch_bounds__(kDecWG == 2 ? kThreadsW4Wide : kThreads, kDecW
       const bool row_ok = n0 + et < p.N;
       const uint8_t* srow =
           p.a_scale + ((size_t)l * p.N + (size_t)(row_ok ? n0 + et : 0)) * (size_t)(p.K / 32) + (size_t)kt0 * 4;
-      for (int kt = 0; kt < k_tiles; ++kt) {
+      ScaleWords scales;
+      scales.load(reinterpret_cast<const uint32_t*>(srow), row_ok, k_tiles);
+      RingPos cp{0, 0u}, sp{0, 0u};   // code-ring stage and TMEM slot of tile kt
+      for (int kt = 0; kt < k_tiles; ++kt, cp.advance(1, stages), sp.advance(1, slots)) {
         if (kt == slots && p.b_loader && !p.w4_smem_tiles) load_activations();
         if (p.w4_smem_tiles && kt == slots) {
           // the tile after the TMEM slots: decoded before the wait into the
           // bf16 stage in shared memory
-          waiter.wait<false>(bar_full0 + 8u * kt, 0u, kRoleEpiDecode, kt);
-          const uint32_t codes = row_ok ? __ldg(reinterpret_cast<const uint32_t*>(srow) + kt) : 0u;
-          w4_decode_stage(kt, et, codes, 0, kEpiJ1);
+          code_wait(cp, kt);
+          const uint32_t codes = scales.take();
+          w4_decode_stage(cp.index, et, codes, 0, kEpiJ1);
+          code_free(kt, cp.index);
           dev::fence_proxy_async_shared();   // generic-proxy stores, read by tcgen05.mma
-          dev::mbar_arrive(bar_w4_stage);
+          warp_arrive(bar_w4_stage);
           if (p.b_loader) load_activations();   // the stage is the last tile
           continue;
         }
-        const int slot = kt % slots;
-        const int round = kt / slots;
-        if (round > 0) waiter.wait<false>(bar_slot_empty0 + 8u * slot, (uint32_t)((round - 1) & 1), kRoleEpiDecode, kt);
-        waiter.wait<false>(bar_full0 + 8u * kt, 0u, kRoleEpiDecode, kt);
-        const uint32_t codes = row_ok ? __ldg(reinterpret_cast<const uint32_t*>(srow) + kt) : 0u;
-        w4_decode_tmem(kt, et, codes, t_row + p.tmem_tile_col0 + (uint32_t)slot * kTmemTileCols, 0, kEpiJ1);
+        const int slot = sp.index;
+        // the slot's previous tile (kt - slots) read by the MMAs
+        if (kt >= slots) waiter.wait<false>(bar_slot_empty0 + 8u * slot, sp.phase ^ 1u, kRoleEpiDecode, kt);
+        code_wait(cp, kt);
+        const uint32_t codes = scales.take();
+        w4_decode_tmem(cp.index, et, codes, t_row + p.tmem_tile_col0 + (uint32_t)slot * kTmemTileCols, 0, kEpiJ1);
+        code_free(kt, cp.index);
         dev::tmem_wait_st();
         dev::tc_fence_before();
-        dev::mbar_arrive(bar_slot_full0 + 8u * slot);
+        warp_arrive(bar_slot_full0 + 8u * slot);
       }
       if (p.b_loader && k_tiles <= slots) load_activations();
     } else if (p.b_loader) {
@@ -842,14 +940,9 @@ __global__ void __launch_bounds__(kDecWG == 2 ? kThreadsW4Wide : kThreads, kDecW
     // before the stage was refilled.
     const unsigned long long drain_ns = 10000000ull;   // 10 ms
     if (threadIdx.x == 0) {
-      if (kW4) {
-        // one barrier per packed tile, used once
-        for (int kt = 0; kt < a_issued; ++kt) drain_wait(bar_full0 + 8u * kt, 0u, drain_ns);
-      } else {
-        for (int s = 0; s < a_issued && s < stages; ++s) {
-          const int round = (a_issued - 1 - s) / stages;   // of the last tile issued to stage s
-          drain_wait(bar_full0 + 8u * s, (uint32_t)(round & 1), drain_ns);
-        }
+      for (int s = 0; s < a_issued && s < stages; ++s) {
+        const int round = (a_issued - 1 - s) / stages;   // of the last tile issued to stage s
+        drain_wait(bar_full0 + 8u * s, (uint32_t)(round & 1), drain_ns);
       }
     }
     if (warp == 1 && lane == 0 && b_issued) drain_wait(bar_b, 0u, drain_ns);

@@ -70,6 +70,26 @@ __device__ __noinline__ bool drain_wait(uint32_t bar, uint32_t parity, unsigned 
   return true;
 }
 
+// A position in a ring of n entries after `count` uses: the entry
+// count % n and the parity of count / n, kept by additions.  (An integer
+// division by a runtime value is a long dependent instruction sequence; in a
+// per-tile loop it sits on the critical path.)
+struct RingPos {
+  int index;
+  uint32_t phase;
+  __device__ __forceinline__ static RingPos at(int count, int n) {
+    return RingPos{count % n, (uint32_t)((count / n) & 1)};
+  }
+  // `by` more uses, 1 <= by <= n
+  __device__ __forceinline__ void advance(int by, int n) {
+    index += by;
+    if (index >= n) {
+      index -= n;
+      phase ^= 1u;
+    }
+  }
+};
+
 struct Waiter {
   uint32_t abort_flag;            // shared-memory u32, sticky per CTA
   unsigned long long limit_ns;

@@ -151,11 +151,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   dev::cluster_arrive_release();
   if (threadIdx.x == 0) {
     const int first = total_kt < stages ? total_kt : stages;
-    for (; a_issued < first; ++a_issued) {
-      const int j = a_issued / k_tiles;
-      const int kt = a_issued - j * k_tiles;
-      int n0, m0, l;
-      tile_coords(j, &n0, &m0, &l);
+    int j = 0, kt = 0, n0 = 0, m0 = 0, l = 0;
+    if (first > 0) tile_coords(0, &n0, &m0, &l);
+    for (; a_issued < first; ++a_issued, ++kt) {
+      if (kt == k_tiles) {
+        kt = 0;
+        tile_coords(++j, &n0, &m0, &l);
+      }
       const uint32_t full = bar_full0 + 8u * a_issued;
       const uint32_t dst = sA + (uint32_t)a_issued * kAStageBytes;
       const int k = (kt0 + kt) * kCtaK;
@@ -184,14 +186,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ---- weight producer: the ring continues across tiles
     if (lane == 0) {
-      for (int g = a_issued; g < total_kt; ++g) {
-        const int s = g % stages;
-        const int r = g / stages;
-        if (!waiter.wait<false>(bar_empty0 + 8u * s, (uint32_t)((r - 1) & 1), kRoleWeightTma, g)) break;
-        const int j = g / k_tiles;
-        const int kt = g - j * k_tiles;
-        int n0, m0, l;
-        tile_coords(j, &n0, &m0, &l);
+      // ring position and (output tile, K tile) of global load g, kept by
+      // additions; the tile's coordinates recomputed once per output tile
+      RingPos pos = RingPos::at(a_issued, stages);
+      int j = a_issued / k_tiles;
+      int kt = a_issued - j * k_tiles;
+      int n0 = 0, m0 = 0, l = 0;
+      if (a_issued < total_kt) tile_coords(j, &n0, &m0, &l);
+      for (int g = a_issued; g < total_kt; ++g, pos.advance(1, stages)) {
+        if (kt == k_tiles) {
+          kt = 0;
+          tile_coords(++j, &n0, &m0, &l);
+        }
+        const int s = pos.index;
+        if (!waiter.wait<false>(bar_empty0 + 8u * s, pos.phase ^ 1u, kRoleWeightTma, g)) break;
         const uint32_t full = bar_full0 + 8u * s;
         const uint32_t dst = sA + (uint32_t)s * kAStageBytes;
         const int k = (kt0 + kt) * kCtaK;
@@ -199,6 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         dev::tma_load_3d_hint(dst, p.a_map, k, n0, l, full, a_policy);
         dev::tma_load_3d_hint(dst + kABoxBytes, p.a_map, k + kAtomK, n0, l, full, a_policy);
         a_issued = g + 1;
+        ++kt;
       }
       stamp(p, kTrWeightsIssued);
       dev::griddep_launch_dependents();
@@ -208,17 +217,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       dev::griddep_wait();
       stamp(p, kTrActReady);
-      for (int g = 0; g < total_kt; ++g) {
-        const int s = g % stages;
-        const int r = g / stages;
-        if (g >= stages &&
-            !waiter.wait<false>(bar_empty0 + 8u * s, (uint32_t)((r - 1) & 1), kRoleActTma, g)) {
+      RingPos pos{0, 0u};
+      int j = 0, kt = 0, n0 = 0, m0 = 0, l = 0;
+      if (total_kt > 0) tile_coords(0, &n0, &m0, &l);
+      for (int g = 0; g < total_kt; ++g, pos.advance(1, stages)) {
+        if (kt == k_tiles) {
+          kt = 0;
+          tile_coords(++j, &n0, &m0, &l);
+        }
+        const int s = pos.index;
+        if (g >= stages && !waiter.wait<false>(bar_empty0 + 8u * s, pos.phase ^ 1u, kRoleActTma, g)) {
           break;
         }
-        const int j = g / k_tiles;
-        const int kt = g - j * k_tiles;
-        int n0, m0, l;
-        tile_coords(j, &n0, &m0, &l);
         const uint32_t full = bar_full0 + 8u * s;
         const uint32_t dst = sB + (uint32_t)s * kBStage;
         const int k = (kt0 + kt) * kCtaK;
@@ -226,6 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         dev::tma_load_3d(dst, &b_map, k, m0, l, full);
         dev::tma_load_3d(dst + kBBox, &b_map, k + kAtomK, m0, l, full);
         b_issued = g + 1;
+        ++kt;
       }
     }
   } else if (warp == 2) {
@@ -234,6 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       bool ok = true;
       int g = 0;
+      RingPos pos{0, 0u};                            // ring position of load g
       for (int j = 0; j < my_tiles && ok; ++j) {
         const int buf = j & 1;
         const int use = j >> 1;
@@ -243,10 +255,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           dev::tc_fence_after();
         }
         const uint32_t d_acc = tmem_base + (uint32_t)buf * kAccCols;
-        for (int kt = 0; kt < k_tiles; ++kt, ++g) {
-          const int s = g % stages;
-          const int r = g / stages;
-          ok = waiter.wait<false>(bar_full0 + 8u * s, (uint32_t)(r & 1), kRoleMma, g);
+        for (int kt = 0; kt < k_tiles; ++kt, ++g, pos.advance(1, stages)) {
+          const int s = pos.index;
+          ok = waiter.wait<false>(bar_full0 + 8u * s, pos.phase, kRoleMma, g);
           if (!ok) break;
           dev::tc_fence_after();
           if (g == 0) stamp(p, kTrFirstFull);

@@ -534,12 +534,16 @@ def test_w8a16_plans(args):
     M, N, K, L, split = args
     p = sk.splitk_plan_w8a16_for(*args, **GB300)
     assert p.weight_format == sk.WEIGHTS_E4M3_E8M0
-    assert p.stages == p.k_tiles_per_cta <= 8 and p.b_resident == 1
+    assert min(2, p.k_tiles_per_cta) <= p.stages <= p.k_tiles_per_cta <= 8 and p.b_resident == 1
     assert 1 <= p.a_tmem_tiles <= 3 and p.mma_n in (16, 32) and p.w4_decoders in (1, 2)
     assert _check(p, M, N, K, L) == 0
-    # 16 KiB of codes a K tile: the layout holds them all
+    # 16 KiB of codes a K tile: the layout holds the ring of them
     b_tiles = max(2, p.k_tiles_per_cta)
-    assert p.smem_bytes >= 1024 + p.k_tiles_per_cta * 16384 + b_tiles * p.mma_n * 256 + p.w4_smem_tiles * 32768
+    assert p.smem_bytes >= 1024 + p.stages * 16384 + b_tiles * p.mma_n * 256 + p.w4_smem_tiles * 32768
+    # a ring shorter than the CTA's tiles only where all of them would not fit two CTAs an SM
+    if p.stages < p.k_tiles_per_cta:
+        assert p.smem_bytes + 1024 <= GB300["smem_per_sm"] // 2
+        assert p.smem_bytes + 16384 + 1024 > GB300["smem_per_sm"] // 2     # one stage more would not
     # a 4-bit plan of the same shape is not an 8-bit one
     w4 = sk.splitk_plan_w4a16_for(*args, **GB300)
     bad = sk.Plan.from_buffer_copy(w4)

@@ -894,3 +894,38 @@ def test_w8a16_all_ones_closed_form():
     c = to_host(sk.splitk_gemm_w8a16(_u8_dev(aq), _u8_dev(a_s), to_dev(b), split_k=4))
     torch.cuda.synchronize()
     assert np.all(c == oracle.f64_to_bf16(4.0 * K))
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_quantized_code_rings_agree(bits):
+    """The packed codes in a ring of 1, 2 or 4 stages instead of all of a
+    CTA's 7 tiles at once (each stage refilled once every decoder has read
+    it): the same bits, within the oracle's tolerance, with one and two
+    decoding warpgroups."""
+    L, M, N, K, split = 1, 16, 512, 7168, 8
+    if bits == 4:
+        aq, a_s, b = _w4_draw(L, M, N, K, seed=3600)
+        plan, run, ref = sk.splitk_plan_w4a16, sk.splitk_gemm_w4a16_planned, oracle.gemm_w4a16(aq, a_s, b)
+        max_w = float(np.max(np.abs(oracle.w4_dequant(aq, a_s))))
+    else:
+        aq, a_s, b = _w8_draw(L, M, N, K, seed=3600)
+        plan, run, ref = sk.splitk_plan_w8a16, sk.splitk_gemm_w8a16_planned, oracle.gemm_w8a16(aq, a_s, b)
+        max_w = float(np.max(np.abs(oracle.w8_dequant(aq, a_s))))
+    ta, ts, tb = _u8_dev(aq), _u8_dev(a_s), to_dev(b)
+    base = plan(M, N, K, L, split)
+    assert base.k_tiles_per_cta == 7
+    outs = []
+    for decoders in (1, 2):
+        for stages in (7, 4, 2, 1):
+            p = sk.Plan.from_buffer_copy(base)
+            p.smem_bytes += max(0, stages - base.stages) * (8192 if bits == 4 else 16384)
+            p.stages = stages
+            p.w4_decoders = decoders
+            for _ in range(2):
+                outs.append(to_host(run(ta, ts, tb, None, p)))
+    torch.cuda.synchronize()
+    assert sk.splitk_get_status() == 0, sk.splitk_get_fault()
+    for o in outs[1:]:
+        assert np.array_equal(o, outs[0])
+    ok, rep = _tol.check(outs[0], ref, K, max_w, _tol.max_abs_bf16(b))
+    assert ok, rep
