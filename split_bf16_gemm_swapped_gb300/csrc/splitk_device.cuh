@@ -308,26 +308,26 @@ __device__ __forceinline__ uint32_t e4m3x2_placed(uint32_t w) {
   return (prmt(w, 0u, sel) << 4) & 0x87F087F0u;
 }
 
-// The multipliers of one 32-k block with E8M0 scale code `code`, for placed
-// codes worth x * 2^-kShift: one product by 2^(code - 127 + kShift) when
-// that is a normal bf16 (code in 1 .. 254 - kShift), else two, by 2^kShift
-// (exact: the placed value times it is x) and by the scale as a bf16
-// (code 0: zero; 255: infinity).  Either way the result is x times the
-// scale rounded once, the value of the exact product.
+// The multipliers of a 32-k block with E8M0 scale code `code`, for placed
+// codes worth x * 2^-kShift.  Fast form: one product by
+// 2^(code - 127 + kShift), a normal bf16 for code in 1 .. 254 - kShift.
+// Slow form (any other code): two products, by 2^kShift (exact: the placed
+// value times it is x) and by the scale as a bf16 (code 0: zero; 255:
+// infinity).  Either way the result is x times the scale rounded once, the
+// value of the exact product.  The bf16 pair of 2^(f - 127) for an exponent
+// field f is f * 0x00800080 (f << 7 in each half).
 template <int kShift>
 struct BlockScale {
-  uint32_t m1, m2;
-  bool two;
-  __device__ __forceinline__ explicit BlockScale(uint32_t code) {
-    two = code - 1u >= (uint32_t)(254 - kShift);
-    const uint32_t f = two ? (uint32_t)(127 + kShift) : code + (uint32_t)kShift;   // bf16 exponent field
-    m1 = (f << 7) | (f << 23);
-    m2 = (code << 7) | (code << 23);
+  static constexpr uint32_t kSlowFirst = (uint32_t)(127 + kShift) * 0x00800080u;
+  __device__ __forceinline__ static bool fast(uint32_t code) { return code - 1u < (uint32_t)(254 - kShift); }
+  // the per-block multiplier of the chosen form
+  template <bool kTwo>
+  __device__ __forceinline__ static uint32_t multiplier(uint32_t code) {
+    return kTwo ? code * 0x00800080u : code * 0x00800080u + (uint32_t)kShift * 0x00800080u;
   }
   template <bool kTwo>
-  __device__ __forceinline__ uint32_t apply(uint32_t placed) const {
-    const uint32_t y = bf16x2_mul(placed, m1);
-    return kTwo ? bf16x2_mul(y, m2) : y;
+  __device__ __forceinline__ static uint32_t apply(uint32_t placed, uint32_t m) {
+    return kTwo ? bf16x2_mul(bf16x2_mul(placed, kSlowFirst), m) : bf16x2_mul(placed, m);
   }
 };
 

@@ -489,12 +489,14 @@ int plan_w4_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t sm
                             smem_bytes_w4(mma_n, kt, code_stages, ded, 1, fmt) + 1024 <= smem_per_sm / 2
                         ? 1
                         : 0;
-  // A second decoding warpgroup halves every tile's decode (384 threads a
-  // CTA: at most 2 CTAs an SM by registers).  Measured on GB300 it pays from
-  // 5 K tiles a CTA (small-batch decode, 7 tiles: 12.17 -> 11.76 us; M=16,
-  // L=4: 48.1 -> 45.9 us) and costs at 4 (single-token decode: 6.56 ->
-  // 6.67 us), where the next kernel's CTAs find fewer free registers.
-  p.w4_decoders = kt >= 5 ? 2 : 1;
+  // One decoding warpgroup.  The decode (about four instructions a weight
+  // pair) is bound by the SM's instruction issue, which a second warpgroup
+  // (384 threads a CTA, at most 2 CTAs an SM by registers) barely raises
+  // while it takes registers the next kernel's CTAs could use.  Measured on
+  // GB300: small-batch decode (7 tiles a CTA) 11.47 us with two groups,
+  // 11.29 with one; M=16, L=4 45.2 -> 44.1 us; single-token decode 7.14 ->
+  // 6.27 us.  Plans may still ask for two (w4_decoders = 2).
+  p.w4_decoders = 1;
   // Shared memory padded when needed so that the CTAs fitting an SM can
   // hold their TMEM.
   auto padded_smem = [&](size_t smem, uint32_t tmem_cols) {

@@ -41,7 +41,6 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include <type_traits>
 
 #include "splitk.h"
 #include "splitk_device.cuh"
@@ -67,6 +66,88 @@ struct ScaleWords {
     return x;
   }
 };
+
+// ---- decode of packed weight codes to bf16 (quantized weights)
+//
+// Decode of the 32-k steps [j0, j1) of one weight row of a packed tile, each
+// step one scale block (scale code byte j of `codes`), into 16 words of bf16
+// pairs: E2M1 codes are 64 B a row in the 64-byte swizzle (step j is the
+// 16-byte chunk at slot j ^ ((row >> 1) & 3)), a byte -> two bf16; E4M3
+// codes are 128 B a row in the 128-byte swizzle (step j is chunks 2j and
+// 2j + 1 at slots c ^ (row & 7)), two bytes -> two bf16.  Both place the
+// code bits in bf16 lanes (exact, a constant power of two apart from the
+// code's value) and take one bf16 product by a power of two (two for scale
+// codes out of that product's range), exact wherever the scaled weight is a
+// bf16 value.
+template <int kFmt>
+struct QFmt {
+  static constexpr int kCodeWords = kFmt == 2 ? 8 : 4;   // 32-bit words of codes a step
+  using Scale = dev::BlockScale<kFmt == 2 ? 120 : 126>;
+};
+
+template <int kFmt>
+__device__ __forceinline__ void q_load_step(uint32_t src, int j, int row, uint32_t (&w)[QFmt<kFmt>::kCodeWords]) {
+  if constexpr (kFmt == 2) {
+    dev::ld_shared_v4(src + (uint32_t)(((2 * j) ^ (row & 7)) * 16), w[0], w[1], w[2], w[3]);
+    dev::ld_shared_v4(src + (uint32_t)(((2 * j + 1) ^ (row & 7)) * 16), w[4], w[5], w[6], w[7]);
+  } else {
+    dev::ld_shared_v4(src + (uint32_t)((j ^ ((row >> 1) & 3)) * 16), w[0], w[1], w[2], w[3]);
+  }
+}
+
+// One step's 16 pairs with the block multiplier `m` of the form kTwo.
+template <int kFmt, bool kTwo>
+__device__ __forceinline__ void q_convert_step(const uint32_t (&w)[QFmt<kFmt>::kCodeWords], uint32_t m,
+                                               uint32_t (&r)[16]) {
+  using S = typename QFmt<kFmt>::Scale;
+  if constexpr (kFmt == 2) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      r[2 * i] = S::template apply<kTwo>(dev::e4m3x2_placed<0>(w[i]), m);
+      r[2 * i + 1] = S::template apply<kTwo>(dev::e4m3x2_placed<1>(w[i]), m);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t w4 = w[i] << 4;
+      r[4 * i + 0] = S::template apply<kTwo>(dev::e2m1x2_placed<0>(w[i], w4), m);
+      r[4 * i + 1] = S::template apply<kTwo>(dev::e2m1x2_placed<1>(w[i], w4), m);
+      r[4 * i + 2] = S::template apply<kTwo>(dev::e2m1x2_placed<2>(w[i], w4), m);
+      r[4 * i + 3] = S::template apply<kTwo>(dev::e2m1x2_placed<3>(w[i], w4), m);
+    }
+  }
+}
+
+// Whether every scale code of steps [j0, j1) takes the one-product form
+// (the form is chosen once for a row's steps of a tile).
+template <int kFmt>
+__device__ __forceinline__ bool q_row_fast(uint32_t codes, int j0, int j1) {
+  bool fast = true;
+#pragma unroll 1
+  for (int j = j0; j < j1; ++j) fast = fast && QFmt<kFmt>::Scale::fast((codes >> (8 * j)) & 0xFFu);
+  return fast;
+}
+
+// Steps [j0, j1) of the row at `src` (j1 - j0 even: 4, or 2 with two
+// decoding warpgroups), two at a time through two code buffers, each step's
+// codes loaded a step ahead so that the load latency overlaps the previous
+// step's conversion; `emit(j, r)` stores step j's 16 words.
+template <int kFmt, bool kTwo, class Emit>
+__device__ __forceinline__ void q_steps(uint32_t src, int row, uint32_t codes, int j0, int j1, Emit& emit) {
+  using S = typename QFmt<kFmt>::Scale;
+  uint32_t a[QFmt<kFmt>::kCodeWords], b[QFmt<kFmt>::kCodeWords];
+  q_load_step<kFmt>(src, j0, row, a);
+#pragma unroll 1
+  for (int j = j0; j < j1; j += 2) {
+    q_load_step<kFmt>(src, j + 1, row, b);
+    uint32_t ra[16], rb[16];
+    q_convert_step<kFmt, kTwo>(a, S::template multiplier<kTwo>((codes >> (8 * j)) & 0xFFu), ra);
+    emit(j, ra);
+    if (j + 2 < j1) q_load_step<kFmt>(src, j + 2, row, a);
+    q_convert_step<kFmt, kTwo>(b, S::template multiplier<kTwo>((codes >> (8 * j + 8)) & 0xFFu), rb);
+    emit(j + 1, rb);
+  }
+}
 
 // kFmt: the weight format (0 bf16; 1 E2M1 codes, 2 E4M3 codes, each with
 // E8M0 scales per 32 k, decoded on chip).  kDecWG: warpgroups decoding
@@ -236,75 +317,18 @@ __global__ void __launch_bounds__(kDecWG == 2 ? kThreadsW4Wide : kThreads, kDecW
   }
   if (threadIdx.x == 128) stamp(p, kTrEpiSynced);
 
-  // Decode of the 32-k steps [j0, j1) of weight row `row` of packed tile kt,
-  // each step one scale block (scale code byte j of `codes`), into 16 words
-  // of bf16 pairs: E2M1 codes are 64 B a row in the 64-byte swizzle (step j
-  // is the 16-byte chunk at slot j ^ ((row >> 1) & 3)), a byte -> two bf16;
-  // E4M3 codes are 128 B a row in the 128-byte swizzle (step j is chunks 2j
-  // and 2j + 1 at slots c ^ (row & 7)), two bytes -> two bf16.  Both place
-  // the code bits in bf16 lanes (exact, a constant power of two apart from
-  // the code's value) and take one bf16 product by a power of two (two for
-  // scale codes out of that product's range), exact wherever the scaled
-  // weight is a bf16 value.
-  //
-  // The loop is software-pipelined: step j + 1's codes are loaded from
-  // shared memory before step j is converted, so the load latency overlaps
-  // the conversions instead of stalling each step (the loads and the TMEM or
-  // shared-memory stores are ordered accesses the compiler keeps in program
-  // order).
-  constexpr int kCodeWords = kFmt == 2 ? 8 : 4;   // 32-bit words of codes a step
-  auto q_load = [&](uint32_t src, int j, int row, uint32_t (&w)[kCodeWords]) {
-    if constexpr (kFmt == 2) {
-      dev::ld_shared_v4(src + (uint32_t)(((2 * j) ^ (row & 7)) * 16), w[0], w[1], w[2], w[3]);
-      dev::ld_shared_v4(src + (uint32_t)(((2 * j + 1) ^ (row & 7)) * 16), w[kCodeWords - 4], w[kCodeWords - 3],
-                        w[kCodeWords - 2], w[kCodeWords - 1]);
-    } else {
-      dev::ld_shared_v4(src + (uint32_t)((j ^ ((row >> 1) & 3)) * 16), w[0], w[1], w[2], w[3]);
-    }
-  };
-  // One step's 16 pairs; scale code `code`.  The one-or-two-product choice
-  // is taken once a step (a branch, not a select per pair).
-  auto q_convert = [&](const uint32_t (&w)[kCodeWords], uint32_t code, uint32_t (&r)[16]) {
-    auto pairs = [&](auto two, const auto& bs) {
-      constexpr bool kTwo = decltype(two)::value;
-      if constexpr (kFmt == 2) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          r[2 * i] = bs.template apply<kTwo>(dev::e4m3x2_placed<0>(w[i]));
-          r[2 * i + 1] = bs.template apply<kTwo>(dev::e4m3x2_placed<1>(w[i]));
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint32_t w4 = w[i] << 4;
-          r[4 * i + 0] = bs.template apply<kTwo>(dev::e2m1x2_placed<0>(w[i], w4));
-          r[4 * i + 1] = bs.template apply<kTwo>(dev::e2m1x2_placed<1>(w[i], w4));
-          r[4 * i + 2] = bs.template apply<kTwo>(dev::e2m1x2_placed<2>(w[i], w4));
-          r[4 * i + 3] = bs.template apply<kTwo>(dev::e2m1x2_placed<3>(w[i], w4));
-        }
-      }
-    };
-    const dev::BlockScale<kFmt == 2 ? 120 : 126> bs(code);
-    if (bs.two) {
-      pairs(std::true_type{}, bs);
-    } else {
-      pairs(std::false_type{}, bs);
-    }
-  };
-  // Steps [j0, j1) of one row: `emit(j, r)` stores step j's 16 words.
+  // Decode of the 32-k steps [j0, j1) of weight row `row` of the packed tile
+  // in code-ring stage `stage` (q_steps above).
+  // The form is chosen for the whole warp (a vote): the steps end in
+  // warp-collective stores (tcgen05.st.sync.aligned), which every lane must
+  // reach at the same instruction.  The two-product form is exact for every
+  // code, so a lane that could use one product loses only time.
   auto q_decode_row = [&](int stage, int row, uint32_t codes, int j0, int j1, auto&& emit) {
     const uint32_t src = sA + (uint32_t)stage * kQTileBytes + (uint32_t)row * kQRowBytes;
-    uint32_t next[kCodeWords];
-    q_load(src, j0, row, next);
-#pragma unroll 1
-    for (int j = j0; j < j1; ++j) {
-      uint32_t cur[kCodeWords];
-#pragma unroll
-      for (int i = 0; i < kCodeWords; ++i) cur[i] = next[i];
-      if (j + 1 < j1) q_load(src, j + 1, row, next);
-      uint32_t r[16];
-      q_convert(cur, (codes >> (8 * j)) & 0xFFu, r);
-      emit(j, r);
+    if (__all_sync(0xffffffffu, q_row_fast<kFmt>(codes, j0, j1))) {
+      q_steps<kFmt, false>(src, row, codes, j0, j1, emit);
+    } else {
+      q_steps<kFmt, true>(src, row, codes, j0, j1, emit);
     }
   };
   // Into TMEM columns t_col + 16 j of the thread's lane, or into the bf16

@@ -505,7 +505,7 @@ def test_w4a16_grids_of_several_waves_trade_tmem_slots_for_residency():
     assert one.a_tmem_tiles == 3 and one.ctas_per_sm == 2
     assert one.w4_decoders == 1                                      # 4 K tiles a CTA: one decoding warpgroup
     small_batch = sk.splitk_plan_w4a16_for(16, 4096, 7168, 1, 8, **GB300)
-    assert small_batch.k_tiles_per_cta == 7 and small_batch.w4_decoders == 2 and small_batch.ctas_per_sm == 2
+    assert small_batch.k_tiles_per_cta == 7 and small_batch.w4_decoders == 1 and small_batch.ctas_per_sm == 2
     many = sk.splitk_plan_w4a16_for(1, 7168, 2048, 8, 4, **GB300)   # 1792 CTAs
     assert (many.a_tmem_tiles, many.mma_issuers, many.w4_smem_tiles, many.w4_decoders) == (1, 1, 0, 1)
     assert many.ctas_per_sm == 3 and many.ctas_per_sm * many.tmem_cols <= 512
