@@ -262,13 +262,17 @@ int plan_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t smem_
   const int rc = plan_ring_impl(M, N, K, L, split_k, num_sms, smem_per_sm, smem_optin, out);
   if (rc != SPLITK_OK) return rc;
   const int split = out->split_k;
-  const long long tiles = tiles_of(M, out->mma_n) * tiles_of(N, kMmaM) * L;
+  // Split 2 with at least 128 tokens: 64-token tiles (twice the tiles, dealt
+  // out evenly; M = 128 sweep point 0.73 -> 0.77 of the HBM copy bandwidth).
+  const bool two_wide = split == 2 && M >= 128;
+  const int pers_n = two_wide ? 64 : 0;
+  const long long tiles = tiles_of(M, pers_n != 0 ? pers_n : out->mma_n) * tiles_of(N, kMmaM) * L;
   const long long clusters = std::max(1, num_sms / split);
   const long long rounds = (tiles + clusters - 1) / clusters;
   const bool balanced = (double)tiles >= 0.9 * (double)(rounds * clusters);
-  if ((split == 8 || (split == 4 && out->mma_n >= 64)) && tiles * split > num_sms && balanced) {
+  if ((split == 8 || (split == 4 && out->mma_n >= 64) || two_wide) && tiles * split > num_sms && balanced) {
     splitk_plan_t p;
-    if (persistent_plan(M, N, K, L, split, 0, 0, num_sms, smem_per_sm, smem_optin, &p)) *out = p;
+    if (persistent_plan(M, N, K, L, split, 0, 0, num_sms, smem_per_sm, smem_optin, &p, pers_n)) *out = p;
   }
   return SPLITK_OK;
 }

@@ -149,6 +149,9 @@ def test_plan_of_the_decode_workloads():
     assert _plan(16, 7168, 16384, 2, 8).persistent == 1
     assert _plan(16, 7168, 16384, 2, 4).persistent == 0  # narrow tiles at split 4: the per-tile kernel
     assert _plan(64, 7168, 16384, 2, 4).persistent == 1
+    p2 = _plan(128, 7168, 16384, 2, 2)             # split 2, 128 tokens: 64-token tiles, 224 over 76 clusters
+    assert (p2.persistent, p2.mma_n, p2.split_k) == (1, 64, 2)
+    assert _plan(64, 7168, 16384, 2, 2).persistent == 0   # fewer tokens at split 2: the per-tile kernel
     assert p.reduce_rounds >= 1 and p.mailbox_quads % 4 == 0
 
 
@@ -231,7 +234,8 @@ def test_every_plan_fits_and_is_consistent(M, split):
     K = 128 * 8 * 4 - 8 * (M % 5)                  # some ragged K
     p = _plan(M, 7168, K, 2, split)
     assert p.k_tiles_per_cta == -(-(-(-K // 128)) // split)
-    assert p.mma_n >= min(M, 128) or p.mma_n == 128
+    # 64-token tiles: the persistent kernel at split 2 with 128 or more tokens
+    assert p.mma_n >= min(M, 128) or p.mma_n == 128 or (p.persistent and split == 2 and M >= 128 and p.mma_n == 64)
     if p.persistent:
         _check_persistent(p, M, 7168, K, 2, split)
         return
