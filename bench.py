@@ -770,6 +770,8 @@ NCU_SUMMARY_METRICS = [
     ("sm__pipe_tensor_cycles_active.avg.pct_of_peak_sustained_active", "tensor pipe active, % of SM-active"),
     ("sm__issue_active.avg.pct_of_peak_sustained_elapsed", "SM issue active, %"),
     ("sm__warps_active.avg.pct_of_peak_sustained_active", "warps active, % of peak"),
+    ("smsp__inst_executed.sum", "warp instructions executed"),
+    ("sm__icc_request_hit_rate.pct", "SM instruction-cache hit rate, %"),
     ("launch__registers_per_thread", "registers per thread"),
     ("launch__shared_mem_per_block_dynamic", "dynamic shared memory per CTA"),
     ("launch__grid_size", "CTAs"),

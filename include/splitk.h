@@ -271,8 +271,10 @@ SPLITK_API int splitk_gemm_w4a16_planned(const void *a_q, const void *a_scale,
  *   a_scale  device, [L][N][K/32] bytes, 4-byte aligned.  Codes 3..246 keep
  *            every decoded weight a finite bf16 value with no bits below
  *            2^-133 (exact); outside that range the decode saturates or
- *            rounds as bf16 arithmetic does, and the not-a-number codes give
- *            not-a-number weights.
+ *            rounds as bf16 arithmetic does (0 and 255 as for the 4-bit
+ *            weights).  The two not-a-number weight codes are outside the
+ *            contract: they decode as +-480 times the scale (their bits
+ *            placed like those of any other code).
  *   b, c     as splitk_gemm_bf16().
  * K must be a multiple of 128, M at most 32, and a CTA's K slice at most 8
  * tiles of 128 (else SPLITK_ERR_INVALID_SHAPE / SPLITK_ERR_NO_FIT).  The

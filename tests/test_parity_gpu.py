@@ -929,3 +929,22 @@ def test_quantized_code_rings_agree(bits):
         assert np.array_equal(o, outs[0])
     ok, rep = _tol.check(outs[0], ref, K, max_w, _tol.max_abs_bf16(b))
     assert ok, rep
+
+
+def test_w8a16_not_a_number_codes_decode_as_documented():
+    """The two E4M3 not-a-number codes are outside the contract; the header
+    documents that they decode as +-480 times the scale.  One-hot
+    activations read them out."""
+    L, M, N, K = 1, 4, 128, 128
+    aq = np.full((L, N, K), 0x38, np.uint8)          # 1.0 elsewhere
+    aq[0, 0:64, 5] = 0x7F
+    aq[0, 64:128, 5] = 0xFF
+    a_s = np.full((L, N, K // 32), 120, np.uint8)    # 2^-7
+    b = np.zeros((L, M, K), np.uint16)
+    b[0, 0, 5] = ONE
+    c = to_host(sk.splitk_gemm_w8a16(_u8_dev(aq), _u8_dev(a_s), to_dev(b), split_k=1))
+    torch.cuda.synchronize()
+    assert sk.splitk_get_status() == 0
+    assert np.all(c[0, 0, :64] == oracle.f64_to_bf16(480.0 * 2.0 ** -7))
+    assert np.all(c[0, 0, 64:] == oracle.f64_to_bf16(-480.0 * 2.0 ** -7))
+    assert np.all(c[0, 1:] == 0)
