@@ -262,9 +262,10 @@ int plan_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t smem_
   const int rc = plan_ring_impl(M, N, K, L, split_k, num_sms, smem_per_sm, smem_optin, out);
   if (rc != SPLITK_OK) return rc;
   const int split = out->split_k;
-  // Split 2 with at least 128 tokens: 64-token tiles (twice the tiles, dealt
-  // out evenly; M = 128 sweep point 0.73 -> 0.77 of the HBM copy bandwidth).
-  const bool two_wide = split == 2 && M >= 128;
+  // Split 2 with at least 64 tokens: 64-token tiles where they deal out
+  // evenly (M = 128 sweep point, twice the tiles: 0.73 -> 0.77 of the HBM
+  // copy bandwidth; the wide projection, 144 tiles: 46.1 -> 45.5 us).
+  const bool two_wide = split == 2 && M >= 64;
   const int pers_n = two_wide ? 64 : 0;
   const long long tiles = tiles_of(M, pers_n != 0 ? pers_n : out->mma_n) * tiles_of(N, kMmaM) * L;
   const long long clusters = std::max(1, num_sms / split);
@@ -346,7 +347,12 @@ int plan_ring_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t 
     out->cluster[2] = 1;
     out->smem_bytes = smem_bytes_for(mma_n, stages, ded, stages);
     out->ctas_per_sm = per_sm_v;
-    out->pdl_trigger = 0;
+    // The early trigger when the grid leaves SMs free: the next launch's CTAs
+    // start their weight streams there while this one finishes (K = 16384
+    // sweep, split 1, 112 CTAs: M = 1..16 0.940-0.949 -> 0.952-0.960 of the
+    // HBM copy bandwidth, unchanged from 32 tokens).  With every SM busy it
+    // measured slower (split 4, M = 16: 75.1 -> 76.2 us).
+    out->pdl_trigger = ctas < num_sms ? 1 : 0;
     out->reduce_scatter = mode == 2 ? 1 : 0;
     out->b_resident = 0;
     out->a_tmem_tiles = 0;

@@ -140,8 +140,8 @@ def test_plan_of_the_decode_workloads():
     p = _plan(16, 4096, 7168, 1, 8)
     assert (p.mma_n, p.split_k, p.k_tiles_per_cta) == (16, 8, 7)
     assert list(p.grid) == [8, 32, 1]
-    p = _plan(64, 18432, 7168, 1, 2)
-    assert (p.mma_n, list(p.grid)) == (64, [2, 144, 1])
+    p = _plan(64, 18432, 7168, 1, 2)                # persistent: 144 tiles over 152 / 2 = 76 clusters
+    assert (p.mma_n, p.persistent, list(p.grid)) == (64, 1, [2, 76, 1])
     p = _plan(128, 7168, 16384, 2, 8)              # persistent: 152 SMs / 8 = 19 clusters
     assert (p.mma_n, list(p.grid), p.k_tiles_per_cta, p.persistent) == (128, [8, 19, 1], 16, 1)
     assert (p.stages, p.mailbox_quads, p.reduce_rounds) == (3, 16, 2)   # two rounds buy a third stage
@@ -151,7 +151,10 @@ def test_plan_of_the_decode_workloads():
     assert _plan(64, 7168, 16384, 2, 4).persistent == 1
     p2 = _plan(128, 7168, 16384, 2, 2)             # split 2, 128 tokens: 64-token tiles, 224 over 76 clusters
     assert (p2.persistent, p2.mma_n, p2.split_k) == (1, 64, 2)
-    assert _plan(64, 7168, 16384, 2, 2).persistent == 0   # fewer tokens at split 2: the per-tile kernel
+    assert _plan(64, 7168, 16384, 2, 2).persistent == 0   # 112 tiles over 76 clusters: the per-tile kernel
+    pw = _plan(64, 18432, 7168, 1, 2)                     # the wide projection: 144 tiles, even enough
+    assert (pw.persistent, pw.mma_n) == (1, 64)
+    assert _plan(32, 7168, 16384, 2, 2).persistent == 0
     assert p.reduce_rounds >= 1 and p.mailbox_quads % 4 == 0
 
 
@@ -234,8 +237,8 @@ def test_every_plan_fits_and_is_consistent(M, split):
     K = 128 * 8 * 4 - 8 * (M % 5)                  # some ragged K
     p = _plan(M, 7168, K, 2, split)
     assert p.k_tiles_per_cta == -(-(-(-K // 128)) // split)
-    # 64-token tiles: the persistent kernel at split 2 with 128 or more tokens
-    assert p.mma_n >= min(M, 128) or p.mma_n == 128 or (p.persistent and split == 2 and M >= 128 and p.mma_n == 64)
+    # 64-token tiles: the persistent kernel at split 2 with 64 or more tokens
+    assert p.mma_n >= min(M, 128) or p.mma_n == 128 or (p.persistent and split == 2 and M >= 64 and p.mma_n == 64)
     if p.persistent:
         _check_persistent(p, M, 7168, K, 2, split)
         return
