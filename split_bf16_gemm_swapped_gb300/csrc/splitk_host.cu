@@ -430,9 +430,11 @@ int plan_ring_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t 
   return SPLITK_ERR_NO_FIT;
 }
 
-// The A16W4 plan: decode-sized tiles (mma_n 16 or 32), the split of the bf16
-// planner (raised until a CTA's K slice is at most 8 tiles, all of whose
-// packed codes are loaded at once), min(3, k_tiles) TMEM slots for decoded
+// The quantized-weight plan (A16W4, or A16W8 with fmt = E4M3): decode-sized
+// tiles (mma_n 16 or 32), the split of the bf16 planner (raised until a
+// CTA's K slice is at most 8 tiles; their packed codes go through a ring of
+// code stages, all at once where two CTAs still share an SM), min(3,
+// k_tiles) TMEM slots for decoded
 // tiles (measured: more slots, decoded before the PDL wait, beat more CTAs
 // per SM), resident activations loaded by TMA, the early trigger, and a
 // dedicated single-round mailbox (scattered from split 4 and 16 token
@@ -997,7 +999,7 @@ int launch_locked(DeviceState& st, const void* a, const void* b, void* c, int M,
   uint32_t ded = 0;
   int rc = check_plan(pl, M, N, K, L, st.smem_optin, st.smem_per_sm, &ded);
   if (rc != SPLITK_OK) return rc;
-  // the A16W4 kernel needs its scales; the bf16 kernel takes none
+  // the quantized kernels need their scales; the bf16 kernel takes none
   if (is_quantized(pl.weight_format) != (a_scale != nullptr)) return SPLITK_ERR_BAD_PLAN;
   const CUtensorMap* a_map = nullptr;
   rc = a_map_for(st, a, N, K, L, stream, &a_map, pl.weight_format);

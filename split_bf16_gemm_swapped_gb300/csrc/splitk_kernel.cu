@@ -156,14 +156,14 @@ __device__ __forceinline__ void q_steps(uint32_t src, int row, uint32_t codes, i
 template <int MMA_N, int kFmt, int kDecWG>
 __global__ void __launch_bounds__(kDecWG == 2 ? kThreadsW4Wide : kThreads, kDecWG == 2 ? 2 : 3)
     splitk_gemm_bf16_kernel(const __grid_constant__ CUtensorMap b_map, const KernelParams p) {
-  constexpr bool kW4 = kFmt != 0;                           // quantized weights, decoded on chip
+  constexpr bool kQuant = kFmt != 0;                           // quantized weights, decoded on chip
   constexpr uint32_t kQTileBytes = kFmt == 2 ? kW8TileBytes : kW4TileBytes;   // one packed K tile
   constexpr uint32_t kQRowBytes = kFmt == 2 ? kW8RowBytes : kW4RowBytes;      // one row of it
   constexpr uint32_t kBStage = b_stage_bytes(MMA_N);
   constexpr uint32_t kBBox = kBStage / 2;                   // MMA_N rows x 128 B
   constexpr uint32_t kAccCols = tmem_acc_cols(MMA_N);       // TMEM columns of one accumulator
   constexpr uint32_t kIdesc = dev::idesc_bf16_f32(kMmaM, MMA_N);
-  constexpr uint32_t kAStage = kW4 ? kQTileBytes : kAStageBytes;   // one weight K tile in shared memory
+  constexpr uint32_t kAStage = kQuant ? kQTileBytes : kAStageBytes;   // one weight K tile in shared memory
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = dev::smem_u32(smem_raw);
@@ -192,8 +192,8 @@ __global__ void __launch_bounds__(kDecWG == 2 ? kThreadsW4Wide : kThreads, kDecW
   // [dedicated mailbox?][barriers].
   const uint32_t sA = base;
   const uint32_t sB = sA + (uint32_t)stages * kAStage;
-  const uint32_t sW4Stage = sB + (uint32_t)p.b_region_tiles * kBStage;   // A16W4 bf16 stage (if any)
-  const uint32_t ring_end = sW4Stage + (kW4 ? (uint32_t)p.w4_smem_tiles * kAStageBytes : 0u);
+  const uint32_t sQStage = sB + (uint32_t)p.b_region_tiles * kBStage;   // quantized weights: the bf16 stage (if any)
+  const uint32_t ring_end = sQStage + (kQuant ? (uint32_t)p.w4_smem_tiles * kAStageBytes : 0u);
   const uint32_t sMail = p.mailbox_dedicated ? ring_end : sA;
   const uint32_t sBar = ring_end + (p.mailbox_dedicated ? p.mailbox_bytes : 0u);
   const uint32_t bar_full0 = sBar;                       // [kMaxStages], count 2
@@ -228,14 +228,14 @@ __global__ void __launch_bounds__(kDecWG == 2 ? kThreadsW4Wide : kThreads, kDecW
         dev::mbar_init(bar_full0 + 8u * s, b_res ? 1u : 2u);   // A (and B when it rides the ring)
         // the stage's MMA commit; quantized weights: every decoding warp,
         // once it has read the stage's codes
-        dev::mbar_init(bar_empty0 + 8u * s, kW4 ? (uint32_t)(kEpiWarps * kDecWG) : 1u);
+        dev::mbar_init(bar_empty0 + 8u * s, kQuant ? (uint32_t)(kEpiWarps * kDecWG) : 1u);
       }
       dev::mbar_init(bar_b, p.b_loader ? (uint32_t)kEpiThreads : 1u);
       dev::mbar_init(bar_mma_done, (uint32_t)p.mma_issuers);
       dev::mbar_init(bar_tmem_empty, kEpiThreads);
       dev::mbar_init(bar_reduce, 1);
       dev::mbar_init(bar_ready, 1);
-      if (kW4) {
+      if (kQuant) {
         for (int i = 0; i < 3; ++i) {
           dev::mbar_init(bar_slot_full0 + 8u * i, (uint32_t)(kEpiWarps * kDecWG));
           dev::mbar_init(bar_slot_empty0 + 8u * i, 1);
@@ -268,7 +268,7 @@ __global__ void __launch_bounds__(kDecWG == 2 ? kThreadsW4Wide : kThreads, kDecW
     }
   }
   dev::cluster_arrive_release();
-  if (kW4 && threadIdx.x == 0) {
+  if (kQuant && threadIdx.x == 0) {
     // the first ring pass of packed weight tiles (usually all of the CTA's):
     // one box each, 8 KiB of 4-bit codes or 16 KiB of 8-bit ones
     const int first = k_tiles < stages ? k_tiles : stages;
@@ -335,14 +335,14 @@ __global__ void __launch_bounds__(kDecWG == 2 ? kThreadsW4Wide : kThreads, kDecW
   // stage in shared memory in the 128-byte-swizzled layout of the bf16 path
   // (two boxes of 64 k; 16-byte chunk c of row r of an 8-row atom at chunk
   // c ^ (r % 8)), read by the MMA from there.
-  auto w4_decode_tmem = [&](int stage, int row, uint32_t codes, uint32_t t_col, int j0, int j1) {
+  auto q_decode_tmem = [&](int stage, int row, uint32_t codes, uint32_t t_col, int j0, int j1) {
     q_decode_row(stage, row, codes, j0, j1, [&](int j, const uint32_t (&r)[16]) {
       __syncwarp();   // tcgen05.st is warp-collective
       dev::tmem_st_x16(t_col + (uint32_t)(j * 16), r);
     });
   };
-  auto w4_decode_stage = [&](int stage, int row, uint32_t codes, int j0, int j1) {
-    const uint32_t atom = sW4Stage + (uint32_t)(row >> 3) * 1024u + (uint32_t)(row & 7) * 128u;
+  auto q_decode_stage = [&](int stage, int row, uint32_t codes, int j0, int j1) {
+    const uint32_t atom = sQStage + (uint32_t)(row >> 3) * 1024u + (uint32_t)(row & 7) * 128u;
     q_decode_row(stage, row, codes, j0, j1, [&](int j, const uint32_t (&r)[16]) {
       // k = 32 j .. 32 j + 31: box j / 2, chunks 4 (j % 2) .. + 3
       const uint32_t box = atom + (uint32_t)(j >> 1) * kABoxBytes;
@@ -384,7 +384,7 @@ __global__ void __launch_bounds__(kDecWG == 2 ? kThreadsW4Wide : kThreads, kDecW
         const uint32_t full = bar_full0 + 8u * s;
         // the stage's previous round (kt - stages) consumed
         if (!waiter.wait<false>(bar_empty0 + 8u * s, pos.phase ^ 1u, kRoleWeightTma, kt)) break;
-        if constexpr (kW4) {
+        if constexpr (kQuant) {
           // packed codes: the stage is free once every decoder has read it
           dev::mbar_arrive_expect_tx(full, kQTileBytes);
           dev::tma_load_3d_hint(sA + (uint32_t)s * kQTileBytes, p.a_map, (kt0 + kt) * (int)kQRowBytes, n0, l,
@@ -439,8 +439,8 @@ __global__ void __launch_bounds__(kDecWG == 2 ? kThreadsW4Wide : kThreads, kDecW
     // adds the two.
     const int issuer = warp - 2;
     const int nis = p.mma_issuers;
-    if (kW4 && lane == 0 && issuer < nis) {
-      // A16W4: the epilogue threads decode each weight tile into a TMEM slot
+    if (kQuant && lane == 0 && issuer < nis) {
+      // Quantized weights: the epilogue threads decode each weight tile into a TMEM slot
       // (tile kt in slot kt % slots); the MMAs read A from there.  Issuer i
       // takes tiles i, i + nis, ... into its own accumulator.  The decoders
       // finish tiles in order, so an issuer that saw tile kt - nis full also
@@ -463,7 +463,7 @@ __global__ void __launch_bounds__(kDecWG == 2 ? kThreadsW4Wide : kThreads, kDecW
           for (int kk = 0; kk < kCtaK / kMmaK; ++kk) {
             const uint32_t a_off = (uint32_t)(kk >> 2) * kABoxBytes + (uint32_t)(kk & 3) * 32u;
             const uint32_t b_off = (uint32_t)(kk >> 2) * kBBox + (uint32_t)(kk & 3) * 32u;
-            dev::mma_bf16(d_acc, dev::smem_desc_sw128(sW4Stage + a_off), dev::smem_desc_sw128(b_st + b_off),
+            dev::mma_bf16(d_acc, dev::smem_desc_sw128(sQStage + a_off), dev::smem_desc_sw128(b_st + b_off),
                           kIdesc, (first | (uint32_t)kk) != 0u ? 1u : 0u);
           }
           continue;
@@ -485,7 +485,7 @@ __global__ void __launch_bounds__(kDecWG == 2 ? kThreadsW4Wide : kThreads, kDecW
       }
       dev::mma_commit(bar_mma_done);
     }
-    if (!kW4 && lane == 0 && issuer < nis) {
+    if (!kQuant && lane == 0 && issuer < nis) {
       const uint32_t d_acc = tmem_base + (uint32_t)issuer * kAccCols;
       bool ok = true;
       // Before the activations can exist: copy this issuer's share of the
@@ -547,7 +547,7 @@ __global__ void __launch_bounds__(kDecWG == 2 ? kThreadsW4Wide : kThreads, kDecW
     }
     __syncwarp();
   } else if (kDecWG == 2 && warp >= 8) {
-    // ---- second A16W4 decoding warpgroup: chunks 2 and 3 (k 64..127) of
+    // ---- second decoding warpgroup (quantized weights): chunks 2 and 3 (k 64..127) of
     // every tile's rows, into the same TMEM slots or bf16 stage
     const int row = (int)threadIdx.x - 256;
     const uint32_t t_row2 = tmem_base + ((uint32_t)((warp & 3) * 32) << 16);
@@ -562,7 +562,7 @@ __global__ void __launch_bounds__(kDecWG == 2 ? kThreadsW4Wide : kThreads, kDecW
       if (p.w4_smem_tiles && kt == slots) {
         code_wait(cp, kt);
         const uint32_t codes = scales.take();
-        w4_decode_stage(cp.index, row, codes, kEpiJ1, 4);
+        q_decode_stage(cp.index, row, codes, kEpiJ1, 4);
         code_free(kt, cp.index);
         dev::fence_proxy_async_shared();
         warp_arrive(bar_w4_stage);
@@ -573,7 +573,7 @@ __global__ void __launch_bounds__(kDecWG == 2 ? kThreadsW4Wide : kThreads, kDecW
       if (kt >= slots) waiter.wait<false>(bar_slot_empty0 + 8u * slot, sp.phase ^ 1u, kRoleEpiDecode, kt);
       code_wait(cp, kt);
       const uint32_t codes = scales.take();
-      w4_decode_tmem(cp.index, row, codes, t_row2 + p.tmem_tile_col0 + (uint32_t)slot * kTmemTileCols, kEpiJ1, 4);
+      q_decode_tmem(cp.index, row, codes, t_row2 + p.tmem_tile_col0 + (uint32_t)slot * kTmemTileCols, kEpiJ1, 4);
       code_free(kt, cp.index);
       dev::tmem_wait_st();
       dev::tc_fence_before();
@@ -639,8 +639,8 @@ __global__ void __launch_bounds__(kDecWG == 2 ? kThreadsW4Wide : kThreads, kDecW
       if (et == 0) stamp(p, kTrActReady);
     };
 
-    if constexpr (kW4) {
-      // A16W4: thread et decodes weight row n0 + et of each K tile into TMEM
+    if constexpr (kQuant) {
+      // Quantized weights: thread et decodes weight row n0 + et of each K tile into TMEM
       // lane et (with a second decoding warpgroup: chunks 0 and 1 of each
       // tile, the other group chunks 2 and 3).  The first `slots` tiles are
       // decoded before the previous kernel completes; with the epilogue
@@ -660,7 +660,7 @@ __global__ void __launch_bounds__(kDecWG == 2 ? kThreadsW4Wide : kThreads, kDecW
           // bf16 stage in shared memory
           code_wait(cp, kt);
           const uint32_t codes = scales.take();
-          w4_decode_stage(cp.index, et, codes, 0, kEpiJ1);
+          q_decode_stage(cp.index, et, codes, 0, kEpiJ1);
           code_free(kt, cp.index);
           dev::fence_proxy_async_shared();   // generic-proxy stores, read by tcgen05.mma
           warp_arrive(bar_w4_stage);
@@ -672,7 +672,7 @@ __global__ void __launch_bounds__(kDecWG == 2 ? kThreadsW4Wide : kThreads, kDecW
         if (kt >= slots) waiter.wait<false>(bar_slot_empty0 + 8u * slot, sp.phase ^ 1u, kRoleEpiDecode, kt);
         code_wait(cp, kt);
         const uint32_t codes = scales.take();
-        w4_decode_tmem(cp.index, et, codes, t_row + p.tmem_tile_col0 + (uint32_t)slot * kTmemTileCols, 0, kEpiJ1);
+        q_decode_tmem(cp.index, et, codes, t_row + p.tmem_tile_col0 + (uint32_t)slot * kTmemTileCols, 0, kEpiJ1);
         code_free(kt, cp.index);
         dev::tmem_wait_st();
         dev::tc_fence_before();
