@@ -368,9 +368,14 @@ SPLITK_API int splitk_gemm_bf16_planned(const void *a, const void *b, void *c,
  * End-to-end call with host activations and host output: enqueues on
  * `stream` the copy b_host -> b_dev (M*K*L bf16), the GEMM with the resident
  * device weights `a`, and the copy c_dev -> c_host (M*N*L bf16).  b_dev and
- * c_dev are caller-owned device buffers of those sizes.  Host buffers should
- * be pinned for the copies to be asynchronous; the caller synchronizes
- * `stream` before reading c_host.
+ * c_dev are caller-owned device buffers of those sizes.  When both host
+ * buffers are page-locked and mapped into the device address space (and all
+ * four buffers 16-byte aligned), the two copies are small kernels chained to
+ * the GEMM by programmatic dependent launch: the GEMM is resident and streams
+ * its weights while the activations arrive, and every copy still waits for
+ * the work ahead of it in the stream before touching memory.  Otherwise the
+ * copy engines do them (pageable host memory: not asynchronous).  The
+ * caller synchronizes `stream` before reading c_host.
  */
 SPLITK_API int splitk_gemm_bf16_hostio(const void *a, const void *b_host,
                                        void *c_host, void *b_dev, void *c_dev,

@@ -28,7 +28,7 @@ SYNTHETIC_LIB = LIBDIR / "libsynthetic.so"
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 # Translation units of the CUDA library; compiled in parallel, linked once.
-SPLITK_SOURCES = ["splitk_kernel.cu", "splitk_persistent.cu", "splitk_host.cu"]
+SPLITK_SOURCES = ["splitk_kernel.cu", "splitk_persistent.cu", "splitk_copy.cu", "splitk_host.cu"]
 SPLITK_HEADERS = ["splitk_device.cuh", "splitk_internal.h", "splitk_kernel_common.cuh"]
 
 

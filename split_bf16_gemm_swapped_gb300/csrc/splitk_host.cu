@@ -1160,6 +1160,17 @@ int enumerate_plans(int M, int N, int K, int L, int split_k, int num_sms, size_t
   return SPLITK_OK;
 }
 
+// The device address of page-locked, device-mapped host memory, or null.
+void* mapped_device_pointer(const void* host) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, host) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (at.type != cudaMemoryTypeHost || at.devicePointer == nullptr) return nullptr;
+  return at.devicePointer;
+}
+
 }  // namespace
 }  // namespace splitk
 
@@ -1224,28 +1235,30 @@ SPLITK_API int splitk_gemm_bf16_hostio(const void* a, const void* b_host, void* 
   if (rc != SPLITK_OK) return rc;
   const size_t b_bytes = (size_t)L * (size_t)M * (size_t)K * 2u;
   const size_t c_bytes = (size_t)L * (size_t)M * (size_t)N * 2u;
-  if (cudaMemcpyAsync(b_dev, b_host, b_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) {
+  // Page-locked, device-mapped host buffers: the copies are kernels chained
+  // to the GEMM by programmatic dependent launch, so the GEMM streams its
+  // weights while the activations arrive and the copy-out is resident when
+  // it completes.  Otherwise (pageable memory, odd alignment) the copy
+  // engines, in stream order.
+  void* b_mapped = mapped_device_pointer(b_host);
+  void* c_mapped = mapped_device_pointer(c_host);
+  const bool kernels = b_mapped != nullptr && c_mapped != nullptr &&
+                       (((uintptr_t)b_mapped | (uintptr_t)b_dev | (uintptr_t)c_mapped | (uintptr_t)c_dev) & 15u) == 0;
+  cudaError_t e = kernels ? launch_pdl_copy(b_mapped, b_dev, b_bytes, st->num_sms, s)
+                          : cudaMemcpyAsync(b_dev, b_host, b_bytes, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) {
     cudaGetLastError();
     return SPLITK_ERR_CUDA;
   }
   rc = launch_locked(*st, a, b_dev, c_dev, M, N, K, L, pl, 0u, s);
   if (rc != SPLITK_OK) return rc;
-  if (cudaMemcpyAsync(c_host, c_dev, c_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) {
+  e = kernels ? launch_pdl_copy(c_dev, c_mapped, c_bytes, st->num_sms, s)
+              : cudaMemcpyAsync(c_host, c_dev, c_bytes, cudaMemcpyDeviceToHost, s);
+  if (e != cudaSuccess) {
     cudaGetLastError();
     return SPLITK_ERR_CUDA;
   }
   return SPLITK_OK;
-}
-
-// The device address of page-locked, device-mapped host memory, or null.
-void* mapped_device_pointer(const void* host) {
-  cudaPointerAttributes at;
-  if (cudaPointerGetAttributes(&at, host) != cudaSuccess) {
-    cudaGetLastError();
-    return nullptr;
-  }
-  if (at.type != cudaMemoryTypeHost || at.devicePointer == nullptr) return nullptr;
-  return at.devicePointer;
 }
 
 SPLITK_API int splitk_gemm_bf16_zerocopy(const void* a, const void* b_host, void* c_host, int M, int N, int K,

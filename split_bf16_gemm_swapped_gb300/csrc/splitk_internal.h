@@ -145,6 +145,10 @@ struct LaunchArgs {
 // Defined in splitk_kernel.cu.
 cudaError_t launch_kernel(const LaunchArgs& la, const CUtensorMap& b_map,
                           const KernelParams& p, cudaStream_t stream);
+// A copy of `bytes` bytes (both pointers 16-byte aligned, either may be the
+// device mapping of page-locked host memory) as a kernel in the stream's
+// programmatic-dependent-launch chain (splitk_copy.cu).
+cudaError_t launch_pdl_copy(const void* src, void* dst, size_t bytes, int num_sms, cudaStream_t stream);
 cudaError_t prepare_kernels(int max_dynamic_smem);
 cudaError_t read_and_clear_fault(int* out_words);
 

@@ -347,3 +347,30 @@ def test_persistent_plans_chain_with_pdl_and_replay_in_a_graph():
     torch.cuda.synchronize()
     assert sk.splitk_get_status() == 0
     assert torch.equal(out.view(torch.int16), c1.view(torch.int16))
+
+
+@pytest.mark.parametrize("M,N,K,L,split", [(16, 7168, 16384, 1, 4), (4, 300, 1024, 2, 1), (33, 2048, 2048, 1, 2)])
+def test_host_io_copy_kernels_chain_calls_in_order(M, N, K, L, split):
+    """splitk_gemm_bf16_hostio with pinned buffers (copy kernels chained to
+    the GEMM): three calls back to back on one stream with different
+    activations and one set of device and host buffers each return their own
+    product, as the device path does; pageable host buffers (the copy
+    engines) the same."""
+    a, _ = _draw(L, M, N, K, seed=2400 + M)
+    ta = to_dev(a)
+    bs = [synthetic.normal_bf16((L, M, K), 2400 + M + i, synthetic.STREAM_B, 1.0) for i in range(3)]
+    wants = [gemm_gpu(a, b, split_k=split) for b in bs]
+    b_dev = torch.empty((L, M, K), dtype=torch.bfloat16, device=DEV)
+    c_dev = torch.empty((L, M, N), dtype=torch.bfloat16, device=DEV)
+    for pinned in (True, False):
+        b_hosts = [torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16) for b in bs]
+        c_hosts = [torch.full((L, M, N), float("nan"), dtype=torch.bfloat16) for _ in bs]
+        if pinned:
+            b_hosts = [x.pin_memory() for x in b_hosts]
+            c_hosts = [x.pin_memory() for x in c_hosts]
+        for i in range(3):
+            sk.splitk_gemm_bf16_hostio(ta, b_hosts[i], c_hosts[i], b_dev, c_dev, split_k=split)
+        torch.cuda.synchronize()
+        assert sk.splitk_get_status() == 0
+        for i in range(3):
+            assert np.array_equal(c_hosts[i].view(torch.int16).numpy().view(np.uint16), wants[i]), (pinned, i)
