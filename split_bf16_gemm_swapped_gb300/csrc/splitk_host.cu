@@ -271,7 +271,12 @@ int plan_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t smem_
   const long long clusters = std::max(1, num_sms / split);
   const long long rounds = (tiles + clusters - 1) / clusters;
   const bool balanced = (double)tiles >= 0.9 * (double)(rounds * clusters);
-  if ((split == 8 || (split == 4 && out->mma_n >= 64) || two_wide) && tiles * split > num_sms && balanced) {
+  // Split 2 at 32-token tiles: the persistent kernel measured faster even
+  // with uneven rounds (M = 32 sweep point, 112 tiles over 76 clusters:
+  // 77.4 -> 75.1 us; at 64-token tiles the two kernels measure level).
+  const bool two_32 = split == 2 && out->mma_n == 32;
+  if ((((split == 8 || (split == 4 && out->mma_n >= 64) || two_wide) && balanced) || two_32) &&
+      tiles * split > num_sms) {
     splitk_plan_t p;
     if (persistent_plan(M, N, K, L, split, 0, 0, num_sms, smem_per_sm, smem_optin, &p, pers_n)) *out = p;
   }

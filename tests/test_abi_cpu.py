@@ -154,7 +154,9 @@ def test_plan_of_the_decode_workloads():
     assert _plan(64, 7168, 16384, 2, 2).persistent == 0   # 112 tiles over 76 clusters: the per-tile kernel
     pw = _plan(64, 18432, 7168, 1, 2)                     # the wide projection: 144 tiles, even enough
     assert (pw.persistent, pw.mma_n) == (1, 64)
-    assert _plan(32, 7168, 16384, 2, 2).persistent == 0
+    p32 = _plan(32, 7168, 16384, 2, 2)                   # 32-token tiles at split 2: persistent
+    assert (p32.persistent, p32.mma_n) == (1, 32)
+    assert _plan(48, 7168, 16384, 2, 2).persistent == 0  # 64-token tiles, uneven: the per-tile kernel
     assert p.reduce_rounds >= 1 and p.mailbox_quads % 4 == 0
 
 
