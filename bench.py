@@ -18,8 +18,11 @@ projections), each reading the next of R weight copies whose total exceeds
 4x the L2 cache, so every call streams its weights from HBM.  The graph is
 replayed back to back at least 5 times and for at least `--min-ms` per
 point, each replay bracketed by CUDA events; the point's time is the median
-replay / steps.  All points are captured first and timed in one block, so
-the clock sampler sees the GPU under load.
+replay / steps.  The two decode workloads run graphs of at least 200 calls
+(a decode step chains hundreds of such projections), with the `--steps`-long
+graph's figure beside it when that is shorter (`short_graph`).  All points
+are captured first and timed in one block, so the clock sampler sees the GPU
+under load.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload sweep|decode_m1|...] [--sweep fixed|w4a16|w8a16|persistent]
@@ -59,6 +62,7 @@ KERNEL_SOURCES = ["split_bf16_gemm_swapped_gb300/csrc/splitk_kernel.cu",
 TRAFFIC_TABLE = ROOT / "profiles" / "splitk_dram_traffic.txt"
 SWEEP_DESC = ("sweep: M in {1,2,4,8,16,32,64,128} x split_k in {1,2,4,8}, N=7168, K=16384, L=2 "
               "independent weight sets")
+EXTRA_MIN_STEPS = 200   # calls per graph of the decode workloads, at least
 VALUE_RULE = "lowest TB/s over the points with M <= 16 (the decode shapes the 75 % HBM target covers)"
 
 
@@ -457,7 +461,7 @@ def point_record(w, ms_per_step, reps, steps, plan, traffic, world):
     return {"M": w.M, "split_k": w.split_k, "N": w.N, "K": w.K, "L": w.L, "key": workload_key(w),
             "us": round(ms_per_step * 1e3, 3), "tbps": tb, "tflops": round(world * w.flops / t / 1e12, 2),
             "hbm_frac": round(w.bytes / t / 1e9 / hbm, 4), "roofline_frac": round(t_roof / t, 4),
-            "repeats": reps, "launches": reps * steps,
+            "steps": steps, "repeats": reps, "launches": reps * steps,
             "traffic": traffic.get(workload_key(w)),
             "plan": {k: v for k, v in plan.as_dict().items()
                      if k in ("mma_n", "stages", "grid", "smem_bytes", "ctas_per_sm", "mailbox_dedicated",
@@ -576,12 +580,19 @@ def run_ours(args):
     main_ws = W.all_sweep() if sweep_mode else [workload_by_name(args.workload)]
     extra_ws = [W.DECODE_M1, W.DECODE_M16] if sweep_mode and not args.no_extras else []
 
-    # prepare every point (weights, activations, graph) before timing any
+    # prepare every point (weights, activations, graph) before timing any.
+    # The decode workloads run graphs of at least EXTRA_MIN_STEPS calls (a
+    # decode step runs hundreds of such GEMMs back to back; the sweep's own
+    # protocol is `--steps` exactly), and, when --steps is shorter, a graph of
+    # --steps calls as well, reported beside it.
     cache, rotations, prepared = {}, {}, []
-    for w in main_ws + extra_ws:
+    extra_steps = max(args.steps, EXTRA_MIN_STEPS)
+    short_extra = extra_steps != args.steps
+    for w in main_ws + extra_ws + (extra_ws if short_extra else []):
         copies, rot = weight_copies(w, dev, l2, args.rotate, cache)
         rotations[workload_key(w)] = rot
-        prepared.append(Point(w, copies, dev, stream, args.steps, args.warmup))
+        is_extra = w in extra_ws and len(prepared) < len(main_ws) + len(extra_ws)
+        prepared.append(Point(w, copies, dev, stream, extra_steps if is_extra else args.steps, args.warmup))
     torch.cuda.synchronize(dev)
 
     # time every point in one block: barrier + synchronize on both sides of
@@ -598,19 +609,22 @@ def run_ours(args):
             torch.cuda.synchronize(dev)
             if world > 1:
                 dist.barrier()
-            ms = max_over_ranks(statistics.median(per_rep) / args.steps, dev)
-            launches += reps * args.steps
+            ms = max_over_ranks(statistics.median(per_rep) / pt.steps, dev)
+            launches += reps * pt.steps
             results.append((pt, ms, reps))
     if sk.splitk_get_status() != 0:
         raise SystemExit(f"kernel fault in the timed region: {sk.splitk_get_fault()}")
 
-    records = [point_record(pt.w, ms, reps, args.steps, pt.plan, traffic, world) for pt, ms, reps in results]
+    records = [point_record(pt.w, ms, reps, pt.steps, pt.plan, traffic, world) for pt, ms, reps in results]
     main_recs = records[:len(main_ws)]
-    extra_recs = records[len(main_ws):]
+    extra_recs = records[len(main_ws):len(main_ws) + len(extra_ws)]
+    for rec, short in zip(extra_recs, records[len(main_ws) + len(extra_ws):]):
+        rec["short_graph"] = {"steps": args.steps, "us": short["us"], "tbps": short["tbps"],
+                              "hbm_frac": short["hbm_frac"], "repeats": short["repeats"]}
     # the decode workloads' single-launch time (one call per graph replay):
     # what the first call of every timed graph costs, with no predecessor to
     # overlap its start with
-    for rec, (pt, _, _) in zip(extra_recs, results[len(main_ws):]):
+    for rec, (pt, _, _) in zip(extra_recs, results[len(main_ws):len(main_ws) + len(extra_ws)]):
         g1 = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g1, stream=stream):
             pt.step(0)
@@ -638,8 +652,8 @@ def run_ours(args):
     e2e = None
     e2e_decode = {}
     if args.e2e:
-        for pt, ms, reps in [results[top_i]] + results[len(main_ws):]:
-            rec = e2e_point(pt.w, pt.As, dev, stream, args.steps, reps, args.warmup, world)
+        for pt, ms, reps in [results[top_i]] + results[len(main_ws):len(main_ws) + len(extra_ws)]:
+            rec = e2e_point(pt.w, pt.As, dev, stream, pt.steps, reps, args.warmup, world)
             if pt is top_pt:
                 e2e = rec
             else:
