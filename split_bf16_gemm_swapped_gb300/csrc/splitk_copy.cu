@@ -39,9 +39,12 @@ __global__ void __launch_bounds__(kCopyThreads) pdl_copy_kernel(const uint8_t* _
 
 cudaError_t launch_pdl_copy(const void* src, void* dst, size_t bytes, int num_sms, cudaStream_t stream) {
   if (bytes == 0) return cudaSuccess;
+  // One 16-byte word a thread where that fits 4 CTAs an SM: every load of
+  // the copy in flight at once (a host-memory round trip is ~1 us).
   const size_t n16 = bytes / 16u + 1u;
   const size_t want = (n16 + kCopyThreads - 1) / kCopyThreads;
-  const unsigned blocks = (unsigned)(want < (size_t)num_sms ? (want > 0 ? want : 1) : (size_t)num_sms);
+  const size_t cap = 4u * (size_t)num_sms;
+  const unsigned blocks = (unsigned)(want < cap ? (want > 0 ? want : 1) : cap);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(blocks, 1, 1);
   cfg.blockDim = dim3(kCopyThreads, 1, 1);
