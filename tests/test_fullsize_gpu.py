@@ -1,7 +1,8 @@
 """Parity at the full workload sizes, in the launch configuration the
 benchmark times (the workload's split_k, the library's plan, PDL on).
 
-The tiny and the two decode workloads are compared with the oracle on every
+The tiny and the two decode workloads (bf16, and with A16W4 and A16W8
+weights) are compared with the oracle on every
 output element (the threaded oracle takes seconds there).  The wide
 projection and the sweep points are checked on sampled outputs one by one
 (every element of the first and last token row of the first and last weight
@@ -117,3 +118,29 @@ def test_full_size_closed_forms(w):
     # zero sum depends on the order of the zero products)
     assert torch.equal(tc.float(), expect.float())
     assert sk.splitk_get_status() == 0
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("w", [workloads.DECODE_M1, workloads.DECODE_M16],
+                         ids=lambda w: f"{w.name.split()[0]}-M{w.M}-s{w.split_k}")
+def test_quantized_decode_workloads_every_output_against_oracle(w, bits):
+    """A16W4 and A16W8 weights (seeded codes and scales) at the decode
+    workloads' full size, in the plan the library picks: every output
+    against the oracle, and run to run the same bits."""
+    from split_bf16_gemm_swapped_gb300 import synthetic
+    gen, run, ref_fn, deq = ((synthetic.w4_weights, sk.splitk_gemm_w4a16, oracle.gemm_w4a16, oracle.w4_dequant)
+                             if bits == 4 else
+                             (synthetic.w8_weights, sk.splitk_gemm_w8a16, oracle.gemm_w8a16, oracle.w8_dequant))
+    aq, a_s = gen(w.L, w.N, w.K, w.seed)
+    b = w.make_b()
+    tq, ts, tb = (torch.from_numpy(np.ascontiguousarray(aq)).to(DEV),
+                  torch.from_numpy(np.ascontiguousarray(a_s)).to(DEV), to_dev(b))
+    tc = run(tq, ts, tb, split_k=w.split_k)
+    torch.cuda.synchronize()
+    assert sk.splitk_get_status() == 0
+    ok, rep = _tol.check(to_host(tc), ref_fn(aq, a_s, b), w.K, float(np.abs(deq(aq, a_s)).max()),
+                         _tol.max_abs_bf16(b))
+    assert ok, f"A16W{bits} {w.name}: {rep}"
+    tc2 = run(tq, ts, tb, split_k=w.split_k)
+    torch.cuda.synchronize()
+    assert torch.equal(tc.view(torch.int16), tc2.view(torch.int16))
