@@ -170,7 +170,15 @@ typedef struct splitk_plan_t {
                               decoded into a 32 KiB bf16 stage in shared
                               memory, so that every tile is decoded before the
                               programmatic-dependent-launch wait returns     */
-    int reserved;          /* must be 0                                      */
+    int b_stages;          /* persistent plans: 0 = each activation K tile
+                              rides the weight ring stage it is multiplied
+                              with (`stages` deep); 2..8 = the activations
+                              have their own ring of b_stages stages and
+                              `stages` is the weight ring's depth alone (at
+                              wide tiles an activation stage is as large as a
+                              weight stage but comes from L2, so a shallower
+                              activation ring leaves room for more weight
+                              tiles in flight).  0 for every other plan      */
     int persistent;        /* 0: one CTA per (output tile, K rank), the grid
                               above.  1: the persistent kernel: grid
                               (split_k, clusters, 1), each cluster of split_k

@@ -67,7 +67,7 @@ class Plan(ctypes.Structure):
         ("a_tmem_tiles", ctypes.c_int), ("tmem_cols", ctypes.c_uint),
         ("mma_issuers", ctypes.c_int), ("b_loader", ctypes.c_int),
         ("l2_prefetch", ctypes.c_int), ("weight_format", ctypes.c_int),
-        ("w4_smem_tiles", ctypes.c_int), ("reserved", ctypes.c_int),
+        ("w4_smem_tiles", ctypes.c_int), ("b_stages", ctypes.c_int),
         ("persistent", ctypes.c_int), ("w4_decoders", ctypes.c_int),
     ]
 

@@ -105,12 +105,14 @@ int resident_by_smem(size_t smem_per_sm, size_t smem) { return (int)(smem_per_sm
 // tile's, or `quads` 4-column groups.
 int persistent_round_cols(int ncols_max, int quads) { return std::min(ncols_max, 4 * quads); }
 
-// Shared memory of a persistent plan: the ring (a weight and an activation K
-// tile per stage), the scattered mailbox of one reduction round's token
-// columns and the barriers.
-size_t smem_bytes_persistent(int mma_n, int stages, int round_cols) {
-  return (size_t)kAlignSlack + (size_t)stages * (kAStageBytes + b_stage_bytes(mma_n)) +
-         (size_t)round_cols * kColumnBytes + kBarRegionBytes;
+// Shared memory of a persistent plan: the weight ring (`stages` K tiles), the
+// activation ring (`b_stages` K tiles, or `stages` when 0), the scattered
+// mailbox of one reduction round's token columns and the barriers (a second
+// set of full/empty barriers when the two rings' depths differ).
+size_t smem_bytes_persistent(int mma_n, int stages, int b_stages, int round_cols) {
+  return (size_t)kAlignSlack + (size_t)stages * kAStageBytes +
+         (size_t)(b_stages != 0 ? b_stages : stages) * b_stage_bytes(mma_n) + (size_t)round_cols * kColumnBytes +
+         (b_stages != 0 && b_stages != stages ? kBarRegionBytesPersistent : kBarRegionBytes);
 }
 
 // 128-wide K tiles covering K; the last one may be ragged (TMA reads zeros
@@ -190,8 +192,10 @@ bool stage_for_decode(splitk_plan_t* out, int ncols_max, long long ctas, int num
 // mailbox, the mailbox holding a whole tile's columns or, when a smaller one
 // leaves room for a deeper ring, reduction rounds of 16, 8 or 4 4-column
 // groups; two accumulators in TMEM; one cluster per `split` SMs (at most one
-// per output tile).  Nonzero `stages` / `quads` fix the ring depth / round.
-bool persistent_plan(int M, int N, int K, int L, int split, int stages, int quads, int num_sms,
+// per output tile).  Nonzero `stages` / `quads` fix the ring depth / round;
+// nonzero `b_stages` gives the activations a ring of their own that deep
+// (`stages` then counts weight tiles alone).
+bool persistent_plan(int M, int N, int K, int L, int split, int stages, int b_stages, int quads, int num_sms,
                      size_t smem_per_sm, size_t smem_optin, splitk_plan_t* out, int mma_n_want = 0) {
   if (split < 2 || !valid_split(split)) return false;
   const int T = total_k_tiles(K);
@@ -200,10 +204,11 @@ bool persistent_plan(int M, int N, int K, int L, int split, int stages, int quad
   if (mma_n != 16 && mma_n != 32 && mma_n != 64 && mma_n != 128) return false;
   const int ncols_max = std::min(M, mma_n);
   const int nquads_max = (ncols_max + 3) / 4;
+  if (b_stages != 0 && (b_stages < 2 || b_stages > kMaxStages)) return false;
   const size_t budget = std::min(smem_optin, smem_per_sm - 1024);
   auto deepest = [&](int qr) {
     int st = kMaxStages;
-    while (st > 2 && smem_bytes_persistent(mma_n, st, persistent_round_cols(ncols_max, qr)) > budget) --st;
+    while (st > 2 && smem_bytes_persistent(mma_n, st, b_stages, persistent_round_cols(ncols_max, qr)) > budget) --st;
     return st;
   };
   int qr = quads;
@@ -218,7 +223,7 @@ bool persistent_plan(int M, int N, int K, int L, int split, int stages, int quad
   qr = std::min(qr, nquads_max);
   const int round_cols = persistent_round_cols(ncols_max, qr);
   const int st = stages != 0 ? stages : deepest(qr);
-  if (st < 2 || st > kMaxStages || smem_bytes_persistent(mma_n, st, round_cols) > budget) return false;
+  if (st < 2 || st > kMaxStages || smem_bytes_persistent(mma_n, st, b_stages, round_cols) > budget) return false;
   const long long tiles = tiles_of(M, mma_n) * tiles_of(N, kMmaM) * L;
   const long long clusters = std::max<long long>(1, std::min<long long>(tiles, num_sms / split));
   std::memset(out, 0, sizeof(*out));
@@ -236,7 +241,8 @@ bool persistent_plan(int M, int N, int K, int L, int split, int stages, int quad
   out->cluster[0] = (unsigned)split;
   out->cluster[1] = 1;
   out->cluster[2] = 1;
-  out->smem_bytes = smem_bytes_persistent(mma_n, st, round_cols);
+  out->b_stages = b_stages;
+  out->smem_bytes = smem_bytes_persistent(mma_n, st, b_stages, round_cols);
   out->ctas_per_sm = 1;
   out->reduce_scatter = 1;
   out->mma_issuers = 1;
@@ -256,7 +262,8 @@ int plan_ring_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t 
 // bandwidth; M = 64: 0.55 -> 0.87), and split 4 for tiles of 64 and 128
 // tokens (M = 64: 0.80 -> 0.82; the wide projection 0.68 -> 0.88), when the
 // grid exceeds one CTA per SM and the output tiles deal out evenly (at least
-// 90 %) over one cluster per `split` SMs.
+// 90 %) over one cluster per `split` SMs; at split 8 with a reduction in
+// rounds, the activations on a ring of their own so that one round does.
 int plan_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t smem_per_sm,
               size_t smem_optin, splitk_plan_t* out) {
   const int rc = plan_ring_impl(M, N, K, L, split_k, num_sms, smem_per_sm, smem_optin, out);
@@ -278,7 +285,21 @@ int plan_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t smem_
   if ((((split == 8 || (split == 4 && out->mma_n >= 64) || two_wide) && balanced) || two_32) &&
       tiles * split > num_sms) {
     splitk_plan_t p;
-    if (persistent_plan(M, N, K, L, split, 0, 0, num_sms, smem_per_sm, smem_optin, &p, pers_n)) *out = p;
+    if (persistent_plan(M, N, K, L, split, 0, 0, 0, num_sms, smem_per_sm, smem_optin, &p, pers_n)) {
+      // At split 8 a tile reduced in two rounds waits twice on all seven
+      // peers; an activation ring of 2 stages of its own leaves room for a
+      // mailbox of the whole tile at the same weight ring depth (M = 128
+      // sweep point: 109.6 -> 96.9 us; at split 4 the shallower activation
+      // ring costs more than the second round: 93.0 -> 97.4 us).
+      splitk_plan_t one;
+      const int nquads_max = (std::min(M, p.mma_n) + 3) / 4;
+      if (split == 8 && p.reduce_rounds > 1 &&
+          persistent_plan(M, N, K, L, split, p.stages, 2, nquads_max, num_sms, smem_per_sm, smem_optin, &one,
+                          p.mma_n)) {
+        p = one;
+      }
+      *out = p;
+    }
   }
   return SPLITK_OK;
 }
@@ -558,7 +579,7 @@ int check_plan_w4(const splitk_plan_t& pl, int M, int N, int K, int L, size_t sm
   const int kt = (T + pl.split_k - 1) / pl.split_k;
   if (pl.k_tiles_per_cta != kt || pl.stages < 1 || pl.stages > kt) return SPLITK_ERR_BAD_PLAN;
   if (kt > kMaxStages) return SPLITK_ERR_NO_FIT;
-  if (pl.reserved != 0 || pl.persistent != 0) return SPLITK_ERR_BAD_PLAN;
+  if (pl.b_stages != 0 || pl.persistent != 0) return SPLITK_ERR_BAD_PLAN;
   if (pl.w4_decoders != 1 && pl.w4_decoders != 2) return SPLITK_ERR_BAD_PLAN;
   const long long m_tiles = tiles_of(M, pl.mma_n);
   const long long n_tiles = ((long long)N + kMmaM - 1) / kMmaM;
@@ -606,6 +627,7 @@ int check_plan_persistent(const splitk_plan_t& pl, int M, int N, int K, int L, s
   if (K % 8 != 0 || K > kMaxK || total_k_tiles(K) < pl.split_k) return SPLITK_ERR_INVALID_SHAPE;
   if (pl.k_tiles_per_cta != (total_k_tiles(K) + pl.split_k - 1) / pl.split_k) return SPLITK_ERR_BAD_PLAN;
   if (pl.stages < 2 || pl.stages > kMaxStages) return SPLITK_ERR_BAD_PLAN;
+  if (pl.b_stages != 0 && (pl.b_stages < 2 || pl.b_stages > kMaxStages)) return SPLITK_ERR_BAD_PLAN;
   if (L > 65535) return SPLITK_ERR_INVALID_SHAPE;
   if (pl.grid[0] != (unsigned)pl.split_k || pl.grid[1] < 1 || pl.grid[1] > 65535 || pl.grid[2] != 1 ||
       pl.cluster[0] != (unsigned)pl.split_k || pl.cluster[1] != 1 || pl.cluster[2] != 1) {
@@ -620,12 +642,12 @@ int check_plan_persistent(const splitk_plan_t& pl, int M, int N, int K, int L, s
     return SPLITK_ERR_BAD_PLAN;
   }
   if (pl.reduce_scatter != 1 || pl.mailbox_dedicated != 1 || pl.b_resident != 0 || pl.a_tmem_tiles != 0 ||
-      pl.mma_issuers != 1 || pl.b_loader != 0 || pl.l2_prefetch != 0 || pl.pdl_trigger != 0 || pl.reserved != 0) {
+      pl.mma_issuers != 1 || pl.b_loader != 0 || pl.l2_prefetch != 0 || pl.pdl_trigger != 0) {
     return SPLITK_ERR_BAD_PLAN;
   }
   if (pl.tmem_cols != pow2_at_least(2u * tmem_acc_cols(pl.mma_n))) return SPLITK_ERR_BAD_PLAN;
   const int round_cols = persistent_round_cols(ncols_max, pl.mailbox_quads);
-  const size_t smem = smem_bytes_persistent(pl.mma_n, pl.stages, round_cols);
+  const size_t smem = smem_bytes_persistent(pl.mma_n, pl.stages, pl.b_stages, round_cols);
   if (smem != pl.smem_bytes) return SPLITK_ERR_BAD_PLAN;
   if (smem > smem_optin) return SPLITK_ERR_NO_FIT;
   if ((size_t)resident_by_smem(smem_per_sm, smem) * pl.tmem_cols > 512u) return SPLITK_ERR_BAD_PLAN;
@@ -651,7 +673,7 @@ int check_plan(const splitk_plan_t& pl, int M, int N, int K, int L, size_t smem_
   const long long m_tiles = tiles_of(M, pl.mma_n);
   const long long n_tiles = ((long long)N + kMmaM - 1) / kMmaM;
   if (m_tiles * pl.split_k > 0x7FFFFFFFLL) return SPLITK_ERR_INVALID_SHAPE;
-  if (pl.reserved != 0) return SPLITK_ERR_BAD_PLAN;
+  if (pl.b_stages != 0) return SPLITK_ERR_BAD_PLAN;
   if (n_tiles > 65535 || L > 65535) return SPLITK_ERR_INVALID_SHAPE;
   if (pl.grid[0] != (unsigned)(pl.split_k * m_tiles) || pl.grid[1] != (unsigned)n_tiles ||
       pl.grid[2] != (unsigned)L || pl.cluster[0] != (unsigned)pl.split_k || pl.cluster[1] != 1 ||
@@ -944,6 +966,7 @@ void fill_params(const splitk_plan_t& pl, int M, int N, int K, int L, uint32_t d
   p->L = L;
   p->split = pl.split_k;
   p->stages = pl.stages;
+  p->b_stages = pl.persistent != 0 && pl.b_stages != 0 ? pl.b_stages : pl.stages;
   p->k_tiles_total = total_k_tiles(K);
   p->mailbox_dedicated = pl.split_k > 1 ? pl.mailbox_dedicated : 0;
   p->mailbox_bytes = ded;
@@ -1142,22 +1165,26 @@ int enumerate_plans(int M, int N, int K, int L, int split_k, int num_sms, size_t
     }
     // the persistent kernel at every ring depth and reduction round that
     // fit, at the shape's token tile and (for more than 64 tokens) at
-    // 64-token tiles, several of which share each weight tile
+    // 64-token tiles, several of which share each weight tile; the
+    // activations on the weight ring or on a ring of their own
     for (int tile_n : {mma_n, 64}) {
       if (tile_n != mma_n && M <= 64) continue;
       const int nq = (std::min(M, tile_n) + 3) / 4;
       for (int stages = 2; split >= 2 && stages <= kMaxStages; ++stages) {
-        for (int quads : {nq, 16, 8, 4}) {
-          if (quads > nq || (quads != nq && quads % 4 != 0)) continue;
-          splitk_plan_t p;
-          uint32_t ded_check = 0;
-          if (!persistent_plan(M, N, K, L, split, stages, quads, num_sms, smem_per_sm, smem_optin, &p, tile_n) ||
-              check_plan(p, M, N, K, L, smem_optin, smem_per_sm, &ded_check) != SPLITK_OK) {
-            continue;
+        for (int b_stages = 0; b_stages <= kMaxStages; b_stages += b_stages == 0 ? 2 : 1) {
+          for (int quads : {nq, 16, 8, 4}) {
+            if (quads > nq || (quads != nq && quads % 4 != 0)) continue;
+            splitk_plan_t p;
+            uint32_t ded_check = 0;
+            if (!persistent_plan(M, N, K, L, split, stages, b_stages, quads, num_sms, smem_per_sm, smem_optin, &p,
+                                 tile_n) ||
+                check_plan(p, M, N, K, L, smem_optin, smem_per_sm, &ded_check) != SPLITK_OK) {
+              continue;
+            }
+            bool dup = false;
+            for (const auto& q : *out) dup = dup || same(p, q);
+            if (!dup) out->push_back(p);
           }
-          bool dup = false;
-          for (const auto& q : *out) dup = dup || same(p, q);
-          if (!dup) out->push_back(p);
         }
       }
     }

@@ -24,6 +24,7 @@ constexpr int kMaxStages = 8;
 constexpr uint32_t kAStageBytes = kMmaM * kCtaK * 2;        // 32 KiB
 constexpr uint32_t kABoxBytes = kMmaM * kAtomK * 2;         // 16 KiB
 constexpr uint32_t kBarRegionBytes = 256;
+constexpr uint32_t kBarRegionBytesPersistent = 384;        // two rings' full/empty barriers
 constexpr uint32_t kAlignSlack = 1024;                      // swizzle-128B atoms
 constexpr uint32_t kColumnBytes = kEpiThreads * 4;          // one token column of f32 partials
 constexpr unsigned long long kDefaultWaitLimitNs = 1000000000ull;
@@ -87,7 +88,8 @@ struct KernelParams {
   const uint8_t* a_scale;     // A16W4: scale codes [L][N][K/32] (null for bf16 weights)
   int M, N, K, L;
   int split;                  // cluster size along K
-  int stages;                 // ring depth
+  int stages;                 // ring depth (persistent kernel: of the weight ring)
+  int b_stages;               // persistent kernel: depth of the activation ring
   int k_tiles_total;          // 128-wide K tiles over all of K (last may be ragged)
   int mailbox_dedicated;      // 1: own region after the ring, 0: rank 0's A ring
   uint32_t mailbox_bytes;     // size of the dedicated region (0 if aliased)

@@ -8,10 +8,13 @@
 // tiles and large splits the memory pipe idles for the reduction.  Here a
 // cluster of split CTAs (one per SM) stays resident and walks the output
 // tiles cy, cy + clusters, cy + 2 clusters, ... (cy = the cluster's index),
-// every rank taking its K slice of each.  The weight and activation ring runs
+// every rank taking its K slice of each.  The weight and activation rings run
 // on across tiles, and the tile's accumulator alternates between two TMEM
 // buffers, so the MMAs of tile j + 1 and the loads behind them proceed while
-// the epilogue reduces tile j.
+// the epilogue reduces tile j.  The two rings have their own depths: at wide
+// tiles an activation K tile is as large as a weight K tile but comes from
+// L2, so a shallower activation ring leaves shared memory for more weight
+// tiles in flight from DRAM.
 //
 // Reduction: the page's rank order, scattered as in the per-tile kernel's
 // reduce_scatter mode -- rank r sums weight rows [r*R, (r+1)*R), R = 128 /
@@ -27,7 +30,7 @@
 //   warp 0      weight producer: TMA, L2 evict_first, the first ring pass
 //               issued before the cluster barrier and the PDL wait
 //   warp 1      activation producer: griddepcontrol.wait, then TMA into the
-//               same ring stages
+//               activation ring
 //   warp 2      TMEM (two accumulators) and the tcgen05.mma issue
 //   warp 3      barrier initialisation, then idle (it keeps warps 4..7 on
 //               TMEM lane quadrants 0..3)
@@ -49,7 +52,7 @@
 
 namespace splitk {
 
-template <int MMA_N>
+template <int MMA_N, bool kOneRing>
 __global__ void __launch_bounds__(kThreads, 1)
     splitk_persistent_kernel(const __grid_constant__ CUtensorMap b_map, const KernelParams p) {
   constexpr uint32_t kBStage = b_stage_bytes(MMA_N);
@@ -64,7 +67,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = (int)(threadIdx.x >> 5);
   const int lane = (int)(threadIdx.x & 31);
   const int split = p.split;
-  const int stages = p.stages;
+  const int a_stages = p.stages;     // weight ring depth
+  const int b_stages = p.b_stages;   // activation ring depth
+  // Rings of one depth (kOneRing) share their barriers: one full barrier per
+  // stage that both producers arrive on, one MMA commit per K tile.  A
+  // compile-time choice: a second wait and commit on the MMA issuer's path
+  // measured 2-6 % slower, and a run-time test of the depths 1.5-2.5 %.
+  constexpr bool one_ring = kOneRing;
   const int rank = (int)dev::cluster_ctarank();
   // Output tiles: m (token tiles) fastest, then n, then l.  The clusters
   // working at the same time then share each weight tile's reads when there
@@ -84,12 +93,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // Shared memory: [A ring][B ring][mailbox][barriers].
   const uint32_t sA = base;
-  const uint32_t sB = sA + (uint32_t)stages * kAStageBytes;
-  const uint32_t sMail = sB + (uint32_t)stages * kBStage;
+  const uint32_t sB = sA + (uint32_t)a_stages * kAStageBytes;
+  const uint32_t sMail = sB + (uint32_t)b_stages * kBStage;
   const uint32_t sBar = sMail + p.mailbox_bytes;
-  const uint32_t bar_full0 = sBar;                          // [kMaxStages], count 2 (A and B)
-  const uint32_t bar_empty0 = sBar + 8u * kMaxStages;       // [kMaxStages], count 1 (MMA commit)
-  const uint32_t bar_acc_full0 = sBar + 16u * kMaxStages;   // [2] accumulator complete, count 1
+  const uint32_t bar_a_full0 = sBar;                        // [kMaxStages] weight tile landed, count 1 (2: one ring)
+  const uint32_t bar_a_empty0 = sBar + 8u * kMaxStages;     // [kMaxStages] its MMAs done (commit), count 1
+  // [kMaxStages] activation tile landed / its MMAs done, count 1 (one ring: the weight ring's)
+  const uint32_t bar_b_full0 = one_ring ? bar_a_full0 : sBar + 16u * kMaxStages;
+  const uint32_t bar_b_empty0 = one_ring ? bar_a_empty0 : sBar + 24u * kMaxStages;
+  const uint32_t bar_acc_full0 = sBar + (one_ring ? 16u : 32u) * kMaxStages;   // [2] accumulator complete, count 1
   const uint32_t bar_acc_empty0 = bar_acc_full0 + 16u;      // [2] accumulator read, count 128
   const uint32_t bar_reduce = bar_acc_full0 + 32u;          // count 1 + tx bytes of the peers
   const uint32_t bar_ready = bar_acc_full0 + 40u;           // count split - 1 (one per peer)
@@ -116,9 +128,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int total_kt = my_tiles * k_tiles;
   if (warp == 3) {
     if (lane == 0) {
-      for (int s = 0; s < stages; ++s) {
-        dev::mbar_init(bar_full0 + 8u * s, 2u);
-        dev::mbar_init(bar_empty0 + 8u * s, 1u);
+      for (int s = 0; s < a_stages; ++s) {
+        dev::mbar_init(bar_a_full0 + 8u * s, one_ring ? 2u : 1u);
+        dev::mbar_init(bar_a_empty0 + 8u * s, 1u);
+      }
+      for (int s = 0; !one_ring && s < b_stages; ++s) {
+        dev::mbar_init(bar_b_full0 + 8u * s, 1u);
+        dev::mbar_init(bar_b_empty0 + 8u * s, 1u);
       }
       for (int i = 0; i < 2; ++i) {
         dev::mbar_init(bar_acc_full0 + 8u * i, 1u);
@@ -150,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   dev::cluster_arrive_release();
   if (threadIdx.x == 0) {
-    const int first = total_kt < stages ? total_kt : stages;
+    const int first = total_kt < a_stages ? total_kt : a_stages;
     int j = 0, kt = 0, n0 = 0, m0 = 0, l = 0;
     if (first > 0) tile_coords(0, &n0, &m0, &l);
     for (; a_issued < first; ++a_issued, ++kt) {
@@ -158,7 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         kt = 0;
         tile_coords(++j, &n0, &m0, &l);
       }
-      const uint32_t full = bar_full0 + 8u * a_issued;
+      const uint32_t full = bar_a_full0 + 8u * a_issued;
       const uint32_t dst = sA + (uint32_t)a_issued * kAStageBytes;
       const int k = (kt0 + kt) * kCtaK;
       dev::mbar_arrive_expect_tx(full, kAStageBytes);
@@ -188,19 +204,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       // ring position and (output tile, K tile) of global load g, kept by
       // additions; the tile's coordinates recomputed once per output tile
-      RingPos pos = RingPos::at(a_issued, stages);
+      RingPos pos = RingPos::at(a_issued, a_stages);
       int j = a_issued / k_tiles;
       int kt = a_issued - j * k_tiles;
       int n0 = 0, m0 = 0, l = 0;
       if (a_issued < total_kt) tile_coords(j, &n0, &m0, &l);
-      for (int g = a_issued; g < total_kt; ++g, pos.advance(1, stages)) {
+      for (int g = a_issued; g < total_kt; ++g, pos.advance(1, a_stages)) {
         if (kt == k_tiles) {
           kt = 0;
           tile_coords(++j, &n0, &m0, &l);
         }
         const int s = pos.index;
-        if (!waiter.wait<false>(bar_empty0 + 8u * s, pos.phase ^ 1u, kRoleWeightTma, g)) break;
-        const uint32_t full = bar_full0 + 8u * s;
+        if (!waiter.wait<false>(bar_a_empty0 + 8u * s, pos.phase ^ 1u, kRoleWeightTma, g)) break;
+        const uint32_t full = bar_a_full0 + 8u * s;
         const uint32_t dst = sA + (uint32_t)s * kAStageBytes;
         const int k = (kt0 + kt) * kCtaK;
         dev::mbar_arrive_expect_tx(full, kAStageBytes);
@@ -220,16 +236,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       RingPos pos{0, 0u};
       int j = 0, kt = 0, n0 = 0, m0 = 0, l = 0;
       if (total_kt > 0) tile_coords(0, &n0, &m0, &l);
-      for (int g = 0; g < total_kt; ++g, pos.advance(1, stages)) {
+      for (int g = 0; g < total_kt; ++g, pos.advance(1, b_stages)) {
         if (kt == k_tiles) {
           kt = 0;
           tile_coords(++j, &n0, &m0, &l);
         }
         const int s = pos.index;
-        if (g >= stages && !waiter.wait<false>(bar_empty0 + 8u * s, pos.phase ^ 1u, kRoleActTma, g)) {
+        if (g >= b_stages && !waiter.wait<false>(bar_b_empty0 + 8u * s, pos.phase ^ 1u, kRoleActTma, g)) {
           break;
         }
-        const uint32_t full = bar_full0 + 8u * s;
+        const uint32_t full = bar_b_full0 + 8u * s;
         const uint32_t dst = sB + (uint32_t)s * kBStage;
         const int k = (kt0 + kt) * kCtaK;
         dev::mbar_arrive_expect_tx(full, kBStage);
@@ -245,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       bool ok = true;
       int g = 0;
-      RingPos pos{0, 0u};                            // ring position of load g
+      RingPos pa{0, 0u}, pb{0, 0u};                  // weight / activation ring positions of load g
       for (int j = 0; j < my_tiles && ok; ++j) {
         const int buf = j & 1;
         const int use = j >> 1;
@@ -255,14 +271,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           dev::tc_fence_after();
         }
         const uint32_t d_acc = tmem_base + (uint32_t)buf * kAccCols;
-        for (int kt = 0; kt < k_tiles; ++kt, ++g, pos.advance(1, stages)) {
-          const int s = pos.index;
-          ok = waiter.wait<false>(bar_full0 + 8u * s, pos.phase, kRoleMma, g);
+        for (int kt = 0; kt < k_tiles; ++kt, ++g, pa.advance(1, a_stages), pb.advance(1, b_stages)) {
+          ok = waiter.wait<false>(bar_a_full0 + 8u * pa.index, pa.phase, kRoleMma, g) &&
+               (one_ring || waiter.wait<false>(bar_b_full0 + 8u * pb.index, pb.phase, kRoleMma, g));
           if (!ok) break;
           dev::tc_fence_after();
           if (g == 0) stamp(p, kTrFirstFull);
-          const uint32_t a_st = sA + (uint32_t)s * kAStageBytes;
-          const uint32_t b_st = sB + (uint32_t)s * kBStage;
+          const uint32_t a_st = sA + (uint32_t)pa.index * kAStageBytes;
+          const uint32_t b_st = sB + (uint32_t)pb.index * kBStage;
 #pragma unroll
           for (int kk = 0; kk < kCtaK / kMmaK; ++kk) {
             const uint32_t a_off = (uint32_t)(kk >> 2) * kABoxBytes + (uint32_t)(kk & 3) * 32u;
@@ -270,7 +286,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             dev::mma_bf16(d_acc, dev::smem_desc_sw128(a_st + a_off), dev::smem_desc_sw128(b_st + b_off), kIdesc,
                           (kt | kk) != 0 ? 1u : 0u);
           }
-          dev::mma_commit(bar_empty0 + 8u * s);      // stage free once these MMAs finish
+          // both stages free once these MMAs finish
+          dev::mma_commit(bar_a_empty0 + 8u * pa.index);
+          if (!one_ring) dev::mma_commit(bar_b_empty0 + 8u * pb.index);
         }
         if (!ok) break;
         dev::mma_commit(bar_acc_full0 + 8u * buf);   // tile j's accumulator complete
@@ -424,10 +442,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // issued is the one to wait for.
     const unsigned long long drain_ns = 10000000ull;   // 10 ms
     const int issued = warp == 0 ? a_issued : warp == 1 ? b_issued : 0;
+    const int ring = warp == 0 ? a_stages : b_stages;
+    const uint32_t full0 = warp == 0 ? bar_a_full0 : bar_b_full0;
     if ((warp == 0 || warp == 1) && lane == 0) {
-      for (int s = 0; s < issued && s < stages; ++s) {
-        const int round = (issued - 1 - s) / stages;
-        drain_wait(bar_full0 + 8u * s, (uint32_t)(round & 1), drain_ns);
+      for (int s = 0; s < issued && s < ring; ++s) {
+        const int round = (issued - 1 - s) / ring;
+        drain_wait(full0 + 8u * s, (uint32_t)(round & 1), drain_ns);
       }
     }
     // the peers' partials of a reduction this CTA stopped waiting for
@@ -482,7 +502,8 @@ cudaError_t launch_p(const LaunchArgs& la, const CUtensorMap& b_map, const Kerne
   }
   cfg.attrs = attrs;
   cfg.numAttrs = n;
-  return cudaLaunchKernelEx(&cfg, splitk_persistent_kernel<MMA_N>, b_map, p);
+  if (p.b_stages == p.stages) return cudaLaunchKernelEx(&cfg, splitk_persistent_kernel<MMA_N, true>, b_map, p);
+  return cudaLaunchKernelEx(&cfg, splitk_persistent_kernel<MMA_N, false>, b_map, p);
 }
 
 template <int MMA_N>
@@ -498,7 +519,7 @@ cudaError_t max_clusters_p(unsigned cluster_x, size_t smem, int* out) {
   attr.val.clusterDim.z = 1;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  return cudaOccupancyMaxActiveClusters(out, splitk_persistent_kernel<MMA_N>, &cfg);
+  return cudaOccupancyMaxActiveClusters(out, splitk_persistent_kernel<MMA_N, true>, &cfg);
 }
 
 }  // namespace
@@ -525,18 +546,16 @@ cudaError_t max_active_clusters_persistent(int mma_n, unsigned cluster_x, size_t
 }
 
 cudaError_t prepare_persistent(int max_dynamic_smem) {
-  cudaError_t e;
-  if ((e = cudaFuncSetAttribute(splitk_persistent_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                max_dynamic_smem)) != cudaSuccess)
-    return e;
-  if ((e = cudaFuncSetAttribute(splitk_persistent_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                max_dynamic_smem)) != cudaSuccess)
-    return e;
-  if ((e = cudaFuncSetAttribute(splitk_persistent_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                max_dynamic_smem)) != cudaSuccess)
-    return e;
-  return cudaFuncSetAttribute(splitk_persistent_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              max_dynamic_smem);
+  const void* fns[] = {
+      (const void*)splitk_persistent_kernel<16, true>,  (const void*)splitk_persistent_kernel<16, false>,
+      (const void*)splitk_persistent_kernel<32, true>,  (const void*)splitk_persistent_kernel<32, false>,
+      (const void*)splitk_persistent_kernel<64, true>,  (const void*)splitk_persistent_kernel<64, false>,
+      (const void*)splitk_persistent_kernel<128, true>, (const void*)splitk_persistent_kernel<128, false>};
+  for (const void* f : fns) {
+    const cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, max_dynamic_smem);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t read_and_clear_fault_persistent(int* out_words) {

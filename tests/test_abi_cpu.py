@@ -144,7 +144,11 @@ def test_plan_of_the_decode_workloads():
     assert (p.mma_n, p.persistent, list(p.grid)) == (64, 1, [2, 76, 1])
     p = _plan(128, 7168, 16384, 2, 8)              # persistent: 152 SMs / 8 = 19 clusters
     assert (p.mma_n, list(p.grid), p.k_tiles_per_cta, p.persistent) == (128, [8, 19, 1], 16, 1)
-    assert (p.stages, p.mailbox_quads, p.reduce_rounds) == (3, 16, 2)   # two rounds buy a third stage
+    # split 8: a 2-deep activation ring of its own buys one reduction round a tile
+    assert (p.stages, p.b_stages, p.mailbox_quads, p.reduce_rounds) == (3, 2, 32, 1)
+    p4 = _plan(128, 7168, 16384, 2, 4)             # split 4: the activations ride the weight ring
+    assert (p4.persistent, p4.stages, p4.b_stages) == (1, 3, 0)
+    assert (p4.mailbox_quads, p4.reduce_rounds) == (16, 2)                # two rounds buy a third stage
     assert _plan(16, 4096, 7168, 1, 8).persistent == 0   # 32 tiles deal out unevenly over 19 clusters
     assert _plan(16, 7168, 16384, 2, 8).persistent == 1
     assert _plan(16, 7168, 16384, 2, 4).persistent == 0  # narrow tiles at split 4: the per-tile kernel
@@ -211,7 +215,7 @@ def _check_persistent(p, M, N, K, L, split):
     """The invariants of a persistent plan: a cluster of split CTAs per
     `split` SMs (at most one per output tile), one CTA per SM, two
     accumulators, the scattered mailbox beside a ring of weight and
-    activation stages."""
+    activation stages (or a weight ring and an activation ring)."""
     tiles = -(-M // p.mma_n) * -(-N // 128) * L
     assert split >= 2 and p.split_k == split
     assert list(p.grid) == [split, max(1, min(tiles, GB300["num_sms"] // split)), 1]
@@ -220,17 +224,21 @@ def _check_persistent(p, M, N, K, L, split):
             p.mma_issuers, p.b_loader, p.l2_prefetch, p.ctas_per_sm) == (1, 1, 0, 0, 1, 0, 0, 1)
     assert p.tmem_cols == next(c for c in (32, 64, 128, 256, 512) if c >= 2 * max(32, p.mma_n))
     assert 2 <= p.stages <= 8
+    assert p.b_stages == 0 or 2 <= p.b_stages <= 8
+    b_ring = p.b_stages or p.stages
     nquads = -(-min(M, p.mma_n) // 4)
     assert p.mailbox_quads == nquads or (p.mailbox_quads % 4 == 0 and p.mailbox_quads < nquads)
     assert p.reduce_rounds == -(-nquads // p.mailbox_quads)
     round_cols = min(min(M, p.mma_n), 4 * p.mailbox_quads)
     budget = min(GB300["smem_per_block_optin"], GB300["smem_per_sm"] - 1024)
-    assert p.smem_bytes == 1024 + p.stages * (32768 + p.mma_n * 256) + round_cols * 512 + 256
+    bars = 256 if b_ring == p.stages else 384       # a second set of ring barriers when the depths differ
+    assert p.smem_bytes == 1024 + p.stages * 32768 + b_ring * p.mma_n * 256 + round_cols * 512 + bars
     assert p.smem_bytes <= budget
-    if p.stages < 8:   # the deepest ring that fits
-        assert p.smem_bytes + 32768 + p.mma_n * 256 > budget
+    one_more = 32768 + (0 if p.b_stages else p.mma_n * 256)
+    if p.stages < 8:   # the deepest weight ring that fits
+        assert p.smem_bytes + one_more > budget
     if p.reduce_rounds > 1:   # rounds only where they buy a deeper ring than one round a tile
-        assert 1024 + p.stages * (32768 + p.mma_n * 256) + min(M, p.mma_n) * 512 + 256 > budget
+        assert 1024 + p.stages * 32768 + b_ring * p.mma_n * 256 + min(M, p.mma_n) * 512 + bars > budget
 
 
 @pytest.mark.parametrize("M", [1, 4, 16, 17, 32, 33, 64, 65, 128, 129, 1000])
@@ -458,7 +466,7 @@ def test_plan_check_rejects_what_a_launch_would():
     assert _check(bad, M, N, K, L) == -10
     assert _check(p, M, N, K + 8, L) == -10             # another shape
     bad = sk.Plan.from_buffer_copy(p)
-    bad.reserved = 2                                    # the reserved field must stay 0
+    bad.b_stages = 2                                    # an activation ring of its own: persistent plans only
     assert _check(bad, M, N, K, L) == -10
     bad = sk.Plan.from_buffer_copy(p)
     bad.w4_decoders = 1                                 # a bf16 plan decodes nothing

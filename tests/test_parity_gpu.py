@@ -645,16 +645,17 @@ def test_w4a16_the_largest_grid_dimensions_index_correctly(L, N):
 
 
 # ---------------------------------------------------------------- persistent plans
-def _persistent(M, N, K, L, split, clusters=None, stages=None, quads=None, mma_n=None):
+def _persistent(M, N, K, L, split, clusters=None, stages=None, quads=None, mma_n=None, b_stages=0):
     """The persistent plan of the shape at `split` (the deepest ring unless
-    `stages` is given, reduction rounds of `quads` 4-column groups if given),
-    with `clusters` as its grid bound if given."""
+    `stages` is given, reduction rounds of `quads` 4-column groups if given,
+    the activations on the weight ring unless `b_stages` gives them a ring
+    of their own), with `clusters` as its grid bound if given."""
     props = torch.cuda.get_device_properties(DEV)
     cands = sk.splitk_plan_candidates_for(M, N, K, L, split, props.multi_processor_count,
                                           props.shared_memory_per_multiprocessor,
                                           props.shared_memory_per_block_optin)
     ps = [p for p in cands if p.persistent and (quads is None or p.mailbox_quads == quads)
-          and (mma_n is None or p.mma_n == mma_n)]
+          and (mma_n is None or p.mma_n == mma_n) and p.b_stages == b_stages]
     assert ps, "no persistent candidate"
     p = max(ps, key=lambda q: q.stages) if stages is None else next(q for q in ps if q.stages == stages)
     p = sk.Plan.from_buffer_copy(p)
@@ -701,6 +702,28 @@ def test_persistent_kernel_equals_the_scattered_per_tile_kernel_bit_for_bit(M, s
         except StopIteration:
             continue                                          # that depth does not fit
         assert np.array_equal(gemm_gpu(a, b, plan=p), want), (stages, clusters)
+
+
+@pytest.mark.parametrize("M,split,stages,b_stages,clusters", [
+    (128, 8, 4, 2, 3),     # the weight ring twice the activation ring's depth
+    (128, 4, 3, 3, 2),     # equal depths, separate rings
+    (64, 4, 5, 2, None),
+    (100, 2, 2, 5, 1),     # a deeper activation ring; one cluster walks every tile
+    (37, 8, 5, 3, 4),      # depths with no common factor
+    (16, 2, 5, 3, 5),
+])
+def test_persistent_activation_ring_of_its_own(M, split, stages, b_stages, clusters):
+    """The activations on a ring of their own depth beside the weight ring:
+    the same MMAs on the same K tiles in the same order, so the same bits as
+    the plan whose activations ride the weight ring, and the oracle's
+    values."""
+    L, N, K = 2, 520, 3000
+    a, b = _draw(L, M, N, K, seed=3200 + M + split)
+    p = _persistent(M, N, K, L, split, clusters, stages, b_stages=b_stages)
+    assert (p.stages, p.b_stages) == (stages, b_stages)
+    c = gemm_gpu(a, b, plan=p)
+    assert np.array_equal(c, gemm_gpu(a, b, plan=_persistent(M, N, K, L, split, clusters, 2)))
+    assert_parity(c, oracle_full(a, b), a, b, K)
 
 
 @pytest.mark.parametrize("M,quads", [(100, 4), (128, 16), (64, 8), (37, 4)])
