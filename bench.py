@@ -466,7 +466,7 @@ def point_record(w, ms_per_step, reps, steps, plan, traffic, world):
             "plan": {k: v for k, v in plan.as_dict().items()
                      if k in ("mma_n", "stages", "grid", "smem_bytes", "ctas_per_sm", "mailbox_dedicated",
                               "reduce_rounds", "reduce_scatter", "b_resident", "a_tmem_tiles",
-                              "mma_issuers", "b_loader", "pdl_trigger")}}
+                              "mma_issuers", "b_loader", "pdl_trigger", "persistent", "b_stages")}}
 
 
 def e2e_point(w, weights, dev, stream, steps, reps, warmup, world):
