@@ -343,6 +343,13 @@ __device__ __forceinline__ void tmem_wait_ld() {
 //   bits 32-45  stride-dimension byte offset >> 4 (1024 B between 8-row atoms)
 //   bits 46-47  descriptor version 1
 //   bits 61-63  layout: 2 = 128-byte swizzle
+// The descriptor of the matrix `bytes` further on (a multiple of 16): the
+// start address field holds (address >> 4) in 14 bits, and no shared-memory
+// address reaches 2^18, so adding to the descriptor never carries out of it.
+__device__ __forceinline__ uint64_t smem_desc_advance(uint64_t desc, uint32_t bytes) {
+  return desc + (uint64_t)(bytes >> 4);
+}
+
 __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
   uint64_t d = 0;
   d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);

@@ -447,12 +447,14 @@ __global__ void __launch_bounds__(kDecWG == 2 ? kThreadsW4Wide : kThreads, kDecW
       // saw every earlier round of tile kt's slot complete (nis <= slots).
       const int slots = p.a_tmem_tiles;
       const uint32_t d_acc = tmem_base + (uint32_t)issuer * kAccCols;
+      // descriptors by addition to the buffers' first (smem_desc_advance)
+      const uint64_t b_desc0 = dev::smem_desc_sw128(sB), q_desc = dev::smem_desc_sw128(sQStage);
       bool ok = waiter.wait<false>(bar_b, 0u, kRoleMma, -1);
       dev::tc_fence_after();
       RingPos sp = RingPos::at(issuer, slots);                  // TMEM slot of tile kt
       for (int kt = issuer; kt < k_tiles && ok; kt += nis, sp.advance(nis, slots)) {
         const uint32_t first = (uint32_t)(kt >= nis);          // 0: this accumulator's first tile
-        const uint32_t b_st = sB + (uint32_t)kt * kBStage;
+        const uint64_t b_d = dev::smem_desc_advance(b_desc0, (uint32_t)kt * kBStage);
         if (p.w4_smem_tiles && kt == slots) {
           // the tile decoded into the bf16 stage in shared memory
           ok = waiter.wait<false>(bar_w4_stage, 0u, kRoleMma, kt);
@@ -463,7 +465,7 @@ __global__ void __launch_bounds__(kDecWG == 2 ? kThreadsW4Wide : kThreads, kDecW
           for (int kk = 0; kk < kCtaK / kMmaK; ++kk) {
             const uint32_t a_off = (uint32_t)(kk >> 2) * kABoxBytes + (uint32_t)(kk & 3) * 32u;
             const uint32_t b_off = (uint32_t)(kk >> 2) * kBBox + (uint32_t)(kk & 3) * 32u;
-            dev::mma_bf16(d_acc, dev::smem_desc_sw128(sQStage + a_off), dev::smem_desc_sw128(b_st + b_off),
+            dev::mma_bf16(d_acc, dev::smem_desc_advance(q_desc, a_off), dev::smem_desc_advance(b_d, b_off),
                           kIdesc, (first | (uint32_t)kk) != 0u ? 1u : 0u);
           }
           continue;
@@ -478,7 +480,7 @@ __global__ void __launch_bounds__(kDecWG == 2 ? kThreadsW4Wide : kThreads, kDecW
 #pragma unroll
         for (int kk = 0; kk < kCtaK / kMmaK; ++kk) {
           const uint32_t b_off = (uint32_t)(kk >> 2) * kBBox + (uint32_t)(kk & 3) * 32u;
-          dev::mma_bf16_ts(d_acc, t_col + (uint32_t)kk * 8u, dev::smem_desc_sw128(b_st + b_off), kIdesc,
+          dev::mma_bf16_ts(d_acc, t_col + (uint32_t)kk * 8u, dev::smem_desc_advance(b_d, b_off), kIdesc,
                            (first | (uint32_t)kk) != 0u ? 1u : 0u);
         }
         dev::mma_commit(bar_slot_empty0 + 8u * slot);   // slot free once these MMAs have read it
@@ -487,6 +489,8 @@ __global__ void __launch_bounds__(kDecWG == 2 ? kThreadsW4Wide : kThreads, kDecW
     }
     if (!kQuant && lane == 0 && issuer < nis) {
       const uint32_t d_acc = tmem_base + (uint32_t)issuer * kAccCols;
+      // descriptors by addition to the buffers' first (smem_desc_advance)
+      const uint64_t a_desc0 = dev::smem_desc_sw128(sA), b_desc0 = dev::smem_desc_sw128(sB);
       bool ok = true;
       // Before the activations can exist: copy this issuer's share of the
       // first `tmem_tiles` weight K tiles from the ring into tensor memory as
@@ -498,12 +502,12 @@ __global__ void __launch_bounds__(kDecWG == 2 ? kThreadsW4Wide : kThreads, kDecW
         ok = waiter.wait<false>(bar_full0 + 8u * s, cpos.phase, kRoleMma, kt);
         if (!ok) break;
         dev::tc_fence_after();
-        const uint32_t a_st = sA + (uint32_t)s * kAStageBytes;
+        const uint64_t a_d = dev::smem_desc_advance(a_desc0, (uint32_t)s * kAStageBytes);
         const uint32_t t_col = tmem_base + p.tmem_tile_col0 + (uint32_t)kt * kTmemTileCols;
 #pragma unroll
         for (int kk = 0; kk < kCtaK / kMmaK; ++kk) {
           const uint32_t a_off = (uint32_t)(kk >> 2) * kABoxBytes + (uint32_t)(kk & 3) * 32u;
-          dev::tmem_cp_128x256b(t_col + (uint32_t)kk * 8u, dev::smem_desc_sw128(a_st + a_off));
+          dev::tmem_cp_128x256b(t_col + (uint32_t)kk * 8u, dev::smem_desc_advance(a_d, a_off));
         }
         dev::mma_commit(bar_empty0 + 8u * s);  // stage free once the copies have read it
       }
@@ -515,7 +519,7 @@ __global__ void __launch_bounds__(kDecWG == 2 ? kThreadsW4Wide : kThreads, kDecW
       for (int kt = issuer; kt < k_tiles && ok; kt += nis, pos.advance(nis, stages)) {
         const int s = pos.index;
         const uint32_t first = (uint32_t)(kt >= nis);          // 0: this accumulator's first tile
-        const uint32_t b_st = sB + (uint32_t)(b_res ? kt : s) * kBStage;
+        const uint64_t b_d = dev::smem_desc_advance(b_desc0, (uint32_t)(b_res ? kt : s) * kBStage);
         if (kt == issuer) stamp(p, kTrFirstFull);
         if (kt < tmem_tiles) {
           // A from tensor memory (copied above, ordered before these MMAs)
@@ -524,7 +528,7 @@ __global__ void __launch_bounds__(kDecWG == 2 ? kThreadsW4Wide : kThreads, kDecW
 #pragma unroll
           for (int kk = 0; kk < kCtaK / kMmaK; ++kk) {
             const uint32_t b_off = (uint32_t)(kk >> 2) * kBBox + (uint32_t)(kk & 3) * 32u;
-            dev::mma_bf16_ts(d_acc, t_col + (uint32_t)kk * 8u, dev::smem_desc_sw128(b_st + b_off), kIdesc,
+            dev::mma_bf16_ts(d_acc, t_col + (uint32_t)kk * 8u, dev::smem_desc_advance(b_d, b_off), kIdesc,
                              (first | (uint32_t)kk) != 0u ? 1u : 0u);
           }
           continue;
@@ -533,12 +537,12 @@ __global__ void __launch_bounds__(kDecWG == 2 ? kThreadsW4Wide : kThreads, kDecW
         if (!ok) break;
         dev::tc_fence_after();
         if (kt == k_tiles - 1) stamp(p, kTrLastFull);
-        const uint32_t a_st = sA + (uint32_t)s * kAStageBytes;
+        const uint64_t a_d = dev::smem_desc_advance(a_desc0, (uint32_t)s * kAStageBytes);
 #pragma unroll
         for (int kk = 0; kk < kCtaK / kMmaK; ++kk) {
           const uint32_t a_off = (uint32_t)(kk >> 2) * kABoxBytes + (uint32_t)(kk & 3) * 32u;
           const uint32_t b_off = (uint32_t)(kk >> 2) * kBBox + (uint32_t)(kk & 3) * 32u;
-          dev::mma_bf16(d_acc, dev::smem_desc_sw128(a_st + a_off), dev::smem_desc_sw128(b_st + b_off), kIdesc,
+          dev::mma_bf16(d_acc, dev::smem_desc_advance(a_d, a_off), dev::smem_desc_advance(b_d, b_off), kIdesc,
                         (first | (uint32_t)kk) != 0u ? 1u : 0u);
         }
         dev::mma_commit(bar_empty0 + 8u * s);  // stage free once these MMAs finish

@@ -262,6 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       int g = 0;
       RingPos pa{0, 0u}, pb{0, 0u};                  // weight / activation ring positions of load g
+      const uint64_t a_desc0 = dev::smem_desc_sw128(sA), b_desc0 = dev::smem_desc_sw128(sB);
       for (int j = 0; j < my_tiles && ok; ++j) {
         const int buf = j & 1;
         const int use = j >> 1;
@@ -277,13 +278,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           dev::tc_fence_after();
           if (g == 0) stamp(p, kTrFirstFull);
-          const uint32_t a_st = sA + (uint32_t)pa.index * kAStageBytes;
-          const uint32_t b_st = sB + (uint32_t)pb.index * kBStage;
+          // the stages' descriptors by addition to the rings' first
+          const uint64_t a_d = dev::smem_desc_advance(a_desc0, (uint32_t)pa.index * kAStageBytes);
+          const uint64_t b_d = dev::smem_desc_advance(b_desc0, (uint32_t)pb.index * kBStage);
 #pragma unroll
           for (int kk = 0; kk < kCtaK / kMmaK; ++kk) {
             const uint32_t a_off = (uint32_t)(kk >> 2) * kABoxBytes + (uint32_t)(kk & 3) * 32u;
             const uint32_t b_off = (uint32_t)(kk >> 2) * kBBox + (uint32_t)(kk & 3) * 32u;
-            dev::mma_bf16(d_acc, dev::smem_desc_sw128(a_st + a_off), dev::smem_desc_sw128(b_st + b_off), kIdesc,
+            dev::mma_bf16(d_acc, dev::smem_desc_advance(a_d, a_off), dev::smem_desc_advance(b_d, b_off), kIdesc,
                           (kt | kk) != 0 ? 1u : 0u);
           }
           // both stages free once these MMAs finish

@@ -77,10 +77,12 @@ def test_no_fault_recorded_in_normal_operation():
     assert sk.splitk_get_fault()["code"] == 0
 
 
-def test_persistent_plan_skipped_publish_times_out_and_the_context_survives():
-    """The persistent kernel's bounded waits: with the peers' partials
-    withheld every rank's reduction wait runs out, the launch ends, and a
-    normal call afterwards is correct."""
+@pytest.mark.parametrize("stages,b_stages", [(2, 0), (3, 2)])
+def test_persistent_plan_skipped_publish_times_out_and_the_context_survives(stages, b_stages):
+    """The persistent kernel's bounded waits (the activations on the weight
+    ring, or on a ring of their own): with the peers' partials withheld
+    every rank's reduction wait runs out, the launch ends, and a normal call
+    afterwards is correct."""
     M, N, K, L, split = 64, 1000, 4096, 1, 4
     a = synthetic.normal_bf16((L, N, K), 901, synthetic.STREAM_A, 0.02)
     b = synthetic.normal_bf16((L, M, K), 901, synthetic.STREAM_B, 1.0)
@@ -89,7 +91,7 @@ def test_persistent_plan_skipped_publish_times_out_and_the_context_survives():
     plan = next(p for p in sk.splitk_plan_candidates_for(M, N, K, L, split, props.multi_processor_count,
                                                           props.shared_memory_per_multiprocessor,
                                                           props.shared_memory_per_block_optin)
-                if p.persistent)
+                if p.persistent and (p.stages, p.b_stages) == (stages, b_stages))
     plan.grid[1] = 2                                     # each cluster walks several tiles
     try:
         sk.splitk_set_wait_limit_ns(50_000_000)          # 50 ms
