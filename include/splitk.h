@@ -177,8 +177,9 @@ typedef struct splitk_plan_t {
                               `stages` is the weight ring's depth alone (at
                               wide tiles an activation stage is as large as a
                               weight stage but comes from L2, so a shallower
-                              activation ring leaves room for more weight
-                              tiles in flight).  0 for every other plan      */
+                              activation ring leaves shared memory for more
+                              weight tiles or for a mailbox that reduces a
+                              tile in one round).  0 for every other plan    */
     int persistent;        /* 0: one CTA per (output tile, K rank), the grid
                               above.  1: the persistent kernel: grid
                               (split_k, clusters, 1), each cluster of split_k
