@@ -111,6 +111,16 @@ __device__ __forceinline__ void st_async_b32(uint32_t cluster_addr, uint32_t a, 
                : "memory");
 }
 
+// Four 32-bit values to 16 bytes of a cluster peer's shared memory (16-byte
+// aligned), completing that many bytes on the peer's mbarrier.
+__device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                            uint32_t cluster_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                   cluster_addr),
+               "r"(a), "r"(b), "r"(c), "r"(d), "r"(cluster_bar)
+               : "memory");
+}
+
 // ---------------------------------------------------------------- PDL
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 

@@ -706,12 +706,16 @@ __global__ void __launch_bounds__(kDecWG == 2 ? kThreadsW4Wide : kThreads, kDecW
       if (et == 0) {
         dev::mbar_arrive_expect_tx(bar_reduce, (uint32_t)((split - 1) * ncols * R) * 4u);
       }
-      // Thread et holds weight row et: its value of column c goes to
-      // [rank][c][et - dst_rank*R] of the rank that sums row et; a warp's 32
-      // rows of one column are 128 contiguous bytes.
+      // Thread et holds weight row et and sends it to the rank that sums it.
+      // Whole quads of columns (ncols % 4 == 0): the mailbox is [source][row]
+      // [column] and the row's columns go as 16-byte st.async, a quarter of
+      // the remote stores.  Otherwise [source][column][row] with 4-byte ones
+      // (a warp's 32 rows of one column are 128 contiguous bytes).
       const int dst_rank = et / R;
       const bool publish = !(p.inject & kInjectSkipPublish);
-      const uint32_t slot = ((uint32_t)(rank * ncols) * (uint32_t)R + (uint32_t)(et - dst_rank * R)) * 4u;
+      const bool by_row = (ncols & 3) == 0;
+      const uint32_t slot = by_row ? (uint32_t)((rank * R + (et - dst_rank * R)) * ncols) * 4u
+                                   : ((uint32_t)(rank * ncols) * (uint32_t)R + (uint32_t)(et - dst_rank * R)) * 4u;
       const uint32_t r_bar = dev::mapa(bar_reduce, (uint32_t)dst_rank);
       const uint32_t r_mail = dev::mapa(sMail, (uint32_t)dst_rank) + slot;
 #pragma unroll 1
@@ -719,14 +723,27 @@ __global__ void __launch_bounds__(kDecWG == 2 ? kThreadsW4Wide : kThreads, kDecW
         uint32_t v[16];
         __syncwarp();   // tcgen05.ld is warp-collective
         load_acc16(t_row + (uint32_t)(g * 16), kAccCols, two_acc, v);
+        if (by_row) {
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int col = g * 16 + e;
-          if (col >= ncols) break;                            // warp-uniform
-          if (dst_rank == rank) {
-            *reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(mb) + slot + (size_t)col * R * 4) = v[e];
-          } else if (publish) {
-            dev::st_async_b32(r_mail + (uint32_t)(col * R) * 4u, v[e], r_bar);
+          for (int q = 0; q < 4; ++q) {
+            const int col = g * 16 + 4 * q;
+            if (col >= ncols) break;                          // warp-uniform
+            if (dst_rank == rank) {
+              dev::st_shared_v4(sMail + slot + (uint32_t)col * 4u, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            } else if (publish) {
+              dev::st_async_v4(r_mail + (uint32_t)col * 4u, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3], r_bar);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int col = g * 16 + e;
+            if (col >= ncols) break;                          // warp-uniform
+            if (dst_rank == rank) {
+              *reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(mb) + slot + (size_t)col * R * 4) = v[e];
+            } else if (publish) {
+              dev::st_async_b32(r_mail + (uint32_t)(col * R) * 4u, v[e], r_bar);
+            }
           }
         }
       }
@@ -736,6 +753,35 @@ __global__ void __launch_bounds__(kDecWG == 2 ? kThreadsW4Wide : kThreads, kDecW
       if (et == 0) stamp(p, kTrReduced);
       dev::named_bar_sync(1, kEpiThreads);                  // own slot complete
       waiter.wait<true>(bar_reduce, 0u, kRoleEpiReduce, 0);
+      if (by_row) {
+        // One weight row and 4 token columns per item: sum the sources in
+        // rank order, four bf16 stores (one per token row of C).
+        const int nq = ncols >> 2;
+        const int items = R * nq;
+#pragma unroll 1
+        for (int it = et; it < items; it += kEpiThreads) {
+          const int r = it / nq;
+          const int c4 = (it - r * nq) * 4;
+          const float* src = mb + (size_t)r * ncols + c4;
+          float4 x = *reinterpret_cast<const float4*>(src);
+#pragma unroll 1
+          for (int sr = 1; sr < split; ++sr) {
+            const float4 a4 = *reinterpret_cast<const float4*>(src + (size_t)sr * R * ncols);
+            x.x += a4.x; x.y += a4.y; x.z += a4.z; x.w += a4.w;
+          }
+          const int n = n0 + my_lo + r;
+          if (n >= p.N) continue;
+          const float bv = p.bias != nullptr
+                               ? __uint_as_float((uint32_t)__ldg(p.bias + (size_t)l * (size_t)p.N + (size_t)n) << 16)
+                               : 0.0f;
+          uint16_t* dst = p.c + ((size_t)((size_t)l * p.M + (size_t)(m0 + c4)) * (size_t)p.N + (size_t)n);
+          dst[0] = (uint16_t)(dev::pack_bf16x2(x.x + bv, 0.0f) & 0xFFFFu);
+          dst[(size_t)p.N] = (uint16_t)(dev::pack_bf16x2(x.y + bv, 0.0f) & 0xFFFFu);
+          dst[(size_t)2 * p.N] = (uint16_t)(dev::pack_bf16x2(x.z + bv, 0.0f) & 0xFFFFu);
+          dst[(size_t)3 * p.N] = (uint16_t)(dev::pack_bf16x2(x.w + bv, 0.0f) & 0xFFFFu);
+        }
+        if (et == 0) stamp(p, kTrStored);
+      } else {
       // 8 weight rows of one token column per item: sum the sources in rank
       // order, pack bf16 pairs, one 16-byte store.
       const int chunks = R / 8;
@@ -769,6 +815,7 @@ __global__ void __launch_bounds__(kDecWG == 2 ? kThreadsW4Wide : kThreads, kDecW
         }
       }
       if (et == 0) stamp(p, kTrStored);
+      }
     } else if (narrow) {
       // One round, each thread its own weight row: peers send each live
       // column with a 4-byte st.async into rank 0's mailbox [peer-1][column]
