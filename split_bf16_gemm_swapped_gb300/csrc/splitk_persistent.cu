@@ -361,23 +361,42 @@ __global__ void __launch_bounds__(kThreads, 1)
           quiet = true;
         }
         const bool send = publish && !quiet;
-        // Thread et's value of column c goes to [rank][c - c_lo][et - dst_rank*R]
-        // of the rank that sums row et; a warp's rows of one column are contiguous.
-        const uint32_t slot = ((uint32_t)(rank * rc) * (uint32_t)R + (uint32_t)(et - dst_rank * R)) * 4u;
+        // Rounds of whole column quads: the mailbox is [source][row][column]
+        // and each thread sends its row's columns as 16-byte st.async (a
+        // quarter of the remote stores).  Otherwise [source][column][row]:
+        // thread et's value of column c goes to [rank][c - c_lo][et - dst_rank*R]
+        // of the rank that sums row et, a warp's rows of one column contiguous.
+        const bool by_row = (rc & 3) == 0;
+        const uint32_t slot = by_row ? (uint32_t)((rank * R + (et - dst_rank * R)) * rc) * 4u
+                                     : ((uint32_t)(rank * rc) * (uint32_t)R + (uint32_t)(et - dst_rank * R)) * 4u;
 #pragma unroll 1
         for (int g = c_lo >> 4; g * 16 < c_hi; ++g) {
           uint32_t v[16];
           __syncwarp();   // tcgen05.ld is warp-collective
           load_acc16(t_row + (uint32_t)buf * kAccCols + (uint32_t)(g * 16), 0u, false, v);
+          if (by_row) {
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int col = g * 16 + e;
-            if (col < c_lo || col >= c_hi) continue;             // warp-uniform
-            const uint32_t off = slot + (uint32_t)((col - c_lo) * R) * 4u;
-            if (dst_rank == rank) {
-              *reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(mb) + off) = v[e];
-            } else if (send) {
-              dev::st_async_b32(r_mail0 + off, v[e], r_bar);
+            for (int q = 0; q < 4; ++q) {
+              const int col = g * 16 + 4 * q;
+              if (col < c_lo || col >= c_hi) continue;           // warp-uniform
+              const uint32_t off = slot + (uint32_t)(col - c_lo) * 4u;
+              if (dst_rank == rank) {
+                dev::st_shared_v4(sMail + off, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+              } else if (send) {
+                dev::st_async_v4(r_mail0 + off, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3], r_bar);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int col = g * 16 + e;
+              if (col < c_lo || col >= c_hi) continue;           // warp-uniform
+              const uint32_t off = slot + (uint32_t)((col - c_lo) * R) * 4u;
+              if (dst_rank == rank) {
+                *reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(mb) + off) = v[e];
+              } else if (send) {
+                dev::st_async_b32(r_mail0 + off, v[e], r_bar);
+              }
             }
           }
         }
@@ -394,6 +413,55 @@ __global__ void __launch_bounds__(kThreads, 1)
             quiet = true;
           }
         }
+        if (by_row) {
+          // 8 weight rows x 4 token columns per item: sum the sources in rank
+          // order, then per column pack bf16 pairs and one 16-byte store.
+          const int nq = rc >> 2;
+          const int items = (R >> 3) * nq;
+#pragma unroll 1
+          for (int it = et; it < items; it += kEpiThreads) {
+            const int rb = it / nq;
+            const int c4 = (it - rb * nq) * 4;
+            const float* src = mb + (size_t)(rb * 8) * rc + c4;
+            float4 x[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) x[i] = *reinterpret_cast<const float4*>(src + (size_t)i * rc);
+#pragma unroll 1
+            for (int sr = 1; sr < split; ++sr) {
+              const float* ps = src + (size_t)sr * R * rc;
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const float4 a4 = *reinterpret_cast<const float4*>(ps + (size_t)i * rc);
+                x[i].x += a4.x; x[i].y += a4.y; x[i].z += a4.z; x[i].w += a4.w;
+              }
+            }
+            const int n = n0 + my_lo + rb * 8;
+            if (n >= p.N) continue;
+            float b8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            if (p.bias != nullptr) {
+              const uint16_t* bp = p.bias + (size_t)l * (size_t)p.N + (size_t)n;
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                if (n + e < p.N) b8[e] = __uint_as_float((uint32_t)__ldg(bp + e) << 16);
+              }
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              float v8[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) v8[i] = (c == 0 ? x[i].x : c == 1 ? x[i].y : c == 2 ? x[i].z : x[i].w) + b8[i];
+              const uint32_t q0 = dev::pack_bf16x2(v8[0], v8[1]), q1 = dev::pack_bf16x2(v8[2], v8[3]);
+              const uint32_t q2 = dev::pack_bf16x2(v8[4], v8[5]), q3 = dev::pack_bf16x2(v8[6], v8[7]);
+              uint16_t* dst =
+                  p.c + ((size_t)((size_t)l * p.M + (size_t)(m0 + c_lo + c4 + c)) * (size_t)p.N + (size_t)n);
+              if (p.vec_store && n + 8 <= p.N) {
+                dev::st_global_v4(dst, q0, q1, q2, q3);
+              } else {
+                store8_clipped(dst, n, p.N, q0, q1, q2, q3);
+              }
+            }
+          }
+        } else {
         // 8 weight rows of one token column per item: sum the sources in rank
         // order, pack bf16 pairs, one 16-byte store.
         const int chunks = R / 8;
@@ -425,6 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             store8_clipped(dst, n, p.N, q0, q1, q2, q3);
           }
+        }
         }
         // Every thread has read the mailbox: the peers may publish the next round.
         dev::named_bar_sync(1, kEpiThreads);
