@@ -259,7 +259,7 @@ int plan_ring_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t 
 // whose reduction overlaps the next tile's stream, where that measured
 // faster on GB300 (the K = 16384 sweep, back to back, the same box): split 8
 // at every tile width (M = 1..16: 0.82-0.95 -> 0.97-0.99 of the HBM copy
-// bandwidth; M = 64: 0.55 -> 0.87), and split 4 for tiles of 64 and 128
+// bandwidth; M = 64: 0.55 -> 0.87), and split 4 for tiles of 32 to 128
 // tokens (M = 64: 0.80 -> 0.82; the wide projection 0.68 -> 0.88), when the
 // grid exceeds one CTA per SM and the output tiles deal out evenly (at least
 // 90 %) over one cluster per `split` SMs; at split 8 with a reduction in
@@ -278,11 +278,12 @@ int plan_impl(int M, int N, int K, int L, int split_k, int num_sms, size_t smem_
   const long long clusters = std::max(1, num_sms / split);
   const long long rounds = (tiles + clusters - 1) / clusters;
   const bool balanced = (double)tiles >= 0.9 * (double)(rounds * clusters);
-  // Split 2 at 32-token tiles: the persistent kernel measured faster even
-  // with uneven rounds (M = 32 sweep point, 112 tiles over 76 clusters:
-  // 77.4 -> 75.1 us; at 64-token tiles the two kernels measure level).
-  const bool two_32 = split == 2 && out->mma_n == 32;
-  if ((((split == 8 || (split == 4 && out->mma_n >= 64) || two_wide) && balanced) || two_32) &&
+  // Split 2 at 32- and 64-token tiles: the persistent kernel measured faster
+  // even with uneven rounds (112 tiles over 76 clusters: M = 32 sweep point
+  // 77.4 -> 75.1 us, M = 64 79.1 -> 77.0 us).  Split 4 from 32-token tiles
+  // when the tiles deal out evenly (M = 32: 76.8 -> 76.0 us).
+  const bool two_uneven = split == 2 && (out->mma_n == 32 || out->mma_n == 64);
+  if ((((split == 8 || (split == 4 && out->mma_n >= 32) || two_wide) && balanced) || two_uneven) &&
       tiles * split > num_sms) {
     splitk_plan_t p;
     if (persistent_plan(M, N, K, L, split, 0, 0, 0, num_sms, smem_per_sm, smem_optin, &p, pers_n)) {

@@ -155,12 +155,15 @@ def test_plan_of_the_decode_workloads():
     assert _plan(64, 7168, 16384, 2, 4).persistent == 1
     p2 = _plan(128, 7168, 16384, 2, 2)             # split 2, 128 tokens: 64-token tiles, 224 over 76 clusters
     assert (p2.persistent, p2.mma_n, p2.split_k) == (1, 64, 2)
-    assert _plan(64, 7168, 16384, 2, 2).persistent == 0   # 112 tiles over 76 clusters: the per-tile kernel
+    p64 = _plan(64, 7168, 16384, 2, 2)                   # 112 tiles over 76 clusters: persistent all the same
+    assert (p64.persistent, p64.mma_n) == (1, 64)
+    p32 = _plan(32, 7168, 16384, 2, 4)                   # 32-token tiles at split 4, evenly dealt: persistent
+    assert (p32.persistent, p32.mma_n) == (1, 32)
     pw = _plan(64, 18432, 7168, 1, 2)                     # the wide projection: 144 tiles, even enough
     assert (pw.persistent, pw.mma_n) == (1, 64)
     p32 = _plan(32, 7168, 16384, 2, 2)                   # 32-token tiles at split 2: persistent
     assert (p32.persistent, p32.mma_n) == (1, 32)
-    assert _plan(48, 7168, 16384, 2, 2).persistent == 0  # 64-token tiles, uneven: the per-tile kernel
+    assert _plan(48, 7168, 16384, 2, 2).persistent == 1  # 64-token tiles, uneven rounds: persistent
     assert p.reduce_rounds >= 1 and p.mailbox_quads % 4 == 0
 
 
