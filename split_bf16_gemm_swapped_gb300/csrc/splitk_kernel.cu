@@ -695,8 +695,9 @@ __global__ void __launch_bounds__(kDecWG == 2 ? kThreadsW4Wide : kThreads, kDecW
     if (p.reduce_scatter) {
       // Scattered reduction: rank r sums and stores weight rows
       // [r*R, (r+1)*R) of the tile, R = 128 / split.  Each rank's partial of
-      // those rows lands in rank r's mailbox [source rank][column][R rows]
-      // (its own by shared stores, the others' by st.async), and every
+      // those rows lands in rank r's mailbox, [source rank][R rows][column]
+      // or [source rank][column][R rows] (below; its own by shared stores,
+      // the others' by st.async), and every
       // element is summed over source ranks 0, 1, ... in order: the same
       // additions in the same order as rank 0 makes in the gathered mode,
       // with 1/split of the DSMEM bytes arriving at each SM.

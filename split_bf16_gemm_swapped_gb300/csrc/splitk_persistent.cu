@@ -20,9 +20,11 @@
 // reduce_scatter mode -- rank r sums weight rows [r*R, (r+1)*R), R = 128 /
 // split, over source ranks 0, 1, ..., split-1 in that order (the same FP32
 // additions as rank 0 makes in the gathered mode, so the same bits).  Each
-// rank has one mailbox [source][column][R rows] holding the columns of one
-// reduction round (a whole tile, or a group of its columns when the mailbox
-// is smaller); before publishing a round into a peer's mailbox a rank waits
+// rank has one mailbox holding the columns of one reduction round (a whole
+// tile, or a group of its columns when the mailbox is smaller), laid out
+// [source][R rows][columns] for rounds of whole column quads (each row sent
+// as 16-byte st.async) and [source][columns][R rows] otherwise (4-byte
+// st.async); before publishing a round into a peer's mailbox a rank waits
 // until every peer has signalled (a remote mbarrier arrival) that it has
 // read its mailbox of the previous round.
 //
